@@ -1,0 +1,310 @@
+// Tree-masked attention, shared by the draft layer and the target's
+// verification layer ([B] "Tree Attention 如何一次验证多条路径": node u sees the
+// committed prefix plus the tree nodes that are its ancestors or itself).
+//
+// Split-KV layout: one CTA per (prefix split or tree part, request, kv head).
+// Every query row of the request that maps to this kv head (tree nodes x GQA
+// group) consumes the same shared-memory K/V tile, so prefix KV bytes are
+// read from HBM once per call however many tree nodes there are.  Each CTA
+// writes (max, sum, unnormalised output) partials; the last CTA of a
+// (request, kv head) merges them in split order.  The ancestor mask of each
+// query row lives in a register (one 64-bit word) and is tested per tree key.
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace eagle {
+namespace {
+
+constexpr int TILE = 64;          // KV rows per shared-memory tile
+constexpr int THREADS = 256;
+constexpr int MAX_DH = 128;
+constexpr int PAD = 8;            // bf16 pad per smem row: conflict-free 16-byte reads
+
+struct AttnParams {
+  int mode;                       // 0 draft, 1 verify
+  int B, Hq, Hkv, dh, G;
+  int n_splits, chunk;            // prefix splits and rows per split
+  int rows_cap;                   // query nodes per request (draft: rows per request; verify: tree stride)
+  const uint16_t* q;              // draft: [n][Hq*dh]; verify: [B][S][Hq][dh]
+  const uint16_t* kp;             // prefix KV [B][cap][Hkv][dh]
+  const uint16_t* vp;
+  int kv_cap;
+  const int32_t* kv_len;
+  const uint16_t* kt;             // draft: [B][E][Hkv][dh] ; verify: [B][S][Hkv][dh]
+  const uint16_t* vt;
+  int tree_cap;                   // E or S
+  const uint64_t* anc;            // draft: pool.anc [B][E]; verify: tree.anc [B][S]
+  const int32_t* tree_size;       // verify: [B]
+  int e0;                         // draft: first expanded slot of this layer
+  float scale;
+  uint16_t* out_bf16;             // verify: [B][S][Hq][dh]
+  uint16_t* b_o;                  // draft: next GEMM operand (hi/lo), [2NP][kp]
+  int NP, bo_ld;
+  float* part;
+  int* counters;
+};
+
+__device__ __forceinline__ int n_nodes(const AttnParams& p, int b) {
+  return p.mode == 0 ? p.rows_cap : min(p.tree_size[b], p.rows_cap);
+}
+
+__device__ __forceinline__ const uint16_t* q_ptr(const AttnParams& p, int b, int node, int hq) {
+  return p.q + ((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * p.dh;
+}
+
+__device__ __forceinline__ uint64_t row_mask(const AttnParams& p, int b, int node) {
+  if (p.mode == 0) return p.anc[static_cast<size_t>(b) * p.tree_cap + p.e0 + node];
+  return p.anc[static_cast<size_t>(b) * p.tree_cap + node];
+}
+
+__global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) {
+  __shared__ __align__(16) uint16_t sk[TILE][MAX_DH + PAD];
+  __shared__ __align__(16) uint16_t sv[TILE][MAX_DH + PAD];
+  __shared__ float sq[8][MAX_DH];
+  __shared__ int s_last;
+
+  const int split = blockIdx.x;              // split == n_splits: the tree part
+  const int pair = blockIdx.y;
+  const int b = pair / p.Hkv, h = pair % p.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int dh = p.dh;
+  const int nodes = n_nodes(p, b);
+  const int R = nodes * p.G;
+  const bool is_tree = split == p.n_splits;
+  int lo = 0, hi = 0;
+  if (!is_tree) {
+    const int L = p.kv_len[b];
+    lo = split * p.chunk;
+    hi = min(L, lo + p.chunk);
+  } else {
+    hi = p.mode == 0 ? p.tree_cap : min(p.tree_size[b], p.tree_cap);
+  }
+  const int rec = dh + 2;
+
+  // Each warp owns query rows r = r0 + warp + 8 i (i < 8); running state in registers.
+  for (int r0 = 0; r0 < R; r0 += 64) {
+    float m_run[8], l_run[8], acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      m_run[i] = -INFINITY;
+      l_run[i] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
+    }
+    for (int t0 = lo; t0 < hi; t0 += TILE) {
+      const int nt = min(TILE, hi - t0);
+      __syncthreads();
+      const int pieces = dh / 8;
+      const uint16_t* ks = is_tree ? p.kt : p.kp;
+      const uint16_t* vs = is_tree ? p.vt : p.vp;
+      const int cap = is_tree ? p.tree_cap : p.kv_cap;
+      for (int idx = threadIdx.x; idx < nt * pieces; idx += THREADS) {
+        const int r = idx / pieces, c = idx % pieces;
+        const size_t g = ((static_cast<size_t>(b) * cap + t0 + r) * p.Hkv + h) * dh + c * 8;
+        *reinterpret_cast<uint4*>(&sk[r][c * 8]) = __ldg(reinterpret_cast<const uint4*>(ks + g));
+        *reinterpret_cast<uint4*>(&sv[r][c * 8]) = __ldg(reinterpret_cast<const uint4*>(vs + g));
+      }
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = r0 + warp + 8 * i;
+        if (r >= R) break;
+        const int node = r / p.G, hq = h * p.G + r % p.G;
+        const uint16_t* qg = q_ptr(p, b, node, hq);
+        for (int d = lane; d < dh; d += 32) sq[warp][d] = bf16_to_f32(qg[d]);
+        __syncwarp();
+        const uint64_t mask = is_tree ? row_mask(p, b, node) : ~0ull;
+        float sc[2];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int j = lane + 32 * half;
+          float s = -INFINITY;
+          const bool vis = j < nt && (!is_tree || ((mask >> (t0 + j)) & 1ull));
+          if (vis) {
+            float dot = 0.f;
+            for (int d0 = 0; d0 < dh; d0 += 8) {
+              const uint4 kv = *reinterpret_cast<const uint4*>(&sk[j][d0]);
+              const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                dot = fmaf(sq[warp][d0 + 2 * c], __uint_as_float(w[c] << 16), dot);
+                dot = fmaf(sq[warp][d0 + 2 * c + 1], __uint_as_float(w[c] & 0xffff0000u), dot);
+              }
+            }
+            s = dot * p.scale;
+          }
+          sc[half] = s;
+        }
+        const float tmax = warp_max(fmaxf(sc[0], sc[1]));
+        __syncwarp();
+        if (tmax == -INFINITY) continue;
+        const float m_new = fmaxf(m_run[i], tmax);
+        const float corr = __expf(m_run[i] - m_new);
+        const float p0 = sc[0] == -INFINITY ? 0.f : __expf(sc[0] - m_new);
+        const float p1 = sc[1] == -INFINITY ? 0.f : __expf(sc[1] - m_new);
+        l_run[i] = l_run[i] * corr + warp_sum(p0 + p1);
+        m_run[i] = m_new;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[i][c] *= corr;
+        for (int j = 0; j < nt; ++j) {
+          const float pj = __shfl_sync(0xffffffffu, j < 32 ? p0 : p1, j & 31);
+          if (pj == 0.f) continue;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int d = lane + 32 * c;
+            if (d < dh) acc[i][c] = fmaf(pj, bf16_to_f32(sv[j][d]), acc[i][c]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = r0 + warp + 8 * i;
+      if (r >= R) break;
+      const int node = r / p.G, hq = h * p.G + r % p.G;
+      const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
+      float* dst = p.part + (qi * (p.n_splits + 1) + split) * rec;
+      if (lane == 0) {
+        dst[0] = m_run[i];
+        dst[1] = l_run[i];
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int d = lane + 32 * c;
+        if (d < dh) dst[2 + d] = acc[i][c];
+      }
+    }
+  }
+
+  // the last CTA of this (request, kv head) merges the splits in order
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(&p.counters[pair], 1);
+    s_last = prev == p.n_splits;
+    if (s_last) p.counters[pair] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int r = warp; r < R; r += 8) {
+    const int node = r / p.G, hq = h * p.G + r % p.G;
+    const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
+    const float* src = p.part + qi * (p.n_splits + 1) * rec;
+    float M = -INFINITY;
+    for (int s = 0; s <= p.n_splits; ++s) M = fmaxf(M, __ldcg(src + s * rec));
+    float Lsum = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s <= p.n_splits; ++s) {
+      const float ms = __ldcg(src + s * rec);
+      if (ms == -INFINITY) continue;
+      const float wgt = __expf(ms - M);
+      Lsum += wgt * __ldcg(src + s * rec + 1);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int d = lane + 32 * c;
+        if (d < dh) o[c] += wgt * __ldcg(src + s * rec + 2 + d);
+      }
+    }
+    const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int d = lane + 32 * c;
+      if (d >= dh) continue;
+      const float v = o[c] * inv;
+      if (p.mode == 1) {
+        p.out_bf16[((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * dh + d] = f32_to_bf16(v);
+      } else {
+        const int j = b * p.rows_cap + node;
+        const int col = hq * dh + d;
+        uint16_t hi16, lo16;
+        split_bf16(v, hi16, lo16);
+        p.b_o[static_cast<size_t>(j) * p.bo_ld + col] = hi16;
+        p.b_o[static_cast<size_t>(p.NP + j) * p.bo_ld + col] = lo16;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+int attn_splits(const eagle_ctx* ctx, int pairs, int cap) {
+  int want = ceil_div(2 * ctx->sm_count, pairs < 1 ? 1 : pairs);
+  const int by_len = ceil_div(cap < 1 ? 1 : cap, TILE);
+  if (want > by_len) want = by_len;
+  if (want < 1) want = 1;
+  if (want > 32) want = 32;
+  return want;
+}
+
+static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
+  p.n_splits = attn_splits(ctx, p.B * p.Hkv, p.kv_cap);
+  p.chunk = ceil_div(ceil_div(p.kv_cap, p.n_splits), TILE) * TILE;
+  dim3 grid(p.n_splits + 1, p.B * p.Hkv);
+  trace_before(ctx, kernel_id, st);
+  tree_attn_kernel<<<grid, THREADS, 0, st>>>(p);
+  ctx->launches++;
+  trace_after(ctx, kernel_id, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_draft_attn(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st) {
+  const eagle_dims& D = ctx->dims;
+  const Workspace& W = ctx->ws;
+  AttnParams p{};
+  p.mode = 0;
+  p.B = L.batch;
+  p.Hq = D.n_q_heads;
+  p.Hkv = D.n_kv_heads;
+  p.dh = D.head_dim;
+  p.G = D.n_q_heads / D.n_kv_heads;
+  p.rows_cap = L.rpr;
+  p.q = ws_ptr<uint16_t>(L.ws, W.qrow);
+  p.kp = L.draft_kv->k;
+  p.vp = L.draft_kv->v;
+  p.kv_cap = L.draft_kv->cap;
+  p.kv_len = L.draft_kv->len;
+  p.kt = L.out->k_tree;
+  p.vt = L.out->v_tree;
+  p.tree_cap = ctx->lim.max_expanded;
+  p.anc = L.pool->anc;
+  p.e0 = L.e0;
+  p.scale = 1.0f / sqrtf(static_cast<float>(D.head_dim));
+  p.b_o = ws_ptr<uint16_t>(L.ws, W.b_o);
+  p.NP = L.NP;
+  p.bo_ld = W.kp_o;
+  p.part = ws_ptr<float>(L.ws, W.attn_part);
+  p.counters = ws_ptr<int>(L.ws, W.attn_cnt);
+  return run_attn(ctx, p, EAGLE_K_DRAFT_ATTN, st);
+}
+
+cudaError_t launch_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, const uint16_t* kt,
+                               const uint16_t* vt, const eagle_kv* prefix, const eagle_tree* tree,
+                               float scale, uint16_t* out, void* ws, cudaStream_t st) {
+  const eagle_dims& D = ctx->dims;
+  const Workspace& W = ctx->ws;
+  AttnParams p{};
+  p.mode = 1;
+  p.B = batch;
+  p.Hq = D.n_q_heads;
+  p.Hkv = D.n_kv_heads;
+  p.dh = D.head_dim;
+  p.G = D.n_q_heads / D.n_kv_heads;
+  p.rows_cap = tree->stride;
+  p.q = q;
+  p.kp = prefix->k;
+  p.vp = prefix->v;
+  p.kv_cap = prefix->cap;
+  p.kv_len = prefix->len;
+  p.kt = kt;
+  p.vt = vt;
+  p.tree_cap = tree->stride;
+  p.anc = tree->anc;
+  p.tree_size = tree->size;
+  p.scale = scale;
+  p.out_bf16 = out;
+  p.part = ws_ptr<float>(ws, W.attn_part);
+  p.counters = ws_ptr<int>(ws, W.attn_cnt) + ctx->lim.max_batch * D.n_kv_heads;
+  return run_attn(ctx, p, EAGLE_K_VERIFY_ATTN, st);
+}
+
+}  // namespace eagle

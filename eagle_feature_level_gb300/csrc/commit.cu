@@ -1,0 +1,131 @@
+// The commit transaction ([B] "KV Cache 必须按事务提交"; [A] §6.2 closing remark,
+// §12 item 3): the root and the accepted path become authoritative, rejected
+// branches are dropped by not copying them.  One CTA per (request, path
+// position): it copies that slot's K/V row of every target layer into the
+// cache at position L_b + i and gathers its true feature; position 0 also
+// writes the next round's state and appends the root's draft K/V row.
+#include "internal.h"
+#include "common.cuh"
+
+namespace eagle {
+namespace {
+
+struct CommitParams {
+  int n_layers, kv_cap, S, E, d, row_elems, path_cap, draft_cap;
+  const uint16_t* kt[EAGLE_MAX_LAYERS];
+  const uint16_t* vt[EAGLE_MAX_LAYERS];
+  uint16_t* kc[EAGLE_MAX_LAYERS];
+  uint16_t* vc[EAGLE_MAX_LAYERS];
+  const int32_t* accept_len;
+  const int32_t* path;
+  const int32_t* final_token;
+  const int32_t* last_slot;
+  const int32_t* t_token;
+  const float* f_true;
+  const int32_t* kv_len;
+  const uint16_t* dk_tree;
+  const uint16_t* dv_tree;
+  uint16_t* dk;
+  uint16_t* dv;
+  const int32_t* draft_len;
+  float* f_commit;
+  int32_t* tok_commit;
+  float* f_last;
+  int32_t* t_next;
+  int32_t* prefix_len_out;
+  int32_t* draft_len_out;
+};
+
+// rows are whole multiples of 8 bf16 (16 bytes)
+__device__ __forceinline__ void copy_row(uint16_t* dst, const uint16_t* src, int elems) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (int i = threadIdx.x; i < elems / 8; i += blockDim.x) d4[i] = s4[i];
+}
+
+__global__ void commit_kernel(const CommitParams p) {
+  const int b = blockIdx.x, i = blockIdx.y;
+  const int a = p.accept_len[b];
+  if (i > a) return;
+  const int slot = p.path[static_cast<size_t>(b) * p.path_cap + i];
+  const int L = p.kv_len[b];
+  for (int l = 0; l < p.n_layers; ++l) {
+    const size_t src = (static_cast<size_t>(b) * p.S + slot) * p.row_elems;
+    const size_t dst = (static_cast<size_t>(b) * p.kv_cap + L + i) * p.row_elems;
+    copy_row(p.kc[l] + dst, p.kt[l] + src, p.row_elems);
+    copy_row(p.vc[l] + dst, p.vt[l] + src, p.row_elems);
+  }
+  const float* f = p.f_true + (static_cast<size_t>(b) * p.S + slot) * p.d;
+  float* fc = p.f_commit + (static_cast<size_t>(b) * p.path_cap + i) * p.d;
+  for (int c = threadIdx.x; c < p.d; c += blockDim.x) fc[c] = f[c];
+  if (threadIdx.x == 0) {
+    int32_t* tc = p.tok_commit + static_cast<size_t>(b) * (p.path_cap + 1);
+    tc[i] = p.t_token[static_cast<size_t>(b) * p.S + slot];
+    if (i == a) tc[a + 1] = p.final_token[b];
+  }
+  if (i == 0) {
+    const int last = p.last_slot[b];
+    const float* fl = p.f_true + (static_cast<size_t>(b) * p.S + last) * p.d;
+    for (int c = threadIdx.x; c < p.d; c += blockDim.x) p.f_last[static_cast<size_t>(b) * p.d + c] = fl[c];
+    if (threadIdx.x == 0) {
+      p.t_next[b] = p.final_token[b];
+      p.prefix_len_out[b] = L + 1 + a;
+    }
+    if (p.dk) {
+      const int Ld = p.draft_len[b];
+      const size_t src = (static_cast<size_t>(b) * p.E + 0) * p.row_elems;
+      const size_t dst = (static_cast<size_t>(b) * p.draft_cap + Ld) * p.row_elems;
+      copy_row(p.dk + dst, p.dk_tree + src, p.row_elems);
+      copy_row(p.dv + dst, p.dv_tree + src, p.row_elems);
+      if (threadIdx.x == 0) p.draft_len_out[b] = Ld + 1;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st) {
+  CommitParams p{};
+  p.n_layers = C.n_layers;
+  p.kv_cap = C.kv_cap;
+  p.S = C.tree->stride;
+  p.E = ctx->lim.max_expanded;
+  p.d = ctx->dims.d;
+  p.row_elems = ctx->dims.n_kv_heads * ctx->dims.head_dim;
+  p.path_cap = C.acc->path_cap;
+  for (int l = 0; l < C.n_layers; ++l) {
+    p.kt[l] = C.kt[l];
+    p.vt[l] = C.vt[l];
+    p.kc[l] = C.kc[l];
+    p.vc[l] = C.vc[l];
+  }
+  p.accept_len = C.acc->accept_len;
+  p.path = C.acc->path;
+  p.final_token = C.acc->final_token;
+  p.last_slot = C.acc->last_slot;
+  p.t_token = C.tree->token;
+  p.f_true = C.f_true;
+  p.kv_len = C.kv_len;
+  if (C.draft && C.draft_kv) {
+    p.dk_tree = C.draft->k_tree;
+    p.dv_tree = C.draft->v_tree;
+    p.dk = C.draft_kv->k;
+    p.dv = C.draft_kv->v;
+    p.draft_cap = C.draft_kv->cap;
+    p.draft_len = C.draft_kv->len;
+  }
+  p.f_commit = C.out->f_commit;
+  p.tok_commit = C.out->tok_commit;
+  p.f_last = C.out->f_last;
+  p.t_next = C.out->t_next;
+  p.prefix_len_out = C.out->prefix_len;
+  p.draft_len_out = C.out->draft_len;
+  dim3 grid(C.batch, C.acc->path_cap);
+  trace_before(ctx, EAGLE_K_COMMIT, st);
+  commit_kernel<<<grid, 128, 0, st>>>(p);
+  ctx->launches++;
+  trace_after(ctx, EAGLE_K_COMMIT, st);
+  return cudaGetLastError();
+}
+
+}  // namespace eagle

@@ -1,0 +1,152 @@
+// Device helpers shared by the libeagle kernels: bf16 bit handling, the
+// hi/lo bf16 split of fp32 activations, Philox4x32-10, block reductions and
+// the device status word.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/eagle.h"
+
+namespace eagle {
+
+// ---- bf16 as raw bits ------------------------------------------------------
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Round-to-nearest-even fp32 -> bf16 bits.
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): two bf16 operands whose
+// sum carries ~16 mantissa bits, so bf16 tensor-core products of fp32
+// activations keep fp32-level accuracy.
+__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
+  hi = f32_to_bf16(x);
+  lo = f32_to_bf16(x - bf16_to_f32(hi));
+}
+
+// ---- Philox4x32-10 (Salmon et al., SC'11) -----------------------------------
+// Four 32-bit counter words, two key words, ten rounds; words 0 and 2 are
+// multiplied by the two round constants, the key is bumped by the Weyl
+// constants between rounds.
+struct Philox4 { uint32_t x, y, z, w; };
+
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2,
+                                                 uint32_t c3, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+    const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+  }
+  return {c0, c1, c2, c3};
+}
+
+enum : uint32_t { PURPOSE_DRAW = 0, PURPOSE_ACCEPT = 1, PURPOSE_FINAL = 2, KEY_TAG = 0x000EA61Eu };
+
+// The round's uniform stream: key (seed, tag), counter
+// (draw index, node slot, purpose << 16 | request, round), word 0.
+__device__ __forceinline__ uint32_t round_uniform(uint32_t seed, uint32_t draw_index, uint32_t slot,
+                                                  uint32_t purpose, uint32_t request, uint32_t round_id) {
+  return philox4x32_10(draw_index, slot, (purpose << 16) | request, round_id, seed, KEY_TAG).x;
+}
+
+// t = floor(u32 * S / 2^32) for S < 2^63.
+__device__ __forceinline__ uint64_t scale_uniform(uint32_t u, uint64_t S) {
+  const uint64_t lo = static_cast<uint64_t>(u) * (S & 0xffffffffull);
+  const uint64_t hi = static_cast<uint64_t>(u) * (S >> 32);
+  return hi + (lo >> 32);
+}
+
+constexpr int QBITS = 40;
+
+// W = floor(p * 2^40) for p in [0, 1] (exact: power-of-two scale).
+__device__ __forceinline__ uint64_t quantize_prob(float p) {
+  const double x = static_cast<double>(p) * 1099511627776.0;
+  return x > 0.0 ? static_cast<uint64_t>(x) : 0ull;  // truncation == floor for x >= 0
+}
+
+// ---- reductions -----------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_max_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide reductions over blockDim.x threads (multiple of 32, <= 1024),
+// with a fixed combination order (deterministic).  `scratch` holds >= 32
+// entries; every thread gets the result.
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum(v);
+  __syncthreads();
+  if (lane == 0) scratch[wid] = v;
+  __syncthreads();
+  float r = lane < nw ? scratch[lane] : 0.f;
+  r = warp_sum(r);
+  return r;
+}
+__device__ __forceinline__ float block_max(float v, float* scratch) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) scratch[wid] = v;
+  __syncthreads();
+  float r = lane < nw ? scratch[lane] : -INFINITY;
+  return warp_max(r);
+}
+__device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* scratch) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_sum_u64(v);
+  __syncthreads();
+  if (lane == 0) scratch[wid] = v;
+  __syncthreads();
+  uint64_t r = lane < nw ? scratch[lane] : 0ull;
+  return warp_sum_u64(r);
+}
+__device__ __forceinline__ int block_max_i(int v, int* scratch) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  v = warp_max_i(v);
+  __syncthreads();
+  if (lane == 0) scratch[wid] = v;
+  __syncthreads();
+  int r = lane < nw ? scratch[lane] : INT32_MIN;
+  return warp_max_i(r);
+}
+
+// ---- device status word -----------------------------------------------------
+// First int of the workspace.  The first error wins; later ones are dropped.
+__device__ __forceinline__ void set_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// A device-side wait gives up after this long and reports EAGLE_ERR_TIMEOUT.
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+}  // namespace eagle

@@ -1,0 +1,635 @@
+// Weight-streaming GEMM for the draft head's contractions (FC, QKV, O,
+// gate/up, down, LM head), Y[n][out] = X[n][K] . W[out][K]^T with n = draft
+// rows (1..256) and W streamed from HBM exactly once per launch.
+//
+// Blackwell design:
+//  * the weight tile (128 rows x 64 k, two 64-row TMA boxes, 128-byte swizzle)
+//    and the activation tile are brought in by TMA into a multi-stage
+//    shared-memory ring guarded by mbarriers;
+//  * one thread issues tcgen05.mma (M = 128 weight rows, N = activation rows,
+//    "swap-AB"), accumulating in tensor memory; a commit per stage releases the
+//    ring slot;
+//  * activations enter as two bf16 halves (x = hi + lo), stacked along N, so
+//    the fp32 activation keeps ~16 mantissa bits while the weights stay bf16;
+//  * work is split stream-K style: the (tile, k-block) units of the whole
+//    matrix are divided evenly over one CTA per SM, so every SM streams the
+//    same number of bytes; each CTA writes its fp32 partial of a tile and the
+//    last CTA to finish the tile sums the partials in CTA order
+//    (deterministic);
+//  * the epilogue of that last CTA fuses the layer's elementwise work: bias,
+//    residual adds, RMSNorm scaling (sum of squares carried as per-tile
+//    partials), RoPE, SiLU-gating, the bf16 hi/lo split of the next
+//    contraction's input, and the scatter into per-node outputs.
+// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer and tensor-memory
+// owner, warps 2-5 = epilogue (one tensor-memory lane quarter each).
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace eagle {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int BOX_BYTES = 64 * BK * 2;
+constexpr int NUM_THREADS = 192;
+constexpr int EPI_THREADS = 128;
+constexpr int XCH_ROWS = 32;
+
+struct GemmParams {
+  int epi;
+  int n, NP, kb, m_tiles;
+  long long total_units;
+  int mblk[3];
+  int n_mats;
+  int two_mma;
+  int tmem_cols, acc_stride, n_acc, stages;
+  uint32_t b_stage_bytes, b_box_rows;
+  int rpr, e0, E;
+  int d, F, V, Hq, Hkv, dh;
+  float eps;
+  double ln_theta;
+  const float* bias;
+  const float* gain;
+  const float* ss_in;
+  int ss_in_tiles;
+  float* ss_out;
+  const float* resid;
+  float* out_f32;
+  uint16_t* bnext;
+  int kp_next;
+  uint16_t* qrow;
+  uint16_t* k_tree;
+  uint16_t* v_tree;
+  const int32_t* pos0;
+  const int32_t* depth;
+  float* part;
+  int* counters;
+  int* status;
+};
+
+struct Smem {
+  uint8_t* a;       // stages x 16 KB
+  uint8_t* b;       // stages x b_stage_bytes
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* tfull;  // [2]
+  uint64_t* tempty; // [2]
+  uint32_t* tmem_holder;
+  int* flags;       // [0] abort, [1] last-arriver, [2] wait ok
+  float* xch;       // [32][128]
+  float* red;       // [4][32]
+  float* rs;        // [32]
+};
+
+__host__ __device__ inline size_t smem_bytes_for(int stages, uint32_t b_stage) {
+  size_t s = 1024;                                  // alignment slack
+  s += static_cast<size_t>(stages) * (A_STAGE_BYTES + b_stage);
+  s += (2 * stages + 4) * 8 + 64;
+  s += XCH_ROWS * BM * 4 + 4 * 32 * 4 + 32 * 4;
+  return s;
+}
+
+__device__ inline Smem carve(uint8_t* raw, const GemmParams& p) {
+  uintptr_t base = (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023);
+  uint8_t* ptr = reinterpret_cast<uint8_t*>(base);
+  Smem s;
+  s.a = ptr;
+  ptr += static_cast<size_t>(p.stages) * A_STAGE_BYTES;
+  s.b = ptr;
+  ptr += static_cast<size_t>(p.stages) * p.b_stage_bytes;
+  s.full = reinterpret_cast<uint64_t*>(ptr);
+  s.empty = s.full + p.stages;
+  s.tfull = s.empty + p.stages;
+  s.tempty = s.tfull + 2;
+  s.tmem_holder = reinterpret_cast<uint32_t*>(s.tempty + 2);
+  s.flags = reinterpret_cast<int*>(s.tmem_holder + 4);
+  s.xch = reinterpret_cast<float*>(s.flags + 12);
+  s.red = s.xch + XCH_ROWS * BM;
+  s.rs = s.red + 4 * 32;
+  return s;
+}
+
+// CTA that owns k-block unit u under the even split of T units over G CTAs
+// (CTA c owns [floor(c T / G), floor((c+1) T / G))).
+__device__ __forceinline__ int cta_of_unit(long long u, long long T, int G) {
+  return static_cast<int>(((u + 1) * G - 1) / T);
+}
+
+__device__ __forceinline__ void locate_box(const GemmParams& p, int t, int half, int& map, int& row) {
+  if (p.epi == EPI_GATEUP) {          // box 0: gate rows, box 1: up rows of the same 64 columns
+    map = half;
+    row = t * 64;
+    return;
+  }
+  const int blk = 2 * t + half;
+  int prev = 0;
+  for (int i = 0; i < p.n_mats; ++i) {
+    if (blk < p.mblk[i] || i == p.n_mats - 1) {
+      map = i;
+      row = (blk - prev) * 64;
+      return;
+    }
+    prev = p.mblk[i];
+  }
+  map = 0;
+  row = 0;
+}
+
+__device__ __forceinline__ void put_split(uint16_t* buf, int NP, int kp, int j, int col, float x) {
+  uint16_t hi, lo;
+  split_bf16(x, hi, lo);
+  buf[static_cast<size_t>(j) * kp + col] = hi;
+  buf[static_cast<size_t>(NP + j) * kp + col] = lo;
+}
+
+// Per-warp sums of v for each of nj rows into red[warp][row].
+__device__ __forceinline__ void reduce_rows(const Smem& s, float (&v)[XCH_ROWS], int nj, int m) {
+  const int lane = m & 31, w = m >> 5;
+#pragma unroll
+  for (int jj = 0; jj < XCH_ROWS; ++jj) {
+    if (jj < nj) {
+      const float t = warp_sum(v[jj]);
+      if (lane == 0) s.red[w * 32 + jj] = t;
+    }
+  }
+  sm100::named_barrier(1, EPI_THREADS);
+}
+
+// Final epilogue of tile t: sum the partials of CTAs [c_first, c_last] and
+// apply the contraction's fused elementwise work.  `m` is the tile row this
+// thread owns (its tensor-memory lane); m >> 5 names its warp, m & 31 its lane.
+__device__ void finalize_tile(const GemmParams& p, const Smem& s, int t, int c_first, int c_last, int m) {
+  for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
+    const int nj = min(XCH_ROWS, p.n - jc);
+    float acc[XCH_ROWS];
+#pragma unroll
+    for (int jj = 0; jj < XCH_ROWS; ++jj) {
+      acc[jj] = 0.f;
+      if (jj < nj) {
+        const int j = jc + jj;
+        for (int c = c_first; c <= c_last; ++c)
+          acc[jj] += __ldcg(p.part + (static_cast<size_t>(t + c) * p.n + j) * BM + m);
+      }
+    }
+    // RMSNorm scale of the input rows (QKV: after FC, GATEUP: after O)
+    if (p.epi == EPI_QKV || p.epi == EPI_GATEUP) {
+      if (m < nj) {
+        const int j = jc + m;
+        float ss = 0.f;
+        for (int i = 0; i < p.ss_in_tiles; ++i) ss += __ldcg(p.ss_in + static_cast<size_t>(j) * p.ss_in_tiles + i);
+        s.rs[m] = 1.0f / sqrtf(ss / static_cast<float>(p.d) + p.eps);
+      }
+      sm100::named_barrier(1, EPI_THREADS);
+#pragma unroll
+      for (int jj = 0; jj < XCH_ROWS; ++jj)
+        if (jj < nj) acc[jj] *= s.rs[jj];
+#pragma unroll
+      for (int jj = 0; jj < XCH_ROWS; ++jj)
+        if (jj < nj) s.xch[jj * BM + m] = acc[jj];
+      sm100::named_barrier(1, EPI_THREADS);
+    }
+
+    if (p.epi == EPI_FC || p.epi == EPI_O) {
+      const int gi = t * BM + m;
+      const bool valid = gi < p.d;
+      float sq[XCH_ROWS];
+#pragma unroll
+      for (int jj = 0; jj < XCH_ROWS; ++jj) {
+        sq[jj] = 0.f;
+        if (jj < nj && valid) {
+          const int j = jc + jj;
+          float v = acc[jj];
+          if (p.epi == EPI_FC) v += p.bias[gi];
+          else v += p.resid[static_cast<size_t>(j) * p.d + gi];
+          p.out_f32[static_cast<size_t>(j) * p.d + gi] = v;
+          put_split(p.bnext, p.NP, p.kp_next, j, gi, v * p.gain[gi]);
+          sq[jj] = v * v;
+        }
+      }
+      reduce_rows(s, sq, nj, m);
+      if (m < nj) {
+        const float tot = s.red[m] + s.red[32 + m] + s.red[64 + m] + s.red[96 + m];
+        p.ss_out[static_cast<size_t>(jc + m) * p.m_tiles + t] = tot;
+      }
+      sm100::named_barrier(1, EPI_THREADS);
+    } else if (p.epi == EPI_QKV) {
+      const int gi = t * BM + m;
+      const int qd = p.Hq * p.dh, kd = p.Hkv * p.dh;
+      const int half = p.dh >> 1;
+      if (gi < qd + 2 * kd) {
+        const bool is_v = gi >= qd + kd;
+        const int base = gi < qd ? 0 : (gi < qd + kd ? qd : qd + kd);
+        const int head = (gi - base) / p.dh, i = (gi - base) % p.dh;
+        const int ii = i < half ? i : i - half;
+        const int partner = i < half ? m + half : m - half;
+        const double inv_freq = exp(-(2.0 * ii / p.dh) * p.ln_theta);
+#pragma unroll
+        for (int jj = 0; jj < XCH_ROWS; ++jj) {
+          if (jj >= nj) continue;
+          const int j = jc + jj;
+          const int b = j / p.rpr, e = p.e0 + j % p.rpr;
+          float v = acc[jj];
+          if (!is_v) {
+            const int pos = p.pos0[b] + p.depth[static_cast<size_t>(b) * p.E + e];
+            double ang = static_cast<double>(pos) * inv_freq;
+            ang -= 6.283185307179586 * rint(ang * 0.15915494309189535);
+            float sn, cs;
+            sincosf(static_cast<float>(ang), &sn, &cs);
+            const float other = s.xch[jj * BM + partner];
+            v = i < half ? v * cs - other * sn : v * cs + other * sn;
+          }
+          if (gi < qd) {
+            p.qrow[static_cast<size_t>(j) * qd + gi] = f32_to_bf16(v);
+          } else {
+            uint16_t* dst = is_v ? p.v_tree : p.k_tree;
+            dst[((static_cast<size_t>(b) * p.E + e) * p.Hkv + head) * p.dh + i] = f32_to_bf16(v);
+          }
+        }
+      }
+      sm100::named_barrier(1, EPI_THREADS);
+    } else if (p.epi == EPI_GATEUP) {
+      const int c = t * 64 + m;
+      if (m < 64 && c < p.F) {
+#pragma unroll
+        for (int jj = 0; jj < XCH_ROWS; ++jj) {
+          if (jj >= nj) continue;
+          const float g = acc[jj], u = s.xch[jj * BM + m + 64];
+          const float sg = g / (1.0f + expf(-g));
+          put_split(p.bnext, p.NP, p.kp_next, jc + jj, c, sg * u);
+        }
+      }
+      sm100::named_barrier(1, EPI_THREADS);
+    } else if (p.epi == EPI_DOWN) {
+      const int gi = t * BM + m;
+      if (gi < p.d) {
+#pragma unroll
+        for (int jj = 0; jj < XCH_ROWS; ++jj) {
+          if (jj >= nj) continue;
+          const int j = jc + jj;
+          const int b = j / p.rpr, e = p.e0 + j % p.rpr;
+          const float v = acc[jj] + p.resid[static_cast<size_t>(j) * p.d + gi];
+          p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.d + gi] = v;
+          put_split(p.bnext, p.NP, p.kp_next, j, gi, v);
+        }
+      }
+    } else {  // EPI_LM
+      const int gi = t * BM + m;
+      if (gi < p.V) {
+#pragma unroll
+        for (int jj = 0; jj < XCH_ROWS; ++jj) {
+          if (jj >= nj) continue;
+          const int j = jc + jj;
+          const int b = j / p.rpr, e = p.e0 + j % p.rpr;
+          p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.V + gi] = acc[jj];
+        }
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_stream_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
+                       const __grid_constant__ CUtensorMap mA2, const __grid_constant__ CUtensorMap mB,
+                       const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const Smem s = carve(smem_raw, p);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long T = p.total_units;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const long long u_begin = static_cast<long long>(cta) * T / G;
+  const long long u_end = static_cast<long long>(cta + 1) * T / G;
+  volatile int* abort_flag = s.flags;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      sm100::mbar_init(&s.full[i], 1);
+      sm100::mbar_init(&s.empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      sm100::mbar_init(&s.tfull[i], 1);
+      sm100::mbar_init(&s.tempty[i], 4);
+    }
+    s.flags[0] = 0;
+    s.flags[1] = 0;
+    s.flags[2] = 0;
+    sm100::fence_barrier_init();
+    sm100::fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    sm100::tma_prefetch_desc(&mA0);
+    sm100::tma_prefetch_desc(&mB);
+  }
+  if (warp == 1) {
+    sm100::tmem_alloc(s.tmem_holder, p.tmem_cols);
+    sm100::tmem_relinquish();
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::tc_fence_after();
+  const uint32_t tmem_base = *s.tmem_holder;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      for (long long u = u_begin; u < u_end; ++u) {
+        const int t = static_cast<int>(u / p.kb), kblk = static_cast<int>(u % p.kb);
+        if (!sm100::mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
+          *abort_flag = 1;
+          set_status(p.status, EAGLE_ERR_TIMEOUT);
+          break;
+        }
+        sm100::mbar_arrive_expect_tx(&s.full[stage], A_STAGE_BYTES + p.b_stage_bytes);
+        uint8_t* a_dst = s.a + static_cast<size_t>(stage) * A_STAGE_BYTES;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          int map, row;
+          locate_box(p, t, h, map, row);
+          const CUtensorMap* mp = map == 0 ? &mA0 : (map == 1 ? &mA1 : &mA2);
+          sm100::tma_load_2d(a_dst + h * BOX_BYTES, mp, kblk * BK, row, &s.full[stage]);
+        }
+        uint8_t* b_dst = s.b + static_cast<size_t>(stage) * p.b_stage_bytes;
+        sm100::tma_load_2d(b_dst, &mB, kblk * BK, 0, &s.full[stage]);
+        if (p.b_box_rows < 2u * p.NP)
+          sm100::tma_load_2d(b_dst + p.b_box_rows * 128u, &mB, kblk * BK, static_cast<int>(p.b_box_rows),
+                             &s.full[stage]);
+        ++issued;
+        if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+      }
+      if (*abort_flag) {
+        // let copies already in flight land before the CTA exits
+        const long long pending = issued < p.stages ? issued : p.stages;
+        for (long long i = 0; i < pending; ++i) {
+          stage = stage == 0 ? p.stages - 1 : stage - 1;
+          if (stage == p.stages - 1) phase ^= 1u;
+          const uint64_t t0 = globaltimer_ns();
+          while (!sm100::mbar_try_wait(&s.full[stage], phase) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t n_total = 2u * p.NP;
+      const uint32_t idesc = p.two_mma ? sm100::idesc_bf16_f32(BM, p.NP) : sm100::idesc_bf16_f32(BM, n_total);
+      int stage = 0;
+      uint32_t phase = 0;
+      int seg = 0;
+      long long u = u_begin;
+      bool ok = true;
+      while (u < u_end && ok) {
+        const int t = static_cast<int>(u / p.kb);
+        const long long seg_end = min(u_end, static_cast<long long>(t + 1) * p.kb);
+        const int buf = seg % p.n_acc;
+        const uint32_t aph = static_cast<uint32_t>(seg / p.n_acc) & 1u;
+        if (!sm100::mbar_wait(&s.tempty[buf], aph ^ 1u, abort_flag)) {
+          *abort_flag = 1;
+          set_status(p.status, EAGLE_ERR_TIMEOUT);
+          break;
+        }
+        sm100::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
+        const long long seg_start = u;
+        for (; u < seg_end; ++u) {
+          if (!sm100::mbar_wait(&s.full[stage], phase, abort_flag)) {
+            *abort_flag = 1;
+            set_status(p.status, EAGLE_ERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+          sm100::tc_fence_after();
+          const uint32_t a_addr = sm100::smem_u32(s.a + static_cast<size_t>(stage) * A_STAGE_BYTES);
+          const uint32_t b_addr = sm100::smem_u32(s.b + static_cast<size_t>(stage) * p.b_stage_bytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sm100::smem_desc_sw128(a_addr + kk * 32);
+            const uint32_t accum = (u != seg_start || kk > 0) ? 1u : 0u;
+            sm100::mma_bf16(d_tmem, ad, sm100::smem_desc_sw128(b_addr + kk * 32), idesc, accum);
+            if (p.two_mma)
+              sm100::mma_bf16(d_tmem + p.NP, ad, sm100::smem_desc_sw128(b_addr + p.NP * 128 + kk * 32), idesc,
+                              accum);
+          }
+          sm100::mma_commit(&s.empty[stage]);
+          if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        sm100::mma_commit(&s.tfull[buf]);
+        ++seg;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int et = threadIdx.x - 64;            // 0..127
+    const int quarter = warp & 3;               // tensor-memory lanes this warp may read
+    const int m = quarter * 32 + lane;          // tile row held by this thread
+    int seg = 0;
+    long long u = u_begin;
+    while (u < u_end) {
+      const int t = static_cast<int>(u / p.kb);
+      const long long seg_end = min(u_end, static_cast<long long>(t + 1) * p.kb);
+      u = seg_end;
+      const int buf = seg % p.n_acc;
+      const uint32_t aph = static_cast<uint32_t>(seg / p.n_acc) & 1u;
+      ++seg;
+      if (et == 0) s.flags[2] = sm100::mbar_wait(&s.tfull[buf], aph, abort_flag) ? 1 : 0;
+      sm100::named_barrier(1, EPI_THREADS);
+      if (!s.flags[2]) {
+        if (et == 0) {
+          *abort_flag = 1;
+          set_status(p.status, EAGLE_ERR_TIMEOUT);
+        }
+        break;
+      }
+      sm100::tc_fence_after();
+      const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 static_cast<uint32_t>(buf * p.acc_stride);
+      const int slot = t + cta;
+      for (int c0 = 0; c0 < p.NP; c0 += 8) {
+        float hi[8], lo[8];
+        sm100::tmem_ld8(lane_addr + c0, hi);
+        sm100::tmem_ld8(lane_addr + p.NP + c0, lo);
+        sm100::tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int j = c0 + i;
+          if (j < p.n) p.part[(static_cast<size_t>(slot) * p.n + j) * BM + m] = hi[i] + lo[i];
+        }
+      }
+      sm100::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) sm100::mbar_arrive(&s.tempty[buf]);
+      __threadfence();
+      sm100::named_barrier(1, EPI_THREADS);
+      const int c_first = cta_of_unit(static_cast<long long>(t) * p.kb, T, G);
+      const int c_last = cta_of_unit(static_cast<long long>(t) * p.kb + p.kb - 1, T, G);
+      if (et == 0) {
+        const int prev = atomicAdd(&p.counters[t], 1);
+        const int last = prev == c_last - c_first;
+        if (last) p.counters[t] = 0;
+        s.flags[1] = last;
+      }
+      sm100::named_barrier(1, EPI_THREADS);
+      if (s.flags[1]) {
+        __threadfence();
+        finalize_tile(p, s, t, c_first, c_last, m);
+      }
+      sm100::named_barrier(1, EPI_THREADS);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    sm100::tc_fence_after();
+    sm100::tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+bool encode_2d(eagle_ctx* ctx, CUtensorMap* map, const void* ptr, int inner, int rows, int ld_elems,
+               int box_inner, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_elems) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStream_t st) {
+  const eagle_dims& D = ctx->dims;
+  const Workspace& W = ctx->ws;
+  const eagle_draft_weights* w = L.w;
+  const int qd = D.n_q_heads * D.head_dim, kd = D.n_kv_heads * D.head_dim;
+  GemmParams p{};
+  p.epi = epi;
+  p.n = L.n;
+  p.NP = L.NP;
+  p.rpr = L.rpr;
+  p.e0 = L.e0;
+  p.E = ctx->lim.max_expanded;
+  p.d = D.d;
+  p.F = D.d_ff;
+  p.V = D.vocab;
+  p.Hq = D.n_q_heads;
+  p.Hkv = D.n_kv_heads;
+  p.dh = D.head_dim;
+  p.eps = D.rms_eps;
+  p.ln_theta = log(static_cast<double>(D.rope_theta));
+  p.status = ws_ptr<int>(L.ws, W.status);
+  p.part = ws_ptr<float>(L.ws, W.gemm_part);
+  p.counters = ws_ptr<int>(L.ws, W.gemm_cnt) + epi * W.max_mtiles;
+  const int tiles_d = ceil_div(D.d, BM);
+
+  const uint16_t* mats[3] = {nullptr, nullptr, nullptr};
+  int rows[3] = {0, 0, 0}, lds[3] = {0, 0, 0};
+  int K = 0, kp_in = 0;
+  size_t b_in = 0;
+  int n_out = 0;
+  switch (epi) {
+    case EPI_FC:
+      mats[0] = w->w_fc; rows[0] = D.d; lds[0] = w->ld_fc; K = 2 * D.d;
+      b_in = W.b_fc; kp_in = W.kp_fc; n_out = D.d;
+      p.bias = w->b_fc; p.gain = w->g1;
+      p.out_f32 = ws_ptr<float>(L.ws, W.h);
+      p.bnext = ws_ptr<uint16_t>(L.ws, W.b_qkv); p.kp_next = W.kp_qkv;
+      p.ss_out = ws_ptr<float>(L.ws, W.ss_fc);
+      break;
+    case EPI_QKV:
+      mats[0] = w->wq; rows[0] = qd; lds[0] = w->ld_q;
+      mats[1] = w->wk; rows[1] = kd; lds[1] = w->ld_k;
+      mats[2] = w->wv; rows[2] = kd; lds[2] = w->ld_v;
+      K = D.d; b_in = W.b_qkv; kp_in = W.kp_qkv; n_out = qd + 2 * kd;
+      p.ss_in = ws_ptr<float>(L.ws, W.ss_fc); p.ss_in_tiles = tiles_d;
+      p.qrow = ws_ptr<uint16_t>(L.ws, W.qrow);
+      p.k_tree = L.out->k_tree; p.v_tree = L.out->v_tree;
+      p.pos0 = L.req->pos0; p.depth = L.pool->depth;
+      break;
+    case EPI_O:
+      mats[0] = w->wo; rows[0] = D.d; lds[0] = w->ld_o; K = qd;
+      b_in = W.b_o; kp_in = W.kp_o; n_out = D.d;
+      p.gain = w->g2;
+      p.resid = ws_ptr<float>(L.ws, W.h);
+      p.out_f32 = ws_ptr<float>(L.ws, W.h2);
+      p.bnext = ws_ptr<uint16_t>(L.ws, W.b_gu); p.kp_next = W.kp_gu;
+      p.ss_out = ws_ptr<float>(L.ws, W.ss_o);
+      break;
+    case EPI_GATEUP:
+      mats[0] = w->w_gate; rows[0] = D.d_ff; lds[0] = w->ld_gate;
+      mats[1] = w->w_up; rows[1] = D.d_ff; lds[1] = w->ld_up;
+      K = D.d; b_in = W.b_gu; kp_in = W.kp_gu; n_out = 2 * D.d_ff;
+      p.ss_in = ws_ptr<float>(L.ws, W.ss_o); p.ss_in_tiles = tiles_d;
+      p.bnext = ws_ptr<uint16_t>(L.ws, W.b_down); p.kp_next = W.kp_down;
+      break;
+    case EPI_DOWN:
+      mats[0] = w->w_down; rows[0] = D.d; lds[0] = w->ld_down; K = D.d_ff;
+      b_in = W.b_down; kp_in = W.kp_down; n_out = D.d;
+      p.resid = ws_ptr<float>(L.ws, W.h2);
+      p.out_f32 = L.out->f_hat;
+      p.bnext = ws_ptr<uint16_t>(L.ws, W.b_lm); p.kp_next = W.kp_lm;
+      break;
+    default:  // EPI_LM
+      mats[0] = w->w_lm; rows[0] = D.vocab; lds[0] = w->ld_lm; K = D.d;
+      b_in = W.b_lm; kp_in = W.kp_lm; n_out = D.vocab;
+      p.out_f32 = L.out->logits;
+      break;
+  }
+  p.n_mats = epi == EPI_QKV ? 3 : (epi == EPI_GATEUP ? 2 : 1);
+  int cum = 0;
+  for (int i = 0; i < p.n_mats; ++i) {
+    cum += ceil_div(rows[i], 64);
+    p.mblk[i] = cum;
+  }
+  p.m_tiles = epi == EPI_GATEUP ? ceil_div(D.d_ff, 64) : ceil_div(n_out, BM);
+  p.kb = ceil_div(K, BK);
+  p.total_units = static_cast<long long>(p.m_tiles) * p.kb;
+  p.two_mma = 2 * p.NP > 256 ? 1 : 0;
+  p.b_box_rows = static_cast<uint32_t>(p.two_mma ? p.NP : 2 * p.NP);
+  p.b_stage_bytes = static_cast<uint32_t>(2 * p.NP * 128);
+  const int acc_cols = 2 * p.NP;
+  p.acc_stride = acc_cols < 32 ? 32 : (acc_cols + 31) / 32 * 32;
+  p.n_acc = 2 * p.acc_stride <= 512 ? 2 : 1;
+  const int need = p.n_acc * p.acc_stride;
+  int cols = 32;
+  while (cols < need) cols <<= 1;
+  p.tmem_cols = cols;
+
+  const size_t smem_cap = 232448;
+  int stages = 8;
+  while (stages > 2 && smem_bytes_for(stages, p.b_stage_bytes) > smem_cap) --stages;
+  p.stages = stages;
+  size_t smem = smem_bytes_for(stages, p.b_stage_bytes);
+  if (smem < 120 * 1024) smem = 120 * 1024;    // one CTA per SM: tensor memory is never contended
+
+  CUtensorMap maps[3], mb;
+  for (int i = 0; i < 3; ++i) {
+    const int src = i < p.n_mats ? i : 0;
+    if (!encode_2d(ctx, &maps[i], mats[src], K, rows[src], lds[src], BK, 64)) return cudaErrorInvalidValue;
+  }
+  if (!encode_2d(ctx, &mb, ws_ptr<uint16_t>(L.ws, b_in), kp_in, 2 * p.NP, kp_in, BK, p.b_box_rows))
+    return cudaErrorInvalidValue;
+
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_cap));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int grid = ctx->sm_count;
+  if (p.total_units < grid) grid = static_cast<int>(p.total_units);
+  trace_before(ctx, epi, st);
+  gemm_stream_kernel<<<grid, NUM_THREADS, smem, st>>>(maps[0], maps[1], maps[2], mb, p);
+  ctx->launches++;
+  trace_after(ctx, epi, st);
+  return cudaGetLastError();
+}
+
+}  // namespace eagle

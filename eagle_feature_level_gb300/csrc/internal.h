@@ -1,0 +1,137 @@
+// Host-side internals of libeagle: the context, the workspace layout and the
+// launchers each kernel file provides.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/eagle.h"
+
+namespace eagle {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// GEMM epilogue kinds (one per contraction of the draft step).
+enum Epi : int { EPI_FC = 0, EPI_QKV = 1, EPI_O = 2, EPI_GATEUP = 3, EPI_DOWN = 4, EPI_LM = 5 };
+
+// Activation rows are padded to NP; the GEMM's B operand holds the bf16 "hi"
+// parts in rows [0, NP) and the "lo" parts in rows [NP, 2NP).  NP is a
+// multiple of 8 (one MMA of N = 2NP <= 256) or of 16 beyond 128 rows (two
+// MMAs of N = NP).
+inline int padded_rows(int n) {
+  if (n <= 8) return 8;
+  if (n <= 128) return (n + 7) / 8 * 8;
+  return (n + 15) / 16 * 16;
+}
+
+struct Workspace {
+  size_t status;                 // int status word
+  size_t b_fc, b_qkv, b_o, b_gu, b_down, b_lm;   // bf16 [2*NPmax][Kpad]
+  int kp_fc, kp_qkv, kp_o, kp_gu, kp_down, kp_lm;
+  size_t h, h2;                  // fp32 [max_rows][d]
+  size_t qrow;                   // bf16 [max_rows][Hq*dh]
+  size_t ss_fc, ss_o;            // fp32 [max_rows][tiles of d]
+  size_t gemm_part;              // fp32 [(max_mtiles + grid) * max_rows * 128]
+  size_t gemm_cnt;               // int [6][max_mtiles]
+  size_t attn_part;              // fp32 partial (m, l, acc[dh]) records
+  size_t attn_cnt;               // int [2][max_batch * Hkv]
+  size_t accept_scratch;         // u64 [max_batch][V] current acceptance weights
+  size_t total;
+  int max_mtiles;
+  int npmax;
+};
+
+struct TraceState {
+  int kernel_id = -2;            // -2: disabled
+  int capacity = 0;
+  std::vector<cudaEvent_t> events;   // pairs
+  int n = 0;
+};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+}  // namespace eagle
+
+struct eagle_ctx {
+  eagle_dims dims;
+  eagle_limits lim;
+  int device = 0;
+  int sm_count = 0;
+  eagle::Workspace ws;
+  eagle::TraceState trace;
+  long long launches = 0;
+  eagle::EncodeTiledFn encode = nullptr;
+};
+
+namespace eagle {
+
+// Launch bookkeeping: optional CUDA-event trace around kernels of one class.
+void trace_before(eagle_ctx* ctx, int kernel_id, cudaStream_t s);
+void trace_after(eagle_ctx* ctx, int kernel_id, cudaStream_t s);
+
+template <typename T>
+inline T* ws_ptr(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+struct DraftLaunch {
+  const eagle_plan* plan;
+  int layer, batch, e0, rpr, n, NP, k;
+  const eagle_draft_weights* w;
+  const eagle_requests* req;
+  const eagle_kv* draft_kv;
+  const eagle_pool* pool;
+  const eagle_draft_out* out;
+  const eagle_children* children;
+  const eagle_sampling* s;
+  void* ws;
+};
+
+cudaError_t launch_prep_fc(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st);
+cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStream_t st);
+cudaError_t launch_draft_attn(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st);
+cudaError_t launch_select(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st);
+
+cudaError_t launch_tree(eagle_ctx* ctx, const eagle_plan* plan, int phase, int layer, int batch,
+                        const eagle_requests* req, const eagle_children* ch, const eagle_pool* pool,
+                        const eagle_tree* tree, int* status, cudaStream_t st);
+
+cudaError_t launch_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, const uint16_t* kt,
+                               const uint16_t* vt, const eagle_kv* prefix, const eagle_tree* tree,
+                               float scale, uint16_t* out, void* ws, cudaStream_t st);
+
+cudaError_t launch_target_softmax(eagle_ctx* ctx, int batch, const eagle_tree* tree, const float* logits,
+                                  const float* temperature, float* probs, int32_t* argmax, void* ws,
+                                  cudaStream_t st);
+cudaError_t launch_accept_walk(eagle_ctx* ctx, const eagle_plan* plan, int batch, const eagle_tree* tree,
+                               const eagle_children* ch, const float* probs, const int32_t* argmax,
+                               const float* q_probs, const eagle_sampling* s, const eagle_accept_out* out,
+                               void* ws, cudaStream_t st);
+
+struct CommitLaunch {
+  int batch, n_layers, kv_cap;
+  const eagle_accept_out* acc;
+  const eagle_tree* tree;
+  const float* f_true;
+  const uint16_t* const* kt;
+  const uint16_t* const* vt;
+  uint16_t* const* kc;
+  uint16_t* const* vc;
+  const int32_t* kv_len;
+  const eagle_draft_out* draft;
+  const eagle_kv* draft_kv;
+  const eagle_commit_out* out;
+};
+cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st);
+
+// Prefix splits of the split-KV attention for `pairs` (request, kv head)
+// pairs over a cache of `cap` rows.
+int attn_splits(const eagle_ctx* ctx, int pairs, int cap);
+
+}  // namespace eagle

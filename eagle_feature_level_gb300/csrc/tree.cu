@@ -1,0 +1,304 @@
+// Tree construction on the device, one CTA per request ([A] §10.3; [C]
+// "EAGLE-2：固定树变成上下文感知动态树").
+//  ROOT     : slot 0 = t_next with value 1; every other expanded slot inactive.
+//  FRONTIER : EAGLE-2 -- candidates are the k drawn children of the previous
+//             layer's expanded nodes, value = value(parent) * q (fp64); keep
+//             the top_k by (value desc, parent slot asc, draw rank asc) as the
+//             new layer.  Static -- the template's nodes of this depth that
+//             have children.
+//  FINAL    : EAGLE-2 -- keep the top_m drawn nodes of the whole pool by
+//             (value desc, depth asc, parent slot asc, rank asc); value never
+//             grows along a path and ties go to the shallower node, so the
+//             kept set is a connected tree.  Static -- every template node.
+//             Then flatten: slots 1..m by (depth asc, selection rank asc),
+//             parent slots, positions, ancestor bitmasks.
+// Ranks come from counting (each thread compares its key with every other
+// valid key), which is exact and independent of thread order.
+#include "internal.h"
+#include "common.cuh"
+
+namespace eagle {
+namespace {
+
+constexpr int TREE_THREADS = 1024;
+constexpr int MAX_POOL = EAGLE_MAX_NODES * EAGLE_MAX_CHILDREN;
+
+struct TreeParams {
+  eagle_plan plan;
+  int phase, layer;
+  int E, K, S;
+  const int32_t* t_next;
+  const int32_t* pos0;
+  const int32_t* ctok;
+  const float* cprob;
+  int32_t* p_token;
+  int32_t* p_parent;
+  int32_t* p_rank;
+  int32_t* p_depth;
+  double* p_value;
+  uint64_t* p_anc;
+  int32_t* p_child_exp;
+  int32_t* t_token;
+  int32_t* t_parent;
+  int32_t* t_depth;
+  int32_t* t_pos;
+  int32_t* t_exp;
+  uint64_t* t_anc;
+  int32_t* t_child_slot;
+  int32_t* t_size;
+  int* status;
+};
+
+// key order: true if entry a ranks before entry b
+__device__ __forceinline__ bool before(double va, int da, int ca, double vb, int db, int cb) {
+  if (va != vb) return va > vb;
+  if (da != db) return da < db;
+  return ca < cb;
+}
+
+__global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) {
+  __shared__ double s_val[MAX_POOL];
+  __shared__ int s_dep[MAX_POOL];
+  __shared__ int s_rank[MAX_POOL];
+  __shared__ int s_slot[MAX_POOL];
+  __shared__ int s_parent_slot[EAGLE_MAX_NODES];
+  __shared__ int s_count;
+
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int E = p.E, K = p.K, S = p.S;
+  const eagle_plan& pl = p.plan;
+  const size_t pb = static_cast<size_t>(b) * E;
+
+  if (p.phase == EAGLE_PHASE_ROOT) {
+    for (int i = tid; i < E * K; i += TREE_THREADS) p.p_child_exp[pb * K + i] = -1;
+    for (int e = tid; e < E; e += TREE_THREADS) {
+      const bool root = e == 0;
+      p.p_token[pb + e] = root ? p.t_next[b] : -1;
+      p.p_parent[pb + e] = -1;
+      p.p_rank[pb + e] = 0;
+      p.p_depth[pb + e] = 0;
+      p.p_value[pb + e] = root ? 1.0 : -1.0;
+      p.p_anc[pb + e] = root ? 1ull : 0ull;
+    }
+    return;
+  }
+
+  if (p.phase == EAGLE_PHASE_FRONTIER) {
+    const int l = p.layer;
+    if (pl.kind == 1) {
+      for (int i = tid; i < pl.n_nodes; i += TREE_THREADS) {
+        if (pl.node_depth[i] != l || pl.node_exp[i] < 0) continue;
+        const int par_e = pl.node_parent[i] < 0 ? 0 : pl.node_exp[pl.node_parent[i]];
+        const int r = pl.node_rank[i];
+        const int e_new = pl.node_exp[i];
+        const int tok = p.ctok[(pb + par_e) * K + r];
+        const bool ok = p.p_token[pb + par_e] >= 0 && tok >= 0;
+        p.p_token[pb + e_new] = ok ? tok : -1;
+        p.p_parent[pb + e_new] = par_e;
+        p.p_rank[pb + e_new] = r;
+        p.p_depth[pb + e_new] = l;
+        p.p_value[pb + e_new] =
+            ok ? p.p_value[pb + par_e] * static_cast<double>(p.cprob[(pb + par_e) * K + r]) : -1.0;
+        p.p_anc[pb + e_new] = ok ? (p.p_anc[pb + par_e] | (1ull << e_new)) : 0ull;
+        if (ok) p.p_child_exp[(pb + par_e) * K + r] = e_new;
+      }
+      return;
+    }
+    const int e_prev = pl.layer_e0[l - 1], n_prev = pl.layer_rows[l - 1];
+    const int e_new0 = pl.layer_e0[l], n_new = pl.layer_rows[l];
+    const int k = pl.top_k;
+    const int n_c = n_prev * k;
+    if (tid == 0) s_count = 0;
+    __syncthreads();
+    for (int c = tid; c < n_c; c += TREE_THREADS) {
+      const int e = e_prev + c / k, r = c % k;
+      const int tok = p.ctok[(pb + e) * K + r];
+      const bool valid = p.p_token[pb + e] >= 0 && tok >= 0;
+      s_val[c] = valid ? p.p_value[pb + e] * static_cast<double>(p.cprob[(pb + e) * K + r]) : -1.0;
+      s_dep[c] = valid ? 1 : 0;
+      if (valid) atomicAdd(&s_count, 1);
+    }
+    __syncthreads();
+    for (int c = tid; c < n_c; c += TREE_THREADS) {
+      if (!s_dep[c]) continue;
+      int rank = 0;
+      for (int o = 0; o < n_c; ++o)
+        if (s_dep[o] && before(s_val[o], 0, o, s_val[c], 0, c)) ++rank;
+      if (rank >= n_new) continue;
+      const int e = e_prev + c / k, r = c % k;
+      const int e_new = e_new0 + rank;
+      p.p_token[pb + e_new] = p.ctok[(pb + e) * K + r];
+      p.p_parent[pb + e_new] = e;
+      p.p_rank[pb + e_new] = r;
+      p.p_depth[pb + e_new] = p.p_depth[pb + e] + 1;
+      p.p_value[pb + e_new] = s_val[c];
+      p.p_anc[pb + e_new] = p.p_anc[pb + e] | (1ull << e_new);
+      p.p_child_exp[(pb + e) * K + r] = e_new;
+    }
+    for (int i = tid; i < n_new; i += TREE_THREADS) {
+      if (i < s_count) continue;
+      const int e_new = e_new0 + i;
+      p.p_token[pb + e_new] = -1;
+      p.p_parent[pb + e_new] = -1;
+      p.p_rank[pb + e_new] = 0;
+      p.p_depth[pb + e_new] = l;
+      p.p_value[pb + e_new] = -1.0;
+      p.p_anc[pb + e_new] = 0ull;
+    }
+    return;
+  }
+
+  // ---------------- FINAL ----------------
+  const size_t tb = static_cast<size_t>(b) * S;
+  for (int i = tid; i < E * K; i += TREE_THREADS) p.t_child_slot[pb * K + i] = -1;
+  int n_sel = 0;
+  if (pl.kind == 1) {
+    n_sel = pl.n_nodes;
+    __syncthreads();
+    for (int i = tid; i < pl.n_nodes; i += TREE_THREADS) {
+      const int par_e = pl.node_parent[i] < 0 ? 0 : pl.node_exp[pl.node_parent[i]];
+      const int r = pl.node_rank[i];
+      const int s = i + 1;
+      const int tok = p.ctok[(pb + par_e) * K + r];
+      const bool ok = p.p_token[pb + par_e] >= 0 && tok >= 0;
+      p.t_token[tb + s] = ok ? tok : -1;
+      const int ps = pl.node_parent[i] < 0 ? 0 : pl.node_parent[i] + 1;
+      p.t_parent[tb + s] = ps;
+      s_parent_slot[s] = ps;
+      p.t_depth[tb + s] = pl.node_depth[i];
+      p.t_pos[tb + s] = p.pos0[b] + pl.node_depth[i];
+      p.t_exp[tb + s] = pl.node_exp[i];
+      p.t_child_slot[(pb + par_e) * K + r] = s;
+    }
+  } else {
+    const int k = pl.top_k, m = pl.top_m;
+    const int n_c = pl.n_expanded * k;
+    if (tid == 0) s_count = 0;
+    __syncthreads();
+    for (int c = tid; c < n_c; c += TREE_THREADS) {
+      const int e = c / k, r = c % k;
+      const int tok = p.ctok[(pb + e) * K + r];
+      const bool valid = p.p_token[pb + e] >= 0 && tok >= 0;
+      s_val[c] = valid ? p.p_value[pb + e] * static_cast<double>(p.cprob[(pb + e) * K + r]) : -1.0;
+      s_dep[c] = valid ? p.p_depth[pb + e] + 1 : -1;
+      s_slot[c] = -1;
+      if (valid) atomicAdd(&s_count, 1);
+    }
+    __syncthreads();
+    for (int c = tid; c < n_c; c += TREE_THREADS) {
+      int rank = INT32_MAX;
+      if (s_dep[c] >= 0) {
+        rank = 0;
+        for (int o = 0; o < n_c; ++o)
+          if (s_dep[o] >= 0 && before(s_val[o], s_dep[o], o, s_val[c], s_dep[c], c)) ++rank;
+      }
+      s_rank[c] = rank;
+    }
+    __syncthreads();
+    n_sel = min(m, s_count);
+    for (int c = tid; c < n_c; c += TREE_THREADS) {
+      const int rk = s_rank[c];
+      if (rk >= n_sel) continue;
+      int pos = 0;
+      for (int o = 0; o < n_c; ++o) {
+        const int ro = s_rank[o];
+        if (ro < n_sel && (s_dep[o] < s_dep[c] || (s_dep[o] == s_dep[c] && ro < rk))) ++pos;
+      }
+      s_slot[c] = 1 + pos;
+    }
+    __syncthreads();
+    for (int c = tid; c < n_c; c += TREE_THREADS) {
+      const int s = s_slot[c];
+      if (s < 0) continue;
+      const int e = c / k, r = c % k;
+      int ps = 0;
+      if (e != 0) {
+        const int pc = p.p_parent[pb + e] * k + p.p_rank[pb + e];
+        ps = (pc >= 0 && pc < n_c) ? s_slot[pc] : -1;
+        if (ps < 0) {
+          set_status(p.status, EAGLE_ERR_INVALID_TREE);
+          ps = 0;
+        }
+      }
+      p.t_token[tb + s] = p.ctok[(pb + e) * K + r];
+      p.t_parent[tb + s] = ps;
+      s_parent_slot[s] = ps;
+      p.t_depth[tb + s] = s_dep[c];
+      p.t_pos[tb + s] = p.pos0[b] + s_dep[c];
+      p.t_exp[tb + s] = p.p_child_exp[(pb + e) * K + r];
+      p.t_child_slot[(pb + e) * K + r] = s;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int size = 1 + n_sel;
+    p.t_size[b] = size;
+    p.t_token[tb] = p.p_token[pb];
+    p.t_parent[tb] = -1;
+    p.t_depth[tb] = 0;
+    p.t_pos[tb] = p.pos0[b];
+    p.t_exp[tb] = 0;
+    uint64_t anc[EAGLE_MAX_NODES];
+    anc[0] = 1ull;
+    p.t_anc[tb] = 1ull;
+    for (int s = 1; s < size; ++s) {
+      const int ps = s_parent_slot[s];
+      const bool ok = ps >= 0 && ps < s;
+      anc[s] = (ok ? anc[ps] : 0ull) | (1ull << s);
+      if (!ok) set_status(p.status, EAGLE_ERR_INVALID_TREE);
+      p.t_anc[tb + s] = anc[s];
+    }
+    for (int s = size; s < S; ++s) {
+      p.t_token[tb + s] = -1;
+      p.t_parent[tb + s] = -1;
+      p.t_depth[tb + s] = 0;
+      p.t_pos[tb + s] = 0;
+      p.t_exp[tb + s] = -1;
+      p.t_anc[tb + s] = 0ull;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tree(eagle_ctx* ctx, const eagle_plan* plan, int phase, int layer, int batch,
+                        const eagle_requests* req, const eagle_children* ch, const eagle_pool* pool,
+                        const eagle_tree* tree, int* status, cudaStream_t st) {
+  TreeParams p{};
+  p.plan = *plan;
+  p.phase = phase;
+  p.layer = layer;
+  p.E = ctx->lim.max_expanded;
+  p.K = ctx->lim.max_children;
+  p.t_next = req ? req->t_next : nullptr;
+  p.pos0 = req ? req->pos0 : nullptr;
+  p.ctok = ch ? ch->token : nullptr;
+  p.cprob = ch ? ch->prob : nullptr;
+  p.p_token = pool->token;
+  p.p_parent = pool->parent;
+  p.p_rank = pool->rank;
+  p.p_depth = pool->depth;
+  p.p_value = pool->value;
+  p.p_anc = pool->anc;
+  p.p_child_exp = pool->child_exp;
+  if (tree) {
+    p.S = tree->stride;
+    p.t_token = tree->token;
+    p.t_parent = tree->parent;
+    p.t_depth = tree->depth;
+    p.t_pos = tree->pos;
+    p.t_exp = tree->exp;
+    p.t_anc = tree->anc;
+    p.t_child_slot = tree->child_slot;
+    p.t_size = tree->size;
+  }
+  p.status = status;
+  trace_before(ctx, EAGLE_K_TREE, st);
+  tree_kernel<<<batch, TREE_THREADS, 0, st>>>(p);
+  ctx->launches++;
+  trace_after(ctx, EAGLE_K_TREE, st);
+  return cudaGetLastError();
+}
+
+}  // namespace eagle
