@@ -93,7 +93,7 @@ void layout(eagle_ctx* c) {
   W.b_lm = take(np2 * W.kp_lm * 2);
   W.h = take(static_cast<size_t>(L.max_rows) * D.d * 4);
   W.h2 = take(static_cast<size_t>(L.max_rows) * D.d * 4);
-  W.qrow = take(static_cast<size_t>(L.max_rows) * D.n_q_heads * D.head_dim * 2);
+  W.qrow = take(static_cast<size_t>(L.max_rows) * D.n_q_heads * D.head_dim * 4);
   const int tiles_d = ceil_div(D.d, 128);
   W.ss_fc = take(static_cast<size_t>(L.max_rows) * tiles_d * 4);
   W.ss_o = take(static_cast<size_t>(L.max_rows) * tiles_d * 4);
@@ -427,7 +427,7 @@ eagle_status eagle_tree_expand_rerank(eagle_ctx* ctx, const eagle_plan* plan, in
 
 eagle_status eagle_tree_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, const uint16_t* k_tree,
                                     const uint16_t* v_tree, const eagle_kv* prefix, const eagle_tree* tree,
-                                    float scale, uint16_t* out, void* workspace, cudaStream_t stream) {
+                                    float scale, float* out, void* workspace, cudaStream_t stream) {
   EAGLE_REQUIRE(ctx, EAGLE_ERR_INVALID_ARG);
   EAGLE_REQUIRE(batch >= 1 && batch <= ctx->lim.max_batch, EAGLE_ERR_CAPACITY);
   EAGLE_PTR(q); EAGLE_PTR(k_tree); EAGLE_PTR(v_tree); EAGLE_PTR(out);

@@ -25,20 +25,23 @@ struct AttnParams {
   int B, Hq, Hkv, dh, G;
   int n_splits, chunk;            // prefix splits and rows per split
   int rows_cap;                   // query nodes per request (draft: rows per request; verify: tree stride)
-  const uint16_t* q;              // draft: [n][Hq*dh]; verify: [B][S][Hq][dh]
-  const uint16_t* kp;             // prefix KV [B][cap][Hkv][dh]
+  const float* q_f32;             // draft: [n][Hq*dh] fp32
+  const uint16_t* q_bf16;         // verify: [B][S][Hq][dh] bf16
+  const uint16_t* kp;             // prefix KV [B][cap][Hkv][dh] bf16
   const uint16_t* vp;
   int kv_cap;
   const int32_t* kv_len;
-  const uint16_t* kt;             // draft: [B][E][Hkv][dh] ; verify: [B][S][Hkv][dh]
-  const uint16_t* vt;
+  const float* kt_f32;            // draft: tree K/V [B][E][Hkv][dh] fp32
+  const float* vt_f32;
+  const uint16_t* kt_bf16;        // verify: tree K/V [B][S][Hkv][dh] bf16
+  const uint16_t* vt_bf16;
   int tree_cap;                   // E or S
   const uint64_t* anc;            // draft: pool.anc [B][E]; verify: tree.anc [B][S]
   const int32_t* tree_size;       // verify: [B]
   int e0;                         // draft: first expanded slot of this layer
   float scale;
-  uint16_t* out_bf16;             // verify: [B][S][Hq][dh]
-  uint16_t* b_o;                  // draft: next GEMM operand (hi/lo), [2NP][kp]
+  float* out_f32;                 // verify: [B][S][Hq][dh]
+  uint16_t* b_o;                  // draft: next GEMM operand (hi/lo), [2NP][bo_ld]
   int NP, bo_ld;
   float* part;
   int* counters;
@@ -48,8 +51,18 @@ __device__ __forceinline__ int n_nodes(const AttnParams& p, int b) {
   return p.mode == 0 ? p.rows_cap : min(p.tree_size[b], p.rows_cap);
 }
 
-__device__ __forceinline__ const uint16_t* q_ptr(const AttnParams& p, int b, int node, int hq) {
-  return p.q + ((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * p.dh;
+__device__ __forceinline__ size_t q_index(const AttnParams& p, int b, int node, int hq) {
+  return ((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * p.dh;
+}
+
+// element d of tree key/value row j (kv head h) of request b
+__device__ __forceinline__ float tree_k(const AttnParams& p, int b, int j, int h, int d) {
+  const size_t i = ((static_cast<size_t>(b) * p.tree_cap + j) * p.Hkv + h) * p.dh + d;
+  return p.mode == 0 ? p.kt_f32[i] : bf16_to_f32(p.kt_bf16[i]);
+}
+__device__ __forceinline__ float tree_v(const AttnParams& p, int b, int j, int h, int d) {
+  const size_t i = ((static_cast<size_t>(b) * p.tree_cap + j) * p.Hkv + h) * p.dh + d;
+  return p.mode == 0 ? p.vt_f32[i] : bf16_to_f32(p.vt_bf16[i]);
 }
 
 __device__ __forceinline__ uint64_t row_mask(const AttnParams& p, int b, int node) {
@@ -94,15 +107,14 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
     for (int t0 = lo; t0 < hi; t0 += TILE) {
       const int nt = min(TILE, hi - t0);
       __syncthreads();
-      const int pieces = dh / 8;
-      const uint16_t* ks = is_tree ? p.kt : p.kp;
-      const uint16_t* vs = is_tree ? p.vt : p.vp;
-      const int cap = is_tree ? p.tree_cap : p.kv_cap;
-      for (int idx = threadIdx.x; idx < nt * pieces; idx += THREADS) {
-        const int r = idx / pieces, c = idx % pieces;
-        const size_t g = ((static_cast<size_t>(b) * cap + t0 + r) * p.Hkv + h) * dh + c * 8;
-        *reinterpret_cast<uint4*>(&sk[r][c * 8]) = __ldg(reinterpret_cast<const uint4*>(ks + g));
-        *reinterpret_cast<uint4*>(&sv[r][c * 8]) = __ldg(reinterpret_cast<const uint4*>(vs + g));
+      if (!is_tree) {   // stage the prefix K/V tile; the (small) tree part is read from global
+        const int pieces = dh / 8;
+        for (int idx = threadIdx.x; idx < nt * pieces; idx += THREADS) {
+          const int r = idx / pieces, c = idx % pieces;
+          const size_t g = ((static_cast<size_t>(b) * p.kv_cap + t0 + r) * p.Hkv + h) * dh + c * 8;
+          *reinterpret_cast<uint4*>(&sk[r][c * 8]) = __ldg(reinterpret_cast<const uint4*>(p.kp + g));
+          *reinterpret_cast<uint4*>(&sv[r][c * 8]) = __ldg(reinterpret_cast<const uint4*>(p.vp + g));
+        }
       }
       __syncthreads();
 #pragma unroll
@@ -110,8 +122,9 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
         const int r = r0 + warp + 8 * i;
         if (r >= R) break;
         const int node = r / p.G, hq = h * p.G + r % p.G;
-        const uint16_t* qg = q_ptr(p, b, node, hq);
-        for (int d = lane; d < dh; d += 32) sq[warp][d] = bf16_to_f32(qg[d]);
+        const size_t qo = q_index(p, b, node, hq);
+        for (int d = lane; d < dh; d += 32)
+          sq[warp][d] = p.mode == 0 ? p.q_f32[qo + d] : bf16_to_f32(p.q_bf16[qo + d]);
         __syncwarp();
         const uint64_t mask = is_tree ? row_mask(p, b, node) : ~0ull;
         float sc[2];
@@ -120,7 +133,11 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
           const int j = lane + 32 * half;
           float s = -INFINITY;
           const bool vis = j < nt && (!is_tree || ((mask >> (t0 + j)) & 1ull));
-          if (vis) {
+          if (vis && is_tree) {
+            float dot = 0.f;
+            for (int d = 0; d < dh; ++d) dot = fmaf(sq[warp][d], tree_k(p, b, t0 + j, h, d), dot);
+            s = dot * p.scale;
+          } else if (vis) {
             float dot = 0.f;
             for (int d0 = 0; d0 < dh; d0 += 8) {
               const uint4 kv = *reinterpret_cast<const uint4*>(&sk[j][d0]);
@@ -152,7 +169,8 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int d = lane + 32 * c;
-            if (d < dh) acc[i][c] = fmaf(pj, bf16_to_f32(sv[j][d]), acc[i][c]);
+            if (d < dh)
+              acc[i][c] = fmaf(pj, is_tree ? tree_v(p, b, t0 + j, h, d) : bf16_to_f32(sv[j][d]), acc[i][c]);
           }
         }
       }
@@ -212,7 +230,7 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
       if (d >= dh) continue;
       const float v = o[c] * inv;
       if (p.mode == 1) {
-        p.out_bf16[((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * dh + d] = f32_to_bf16(v);
+        p.out_f32[((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * dh + d] = v;
       } else {
         const int j = b * p.rows_cap + node;
         const int col = hq * dh + d;
@@ -258,13 +276,13 @@ cudaError_t launch_draft_attn(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t
   p.dh = D.head_dim;
   p.G = D.n_q_heads / D.n_kv_heads;
   p.rows_cap = L.rpr;
-  p.q = ws_ptr<uint16_t>(L.ws, W.qrow);
+  p.q_f32 = ws_ptr<float>(L.ws, W.qrow);
   p.kp = L.draft_kv->k;
   p.vp = L.draft_kv->v;
   p.kv_cap = L.draft_kv->cap;
   p.kv_len = L.draft_kv->len;
-  p.kt = L.out->k_tree;
-  p.vt = L.out->v_tree;
+  p.kt_f32 = L.out->k_tree;
+  p.vt_f32 = L.out->v_tree;
   p.tree_cap = ctx->lim.max_expanded;
   p.anc = L.pool->anc;
   p.e0 = L.e0;
@@ -279,7 +297,7 @@ cudaError_t launch_draft_attn(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t
 
 cudaError_t launch_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, const uint16_t* kt,
                                const uint16_t* vt, const eagle_kv* prefix, const eagle_tree* tree,
-                               float scale, uint16_t* out, void* ws, cudaStream_t st) {
+                               float scale, float* out, void* ws, cudaStream_t st) {
   const eagle_dims& D = ctx->dims;
   const Workspace& W = ctx->ws;
   AttnParams p{};
@@ -290,18 +308,18 @@ cudaError_t launch_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, con
   p.dh = D.head_dim;
   p.G = D.n_q_heads / D.n_kv_heads;
   p.rows_cap = tree->stride;
-  p.q = q;
+  p.q_bf16 = q;
   p.kp = prefix->k;
   p.vp = prefix->v;
   p.kv_cap = prefix->cap;
   p.kv_len = prefix->len;
-  p.kt = kt;
-  p.vt = vt;
+  p.kt_bf16 = kt;
+  p.vt_bf16 = vt;
   p.tree_cap = tree->stride;
   p.anc = tree->anc;
   p.tree_size = tree->size;
   p.scale = scale;
-  p.out_bf16 = out;
+  p.out_f32 = out;
   p.part = ws_ptr<float>(ws, W.attn_part);
   p.counters = ws_ptr<int>(ws, W.attn_cnt) + ctx->lim.max_batch * D.n_kv_heads;
   return run_attn(ctx, p, EAGLE_K_VERIFY_ATTN, st);

@@ -23,8 +23,8 @@ struct CommitParams {
   const int32_t* t_token;
   const float* f_true;
   const int32_t* kv_len;
-  const uint16_t* dk_tree;
-  const uint16_t* dv_tree;
+  const float* dk_tree;
+  const float* dv_tree;
   uint16_t* dk;
   uint16_t* dv;
   const int32_t* draft_len;
@@ -75,8 +75,10 @@ __global__ void commit_kernel(const CommitParams p) {
       const int Ld = p.draft_len[b];
       const size_t src = (static_cast<size_t>(b) * p.E + 0) * p.row_elems;
       const size_t dst = (static_cast<size_t>(b) * p.draft_cap + Ld) * p.row_elems;
-      copy_row(p.dk + dst, p.dk_tree + src, p.row_elems);
-      copy_row(p.dv + dst, p.dv_tree + src, p.row_elems);
+      for (int c = threadIdx.x; c < p.row_elems; c += blockDim.x) {
+        p.dk[dst + c] = f32_to_bf16(p.dk_tree[src + c]);
+        p.dv[dst + c] = f32_to_bf16(p.dv_tree[src + c]);
+      }
       if (threadIdx.x == 0) p.draft_len_out[b] = Ld + 1;
     }
   }

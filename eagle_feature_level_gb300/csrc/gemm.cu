@@ -58,9 +58,9 @@ struct GemmParams {
   float* out_f32;
   uint16_t* bnext;
   int kp_next;
-  uint16_t* qrow;
-  uint16_t* k_tree;
-  uint16_t* v_tree;
+  float* qrow;
+  float* k_tree;
+  float* v_tree;
   const int32_t* pos0;
   const int32_t* depth;
   float* part;
@@ -240,10 +240,10 @@ __device__ void finalize_tile(const GemmParams& p, const Smem& s, int t, int c_f
             v = i < half ? v * cs - other * sn : v * cs + other * sn;
           }
           if (gi < qd) {
-            p.qrow[static_cast<size_t>(j) * qd + gi] = f32_to_bf16(v);
+            p.qrow[static_cast<size_t>(j) * qd + gi] = v;
           } else {
-            uint16_t* dst = is_v ? p.v_tree : p.k_tree;
-            dst[((static_cast<size_t>(b) * p.E + e) * p.Hkv + head) * p.dh + i] = f32_to_bf16(v);
+            float* dst = is_v ? p.v_tree : p.k_tree;
+            dst[((static_cast<size_t>(b) * p.E + e) * p.Hkv + head) * p.dh + i] = v;
           }
         }
       }
@@ -548,7 +548,7 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
       mats[2] = w->wv; rows[2] = kd; lds[2] = w->ld_v;
       K = D.d; b_in = W.b_qkv; kp_in = W.kp_qkv; n_out = qd + 2 * kd;
       p.ss_in = ws_ptr<float>(L.ws, W.ss_fc); p.ss_in_tiles = tiles_d;
-      p.qrow = ws_ptr<uint16_t>(L.ws, W.qrow);
+      p.qrow = ws_ptr<float>(L.ws, W.qrow);
       p.k_tree = L.out->k_tree; p.v_tree = L.out->v_tree;
       p.pos0 = L.req->pos0; p.depth = L.pool->depth;
       break;

@@ -33,7 +33,7 @@ struct Workspace {
   size_t b_fc, b_qkv, b_o, b_gu, b_down, b_lm;   // bf16 [2*NPmax][Kpad]
   int kp_fc, kp_qkv, kp_o, kp_gu, kp_down, kp_lm;
   size_t h, h2;                  // fp32 [max_rows][d]
-  size_t qrow;                   // bf16 [max_rows][Hq*dh]
+  size_t qrow;                   // fp32 [max_rows][Hq*dh]
   size_t ss_fc, ss_o;            // fp32 [max_rows][tiles of d]
   size_t gemm_part;              // fp32 [(max_mtiles + grid) * max_rows * 128]
   size_t gemm_cnt;               // int [6][max_mtiles]
@@ -104,7 +104,7 @@ cudaError_t launch_tree(eagle_ctx* ctx, const eagle_plan* plan, int phase, int l
 
 cudaError_t launch_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, const uint16_t* kt,
                                const uint16_t* vt, const eagle_kv* prefix, const eagle_tree* tree,
-                               float scale, uint16_t* out, void* ws, cudaStream_t st);
+                               float scale, float* out, void* ws, cudaStream_t st);
 
 cudaError_t launch_target_softmax(eagle_ctx* ctx, int batch, const eagle_tree* tree, const float* logits,
                                   const float* temperature, float* probs, int32_t* argmax, void* ws,

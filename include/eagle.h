@@ -189,8 +189,8 @@ typedef struct {
   float* f_hat;         /* [B][E][d]  predicted feature f^ ([A] §4.1) */
   float* logits;        /* [B][E][V]  z = LM_Head(f^) */
   float* probs;         /* [B][E][V]  q = softmax(z / T) (T = 1 for greedy requests) */
-  uint16_t* k_tree;     /* [B][E][Hkv][dh] the draft layer's K of each expanded row (post-RoPE) */
-  uint16_t* v_tree;     /* [B][E][Hkv][dh] */
+  float* k_tree;        /* [B][E][Hkv][dh] fp32: the draft layer's K of each expanded row (post-RoPE) */
+  float* v_tree;        /* [B][E][Hkv][dh] fp32 */
 } eagle_draft_out;
 
 /* Flattened verification tree, [B][S] arrays with S = tree stride. */
@@ -298,12 +298,12 @@ eagle_status eagle_tree_expand_rerank(eagle_ctx* ctx, const eagle_plan* plan, in
  *   out[b][s][h] = softmax(scale * q[b][s][h] . K^T) V over prefix rows
  *   0..prefix.len[b]-1 and tree slots j < tree.size[b] with bit j of
  *   tree.anc[b][s]; kv head = h / (Hq / Hkv).
- * q: [B][S][Hq][dh] bf16; k_tree, v_tree: [B][S][Hkv][dh] bf16; out: [B][S][Hq][dh] bf16,
+ * q: [B][S][Hq][dh] bf16; k_tree, v_tree: [B][S][Hkv][dh] bf16; out: [B][S][Hq][dh] fp32,
  * S = tree.stride.  Slots s >= tree.size[b] are not written. */
 eagle_status eagle_tree_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q,
                                     const uint16_t* k_tree, const uint16_t* v_tree,
                                     const eagle_kv* prefix, const eagle_tree* tree, float scale,
-                                    uint16_t* out, void* workspace, cudaStream_t stream);
+                                    float* out, void* workspace, cudaStream_t stream);
 
 /* eagle_accept -- acceptance on the verified tree ([A] §6.2; [B] "Greedy 验证",
  * "随机采样验证"; [C] "为什么普通草稿模型不够理想").
@@ -350,8 +350,9 @@ typedef struct {
  * closing remark and §12 item 3): for every layer l < n_layers, copy the
  * tree K/V rows of path slots 0..a of request b to target cache rows
  * L_b..L_b+a (L_b = target_kv_len[b]); gather the true features f_true[b][path];
- * append the root's draft K/V (its row used the verified f_last) to the draft
- * cache at row draft_kv.len[b]; rejected branches are simply not copied.
+ * append the root's draft K/V (its row used the verified f_last; rounded to the
+ * cache's bf16) to the draft cache at row draft_kv.len[b]; rejected branches
+ * are simply not copied.
  * k_tree_layers / v_tree_layers / k_cache_layers / v_cache_layers are HOST
  * arrays of n_layers device pointers ([B][S][Hkv][dh] and [B][kv_cap][Hkv][dh]).
  * f_true: [B][S][d] fp32.  Output buffers must not alias inputs. */

@@ -1,0 +1,235 @@
+"""GPU-vs-oracle round harness used by the parity tests and smoke().
+
+run_gpu_round: seeded inputs -> one round through libeagle's C ABI on cuda:0.
+run_oracle_round: the same inputs (copied to the host) through the CPU oracle.
+compare_round: element-wise comparison.  Discrete results (children, tree,
+accept length, path, tokens) must be identical; a mismatch is tolerated only
+as a flagged near-tie, when the oracle's own margin for that decision is
+below the floating-point tolerance, and the request's later comparisons are
+then skipped.  Floating point: features, logits and attention outputs within
+max-abs 1e-4 (fp32 workload) or 2e-2 (bf16 workloads); probabilities within
+1e-3.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import eagle_synth as S
+from eagle_synth.standin import target_logits_from_draft
+from eagle_feature_level_gb300 import runtime as R
+
+TOL_PROB = 1e-3
+
+
+def feature_tol(w) -> float:
+    return 1e-4 if w.name.startswith("tiny") else 2e-2
+
+
+def limits_for(w):
+    tree_slots = 1 + w.top_m
+    E = S.max_expanded(w)
+    rows = w.batch * (1 if w.tree != "eagle2" else w.top_k)
+    if w.tree != "eagle2":
+        plan = R.plan_for(w.tree)
+        rows = w.batch * max(plan.layer_rows[l] for l in range(plan.n_layers))
+    return dict(max_batch=w.batch, max_rows=rows, max_expanded=E, max_children=w.top_k,
+                max_tree=tree_slots)
+
+
+def dims_of(w):
+    return dict(d=w.d, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, d_ff=w.d_ff,
+                vocab=w.vocab, rms_eps=w.rms_eps, rope_theta=w.rope_theta)
+
+
+def make_round(w, inp, device="cuda"):
+    lim = limits_for(w)
+    eng = R.Engine(dims_of(w), max_prefix=inp["kv_cap"], device=device, **lim)
+    plan = R.plan_for(w.tree, w.top_k, w.depth, w.top_m)
+    rd = R.Round(eng, plan, w.batch, inp["kv_cap"])
+    load_round(rd, w, inp)
+    return eng, rd
+
+
+def load_round(rd, w, inp):
+    dev = rd.eng.device
+    L = torch.tensor(inp["prefix_len"], dtype=torch.int32, device=dev)
+    rd.t_next.copy_(inp["t_next"])
+    rd.f_last.copy_(inp["f_last"])
+    rd.pos0.copy_(L)
+    rd.temps.copy_(torch.tensor(inp["temps"], dtype=torch.float32, device=dev))
+    rd.draft_k.copy_(inp["draft_k"])
+    rd.draft_v.copy_(inp["draft_v"])
+    rd.draft_len.copy_(torch.tensor(inp["draft_len"], dtype=torch.int32, device=dev))
+    rd.tgt_k[0].copy_(inp["tgt_k"])
+    rd.tgt_v[0].copy_(inp["tgt_v"])
+    rd.tgt_len.copy_(L)
+    rd.tree_q.copy_(inp["tree_q"])
+    rd.tree_k[0].copy_(inp["tree_k"])
+    rd.tree_v[0].copy_(inp["tree_v"])
+    rd.f_true.copy_(inp["f_true"])
+    rd.set_sampling(inp["philox_seed"], inp["round_id"])
+
+
+def standin(inp):
+    def fn(rd):
+        target_logits_from_draft(rd.logits, rd.t_exp, inp["tgt_noise"], inp["tgt_fresh"], rd.target_logits)
+    return fn
+
+
+GPU_FIELDS = ["p_token", "p_parent", "p_depth", "p_value", "c_token", "c_prob", "f_hat", "logits", "probs",
+              "dk_tree", "t_token", "t_parent", "t_depth", "t_pos", "t_exp", "t_anc", "t_size", "attn_out",
+              "target_logits", "target_probs", "target_argmax", "accept_len", "path", "final_token", "last_slot",
+              "f_commit", "tok_commit", "f_last_out", "t_next_out", "prefix_len_out", "draft_len_out",
+              "draft_k", "draft_v"]
+
+
+def run_gpu_round(w, seed, device="cuda", weights=None, inputs=None):
+    W = weights if weights is not None else S.draft_weights(w, seed, device=device)
+    inp = inputs if inputs is not None else S.round_inputs(w, seed, device=device)
+    eng, rd = make_round(w, inp, device)
+    rd.run(eng.weights(W), target_fn=standin(inp))
+    torch.cuda.synchronize()
+    status = eng.status()
+    out = {k: getattr(rd, k).detach().to("cpu") for k in GPU_FIELDS}
+    out["tgt_k_after"] = rd.tgt_k[0].detach().to("cpu")
+    out["status"] = status
+    out["launches"] = R.B.eagle_launch_count(eng.ctx)
+    out["inputs_cpu"] = {k: (v.detach().to("cpu") if torch.is_tensor(v) else v) for k, v in inp.items()}
+    out["weights_cpu"] = {k: v.detach().to("cpu") for k, v in W.items()}
+    eng.close()
+    return out
+
+
+def run_oracle_round(w, seed, inputs_cpu, weights_cpu, requests=None):
+    from oracle.layer import DraftWeights
+    from oracle.round import run_round
+    Wd = DraftWeights(weights_cpu, w)
+    return run_round(Wd, w, inputs_cpu, requests=requests)
+
+
+def _maxerr(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.max(np.abs(a - b))) if a.size else 0.0
+
+
+def _f64(t):
+    return t.to(torch.float64).numpy() if torch.is_tensor(t) else np.asarray(t, dtype=np.float64)
+
+
+def compare_round(w, gpu, ref, requests=None):
+    """Returns a report dict; report['ok'] is False on any non-near-tie mismatch."""
+    from oracle import philox
+    from oracle.sampling import quantize
+    tol = feature_tol(w)
+    reqs = list(range(w.batch)) if requests is None else list(requests)
+    rep = {"ok": True, "near_ties": [], "errors": [], "max_err": {}}
+
+    def err(name, val, lim):
+        rep["max_err"][name] = max(rep["max_err"].get(name, 0.0), val)
+        if not val <= lim:
+            rep["ok"] = False
+            rep["errors"].append(f"{name}: {val:.3g} > {lim:g}")
+
+    def fail(msg):
+        rep["ok"] = False
+        rep["errors"].append(msg)
+
+    if gpu["status"] != 0:
+        fail(f"device status {gpu['status']}")
+    inp = gpu["inputs_cpu"]
+    for i, b in enumerate(reqs):
+        r = ref[i]
+        st, tr = r["draft"], r["tree"]
+        ex = st.ex
+        temp = float(inp["temps"][b])
+        diverged = False
+        # draft head outputs, per expanded node in creation order
+        for e in range(len(ex.token)):
+            if int(gpu["p_token"][b, e]) != ex.token[e]:
+                fail(f"b{b} pool token e{e}: {int(gpu['p_token'][b, e])} vs {ex.token[e]}")
+                diverged = True
+                break
+            err("f_hat", _maxerr(gpu["f_hat"][b, e], st.f_hat[e]), tol)
+            err("logits", _maxerr(gpu["logits"][b, e], st.z[e]), tol)
+            err("probs", _maxerr(gpu["probs"][b, e], st.q[e]), TOL_PROB)
+            err("draft_k", _maxerr(gpu["dk_tree"][b, e], st.k_tree[e]), tol)
+            k = len(st.child_tok[e])
+            g_ch = [int(x) for x in gpu["c_token"][b, e, :k]]
+            if g_ch != list(st.child_tok[e]):
+                rank = next(j for j in range(k) if g_ch[j] != st.child_tok[e][j])
+                a_tok, g_tok = st.child_tok[e][rank], g_ch[rank]
+                if temp <= 0:
+                    margin = abs(st.z[e][a_tok] - st.z[e][g_tok]) if g_tok >= 0 else np.inf
+                    near = margin < 2 * tol
+                else:
+                    u = philox.uniform_u32(inp["philox_seed"], rank, e, philox.PURPOSE_DRAW, b, inp["round_id"])
+                    wq = quantize(st.q[e]).astype(np.float64)
+                    for t in st.child_tok[e][:rank]:
+                        wq[t] = 0.0
+                    cdf = np.cumsum(wq) / wq.sum()
+                    margin = float(np.min(np.abs(cdf - u / 2.0 ** 32)))
+                    near = margin < 1e-5
+                if near:
+                    rep["near_ties"].append(f"b{b} e{e} rank{rank} margin {margin:.2e}")
+                    diverged = True
+                    break
+                fail(f"b{b} children of e{e}: {g_ch} vs {list(st.child_tok[e])}")
+                diverged = True
+                break
+            err("child_prob", _maxerr(gpu["c_prob"][b, e, :k], st.child_q[e]), TOL_PROB)
+        if diverged:
+            continue
+        # tree
+        size = tr.size
+        if int(gpu["t_size"][b]) != size:
+            fail(f"b{b} tree size {int(gpu['t_size'][b])} vs {size}")
+            continue
+        for name, mine, want in (("token", gpu["t_token"], tr.token), ("parent", gpu["t_parent"], tr.parent),
+                                 ("depth", gpu["t_depth"], tr.depth), ("exp", gpu["t_exp"], tr.exp)):
+            got = [int(x) for x in mine[b, :size]]
+            if got != list(want):
+                fail(f"b{b} tree {name}: {got} vs {list(want)}")
+                diverged = True
+        anc = [int(x) & 0xFFFFFFFFFFFFFFFF for x in gpu["t_anc"][b, :size]]
+        if anc != list(tr.anc):
+            fail(f"b{b} tree anc differs")
+            diverged = True
+        pos = [int(x) for x in gpu["t_pos"][b, :size]]
+        if pos != [inp["prefix_len"][b] + dd for dd in tr.depth]:
+            fail(f"b{b} tree pos differs")
+        if diverged:
+            continue
+        # verification attention, target distribution
+        err("verify_out", _maxerr(gpu["attn_out"][b, :size], r["verify_out"]), tol)
+        err("target_logits", _maxerr(gpu["target_logits"][b, :size], r["target_logits"]), tol)
+        if temp > 0:
+            err("target_probs", _maxerr(gpu["target_probs"][b, :size], r["target_probs"]), TOL_PROB)
+        # acceptance
+        a = int(gpu["accept_len"][b])
+        path = [int(x) for x in gpu["path"][b, :a + 1]]
+        final = int(gpu["final_token"][b])
+        if (a, path, final) != (r["accept_len"], list(r["path"]), r["final"]):
+            fail(f"b{b} accept: gpu ({a}, {path}, {final}) vs oracle ({r['accept_len']}, {r['path']}, {r['final']})")
+            continue
+        # commit
+        cm = r["commit"]
+        toks = [int(x) for x in gpu["tok_commit"][b, :a + 2]]
+        if toks != cm["tok_commit"]:
+            fail(f"b{b} tok_commit {toks} vs {cm['tok_commit']}")
+        err("f_commit", _maxerr(gpu["f_commit"][b, :a + 1], cm["f_commit"]), 0.0)
+        err("f_last", _maxerr(gpu["f_last_out"][b], cm["f_last"]), 0.0)
+        if int(gpu["t_next_out"][b]) != cm["t_next"] or int(gpu["prefix_len_out"][b]) != cm["prefix_len"]:
+            fail(f"b{b} next-round state differs")
+        if int(gpu["draft_len_out"][b]) != cm["draft_len"]:
+            fail(f"b{b} draft_len differs")
+        L = inp["prefix_len"][b]
+        got_kv = _f64(gpu["tgt_k_after"][b, L:L + a + 1])
+        err("kv_commit", _maxerr(got_kv, cm["kv_rows_k"]), 0.0)
+        Ld = inp["draft_len"][b]
+        root_k = np.asarray(cm["draft_root_k"])
+        # the cache is bf16: the appended row carries one bf16 rounding (2^-9 relative)
+        err("draft_kv_append", _maxerr(_f64(gpu["draft_k"][b, Ld]), root_k),
+            tol + 2.0 ** -8 * float(np.max(np.abs(root_k))))
+    return rep

@@ -1,0 +1,59 @@
+"""GPU parity: whole rounds through the C ABI against the oracle, element by
+element, on small cases that span several tiles and ragged tails, and on the
+full-size workloads (sampled requests)."""
+import pytest
+import torch
+
+import eagle_synth as S
+from tests.gpu_harness import compare_round, run_gpu_round, run_oracle_round
+
+SMALL = {
+    "tiny_greedy_static8": S.WORKLOADS["tiny_fp32"],
+    "tiny_sampling_static8": S.variant("tiny_fp32", name="tiny_sampling_static8", temps=(1.0,)),
+    "tiny_greedy_chain4": S.variant("tiny_fp32", name="tiny_greedy_chain4", tree="chain4", top_k=1, depth=4,
+                                    top_m=4),
+    "tiny_sampling_chain4": S.variant("tiny_fp32", name="tiny_sampling_chain4", tree="chain4", top_k=1,
+                                      depth=4, top_m=4, temps=(1.0,)),
+    "small_eagle2_gqa_mixed": S.variant("70b_x16_eagle2", name="small_eagle2_gqa_mixed", d=256, n_q_heads=8,
+                                        n_kv_heads=2, head_dim=32, d_ff=688, vocab=1000, batch=3,
+                                        prefix_len=100, top_k=4, depth=4, top_m=12, weight_std=0.05),
+    "small_static26_dh128": S.variant("7b_static26", name="small_static26_dh128", d=256, n_q_heads=2,
+                                      n_kv_heads=2, head_dim=128, d_ff=688, vocab=2000, prefix_len=300,
+                                      weight_std=0.05),
+    "small_eagle2_ragged_k10": S.variant("13b_x8_eagle2", name="small_eagle2_ragged_k10", d=128, n_q_heads=2,
+                                         n_kv_heads=2, head_dim=64, d_ff=344, vocab=3000, batch=4,
+                                         prefix_range=(50, 400), weight_std=0.05),
+    "small_rows160_two_mma": S.variant("70b_x16_eagle2", name="small_rows160_two_mma", d=128, n_q_heads=4,
+                                       n_kv_heads=2, head_dim=32, d_ff=256, vocab=700, prefix_len=64,
+                                       weight_std=0.05),
+}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", list(SMALL))
+def test_round_parity_small(name):
+    w = SMALL[name]
+    seed = 77
+    gpu = run_gpu_round(w, seed)
+    ref = run_oracle_round(w, seed, gpu["inputs_cpu"], gpu["weights_cpu"])
+    rep = compare_round(w, gpu, ref)
+    assert rep["ok"], rep
+    assert not rep["near_ties"], rep        # expected count 0 for these seeds
+
+
+FULL = {"7b_static26": None, "7b_eagle2": None, "13b_x8_eagle2": [0, 7], "70b_x16_eagle2": [0, 1]}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", list(FULL))
+def test_round_parity_full_size(name):
+    """Full-size workloads in the bench's launch configuration; the oracle
+    recomputes the listed requests (all when None)."""
+    w = S.WORKLOADS[name]
+    seed = S.WORKLOAD_SEEDS[name]
+    gpu = run_gpu_round(w, seed)
+    reqs = FULL[name]
+    ref = run_oracle_round(w, seed, gpu["inputs_cpu"], gpu["weights_cpu"], requests=reqs)
+    rep = compare_round(w, gpu, ref, requests=reqs)
+    assert rep["ok"], rep
+    assert len(rep["near_ties"]) == 0, rep
