@@ -144,7 +144,7 @@ def _declare(L):
         "eagle_commit": [P, I, C.POINTER(eagle_accept_out), C.POINTER(eagle_tree), P, I, P, P, P, P, I, P,
                          C.POINTER(eagle_draft_out), C.POINTER(eagle_kv), C.POINTER(eagle_commit_out), P],
         "eagle_trace_enable": [P, I, I],
-        "eagle_trace_read": [P, C.POINTER(C.c_float), I, C.POINTER(I)],
+        "eagle_trace_read": [P, C.POINTER(C.c_float), C.POINTER(I), I, C.POINTER(I)],
         "eagle_trace_disable": [P],
     }
     for name, args in sig.items():
@@ -263,10 +263,13 @@ def eagle_trace_enable(ctx, kernel: str, capacity: int):
 
 
 def eagle_trace_read(ctx, cap: int):
+    """[(kernel class name, ms)] of the recorded launches, in launch order."""
     buf = (C.c_float * cap)()
+    ids = (I * cap)()
     n = I()
-    _check("eagle_trace_read", lib().eagle_trace_read(ctx, buf, cap, C.byref(n)))
-    return list(buf[: n.value])
+    _check("eagle_trace_read", lib().eagle_trace_read(ctx, buf, ids, cap, C.byref(n)))
+    names = {v: k for k, v in KERNEL_ID.items()}
+    return [(names.get(ids[i], str(ids[i])), buf[i]) for i in range(n.value)]
 
 
 def eagle_trace_disable(ctx):

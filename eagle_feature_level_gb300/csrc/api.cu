@@ -183,6 +183,7 @@ void trace_after(eagle_ctx* ctx, int kernel_id, cudaStream_t s) {
   TraceState& t = ctx->trace;
   if (t.kernel_id == -2 || (t.kernel_id != -1 && t.kernel_id != kernel_id) || t.n >= t.capacity) return;
   cudaEventRecord(t.events[2 * t.n + 1], s);
+  t.ids[t.n] = kernel_id;
   ++t.n;
 }
 
@@ -544,13 +545,14 @@ eagle_status eagle_trace_enable(eagle_ctx* ctx, int kernel_id, int capacity) {
     EAGLE_CUDA(cudaEventCreate(&e));
     t.events.push_back(e);
   }
+  t.ids.assign(capacity, -1);
   t.capacity = capacity;
   t.kernel_id = kernel_id;
   t.n = 0;
   return EAGLE_OK;
 }
 
-eagle_status eagle_trace_read(eagle_ctx* ctx, float* ms_out, int cap, int* n_out) {
+eagle_status eagle_trace_read(eagle_ctx* ctx, float* ms_out, int* ids_out, int cap, int* n_out) {
   EAGLE_REQUIRE(ctx && n_out && (ms_out || cap == 0), EAGLE_ERR_INVALID_ARG);
   TraceState& t = ctx->trace;
   const int n = std::min(t.n, cap);
@@ -559,6 +561,7 @@ eagle_status eagle_trace_read(eagle_ctx* ctx, float* ms_out, int cap, int* n_out
     float ms = 0.f;
     EAGLE_CUDA(cudaEventElapsedTime(&ms, t.events[2 * i], t.events[2 * i + 1]));
     ms_out[i] = ms;
+    if (ids_out) ids_out[i] = t.ids[i];
   }
   *n_out = n;
   return EAGLE_OK;

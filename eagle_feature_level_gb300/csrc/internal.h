@@ -49,6 +49,7 @@ struct TraceState {
   int kernel_id = -2;            // -2: disabled
   int capacity = 0;
   std::vector<cudaEvent_t> events;   // pairs
+  std::vector<int> ids;              // kernel class of each pair
   int n = 0;
 };
 

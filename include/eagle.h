@@ -377,8 +377,9 @@ typedef enum {
   EAGLE_K_COMMIT = 11, EAGLE_K_PREP = 12
 } eagle_kernel_id;
 eagle_status eagle_trace_enable(eagle_ctx* ctx, int kernel_id, int capacity);
-/* Synchronises the recorded events; writes up to `cap` durations in ms and the count. */
-eagle_status eagle_trace_read(eagle_ctx* ctx, float* ms_out, int cap, int* n_out);
+/* Synchronises the recorded events; writes up to `cap` durations in ms, the
+ * kernel class of each (ids_out may be NULL) and the count. */
+eagle_status eagle_trace_read(eagle_ctx* ctx, float* ms_out, int* ids_out, int cap, int* n_out);
 eagle_status eagle_trace_disable(eagle_ctx* ctx);
 
 /* Kernels this context has launched so far (host-side count). */

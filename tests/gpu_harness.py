@@ -16,65 +16,14 @@ import numpy as np
 import torch
 
 import eagle_synth as S
-from eagle_synth.standin import target_logits_from_draft
 from eagle_feature_level_gb300 import runtime as R
+from eagle_feature_level_gb300.workload import make_round, standin
 
 TOL_PROB = 1e-3
 
 
 def feature_tol(w) -> float:
     return 1e-4 if w.name.startswith("tiny") else 2e-2
-
-
-def limits_for(w):
-    tree_slots = 1 + w.top_m
-    E = S.max_expanded(w)
-    rows = w.batch * (1 if w.tree != "eagle2" else w.top_k)
-    if w.tree != "eagle2":
-        plan = R.plan_for(w.tree)
-        rows = w.batch * max(plan.layer_rows[l] for l in range(plan.n_layers))
-    return dict(max_batch=w.batch, max_rows=rows, max_expanded=E, max_children=w.top_k,
-                max_tree=tree_slots)
-
-
-def dims_of(w):
-    return dict(d=w.d, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, d_ff=w.d_ff,
-                vocab=w.vocab, rms_eps=w.rms_eps, rope_theta=w.rope_theta)
-
-
-def make_round(w, inp, device="cuda"):
-    lim = limits_for(w)
-    eng = R.Engine(dims_of(w), max_prefix=inp["kv_cap"], device=device, **lim)
-    plan = R.plan_for(w.tree, w.top_k, w.depth, w.top_m)
-    rd = R.Round(eng, plan, w.batch, inp["kv_cap"])
-    load_round(rd, w, inp)
-    return eng, rd
-
-
-def load_round(rd, w, inp):
-    dev = rd.eng.device
-    L = torch.tensor(inp["prefix_len"], dtype=torch.int32, device=dev)
-    rd.t_next.copy_(inp["t_next"])
-    rd.f_last.copy_(inp["f_last"])
-    rd.pos0.copy_(L)
-    rd.temps.copy_(torch.tensor(inp["temps"], dtype=torch.float32, device=dev))
-    rd.draft_k.copy_(inp["draft_k"])
-    rd.draft_v.copy_(inp["draft_v"])
-    rd.draft_len.copy_(torch.tensor(inp["draft_len"], dtype=torch.int32, device=dev))
-    rd.tgt_k[0].copy_(inp["tgt_k"])
-    rd.tgt_v[0].copy_(inp["tgt_v"])
-    rd.tgt_len.copy_(L)
-    rd.tree_q.copy_(inp["tree_q"])
-    rd.tree_k[0].copy_(inp["tree_k"])
-    rd.tree_v[0].copy_(inp["tree_v"])
-    rd.f_true.copy_(inp["f_true"])
-    rd.set_sampling(inp["philox_seed"], inp["round_id"])
-
-
-def standin(inp):
-    def fn(rd):
-        target_logits_from_draft(rd.logits, rd.t_exp, inp["tgt_noise"], inp["tgt_fresh"], rd.target_logits)
-    return fn
 
 
 GPU_FIELDS = ["p_token", "p_parent", "p_depth", "p_value", "c_token", "c_prob", "f_hat", "logits", "probs",
