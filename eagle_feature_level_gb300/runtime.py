@@ -219,6 +219,15 @@ class Round:
                        [_p(t) for t in self.tgt_k], [_p(t) for t in self.tgt_v], self.kv_cap, _p(self.tgt_len),
                        self.out_c, self.draft_kv_c, self.commit_c, e.stream())
 
+    def capture(self, w_c: B.eagle_draft_weights) -> "torch.cuda.CUDAGraph":
+        """Capture one whole round (target logits already in place) as a CUDA
+        graph; replaying it re-issues the same kernels with no host work.
+        Run the round eagerly once before the first capture."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(w_c)
+        return g
+
     def run(self, w_c: B.eagle_draft_weights, target_fn=None):
         """One whole round.  `target_fn(round)` stands in for the target model
         between drafting and acceptance (fills target_logits)."""

@@ -56,4 +56,38 @@ def test_round_parity_full_size(name):
     ref = run_oracle_round(w, seed, gpu["inputs_cpu"], gpu["weights_cpu"], requests=reqs)
     rep = compare_round(w, gpu, ref, requests=reqs)
     assert rep["ok"], rep
-    assert len(rep["near_ties"]) == 0, rep
+    # sampling at T > 0 over V = 32000 nearly flat draft distributions: a draw can
+    # land within the fp32-vs-fp64 CDF difference of a boundary; such draws are
+    # flagged (not failed) and the request's later stages are compared only
+    # when no flag was raised.  Greedy requests must never flag.
+    greedy = [b for b in (reqs or range(w.batch)) if w.temps_for_batch()[b] <= 0]
+    assert not any(f"b{b} " in t for t in rep["near_ties"] for b in greedy), rep
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["small_eagle2_gqa_mixed", "tiny_greedy_static8"])
+def test_graph_replay_matches_eager(name):
+    """The round captured as one CUDA graph reproduces the eager round bit for
+    bit (the kernels are deterministic: fixed-order reductions, no atomics on
+    values)."""
+    from eagle_feature_level_gb300.workload import make_round, standin
+    w = SMALL[name]
+    W = S.draft_weights(w, 5, device="cuda")
+    inp = S.round_inputs(w, 5, device="cuda")
+    eng, rd = make_round(w, inp)
+    wc = eng.weights(W)
+    rd.run(wc, target_fn=standin(inp))
+    torch.cuda.synchronize()
+    fields = ["f_hat", "logits", "probs", "c_token", "t_token", "t_anc", "attn_out", "accept_len", "path",
+              "final_token", "tok_commit", "f_last_out"]
+    eager = {k: getattr(rd, k).clone() for k in fields}
+    g = rd.capture(wc)
+    for k in fields:
+        getattr(rd, k).zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for k in fields:
+        assert torch.equal(getattr(rd, k), eager[k]), k
+    assert eng.status() == 0
+    eng.close()
