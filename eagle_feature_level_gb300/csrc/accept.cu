@@ -187,12 +187,15 @@ __global__ void __launch_bounds__(SM_THREADS) accept_walk_kernel(const WalkParam
         __syncthreads();
         if (s_flag) {
           const int slot = s_u;
-          if (slot >= 0) {
+          if (slot >= 0 && a + 1 < p.path_cap) {
             u = slot;
             ++a;
             if (tid == 0) path[a] = u;
             descended = true;
           } else {
+            // accepted but pruned: x is the final token (a full path cannot
+            // occur: path_cap >= depth + 1 is checked on the host)
+            if (slot >= 0) set_status(p.status, EAGLE_ERR_CAPACITY);
             final_tok = x;
           }
           break;
@@ -228,8 +231,7 @@ __global__ void __launch_bounds__(SM_THREADS) accept_walk_kernel(const WalkParam
         __syncthreads();
       }
     }
-    if (descended && a + 1 < p.path_cap) continue;
-    if (descended) set_status(p.status, EAGLE_ERR_CAPACITY);
+    if (descended) continue;          // reload P for the accepted child
     if (final_tok < 0) {
       // one draw from P: thread slices, inclusive scan, search
       uint64_t ls3 = 0;

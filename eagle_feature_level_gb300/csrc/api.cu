@@ -177,12 +177,13 @@ namespace eagle {
 void trace_before(eagle_ctx* ctx, int kernel_id, cudaStream_t s) {
   TraceState& t = ctx->trace;
   if (t.kernel_id == -2 || (t.kernel_id != -1 && t.kernel_id != kernel_id) || t.n >= t.capacity) return;
-  cudaEventRecord(t.events[2 * t.n], s);
+  // external records: inside a stream capture they become timing nodes of the graph
+  cudaEventRecordWithFlags(t.events[2 * t.n], s, cudaEventRecordExternal);
 }
 void trace_after(eagle_ctx* ctx, int kernel_id, cudaStream_t s) {
   TraceState& t = ctx->trace;
   if (t.kernel_id == -2 || (t.kernel_id != -1 && t.kernel_id != kernel_id) || t.n >= t.capacity) return;
-  cudaEventRecord(t.events[2 * t.n + 1], s);
+  cudaEventRecordWithFlags(t.events[2 * t.n + 1], s, cudaEventRecordExternal);
   t.ids[t.n] = kernel_id;
   ++t.n;
 }

@@ -1,6 +1,8 @@
 """GPU parity: whole rounds through the C ABI against the oracle, element by
 element, on small cases that span several tiles and ragged tails, and on the
 full-size workloads (sampled requests)."""
+import json
+
 import pytest
 import torch
 
@@ -37,8 +39,8 @@ def test_round_parity_small(name):
     gpu = run_gpu_round(w, seed)
     ref = run_oracle_round(w, seed, gpu["inputs_cpu"], gpu["weights_cpu"])
     rep = compare_round(w, gpu, ref)
-    assert rep["ok"], rep
-    assert not rep["near_ties"], rep        # expected count 0 for these seeds
+    if not rep["ok"] or rep["near_ties"]:   # expected near-tie count 0 for these seeds
+        pytest.fail(json.dumps(rep, indent=1))
 
 
 FULL = {"7b_static26": None, "7b_eagle2": None, "13b_x8_eagle2": [0, 7], "70b_x16_eagle2": [0, 1]}
@@ -55,7 +57,8 @@ def test_round_parity_full_size(name):
     reqs = FULL[name]
     ref = run_oracle_round(w, seed, gpu["inputs_cpu"], gpu["weights_cpu"], requests=reqs)
     rep = compare_round(w, gpu, ref, requests=reqs)
-    assert rep["ok"], rep
+    if not rep["ok"]:
+        pytest.fail(json.dumps(rep, indent=1))
     # sampling at T > 0 over V = 32000 nearly flat draft distributions: a draw can
     # land within the fp32-vs-fp64 CDF difference of a boundary; such draws are
     # flagged (not failed) and the request's later stages are compared only
