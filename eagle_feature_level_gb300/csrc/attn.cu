@@ -18,7 +18,6 @@ namespace {
 constexpr int TILE = 64;          // KV rows per shared-memory tile
 constexpr int THREADS = 256;
 constexpr int MAX_DH = 128;
-constexpr int PAD = 8;            // bf16 pad per smem row: conflict-free 16-byte reads
 
 struct AttnParams {
   int mode;                       // 0 draft, 1 verify
@@ -55,25 +54,41 @@ __device__ __forceinline__ size_t q_index(const AttnParams& p, int b, int node, 
   return ((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * p.dh;
 }
 
-// element d of tree key/value row j (kv head h) of request b
-__device__ __forceinline__ float tree_k(const AttnParams& p, int b, int j, int h, int d) {
-  const size_t i = ((static_cast<size_t>(b) * p.tree_cap + j) * p.Hkv + h) * p.dh + d;
-  return p.mode == 0 ? p.kt_f32[i] : bf16_to_f32(p.kt_bf16[i]);
-}
-__device__ __forceinline__ float tree_v(const AttnParams& p, int b, int j, int h, int d) {
-  const size_t i = ((static_cast<size_t>(b) * p.tree_cap + j) * p.Hkv + h) * p.dh + d;
-  return p.mode == 0 ? p.vt_f32[i] : bf16_to_f32(p.vt_bf16[i]);
-}
-
 __device__ __forceinline__ uint64_t row_mask(const AttnParams& p, int b, int node) {
   if (p.mode == 0) return p.anc[static_cast<size_t>(b) * p.tree_cap + p.e0 + node];
   return p.anc[static_cast<size_t>(b) * p.tree_cap + node];
 }
 
+// fp32 K/V tiles in dynamic shared memory: [TILE][dh + 4] each; the 4-word
+// row pad keeps lane-per-row float4 reads conflict-free.
+__device__ __forceinline__ void stage_rows(float* dst, int ld, const uint16_t* src_bf16, const float* src_f32,
+                                           size_t row0, size_t row_stride, int nt, int dh) {
+  if (src_f32) {
+    const int pieces = dh / 4;
+    for (int idx = threadIdx.x; idx < nt * pieces; idx += THREADS) {
+      const int r = idx / pieces, c = idx % pieces;
+      *reinterpret_cast<float4*>(dst + r * ld + c * 4) =
+          __ldg(reinterpret_cast<const float4*>(src_f32 + row0 + r * row_stride) + c);
+    }
+  } else {
+    const int pieces = dh / 8;
+    for (int idx = threadIdx.x; idx < nt * pieces; idx += THREADS) {
+      const int r = idx / pieces, c = idx % pieces;
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(src_bf16 + row0 + r * row_stride) + c);
+      float4 a, b;
+      a.x = __uint_as_float(w.x << 16); a.y = __uint_as_float(w.x & 0xffff0000u);
+      a.z = __uint_as_float(w.y << 16); a.w = __uint_as_float(w.y & 0xffff0000u);
+      b.x = __uint_as_float(w.z << 16); b.y = __uint_as_float(w.z & 0xffff0000u);
+      b.z = __uint_as_float(w.w << 16); b.w = __uint_as_float(w.w & 0xffff0000u);
+      *reinterpret_cast<float4*>(dst + r * ld + c * 8) = a;
+      *reinterpret_cast<float4*>(dst + r * ld + c * 8 + 4) = b;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) {
-  __shared__ __align__(16) uint16_t sk[TILE][MAX_DH + PAD];
-  __shared__ __align__(16) uint16_t sv[TILE][MAX_DH + PAD];
-  __shared__ float sq[8][MAX_DH];
+  extern __shared__ __align__(16) float smem_kv[];
+  __shared__ __align__(16) float sq[8][MAX_DH];
   __shared__ int s_last;
 
   const int split = blockIdx.x;              // split == n_splits: the tree part
@@ -81,6 +96,9 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
   const int b = pair / p.Hkv, h = pair % p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int dh = p.dh;
+  const int ld = dh + 4;
+  float* sk = smem_kv;
+  float* sv = smem_kv + TILE * ld;
   const int nodes = n_nodes(p, b);
   const int R = nodes * p.G;
   const bool is_tree = split == p.n_splits;
@@ -93,6 +111,7 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
     hi = p.mode == 0 ? p.tree_cap : min(p.tree_size[b], p.tree_cap);
   }
   const int rec = dh + 2;
+  const size_t row_stride = static_cast<size_t>(p.Hkv) * dh;
 
   // Each warp owns query rows r = r0 + warp + 8 i (i < 8); running state in registers.
   for (int r0 = 0; r0 < R; r0 += 64) {
@@ -107,14 +126,14 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
     for (int t0 = lo; t0 < hi; t0 += TILE) {
       const int nt = min(TILE, hi - t0);
       __syncthreads();
-      if (!is_tree) {   // stage the prefix K/V tile; the (small) tree part is read from global
-        const int pieces = dh / 8;
-        for (int idx = threadIdx.x; idx < nt * pieces; idx += THREADS) {
-          const int r = idx / pieces, c = idx % pieces;
-          const size_t g = ((static_cast<size_t>(b) * p.kv_cap + t0 + r) * p.Hkv + h) * dh + c * 8;
-          *reinterpret_cast<uint4*>(&sk[r][c * 8]) = __ldg(reinterpret_cast<const uint4*>(p.kp + g));
-          *reinterpret_cast<uint4*>(&sv[r][c * 8]) = __ldg(reinterpret_cast<const uint4*>(p.vp + g));
-        }
+      if (!is_tree) {
+        const size_t row0 = ((static_cast<size_t>(b) * p.kv_cap + t0) * p.Hkv + h) * dh;
+        stage_rows(sk, ld, p.kp, nullptr, row0, row_stride, nt, dh);
+        stage_rows(sv, ld, p.vp, nullptr, row0, row_stride, nt, dh);
+      } else {
+        const size_t row0 = ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh;
+        stage_rows(sk, ld, p.kt_bf16, p.kt_f32, row0, row_stride, nt, dh);
+        stage_rows(sv, ld, p.vt_bf16, p.vt_f32, row0, row_stride, nt, dh);
       }
       __syncthreads();
 #pragma unroll
@@ -133,20 +152,16 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
           const int j = lane + 32 * half;
           float s = -INFINITY;
           const bool vis = j < nt && (!is_tree || ((mask >> (t0 + j)) & 1ull));
-          if (vis && is_tree) {
+          if (vis) {
+            const float* kr = sk + j * ld;
             float dot = 0.f;
-            for (int d = 0; d < dh; ++d) dot = fmaf(sq[warp][d], tree_k(p, b, t0 + j, h, d), dot);
-            s = dot * p.scale;
-          } else if (vis) {
-            float dot = 0.f;
-            for (int d0 = 0; d0 < dh; d0 += 8) {
-              const uint4 kv = *reinterpret_cast<const uint4*>(&sk[j][d0]);
-              const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                dot = fmaf(sq[warp][d0 + 2 * c], __uint_as_float(w[c] << 16), dot);
-                dot = fmaf(sq[warp][d0 + 2 * c + 1], __uint_as_float(w[c] & 0xffff0000u), dot);
-              }
+            for (int d0 = 0; d0 < dh; d0 += 4) {
+              const float4 kv = *reinterpret_cast<const float4*>(kr + d0);
+              const float4 qv = *reinterpret_cast<const float4*>(&sq[warp][d0]);
+              dot = fmaf(qv.x, kv.x, dot);
+              dot = fmaf(qv.y, kv.y, dot);
+              dot = fmaf(qv.z, kv.z, dot);
+              dot = fmaf(qv.w, kv.w, dot);
             }
             s = dot * p.scale;
           }
@@ -166,11 +181,11 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
         for (int j = 0; j < nt; ++j) {
           const float pj = __shfl_sync(0xffffffffu, j < 32 ? p0 : p1, j & 31);
           if (pj == 0.f) continue;
+          const float* vr = sv + j * ld;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             const int d = lane + 32 * c;
-            if (d < dh)
-              acc[i][c] = fmaf(pj, is_tree ? tree_v(p, b, t0 + j, h, d) : bf16_to_f32(sv[j][d]), acc[i][c]);
+            if (d < dh) acc[i][c] = fmaf(pj, vr[d], acc[i][c]);
           }
         }
       }
@@ -258,8 +273,16 @@ static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaSt
   p.n_splits = attn_splits(ctx, p.B * p.Hkv, p.kv_cap);
   p.chunk = ceil_div(ceil_div(p.kv_cap, p.n_splits), TILE) * TILE;
   dim3 grid(p.n_splits + 1, p.B * p.Hkv);
+  const size_t smem = static_cast<size_t>(2) * TILE * (p.dh + 4) * sizeof(float);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(2 * TILE * (MAX_DH + 4) * sizeof(float)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   trace_before(ctx, kernel_id, st);
-  tree_attn_kernel<<<grid, THREADS, 0, st>>>(p);
+  tree_attn_kernel<<<grid, THREADS, smem, st>>>(p);
   ctx->launches++;
   trace_after(ctx, kernel_id, st);
   return cudaGetLastError();

@@ -55,9 +55,9 @@ __global__ void commit_kernel(const CommitParams p) {
     copy_row(p.kc[l] + dst, p.kt[l] + src, p.row_elems);
     copy_row(p.vc[l] + dst, p.vt[l] + src, p.row_elems);
   }
-  const float* f = p.f_true + (static_cast<size_t>(b) * p.S + slot) * p.d;
-  float* fc = p.f_commit + (static_cast<size_t>(b) * p.path_cap + i) * p.d;
-  for (int c = threadIdx.x; c < p.d; c += blockDim.x) fc[c] = f[c];
+  const float4* f = reinterpret_cast<const float4*>(p.f_true + (static_cast<size_t>(b) * p.S + slot) * p.d);
+  float4* fc = reinterpret_cast<float4*>(p.f_commit + (static_cast<size_t>(b) * p.path_cap + i) * p.d);
+  for (int c = threadIdx.x; c < p.d / 4; c += blockDim.x) fc[c] = f[c];
   if (threadIdx.x == 0) {
     int32_t* tc = p.tok_commit + static_cast<size_t>(b) * (p.path_cap + 1);
     tc[i] = p.t_token[static_cast<size_t>(b) * p.S + slot];
@@ -65,8 +65,9 @@ __global__ void commit_kernel(const CommitParams p) {
   }
   if (i == 0) {
     const int last = p.last_slot[b];
-    const float* fl = p.f_true + (static_cast<size_t>(b) * p.S + last) * p.d;
-    for (int c = threadIdx.x; c < p.d; c += blockDim.x) p.f_last[static_cast<size_t>(b) * p.d + c] = fl[c];
+    const float4* fl = reinterpret_cast<const float4*>(p.f_true + (static_cast<size_t>(b) * p.S + last) * p.d);
+    float4* fo = reinterpret_cast<float4*>(p.f_last + static_cast<size_t>(b) * p.d);
+    for (int c = threadIdx.x; c < p.d / 4; c += blockDim.x) fo[c] = fl[c];
     if (threadIdx.x == 0) {
       p.t_next[b] = p.final_token[b];
       p.prefix_len_out[b] = L + 1 + a;
@@ -124,7 +125,7 @@ cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st
   p.draft_len_out = C.out->draft_len;
   dim3 grid(C.batch, C.acc->path_cap);
   trace_before(ctx, EAGLE_K_COMMIT, st);
-  commit_kernel<<<grid, 128, 0, st>>>(p);
+  commit_kernel<<<grid, 512, 0, st>>>(p);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_COMMIT, st);
   return cudaGetLastError();

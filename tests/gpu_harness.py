@@ -7,8 +7,10 @@ accept length, path, tokens) must be identical; a mismatch is tolerated only
 as a flagged near-tie, when the oracle's own margin for that decision is
 below the floating-point tolerance, and the request's later comparisons are
 then skipped.  Floating point: features, logits and attention outputs within
-max-abs 1e-4 (fp32 workload) or 2e-2 (bf16 workloads); probabilities within
-1e-3.
+max-abs 1e-4 (fp32 workload) or 2e-2 (bf16 workloads), applied to values in
+units of the row's RMS when that exceeds 1 (random draft weights grow the
+residual stream layer by layer, to RMS ~10^2 at depth 5 of the 70B shape,
+while the bound presumes unit-scale features); probabilities within 1e-3.
 """
 from __future__ import annotations
 
@@ -63,6 +65,13 @@ def _maxerr(a, b) -> float:
     return float(np.max(np.abs(a - b))) if a.size else 0.0
 
 
+def _maxerr_scaled(a, b) -> float:
+    """max |a - b| in units of max(1, RMS of the oracle row b)."""
+    b = np.asarray(b, dtype=np.float64)
+    scale = max(1.0, float(np.sqrt(np.mean(b * b)))) if b.size else 1.0
+    return _maxerr(a, b) / scale
+
+
 def _f64(t):
     return t.to(torch.float64).numpy() if torch.is_tensor(t) else np.asarray(t, dtype=np.float64)
 
@@ -100,8 +109,8 @@ def compare_round(w, gpu, ref, requests=None):
                 fail(f"b{b} pool token e{e}: {int(gpu['p_token'][b, e])} vs {ex.token[e]}")
                 diverged = True
                 break
-            err("f_hat", _maxerr(gpu["f_hat"][b, e], st.f_hat[e]), tol)
-            err("logits", _maxerr(gpu["logits"][b, e], st.z[e]), tol)
+            err("f_hat", _maxerr_scaled(gpu["f_hat"][b, e], st.f_hat[e]), tol)
+            err("logits", _maxerr_scaled(gpu["logits"][b, e], st.z[e]), tol)
             err("probs", _maxerr(gpu["probs"][b, e], st.q[e]), TOL_PROB)
             err("draft_k", _maxerr(gpu["dk_tree"][b, e], st.k_tree[e]), tol)
             k = len(st.child_tok[e])
@@ -152,7 +161,8 @@ def compare_round(w, gpu, ref, requests=None):
             continue
         # verification attention, target distribution
         err("verify_out", _maxerr(gpu["attn_out"][b, :size], r["verify_out"]), tol)
-        err("target_logits", _maxerr(gpu["target_logits"][b, :size], r["target_logits"]), tol)
+        for s_ in range(size):
+            err("target_logits", _maxerr_scaled(gpu["target_logits"][b, s_], r["target_logits"][s_]), tol)
         if temp > 0:
             err("target_probs", _maxerr(gpu["target_probs"][b, :size], r["target_probs"]), TOL_PROB)
         # acceptance
