@@ -128,7 +128,11 @@ def compare_round(w, gpu, ref, requests=None):
                         wq[t] = 0.0
                     cdf = np.cumsum(wq) / wq.sum()
                     margin = float(np.min(np.abs(cdf - u / 2.0 ** 32)))
-                    near = margin < 1e-5
+                    # q = softmax(z / T): a logit error dz moves every CDF point by at
+                    # most 2 max|dz| / T (relative to the remaining mass)
+                    dz = _maxerr(gpu["logits"][b, e], st.z[e])
+                    rem = wq.sum() / max(1.0, float(quantize(st.q[e]).sum()))
+                    near = margin < 2.0 * dz / temp / max(rem, 1e-12) + 1e-6
                 if near:
                     rep["near_ties"].append(f"b{b} e{e} rank{rank} margin {margin:.2e}")
                     diverged = True
