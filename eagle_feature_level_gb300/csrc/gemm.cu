@@ -143,148 +143,134 @@ __device__ __forceinline__ void put_split(uint16_t* buf, int NP, int kp, int j, 
   buf[static_cast<size_t>(NP + j) * kp + col] = lo;
 }
 
-// Per-warp sums of v for each of nj rows into red[warp][row].
-__device__ __forceinline__ void reduce_rows(const Smem& s, float (&v)[XCH_ROWS], int nj, int m) {
-  const int lane = m & 31, w = m >> 5;
-#pragma unroll
-  for (int jj = 0; jj < XCH_ROWS; ++jj) {
-    if (jj < nj) {
-      const float t = warp_sum(v[jj]);
-      if (lane == 0) s.red[w * 32 + jj] = t;
-    }
-  }
-  sm100::named_barrier(1, EPI_THREADS);
-}
-
 // Final epilogue of tile t: sum the partials of CTAs [c_first, c_last] and
 // apply the contraction's fused elementwise work.  `m` is the tile row this
-// thread owns (its tensor-memory lane); m >> 5 names its warp, m & 31 its lane.
-__device__ void finalize_tile(const GemmParams& p, const Smem& s, int t, int c_first, int c_last, int m) {
+// thread owns (its tensor-memory lane); m >> 5 names its warp, m & 31 its
+// lane.  Runs once per tile, so it is written as compact loops over shared
+// memory (small code, few instruction-cache misses) rather than unrolled.
+__device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, int t, int c_first, int c_last,
+                                           int m) {
+  const int lane = m & 31, w = m >> 5;
+  // per-row constants of this thread's output index
+  int gi = t * BM + m;
+  const int qd = p.Hq * p.dh, kd = p.Hkv * p.dh;
+  const int half = p.dh >> 1;
+  bool rope = false, is_v = false, rot_first = false;
+  int head = 0, di = 0, partner = m;
+  double inv_freq = 0.0;
+  if (p.epi == EPI_QKV && gi < qd + 2 * kd) {
+    is_v = gi >= qd + kd;
+    const int base = gi < qd ? 0 : (gi < qd + kd ? qd : qd + kd);
+    head = (gi - base) / p.dh;
+    di = (gi - base) % p.dh;
+    rot_first = di < half;
+    partner = rot_first ? m + half : m - half;
+    rope = !is_v;
+    inv_freq = exp(-(2.0 * (rot_first ? di : di - half) / p.dh) * p.ln_theta);
+  }
   for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
     const int nj = min(XCH_ROWS, p.n - jc);
-    float acc[XCH_ROWS];
-#pragma unroll
-    for (int jj = 0; jj < XCH_ROWS; ++jj) {
-      acc[jj] = 0.f;
-      if (jj < nj) {
-        const int j = jc + jj;
-        for (int c = c_first; c <= c_last; ++c)
-          acc[jj] += __ldcg(p.part + (static_cast<size_t>(t + c) * p.n + j) * BM + m);
-      }
+    // 1. accumulate the partials of every CTA that worked on this tile, in CTA order
+#pragma unroll 1
+    for (int jj = 0; jj < nj; ++jj) {
+      float a = 0.f;
+      for (int c = c_first; c <= c_last; ++c)
+        a += __ldcg(p.part + (static_cast<size_t>(t + c) * p.n + jc + jj) * BM + m);
+      s.xch[jj * BM + m] = a;
     }
-    // RMSNorm scale of the input rows (QKV: after FC, GATEUP: after O)
+    // 2. RMSNorm scale of the input rows (QKV: after FC, GATEUP: after O)
     if (p.epi == EPI_QKV || p.epi == EPI_GATEUP) {
       if (m < nj) {
-        const int j = jc + m;
-        float ss = 0.f;
-        for (int i = 0; i < p.ss_in_tiles; ++i) ss += __ldcg(p.ss_in + static_cast<size_t>(j) * p.ss_in_tiles + i);
-        s.rs[m] = 1.0f / sqrtf(ss / static_cast<float>(p.d) + p.eps);
+        const float* ss = p.ss_in + static_cast<size_t>(jc + m) * p.ss_in_tiles;
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        int i = 0;
+        for (; i + 4 <= p.ss_in_tiles; i += 4) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) acc4[u] += __ldcg(ss + i + u);
+        }
+        for (; i < p.ss_in_tiles; ++i) acc4[0] += __ldcg(ss + i);
+        const float tot = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+        s.rs[m] = 1.0f / sqrtf(tot / static_cast<float>(p.d) + p.eps);
       }
-      sm100::named_barrier(1, EPI_THREADS);
-#pragma unroll
-      for (int jj = 0; jj < XCH_ROWS; ++jj)
-        if (jj < nj) acc[jj] *= s.rs[jj];
-#pragma unroll
-      for (int jj = 0; jj < XCH_ROWS; ++jj)
-        if (jj < nj) s.xch[jj * BM + m] = acc[jj];
-      sm100::named_barrier(1, EPI_THREADS);
     }
-
+    sm100::named_barrier(1, EPI_THREADS);
+    // 3. the contraction's elementwise epilogue, one activation row at a time
     if (p.epi == EPI_FC || p.epi == EPI_O) {
-      const int gi = t * BM + m;
       const bool valid = gi < p.d;
-      float sq[XCH_ROWS];
-#pragma unroll
-      for (int jj = 0; jj < XCH_ROWS; ++jj) {
-        sq[jj] = 0.f;
-        if (jj < nj && valid) {
-          const int j = jc + jj;
-          float v = acc[jj];
-          if (p.epi == EPI_FC) v += p.bias[gi];
-          else v += p.resid[static_cast<size_t>(j) * p.d + gi];
+#pragma unroll 1
+      for (int jj = 0; jj < nj; ++jj) {
+        const int j = jc + jj;
+        float v = 0.f;
+        if (valid) {
+          v = s.xch[jj * BM + m];
+          v += p.epi == EPI_FC ? p.bias[gi] : p.resid[static_cast<size_t>(j) * p.d + gi];
           p.out_f32[static_cast<size_t>(j) * p.d + gi] = v;
           put_split(p.bnext, p.NP, p.kp_next, j, gi, v * p.gain[gi]);
-          sq[jj] = v * v;
         }
-      }
-      reduce_rows(s, sq, nj, m);
-      if (m < nj) {
-        const float tot = s.red[m] + s.red[32 + m] + s.red[64 + m] + s.red[96 + m];
-        p.ss_out[static_cast<size_t>(jc + m) * p.m_tiles + t] = tot;
+        const float sq = warp_sum(v * v);
+        if (lane == 0) s.red[w * 32 + jj] = sq;
       }
       sm100::named_barrier(1, EPI_THREADS);
+      if (m < nj)
+        p.ss_out[static_cast<size_t>(jc + m) * p.m_tiles + t] =
+            (s.red[m] + s.red[32 + m]) + (s.red[64 + m] + s.red[96 + m]);
     } else if (p.epi == EPI_QKV) {
-      const int gi = t * BM + m;
-      const int qd = p.Hq * p.dh, kd = p.Hkv * p.dh;
-      const int half = p.dh >> 1;
       if (gi < qd + 2 * kd) {
-        const bool is_v = gi >= qd + kd;
-        const int base = gi < qd ? 0 : (gi < qd + kd ? qd : qd + kd);
-        const int head = (gi - base) / p.dh, i = (gi - base) % p.dh;
-        const int ii = i < half ? i : i - half;
-        const int partner = i < half ? m + half : m - half;
-        const double inv_freq = exp(-(2.0 * ii / p.dh) * p.ln_theta);
-#pragma unroll
-        for (int jj = 0; jj < XCH_ROWS; ++jj) {
-          if (jj >= nj) continue;
+#pragma unroll 1
+        for (int jj = 0; jj < nj; ++jj) {
           const int j = jc + jj;
           const int b = j / p.rpr, e = p.e0 + j % p.rpr;
-          float v = acc[jj];
-          if (!is_v) {
+          const float sc = s.rs[jj];
+          float v = s.xch[jj * BM + m] * sc;
+          if (rope) {
             const int pos = p.pos0[b] + p.depth[static_cast<size_t>(b) * p.E + e];
             double ang = static_cast<double>(pos) * inv_freq;
             ang -= 6.283185307179586 * rint(ang * 0.15915494309189535);
             float sn, cs;
             sincosf(static_cast<float>(ang), &sn, &cs);
-            const float other = s.xch[jj * BM + partner];
-            v = i < half ? v * cs - other * sn : v * cs + other * sn;
+            const float other = s.xch[jj * BM + partner] * sc;
+            v = rot_first ? v * cs - other * sn : v * cs + other * sn;
           }
           if (gi < qd) {
             p.qrow[static_cast<size_t>(j) * qd + gi] = v;
           } else {
             float* dst = is_v ? p.v_tree : p.k_tree;
-            dst[((static_cast<size_t>(b) * p.E + e) * p.Hkv + head) * p.dh + i] = v;
+            dst[((static_cast<size_t>(b) * p.E + e) * p.Hkv + head) * p.dh + di] = v;
           }
         }
       }
-      sm100::named_barrier(1, EPI_THREADS);
     } else if (p.epi == EPI_GATEUP) {
       const int c = t * 64 + m;
       if (m < 64 && c < p.F) {
-#pragma unroll
-        for (int jj = 0; jj < XCH_ROWS; ++jj) {
-          if (jj >= nj) continue;
-          const float g = acc[jj], u = s.xch[jj * BM + m + 64];
-          const float sg = g / (1.0f + expf(-g));
-          put_split(p.bnext, p.NP, p.kp_next, jc + jj, c, sg * u);
+#pragma unroll 1
+        for (int jj = 0; jj < nj; ++jj) {
+          const float sc = s.rs[jj];
+          const float g = s.xch[jj * BM + m] * sc, u = s.xch[jj * BM + m + 64] * sc;
+          put_split(p.bnext, p.NP, p.kp_next, jc + jj, c, g / (1.0f + expf(-g)) * u);
         }
       }
-      sm100::named_barrier(1, EPI_THREADS);
     } else if (p.epi == EPI_DOWN) {
-      const int gi = t * BM + m;
       if (gi < p.d) {
-#pragma unroll
-        for (int jj = 0; jj < XCH_ROWS; ++jj) {
-          if (jj >= nj) continue;
+#pragma unroll 1
+        for (int jj = 0; jj < nj; ++jj) {
           const int j = jc + jj;
           const int b = j / p.rpr, e = p.e0 + j % p.rpr;
-          const float v = acc[jj] + p.resid[static_cast<size_t>(j) * p.d + gi];
+          const float v = s.xch[jj * BM + m] + p.resid[static_cast<size_t>(j) * p.d + gi];
           p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.d + gi] = v;
           put_split(p.bnext, p.NP, p.kp_next, j, gi, v);
         }
       }
     } else {  // EPI_LM
-      const int gi = t * BM + m;
       if (gi < p.V) {
-#pragma unroll
-        for (int jj = 0; jj < XCH_ROWS; ++jj) {
-          if (jj >= nj) continue;
+#pragma unroll 1
+        for (int jj = 0; jj < nj; ++jj) {
           const int j = jc + jj;
           const int b = j / p.rpr, e = p.e0 + j % p.rpr;
-          p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.V + gi] = acc[jj];
+          p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.V + gi] = s.xch[jj * BM + m];
         }
       }
     }
+    sm100::named_barrier(1, EPI_THREADS);
   }
 }
 
