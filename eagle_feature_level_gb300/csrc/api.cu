@@ -64,7 +64,7 @@ eagle_status check_plan(const eagle_ctx* c, const eagle_plan* p) {
 
 int splits_bound(const eagle_ctx* c, int pairs) {
   int s = ceil_div(2 * c->sm_count, std::max(1, pairs));
-  return std::min(32, std::max(1, s));
+  return std::min(31, std::max(1, s));
 }
 
 void layout(eagle_ctx* c) {

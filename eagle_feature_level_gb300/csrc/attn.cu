@@ -224,18 +224,30 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
     const int node = r / p.G, hq = h * p.G + r % p.G;
     const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
     const float* src = p.part + qi * (p.n_splits + 1) * rec;
-    float M = -INFINITY;
-    for (int s = 0; s <= p.n_splits; ++s) M = fmaxf(M, __ldcg(src + s * rec));
-    float Lsum = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s <= p.n_splits; ++s) {
-      const float ms = __ldcg(src + s * rec);
-      if (ms == -INFINITY) continue;
-      const float wgt = __expf(ms - M);
-      Lsum += wgt * __ldcg(src + s * rec + 1);
+    // lane s holds split s (n_splits + 1 <= 32): all partial headers load at once
+    const int ns = p.n_splits + 1;
+    const float ms = lane < ns ? __ldcg(src + lane * rec) : -INFINITY;
+    const float ls = lane < ns ? __ldcg(src + lane * rec + 1) : 0.f;
+    const float M = warp_max(ms);
+    const float wgt = ms == -INFINITY ? 0.f : __expf(ms - M);
+    const float Lsum = warp_sum(wgt * ls);
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+      float vals[8][4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int d = lane + 32 * c;
-        if (d < dh) o[c] += wgt * __ldcg(src + s * rec + 2 + d);
+      for (int u = 0; u < 8; ++u) {
+        const int s = s0 + u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int d = lane + 32 * c;
+          vals[u][c] = (s < ns && d < dh) ? __ldcg(src + s * rec + 2 + d) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float ws = __shfl_sync(0xffffffffu, wgt, (s0 + u) & 31);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) o[c] = fmaf(ws, vals[u][c], o[c]);
       }
     }
     const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
@@ -265,7 +277,7 @@ int attn_splits(const eagle_ctx* ctx, int pairs, int cap) {
   const int by_len = ceil_div(cap < 1 ? 1 : cap, TILE);
   if (want > by_len) want = by_len;
   if (want < 1) want = 1;
-  if (want > 32) want = 32;
+  if (want > 31) want = 31;        // n_splits + 1 records fit one warp in the merge
   return want;
 }
 

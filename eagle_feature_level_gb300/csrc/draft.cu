@@ -105,28 +105,40 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelParams p) 
   const float inv_t = greedy ? 1.0f : 1.0f / T;
   const int V = p.V;
 
-  // pass 1: stage logits, row max, per-thread top-k (greedy)
+  // pass 1: stage logits, row max, per-thread top-k (greedy).  Loads are
+  // issued in batches of 8 ahead of the branchy top-k insertion so they overlap.
   float tv[EAGLE_MAX_CHILDREN];
   int ti[EAGLE_MAX_CHILDREN];
   int cnt = 0;
   float lmax = -INFINITY;
   bool bad = false;
-  for (int v = tid; v < V; v += SEL_THREADS) {
-    const float x = z[v];
-    qs[pad32(v)] = x;
-    if (!isfinite(x)) bad = true;
-    lmax = fmaxf(lmax, x);
-    if (greedy) {
-      if (cnt == p.k && !ranks_before(x, v, tv[cnt - 1], ti[cnt - 1])) continue;
-      int pos = cnt < p.k ? cnt : p.k - 1;
-      while (pos > 0 && ranks_before(x, v, tv[pos - 1], ti[pos - 1])) {
-        tv[pos] = tv[pos - 1];
-        ti[pos] = ti[pos - 1];
-        --pos;
+  for (int base = tid; base < V; base += 8 * SEL_THREADS) {
+    float xs[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int v = base + u * SEL_THREADS;
+      xs[u] = v < V ? __ldg(z + v) : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int v = base + u * SEL_THREADS;
+      if (v >= V) break;
+      const float x = xs[u];
+      qs[pad32(v)] = x;
+      if (!isfinite(x)) bad = true;
+      lmax = fmaxf(lmax, x);
+      if (greedy) {
+        if (cnt == p.k && !ranks_before(x, v, tv[cnt - 1], ti[cnt - 1])) continue;
+        int pos = cnt < p.k ? cnt : p.k - 1;
+        while (pos > 0 && ranks_before(x, v, tv[pos - 1], ti[pos - 1])) {
+          tv[pos] = tv[pos - 1];
+          ti[pos] = ti[pos - 1];
+          --pos;
+        }
+        tv[pos] = x;
+        ti[pos] = v;
+        if (cnt < p.k) ++cnt;
       }
-      tv[pos] = x;
-      ti[pos] = v;
-      if (cnt < p.k) ++cnt;
     }
   }
   if (bad) set_status(p.status, EAGLE_ERR_NUMERIC);
