@@ -60,33 +60,73 @@ __device__ __forceinline__ uint64_t row_mask(const AttnParams& p, int b, int nod
 }
 
 // fp32 K/V tiles in dynamic shared memory: [TILE][dh + 4] each; the 4-word
-// row pad keeps lane-per-row float4 reads conflict-free.
-__device__ __forceinline__ void stage_rows(float* dst, int ld, const uint16_t* src_bf16, const float* src_f32,
-                                           size_t row0, size_t row_stride, int nt, int dh) {
-  if (src_f32) {
-    const int pieces = dh / 4;
-    for (int idx = threadIdx.x; idx < nt * pieces; idx += THREADS) {
-      const int r = idx / pieces, c = idx % pieces;
-      *reinterpret_cast<float4*>(dst + r * ld + c * 4) =
-          __ldg(reinterpret_cast<const float4*>(src_f32 + row0 + r * row_stride) + c);
+// row pad keeps lane-per-row float4 reads conflict-free.  Each thread issues
+// all of its loads for the tile (K and V, up to 4 pieces each) before
+// converting and storing, so the tile costs one memory latency, not one per
+// piece.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float* dst) {
+  float4 a, b;
+  a.x = __uint_as_float(w.x << 16); a.y = __uint_as_float(w.x & 0xffff0000u);
+  a.z = __uint_as_float(w.y << 16); a.w = __uint_as_float(w.y & 0xffff0000u);
+  b.x = __uint_as_float(w.z << 16); b.y = __uint_as_float(w.z & 0xffff0000u);
+  b.z = __uint_as_float(w.w << 16); b.w = __uint_as_float(w.w & 0xffff0000u);
+  *reinterpret_cast<float4*>(dst) = a;
+  *reinterpret_cast<float4*>(dst + 4) = b;
+}
+
+__device__ __forceinline__ void stage_kv(float* sk, float* sv, int ld, const uint16_t* kb, const uint16_t* vb,
+                                         const float* kf, const float* vf, size_t row0, size_t row_stride, int nt,
+                                         int dh) {
+  if (kf) {
+    const int pieces = dh / 4, total = nt * pieces;
+    for (int base = threadIdx.x; base < total; base += 2 * THREADS) {
+      float4 kk[2], vv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int idx = base + u * THREADS;
+        if (idx < total) {
+          const int r = idx / pieces, c = idx % pieces;
+          kk[u] = __ldg(reinterpret_cast<const float4*>(kf + row0 + r * row_stride) + c);
+          vv[u] = __ldg(reinterpret_cast<const float4*>(vf + row0 + r * row_stride) + c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int idx = base + u * THREADS;
+        if (idx < total) {
+          const int r = idx / pieces, c = idx % pieces;
+          *reinterpret_cast<float4*>(sk + r * ld + c * 4) = kk[u];
+          *reinterpret_cast<float4*>(sv + r * ld + c * 4) = vv[u];
+        }
+      }
     }
   } else {
-    const int pieces = dh / 8;
-    for (int idx = threadIdx.x; idx < nt * pieces; idx += THREADS) {
-      const int r = idx / pieces, c = idx % pieces;
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(src_bf16 + row0 + r * row_stride) + c);
-      float4 a, b;
-      a.x = __uint_as_float(w.x << 16); a.y = __uint_as_float(w.x & 0xffff0000u);
-      a.z = __uint_as_float(w.y << 16); a.w = __uint_as_float(w.y & 0xffff0000u);
-      b.x = __uint_as_float(w.z << 16); b.y = __uint_as_float(w.z & 0xffff0000u);
-      b.z = __uint_as_float(w.w << 16); b.w = __uint_as_float(w.w & 0xffff0000u);
-      *reinterpret_cast<float4*>(dst + r * ld + c * 8) = a;
-      *reinterpret_cast<float4*>(dst + r * ld + c * 8 + 4) = b;
+    const int pieces = dh / 8, total = nt * pieces;
+    for (int base = threadIdx.x; base < total; base += 2 * THREADS) {
+      uint4 kk[2], vv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int idx = base + u * THREADS;
+        if (idx < total) {
+          const int r = idx / pieces, c = idx % pieces;
+          kk[u] = __ldg(reinterpret_cast<const uint4*>(kb + row0 + r * row_stride) + c);
+          vv[u] = __ldg(reinterpret_cast<const uint4*>(vb + row0 + r * row_stride) + c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int idx = base + u * THREADS;
+        if (idx < total) {
+          const int r = idx / pieces, c = idx % pieces;
+          bf16x8_to_f32(kk[u], sk + r * ld + c * 8);
+          bf16x8_to_f32(vv[u], sv + r * ld + c * 8);
+        }
+      }
     }
   }
 }
 
-__global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams p) {
   extern __shared__ __align__(16) float smem_kv[];
   __shared__ __align__(16) float sq[8][MAX_DH];
   __shared__ int s_last;
@@ -128,12 +168,10 @@ __global__ void __launch_bounds__(THREADS) tree_attn_kernel(const AttnParams p) 
       __syncthreads();
       if (!is_tree) {
         const size_t row0 = ((static_cast<size_t>(b) * p.kv_cap + t0) * p.Hkv + h) * dh;
-        stage_rows(sk, ld, p.kp, nullptr, row0, row_stride, nt, dh);
-        stage_rows(sv, ld, p.vp, nullptr, row0, row_stride, nt, dh);
+        stage_kv(sk, sv, ld, p.kp, p.vp, nullptr, nullptr, row0, row_stride, nt, dh);
       } else {
         const size_t row0 = ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh;
-        stage_rows(sk, ld, p.kt_bf16, p.kt_f32, row0, row_stride, nt, dh);
-        stage_rows(sv, ld, p.vt_bf16, p.vt_f32, row0, row_stride, nt, dh);
+        stage_kv(sk, sv, ld, p.kt_bf16, p.vt_bf16, p.kt_f32, p.vt_f32, row0, row_stride, nt, dh);
       }
       __syncthreads();
 #pragma unroll

@@ -54,7 +54,7 @@ __global__ void prep_fc_kernel(const float* __restrict__ f_last, const float* __
   *reinterpret_cast<uint4*>(bfc + static_cast<size_t>(NP + j) * kp + c0) = lv;
 }
 
-constexpr int SEL_THREADS = 1024;
+constexpr int SEL_THREADS = 512;
 
 // (value desc, id asc) total order: true if a ranks before b.
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
@@ -106,10 +106,12 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelParams p) 
   const int V = p.V;
 
   // pass 1: stage logits, row max, per-thread top-k (greedy).  Loads are
-  // issued in batches of 8 ahead of the branchy top-k insertion so they overlap.
+  // issued in batches of 8 ahead of the insertion; the top-k list lives in
+  // registers (fully unrolled bubble insertion, no dynamic indexing).
   float tv[EAGLE_MAX_CHILDREN];
   int ti[EAGLE_MAX_CHILDREN];
-  int cnt = 0;
+#pragma unroll
+  for (int s = 0; s < EAGLE_MAX_CHILDREN; ++s) { tv[s] = -INFINITY; ti[s] = INT32_MAX; }
   float lmax = -INFINITY;
   bool bad = false;
   for (int base = tid; base < V; base += 8 * SEL_THREADS) {
@@ -127,17 +129,16 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelParams p) 
       qs[pad32(v)] = x;
       if (!isfinite(x)) bad = true;
       lmax = fmaxf(lmax, x);
-      if (greedy) {
-        if (cnt == p.k && !ranks_before(x, v, tv[cnt - 1], ti[cnt - 1])) continue;
-        int pos = cnt < p.k ? cnt : p.k - 1;
-        while (pos > 0 && ranks_before(x, v, tv[pos - 1], ti[pos - 1])) {
-          tv[pos] = tv[pos - 1];
-          ti[pos] = ti[pos - 1];
-          --pos;
+      if (greedy && ranks_before(x, v, tv[EAGLE_MAX_CHILDREN - 1], ti[EAGLE_MAX_CHILDREN - 1])) {
+        float cv = x;
+        int ci = v;
+#pragma unroll
+        for (int s = 0; s < EAGLE_MAX_CHILDREN; ++s) {
+          if (ranks_before(cv, ci, tv[s], ti[s])) {
+            const float tf = tv[s]; tv[s] = cv; cv = tf;
+            const int tn = ti[s]; ti[s] = ci; ci = tn;
+          }
         }
-        tv[pos] = x;
-        ti[pos] = v;
-        if (cnt < p.k) ++cnt;
       }
     }
   }
@@ -164,8 +165,11 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelParams p) 
     int ptr = 0;
     const int lane = tid & 31, wid = tid >> 5;
     for (int r = 0; r < p.k; ++r) {
-      float bv = ptr < cnt ? tv[ptr] : -INFINITY;
-      int bi = ptr < cnt ? ti[ptr] : INT32_MAX;
+      float bv = -INFINITY;
+      int bi = INT32_MAX;
+#pragma unroll
+      for (int s = 0; s < EAGLE_MAX_CHILDREN; ++s)
+        if (s == ptr) { bv = tv[s]; bi = ti[s]; }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -188,7 +192,14 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelParams p) 
       }
       __syncthreads();
       const int win = red_i[0];
-      if (ptr < cnt && ti[ptr] == win) ++ptr;
+      if (bi != INT32_MAX && win == bi && ptr < EAGLE_MAX_CHILDREN) {
+        // this thread's candidate won (ids are unique across threads)
+        bool mine = false;
+#pragma unroll
+        for (int s = 0; s < EAGLE_MAX_CHILDREN; ++s)
+          if (s == ptr) mine = ti[s] == win;
+        if (mine) ++ptr;
+      }
       if (tid == 0) {
         const bool ok = win != INT32_MAX && win < V;
         ct[r] = ok ? win : -1;
