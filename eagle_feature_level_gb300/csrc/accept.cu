@@ -55,8 +55,9 @@ __global__ void __launch_bounds__(SM_THREADS)
   if (lane == 0) { red_f[wid] = bv; red_i[wid] = bi; }
   __syncthreads();
   if (wid == 0) {
-    bv = red_f[lane];
-    bi = red_i[lane];
+    const int nw = SM_THREADS / 32;
+    bv = lane < nw ? red_f[lane] : -INFINITY;
+    bi = lane < nw ? red_i[lane] : INT32_MAX;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);

@@ -9,6 +9,8 @@
 // writes (max, sum, unnormalised output) partials; the last CTA of a
 // (request, kv head) merges them in split order.  The ancestor mask of each
 // query row lives in a register (one 64-bit word) and is tested per tree key.
+#include <algorithm>
+
 #include "internal.h"
 #include "sm100.cuh"
 
@@ -17,13 +19,18 @@ namespace {
 
 constexpr int TILE = 64;          // KV rows per shared-memory tile
 constexpr int THREADS = 256;
+constexpr int WARPS = THREADS / 32;
 constexpr int MAX_DH = 128;
+constexpr int RW = 8;             // query rows a warp owns in one pass
+constexpr int ROWS_PASS = WARPS * RW;
+constexpr int PF = TILE * (MAX_DH / 8) / THREADS;   // 16-byte prefix pieces per thread per K (or V) tile
 
 struct AttnParams {
   int mode;                       // 0 draft, 1 verify
   int B, Hq, Hkv, dh, G;
-  int n_splits, chunk;            // prefix splits and rows per split
+  int n_splits, chunk;            // prefix splits and rows per split (a multiple of TILE)
   int rows_cap;                   // query nodes per request (draft: rows per request; verify: tree stride)
+  int rows_pass;                  // query rows staged per pass: min(ROWS_PASS, rows_cap * G)
   const float* q_f32;             // draft: [n][Hq*dh] fp32
   const uint16_t* q_bf16;         // verify: [B][S][Hq][dh] bf16
   const uint16_t* kp;             // prefix KV [B][cap][Hkv][dh] bf16
@@ -59,11 +66,6 @@ __device__ __forceinline__ uint64_t row_mask(const AttnParams& p, int b, int nod
   return p.anc[static_cast<size_t>(b) * p.tree_cap + node];
 }
 
-// fp32 K/V tiles in dynamic shared memory: [TILE][dh + 4] each; the 4-word
-// row pad keeps lane-per-row float4 reads conflict-free.  Each thread issues
-// all of its loads for the tile (K and V, up to 4 pieces each) before
-// converting and storing, so the tile costs one memory latency, not one per
-// piece.
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float* dst) {
   float4 a, b;
   a.x = __uint_as_float(w.x << 16); a.y = __uint_as_float(w.x & 0xffff0000u);
@@ -74,62 +76,86 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float* dst) {
   *reinterpret_cast<float4*>(dst + 4) = b;
 }
 
-__device__ __forceinline__ void stage_kv(float* sk, float* sv, int ld, const uint16_t* kb, const uint16_t* vb,
-                                         const float* kf, const float* vf, size_t row0, size_t row_stride, int nt,
-                                         int dh) {
-  if (kf) {
-    const int pieces = dh / 4, total = nt * pieces;
-    for (int base = threadIdx.x; base < total; base += 2 * THREADS) {
-      float4 kk[2], vv[2];
+// A bf16 prefix tile in flight: piece i of this thread is row (tid + i*THREADS)
+// / (dh/8), 8 columns.  Loads are issued for the next tile before the current
+// one is consumed; rows past the tile's end stay zero.
+struct PrefixTile {
+  uint4 k[PF], v[PF];
+};
+
+__device__ __forceinline__ void prefix_load(PrefixTile& t, const uint16_t* kb, const uint16_t* vb, size_t row0,
+                                            size_t row_stride, int nt, int dh) {
+  const int pieces = dh >> 3;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int idx = base + u * THREADS;
-        if (idx < total) {
-          const int r = idx / pieces, c = idx % pieces;
-          kk[u] = __ldg(reinterpret_cast<const float4*>(kf + row0 + r * row_stride) + c);
-          vv[u] = __ldg(reinterpret_cast<const float4*>(vf + row0 + r * row_stride) + c);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int idx = base + u * THREADS;
-        if (idx < total) {
-          const int r = idx / pieces, c = idx % pieces;
-          *reinterpret_cast<float4*>(sk + r * ld + c * 4) = kk[u];
-          *reinterpret_cast<float4*>(sv + r * ld + c * 4) = vv[u];
-        }
-      }
-    }
-  } else {
-    const int pieces = dh / 8, total = nt * pieces;
-    for (int base = threadIdx.x; base < total; base += 2 * THREADS) {
-      uint4 kk[2], vv[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int idx = base + u * THREADS;
-        if (idx < total) {
-          const int r = idx / pieces, c = idx % pieces;
-          kk[u] = __ldg(reinterpret_cast<const uint4*>(kb + row0 + r * row_stride) + c);
-          vv[u] = __ldg(reinterpret_cast<const uint4*>(vb + row0 + r * row_stride) + c);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int idx = base + u * THREADS;
-        if (idx < total) {
-          const int r = idx / pieces, c = idx % pieces;
-          bf16x8_to_f32(kk[u], sk + r * ld + c * 8);
-          bf16x8_to_f32(vv[u], sv + r * ld + c * 8);
-        }
-      }
+  for (int i = 0; i < PF; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    const int r = idx / pieces, c = idx - r * pieces;
+    if (r < nt) {
+      t.k[i] = __ldg(reinterpret_cast<const uint4*>(kb + row0 + r * row_stride) + c);
+      t.v[i] = __ldg(reinterpret_cast<const uint4*>(vb + row0 + r * row_stride) + c);
+    } else {
+      t.k[i] = make_uint4(0u, 0u, 0u, 0u);
+      t.v[i] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
 }
 
+__device__ __forceinline__ void prefix_store(const PrefixTile& t, float* sk, float* sv, int ld, int dh) {
+  const int pieces = dh >> 3;
+#pragma unroll
+  for (int i = 0; i < PF; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    const int r = idx / pieces, c = idx - r * pieces;
+    if (r < TILE) {
+      bf16x8_to_f32(t.k[i], sk + r * ld + c * 8);
+      bf16x8_to_f32(t.v[i], sv + r * ld + c * 8);
+    }
+  }
+}
+
+// The tree part (at most one tile): fp32 (draft) or bf16 (verify) rows, zero past nt.
+__device__ __forceinline__ void tree_stage(const AttnParams& p, float* sk, float* sv, int ld, size_t row0,
+                                           size_t row_stride, int nt) {
+  const int dh = p.dh;
+  if (p.mode == 0) {
+    const int pieces = dh >> 2;
+    for (int idx = threadIdx.x; idx < TILE * pieces; idx += THREADS) {
+      const int r = idx / pieces, c = idx - r * pieces;
+      float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
+      if (r < nt) {
+        kk = __ldg(reinterpret_cast<const float4*>(p.kt_f32 + row0 + r * row_stride) + c);
+        vv = __ldg(reinterpret_cast<const float4*>(p.vt_f32 + row0 + r * row_stride) + c);
+      }
+      *reinterpret_cast<float4*>(sk + r * ld + c * 4) = kk;
+      *reinterpret_cast<float4*>(sv + r * ld + c * 4) = vv;
+    }
+  } else {
+    const int pieces = dh >> 3;
+    for (int idx = threadIdx.x; idx < TILE * pieces; idx += THREADS) {
+      const int r = idx / pieces, c = idx - r * pieces;
+      uint4 kk = make_uint4(0u, 0u, 0u, 0u), vv = kk;
+      if (r < nt) {
+        kk = __ldg(reinterpret_cast<const uint4*>(p.kt_bf16 + row0 + r * row_stride) + c);
+        vv = __ldg(reinterpret_cast<const uint4*>(p.vt_bf16 + row0 + r * row_stride) + c);
+      }
+      bf16x8_to_f32(kk, sk + r * ld + c * 8);
+      bf16x8_to_f32(vv, sv + r * ld + c * 8);
+    }
+  }
+}
+
+// Dynamic shared memory: K tile, V tile ([TILE][dh+4] fp32 each; the 4-word
+// pad makes lane-per-row float4 reads conflict-free), the pass's query rows
+// [rows_pass][dh] and each warp's probabilities [WARPS][RW][TILE].
+//
+// Warp w owns query rows w + 8 i of the pass: it scores them against the tile
+// (lane = keys lane and lane + 32), runs the online softmax and accumulates
+// P V for them (lane = 4 output columns), so after the tile is staged no
+// further block-wide barrier is needed.
 __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams p) {
-  extern __shared__ __align__(16) float smem_kv[];
-  __shared__ __align__(16) float sq[8][MAX_DH];
+  extern __shared__ __align__(16) float smem_attn[];
   __shared__ int s_last;
+  __shared__ uint64_t s_mask[ROWS_PASS];     // ancestor masks of the tree part's rows
 
   const int split = blockIdx.x;              // split == n_splits: the tree part
   const int pair = blockIdx.y;
@@ -137,8 +163,10 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int dh = p.dh;
   const int ld = dh + 4;
-  float* sk = smem_kv;
-  float* sv = smem_kv + TILE * ld;
+  float* sk = smem_attn;
+  float* sv = sk + TILE * ld;
+  float* sq = sv + TILE * ld;
+  float* sp = sq + p.rows_pass * dh + (warp * RW) * TILE;
   const int nodes = n_nodes(p, b);
   const int R = nodes * p.G;
   const bool is_tree = split == p.n_splits;
@@ -152,97 +180,136 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams 
   }
   const int rec = dh + 2;
   const size_t row_stride = static_cast<size_t>(p.Hkv) * dh;
+  const int dcol = 4 * lane;                 // this lane's output columns
+  const bool has_cols = dcol < dh;
 
-  // Each warp owns query rows r = r0 + warp + 8 i (i < 8); running state in registers.
-  for (int r0 = 0; r0 < R; r0 += 64) {
-    float m_run[8], l_run[8], acc[8][4];
+  for (int r0 = 0; r0 < R; r0 += p.rows_pass) {
+    const int rp = min(p.rows_pass, R - r0);
+    // rows of this warp in the pass: w, w + 8, ... < rp
+    const int nr = rp > warp ? (rp - warp + WARPS - 1) / WARPS : 0;
+    __syncthreads();                         // previous pass done with sq
+    for (int idx = threadIdx.x; idx < rp * (dh >> 2); idx += THREADS) {
+      const int rr = idx / (dh >> 2), c = idx - rr * (dh >> 2);
+      const int r = r0 + rr, node = r / p.G, hq = h * p.G + r % p.G;
+      const size_t qo = q_index(p, b, node, hq) + 4 * c;
+      float4 v;
+      if (p.mode == 0) {
+        v = *reinterpret_cast<const float4*>(p.q_f32 + qo);
+      } else {
+        const uint2 w = *reinterpret_cast<const uint2*>(p.q_bf16 + qo);
+        v.x = __uint_as_float(w.x << 16); v.y = __uint_as_float(w.x & 0xffff0000u);
+        v.z = __uint_as_float(w.y << 16); v.w = __uint_as_float(w.y & 0xffff0000u);
+      }
+      *reinterpret_cast<float4*>(sq + rr * dh + 4 * c) = v;
+    }
+    if (is_tree && lane < RW && lane < nr)
+      s_mask[warp * RW + lane] = row_mask(p, b, (r0 + warp + WARPS * lane) / p.G);
+    float m_run[RW], l_run[RW], acc[RW][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < RW; ++i) {
       m_run[i] = -INFINITY;
       l_run[i] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
     }
+
+    PrefixTile pre;
+    if (!is_tree && lo < hi)
+      prefix_load(pre, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + lo) * p.Hkv + h) * dh, row_stride,
+                  min(TILE, hi - lo), dh);
     for (int t0 = lo; t0 < hi; t0 += TILE) {
       const int nt = min(TILE, hi - t0);
-      __syncthreads();
+      __syncthreads();                       // all warps done with the previous tile
       if (!is_tree) {
-        const size_t row0 = ((static_cast<size_t>(b) * p.kv_cap + t0) * p.Hkv + h) * dh;
-        stage_kv(sk, sv, ld, p.kp, p.vp, nullptr, nullptr, row0, row_stride, nt, dh);
+        prefix_store(pre, sk, sv, ld, dh);
+        if (t0 + TILE < hi)                  // next tile's loads fly while this one is consumed
+          prefix_load(pre, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + t0 + TILE) * p.Hkv + h) * dh,
+                      row_stride, min(TILE, hi - t0 - TILE), dh);
       } else {
-        const size_t row0 = ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh;
-        stage_kv(sk, sv, ld, p.kt_bf16, p.vt_bf16, p.kt_f32, p.vt_f32, row0, row_stride, nt, dh);
+        tree_stage(p, sk, sv, ld, ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh, row_stride, nt);
       }
       __syncthreads();
+      if (nr == 0) continue;
+
+      // scores of keys lane and lane + 32 for each owned row
+      float s0[RW], s1[RW];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = r0 + warp + 8 * i;
-        if (r >= R) break;
-        const int node = r / p.G, hq = h * p.G + r % p.G;
-        const size_t qo = q_index(p, b, node, hq);
-        for (int d = lane; d < dh; d += 32)
-          sq[warp][d] = p.mode == 0 ? p.q_f32[qo + d] : bf16_to_f32(p.q_bf16[qo + d]);
-        __syncwarp();
-        const uint64_t mask = is_tree ? row_mask(p, b, node) : ~0ull;
-        float sc[2];
+      for (int i = 0; i < RW; ++i) { s0[i] = 0.f; s1[i] = 0.f; }
+      const float* k0 = sk + lane * ld;
+      const float* k1 = sk + (lane + 32) * ld;
+      for (int d = 0; d < dh; d += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(k0 + d);
+        const float4 c = *reinterpret_cast<const float4*>(k1 + d);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int j = lane + 32 * half;
-          float s = -INFINITY;
-          const bool vis = j < nt && (!is_tree || ((mask >> (t0 + j)) & 1ull));
-          if (vis) {
-            const float* kr = sk + j * ld;
-            float dot = 0.f;
-            for (int d0 = 0; d0 < dh; d0 += 4) {
-              const float4 kv = *reinterpret_cast<const float4*>(kr + d0);
-              const float4 qv = *reinterpret_cast<const float4*>(&sq[warp][d0]);
-              dot = fmaf(qv.x, kv.x, dot);
-              dot = fmaf(qv.y, kv.y, dot);
-              dot = fmaf(qv.z, kv.z, dot);
-              dot = fmaf(qv.w, kv.w, dot);
-            }
-            s = dot * p.scale;
-          }
-          sc[half] = s;
-        }
-        const float tmax = warp_max(fmaxf(sc[0], sc[1]));
-        __syncwarp();
-        if (tmax == -INFINITY) continue;
-        const float m_new = fmaxf(m_run[i], tmax);
-        const float corr = __expf(m_run[i] - m_new);
-        const float p0 = sc[0] == -INFINITY ? 0.f : __expf(sc[0] - m_new);
-        const float p1 = sc[1] == -INFINITY ? 0.f : __expf(sc[1] - m_new);
-        l_run[i] = l_run[i] * corr + warp_sum(p0 + p1);
-        m_run[i] = m_new;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[i][c] *= corr;
-        for (int j = 0; j < nt; ++j) {
-          const float pj = __shfl_sync(0xffffffffu, j < 32 ? p0 : p1, j & 31);
-          if (pj == 0.f) continue;
-          const float* vr = sv + j * ld;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int d = lane + 32 * c;
-            if (d < dh) acc[i][c] = fmaf(pj, vr[d], acc[i][c]);
+        for (int i = 0; i < RW; ++i) {
+          if (i < nr) {
+            const float4 q = *reinterpret_cast<const float4*>(sq + (warp + WARPS * i) * dh + d);
+            s0[i] += fmaf(q.x, a.x, q.y * a.y) + fmaf(q.z, a.z, q.w * a.w);
+            s1[i] += fmaf(q.x, c.x, q.y * c.y) + fmaf(q.z, c.z, q.w * c.w);
           }
         }
       }
+      // online softmax per row; probabilities to this warp's shared rows
+#pragma unroll
+      for (int i = 0; i < RW; ++i) {
+        if (i < nr) {
+          // tree keys: one tile (t0 == 0), bit j of the row's ancestor mask
+          const uint64_t mask = is_tree ? s_mask[warp * RW + i] : ~0ull;
+          const bool v0 = lane < nt && ((mask >> lane) & 1ull);
+          const bool v1 = lane + 32 < nt && ((mask >> (lane + 32)) & 1ull);
+          const float a = v0 ? s0[i] * p.scale : -INFINITY;
+          const float c = v1 ? s1[i] * p.scale : -INFINITY;
+          const float m_new = fmaxf(m_run[i], warp_max(fmaxf(a, c)));
+          float p0 = 0.f, p1 = 0.f, corr = 1.f;
+          if (m_new != -INFINITY) {
+            p0 = __expf(a - m_new);
+            p1 = __expf(c - m_new);
+            corr = __expf(m_run[i] - m_new);
+          }
+          l_run[i] = l_run[i] * corr + warp_sum(p0 + p1);
+          m_run[i] = m_new;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) acc[i][c4] *= corr;
+          sp[i * TILE + lane] = p0;
+          sp[i * TILE + lane + 32] = p1;
+        }
+      }
+      __syncwarp();
+      // acc += P V over the tile, 4 keys per step (V rows past nt are zero)
+      if (has_cols) {
+        for (int j = 0; j < nt; j += 4) {
+          float4 vv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) vv[u] = *reinterpret_cast<const float4*>(sv + (j + u) * ld + dcol);
+#pragma unroll
+          for (int i = 0; i < RW; ++i) {
+            if (i < nr) {
+              const float4 pj = *reinterpret_cast<const float4*>(sp + i * TILE + j);
+              acc[i][0] = fmaf(pj.x, vv[0].x, fmaf(pj.y, vv[1].x, fmaf(pj.z, vv[2].x, fmaf(pj.w, vv[3].x, acc[i][0]))));
+              acc[i][1] = fmaf(pj.x, vv[0].y, fmaf(pj.y, vv[1].y, fmaf(pj.z, vv[2].y, fmaf(pj.w, vv[3].y, acc[i][1]))));
+              acc[i][2] = fmaf(pj.x, vv[0].z, fmaf(pj.y, vv[1].z, fmaf(pj.z, vv[2].z, fmaf(pj.w, vv[3].z, acc[i][2]))));
+              acc[i][3] = fmaf(pj.x, vv[0].w, fmaf(pj.y, vv[1].w, fmaf(pj.z, vv[2].w, fmaf(pj.w, vv[3].w, acc[i][3]))));
+            }
+          }
+        }
+      }
+      __syncwarp();
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = r0 + warp + 8 * i;
-      if (r >= R) break;
-      const int node = r / p.G, hq = h * p.G + r % p.G;
-      const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
-      float* dst = p.part + (qi * (p.n_splits + 1) + split) * rec;
-      if (lane == 0) {
-        dst[0] = m_run[i];
-        dst[1] = l_run[i];
-      }
+    for (int i = 0; i < RW; ++i) {
+      if (i < nr) {
+        const int r = r0 + warp + WARPS * i;
+        const int node = r / p.G, hq = h * p.G + r % p.G;
+        const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
+        float* dst = p.part + (qi * (p.n_splits + 1) + split) * rec;
+        if (lane == 0) {
+          dst[0] = m_run[i];
+          dst[1] = l_run[i];
+        }
+        if (has_cols) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int d = lane + 32 * c;
-        if (d < dh) dst[2 + d] = acc[i][c];
+          for (int c = 0; c < 4; ++c) dst[2 + dcol + c] = acc[i][c];
+        }
       }
     }
   }
@@ -311,23 +378,28 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams 
 }  // namespace
 
 int attn_splits(const eagle_ctx* ctx, int pairs, int cap) {
+  const int tiles = ceil_div(cap < 1 ? 1 : cap, TILE);
   int want = ceil_div(2 * ctx->sm_count, pairs < 1 ? 1 : pairs);
-  const int by_len = ceil_div(cap < 1 ? 1 : cap, TILE);
-  if (want > by_len) want = by_len;
-  if (want < 1) want = 1;
+  if (want > tiles) want = tiles;
   if (want > 31) want = 31;        // n_splits + 1 records fit one warp in the merge
-  return want;
+  if (want < 1) want = 1;
+  const int per = ceil_div(tiles, want);
+  return ceil_div(tiles, per);     // every split non-empty at full length
 }
 
 static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
   p.n_splits = attn_splits(ctx, p.B * p.Hkv, p.kv_cap);
-  p.chunk = ceil_div(ceil_div(p.kv_cap, p.n_splits), TILE) * TILE;
+  p.chunk = ceil_div(ceil_div(p.kv_cap, TILE), p.n_splits) * TILE;
+  p.rows_pass = std::min(ROWS_PASS, p.rows_cap * p.G);
   dim3 grid(p.n_splits + 1, p.B * p.Hkv);
-  const size_t smem = static_cast<size_t>(2) * TILE * (p.dh + 4) * sizeof(float);
+  const size_t smem = (static_cast<size_t>(2) * TILE * (p.dh + 4) + static_cast<size_t>(p.rows_pass) * p.dh +
+                       static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
   static bool attr_set = false;
   if (!attr_set) {
+    const size_t most = (static_cast<size_t>(2) * TILE * (MAX_DH + 4) + static_cast<size_t>(ROWS_PASS) * MAX_DH +
+                         static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(2 * TILE * (MAX_DH + 4) * sizeof(float)));
+                                         static_cast<int>(most));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }

@@ -54,17 +54,73 @@ __global__ void prep_fc_kernel(const float* __restrict__ f_last, const float* __
   *reinterpret_cast<uint4*>(bfc + static_cast<size_t>(NP + j) * kp + c0) = lv;
 }
 
-constexpr int SEL_THREADS = 512;
+// select: a cluster of SEL_CL CTAs per row, each CTA one contiguous
+// SEL_THREADS * SEL_PER slice of the vocabulary, SEL_PER consecutive logits
+// per thread held in registers.  Row max, sum, top-k candidates and sampling
+// draws are exchanged through distributed shared memory; every CTA reduces
+// the exchanged partials in rank order, so all see the same max and sum.
+constexpr int SEL_CL = 8;
+constexpr int SEL_THREADS = 256;
+constexpr int SEL_WARPS = SEL_THREADS / 32;
+constexpr int SEL_PER = 16;
+constexpr int SEL_SLICE = SEL_THREADS * SEL_PER;
+static_assert(SEL_CL * SEL_SLICE >= EAGLE_MAX_VOCAB, "one cluster covers the largest vocabulary");
+static_assert(SEL_CL * EAGLE_MAX_CHILDREN <= 128 && SEL_WARPS * EAGLE_MAX_CHILDREN <= 128,
+              "candidate lists fit four per lane");
 
 // (value desc, id asc) total order: true if a ranks before b.
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
-// Shared-memory slot of vocabulary entry v: one pad word per 32 entries, so
-// both strided (v = tid + i * 1024) and per-thread contiguous chunks of 32
-// entries hit 32 distinct banks.
-__device__ __forceinline__ int pad32(int v) { return v + (v >> 5); }
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (ranks_before(ov, oi, v, i)) { v = ov; i = oi; }
+  }
+}
+
+// One warp: the k best of n <= 128 candidates (z, id, q), in order, to out.
+// Lane l holds candidates l, l + 32, l + 64, l + 96.
+__device__ __forceinline__ void warp_merge_topk(const float* cz, const int* ci, const float* cq, int n, int k,
+                                                float* oz, int* oi, float* oq) {
+  const int lane = threadIdx.x & 31;
+  float z[4];
+  int id[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int c = lane + 32 * u;
+    z[u] = c < n ? cz[c] : -INFINITY;
+    id[u] = c < n ? ci[c] : INT32_MAX;
+  }
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = INT32_MAX, bs = -1;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (ranks_before(z[u], id[u], bv, bi)) { bv = z[u]; bi = id[u]; bs = u; }
+    float wv = bv;
+    int wi = bi;
+    warp_argmax(wv, wi);
+    if (bs >= 0 && wi == bi && bi != INT32_MAX) {   // this lane holds the winner
+      const int c = lane + 32 * bs;
+      if (oz) oz[r] = z[bs];
+      oi[r] = bi;
+      oq[r] = cq[c];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (u == bs) { z[u] = -INFINITY; id[u] = INT32_MAX; }
+    }
+    if (wi == INT32_MAX && lane == 0) {               // fewer than k candidates
+      if (oz) oz[r] = -INFINITY;
+      oi[r] = INT32_MAX;
+      oq[r] = 0.f;
+    }
+  }
+  __syncwarp();
+}
 
 struct SelParams {
   const float* logits;     // [B][E][V]
@@ -78,198 +134,241 @@ struct SelParams {
   int* status;
 };
 
-// One CTA per draft row.  Logits are read once (coalesced) into shared
-// memory; max, exp, sum and q all work there; q is written back coalesced.
-__global__ void __launch_bounds__(SEL_THREADS) select_kernel(const SelParams p) {
-  extern __shared__ float qs[];                  // [pad32(V)]
-  __shared__ float red_f[32];
-  __shared__ int red_i[32];
-  __shared__ uint64_t tprefix[SEL_THREADS];      // inclusive prefix of per-thread weight sums
-  __shared__ int s_taken[EAGLE_MAX_CHILDREN];
-  __shared__ uint64_t s_wtaken[EAGLE_MAX_CHILDREN];
+__global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) select_kernel(const SelParams p) {
+  __shared__ float s_red[SEL_WARPS];
+  __shared__ float s_cmax[SEL_CL], s_csum[SEL_CL];         // per-rank partials (pushed)
+  __shared__ uint64_t s_ctot[SEL_CL];
+  __shared__ uint64_t s_wscan[SEL_WARPS];
+  __shared__ float s_wz[SEL_WARPS * EAGLE_MAX_CHILDREN], s_wq[SEL_WARPS * EAGLE_MAX_CHILDREN];
+  __shared__ int s_wi[SEL_WARPS * EAGLE_MAX_CHILDREN];
+  __shared__ float s_cz[SEL_CL * EAGLE_MAX_CHILDREN], s_cq[SEL_CL * EAGLE_MAX_CHILDREN];  // rank 0: per-CTA lists
+  __shared__ int s_ci[SEL_CL * EAGLE_MAX_CHILDREN];
+  __shared__ int s_pick[EAGLE_MAX_CHILDREN];                // sampling: drawn token of each round (pushed)
+  __shared__ uint64_t s_pw[EAGLE_MAX_CHILDREN];
+  __shared__ float s_pq[EAGLE_MAX_CHILDREN];
 
-  const int j = blockIdx.x;
-  const int b = j / p.rpr, e = p.e0 + j % p.rpr;
+  const int row = blockIdx.x / SEL_CL;
+  const uint32_t rank = sm100::cluster_rank();
+  const int b = row / p.rpr, e = p.e0 + row % p.rpr;
   const size_t node = static_cast<size_t>(b) * p.E + e;
-  const float* z = p.logits + node * p.V;
-  float* q = p.probs + node * p.V;
   int32_t* ct = p.child_tok + node * p.K;
   float* cp = p.child_prob + node * p.K;
-  const int tid = threadIdx.x;
-  if (p.token[node] < 0) {
-    if (tid < p.K) { ct[tid] = -1; cp[tid] = 0.f; }
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (p.token[node] < 0) {                   // uniform over the cluster: no barrier is reached
+    if (rank == 0 && tid < p.K) { ct[tid] = -1; cp[tid] = 0.f; }
     return;
   }
   const float T = p.temperature[b];
   const bool greedy = !(T > 0.f);
   const float inv_t = greedy ? 1.0f : 1.0f / T;
-  const int V = p.V;
+  const int V = p.V, k = p.k;
+  const int v0 = static_cast<int>(rank) * SEL_SLICE + tid * SEL_PER;
+  const float* zrow = p.logits + node * V;
+  float* qrow = p.probs + node * V;
+  const bool vec = (V & 3) == 0 && v0 + SEL_PER <= V;
+  if (tid < EAGLE_MAX_CHILDREN) s_pick[tid] = -1;
 
-  // pass 1: stage logits, row max, per-thread top-k (greedy).  Loads are
-  // issued in batches of 8 ahead of the insertion; the top-k list lives in
-  // registers (fully unrolled bubble insertion, no dynamic indexing).
-  float tv[EAGLE_MAX_CHILDREN];
-  int ti[EAGLE_MAX_CHILDREN];
+  // logits, finiteness, slice max
+  float x[SEL_PER];
+  if (vec) {
 #pragma unroll
-  for (int s = 0; s < EAGLE_MAX_CHILDREN; ++s) { tv[s] = -INFINITY; ti[s] = INT32_MAX; }
+    for (int u = 0; u < SEL_PER / 4; ++u) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(zrow + v0) + u);
+      x[4 * u] = f.x; x[4 * u + 1] = f.y; x[4 * u + 2] = f.z; x[4 * u + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < SEL_PER; ++u) x[u] = v0 + u < V ? __ldg(zrow + v0 + u) : -INFINITY;
+  }
   float lmax = -INFINITY;
   bool bad = false;
-  for (int base = tid; base < V; base += 8 * SEL_THREADS) {
-    float xs[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int v = base + u * SEL_THREADS;
-      xs[u] = v < V ? __ldg(z + v) : -INFINITY;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int v = base + u * SEL_THREADS;
-      if (v >= V) break;
-      const float x = xs[u];
-      qs[pad32(v)] = x;
-      if (!isfinite(x)) bad = true;
-      lmax = fmaxf(lmax, x);
-      if (greedy && ranks_before(x, v, tv[EAGLE_MAX_CHILDREN - 1], ti[EAGLE_MAX_CHILDREN - 1])) {
-        float cv = x;
-        int ci = v;
-#pragma unroll
-        for (int s = 0; s < EAGLE_MAX_CHILDREN; ++s) {
-          if (ranks_before(cv, ci, tv[s], ti[s])) {
-            const float tf = tv[s]; tv[s] = cv; cv = tf;
-            const int tn = ti[s]; ti[s] = ci; ci = tn;
-          }
-        }
-      }
+  for (int u = 0; u < SEL_PER; ++u) {
+    if (v0 + u < V) {
+      bad |= !isfinite(x[u]);
+      lmax = fmaxf(lmax, x[u]);
     }
   }
   if (bad) set_status(p.status, EAGLE_ERR_NUMERIC);
-  const float m = block_max(lmax, red_f);
-  // pass 2: exponentials and their sum (fixed-order reduction)
-  float lsum = 0.f;
-  for (int v = tid; v < V; v += SEL_THREADS) {
-    const float ex = expf((qs[pad32(v)] - m) * inv_t);
-    qs[pad32(v)] = ex;
-    lsum += ex;
-  }
-  const float invS = 1.0f / block_sum(lsum, red_f);
-  // pass 3: q, in shared memory and to the output row
-  for (int v = tid; v < V; v += SEL_THREADS) {
-    const float qv = qs[pad32(v)] * invS;
-    qs[pad32(v)] = qv;
-    q[v] = qv;
-  }
+  lmax = warp_max(lmax);
+  if (lane == 0) s_red[wid] = lmax;
   __syncthreads();
+  if (tid < SEL_CL) {                        // push this CTA's max to every rank
+    float m = s_red[0];
+    for (int w = 1; w < SEL_WARPS; ++w) m = fmaxf(m, s_red[w]);
+    sm100::dsmem_st_f32(sm100::dsmem_addr(&s_cmax[rank], tid), m);
+  }
+  // The first cluster barrier also orders every later remote write after
+  // every CTA of the cluster has started.
+  sm100::cluster_sync();
+  float m = s_cmax[0];
+  for (int c = 1; c < SEL_CL; ++c) m = fmaxf(m, s_cmax[c]);
+
+  // exponentials, slice sum in a fixed order, cluster sum in rank order
+  float ex[SEL_PER];
+  float lsum = 0.f;
+#pragma unroll
+  for (int u = 0; u < SEL_PER; ++u) {
+    ex[u] = v0 + u < V ? expf((x[u] - m) * inv_t) : 0.f;
+    lsum += ex[u];
+  }
+  lsum = warp_sum(lsum);
+  __syncthreads();                           // s_red reuse
+  if (lane == 0) s_red[wid] = lsum;
+  __syncthreads();
+  if (tid < SEL_CL) {
+    float sum = 0.f;
+    for (int w = 0; w < SEL_WARPS; ++w) sum += s_red[w];
+    sm100::dsmem_st_f32(sm100::dsmem_addr(&s_csum[rank], tid), sum);
+  }
+  sm100::cluster_sync();
+  float S = 0.f;
+  for (int c = 0; c < SEL_CL; ++c) S += s_csum[c];
+  const float invS = 1.0f / S;
+  float q[SEL_PER];
+#pragma unroll
+  for (int u = 0; u < SEL_PER; ++u) q[u] = ex[u] * invS;
+  if (vec) {
+#pragma unroll
+    for (int u = 0; u < SEL_PER / 4; ++u)
+      reinterpret_cast<float4*>(qrow + v0)[u] = make_float4(q[4 * u], q[4 * u + 1], q[4 * u + 2], q[4 * u + 3]);
+  } else {
+#pragma unroll
+    for (int u = 0; u < SEL_PER; ++u)
+      if (v0 + u < V) qrow[v0 + u] = q[u];
+  }
 
   if (greedy) {
-    // k rounds of a block-wide argmax over each thread's next candidate
-    int ptr = 0;
-    const int lane = tid & 31, wid = tid >> 5;
-    for (int r = 0; r < p.k; ++r) {
-      float bv = -INFINITY;
-      int bi = INT32_MAX;
+    // each warp's k best (logit desc, id asc), then the CTA's, then rank 0 merges the cluster's
+    uint32_t taken = 0;
+    float bv = -INFINITY;
+    int bi = INT32_MAX, bs = -1;
 #pragma unroll
-      for (int s = 0; s < EAGLE_MAX_CHILDREN; ++s)
-        if (s == ptr) { bv = tv[s]; bi = ti[s]; }
+    for (int u = 0; u < SEL_PER; ++u)
+      if (v0 + u < V && ranks_before(x[u], v0 + u, bv, bi)) { bv = x[u]; bi = v0 + u; bs = u; }
+    for (int r = 0; r < k; ++r) {
+      float wv = bv;
+      int wi = bi;
+      warp_argmax(wv, wi);
+      if (bs >= 0 && wi == bi && bi != INT32_MAX) {
+        float qv = 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        for (int u = 0; u < SEL_PER; ++u)
+          if (u == bs) qv = q[u];
+        s_wz[wid * k + r] = bv;
+        s_wi[wid * k + r] = bi;
+        s_wq[wid * k + r] = qv;
+        taken |= 1u << bs;
+        bv = -INFINITY; bi = INT32_MAX; bs = -1;
+#pragma unroll
+        for (int u = 0; u < SEL_PER; ++u)
+          if (!((taken >> u) & 1u) && v0 + u < V && ranks_before(x[u], v0 + u, bv, bi)) {
+            bv = x[u]; bi = v0 + u; bs = u;
+          }
       }
-      __syncthreads();
-      if (lane == 0) { red_f[wid] = bv; red_i[wid] = bi; }
-      __syncthreads();
-      if (wid == 0) {
-        bv = red_f[lane];
-        bi = red_i[lane];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-          if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-        }
-        if (lane == 0) red_i[0] = bi;
-      }
-      __syncthreads();
-      const int win = red_i[0];
-      if (bi != INT32_MAX && win == bi && ptr < EAGLE_MAX_CHILDREN) {
-        // this thread's candidate won (ids are unique across threads)
-        bool mine = false;
-#pragma unroll
-        for (int s = 0; s < EAGLE_MAX_CHILDREN; ++s)
-          if (s == ptr) mine = ti[s] == win;
-        if (mine) ++ptr;
-      }
-      if (tid == 0) {
-        const bool ok = win != INT32_MAX && win < V;
-        ct[r] = ok ? win : -1;
-        cp[r] = ok ? qs[pad32(win)] : 0.f;
+      if (wi == INT32_MAX && lane == 0) {
+        s_wz[wid * k + r] = -INFINITY;
+        s_wi[wid * k + r] = INT32_MAX;
+        s_wq[wid * k + r] = 0.f;
       }
     }
-    if (tid == 0)
-      for (int r = p.k; r < p.K; ++r) { ct[r] = -1; cp[r] = 0.f; }
+    __syncthreads();
+    if (wid == 0) {
+      // the CTA's list goes straight into rank 0's candidate table
+      warp_merge_topk(s_wz, s_wi, s_wq, SEL_WARPS * k, k, s_cz + rank * k, s_ci + rank * k, s_cq + rank * k);
+      if (lane < k) {
+        const int c = rank * k + lane;
+        sm100::dsmem_st_f32(sm100::dsmem_addr(&s_cz[c], 0), s_cz[c]);
+        sm100::dsmem_st_s32(sm100::dsmem_addr(&s_ci[c], 0), s_ci[c]);
+        sm100::dsmem_st_f32(sm100::dsmem_addr(&s_cq[c], 0), s_cq[c]);
+      }
+    }
+    sm100::cluster_sync();
+    if (rank != 0 || wid != 0) return;
+    warp_merge_topk(s_cz, s_ci, s_cq, SEL_CL * k, k, nullptr, s_wi, s_wq);
+    if (lane < p.K) {
+      const bool ok = lane < k && s_wi[lane] != INT32_MAX && s_wi[lane] < V;
+      ct[lane] = ok ? s_wi[lane] : -1;
+      cp[lane] = ok ? s_wq[lane] : 0.f;
+    }
     return;
   }
 
-  // sampling: exact integer weights over contiguous per-thread chunks, a
-  // block-wide inclusive scan of the chunk sums, then k sequential draws
-  const int per = (V + SEL_THREADS - 1) / SEL_THREADS;
-  const int v0 = tid * per, v1 = min(V, v0 + per);
+  // sampling: exact integer weights, this thread's chunk sum, its exclusive
+  // prefix within the cluster (CTA scan + earlier ranks' totals)
+  uint64_t W[SEL_PER];
   uint64_t wsum = 0;
-  for (int v = v0; v < v1; ++v) wsum += quantize_prob(qs[pad32(v)]);
-  tprefix[tid] = wsum;
+#pragma unroll
+  for (int u = 0; u < SEL_PER; ++u) {
+    W[u] = v0 + u < V ? quantize_prob(q[u]) : 0ull;
+    wsum += W[u];
+  }
+  uint64_t incl = wsum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_wscan[wid] = incl;
   __syncthreads();
-  for (int off = 1; off < SEL_THREADS; off <<= 1) {
-    const uint64_t add = tid >= off ? tprefix[tid - off] : 0ull;
-    __syncthreads();
-    tprefix[tid] += add;
-    __syncthreads();
+  uint64_t before = incl - wsum, cta_total = 0;
+  for (int w = 0; w < SEL_WARPS; ++w) {
+    if (w < wid) before += s_wscan[w];
+    cta_total += s_wscan[w];
   }
-  if (tid == 0) {
-    uint64_t remaining = tprefix[SEL_THREADS - 1];
-    int n_taken = 0;
-    for (int r = 0; r < p.k; ++r) {
-      if (remaining == 0) { ct[r] = -1; cp[r] = 0.f; continue; }
-      const uint32_t u = round_uniform(p.seed, r, e, PURPOSE_DRAW, b, p.round_id);
-      const uint64_t t = scale_uniform(u, remaining);
-      // inclusive prefix at the end of chunk tt, minus the weights already drawn
-      auto adj_prefix = [&](int tt) {
-        uint64_t v = tprefix[tt];
-        const int end = min(V, (tt + 1) * per);
-        for (int x = 0; x < n_taken; ++x)
-          if (s_taken[x] < end) v -= s_wtaken[x];
-        return v;
-      };
-      int lo = 0, hi = SEL_THREADS - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (adj_prefix(mid) > t) hi = mid; else lo = mid + 1;
-      }
-      uint64_t run = lo > 0 ? adj_prefix(lo - 1) : 0ull;
-      int pick = -1;
-      const int s0 = lo * per, s1 = min(V, s0 + per);
-      for (int v = s0; v < s1; ++v) {
-        bool taken = false;
-        for (int x = 0; x < n_taken; ++x) taken |= s_taken[x] == v;
-        if (taken) continue;
-        run += quantize_prob(qs[pad32(v)]);
-        if (run > t) { pick = v; break; }
-      }
-      if (pick < 0) {      // cannot happen with consistent prefix sums
-        set_status(p.status, EAGLE_ERR_NUMERIC);
-        ct[r] = -1; cp[r] = 0.f;
-        continue;
-      }
-      const uint64_t wp = quantize_prob(qs[pad32(pick)]);
-      s_taken[n_taken] = pick;
-      s_wtaken[n_taken] = wp;
-      ++n_taken;
-      remaining -= wp;
-      ct[r] = pick;
-      cp[r] = qs[pad32(pick)];
+  if (tid < SEL_CL) sm100::dsmem_st_u64(sm100::dsmem_addr(&s_ctot[rank], tid), cta_total);
+  sm100::cluster_sync();
+  uint64_t remaining = 0;
+  for (int c = 0; c < SEL_CL; ++c) {
+    if (c < static_cast<int>(rank)) before += s_ctot[c];
+    remaining += s_ctot[c];
+  }
+  const int v1 = v0 + SEL_PER;
+  bool lost = false;
+  for (int r = 0; r < k; ++r) {
+    if (remaining == 0) break;               // uniform: every CTA tracks the same total
+    const uint32_t u32 = round_uniform(p.seed, r, e, PURPOSE_DRAW, b, p.round_id);
+    const uint64_t t = scale_uniform(u32, remaining);
+    // this thread's range of the remaining (not yet drawn) mass
+    uint64_t start = before, own = wsum;
+    for (int x2 = 0; x2 < r; ++x2) {
+      const int y = s_pick[x2];
+      if (y < 0) continue;
+      if (y < v0) start -= s_pw[x2];
+      else if (y < v1) own -= s_pw[x2];
     }
-    for (int r = p.k; r < p.K; ++r) { ct[r] = -1; cp[r] = 0.f; }
+    if (own > 0 && start <= t && t - start < own) {
+      uint64_t run = start;
+      int pick = -1;
+      uint64_t wp = 0;
+      float qp = 0.f;
+#pragma unroll
+      for (int u = 0; u < SEL_PER; ++u) {
+        bool drawn = false;
+        for (int x2 = 0; x2 < r; ++x2) drawn |= s_pick[x2] == v0 + u;
+        if (pick < 0 && !drawn && W[u] > 0) {
+          run += W[u];
+          if (run > t) { pick = v0 + u; wp = W[u]; qp = q[u]; }
+        }
+      }
+      if (pick >= 0) {
+        for (int c = 0; c < SEL_CL; ++c) {
+          sm100::dsmem_st_s32(sm100::dsmem_addr(&s_pick[r], c), pick);
+          sm100::dsmem_st_u64(sm100::dsmem_addr(&s_pw[r], c), wp);
+          sm100::dsmem_st_f32(sm100::dsmem_addr(&s_pq[r], c), qp);
+        }
+      }
+    }
+    sm100::cluster_sync();
+    if (s_pick[r] < 0) { lost = true; break; }   // cannot happen with consistent prefix sums
+    remaining -= s_pw[r];
   }
+  if (rank == 0 && tid < p.K) {
+    const bool ok = tid < k && s_pick[tid] >= 0;
+    ct[tid] = ok ? s_pick[tid] : -1;
+    cp[tid] = ok ? s_pq[tid] : 0.f;
+  }
+  if (lost && rank == 0 && tid == 0) set_status(p.status, EAGLE_ERR_NUMERIC);
 }
 
 }  // namespace
@@ -303,16 +402,8 @@ cudaError_t launch_select(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st)
   p.seed = L.s->seed;
   p.round_id = L.s->round_id;
   p.status = ws_ptr<int>(L.ws, ctx->ws.status);
-  const size_t smem = static_cast<size_t>(p.V + (p.V >> 5) + 1) * sizeof(float);
-  static size_t attr = 0;
-  if (smem > attr) {
-    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr = smem;
-  }
   trace_before(ctx, EAGLE_K_SELECT, st);
-  select_kernel<<<L.n, SEL_THREADS, smem, st>>>(p);
+  select_kernel<<<L.n * SEL_CL, SEL_THREADS, 0, st>>>(p);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_SELECT, st);
   return cudaGetLastError();

@@ -5,8 +5,10 @@ run_oracle_round: the same inputs (copied to the host) through the CPU oracle.
 compare_round: element-wise comparison.  Discrete results (children, tree,
 accept length, path, tokens) must be identical; a mismatch is tolerated only
 as a flagged near-tie, when the oracle's own margin for that decision is
-below the floating-point tolerance, and the request's later comparisons are
-then skipped.  Floating point: features, logits and attention outputs within
+below the floating-point tolerance (a logit gap, a sampling CDF margin, or
+for EAGLE-2 two node values -- products of draft confidences -- closer than
+the confidences' observed error can reorder), and the request's later
+comparisons are then skipped.  Floating point: features, logits and attention outputs within
 max-abs 1e-4 (fp32 workload) or 2e-2 (bf16 workloads), applied to values in
 units of the row's RMS when that exceeds 1 (random draft weights grow the
 residual stream layer by layer, to RMS ~10^2 at depth 5 of the 70B shape,
@@ -76,6 +78,55 @@ def _f64(t):
     return t.to(torch.float64).numpy() if torch.is_tensor(t) else np.asarray(t, dtype=np.float64)
 
 
+def _conf_rel_err(gpu, b, st):
+    """Largest relative error of a GPU draft confidence against the oracle's."""
+    rho = 0.0
+    for e in range(len(st.ex.token)):
+        k = len(st.child_tok[e])
+        want = np.asarray(st.child_q[e], dtype=np.float64)
+        got = np.asarray(gpu["c_prob"][b, e, :k], dtype=np.float64)
+        ok = want > 0
+        if ok.any():
+            rho = max(rho, float(np.max(np.abs(got[ok] - want[ok]) / want[ok])))
+    return rho
+
+
+def _value_tie(gpu, b, st, e_par, tok, v_ref, depth):
+    """EAGLE-2 value near-tie: the GPU kept (child `tok` of expanded node
+    `e_par`) where the oracle kept a node of value v_ref.  Values are products
+    of at most `depth` draft confidences, so two values closer than twice
+    depth x (the confidences' observed relative error + fp32 rounding) may
+    order either way.  Returns a description, or None."""
+    ex = st.ex
+    if not 0 <= e_par < len(ex.token):
+        return None
+    ranks = [r for r, t in enumerate(st.child_tok[e_par]) if t == tok]
+    if not ranks:
+        return None
+    v_gpu = ex.value[e_par] * float(st.child_q[e_par][ranks[0]])
+    bound = 2.0 * depth * (_conf_rel_err(gpu, b, st) + 2.0 ** -23) * max(v_gpu, v_ref)
+    gap = abs(v_gpu - v_ref)
+    if gap <= bound:
+        return f"values {v_ref:.9g} vs {v_gpu:.9g} (gap {gap:.2e} <= {bound:.2e})"
+    return None
+
+
+def _rerank_near_tie(gpu, b, st, tr, depth):
+    """The final trees first differ at a slot whose two candidates are an
+    EAGLE-2 value near-tie (see _value_tie)."""
+    size = tr.size
+    g_tok = [int(x) for x in gpu["t_token"][b, :size]]
+    g_par = [int(x) for x in gpu["t_parent"][b, :size]]
+    s = next((j for j in range(size) if (g_tok[j], g_par[j]) != (tr.token[j], tr.parent[j])), None)
+    if s is None or s == 0:
+        return None
+    p = g_par[s]
+    if not 0 <= p < s or tr.exp[p] < 0:
+        return None
+    tie = _value_tie(gpu, b, st, tr.exp[p], g_tok[s], tr.value[s], depth)
+    return None if tie is None else f"slot {s}: {tie}"
+
+
 def compare_round(w, gpu, ref, requests=None):
     """Returns a report dict; report['ok'] is False on any non-near-tie mismatch."""
     from oracle import philox
@@ -105,8 +156,15 @@ def compare_round(w, gpu, ref, requests=None):
         diverged = False
         # draft head outputs, per expanded node in creation order
         for e in range(len(ex.token)):
-            if int(gpu["p_token"][b, e]) != ex.token[e]:
-                fail(f"b{b} pool token e{e}: {int(gpu['p_token'][b, e])} vs {ex.token[e]}")
+            if int(gpu["p_token"][b, e]) != ex.token[e] or int(gpu["p_parent"][b, e]) != ex.parent[e]:
+                tie = None
+                if e > 0 and w.tree == "eagle2":
+                    tie = _value_tie(gpu, b, st, int(gpu["p_parent"][b, e]), int(gpu["p_token"][b, e]),
+                                     ex.value[e], w.depth)
+                if tie is not None:
+                    rep["near_ties"].append(f"b{b} frontier e{e}: {tie}")
+                else:
+                    fail(f"b{b} pool token e{e}: {int(gpu['p_token'][b, e])} vs {ex.token[e]}")
                 diverged = True
                 break
             err("f_hat", _maxerr_scaled(gpu["f_hat"][b, e], st.f_hat[e]), tol)
@@ -134,7 +192,7 @@ def compare_round(w, gpu, ref, requests=None):
                     rem = wq.sum() / max(1.0, float(quantize(st.q[e]).sum()))
                     near = margin < 2.0 * dz / temp / max(rem, 1e-12) + 1e-6
                 if near:
-                    rep["near_ties"].append(f"b{b} e{e} rank{rank} margin {margin:.2e}")
+                    rep["near_ties"].append(f"b{b} children e{e} rank{rank} margin {margin:.2e}")
                     diverged = True
                     break
                 fail(f"b{b} children of e{e}: {g_ch} vs {list(st.child_tok[e])}")
@@ -147,6 +205,10 @@ def compare_round(w, gpu, ref, requests=None):
         size = tr.size
         if int(gpu["t_size"][b]) != size:
             fail(f"b{b} tree size {int(gpu['t_size'][b])} vs {size}")
+            continue
+        tie = _rerank_near_tie(gpu, b, st, tr, w.depth)
+        if tie is not None:
+            rep["near_ties"].append(f"b{b} rerank {tie}")
             continue
         for name, mine, want in (("token", gpu["t_token"], tr.token), ("parent", gpu["t_parent"], tr.parent),
                                  ("depth", gpu["t_depth"], tr.depth), ("exp", gpu["t_exp"], tr.exp)):
