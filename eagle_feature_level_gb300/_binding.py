@@ -136,6 +136,8 @@ def _declare(L):
                                      C.POINTER(eagle_children), C.POINTER(eagle_pool), C.POINTER(eagle_tree),
                                      P, P],
         "eagle_tree_verify_attn": [P, I, P, P, P, C.POINTER(eagle_kv), C.POINTER(eagle_tree), C.c_float, P, P, P],
+        "eagle_tree_verify_attn_noalloc": [P, I, P, P, P, C.POINTER(eagle_kv), C.POINTER(eagle_tree), C.c_float,
+                                           P, P],
         "eagle_accept": [P, C.POINTER(eagle_plan), I, C.POINTER(eagle_tree), C.POINTER(eagle_children), P, P,
                          C.POINTER(eagle_sampling), P, P, C.POINTER(eagle_accept_out), P, P],
         "eagle_accept_from_probs": [P, C.POINTER(eagle_plan), I, C.POINTER(eagle_tree),
@@ -159,7 +161,8 @@ def _declare(L):
 
 EXPORTED = ["eagle_create", "eagle_destroy", "eagle_workspace_init", "eagle_read_device_status",
             "eagle_status_string", "eagle_plan_eagle2", "eagle_plan_static", "eagle_draft_step",
-            "eagle_tree_expand_rerank", "eagle_tree_verify_attn", "eagle_accept", "eagle_accept_from_probs",
+            "eagle_tree_expand_rerank", "eagle_tree_verify_attn", "eagle_tree_verify_attn_noalloc",
+            "eagle_accept", "eagle_accept_from_probs",
             "eagle_commit", "eagle_trace_enable", "eagle_trace_read", "eagle_trace_disable",
             "eagle_launch_count"]
 
@@ -231,6 +234,14 @@ def eagle_tree_verify_attn(ctx, batch, q, k_tree, v_tree, prefix, tree, scale, o
     _check("eagle_tree_verify_attn",
            lib().eagle_tree_verify_attn(ctx, batch, q, k_tree, v_tree, C.byref(prefix), C.byref(tree), scale, out,
                                         ws_ptr, stream))
+
+
+def eagle_tree_verify_attn_noalloc(ctx, batch, q, k_tree, v_tree, prefix, tree, scale, out, stream):
+    """eagle_tree_verify_attn with its scratch in the library's fixed device
+    array (no workspace); see the C header for the size limit and races."""
+    _check("eagle_tree_verify_attn_noalloc",
+           lib().eagle_tree_verify_attn_noalloc(ctx, batch, q, k_tree, v_tree, C.byref(prefix), C.byref(tree), scale,
+                                                out, stream))
 
 
 def eagle_accept(ctx, plan, batch, tree, children, target_logits, q_probs, s, target_probs, target_argmax, out,

@@ -442,6 +442,19 @@ eagle_status eagle_tree_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q
   return EAGLE_OK;
 }
 
+eagle_status eagle_tree_verify_attn_noalloc(eagle_ctx* ctx, int batch, const uint16_t* q, const uint16_t* k_tree,
+                                            const uint16_t* v_tree, const eagle_kv* prefix, const eagle_tree* tree,
+                                            float scale, float* out, cudaStream_t stream) {
+  EAGLE_REQUIRE(ctx, EAGLE_ERR_INVALID_ARG);
+  EAGLE_REQUIRE(batch >= 1 && batch <= ctx->lim.max_batch, EAGLE_ERR_CAPACITY);
+  EAGLE_PTR(q); EAGLE_PTR(k_tree); EAGLE_PTR(v_tree); EAGLE_PTR(out);
+  eagle_status st = check_kv(ctx, prefix);
+  if (st != EAGLE_OK) return st;
+  if ((st = check_tree(ctx, tree)) != EAGLE_OK) return st;
+  EAGLE_REQUIRE(std::isfinite(scale) && scale > 0.f, EAGLE_ERR_INVALID_ARG);
+  return launch_verify_attn_noalloc(ctx, batch, q, k_tree, v_tree, prefix, tree, scale, out, stream);
+}
+
 static eagle_status check_accept(eagle_ctx* ctx, const eagle_plan* plan, int batch, const eagle_tree* tree,
                                  const eagle_children* children, const float* q_probs, const eagle_sampling* s,
                                  const eagle_accept_out* out, void* workspace) {

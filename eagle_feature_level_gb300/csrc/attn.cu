@@ -10,6 +10,7 @@
 // (request, kv head) merges them in split order.  The ancestor mask of each
 // query row lives in a register (one 64-bit word) and is tested per tree key.
 #include <algorithm>
+#include <mutex>
 
 #include "internal.h"
 #include "sm100.cuh"
@@ -468,6 +469,82 @@ cudaError_t launch_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, con
   p.part = ws_ptr<float>(ws, W.attn_part);
   p.counters = ws_ptr<int>(ws, W.attn_cnt) + ctx->lim.max_batch * D.n_kv_heads;
   return run_attn(ctx, p, EAGLE_K_VERIFY_ATTN, st);
+}
+
+// ---- verify attention from a fixed device scratch (no workspace) ----------
+//
+// For callers that cannot hand the library device memory (a C host that
+// links only libeagle and owns no allocator, a serving loop whose memory is
+// fully reserved at start-up): the split partials and the arrival counters
+// of eagle_tree_verify_attn_noalloc live in this file-scope array, one per
+// device, instead of the caller's workspace.  Layout: [0, 64 KiB) int
+// counters, one per (request, kv head), which must be zero when a call
+// starts; then the fp32 partial records, which need no initial value.
+constexpr size_t kScratchBytes = static_cast<size_t>(32) << 20;
+constexpr size_t kScratchCounterBytes = static_cast<size_t>(64) << 10;
+constexpr int kScratchMaxPairs = static_cast<int>(kScratchCounterBytes / sizeof(int));
+constexpr int kScratchMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char verify_scratch[kScratchBytes];
+
+namespace {
+std::mutex scratch_mu;
+void* scratch_base[kScratchMaxDevices] = {};
+}  // namespace
+
+size_t verify_scratch_need(const eagle_ctx* ctx, int batch, const eagle_kv* prefix, const eagle_tree* tree) {
+  const eagle_dims& D = ctx->dims;
+  const int splits = attn_splits(ctx, batch * D.n_kv_heads, prefix->cap);
+  const size_t records = static_cast<size_t>(batch) * tree->stride * D.n_q_heads * (splits + 1);
+  return records * (D.head_dim + 2) * sizeof(float);
+}
+
+eagle_status launch_verify_attn_noalloc(eagle_ctx* ctx, int batch, const uint16_t* q, const uint16_t* kt,
+                                        const uint16_t* vt, const eagle_kv* prefix, const eagle_tree* tree,
+                                        float scale, float* out, cudaStream_t st) {
+  const eagle_dims& D = ctx->dims;
+  if (batch * D.n_kv_heads > kScratchMaxPairs ||
+      verify_scratch_need(ctx, batch, prefix, tree) > kScratchBytes - kScratchCounterBytes)
+    return EAGLE_ERR_CAPACITY;                 // nothing launched
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kScratchMaxDevices) return EAGLE_ERR_CUDA;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(scratch_mu);
+    base = scratch_base[dev];
+    if (base == nullptr) {
+      // first call on this device: the array's address, then zeroed counters
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, verify_scratch) != cudaSuccess) return EAGLE_ERR_CUDA;
+      if (cudaMemsetAsync(ptr, 0, kScratchCounterBytes, st) != cudaSuccess) return EAGLE_ERR_CUDA;
+      if (cudaStreamSynchronize(st) != cudaSuccess) return EAGLE_ERR_CUDA;
+      scratch_base[dev] = base = ptr;
+    }
+  }
+  AttnParams p{};
+  p.mode = 1;
+  p.B = batch;
+  p.Hq = D.n_q_heads;
+  p.Hkv = D.n_kv_heads;
+  p.dh = D.head_dim;
+  p.G = D.n_q_heads / D.n_kv_heads;
+  p.rows_cap = tree->stride;
+  p.q_bf16 = q;
+  p.kp = prefix->k;
+  p.vp = prefix->v;
+  p.kv_cap = prefix->cap;
+  p.kv_len = prefix->len;
+  p.kt_bf16 = kt;
+  p.vt_bf16 = vt;
+  p.tree_cap = tree->stride;
+  p.anc = tree->anc;
+  p.tree_size = tree->size;
+  p.scale = scale;
+  p.out_f32 = out;
+  // the last CTA of each (request, kv head) puts its counter back to zero
+  p.counters = static_cast<int*>(base);
+  p.part = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + kScratchCounterBytes);
+  return run_attn(ctx, p, EAGLE_K_VERIFY_ATTN, st) == cudaSuccess ? EAGLE_OK : EAGLE_ERR_CUDA;
 }
 
 }  // namespace eagle

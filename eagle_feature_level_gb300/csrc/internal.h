@@ -106,6 +106,12 @@ cudaError_t launch_tree(eagle_ctx* ctx, const eagle_plan* plan, int phase, int l
 cudaError_t launch_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, const uint16_t* kt,
                                const uint16_t* vt, const eagle_kv* prefix, const eagle_tree* tree,
                                float scale, float* out, void* ws, cudaStream_t st);
+// eagle_tree_verify_attn_noalloc: the same kernel with its partials and
+// counters in a fixed static device array; EAGLE_ERR_CAPACITY when the call
+// does not fit it (nothing launched).
+eagle_status launch_verify_attn_noalloc(eagle_ctx* ctx, int batch, const uint16_t* q, const uint16_t* kt,
+                                        const uint16_t* vt, const eagle_kv* prefix, const eagle_tree* tree,
+                                        float scale, float* out, cudaStream_t st);
 
 cudaError_t launch_target_softmax(eagle_ctx* ctx, int batch, const eagle_tree* tree, const float* logits,
                                   const float* temperature, float* probs, int32_t* argmax, void* ws,

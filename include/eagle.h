@@ -305,6 +305,44 @@ eagle_status eagle_tree_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q
                                     const eagle_kv* prefix, const eagle_tree* tree, float scale,
                                     float* out, void* workspace, cudaStream_t stream);
 
+/* eagle_tree_verify_attn_noalloc -- eagle_tree_verify_attn without a
+ * workspace argument.  None of the three pages has a counterpart: this is a
+ * deployment convenience around the same kernel, not part of the method.
+ *
+ * Who needs it: callers that cannot hand the library device memory -- a
+ * plain C host that links only libeagle and owns no device allocator, or a
+ * serving loop whose device memory is fully reserved at start-up and may not
+ * allocate per call.  The call allocates nothing: no cudaMalloc / cudaFree
+ * and no allocating library.  The split partials and the per-(request,
+ * kv head) arrival counters live in a fixed 32 MiB static device array
+ * inside libeagle, one per device.
+ *
+ * Limit: batch * n_kv_heads <= 16384 and
+ *   batch * tree.stride * n_q_heads * (splits + 1) * (head_dim + 2) * 4 bytes
+ *   <= 32 MiB - 64 KiB,
+ * splits being the prefix split count the library picks (<= 31; about
+ * 2 * SMs / (batch * n_kv_heads), at most one per 64 rows of prefix.cap).
+ * Example: batch 1, 32 query heads of 128, stride 64, 10 splits: 11.7 MB.
+ * Beyond the limit the call returns EAGLE_ERR_CAPACITY and launches nothing;
+ * use eagle_tree_verify_attn with a workspace instead.
+ *
+ * Zero state: the counters must be zero when a call starts.  The first call
+ * on a device looks up the array's address, zeroes the counters on `stream`
+ * and waits for `stream`; make that first call before any stream capture
+ * begins.  Every call leaves the counters at zero again.  The partials need
+ * no initial value.
+ *
+ * Races: every call on one device shares the one array.  Two calls whose
+ * kernels may overlap in time (different streams with no ordering between
+ * them, or several host threads) corrupt each other's partials and counters;
+ * order them, e.g. on one stream.
+ *
+ * Arguments, layouts, results and the other errors: as eagle_tree_verify_attn. */
+eagle_status eagle_tree_verify_attn_noalloc(eagle_ctx* ctx, int batch, const uint16_t* q,
+                                            const uint16_t* k_tree, const uint16_t* v_tree,
+                                            const eagle_kv* prefix, const eagle_tree* tree, float scale,
+                                            float* out, cudaStream_t stream);
+
 /* eagle_accept -- acceptance on the verified tree ([A] §6.2; [B] "Greedy 验证",
  * "随机采样验证"; [C] "为什么普通草稿模型不够理想").
  * target_logits [B][S][V] fp32 (the target's logits at every tree slot).
