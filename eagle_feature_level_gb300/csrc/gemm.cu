@@ -3,9 +3,19 @@
 // rows (1..256) and W streamed from HBM exactly once per launch.
 //
 // Blackwell design:
-//  * the weight tile (128 rows x 64 k, two 64-row TMA boxes, 128-byte swizzle)
-//    and the activation tile are brought in by TMA into a multi-stage
-//    shared-memory ring guarded by mbarriers;
+//  * a pipeline stage holds 128 weight rows x kps k-blocks of 64 (kps = 2
+//    unless the activation tile is large): each 64-row half is one TMA box of
+//    a 4-D tensor map {64 k, 8 rows, k-block, 8-row group}, so every request
+//    fetches kps x 128 contiguous bytes per weight row (HBM streams markedly
+//    faster at 256 B per row than at 128 B); shared memory receives
+//    [group][k-block][8 rows][128 B] with the 128-byte swizzle, which the MMA
+//    reads with an 8-row group stride of kps x 1024 B.  The 4-D map covers
+//    only whole k-blocks and whole 8-row groups, so it never reads past a row
+//    pitch or the last row; a half that reaches a matrix's row tail or K tail
+//    is fetched as 8 x kps boxes {64 k, 8 rows} of a 2-D map over the used
+//    [rows][K] extent, whose out-of-range elements fill with zeros;
+//  * the activation tile arrives the same way (one 4-D box); stages cycle
+//    through a multi-stage shared-memory ring guarded by mbarriers;
 //  * one thread issues tcgen05.mma (M = 128 weight rows, N = activation rows,
 //    "swap-AB"), accumulating in tensor memory; a commit per stage releases the
 //    ring slot;
@@ -29,9 +39,8 @@ namespace eagle {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;
-constexpr int A_STAGE_BYTES = BM * BK * 2;
-constexpr int BOX_BYTES = 64 * BK * 2;
+constexpr int BK = 64;                     // elements per k-block (one 128-byte swizzle row)
+constexpr int KBLK_BYTES = BK * 2;
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
 constexpr int XCH_ROWS = 32;
@@ -44,7 +53,10 @@ struct GemmParams {
   int n_mats;
   int two_mma;
   int tmem_cols, acc_stride, n_acc, stages;
-  uint32_t b_stage_bytes, b_box_rows;
+  int kps;                  // k-blocks per stage
+  uint32_t a_stage_bytes, b_stage_bytes;
+  int full_rows[3];         // rows of each matrix in whole 8-row groups
+  int full_kb;              // whole 64-wide k-blocks of K
   int rpr, e0, E;
   int d, F, V, Hq, Hkv, dh;
   float eps;
@@ -69,7 +81,7 @@ struct GemmParams {
 };
 
 struct Smem {
-  uint8_t* a;       // stages x 16 KB
+  uint8_t* a;       // stages x a_stage_bytes
   uint8_t* b;       // stages x b_stage_bytes
   uint64_t* full;
   uint64_t* empty;
@@ -82,9 +94,9 @@ struct Smem {
   float* rs;        // [32]
 };
 
-__host__ __device__ inline size_t smem_bytes_for(int stages, uint32_t b_stage) {
+__host__ __device__ inline size_t smem_bytes_for(int stages, uint32_t a_stage, uint32_t b_stage) {
   size_t s = 1024;                                  // alignment slack
-  s += static_cast<size_t>(stages) * (A_STAGE_BYTES + b_stage);
+  s += static_cast<size_t>(stages) * (a_stage + b_stage);
   s += (2 * stages + 4) * 8 + 64;
   s += XCH_ROWS * BM * 4 + 4 * 32 * 4 + 32 * 4;
   return s;
@@ -95,7 +107,7 @@ __device__ inline Smem carve(uint8_t* raw, const GemmParams& p) {
   uint8_t* ptr = reinterpret_cast<uint8_t*>(base);
   Smem s;
   s.a = ptr;
-  ptr += static_cast<size_t>(p.stages) * A_STAGE_BYTES;
+  ptr += static_cast<size_t>(p.stages) * p.a_stage_bytes;
   s.b = ptr;
   ptr += static_cast<size_t>(p.stages) * p.b_stage_bytes;
   s.full = reinterpret_cast<uint64_t*>(ptr);
@@ -276,8 +288,9 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, i
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_stream_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
-                       const __grid_constant__ CUtensorMap mA2, const __grid_constant__ CUtensorMap mB,
-                       const GemmParams p) {
+                       const __grid_constant__ CUtensorMap mA2, const __grid_constant__ CUtensorMap mT0,
+                       const __grid_constant__ CUtensorMap mT1, const __grid_constant__ CUtensorMap mT2,
+                       const __grid_constant__ CUtensorMap mB, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const Smem s = carve(smem_raw, p);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -304,6 +317,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     sm100::tma_prefetch_desc(&mA0);
+    if (p.n_mats > 1) sm100::tma_prefetch_desc(&mA1);
+    if (p.n_mats > 2) sm100::tma_prefetch_desc(&mA2);
     sm100::tma_prefetch_desc(&mB);
   }
   if (warp == 1) {
@@ -328,20 +343,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           set_status(p.status, EAGLE_ERR_TIMEOUT);
           break;
         }
-        sm100::mbar_arrive_expect_tx(&s.full[stage], A_STAGE_BYTES + p.b_stage_bytes);
-        uint8_t* a_dst = s.a + static_cast<size_t>(stage) * A_STAGE_BYTES;
-#pragma unroll
+        sm100::mbar_arrive_expect_tx(&s.full[stage], p.a_stage_bytes + p.b_stage_bytes);
+        uint8_t* a_dst = s.a + static_cast<size_t>(stage) * p.a_stage_bytes;
+        const int kz = kblk * p.kps;                 // first 64-wide k-block of the stage
+        const uint32_t group_bytes = static_cast<uint32_t>(p.kps) * 1024u;
+#pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           int map, row;
           locate_box(p, t, h, map, row);
-          const CUtensorMap* mp = map == 0 ? &mA0 : (map == 1 ? &mA1 : &mA2);
-          sm100::tma_load_2d(a_dst + h * BOX_BYTES, mp, kblk * BK, row, &s.full[stage]);
+          uint8_t* dst = a_dst + h * 8 * group_bytes;
+          if (row + 64 <= p.full_rows[map] && kz + p.kps <= p.full_kb) {
+            const CUtensorMap* mp = map == 0 ? &mA0 : (map == 1 ? &mA1 : &mA2);
+            sm100::tma_load_4d(dst, mp, 0, 0, kz, row >> 3, &s.full[stage]);
+          } else {                                   // row or K tail: 8-row x 64-k boxes, zero past the end
+            const CUtensorMap* mp = map == 0 ? &mT0 : (map == 1 ? &mT1 : &mT2);
+#pragma unroll 1
+            for (int g = 0; g < 8; ++g)
+              for (int c = 0; c < p.kps; ++c)
+                sm100::tma_load_2d(dst + g * group_bytes + c * 1024, mp, (kz + c) * BK, row + 8 * g,
+                                   &s.full[stage]);
+          }
         }
         uint8_t* b_dst = s.b + static_cast<size_t>(stage) * p.b_stage_bytes;
-        sm100::tma_load_2d(b_dst, &mB, kblk * BK, 0, &s.full[stage]);
-        if (p.b_box_rows < 2u * p.NP)
-          sm100::tma_load_2d(b_dst + p.b_box_rows * 128u, &mB, kblk * BK, static_cast<int>(p.b_box_rows),
-                             &s.full[stage]);
+        sm100::tma_load_4d(b_dst, &mB, 0, 0, kz, 0, &s.full[stage]);
         ++issued;
         if (++stage == p.stages) { stage = 0; phase ^= 1u; }
       }
@@ -389,16 +413,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           sm100::tc_fence_after();
-          const uint32_t a_addr = sm100::smem_u32(s.a + static_cast<size_t>(stage) * A_STAGE_BYTES);
+          const uint32_t a_addr = sm100::smem_u32(s.a + static_cast<size_t>(stage) * p.a_stage_bytes);
           const uint32_t b_addr = sm100::smem_u32(s.b + static_cast<size_t>(stage) * p.b_stage_bytes);
+          const uint32_t sbo = static_cast<uint32_t>(p.kps) * 1024u;
+          const uint32_t b2 = static_cast<uint32_t>(p.NP >> 3) * sbo;   // second activation half
+          for (int c = 0; c < p.kps; ++c) {
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = sm100::smem_desc_sw128(a_addr + kk * 32);
-            const uint32_t accum = (u != seg_start || kk > 0) ? 1u : 0u;
-            sm100::mma_bf16(d_tmem, ad, sm100::smem_desc_sw128(b_addr + kk * 32), idesc, accum);
-            if (p.two_mma)
-              sm100::mma_bf16(d_tmem + p.NP, ad, sm100::smem_desc_sw128(b_addr + p.NP * 128 + kk * 32), idesc,
-                              accum);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint32_t off = static_cast<uint32_t>(c) * 1024u + kk * 32;
+              const uint64_t ad = sm100::smem_desc_sw128_sbo(a_addr + off, sbo);
+              const uint32_t accum = (u != seg_start || c > 0 || kk > 0) ? 1u : 0u;
+              sm100::mma_bf16(d_tmem, ad, sm100::smem_desc_sw128_sbo(b_addr + off, sbo), idesc, accum);
+              if (p.two_mma)
+                sm100::mma_bf16(d_tmem + p.NP, ad, sm100::smem_desc_sw128_sbo(b_addr + b2 + off, sbo), idesc,
+                                accum);
+            }
           }
           sm100::mma_commit(&s.empty[stage]);
           if (++stage == p.stages) { stage = 0; phase ^= 1u; }
@@ -475,11 +504,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-bool encode_2d(eagle_ctx* ctx, CUtensorMap* map, const void* ptr, int inner, int rows, int ld_elems,
-               int box_inner, int box_rows) {
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+// [rows][ld] bf16 matrix seen as {64 k, 8 rows, k-block, 8-row group} over
+// its whole k-blocks and whole 8-row groups only (every element the map can
+// address lies inside the used [rows][K] extent); box = kps k-blocks x
+// box_groups groups.
+bool encode_grouped(eagle_ctx* ctx, CUtensorMap* map, const void* ptr, int K, int rows, int ld_elems, int kps,
+                    int box_groups) {
+  const int groups = rows / 8 > 0 ? rows / 8 : 1;   // a dimension under one unit is never addressed
+  const int kblocks = K / BK > 0 ? K / BK : 1;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(BK), 8, static_cast<cuuint64_t>(kblocks),
+                        static_cast<cuuint64_t>(groups)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(ld_elems) * 2, KBLK_BYTES,
+                           static_cast<cuuint64_t>(ld_elems) * 16};
+  cuuint32_t box[4] = {BK, 8, static_cast<cuuint32_t>(kps), static_cast<cuuint32_t>(box_groups)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The used [rows][K] extent as a 2-D map; box = 64 k x 8 rows (elements
+// past K or past the last row read as zero).
+bool encode_tail(eagle_ctx* ctx, CUtensorMap* map, const void* ptr, int K, int rows, int ld_elems) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_elems) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {BK, 8};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -574,11 +624,16 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
     p.mblk[i] = cum;
   }
   p.m_tiles = epi == EPI_GATEUP ? ceil_div(D.d_ff, 64) : ceil_div(n_out, BM);
-  p.kb = ceil_div(K, BK);
-  p.total_units = static_cast<long long>(p.m_tiles) * p.kb;
   p.two_mma = 2 * p.NP > 256 ? 1 : 0;
-  p.b_box_rows = static_cast<uint32_t>(p.two_mma ? p.NP : 2 * p.NP);
-  p.b_stage_bytes = static_cast<uint32_t>(2 * p.NP * 128);
+  for (int i = 0; i < 3; ++i) p.full_rows[i] = i < p.n_mats ? rows[i] / 8 * 8 : 0;
+  p.full_kb = K / BK;
+  // two k-blocks per stage while that still leaves a ring of >= 3 stages
+  const size_t smem_cap = 232448;
+  p.kps = smem_bytes_for(3, BM * KBLK_BYTES * 2, 2 * p.NP * KBLK_BYTES * 2) <= smem_cap ? 2 : 1;
+  p.a_stage_bytes = static_cast<uint32_t>(BM * KBLK_BYTES * p.kps);
+  p.b_stage_bytes = static_cast<uint32_t>(2 * p.NP * KBLK_BYTES * p.kps);
+  p.kb = ceil_div(K, BK * p.kps);
+  p.total_units = static_cast<long long>(p.m_tiles) * p.kb;
   const int acc_cols = 2 * p.NP;
   p.acc_stride = acc_cols < 32 ? 32 : (acc_cols + 31) / 32 * 32;
   p.n_acc = 2 * p.acc_stride <= 512 ? 2 : 1;
@@ -587,19 +642,20 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   while (cols < need) cols <<= 1;
   p.tmem_cols = cols;
 
-  const size_t smem_cap = 232448;
   int stages = 8;
-  while (stages > 2 && smem_bytes_for(stages, p.b_stage_bytes) > smem_cap) --stages;
+  while (stages > 2 && smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes) > smem_cap) --stages;
   p.stages = stages;
-  size_t smem = smem_bytes_for(stages, p.b_stage_bytes);
+  size_t smem = smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes);
+  if (smem > smem_cap) return cudaErrorInvalidConfiguration;
   if (smem < 120 * 1024) smem = 120 * 1024;    // one CTA per SM: tensor memory is never contended
 
-  CUtensorMap maps[3], mb;
+  CUtensorMap maps[3], tails[3], mb;
   for (int i = 0; i < 3; ++i) {
     const int src = i < p.n_mats ? i : 0;
-    if (!encode_2d(ctx, &maps[i], mats[src], K, rows[src], lds[src], BK, 64)) return cudaErrorInvalidValue;
+    if (!encode_grouped(ctx, &maps[i], mats[src], K, rows[src], lds[src], p.kps, 8)) return cudaErrorInvalidValue;
+    if (!encode_tail(ctx, &tails[i], mats[src], K, rows[src], lds[src])) return cudaErrorInvalidValue;
   }
-  if (!encode_2d(ctx, &mb, ws_ptr<uint16_t>(L.ws, b_in), kp_in, 2 * p.NP, kp_in, BK, p.b_box_rows))
+  if (!encode_grouped(ctx, &mb, ws_ptr<uint16_t>(L.ws, b_in), kp_in, 2 * p.NP, kp_in, p.kps, 2 * p.NP / 8))
     return cudaErrorInvalidValue;
 
   static bool attr_set = false;
@@ -612,7 +668,8 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   int grid = ctx->sm_count;
   if (p.total_units < grid) grid = static_cast<int>(p.total_units);
   trace_before(ctx, epi, st);
-  gemm_stream_kernel<<<grid, NUM_THREADS, smem, st>>>(maps[0], maps[1], maps[2], mb, p);
+  gemm_stream_kernel<<<grid, NUM_THREADS, smem, st>>>(maps[0], maps[1], maps[2], tails[0], tails[1], tails[2],
+                                                     mb, p);
   ctx->launches++;
   trace_after(ctx, epi, st);
   return cudaGetLastError();
