@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(SM_THREADS)
     target_softmax_kernel(const float* __restrict__ logits, const float* __restrict__ temperature,
                           const int32_t* __restrict__ tree_size, int S, int V, float* __restrict__ probs,
                           int32_t* __restrict__ argmax, int* status) {
+  pdl_wait();      // predecessor outputs visible from here on
+  pdl_trigger();
   __shared__ float red_f[32];
   __shared__ int red_i[32];
   const int s = blockIdx.x, b = blockIdx.y;
@@ -112,6 +114,8 @@ struct WalkParams {
 };
 
 __global__ void __launch_bounds__(SM_THREADS) accept_walk_kernel(const WalkParams p) {
+  pdl_wait();      // predecessor outputs visible from here on
+  pdl_trigger();
   __shared__ uint64_t red_u[32];
   __shared__ int red_i[32];
   __shared__ uint64_t tprefix[SM_THREADS];
@@ -286,12 +290,12 @@ cudaError_t launch_target_softmax(eagle_ctx* ctx, int batch, const eagle_tree* t
                                   cudaStream_t st) {
   dim3 grid(tree->stride, batch);
   trace_before(ctx, EAGLE_K_ACCEPT, st);
-  target_softmax_kernel<<<grid, SM_THREADS, 0, st>>>(logits, temperature, tree->size, tree->stride,
-                                                     ctx->dims.vocab, probs, argmax,
-                                                     ws_ptr<int>(ws, ctx->ws.status));
+  const cudaError_t e = launch_pdl(target_softmax_kernel, grid, dim3(SM_THREADS), 0, st, logits, temperature,
+                                   tree->size, tree->stride, ctx->dims.vocab, probs, argmax,
+                                   ws_ptr<int>(ws, ctx->ws.status));
   ctx->launches++;
   trace_after(ctx, EAGLE_K_ACCEPT, st);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_accept_walk(eagle_ctx* ctx, const eagle_plan* plan, int batch, const eagle_tree* tree,
@@ -324,10 +328,10 @@ cudaError_t launch_accept_walk(eagle_ctx* ctx, const eagle_plan* plan, int batch
   p.last_slot = out->last_slot;
   p.status = ws_ptr<int>(ws, ctx->ws.status);
   trace_before(ctx, EAGLE_K_ACCEPT, st);
-  accept_walk_kernel<<<batch, SM_THREADS, 0, st>>>(p);
+  const cudaError_t e = launch_pdl(accept_walk_kernel, dim3(batch), dim3(SM_THREADS), 0, st, p);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_ACCEPT, st);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace eagle

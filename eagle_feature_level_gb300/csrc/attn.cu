@@ -154,6 +154,8 @@ __device__ __forceinline__ void tree_stage(const AttnParams& p, float* sk, float
 // P V for them (lane = 4 output columns), so after the tile is staged no
 // further block-wide barrier is needed.
 __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams p) {
+  pdl_wait();      // predecessor outputs visible from here on
+  pdl_trigger();
   extern __shared__ __align__(16) float smem_attn[];
   __shared__ int s_last;
   __shared__ uint64_t s_mask[ROWS_PASS];     // ancestor masks of the tree part's rows
@@ -405,10 +407,10 @@ static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaSt
     attr_set = true;
   }
   trace_before(ctx, kernel_id, st);
-  tree_attn_kernel<<<grid, THREADS, smem, st>>>(p);
+  const cudaError_t e = launch_pdl(tree_attn_kernel, grid, dim3(THREADS), smem, st, p);
   ctx->launches++;
   trace_after(ctx, kernel_id, st);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_draft_attn(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st) {

@@ -44,6 +44,8 @@ __device__ __forceinline__ void copy_row(uint16_t* dst, const uint16_t* src, int
 }
 
 __global__ void commit_kernel(const CommitParams p) {
+  pdl_wait();      // predecessor outputs visible from here on
+  pdl_trigger();
   const int b = blockIdx.x, i = blockIdx.y;
   const int a = p.accept_len[b];
   if (i > a) return;
@@ -125,10 +127,10 @@ cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st
   p.draft_len_out = C.out->draft_len;
   dim3 grid(C.batch, C.acc->path_cap);
   trace_before(ctx, EAGLE_K_COMMIT, st);
-  commit_kernel<<<grid, 512, 0, st>>>(p);
+  const cudaError_t e = launch_pdl(commit_kernel, grid, dim3(512), 0, st, p);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_COMMIT, st);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace eagle

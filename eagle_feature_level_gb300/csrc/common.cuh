@@ -28,6 +28,15 @@ __device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) 
   lo = f32_to_bf16(x - bf16_to_f32(hi));
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+// Kernels are launched so that the next kernel in the stream may start while
+// this one drains.  pdl_wait: block until every preceding grid has completed
+// and its memory is visible (each thread that reads a predecessor's output or
+// writes global memory passes it first); pdl_trigger: let the next grid be
+// scheduled (it still waits for this grid to complete before its reads).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---- Philox4x32-10 (Salmon et al., SC'11) -----------------------------------
 // Four 32-bit counter words, two key words, ten rounds; words 0 and 2 are
 // multiplied by the two round constants, the key is bumped by the Weyl

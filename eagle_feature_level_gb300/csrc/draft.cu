@@ -18,6 +18,8 @@ __global__ void prep_fc_kernel(const float* __restrict__ f_last, const float* __
                                const int32_t* __restrict__ token, const int32_t* __restrict__ parent,
                                const uint16_t* __restrict__ embed, int ld_embed, int d, int E, int rpr, int e0,
                                int NP, int kp, uint16_t* __restrict__ bfc) {
+  pdl_wait();      // predecessor outputs visible from here on
+  pdl_trigger();
   const int j = blockIdx.x;
   const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
   if (c0 >= 2 * d) return;
@@ -135,6 +137,8 @@ struct SelParams {
 };
 
 __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) select_kernel(const SelParams p) {
+  pdl_wait();      // predecessor outputs visible from here on
+  pdl_trigger();
   __shared__ float s_red[SEL_WARPS];
   __shared__ float s_cmax[SEL_CL], s_csum[SEL_CL];         // per-rank partials (pushed)
   __shared__ uint64_t s_ctot[SEL_CL];
@@ -377,12 +381,13 @@ cudaError_t launch_prep_fc(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st
   const eagle_dims& D = ctx->dims;
   trace_before(ctx, EAGLE_K_PREP, st);
   const dim3 grid(L.n, ceil_div(2 * D.d / 8, 128));
-  prep_fc_kernel<<<grid, 128, 0, st>>>(L.req->f_last, L.out->f_hat, L.pool->token, L.pool->parent, L.w->embed,
-                                     L.w->ld_embed, D.d, ctx->lim.max_expanded, L.rpr, L.e0, L.NP,
-                                     ctx->ws.kp_fc, ws_ptr<uint16_t>(L.ws, ctx->ws.b_fc));
+  const cudaError_t e =
+      launch_pdl(prep_fc_kernel, grid, dim3(128), 0, st, L.req->f_last, L.out->f_hat, L.pool->token, L.pool->parent,
+                 L.w->embed, L.w->ld_embed, D.d, ctx->lim.max_expanded, L.rpr, L.e0, L.NP, ctx->ws.kp_fc,
+                 ws_ptr<uint16_t>(L.ws, ctx->ws.b_fc));
   ctx->launches++;
   trace_after(ctx, EAGLE_K_PREP, st);
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_select(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st) {
@@ -403,10 +408,10 @@ cudaError_t launch_select(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st)
   p.round_id = L.s->round_id;
   p.status = ws_ptr<int>(L.ws, ctx->ws.status);
   trace_before(ctx, EAGLE_K_SELECT, st);
-  select_kernel<<<L.n * SEL_CL, SEL_THREADS, 0, st>>>(p);
+  const cudaError_t e = launch_pdl(select_kernel, dim3(L.n * SEL_CL), dim3(SEL_THREADS), 0, st, p);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_SELECT, st);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace eagle

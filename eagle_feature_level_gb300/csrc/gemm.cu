@@ -155,6 +155,25 @@ __device__ __forceinline__ void put_split(uint16_t* buf, int NP, int kp, int j, 
   buf[static_cast<size_t>(NP + j) * kp + col] = lo;
 }
 
+// RoPE angle pos * f reduced to about [-pi, pi] in fp32: f = f_hi + f_lo,
+// the product's rounding error recovered with an FMA, then Cody-Waite
+// reduction by 2 pi = C1 + C2 + C3 (Cody & Waite, "Software Manual for the
+// Elementary Functions", 1980), C1 carrying 8 significant bits so k * C1 is
+// exact for the |k| < 2^16 that positions below 2^18 can produce.
+__device__ __forceinline__ float rope_angle(int pos, float f_hi, float f_lo) {
+  constexpr float C1 = 6.28125f;
+  constexpr float C2 = 1.9353071795864769253e-3f;
+  constexpr float C3 = static_cast<float>(1.9353071795864769253e-3 - static_cast<double>(C2));
+  const float P = static_cast<float>(pos);            // exact: pos < 2^24
+  const float a = P * f_hi;
+  const float a_lo = fmaf(P, f_lo, fmaf(P, f_hi, -a));
+  const float k = rintf(a * 0.15915494309189535f);
+  float r = a - k * C1;                                // exact
+  r = fmaf(-k, C2, r);
+  r = fmaf(-k, C3, r);
+  return r + a_lo;
+}
+
 // Final epilogue of tile t: sum the partials of CTAs [c_first, c_last] and
 // apply the contraction's fused elementwise work.  `m` is the tile row this
 // thread owns (its tensor-memory lane); m >> 5 names its warp, m & 31 its
@@ -169,7 +188,7 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, i
   const int half = p.dh >> 1;
   bool rope = false, is_v = false, rot_first = false;
   int head = 0, di = 0, partner = m;
-  double inv_freq = 0.0;
+  float f_hi = 0.f, f_lo = 0.f;        // inverse frequency as an unevaluated float pair
   if (p.epi == EPI_QKV && gi < qd + 2 * kd) {
     is_v = gi >= qd + kd;
     const int base = gi < qd ? 0 : (gi < qd + kd ? qd : qd + kd);
@@ -178,17 +197,31 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, i
     rot_first = di < half;
     partner = rot_first ? m + half : m - half;
     rope = !is_v;
-    inv_freq = exp(-(2.0 * (rot_first ? di : di - half) / p.dh) * p.ln_theta);
+    const double inv_freq = exp(-(2.0 * (rot_first ? di : di - half) / p.dh) * p.ln_theta);
+    f_hi = static_cast<float>(inv_freq);
+    f_lo = static_cast<float>(inv_freq - static_cast<double>(f_hi));
   }
   for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
     const int nj = min(XCH_ROWS, p.n - jc);
-    // 1. accumulate the partials of every CTA that worked on this tile, in CTA order
+    // 1. accumulate the partials of every CTA that worked on this tile, in CTA
+    //    order; 16 rows' loads are issued together per contributing CTA
 #pragma unroll 1
-    for (int jj = 0; jj < nj; ++jj) {
-      float a = 0.f;
-      for (int c = c_first; c <= c_last; ++c)
-        a += __ldcg(p.part + (static_cast<size_t>(t + c) * p.n + jc + jj) * BM + m);
-      s.xch[jj * BM + m] = a;
+    for (int j0 = 0; j0 < nj; j0 += 16) {
+      float acc[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) acc[u] = 0.f;
+#pragma unroll 1
+      for (int c = c_first; c <= c_last; ++c) {
+        const float* src = p.part + (static_cast<size_t>(t + c) * p.n + jc + j0) * BM + m;
+        float v[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) v[u] = j0 + u < nj ? __ldcg(src + u * BM) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) acc[u] += v[u];
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (j0 + u < nj) s.xch[(j0 + u) * BM + m] = acc[u];
     }
     // 2. RMSNorm scale of the input rows (QKV: after FC, GATEUP: after O)
     if (p.epi == EPI_QKV || p.epi == EPI_GATEUP) {
@@ -236,10 +269,8 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, i
           float v = s.xch[jj * BM + m] * sc;
           if (rope) {
             const int pos = p.pos0[b] + p.depth[static_cast<size_t>(b) * p.E + e];
-            double ang = static_cast<double>(pos) * inv_freq;
-            ang -= 6.283185307179586 * rint(ang * 0.15915494309189535);
             float sn, cs;
-            sincosf(static_cast<float>(ang), &sn, &cs);
+            sincosf(rope_angle(pos, f_hi, f_lo), &sn, &cs);
             const float other = s.xch[jj * BM + partner] * sc;
             v = rot_first ? v * cs - other * sn : v * cs + other * sn;
           }
@@ -299,6 +330,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const long long u_begin = static_cast<long long>(cta) * T / G;
   const long long u_end = static_cast<long long>(cta + 1) * T / G;
   volatile int* abort_flag = s.flags;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.stages; ++i) {
@@ -336,17 +368,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long issued = 0;
-      for (long long u = u_begin; u < u_end; ++u) {
-        const int t = static_cast<int>(u / p.kb), kblk = static_cast<int>(u % p.kb);
-        if (!sm100::mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
-          *abort_flag = 1;
-          set_status(p.status, EAGLE_ERR_TIMEOUT);
-          break;
-        }
-        sm100::mbar_arrive_expect_tx(&s.full[stage], p.a_stage_bytes + p.b_stage_bytes);
-        uint8_t* a_dst = s.a + static_cast<size_t>(stage) * p.a_stage_bytes;
-        const int kz = kblk * p.kps;                 // first 64-wide k-block of the stage
-        const uint32_t group_bytes = static_cast<uint32_t>(p.kps) * 1024u;
+      const uint32_t group_bytes = static_cast<uint32_t>(p.kps) * 1024u;
+      // weight rows of unit u into ring slot st (64-row halves)
+      auto issue_a = [&](long long u, int st) {
+        const int t = static_cast<int>(u / p.kb), kz = static_cast<int>(u % p.kb) * p.kps;
+        uint8_t* a_dst = s.a + static_cast<size_t>(st) * p.a_stage_bytes;
 #pragma unroll 1
         for (int h = 0; h < 2; ++h) {
           int map, row;
@@ -354,18 +380,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t* dst = a_dst + h * 8 * group_bytes;
           if (row + 64 <= p.full_rows[map] && kz + p.kps <= p.full_kb) {
             const CUtensorMap* mp = map == 0 ? &mA0 : (map == 1 ? &mA1 : &mA2);
-            sm100::tma_load_4d(dst, mp, 0, 0, kz, row >> 3, &s.full[stage]);
+            sm100::tma_load_4d(dst, mp, 0, 0, kz, row >> 3, &s.full[st]);
           } else {                                   // row or K tail: 8-row x 64-k boxes, zero past the end
             const CUtensorMap* mp = map == 0 ? &mT0 : (map == 1 ? &mT1 : &mT2);
 #pragma unroll 1
             for (int g = 0; g < 8; ++g)
               for (int c = 0; c < p.kps; ++c)
-                sm100::tma_load_2d(dst + g * group_bytes + c * 1024, mp, (kz + c) * BK, row + 8 * g,
-                                   &s.full[stage]);
+                sm100::tma_load_2d(dst + g * group_bytes + c * 1024, mp, (kz + c) * BK, row + 8 * g, &s.full[st]);
           }
         }
-        uint8_t* b_dst = s.b + static_cast<size_t>(stage) * p.b_stage_bytes;
-        sm100::tma_load_4d(b_dst, &mB, 0, 0, kz, 0, &s.full[stage]);
+      };
+      // activation rows (the previous kernel's output) of unit u into slot st
+      auto issue_b = [&](long long u, int st) {
+        const int kz = static_cast<int>(u % p.kb) * p.kps;
+        sm100::tma_load_4d(s.b + static_cast<size_t>(st) * p.b_stage_bytes, &mB, 0, 0, kz, 0, &s.full[st]);
+      };
+      // The first ring's worth of weights does not depend on the previous
+      // kernel: it streams while that kernel drains.
+      const long long n_pre = min(static_cast<long long>(p.stages), u_end - u_begin);
+      for (long long i = 0; i < n_pre; ++i) {
+        sm100::mbar_arrive_expect_tx(&s.full[i], p.a_stage_bytes + p.b_stage_bytes);
+        issue_a(u_begin + i, static_cast<int>(i));
+      }
+      pdl_wait();
+      for (long long i = 0; i < n_pre; ++i) issue_b(u_begin + i, static_cast<int>(i));
+      issued = n_pre;
+      stage = static_cast<int>(n_pre % p.stages);
+      phase = n_pre == p.stages ? 1u : 0u;
+      for (long long u = u_begin + n_pre; u < u_end; ++u) {
+        if (!sm100::mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
+          *abort_flag = 1;
+          set_status(p.status, EAGLE_ERR_TIMEOUT);
+          break;
+        }
+        sm100::mbar_arrive_expect_tx(&s.full[stage], p.a_stage_bytes + p.b_stage_bytes);
+        issue_a(u, stage);
+        issue_b(u, stage);
         ++issued;
         if (++stage == p.stages) { stage = 0; phase ^= 1u; }
       }
@@ -440,6 +490,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
+    pdl_wait();                                 // residuals, norms, positions of earlier kernels
     const int et = threadIdx.x - 64;            // 0..127
     const int quarter = warp & 3;               // tensor-memory lanes this warp may read
     const int m = quarter * 32 + lane;          // tile row held by this thread
@@ -668,11 +719,11 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   int grid = ctx->sm_count;
   if (p.total_units < grid) grid = static_cast<int>(p.total_units);
   trace_before(ctx, epi, st);
-  gemm_stream_kernel<<<grid, NUM_THREADS, smem, st>>>(maps[0], maps[1], maps[2], tails[0], tails[1], tails[2],
-                                                     mb, p);
+  const cudaError_t e = launch_pdl(gemm_stream_kernel, dim3(grid), dim3(NUM_THREADS), smem, st, maps[0], maps[1],
+                                   maps[2], tails[0], tails[1], tails[2], mb, p);
   ctx->launches++;
   trace_after(ctx, epi, st);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace eagle

@@ -6,6 +6,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <vector>
 
 #include "../../include/eagle.h"
@@ -71,6 +72,26 @@ struct eagle_ctx {
 };
 
 namespace eagle {
+
+// Every kernel of the library is launched with programmatic stream
+// serialization: the next kernel in the stream may be scheduled while this
+// one drains, and waits in-kernel (griddepcontrol.wait) before touching what
+// its predecessor wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launch bookkeeping: optional CUDA-event trace around kernels of one class.
 void trace_before(eagle_ctx* ctx, int kernel_id, cudaStream_t s);

@@ -57,6 +57,8 @@ __device__ __forceinline__ bool before(double va, int da, int ca, double vb, int
 }
 
 __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) {
+  pdl_wait();      // predecessor outputs visible from here on
+  pdl_trigger();
   __shared__ double s_val[MAX_POOL];
   __shared__ int s_dep[MAX_POOL];
   __shared__ int s_rank[MAX_POOL];
@@ -295,10 +297,10 @@ cudaError_t launch_tree(eagle_ctx* ctx, const eagle_plan* plan, int phase, int l
   }
   p.status = status;
   trace_before(ctx, EAGLE_K_TREE, st);
-  tree_kernel<<<batch, TREE_THREADS, 0, st>>>(p);
+  const cudaError_t e = launch_pdl(tree_kernel, dim3(batch), dim3(TREE_THREADS), 0, st, p);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_TREE, st);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace eagle
