@@ -145,6 +145,156 @@ __device__ __forceinline__ void tree_stage(const AttnParams& p, float* sk, float
   }
 }
 
+// Per-CTA constants of one attention launch, shared by the pass bodies.
+struct PassCtx {
+  int b, h, warp, lane, dh, ld, lo, hi, rec, split, dcol;
+  bool is_tree, has_cols;
+  size_t row_stride;
+  float *sk, *sv, *sq, *sp;
+  uint64_t* s_mask;
+};
+
+// One pass over this CTA's keys for query rows r0 .. r0 + rp - 1; warp w owns
+// rows w + 8 i, i < nr <= NR.  The kernel is instantiated for NR = 1, 2, 4, 8
+// (chosen from the launch's rows per pass) so that a warp issues work only
+// for row slots that can exist: with one query row per warp the unrolled
+// code of eight would cost eight times the issue slots.
+template <int NR>
+__device__ __forceinline__ void attn_pass(const AttnParams& p, const PassCtx& x, int r0, int rp) {
+  const int b = x.b, h = x.h, warp = x.warp, lane = x.lane, dh = x.dh, ld = x.ld, lo = x.lo, hi = x.hi;
+  const int rec = x.rec, split = x.split, dcol = x.dcol;
+  const bool is_tree = x.is_tree, has_cols = x.has_cols;
+  const size_t row_stride = x.row_stride;
+  float *sk = x.sk, *sv = x.sv, *sq = x.sq, *sp = x.sp;
+  uint64_t* s_mask = x.s_mask;
+  const int nr = rp > warp ? (rp - warp + WARPS - 1) / WARPS : 0;   // <= NR
+  __syncthreads();                         // previous pass done with sq
+  for (int idx = threadIdx.x; idx < rp * (dh >> 2); idx += THREADS) {
+    const int rr = idx / (dh >> 2), c = idx - rr * (dh >> 2);
+    const int r = r0 + rr, node = r / p.G, hq = h * p.G + r % p.G;
+    const size_t qo = q_index(p, b, node, hq) + 4 * c;
+    float4 v;
+    if (p.mode == 0) {
+      v = *reinterpret_cast<const float4*>(p.q_f32 + qo);
+    } else {
+      const uint2 w = *reinterpret_cast<const uint2*>(p.q_bf16 + qo);
+      v.x = __uint_as_float(w.x << 16); v.y = __uint_as_float(w.x & 0xffff0000u);
+      v.z = __uint_as_float(w.y << 16); v.w = __uint_as_float(w.y & 0xffff0000u);
+    }
+    *reinterpret_cast<float4*>(sq + rr * dh + 4 * c) = v;
+  }
+  if (is_tree && lane < RW && lane < nr)
+    s_mask[warp * RW + lane] = row_mask(p, b, (r0 + warp + WARPS * lane) / p.G);
+  float m_run[NR], l_run[NR], acc[NR][4];
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    m_run[i] = -INFINITY;
+    l_run[i] = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
+  }
+
+  PrefixTile pre;
+  if (!is_tree && lo < hi)
+    prefix_load(pre, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + lo) * p.Hkv + h) * dh, row_stride,
+                min(TILE, hi - lo), dh);
+  for (int t0 = lo; t0 < hi; t0 += TILE) {
+    const int nt = min(TILE, hi - t0);
+    __syncthreads();                       // all warps done with the previous tile
+    if (!is_tree) {
+      prefix_store(pre, sk, sv, ld, dh);
+      if (t0 + TILE < hi)                  // next tile's loads fly while this one is consumed
+        prefix_load(pre, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + t0 + TILE) * p.Hkv + h) * dh,
+                    row_stride, min(TILE, hi - t0 - TILE), dh);
+    } else {
+      tree_stage(p, sk, sv, ld, ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh, row_stride, nt);
+    }
+    __syncthreads();
+    if (nr == 0) continue;
+
+    // scores of keys lane and lane + 32 for each owned row
+    float s0[NR], s1[NR];
+#pragma unroll
+    for (int i = 0; i < NR; ++i) { s0[i] = 0.f; s1[i] = 0.f; }
+    const float* k0 = sk + lane * ld;
+    const float* k1 = sk + (lane + 32) * ld;
+    for (int d = 0; d < dh; d += 4) {
+      const float4 a = *reinterpret_cast<const float4*>(k0 + d);
+      const float4 c = *reinterpret_cast<const float4*>(k1 + d);
+#pragma unroll
+      for (int i = 0; i < NR; ++i) {
+        if (i < nr) {
+          const float4 q = *reinterpret_cast<const float4*>(sq + (warp + WARPS * i) * dh + d);
+          s0[i] += fmaf(q.x, a.x, q.y * a.y) + fmaf(q.z, a.z, q.w * a.w);
+          s1[i] += fmaf(q.x, c.x, q.y * c.y) + fmaf(q.z, c.z, q.w * c.w);
+        }
+      }
+    }
+    // online softmax per row; probabilities to this warp's shared rows
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      if (i < nr) {
+        // tree keys: one tile (t0 == 0), bit j of the row's ancestor mask
+        const uint64_t mask = is_tree ? s_mask[warp * RW + i] : ~0ull;
+        const bool v0 = lane < nt && ((mask >> lane) & 1ull);
+        const bool v1 = lane + 32 < nt && ((mask >> (lane + 32)) & 1ull);
+        const float a = v0 ? s0[i] * p.scale : -INFINITY;
+        const float c = v1 ? s1[i] * p.scale : -INFINITY;
+        const float m_new = fmaxf(m_run[i], warp_max(fmaxf(a, c)));
+        float p0 = 0.f, p1 = 0.f, corr = 1.f;
+        if (m_new != -INFINITY) {
+          p0 = __expf(a - m_new);
+          p1 = __expf(c - m_new);
+          corr = __expf(m_run[i] - m_new);
+        }
+        l_run[i] = l_run[i] * corr + warp_sum(p0 + p1);
+        m_run[i] = m_new;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) acc[i][c4] *= corr;
+        sp[i * TILE + lane] = p0;
+        sp[i * TILE + lane + 32] = p1;
+      }
+    }
+    __syncwarp();
+    // acc += P V over the tile, 4 keys per step (V rows past nt are zero)
+    if (has_cols) {
+      for (int j = 0; j < nt; j += 4) {
+        float4 vv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) vv[u] = *reinterpret_cast<const float4*>(sv + (j + u) * ld + dcol);
+#pragma unroll
+        for (int i = 0; i < NR; ++i) {
+          if (i < nr) {
+            const float4 pj = *reinterpret_cast<const float4*>(sp + i * TILE + j);
+            acc[i][0] = fmaf(pj.x, vv[0].x, fmaf(pj.y, vv[1].x, fmaf(pj.z, vv[2].x, fmaf(pj.w, vv[3].x, acc[i][0]))));
+            acc[i][1] = fmaf(pj.x, vv[0].y, fmaf(pj.y, vv[1].y, fmaf(pj.z, vv[2].y, fmaf(pj.w, vv[3].y, acc[i][1]))));
+            acc[i][2] = fmaf(pj.x, vv[0].z, fmaf(pj.y, vv[1].z, fmaf(pj.z, vv[2].z, fmaf(pj.w, vv[3].z, acc[i][2]))));
+            acc[i][3] = fmaf(pj.x, vv[0].w, fmaf(pj.y, vv[1].w, fmaf(pj.z, vv[2].w, fmaf(pj.w, vv[3].w, acc[i][3]))));
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    if (i < nr) {
+      const int r = r0 + warp + WARPS * i;
+      const int node = r / p.G, hq = h * p.G + r % p.G;
+      const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
+      float* dst = p.part + (qi * (p.n_splits + 1) + split) * rec;
+      if (lane == 0) {
+        dst[0] = m_run[i];
+        dst[1] = l_run[i];
+      }
+      if (has_cols) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dst[2 + dcol + c] = acc[i][c];
+      }
+    }
+  }
+}
+
 // Dynamic shared memory: K tile, V tile ([TILE][dh+4] fp32 each; the 4-word
 // pad makes lane-per-row float4 reads conflict-free), the pass's query rows
 // [rows_pass][dh] and each warp's probabilities [WARPS][RW][TILE].
@@ -153,6 +303,7 @@ __device__ __forceinline__ void tree_stage(const AttnParams& p, float* sk, float
 // (lane = keys lane and lane + 32), runs the online softmax and accumulates
 // P V for them (lane = 4 output columns), so after the tile is staged no
 // further block-wide barrier is needed.
+template <int NR>
 __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams p) {
   pdl_wait();      // predecessor outputs visible from here on
   pdl_trigger();
@@ -186,135 +337,10 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams 
   const int dcol = 4 * lane;                 // this lane's output columns
   const bool has_cols = dcol < dh;
 
+  const PassCtx x{b, h, warp, lane, dh, ld, lo, hi, rec, split, dcol, is_tree, has_cols, row_stride,
+                  sk, sv, sq, sp, s_mask};
   for (int r0 = 0; r0 < R; r0 += p.rows_pass) {
-    const int rp = min(p.rows_pass, R - r0);
-    // rows of this warp in the pass: w, w + 8, ... < rp
-    const int nr = rp > warp ? (rp - warp + WARPS - 1) / WARPS : 0;
-    __syncthreads();                         // previous pass done with sq
-    for (int idx = threadIdx.x; idx < rp * (dh >> 2); idx += THREADS) {
-      const int rr = idx / (dh >> 2), c = idx - rr * (dh >> 2);
-      const int r = r0 + rr, node = r / p.G, hq = h * p.G + r % p.G;
-      const size_t qo = q_index(p, b, node, hq) + 4 * c;
-      float4 v;
-      if (p.mode == 0) {
-        v = *reinterpret_cast<const float4*>(p.q_f32 + qo);
-      } else {
-        const uint2 w = *reinterpret_cast<const uint2*>(p.q_bf16 + qo);
-        v.x = __uint_as_float(w.x << 16); v.y = __uint_as_float(w.x & 0xffff0000u);
-        v.z = __uint_as_float(w.y << 16); v.w = __uint_as_float(w.y & 0xffff0000u);
-      }
-      *reinterpret_cast<float4*>(sq + rr * dh + 4 * c) = v;
-    }
-    if (is_tree && lane < RW && lane < nr)
-      s_mask[warp * RW + lane] = row_mask(p, b, (r0 + warp + WARPS * lane) / p.G);
-    float m_run[RW], l_run[RW], acc[RW][4];
-#pragma unroll
-    for (int i = 0; i < RW; ++i) {
-      m_run[i] = -INFINITY;
-      l_run[i] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
-    }
-
-    PrefixTile pre;
-    if (!is_tree && lo < hi)
-      prefix_load(pre, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + lo) * p.Hkv + h) * dh, row_stride,
-                  min(TILE, hi - lo), dh);
-    for (int t0 = lo; t0 < hi; t0 += TILE) {
-      const int nt = min(TILE, hi - t0);
-      __syncthreads();                       // all warps done with the previous tile
-      if (!is_tree) {
-        prefix_store(pre, sk, sv, ld, dh);
-        if (t0 + TILE < hi)                  // next tile's loads fly while this one is consumed
-          prefix_load(pre, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + t0 + TILE) * p.Hkv + h) * dh,
-                      row_stride, min(TILE, hi - t0 - TILE), dh);
-      } else {
-        tree_stage(p, sk, sv, ld, ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh, row_stride, nt);
-      }
-      __syncthreads();
-      if (nr == 0) continue;
-
-      // scores of keys lane and lane + 32 for each owned row
-      float s0[RW], s1[RW];
-#pragma unroll
-      for (int i = 0; i < RW; ++i) { s0[i] = 0.f; s1[i] = 0.f; }
-      const float* k0 = sk + lane * ld;
-      const float* k1 = sk + (lane + 32) * ld;
-      for (int d = 0; d < dh; d += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(k0 + d);
-        const float4 c = *reinterpret_cast<const float4*>(k1 + d);
-#pragma unroll
-        for (int i = 0; i < RW; ++i) {
-          if (i < nr) {
-            const float4 q = *reinterpret_cast<const float4*>(sq + (warp + WARPS * i) * dh + d);
-            s0[i] += fmaf(q.x, a.x, q.y * a.y) + fmaf(q.z, a.z, q.w * a.w);
-            s1[i] += fmaf(q.x, c.x, q.y * c.y) + fmaf(q.z, c.z, q.w * c.w);
-          }
-        }
-      }
-      // online softmax per row; probabilities to this warp's shared rows
-#pragma unroll
-      for (int i = 0; i < RW; ++i) {
-        if (i < nr) {
-          // tree keys: one tile (t0 == 0), bit j of the row's ancestor mask
-          const uint64_t mask = is_tree ? s_mask[warp * RW + i] : ~0ull;
-          const bool v0 = lane < nt && ((mask >> lane) & 1ull);
-          const bool v1 = lane + 32 < nt && ((mask >> (lane + 32)) & 1ull);
-          const float a = v0 ? s0[i] * p.scale : -INFINITY;
-          const float c = v1 ? s1[i] * p.scale : -INFINITY;
-          const float m_new = fmaxf(m_run[i], warp_max(fmaxf(a, c)));
-          float p0 = 0.f, p1 = 0.f, corr = 1.f;
-          if (m_new != -INFINITY) {
-            p0 = __expf(a - m_new);
-            p1 = __expf(c - m_new);
-            corr = __expf(m_run[i] - m_new);
-          }
-          l_run[i] = l_run[i] * corr + warp_sum(p0 + p1);
-          m_run[i] = m_new;
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) acc[i][c4] *= corr;
-          sp[i * TILE + lane] = p0;
-          sp[i * TILE + lane + 32] = p1;
-        }
-      }
-      __syncwarp();
-      // acc += P V over the tile, 4 keys per step (V rows past nt are zero)
-      if (has_cols) {
-        for (int j = 0; j < nt; j += 4) {
-          float4 vv[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) vv[u] = *reinterpret_cast<const float4*>(sv + (j + u) * ld + dcol);
-#pragma unroll
-          for (int i = 0; i < RW; ++i) {
-            if (i < nr) {
-              const float4 pj = *reinterpret_cast<const float4*>(sp + i * TILE + j);
-              acc[i][0] = fmaf(pj.x, vv[0].x, fmaf(pj.y, vv[1].x, fmaf(pj.z, vv[2].x, fmaf(pj.w, vv[3].x, acc[i][0]))));
-              acc[i][1] = fmaf(pj.x, vv[0].y, fmaf(pj.y, vv[1].y, fmaf(pj.z, vv[2].y, fmaf(pj.w, vv[3].y, acc[i][1]))));
-              acc[i][2] = fmaf(pj.x, vv[0].z, fmaf(pj.y, vv[1].z, fmaf(pj.z, vv[2].z, fmaf(pj.w, vv[3].z, acc[i][2]))));
-              acc[i][3] = fmaf(pj.x, vv[0].w, fmaf(pj.y, vv[1].w, fmaf(pj.z, vv[2].w, fmaf(pj.w, vv[3].w, acc[i][3]))));
-            }
-          }
-        }
-      }
-      __syncwarp();
-    }
-#pragma unroll
-    for (int i = 0; i < RW; ++i) {
-      if (i < nr) {
-        const int r = r0 + warp + WARPS * i;
-        const int node = r / p.G, hq = h * p.G + r % p.G;
-        const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
-        float* dst = p.part + (qi * (p.n_splits + 1) + split) * rec;
-        if (lane == 0) {
-          dst[0] = m_run[i];
-          dst[1] = l_run[i];
-        }
-        if (has_cols) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) dst[2 + dcol + c] = acc[i][c];
-        }
-      }
-    }
+    attn_pass<NR>(p, x, r0, min(p.rows_pass, R - r0));
   }
 
   // the last CTA of this (request, kv head) merges the splits in order
@@ -382,12 +408,27 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams 
 
 int attn_splits(const eagle_ctx* ctx, int pairs, int cap) {
   const int tiles = ceil_div(cap < 1 ? 1 : cap, TILE);
-  int want = ceil_div(2 * ctx->sm_count, pairs < 1 ? 1 : pairs);
+  // one wave at two CTAs per SM, the tree part's CTA included
+  int want = 2 * ctx->sm_count / (pairs < 1 ? 1 : pairs) - 1;
   if (want > tiles) want = tiles;
   if (want > 31) want = 31;        // n_splits + 1 records fit one warp in the merge
   if (want < 1) want = 1;
   const int per = ceil_div(tiles, want);
   return ceil_div(tiles, per);     // every split non-empty at full length
+}
+
+template <int NR>
+static cudaError_t launch_attn_nr(const AttnParams& p, dim3 grid, size_t smem, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const size_t most = (static_cast<size_t>(2) * TILE * (MAX_DH + 4) + static_cast<size_t>(ROWS_PASS) * MAX_DH +
+                         static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(most));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_pdl(tree_attn_kernel<NR>, grid, dim3(THREADS), smem, st, p);
 }
 
 static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
@@ -397,17 +438,13 @@ static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaSt
   dim3 grid(p.n_splits + 1, p.B * p.Hkv);
   const size_t smem = (static_cast<size_t>(2) * TILE * (p.dh + 4) + static_cast<size_t>(p.rows_pass) * p.dh +
                        static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    const size_t most = (static_cast<size_t>(2) * TILE * (MAX_DH + 4) + static_cast<size_t>(ROWS_PASS) * MAX_DH +
-                         static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(most));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const int per_warp = ceil_div(p.rows_pass, WARPS);
   trace_before(ctx, kernel_id, st);
-  const cudaError_t e = launch_pdl(tree_attn_kernel, grid, dim3(THREADS), smem, st, p);
+  cudaError_t e;
+  if (per_warp <= 1) e = launch_attn_nr<1>(p, grid, smem, st);
+  else if (per_warp <= 2) e = launch_attn_nr<2>(p, grid, smem, st);
+  else if (per_warp <= 4) e = launch_attn_nr<4>(p, grid, smem, st);
+  else e = launch_attn_nr<RW>(p, grid, smem, st);
   ctx->launches++;
   trace_after(ctx, kernel_id, st);
   return e;

@@ -44,6 +44,7 @@ constexpr int KBLK_BYTES = BK * 2;
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
 constexpr int XCH_ROWS = 32;
+constexpr int STG_FLOATS = XCH_ROWS * BM;   // finalize staging: 32 rows of a tile
 
 struct GemmParams {
   int epi;
@@ -92,13 +93,15 @@ struct Smem {
   float* xch;       // [32][128]
   float* red;       // [4][32]
   float* rs;        // [32]
+  int* rowi;        // [32]
+  float* stg;       // [STG_FLOATS], 16-byte aligned
 };
 
 __host__ __device__ inline size_t smem_bytes_for(int stages, uint32_t a_stage, uint32_t b_stage) {
   size_t s = 1024;                                  // alignment slack
   s += static_cast<size_t>(stages) * (a_stage + b_stage);
   s += (2 * stages + 4) * 8 + 64;
-  s += XCH_ROWS * BM * 4 + 4 * 32 * 4 + 32 * 4;
+  s += XCH_ROWS * BM * 4 + 4 * 32 * 4 + 32 * 4 + 32 * 4 + STG_FLOATS * 4;
   return s;
 }
 
@@ -119,6 +122,8 @@ __device__ inline Smem carve(uint8_t* raw, const GemmParams& p) {
   s.xch = reinterpret_cast<float*>(s.flags + 12);
   s.red = s.xch + XCH_ROWS * BM;
   s.rs = s.red + 4 * 32;
+  s.rowi = reinterpret_cast<int*>(s.rs + 32);
+  s.stg = reinterpret_cast<float*>(s.rowi + 32);
   return s;
 }
 
@@ -174,15 +179,31 @@ __device__ __forceinline__ float rope_angle(int pos, float f_hi, float f_lo) {
   return r + a_lo;
 }
 
+// 16-byte global -> shared copies that bypass L1 (the sources are rewritten
+// by other CTAs and kernels), issued without waiting.
+__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm100::smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// The 128 epilogue threads copy n contiguous floats (n % 4 == 0, both ends
+// 16-byte aligned) into shared memory.
+__device__ __forceinline__ void stage_block(float* dst, const float* src, int n, int et) {
+  for (int i = 4 * et; i < n; i += 4 * EPI_THREADS) cp_async16(dst + i, src + i);
+}
+
 // Final epilogue of tile t: sum the partials of CTAs [c_first, c_last] and
 // apply the contraction's fused elementwise work.  `m` is the tile row this
-// thread owns (its tensor-memory lane); m >> 5 names its warp, m & 31 its
-// lane.  Runs once per tile, so it is written as compact loops over shared
-// memory (small code, few instruction-cache misses) rather than unrolled.
+// thread owns (its tensor-memory lane).  It runs once per tile, cold, at the
+// end of the stream, so both its instruction footprint and its chain of
+// memory latencies are on the kernel's critical path: every global input of
+// a 32-row chunk is brought into shared memory by asynchronous copies issued
+// from compact loops (many in flight, one wait), then the per-row loops read
+// shared memory only.
 __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, int t, int c_first, int c_last,
                                            int m) {
-  const int lane = m & 31, w = m >> 5;
-  // per-row constants of this thread's output index
+  const int et = m;                    // epilogue thread index == tile row
+  // per-column constants of this thread's output index
   int gi = t * BM + m;
   const int qd = p.Hq * p.dh, kd = p.Hkv * p.dh;
   const int half = p.dh >> 1;
@@ -201,64 +222,101 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, i
     f_hi = static_cast<float>(inv_freq);
     f_lo = static_cast<float>(inv_freq - static_cast<double>(f_hi));
   }
+  const bool d_col = gi < p.d;
+  float col_bias = 0.f, col_gain = 0.f;
+  if (p.epi == EPI_FC && d_col) { col_bias = p.bias[gi]; col_gain = p.gain[gi]; }
+  if (p.epi == EPI_O && d_col) col_gain = p.gain[gi];
+  const int C = c_last - c_first + 1;
   for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
     const int nj = min(XCH_ROWS, p.n - jc);
-    // 1. accumulate the partials of every CTA that worked on this tile, in CTA
-    //    order; 16 rows' loads are issued together per contributing CTA
+    // 1. partials of the contributing CTAs (each one contiguous block of nj
+    //    rows), as many CTAs per batch as the staging area holds; summed in
+    //    CTA order
+    const int cb = max(1, XCH_ROWS / nj);
 #pragma unroll 1
-    for (int j0 = 0; j0 < nj; j0 += 16) {
-      float acc[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) acc[u] = 0.f;
+    for (int c0 = 0; c0 < C; c0 += cb) {
+      const int cn = min(cb, C - c0);
 #pragma unroll 1
-      for (int c = c_first; c <= c_last; ++c) {
-        const float* src = p.part + (static_cast<size_t>(t + c) * p.n + jc + j0) * BM + m;
-        float v[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) v[u] = j0 + u < nj ? __ldcg(src + u * BM) : 0.f;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) acc[u] += v[u];
+      for (int c = 0; c < cn; ++c)
+        stage_block(s.stg + c * nj * BM, p.part + (static_cast<size_t>(t + c_first + c0 + c) * p.n + jc) * BM,
+                    nj * BM, et);
+      cp_async_wait_all();
+      sm100::named_barrier(1, EPI_THREADS);
+#pragma unroll 1
+      for (int jj = 0; jj < nj; ++jj) {
+        float a = c0 == 0 ? s.stg[jj * BM + m] : s.xch[jj * BM + m] + s.stg[jj * BM + m];
+#pragma unroll 1
+        for (int c = 1; c < cn; ++c) a += s.stg[(c * nj + jj) * BM + m];
+        s.xch[jj * BM + m] = a;
       }
-#pragma unroll
-      for (int u = 0; u < 16; ++u)
-        if (j0 + u < nj) s.xch[(j0 + u) * BM + m] = acc[u];
+      sm100::named_barrier(1, EPI_THREADS);
     }
-    // 2. RMSNorm scale of the input rows (QKV: after FC, GATEUP: after O)
-    if (p.epi == EPI_QKV || p.epi == EPI_GATEUP) {
-      if (m < nj) {
-        const float* ss = p.ss_in + static_cast<size_t>(jc + m) * p.ss_in_tiles;
-        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-        int i = 0;
-        for (; i + 4 <= p.ss_in_tiles; i += 4) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) acc4[u] += __ldcg(ss + i + u);
-        }
-        for (; i < p.ss_in_tiles; ++i) acc4[0] += __ldcg(ss + i);
-        const float tot = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-        s.rs[m] = 1.0f / sqrtf(tot / static_cast<float>(p.d) + p.eps);
+    // 2. row inputs written by earlier kernels, staged the same way
+    const int tiles = p.ss_in_tiles;
+    if (p.epi == EPI_O || p.epi == EPI_DOWN) {                      // residual rows, this tile's columns
+      const int ncol = min(BM, p.d - t * BM);                         // a multiple of 64
+      for (int i = et; i < nj * (BM / 4); i += EPI_THREADS) {
+        const int r = i / (BM / 4), q = 4 * (i % (BM / 4));
+        if (q < ncol) cp_async16(s.stg + r * BM + q, p.resid + static_cast<size_t>(jc + r) * p.d + t * BM + q);
       }
+    } else if (p.epi == EPI_QKV || p.epi == EPI_GATEUP) {           // norm partials of rows jc..jc+nj-1
+      const float* ss = p.ss_in + static_cast<size_t>(jc) * tiles;
+      if (tiles % 4 == 0) {
+        stage_block(s.stg, ss, nj * tiles, et);
+      } else {
+        for (int i = et; i < nj * tiles; i += EPI_THREADS) s.stg[i] = __ldcg(ss + i);
+      }
+      if (p.epi == EPI_QKV && m < nj) {
+        const int j = jc + m, b = j / p.rpr, e = p.e0 + j % p.rpr;
+        s.rowi[m] = p.pos0[b] + p.depth[static_cast<size_t>(b) * p.E + e];
+      }
+    }
+    cp_async_wait_all();
+    sm100::named_barrier(1, EPI_THREADS);
+    if ((p.epi == EPI_O || p.epi == EPI_DOWN) && d_col) {
+#pragma unroll 1
+      for (int jj = 0; jj < nj; ++jj) s.xch[jj * BM + m] += s.stg[jj * BM + m];
+    }
+    if ((p.epi == EPI_QKV || p.epi == EPI_GATEUP) && m < nj) {      // RMSNorm scale of input row jc + m
+      const float* ss = s.stg + m * tiles;
+      float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+      int i = 0;
+#pragma unroll 1
+      for (; i + 4 <= tiles; i += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc4[u] += ss[i + u];
+      }
+#pragma unroll 1
+      for (; i < tiles; ++i) acc4[0] += ss[i];
+      const float tot = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+      s.rs[m] = 1.0f / sqrtf(tot / static_cast<float>(p.d) + p.eps);
     }
     sm100::named_barrier(1, EPI_THREADS);
     // 3. the contraction's elementwise epilogue, one activation row at a time
     if (p.epi == EPI_FC || p.epi == EPI_O) {
-      const bool valid = gi < p.d;
 #pragma unroll 1
       for (int jj = 0; jj < nj; ++jj) {
         const int j = jc + jj;
         float v = 0.f;
-        if (valid) {
-          v = s.xch[jj * BM + m];
-          v += p.epi == EPI_FC ? p.bias[gi] : p.resid[static_cast<size_t>(j) * p.d + gi];
+        if (d_col) {
+          v = s.xch[jj * BM + m] + col_bias;
           p.out_f32[static_cast<size_t>(j) * p.d + gi] = v;
-          put_split(p.bnext, p.NP, p.kp_next, j, gi, v * p.gain[gi]);
+          put_split(p.bnext, p.NP, p.kp_next, j, gi, v * col_gain);
         }
-        const float sq = warp_sum(v * v);
-        if (lane == 0) s.red[w * 32 + jj] = sq;
+        s.xch[jj * BM + m] = v;
       }
       sm100::named_barrier(1, EPI_THREADS);
-      if (m < nj)
-        p.ss_out[static_cast<size_t>(jc + m) * p.m_tiles + t] =
-            (s.red[m] + s.red[32 + m]) + (s.red[64 + m] + s.red[96 + m]);
+      // sum of squares of the tile's columns of row jc + m (next RMSNorm);
+      // the rotated start keeps the threads on distinct banks
+      if (m < nj) {
+        float sq = 0.f;
+#pragma unroll 4
+        for (int k = 0; k < BM; ++k) {
+          const float x = s.xch[m * BM + ((k + m) & (BM - 1))];
+          sq = fmaf(x, x, sq);
+        }
+        p.ss_out[static_cast<size_t>(jc + m) * p.m_tiles + t] = sq;
+      }
     } else if (p.epi == EPI_QKV) {
       if (gi < qd + 2 * kd) {
 #pragma unroll 1
@@ -268,9 +326,8 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, i
           const float sc = s.rs[jj];
           float v = s.xch[jj * BM + m] * sc;
           if (rope) {
-            const int pos = p.pos0[b] + p.depth[static_cast<size_t>(b) * p.E + e];
             float sn, cs;
-            sincosf(rope_angle(pos, f_hi, f_lo), &sn, &cs);
+            sincosf(rope_angle(s.rowi[jj], f_hi, f_lo), &sn, &cs);
             const float other = s.xch[jj * BM + partner] * sc;
             v = rot_first ? v * cs - other * sn : v * cs + other * sn;
           }
@@ -293,12 +350,12 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, i
         }
       }
     } else if (p.epi == EPI_DOWN) {
-      if (gi < p.d) {
+      if (d_col) {
 #pragma unroll 1
         for (int jj = 0; jj < nj; ++jj) {
           const int j = jc + jj;
           const int b = j / p.rpr, e = p.e0 + j % p.rpr;
-          const float v = s.xch[jj * BM + m] + p.resid[static_cast<size_t>(j) * p.d + gi];
+          const float v = s.xch[jj * BM + m];
           p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.d + gi] = v;
           put_split(p.bnext, p.NP, p.kp_next, j, gi, v);
         }
