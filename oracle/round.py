@@ -113,7 +113,7 @@ def draft_tree(W, w, b: int, inp: dict) -> (RequestDraft, T.Tree):
         tpl = T.template(w.tree)
         draft_step(W, w, st, [0], k=tpl.k_max, **args)
         for depth in range(1, max(tpl.depth)):
-            rows = T.static_frontier(st.ex, st.child_tok, tpl, depth)
+            rows = T.static_frontier(st.ex, st.child_tok, tpl, depth, st.child_q)
             draft_step(W, w, st, rows, k=tpl.k_max, **args)
         tr = T.static_final(st.ex, st.child_tok, tpl)
     return st, tr

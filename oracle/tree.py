@@ -127,9 +127,12 @@ def eagle2_frontier(ex: Expanded, child_tok, child_q, prev: Sequence[int], k: in
     return new
 
 
-def static_frontier(ex: Expanded, child_tok, tpl: Template, depth: int) -> List[int]:
+def static_frontier(ex: Expanded, child_tok, tpl: Template, depth: int, child_q=None) -> List[int]:
     """Expansion step of a static template: the template's nodes at ``depth``
-    that have children become expanded nodes, in template order."""
+    that have children become expanded nodes, in template order.  A node's
+    value is the product of the draft confidences along its path (Page A
+    §10.3 defines it for every tree node; a static template does not select
+    by it); without ``child_q`` values stay 1."""
     # map template node -> expanded slot of its parent
     new = []
     for i in range(len(tpl.paths)):
@@ -137,7 +140,8 @@ def static_frontier(ex: Expanded, child_tok, tpl: Template, depth: int) -> List[
             continue
         par_e = 0 if tpl.parent[i] < 0 else tpl.exp_slot[tpl.parent[i]]
         tok = child_tok[par_e][tpl.rank[i]]
-        e = ex.add(tok, par_e, tpl.rank[i], depth, 1.0)
+        value = 1.0 if child_q is None else ex.value[par_e] * float(child_q[par_e][tpl.rank[i]])
+        e = ex.add(tok, par_e, tpl.rank[i], depth, value)
         assert e == tpl.exp_slot[i]
         new.append(e)
     return new

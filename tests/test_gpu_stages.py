@@ -1,0 +1,191 @@
+"""Stage parity on identical inputs: the GPU tree construction (root,
+EAGLE-2 frontier / static expansion, rerank and flatten) and the acceptance
+walk (greedy and recursive multi-candidate rejection) against the oracle,
+both fed the same seeded fp32 confidences and probabilities.  With the same
+inputs every discrete result is fixed, so everything is compared bit-exact:
+pool tokens, parents, depths and fp64 values, the flattened tree, the
+ancestor masks, and accept lengths, paths and final tokens.  No near-tie
+allowance applies here.
+
+Confidences are drawn on a coarse grid (multiples of 1/8, 1 included) so
+that equal node values -- across siblings, parents and depths -- are common
+and the tie-break order (value, depth, parent slot, draw rank) is exercised."""
+import numpy as np
+import pytest
+import torch
+
+import eagle_synth as S
+from eagle_feature_level_gb300 import _binding as B
+from eagle_feature_level_gb300.runtime import _p
+from eagle_feature_level_gb300.workload import make_round
+from oracle import tree as T
+from oracle import verify as Vf
+
+pytestmark = pytest.mark.gpu
+
+_SMALL = dict(d=128, n_q_heads=2, n_kv_heads=2, head_dim=64, d_ff=344, vocab=1000, batch=4, prefix_len=64,
+              prefix_range=None, weight_std=0.05)
+CASES = {
+    "eagle2_k10_d6_m60": S.variant("7b_eagle2", name="stage_eagle2_k10", temps=(0.0, 1.0, 0.0, 0.7), **_SMALL),
+    "eagle2_k4_d4_m12": S.variant("7b_eagle2", name="stage_eagle2_k4", top_k=4, depth=4, top_m=12,
+                                  temps=(1.0, 0.0), **_SMALL),
+    "static26": S.variant("7b_static26", name="stage_static26", temps=(0.0, 1.0), **_SMALL),
+    "chain4": S.variant("7b_static26", name="stage_chain4", tree="chain4", top_k=1, depth=4, top_m=4,
+                        temps=(0.0, 1.0), **_SMALL),
+}
+
+
+def _uniform(shape, seed, name):
+    x = S.random_tensor(shape, seed, name).double()
+    return (0.5 * (1.0 + torch.erf(x / np.sqrt(2.0)))).numpy()
+
+
+def _children(w, seed, Bn, E, K, V):
+    """Drawn children: k distinct tokens per expanded slot in draw order,
+    fp32 confidences on the 1/8 grid, some lists cut short by -1."""
+    keys = S.random_tensor((Bn, E, V), seed, "stage_child_keys").numpy()
+    tok = np.argsort(keys, axis=-1, kind="stable")[..., :K].astype(np.int32)
+    q = ((np.floor(_uniform((Bn, E, K), seed, "stage_child_q") * 8.0) + 1.0) / 8.0).astype(np.float32)
+    cut = _uniform((Bn, E), seed, "stage_child_cut")
+    k = w.top_k
+    tok[..., k:] = -1
+    q[..., k:] = 0.0
+    for b in range(Bn):
+        for e in range(E):
+            if w.tree == "eagle2" and cut[b, e] < 0.1 and k > 1:   # mass ran out after the first draws
+                n = 1 + int(cut[b, e] * 10 * (k - 1)) % (k - 1)
+                tok[b, e, n:] = -1
+                q[b, e, n:] = 0.0
+    return tok, q
+
+
+def _gpu_tree(eng, rd, tok, q):
+    rd.c_token.copy_(torch.from_numpy(tok))
+    rd.c_prob.copy_(torch.from_numpy(q))
+    st, ws = eng.stream(), eng.ws.data_ptr()
+    B.eagle_tree_expand_rerank(eng.ctx, rd.plan, B.PHASE_ROOT, 0, rd.B, rd.req_c, None, rd.pool_c, None, ws, st)
+    for layer in range(1, rd.plan.n_layers):
+        B.eagle_tree_expand_rerank(eng.ctx, rd.plan, B.PHASE_FRONTIER, layer, rd.B, rd.req_c, rd.children_c,
+                                   rd.pool_c, None, ws, st)
+    B.eagle_tree_expand_rerank(eng.ctx, rd.plan, B.PHASE_FINAL, 0, rd.B, rd.req_c, rd.children_c, rd.pool_c,
+                               rd.tree_c, ws, st)
+    torch.cuda.synchronize()
+    assert B.eagle_read_device_status(eng.ctx, ws, st) == 0
+
+
+def _oracle_tree(w, t_next, tok_b, q_b, n_layers):
+    child_tok = [[int(x) for x in row] for row in tok_b]
+    child_q = [[float(x) for x in row] for row in q_b]       # fp32 -> fp64, exact
+    ex = T.root(int(t_next))
+    if w.tree == "eagle2":
+        prev = [0]
+        for _layer in range(1, n_layers):
+            prev = T.eagle2_frontier(ex, child_tok, child_q, prev, w.top_k)
+        tr = T.eagle2_final(ex, child_tok, child_q, w.top_m)
+    else:
+        tpl = T.template(w.tree)
+        for depth in range(1, n_layers):
+            T.static_frontier(ex, child_tok, tpl, depth, child_q)
+        tr = T.static_final(ex, child_tok, tpl)
+    return ex, tr, child_tok
+
+
+def _build(name):
+    w = CASES[name]
+    seed = 5150 + sorted(CASES).index(name)
+    inp = S.round_inputs(w, seed, device="cuda")
+    eng, rd = make_round(w, inp)
+    tok, q = _children(w, seed, rd.B, rd.E, rd.K, w.vocab)
+    _gpu_tree(eng, rd, tok, q)
+    t_next = inp["t_next"].cpu().numpy()
+    refs = [_oracle_tree(w, t_next[b], tok[b], q[b], rd.plan.n_layers) for b in range(rd.B)]
+    return w, seed, inp, eng, rd, tok, q, refs
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_tree_stage_bit_exact(name):
+    w, seed, inp, eng, rd, tok, q, refs = _build(name)
+    L = inp["prefix_len"]
+    for b, (ex, tr, _ct) in enumerate(refs):
+        n = len(ex.token)
+        assert rd.p_token[b, :n].tolist() == ex.token, (name, b)
+        assert rd.p_parent[b, :n].tolist() == ex.parent, (name, b)
+        assert rd.p_depth[b, :n].tolist() == ex.depth, (name, b)
+        assert rd.p_value[b, :n].cpu().numpy().tolist() == ex.value, (name, b)     # fp64, bit-exact
+        assert int(rd.t_size[b]) == tr.size, (name, b)
+        s = tr.size
+        assert rd.t_token[b, :s].tolist() == tr.token, (name, b)
+        assert rd.t_parent[b, :s].tolist() == tr.parent, (name, b)
+        assert rd.t_depth[b, :s].tolist() == tr.depth, (name, b)
+        assert rd.t_exp[b, :s].tolist() == tr.exp, (name, b)
+        assert [int(x) & 0xFFFFFFFFFFFFFFFF for x in rd.t_anc[b, :s].tolist()] == tr.anc, (name, b)
+        assert rd.t_pos[b, :s].tolist() == [L[b] + dd for dd in tr.depth], (name, b)
+        cs = rd.t_child_slot[b].cpu().numpy()
+        for e in range(n):
+            for r in range(rd.K):
+                assert int(cs[e, r]) == tr.child_slot.get((e, r), -1), (name, b, e, r)
+
+
+def _accept_inputs(w, seed, rd, refs, tok):
+    """Target probabilities p per tree slot and draft rows q per expanded
+    slot (fp32).  p near q at expanded slots, and the greedy argmax often a
+    drawn child, so that walks descend."""
+    Bn, Sn, E, V = rd.B, rd.S, rd.E, w.vocab
+    qrows = S.random_probs(Bn * E, V, seed, "stage_q", sigma=1.5).view(Bn, E, V).numpy().astype(np.float64)
+    for b in range(Bn):
+        for e in range(E):
+            for t in tok[b, e]:
+                if t >= 0:
+                    qrows[b, e, t] += 0.05
+    qrows = (qrows / qrows.sum(-1, keepdims=True)).astype(np.float32)
+    noise = S.random_tensor((Bn, Sn, V), seed, "stage_p_noise").numpy()
+    fresh = S.random_probs(Bn * Sn, V, seed, "stage_p_fresh", sigma=1.5).view(Bn, Sn, V).numpy()
+    boost = _uniform((Bn, Sn), seed, "stage_p_boost")
+    p = np.zeros((Bn, Sn, V), dtype=np.float64)
+    for b, (_ex, tr, _ct) in enumerate(refs):
+        for s_ in range(Sn):
+            e = tr.exp[s_] if s_ < tr.size else -1
+            if e >= 0:
+                row = qrows[b, e].astype(np.float64) * np.exp(0.3 * noise[b, s_])
+                kids = [int(t) for t in tok[b, e] if t >= 0]
+                if kids and boost[b, s_] < 0.7:       # the target's argmax is a drawn child
+                    row[kids[int(boost[b, s_] * 10) % len(kids)]] = row.max() * 1.5
+            else:
+                row = fresh[b, s_].astype(np.float64)
+            p[b, s_] = row / row.sum()
+    p = p.astype(np.float32)
+    argmax = np.argmax(p, axis=-1).astype(np.int32)        # first maximum = lowest id
+    return qrows, p, argmax
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_accept_stage_bit_exact(name):
+    w, seed, inp, eng, rd, tok, q, refs = _build(name)
+    qrows, p, argmax = _accept_inputs(w, seed, rd, refs, tok)
+    temps = w.temps_for_batch()
+    rd.temps.copy_(torch.tensor(temps, dtype=torch.float32))
+    rd.set_sampling(inp["philox_seed"], inp["round_id"])
+    rd.probs.copy_(torch.from_numpy(qrows))
+    rd.target_probs.copy_(torch.from_numpy(p))
+    rd.target_argmax.copy_(torch.from_numpy(argmax))
+    st, ws = eng.stream(), eng.ws.data_ptr()
+    B.eagle_accept_from_probs(eng.ctx, rd.plan, rd.B, rd.tree_c, rd.children_c, _p(rd.target_probs),
+                              _p(rd.target_argmax), _p(rd.probs), rd.sampling_c, rd.acc_c, ws, st)
+    torch.cuda.synchronize()
+    assert B.eagle_read_device_status(eng.ctx, ws, st) == 0
+    descended = 0
+    for b, (_ex, tr, child_tok) in enumerate(refs):
+        p_rows = p[b].astype(np.float64)
+        if temps[b] <= 0:
+            a, path, final = Vf.accept_greedy(tr, p_rows)
+        else:
+            a, path, final = Vf.accept_sampling(tr, p[b], qrows[b], child_tok, b, inp["philox_seed"],
+                                                inp["round_id"])
+        got_a = int(rd.accept_len[b])
+        assert got_a == a, (name, b, got_a, a)
+        assert rd.path[b, :a + 1].tolist() == list(path), (name, b)
+        assert int(rd.final_token[b]) == int(final), (name, b)
+        assert int(rd.last_slot[b]) == path[-1], (name, b)
+        descended += a
+    # the inputs make walks descend: the comparison covers more than the root
+    assert descended > 0, name
