@@ -168,6 +168,13 @@ __device__ __forceinline__ void attn_pass(const AttnParams& p, const PassCtx& x,
   float *sk = x.sk, *sv = x.sv, *sq = x.sq, *sp = x.sp;
   uint64_t* s_mask = x.s_mask;
   const int nr = rp > warp ? (rp - warp + WARPS - 1) / WARPS : 0;   // <= NR
+  // The prefix KV is not written by the kernels of this draft step: its
+  // first tile is requested before waiting on the predecessor.
+  PrefixTile pre;
+  if (!is_tree && lo < hi)
+    prefix_load(pre, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + lo) * p.Hkv + h) * dh, row_stride,
+                min(TILE, hi - lo), dh);
+  if (r0 == 0) pdl_wait();                 // q rows, tree K/V and masks come from the predecessors
   __syncthreads();                         // previous pass done with sq
   for (int idx = threadIdx.x; idx < rp * (dh >> 2); idx += THREADS) {
     const int rr = idx / (dh >> 2), c = idx - rr * (dh >> 2);
@@ -194,10 +201,6 @@ __device__ __forceinline__ void attn_pass(const AttnParams& p, const PassCtx& x,
     for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
   }
 
-  PrefixTile pre;
-  if (!is_tree && lo < hi)
-    prefix_load(pre, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + lo) * p.Hkv + h) * dh, row_stride,
-                min(TILE, hi - lo), dh);
   for (int t0 = lo; t0 < hi; t0 += TILE) {
     const int nt = min(TILE, hi - t0);
     __syncthreads();                       // all warps done with the previous tile
@@ -225,8 +228,9 @@ __device__ __forceinline__ void attn_pass(const AttnParams& p, const PassCtx& x,
       for (int i = 0; i < NR; ++i) {
         if (i < nr) {
           const float4 q = *reinterpret_cast<const float4*>(sq + (warp + WARPS * i) * dh + d);
-          s0[i] += fmaf(q.x, a.x, q.y * a.y) + fmaf(q.z, a.z, q.w * a.w);
-          s1[i] += fmaf(q.x, c.x, q.y * c.y) + fmaf(q.z, c.z, q.w * c.w);
+          // plain FMA chains: the 2 x NR independent (row, key) sums give the ILP
+          s0[i] = fmaf(q.w, a.w, fmaf(q.z, a.z, fmaf(q.y, a.y, fmaf(q.x, a.x, s0[i]))));
+          s1[i] = fmaf(q.w, c.w, fmaf(q.z, c.z, fmaf(q.y, c.y, fmaf(q.x, c.x, s1[i]))));
         }
       }
     }
@@ -305,8 +309,8 @@ __device__ __forceinline__ void attn_pass(const AttnParams& p, const PassCtx& x,
 // further block-wide barrier is needed.
 template <int NR>
 __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams p) {
-  pdl_wait();      // predecessor outputs visible from here on
   pdl_trigger();
+  if (p.mode == 1) pdl_wait();               // verification reads the tree's size first
   extern __shared__ __align__(16) float smem_attn[];
   __shared__ int s_last;
   __shared__ uint64_t s_mask[ROWS_PASS];     // ancestor masks of the tree part's rows
@@ -343,6 +347,7 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams 
     attn_pass<NR>(p, x, r0, min(p.rows_pass, R - r0));
   }
 
+  pdl_wait();                                 // (no-op once waited; a pass-less CTA waits here)
   // the last CTA of this (request, kv head) merges the splits in order
   __threadfence();
   __syncthreads();

@@ -94,14 +94,15 @@ struct Smem {
   float* red;       // [4][32]
   float* rs;        // [32]
   int* rowi;        // [32]
-  float* stg;       // [STG_FLOATS], 16-byte aligned
+  float* stg;       // [STG_FLOATS], 16-byte aligned: partial tiles of other CTAs
+  float* stg2;      // [STG_FLOATS]: the tile's row inputs from earlier kernels
 };
 
 __host__ __device__ inline size_t smem_bytes_for(int stages, uint32_t a_stage, uint32_t b_stage) {
   size_t s = 1024;                                  // alignment slack
   s += static_cast<size_t>(stages) * (a_stage + b_stage);
   s += (2 * stages + 4) * 8 + 64;
-  s += XCH_ROWS * BM * 4 + 4 * 32 * 4 + 32 * 4 + 32 * 4 + STG_FLOATS * 4;
+  s += XCH_ROWS * BM * 4 + 4 * 32 * 4 + 32 * 4 + 32 * 4 + 2 * STG_FLOATS * 4;
   return s;
 }
 
@@ -124,6 +125,7 @@ __device__ inline Smem carve(uint8_t* raw, const GemmParams& p) {
   s.rs = s.red + 4 * 32;
   s.rowi = reinterpret_cast<int*>(s.rs + 32);
   s.stg = reinterpret_cast<float*>(s.rowi + 32);
+  s.stg2 = s.stg + STG_FLOATS;
   return s;
 }
 
@@ -192,6 +194,190 @@ __device__ __forceinline__ void stage_block(float* dst, const float* src, int n,
   for (int i = 4 * et; i < n; i += 4 * EPI_THREADS) cp_async16(dst + i, src + i);
 }
 
+// Per-column constants of the fused epilogue for tile row m of tile t.
+struct EpiCol {
+  int gi, qd, kd, head, di, partner;
+  bool rope, is_v, rot_first, d_col;
+  float f_hi, f_lo, col_bias, col_gain;
+};
+
+__device__ __noinline__ EpiCol epi_column(const GemmParams& p, int t, int m) {
+  EpiCol c;
+  c.gi = t * BM + m;
+  c.qd = p.Hq * p.dh;
+  c.kd = p.Hkv * p.dh;
+  const int half = p.dh >> 1;
+  c.rope = false; c.is_v = false; c.rot_first = false;
+  c.head = 0; c.di = 0; c.partner = m;
+  c.f_hi = 0.f; c.f_lo = 0.f;          // inverse frequency as an unevaluated float pair
+  if (p.epi == EPI_QKV && c.gi < c.qd + 2 * c.kd) {
+    c.is_v = c.gi >= c.qd + c.kd;
+    const int base = c.gi < c.qd ? 0 : (c.gi < c.qd + c.kd ? c.qd : c.qd + c.kd);
+    c.head = (c.gi - base) / p.dh;
+    c.di = (c.gi - base) % p.dh;
+    c.rot_first = c.di < half;
+    c.partner = c.rot_first ? m + half : m - half;
+    c.rope = !c.is_v;
+    const double inv_freq = exp(-(2.0 * (c.rot_first ? c.di : c.di - half) / p.dh) * p.ln_theta);
+    c.f_hi = static_cast<float>(inv_freq);
+    c.f_lo = static_cast<float>(inv_freq - static_cast<double>(c.f_hi));
+  }
+  c.d_col = c.gi < p.d;
+  c.col_bias = 0.f; c.col_gain = 0.f;
+  if (p.epi == EPI_FC && c.d_col) { c.col_bias = p.bias[c.gi]; c.col_gain = p.gain[c.gi]; }
+  if (p.epi == EPI_O && c.d_col) c.col_gain = p.gain[c.gi];
+  return c;
+}
+
+// Issue the asynchronous copies of rows jc .. jc + nj - 1's inputs from
+// earlier kernels into s.stg2 (residual rows for O / down, RMSNorm partial
+// sums for QKV / gate-up) and, for QKV, the rows' RoPE positions into
+// s.rowi.  Completion: cp_async_wait_all + an epilogue barrier.
+__device__ __noinline__ void stage_row_inputs(const GemmParams& p, const Smem& s, int t, int jc, int nj, int m) {
+  const int et = m;
+  const int tiles = p.ss_in_tiles;
+  if (p.epi == EPI_O || p.epi == EPI_DOWN) {                      // residual rows, this tile's columns
+    const int ncol = min(BM, p.d - t * BM);                         // a multiple of 64
+    for (int i = et; i < nj * (BM / 4); i += EPI_THREADS) {
+      const int r = i / (BM / 4), q = 4 * (i % (BM / 4));
+      if (q < ncol) cp_async16(s.stg2 + r * BM + q, p.resid + static_cast<size_t>(jc + r) * p.d + t * BM + q);
+    }
+  } else if (p.epi == EPI_QKV || p.epi == EPI_GATEUP) {           // norm partials of rows jc..jc+nj-1
+    const float* ss = p.ss_in + static_cast<size_t>(jc) * tiles;
+    if (tiles % 4 == 0) {
+      stage_block(s.stg2, ss, nj * tiles, et);
+    } else {
+      for (int i = et; i < nj * tiles; i += EPI_THREADS) s.stg2[i] = __ldcg(ss + i);
+    }
+    if (p.epi == EPI_QKV && m < nj) {
+      const int j = jc + m, b = j / p.rpr, e = p.e0 + j % p.rpr;
+      s.rowi[m] = p.pos0[b] + p.depth[static_cast<size_t>(b) * p.E + e];
+    }
+  }
+}
+
+// Steps 2-3 of a tile's epilogue for rows jc .. jc + nj - 1, whose summed
+// accumulators are in s.xch: stage the rows' inputs written by earlier
+// kernels, then the contraction's elementwise work.  Ends with the epilogue
+// warps synchronised.
+__device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, const EpiCol& col, int t, int jc,
+                                            int nj, int m, bool prestaged) {
+  const int gi = col.gi, qd = col.qd, kd = col.kd, head = col.head, di = col.di, partner = col.partner;
+  const bool rope = col.rope, is_v = col.is_v, rot_first = col.rot_first, d_col = col.d_col;
+  const float f_hi = col.f_hi, f_lo = col.f_lo, col_bias = col.col_bias, col_gain = col.col_gain;
+  // 2. row inputs written by earlier kernels (staged in s.stg2)
+  const int tiles = p.ss_in_tiles;
+  if (!prestaged) stage_row_inputs(p, s, t, jc, nj, m);
+  cp_async_wait_all();
+  sm100::named_barrier(1, EPI_THREADS);
+  if ((p.epi == EPI_O || p.epi == EPI_DOWN) && d_col) {
+#pragma unroll 1
+    for (int jj = 0; jj < nj; ++jj) s.xch[jj * BM + m] += s.stg2[jj * BM + m];
+  }
+  if ((p.epi == EPI_QKV || p.epi == EPI_GATEUP) && m < nj) {      // RMSNorm scale of input row jc + m
+    const float* ss = s.stg2 + m * tiles;
+    float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+    int i = 0;
+#pragma unroll 1
+    for (; i + 4 <= tiles; i += 4) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc4[u] += ss[i + u];
+    }
+#pragma unroll 1
+    for (; i < tiles; ++i) acc4[0] += ss[i];
+    const float tot = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+    s.rs[m] = 1.0f / sqrtf(tot / static_cast<float>(p.d) + p.eps);
+  }
+  sm100::named_barrier(1, EPI_THREADS);
+  // 3. the contraction's elementwise epilogue, one activation row at a time
+  if (p.epi == EPI_FC || p.epi == EPI_O) {
+#pragma unroll 1
+    for (int jj = 0; jj < nj; ++jj) {
+      const int j = jc + jj;
+      float v = 0.f;
+      if (d_col) {
+        v = s.xch[jj * BM + m] + col_bias;
+        p.out_f32[static_cast<size_t>(j) * p.d + gi] = v;
+        put_split(p.bnext, p.NP, p.kp_next, j, gi, v * col_gain);
+      }
+      s.xch[jj * BM + m] = v;
+    }
+    sm100::named_barrier(1, EPI_THREADS);
+    // sum of squares of the tile's columns of each row (next RMSNorm): warp
+    // w sums columns 32w .. 32w + 31 of row r = lane (the rotated start keeps
+    // the lanes on distinct banks), then thread r adds the four warp sums
+    {
+      const int w = m >> 5, r = m & 31;
+      if (r < nj) {
+        float sq = 0.f;
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+          const float x = s.xch[r * BM + 32 * w + ((k + r) & 31)];
+          sq = fmaf(x, x, sq);
+        }
+        s.red[w * 32 + r] = sq;
+      }
+      sm100::named_barrier(1, EPI_THREADS);
+      if (m < nj)
+        p.ss_out[static_cast<size_t>(jc + m) * p.m_tiles + t] =
+            (s.red[m] + s.red[32 + m]) + (s.red[64 + m] + s.red[96 + m]);
+    }
+  } else if (p.epi == EPI_QKV) {
+    if (gi < qd + 2 * kd) {
+#pragma unroll 1
+      for (int jj = 0; jj < nj; ++jj) {
+        const int j = jc + jj;
+        const int b = j / p.rpr, e = p.e0 + j % p.rpr;
+        const float sc = s.rs[jj];
+        float v = s.xch[jj * BM + m] * sc;
+        if (rope) {
+          float sn, cs;
+          sincosf(rope_angle(s.rowi[jj], f_hi, f_lo), &sn, &cs);
+          const float other = s.xch[jj * BM + partner] * sc;
+          v = rot_first ? v * cs - other * sn : v * cs + other * sn;
+        }
+        if (gi < qd) {
+          p.qrow[static_cast<size_t>(j) * qd + gi] = v;
+        } else {
+          float* dst = is_v ? p.v_tree : p.k_tree;
+          dst[((static_cast<size_t>(b) * p.E + e) * p.Hkv + head) * p.dh + di] = v;
+        }
+      }
+    }
+  } else if (p.epi == EPI_GATEUP) {
+    const int c = t * 64 + m;
+    if (m < 64 && c < p.F) {
+#pragma unroll 1
+      for (int jj = 0; jj < nj; ++jj) {
+        const float sc = s.rs[jj];
+        const float g = s.xch[jj * BM + m] * sc, u = s.xch[jj * BM + m + 64] * sc;
+        put_split(p.bnext, p.NP, p.kp_next, jc + jj, c, g / (1.0f + expf(-g)) * u);
+      }
+    }
+  } else if (p.epi == EPI_DOWN) {
+    if (d_col) {
+#pragma unroll 1
+      for (int jj = 0; jj < nj; ++jj) {
+        const int j = jc + jj;
+        const int b = j / p.rpr, e = p.e0 + j % p.rpr;
+        const float v = s.xch[jj * BM + m];
+        p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.d + gi] = v;
+        put_split(p.bnext, p.NP, p.kp_next, j, gi, v);
+      }
+    }
+  } else {  // EPI_LM
+    if (gi < p.V) {
+#pragma unroll 1
+      for (int jj = 0; jj < nj; ++jj) {
+        const int j = jc + jj;
+        const int b = j / p.rpr, e = p.e0 + j % p.rpr;
+        p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.V + gi] = s.xch[jj * BM + m];
+      }
+    }
+  }
+  sm100::named_barrier(1, EPI_THREADS);
+}
+
 // Final epilogue of tile t: sum the partials of CTAs [c_first, c_last] and
 // apply the contraction's fused elementwise work.  `m` is the tile row this
 // thread owns (its tensor-memory lane).  It runs once per tile, cold, at the
@@ -200,32 +386,9 @@ __device__ __forceinline__ void stage_block(float* dst, const float* src, int n,
 // a 32-row chunk is brought into shared memory by asynchronous copies issued
 // from compact loops (many in flight, one wait), then the per-row loops read
 // shared memory only.
-__device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, int t, int c_first, int c_last,
-                                           int m) {
+__device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, const EpiCol& col, int t,
+                                           int c_first, int c_last, int m) {
   const int et = m;                    // epilogue thread index == tile row
-  // per-column constants of this thread's output index
-  int gi = t * BM + m;
-  const int qd = p.Hq * p.dh, kd = p.Hkv * p.dh;
-  const int half = p.dh >> 1;
-  bool rope = false, is_v = false, rot_first = false;
-  int head = 0, di = 0, partner = m;
-  float f_hi = 0.f, f_lo = 0.f;        // inverse frequency as an unevaluated float pair
-  if (p.epi == EPI_QKV && gi < qd + 2 * kd) {
-    is_v = gi >= qd + kd;
-    const int base = gi < qd ? 0 : (gi < qd + kd ? qd : qd + kd);
-    head = (gi - base) / p.dh;
-    di = (gi - base) % p.dh;
-    rot_first = di < half;
-    partner = rot_first ? m + half : m - half;
-    rope = !is_v;
-    const double inv_freq = exp(-(2.0 * (rot_first ? di : di - half) / p.dh) * p.ln_theta);
-    f_hi = static_cast<float>(inv_freq);
-    f_lo = static_cast<float>(inv_freq - static_cast<double>(f_hi));
-  }
-  const bool d_col = gi < p.d;
-  float col_bias = 0.f, col_gain = 0.f;
-  if (p.epi == EPI_FC && d_col) { col_bias = p.bias[gi]; col_gain = p.gain[gi]; }
-  if (p.epi == EPI_O && d_col) col_gain = p.gain[gi];
   const int C = c_last - c_first + 1;
   for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
     const int nj = min(XCH_ROWS, p.n - jc);
@@ -251,126 +414,146 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, i
       }
       sm100::named_barrier(1, EPI_THREADS);
     }
-    // 2. row inputs written by earlier kernels, staged the same way
-    const int tiles = p.ss_in_tiles;
-    if (p.epi == EPI_O || p.epi == EPI_DOWN) {                      // residual rows, this tile's columns
-      const int ncol = min(BM, p.d - t * BM);                         // a multiple of 64
-      for (int i = et; i < nj * (BM / 4); i += EPI_THREADS) {
-        const int r = i / (BM / 4), q = 4 * (i % (BM / 4));
-        if (q < ncol) cp_async16(s.stg + r * BM + q, p.resid + static_cast<size_t>(jc + r) * p.d + t * BM + q);
+    epilogue_chunk(p, s, col, t, jc, nj, m, jc == 0);   // chunk 0's row inputs were staged early
+  }
+}
+
+// Tensor maps of one launch: the (up to three) weight matrices as 4-D
+// grouped maps, their 2-D tail maps, and the activation operand.
+struct GemmMaps {
+  const CUtensorMap *a0, *a1, *a2, *t0, *t1, *t2, *b;
+};
+
+// TMA producer (warp 0, lane 0) over units [u_begin, u_end).
+__device__ __forceinline__ void gemm_produce(const GemmParams& p, const Smem& s, const GemmMaps& mp, int lane,
+                                             long long u_begin, long long u_end, volatile int* abort_flag) {
+  // ---------------- TMA producer ----------------
+  if (lane == 0) {
+    int stage = 0;
+    uint32_t phase = 0;
+    long long issued = 0;
+    const uint32_t group_bytes = static_cast<uint32_t>(p.kps) * 1024u;
+    // weight rows of unit u into ring slot st (64-row halves)
+    auto issue_a = [&](long long u, int st) {
+      const int t = static_cast<int>(u / p.kb), kz = static_cast<int>(u % p.kb) * p.kps;
+      uint8_t* a_dst = s.a + static_cast<size_t>(st) * p.a_stage_bytes;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        int map, row;
+        locate_box(p, t, h, map, row);
+        uint8_t* dst = a_dst + h * 8 * group_bytes;
+        if (row + 64 <= p.full_rows[map] && kz + p.kps <= p.full_kb) {
+          const CUtensorMap* m4 = map == 0 ? mp.a0 : (map == 1 ? mp.a1 : mp.a2);
+          sm100::tma_load_4d(dst, m4, 0, 0, kz, row >> 3, &s.full[st]);
+        } else {                                   // row or K tail: 8-row x 64-k boxes, zero past the end
+          const CUtensorMap* m2 = map == 0 ? mp.t0 : (map == 1 ? mp.t1 : mp.t2);
+#pragma unroll 1
+          for (int g = 0; g < 8; ++g)
+            for (int c = 0; c < p.kps; ++c)
+              sm100::tma_load_2d(dst + g * group_bytes + c * 1024, m2, (kz + c) * BK, row + 8 * g, &s.full[st]);
+        }
       }
-    } else if (p.epi == EPI_QKV || p.epi == EPI_GATEUP) {           // norm partials of rows jc..jc+nj-1
-      const float* ss = p.ss_in + static_cast<size_t>(jc) * tiles;
-      if (tiles % 4 == 0) {
-        stage_block(s.stg, ss, nj * tiles, et);
-      } else {
-        for (int i = et; i < nj * tiles; i += EPI_THREADS) s.stg[i] = __ldcg(ss + i);
+    };
+    // activation rows (the previous kernel's output) of unit u into slot st
+    auto issue_b = [&](long long u, int st) {
+      const int kz = static_cast<int>(u % p.kb) * p.kps;
+      sm100::tma_load_4d(s.b + static_cast<size_t>(st) * p.b_stage_bytes, mp.b, 0, 0, kz, 0, &s.full[st]);
+    };
+    // The first ring's worth of weights does not depend on the previous
+    // kernel: it streams while that kernel drains.
+    const long long n_pre = min(static_cast<long long>(p.stages), u_end - u_begin);
+    for (long long i = 0; i < n_pre; ++i) {
+      sm100::mbar_arrive_expect_tx(&s.full[i], p.a_stage_bytes + p.b_stage_bytes);
+      issue_a(u_begin + i, static_cast<int>(i));
+    }
+    pdl_wait();
+    for (long long i = 0; i < n_pre; ++i) issue_b(u_begin + i, static_cast<int>(i));
+    issued = n_pre;
+    stage = static_cast<int>(n_pre % p.stages);
+    phase = n_pre == p.stages ? 1u : 0u;
+    for (long long u = u_begin + n_pre; u < u_end; ++u) {
+      if (!sm100::mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
+        *abort_flag = 1;
+        set_status(p.status, EAGLE_ERR_TIMEOUT);
+        break;
       }
-      if (p.epi == EPI_QKV && m < nj) {
-        const int j = jc + m, b = j / p.rpr, e = p.e0 + j % p.rpr;
-        s.rowi[m] = p.pos0[b] + p.depth[static_cast<size_t>(b) * p.E + e];
+      sm100::mbar_arrive_expect_tx(&s.full[stage], p.a_stage_bytes + p.b_stage_bytes);
+      issue_a(u, stage);
+      issue_b(u, stage);
+      ++issued;
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+    }
+    if (*abort_flag) {
+      // let copies already in flight land before the CTA exits
+      const long long pending = issued < p.stages ? issued : p.stages;
+      for (long long i = 0; i < pending; ++i) {
+        stage = stage == 0 ? p.stages - 1 : stage - 1;
+        if (stage == p.stages - 1) phase ^= 1u;
+        const uint64_t t0 = globaltimer_ns();
+        while (!sm100::mbar_try_wait(&s.full[stage], phase) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
+        }
       }
     }
-    cp_async_wait_all();
-    sm100::named_barrier(1, EPI_THREADS);
-    if ((p.epi == EPI_O || p.epi == EPI_DOWN) && d_col) {
-#pragma unroll 1
-      for (int jj = 0; jj < nj; ++jj) s.xch[jj * BM + m] += s.stg[jj * BM + m];
-    }
-    if ((p.epi == EPI_QKV || p.epi == EPI_GATEUP) && m < nj) {      // RMSNorm scale of input row jc + m
-      const float* ss = s.stg + m * tiles;
-      float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-      int i = 0;
-#pragma unroll 1
-      for (; i + 4 <= tiles; i += 4) {
+  }
+}
+
+// MMA issuer (warp 1, lane 0): one accumulator per tile segment of
+// [u_begin, u_end), double-buffered in tensor memory when two fit.
+__device__ __forceinline__ void gemm_mma(const GemmParams& p, const Smem& s, int lane, uint32_t tmem_base,
+                                         long long u_begin, long long u_end, volatile int* abort_flag) {
+  // ---------------- MMA issuer ----------------
+  if (lane == 0) {
+    const uint32_t n_total = 2u * p.NP;
+    const uint32_t idesc = p.two_mma ? sm100::idesc_bf16_f32(BM, p.NP) : sm100::idesc_bf16_f32(BM, n_total);
+    int stage = 0;
+    uint32_t phase = 0;
+    int seg = 0;
+    long long u = u_begin;
+    bool ok = true;
+    while (u < u_end && ok) {
+      const int t = static_cast<int>(u / p.kb);
+      const long long seg_end = min(u_end, static_cast<long long>(t + 1) * p.kb);
+      const int buf = seg % p.n_acc;
+      const uint32_t aph = static_cast<uint32_t>(seg / p.n_acc) & 1u;
+      if (!sm100::mbar_wait(&s.tempty[buf], aph ^ 1u, abort_flag)) {
+        *abort_flag = 1;
+        set_status(p.status, EAGLE_ERR_TIMEOUT);
+        break;
+      }
+      sm100::tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
+      const long long seg_start = u;
+      for (; u < seg_end; ++u) {
+        if (!sm100::mbar_wait(&s.full[stage], phase, abort_flag)) {
+          *abort_flag = 1;
+          set_status(p.status, EAGLE_ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        sm100::tc_fence_after();
+        const uint32_t a_addr = sm100::smem_u32(s.a + static_cast<size_t>(stage) * p.a_stage_bytes);
+        const uint32_t b_addr = sm100::smem_u32(s.b + static_cast<size_t>(stage) * p.b_stage_bytes);
+        const uint32_t sbo = static_cast<uint32_t>(p.kps) * 1024u;
+        const uint32_t b2 = static_cast<uint32_t>(p.NP >> 3) * sbo;   // second activation half
+        for (int c = 0; c < p.kps; ++c) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) acc4[u] += ss[i + u];
-      }
-#pragma unroll 1
-      for (; i < tiles; ++i) acc4[0] += ss[i];
-      const float tot = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-      s.rs[m] = 1.0f / sqrtf(tot / static_cast<float>(p.d) + p.eps);
-    }
-    sm100::named_barrier(1, EPI_THREADS);
-    // 3. the contraction's elementwise epilogue, one activation row at a time
-    if (p.epi == EPI_FC || p.epi == EPI_O) {
-#pragma unroll 1
-      for (int jj = 0; jj < nj; ++jj) {
-        const int j = jc + jj;
-        float v = 0.f;
-        if (d_col) {
-          v = s.xch[jj * BM + m] + col_bias;
-          p.out_f32[static_cast<size_t>(j) * p.d + gi] = v;
-          put_split(p.bnext, p.NP, p.kp_next, j, gi, v * col_gain);
-        }
-        s.xch[jj * BM + m] = v;
-      }
-      sm100::named_barrier(1, EPI_THREADS);
-      // sum of squares of the tile's columns of row jc + m (next RMSNorm);
-      // the rotated start keeps the threads on distinct banks
-      if (m < nj) {
-        float sq = 0.f;
-#pragma unroll 4
-        for (int k = 0; k < BM; ++k) {
-          const float x = s.xch[m * BM + ((k + m) & (BM - 1))];
-          sq = fmaf(x, x, sq);
-        }
-        p.ss_out[static_cast<size_t>(jc + m) * p.m_tiles + t] = sq;
-      }
-    } else if (p.epi == EPI_QKV) {
-      if (gi < qd + 2 * kd) {
-#pragma unroll 1
-        for (int jj = 0; jj < nj; ++jj) {
-          const int j = jc + jj;
-          const int b = j / p.rpr, e = p.e0 + j % p.rpr;
-          const float sc = s.rs[jj];
-          float v = s.xch[jj * BM + m] * sc;
-          if (rope) {
-            float sn, cs;
-            sincosf(rope_angle(s.rowi[jj], f_hi, f_lo), &sn, &cs);
-            const float other = s.xch[jj * BM + partner] * sc;
-            v = rot_first ? v * cs - other * sn : v * cs + other * sn;
-          }
-          if (gi < qd) {
-            p.qrow[static_cast<size_t>(j) * qd + gi] = v;
-          } else {
-            float* dst = is_v ? p.v_tree : p.k_tree;
-            dst[((static_cast<size_t>(b) * p.E + e) * p.Hkv + head) * p.dh + di] = v;
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint32_t off = static_cast<uint32_t>(c) * 1024u + kk * 32;
+            const uint64_t ad = sm100::smem_desc_sw128_sbo(a_addr + off, sbo);
+            const uint32_t accum = (u != seg_start || c > 0 || kk > 0) ? 1u : 0u;
+            sm100::mma_bf16(d_tmem, ad, sm100::smem_desc_sw128_sbo(b_addr + off, sbo), idesc, accum);
+            if (p.two_mma)
+              sm100::mma_bf16(d_tmem + p.NP, ad, sm100::smem_desc_sw128_sbo(b_addr + b2 + off, sbo), idesc,
+                              accum);
           }
         }
+        sm100::mma_commit(&s.empty[stage]);
+        if (++stage == p.stages) { stage = 0; phase ^= 1u; }
       }
-    } else if (p.epi == EPI_GATEUP) {
-      const int c = t * 64 + m;
-      if (m < 64 && c < p.F) {
-#pragma unroll 1
-        for (int jj = 0; jj < nj; ++jj) {
-          const float sc = s.rs[jj];
-          const float g = s.xch[jj * BM + m] * sc, u = s.xch[jj * BM + m + 64] * sc;
-          put_split(p.bnext, p.NP, p.kp_next, jc + jj, c, g / (1.0f + expf(-g)) * u);
-        }
-      }
-    } else if (p.epi == EPI_DOWN) {
-      if (d_col) {
-#pragma unroll 1
-        for (int jj = 0; jj < nj; ++jj) {
-          const int j = jc + jj;
-          const int b = j / p.rpr, e = p.e0 + j % p.rpr;
-          const float v = s.xch[jj * BM + m];
-          p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.d + gi] = v;
-          put_split(p.bnext, p.NP, p.kp_next, j, gi, v);
-        }
-      }
-    } else {  // EPI_LM
-      if (gi < p.V) {
-#pragma unroll 1
-        for (int jj = 0; jj < nj; ++jj) {
-          const int j = jc + jj;
-          const int b = j / p.rpr, e = p.e0 + j % p.rpr;
-          p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.V + gi] = s.xch[jj * BM + m];
-        }
-      }
+      if (!ok) break;
+      sm100::mma_commit(&s.tfull[buf]);
+      ++seg;
     }
-    sm100::named_barrier(1, EPI_THREADS);
   }
 }
 
@@ -387,6 +570,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const long long u_begin = static_cast<long long>(cta) * T / G;
   const long long u_end = static_cast<long long>(cta + 1) * T / G;
   volatile int* abort_flag = s.flags;
+  const GemmMaps maps{&mA0, &mA1, &mA2, &mT0, &mT1, &mT2, &mB};
   pdl_trigger();
 
   if (threadIdx.x == 0) {
@@ -420,130 +604,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *s.tmem_holder;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      long long issued = 0;
-      const uint32_t group_bytes = static_cast<uint32_t>(p.kps) * 1024u;
-      // weight rows of unit u into ring slot st (64-row halves)
-      auto issue_a = [&](long long u, int st) {
-        const int t = static_cast<int>(u / p.kb), kz = static_cast<int>(u % p.kb) * p.kps;
-        uint8_t* a_dst = s.a + static_cast<size_t>(st) * p.a_stage_bytes;
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          int map, row;
-          locate_box(p, t, h, map, row);
-          uint8_t* dst = a_dst + h * 8 * group_bytes;
-          if (row + 64 <= p.full_rows[map] && kz + p.kps <= p.full_kb) {
-            const CUtensorMap* mp = map == 0 ? &mA0 : (map == 1 ? &mA1 : &mA2);
-            sm100::tma_load_4d(dst, mp, 0, 0, kz, row >> 3, &s.full[st]);
-          } else {                                   // row or K tail: 8-row x 64-k boxes, zero past the end
-            const CUtensorMap* mp = map == 0 ? &mT0 : (map == 1 ? &mT1 : &mT2);
-#pragma unroll 1
-            for (int g = 0; g < 8; ++g)
-              for (int c = 0; c < p.kps; ++c)
-                sm100::tma_load_2d(dst + g * group_bytes + c * 1024, mp, (kz + c) * BK, row + 8 * g, &s.full[st]);
-          }
-        }
-      };
-      // activation rows (the previous kernel's output) of unit u into slot st
-      auto issue_b = [&](long long u, int st) {
-        const int kz = static_cast<int>(u % p.kb) * p.kps;
-        sm100::tma_load_4d(s.b + static_cast<size_t>(st) * p.b_stage_bytes, &mB, 0, 0, kz, 0, &s.full[st]);
-      };
-      // The first ring's worth of weights does not depend on the previous
-      // kernel: it streams while that kernel drains.
-      const long long n_pre = min(static_cast<long long>(p.stages), u_end - u_begin);
-      for (long long i = 0; i < n_pre; ++i) {
-        sm100::mbar_arrive_expect_tx(&s.full[i], p.a_stage_bytes + p.b_stage_bytes);
-        issue_a(u_begin + i, static_cast<int>(i));
-      }
-      pdl_wait();
-      for (long long i = 0; i < n_pre; ++i) issue_b(u_begin + i, static_cast<int>(i));
-      issued = n_pre;
-      stage = static_cast<int>(n_pre % p.stages);
-      phase = n_pre == p.stages ? 1u : 0u;
-      for (long long u = u_begin + n_pre; u < u_end; ++u) {
-        if (!sm100::mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
-          *abort_flag = 1;
-          set_status(p.status, EAGLE_ERR_TIMEOUT);
-          break;
-        }
-        sm100::mbar_arrive_expect_tx(&s.full[stage], p.a_stage_bytes + p.b_stage_bytes);
-        issue_a(u, stage);
-        issue_b(u, stage);
-        ++issued;
-        if (++stage == p.stages) { stage = 0; phase ^= 1u; }
-      }
-      if (*abort_flag) {
-        // let copies already in flight land before the CTA exits
-        const long long pending = issued < p.stages ? issued : p.stages;
-        for (long long i = 0; i < pending; ++i) {
-          stage = stage == 0 ? p.stages - 1 : stage - 1;
-          if (stage == p.stages - 1) phase ^= 1u;
-          const uint64_t t0 = globaltimer_ns();
-          while (!sm100::mbar_try_wait(&s.full[stage], phase) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
-          }
-        }
-      }
-    }
+    gemm_produce(p, s, maps, lane, u_begin, u_end, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t n_total = 2u * p.NP;
-      const uint32_t idesc = p.two_mma ? sm100::idesc_bf16_f32(BM, p.NP) : sm100::idesc_bf16_f32(BM, n_total);
-      int stage = 0;
-      uint32_t phase = 0;
-      int seg = 0;
-      long long u = u_begin;
-      bool ok = true;
-      while (u < u_end && ok) {
-        const int t = static_cast<int>(u / p.kb);
-        const long long seg_end = min(u_end, static_cast<long long>(t + 1) * p.kb);
-        const int buf = seg % p.n_acc;
-        const uint32_t aph = static_cast<uint32_t>(seg / p.n_acc) & 1u;
-        if (!sm100::mbar_wait(&s.tempty[buf], aph ^ 1u, abort_flag)) {
-          *abort_flag = 1;
-          set_status(p.status, EAGLE_ERR_TIMEOUT);
-          break;
-        }
-        sm100::tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
-        const long long seg_start = u;
-        for (; u < seg_end; ++u) {
-          if (!sm100::mbar_wait(&s.full[stage], phase, abort_flag)) {
-            *abort_flag = 1;
-            set_status(p.status, EAGLE_ERR_TIMEOUT);
-            ok = false;
-            break;
-          }
-          sm100::tc_fence_after();
-          const uint32_t a_addr = sm100::smem_u32(s.a + static_cast<size_t>(stage) * p.a_stage_bytes);
-          const uint32_t b_addr = sm100::smem_u32(s.b + static_cast<size_t>(stage) * p.b_stage_bytes);
-          const uint32_t sbo = static_cast<uint32_t>(p.kps) * 1024u;
-          const uint32_t b2 = static_cast<uint32_t>(p.NP >> 3) * sbo;   // second activation half
-          for (int c = 0; c < p.kps; ++c) {
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint32_t off = static_cast<uint32_t>(c) * 1024u + kk * 32;
-              const uint64_t ad = sm100::smem_desc_sw128_sbo(a_addr + off, sbo);
-              const uint32_t accum = (u != seg_start || c > 0 || kk > 0) ? 1u : 0u;
-              sm100::mma_bf16(d_tmem, ad, sm100::smem_desc_sw128_sbo(b_addr + off, sbo), idesc, accum);
-              if (p.two_mma)
-                sm100::mma_bf16(d_tmem + p.NP, ad, sm100::smem_desc_sw128_sbo(b_addr + b2 + off, sbo), idesc,
-                                accum);
-            }
-          }
-          sm100::mma_commit(&s.empty[stage]);
-          if (++stage == p.stages) { stage = 0; phase ^= 1u; }
-        }
-        if (!ok) break;
-        sm100::mma_commit(&s.tfull[buf]);
-        ++seg;
-      }
-    }
+    gemm_mma(p, s, lane, tmem_base, u_begin, u_end, abort_flag);
     __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
@@ -560,6 +624,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int buf = seg % p.n_acc;
       const uint32_t aph = static_cast<uint32_t>(seg / p.n_acc) & 1u;
       ++seg;
+      // While the tile streams: its epilogue constants and the first row
+      // chunk's inputs from earlier kernels (used only if this CTA finalizes).
+      const EpiCol col = epi_column(p, t, m);
+      cp_async_wait_all();                      // the previous segment's copies into s.stg2 have landed
+      sm100::named_barrier(1, EPI_THREADS);
+      stage_row_inputs(p, s, t, 0, min(XCH_ROWS, p.n), m);
       if (et == 0) s.flags[2] = sm100::mbar_wait(&s.tfull[buf], aph, abort_flag) ? 1 : 0;
       sm100::named_barrier(1, EPI_THREADS);
       if (!s.flags[2]) {
@@ -567,6 +637,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           *abort_flag = 1;
           set_status(p.status, EAGLE_ERR_TIMEOUT);
         }
+        cp_async_wait_all();
         break;
       }
       sm100::tc_fence_after();
@@ -600,10 +671,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       sm100::named_barrier(1, EPI_THREADS);
       if (s.flags[1]) {
         __threadfence();
-        finalize_tile(p, s, t, c_first, c_last, m);
+        finalize_tile(p, s, col, t, c_first, c_last, m);
       }
       sm100::named_barrier(1, EPI_THREADS);
     }
+    cp_async_wait_all();                        // no copy may land after the CTA has left
   }
   __syncthreads();
   if (warp == 1) {
