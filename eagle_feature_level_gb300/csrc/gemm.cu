@@ -58,6 +58,8 @@ struct GemmParams {
   uint32_t a_stage_bytes, b_stage_bytes;
   int full_rows[3];         // rows of each matrix in whole 8-row groups
   int full_kb;              // whole 64-wide k-blocks of K
+  int sk_tiles;             // tiles [0, sk_tiles) split stream-K over all CTAs (processed first)
+  int dp_waves;             // then tiles sk_tiles + c + i * grid, i < dp_waves, owned by CTA c alone
   int rpr, e0, E;
   int d, F, V, Hq, Hkv, dh;
   float eps;
@@ -133,6 +135,52 @@ __device__ inline Smem carve(uint8_t* raw, const GemmParams& p) {
 // (CTA c owns [floor(c T / G), floor((c+1) T / G))).
 __device__ __forceinline__ int cta_of_unit(long long u, long long T, int G) {
   return static_cast<int>(((u + 1) * G - 1) / T);
+}
+
+// The CTA's work: first its even share [sk_begin, sk_end) of the stream-K
+// units (tiles [0, sk_tiles), kb units each), then dp_waves whole tiles of
+// its own.  Virtual unit v in [0, n_units) names the v-th unit it processes.
+struct CtaWork {
+  long long sk_begin, sk_end;
+  int cta, grid;
+  __device__ long long n_units(const GemmParams& p) const {
+    return (sk_end - sk_begin) + static_cast<long long>(p.dp_waves) * p.kb;
+  }
+  __device__ long long unit(const GemmParams& p, long long v) const {
+    const long long n_sk = sk_end - sk_begin;
+    if (v < n_sk) return sk_begin + v;
+    const long long w = (v - n_sk) / p.kb, k = (v - n_sk) % p.kb;
+    return (static_cast<long long>(p.sk_tiles) + cta + w * grid) * p.kb + k;
+  }
+  // segment seg: tile t, virtual units [v0, v1); false past the last one
+  __device__ bool segment(const GemmParams& p, int seg, int& t, long long& v0, long long& v1) const {
+    const long long n_sk = sk_end - sk_begin;
+    const int n_sk_seg = n_sk > 0 ? static_cast<int>((sk_end - 1) / p.kb - sk_begin / p.kb + 1) : 0;
+    if (seg < n_sk_seg) {
+      t = static_cast<int>(sk_begin / p.kb) + seg;
+      const long long u0 = max(sk_begin, static_cast<long long>(t) * p.kb);
+      const long long u1 = min(sk_end, static_cast<long long>(t + 1) * p.kb);
+      v0 = u0 - sk_begin;
+      v1 = u1 - sk_begin;
+      return true;
+    }
+    const int w = seg - n_sk_seg;
+    if (w >= p.dp_waves) return false;
+    t = p.sk_tiles + cta + w * grid;
+    v0 = n_sk + static_cast<long long>(w) * p.kb;
+    v1 = v0 + p.kb;
+    return true;
+  }
+};
+
+__device__ __forceinline__ CtaWork cta_work(const GemmParams& p) {
+  CtaWork wk;
+  wk.cta = blockIdx.x;
+  wk.grid = gridDim.x;
+  const long long U = static_cast<long long>(p.sk_tiles) * p.kb;
+  wk.sk_begin = static_cast<long long>(wk.cta) * U / wk.grid;
+  wk.sk_end = static_cast<long long>(wk.cta + 1) * U / wk.grid;
+  return wk;
 }
 
 __device__ __forceinline__ void locate_box(const GemmParams& p, int t, int half, int& map, int& row) {
@@ -424,9 +472,9 @@ struct GemmMaps {
   const CUtensorMap *a0, *a1, *a2, *t0, *t1, *t2, *b;
 };
 
-// TMA producer (warp 0, lane 0) over units [u_begin, u_end).
+// TMA producer (warp 0, lane 0) over the CTA's units in order.
 __device__ __forceinline__ void gemm_produce(const GemmParams& p, const Smem& s, const GemmMaps& mp, int lane,
-                                             long long u_begin, long long u_end, volatile int* abort_flag) {
+                                             const CtaWork& wk, volatile int* abort_flag) {
   // ---------------- TMA producer ----------------
   if (lane == 0) {
     int stage = 0;
@@ -461,17 +509,19 @@ __device__ __forceinline__ void gemm_produce(const GemmParams& p, const Smem& s,
     };
     // The first ring's worth of weights does not depend on the previous
     // kernel: it streams while that kernel drains.
-    const long long n_pre = min(static_cast<long long>(p.stages), u_end - u_begin);
+    const long long nv = wk.n_units(p);
+    const long long n_pre = min(static_cast<long long>(p.stages), nv);
     for (long long i = 0; i < n_pre; ++i) {
       sm100::mbar_arrive_expect_tx(&s.full[i], p.a_stage_bytes + p.b_stage_bytes);
-      issue_a(u_begin + i, static_cast<int>(i));
+      issue_a(wk.unit(p, i), static_cast<int>(i));
     }
     pdl_wait();
-    for (long long i = 0; i < n_pre; ++i) issue_b(u_begin + i, static_cast<int>(i));
+    for (long long i = 0; i < n_pre; ++i) issue_b(wk.unit(p, i), static_cast<int>(i));
     issued = n_pre;
     stage = static_cast<int>(n_pre % p.stages);
     phase = n_pre == p.stages ? 1u : 0u;
-    for (long long u = u_begin + n_pre; u < u_end; ++u) {
+    for (long long v = n_pre; v < nv; ++v) {
+      const long long u = wk.unit(p, v);
       if (!sm100::mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
         *abort_flag = 1;
         set_status(p.status, EAGLE_ERR_TIMEOUT);
@@ -497,22 +547,19 @@ __device__ __forceinline__ void gemm_produce(const GemmParams& p, const Smem& s,
   }
 }
 
-// MMA issuer (warp 1, lane 0): one accumulator per tile segment of
-// [u_begin, u_end), double-buffered in tensor memory when two fit.
+// MMA issuer (warp 1, lane 0): one accumulator per tile segment of the
+// CTA's work, double-buffered in tensor memory when two fit.
 __device__ __forceinline__ void gemm_mma(const GemmParams& p, const Smem& s, int lane, uint32_t tmem_base,
-                                         long long u_begin, long long u_end, volatile int* abort_flag) {
-  // ---------------- MMA issuer ----------------
+                                         const CtaWork& wk, volatile int* abort_flag) {
   if (lane == 0) {
     const uint32_t n_total = 2u * p.NP;
     const uint32_t idesc = p.two_mma ? sm100::idesc_bf16_f32(BM, p.NP) : sm100::idesc_bf16_f32(BM, n_total);
     int stage = 0;
     uint32_t phase = 0;
-    int seg = 0;
-    long long u = u_begin;
     bool ok = true;
-    while (u < u_end && ok) {
-      const int t = static_cast<int>(u / p.kb);
-      const long long seg_end = min(u_end, static_cast<long long>(t + 1) * p.kb);
+    int t;
+    long long v0, v1;
+    for (int seg = 0; ok && wk.segment(p, seg, t, v0, v1); ++seg) {
       const int buf = seg % p.n_acc;
       const uint32_t aph = static_cast<uint32_t>(seg / p.n_acc) & 1u;
       if (!sm100::mbar_wait(&s.tempty[buf], aph ^ 1u, abort_flag)) {
@@ -522,8 +569,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, const Smem& s, int
       }
       sm100::tc_fence_after();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
-      const long long seg_start = u;
-      for (; u < seg_end; ++u) {
+      for (long long v = v0; v < v1; ++v) {
         if (!sm100::mbar_wait(&s.full[stage], phase, abort_flag)) {
           *abort_flag = 1;
           set_status(p.status, EAGLE_ERR_TIMEOUT);
@@ -540,7 +586,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, const Smem& s, int
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint32_t off = static_cast<uint32_t>(c) * 1024u + kk * 32;
             const uint64_t ad = sm100::smem_desc_sw128_sbo(a_addr + off, sbo);
-            const uint32_t accum = (u != seg_start || c > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t accum = (v != v0 || c > 0 || kk > 0) ? 1u : 0u;
             sm100::mma_bf16(d_tmem, ad, sm100::smem_desc_sw128_sbo(b_addr + off, sbo), idesc, accum);
             if (p.two_mma)
               sm100::mma_bf16(d_tmem + p.NP, ad, sm100::smem_desc_sw128_sbo(b_addr + b2 + off, sbo), idesc,
@@ -552,7 +598,6 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, const Smem& s, int
       }
       if (!ok) break;
       sm100::mma_commit(&s.tfull[buf]);
-      ++seg;
     }
   }
 }
@@ -565,10 +610,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const Smem s = carve(smem_raw, p);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long T = p.total_units;
   const int G = gridDim.x, cta = blockIdx.x;
-  const long long u_begin = static_cast<long long>(cta) * T / G;
-  const long long u_end = static_cast<long long>(cta + 1) * T / G;
+  const CtaWork wk = cta_work(p);
+  const long long U_sk = static_cast<long long>(p.sk_tiles) * p.kb;
   volatile int* abort_flag = s.flags;
   const GemmMaps maps{&mA0, &mA1, &mA2, &mT0, &mT1, &mT2, &mB};
   pdl_trigger();
@@ -604,10 +648,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *s.tmem_holder;
 
   if (warp == 0) {
-    gemm_produce(p, s, maps, lane, u_begin, u_end, abort_flag);
+    gemm_produce(p, s, maps, lane, wk, abort_flag);
     __syncwarp();
   } else if (warp == 1) {
-    gemm_mma(p, s, lane, tmem_base, u_begin, u_end, abort_flag);
+    gemm_mma(p, s, lane, tmem_base, wk, abort_flag);
     __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
@@ -615,17 +659,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int et = threadIdx.x - 64;            // 0..127
     const int quarter = warp & 3;               // tensor-memory lanes this warp may read
     const int m = quarter * 32 + lane;          // tile row held by this thread
-    int seg = 0;
-    long long u = u_begin;
-    while (u < u_end) {
-      const int t = static_cast<int>(u / p.kb);
-      const long long seg_end = min(u_end, static_cast<long long>(t + 1) * p.kb);
-      u = seg_end;
+    int t;
+    long long v0, v1;
+    for (int seg = 0; wk.segment(p, seg, t, v0, v1); ++seg) {
       const int buf = seg % p.n_acc;
       const uint32_t aph = static_cast<uint32_t>(seg / p.n_acc) & 1u;
-      ++seg;
       // While the tile streams: its epilogue constants and the first row
-      // chunk's inputs from earlier kernels (used only if this CTA finalizes).
+      // chunk's inputs from earlier kernels.
       const EpiCol col = epi_column(p, t, m);
       cp_async_wait_all();                      // the previous segment's copies into s.stg2 have landed
       sm100::named_barrier(1, EPI_THREADS);
@@ -643,6 +683,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       sm100::tc_fence_after();
       const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                  static_cast<uint32_t>(buf * p.acc_stride);
+      int c_first = cta, c_last = cta;
+      if (t < p.sk_tiles) {
+        c_first = cta_of_unit(static_cast<long long>(t) * p.kb, U_sk, G);
+        c_last = cta_of_unit(static_cast<long long>(t) * p.kb + p.kb - 1, U_sk, G);
+      }
+      if (c_first == c_last) {
+        // the whole tile is this CTA's: epilogue straight from tensor memory
+        for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
+          const int nj = min(XCH_ROWS, p.n - jc);
+          for (int c0 = 0; c0 < nj; c0 += 8) {
+            float hi[8], lo[8];
+            sm100::tmem_ld8(lane_addr + jc + c0, hi);
+            sm100::tmem_ld8(lane_addr + p.NP + jc + c0, lo);
+            sm100::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (c0 + i < nj) s.xch[(c0 + i) * BM + m] = hi[i] + lo[i];
+          }
+          sm100::named_barrier(1, EPI_THREADS);
+          epilogue_chunk(p, s, col, t, jc, nj, m, jc == 0);
+        }
+        sm100::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) sm100::mbar_arrive(&s.tempty[buf]);
+        continue;
+      }
       const int slot = t + cta;
       for (int c0 = 0; c0 < p.NP; c0 += 8) {
         float hi[8], lo[8];
@@ -660,8 +726,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) sm100::mbar_arrive(&s.tempty[buf]);
       __threadfence();
       sm100::named_barrier(1, EPI_THREADS);
-      const int c_first = cta_of_unit(static_cast<long long>(t) * p.kb, T, G);
-      const int c_last = cta_of_unit(static_cast<long long>(t) * p.kb + p.kb - 1, T, G);
       if (et == 0) {
         const int prev = atomicAdd(&p.counters[t], 1);
         const int last = prev == c_last - c_first;
@@ -847,6 +911,10 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   }
   int grid = ctx->sm_count;
   if (p.total_units < grid) grid = static_cast<int>(p.total_units);
+  // whole waves of tiles go data-parallel at the end of every CTA's work;
+  // the remaining tiles are split stream-K and processed first
+  p.dp_waves = p.m_tiles / grid;
+  p.sk_tiles = p.m_tiles - p.dp_waves * grid;
   trace_before(ctx, epi, st);
   const cudaError_t e = launch_pdl(gemm_stream_kernel, dim3(grid), dim3(NUM_THREADS), smem, st, maps[0], maps[1],
                                    maps[2], tails[0], tails[1], tails[2], mb, p);
