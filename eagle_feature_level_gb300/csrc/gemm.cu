@@ -481,6 +481,7 @@ __device__ __forceinline__ void gemm_produce(const GemmParams& p, const Smem& s,
     uint32_t phase = 0;
     long long issued = 0;
     const uint32_t group_bytes = static_cast<uint32_t>(p.kps) * 1024u;
+    const uint64_t stream_policy = sm100::l2_policy_evict_first();   // weights are read once per launch
     // weight rows of unit u into ring slot st (64-row halves)
     auto issue_a = [&](long long u, int st) {
       const int t = static_cast<int>(u / p.kb), kz = static_cast<int>(u % p.kb) * p.kps;
@@ -492,13 +493,14 @@ __device__ __forceinline__ void gemm_produce(const GemmParams& p, const Smem& s,
         uint8_t* dst = a_dst + h * 8 * group_bytes;
         if (row + 64 <= p.full_rows[map] && kz + p.kps <= p.full_kb) {
           const CUtensorMap* m4 = map == 0 ? mp.a0 : (map == 1 ? mp.a1 : mp.a2);
-          sm100::tma_load_4d(dst, m4, 0, 0, kz, row >> 3, &s.full[st]);
+          sm100::tma_load_4d_hint(dst, m4, 0, 0, kz, row >> 3, &s.full[st], stream_policy);
         } else {                                   // row or K tail: 8-row x 64-k boxes, zero past the end
           const CUtensorMap* m2 = map == 0 ? mp.t0 : (map == 1 ? mp.t1 : mp.t2);
 #pragma unroll 1
           for (int g = 0; g < 8; ++g)
             for (int c = 0; c < p.kps; ++c)
-              sm100::tma_load_2d(dst + g * group_bytes + c * 1024, m2, (kz + c) * BK, row + 8 * g, &s.full[st]);
+              sm100::tma_load_2d_hint(dst + g * group_bytes + c * 1024, m2, (kz + c) * BK, row + 8 * g, &s.full[st],
+                                      stream_policy);
         }
       }
     };
