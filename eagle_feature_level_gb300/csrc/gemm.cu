@@ -472,81 +472,98 @@ struct GemmMaps {
   const CUtensorMap *a0, *a1, *a2, *t0, *t1, *t2, *b;
 };
 
-// TMA producer (warp 0, lane 0) over the CTA's units in order.
+// Weight rows of unit u into ring slot st (two 64-row halves).
+__device__ __forceinline__ void issue_a(const GemmParams& p, const Smem& s, const GemmMaps& mp, long long u, int st,
+                                        uint64_t policy) {
+  const uint32_t group_bytes = static_cast<uint32_t>(p.kps) * 1024u;
+  const int t = static_cast<int>(u / p.kb), kz = static_cast<int>(u % p.kb) * p.kps;
+  uint8_t* a_dst = s.a + static_cast<size_t>(st) * p.a_stage_bytes;
+#pragma unroll 1
+  for (int h = 0; h < 2; ++h) {
+    int map, row;
+    locate_box(p, t, h, map, row);
+    uint8_t* dst = a_dst + h * 8 * group_bytes;
+    if (row + 64 <= p.full_rows[map] && kz + p.kps <= p.full_kb) {
+      const CUtensorMap* m4 = map == 0 ? mp.a0 : (map == 1 ? mp.a1 : mp.a2);
+      sm100::tma_load_4d_hint(dst, m4, 0, 0, kz, row >> 3, &s.full[st], policy);
+    } else {                                     // row or K tail: 8-row x 64-k boxes, zero past the end
+      const CUtensorMap* m2 = map == 0 ? mp.t0 : (map == 1 ? mp.t1 : mp.t2);
+#pragma unroll 1
+      for (int g = 0; g < 8; ++g)
+        for (int c = 0; c < p.kps; ++c)
+          sm100::tma_load_2d_hint(dst + g * group_bytes + c * 1024, m2, (kz + c) * BK, row + 8 * g, &s.full[st],
+                                  policy);
+    }
+  }
+}
+
+// Activation rows (the previous kernel's output) of unit u into slot st.
+__device__ __forceinline__ void issue_b(const GemmParams& p, const Smem& s, const GemmMaps& mp, long long u, int st) {
+  const int kz = static_cast<int>(u % p.kb) * p.kps;
+  sm100::tma_load_4d(s.b + static_cast<size_t>(st) * p.b_stage_bytes, mp.b, 0, 0, kz, 0, &s.full[st]);
+}
+
+__device__ __forceinline__ long long first_ring(const GemmParams& p, const CtaWork& wk) {
+  return min(static_cast<long long>(p.stages), wk.n_units(p));
+}
+
+// TMA producer (warp 0; lane 0 issues) over the CTA's units in order.  The
+// first ring's weights do not depend on the previous kernel: they stream
+// while it drains.  Their activation boxes are issued by warp 2
+// (gemm_produce_first_b) as soon as the previous kernel has completed, so a
+// CTA that starts late is not held up behind its own weight requests.
 __device__ __forceinline__ void gemm_produce(const GemmParams& p, const Smem& s, const GemmMaps& mp, int lane,
                                              const CtaWork& wk, volatile int* abort_flag) {
-  // ---------------- TMA producer ----------------
-  if (lane == 0) {
-    int stage = 0;
-    uint32_t phase = 0;
-    long long issued = 0;
-    const uint32_t group_bytes = static_cast<uint32_t>(p.kps) * 1024u;
-    const uint64_t stream_policy = sm100::l2_policy_evict_first();   // weights are read once per launch
-    // weight rows of unit u into ring slot st (64-row halves)
-    auto issue_a = [&](long long u, int st) {
-      const int t = static_cast<int>(u / p.kb), kz = static_cast<int>(u % p.kb) * p.kps;
-      uint8_t* a_dst = s.a + static_cast<size_t>(st) * p.a_stage_bytes;
-#pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        int map, row;
-        locate_box(p, t, h, map, row);
-        uint8_t* dst = a_dst + h * 8 * group_bytes;
-        if (row + 64 <= p.full_rows[map] && kz + p.kps <= p.full_kb) {
-          const CUtensorMap* m4 = map == 0 ? mp.a0 : (map == 1 ? mp.a1 : mp.a2);
-          sm100::tma_load_4d_hint(dst, m4, 0, 0, kz, row >> 3, &s.full[st], stream_policy);
-        } else {                                   // row or K tail: 8-row x 64-k boxes, zero past the end
-          const CUtensorMap* m2 = map == 0 ? mp.t0 : (map == 1 ? mp.t1 : mp.t2);
-#pragma unroll 1
-          for (int g = 0; g < 8; ++g)
-            for (int c = 0; c < p.kps; ++c)
-              sm100::tma_load_2d_hint(dst + g * group_bytes + c * 1024, m2, (kz + c) * BK, row + 8 * g, &s.full[st],
-                                      stream_policy);
-        }
-      }
-    };
-    // activation rows (the previous kernel's output) of unit u into slot st
-    auto issue_b = [&](long long u, int st) {
-      const int kz = static_cast<int>(u % p.kb) * p.kps;
-      sm100::tma_load_4d(s.b + static_cast<size_t>(st) * p.b_stage_bytes, mp.b, 0, 0, kz, 0, &s.full[st]);
-    };
-    // The first ring's worth of weights does not depend on the previous
-    // kernel: it streams while that kernel drains.
-    const long long nv = wk.n_units(p);
-    const long long n_pre = min(static_cast<long long>(p.stages), nv);
-    for (long long i = 0; i < n_pre; ++i) {
+  const long long nv = wk.n_units(p);
+  const long long n_pre = first_ring(p, wk);
+  if (lane == 0)
+    for (long long i = 0; i < n_pre; ++i)
       sm100::mbar_arrive_expect_tx(&s.full[i], p.a_stage_bytes + p.b_stage_bytes);
-      issue_a(wk.unit(p, i), static_cast<int>(i));
+  __syncwarp();
+  sm100::named_barrier_arrive(2, 64);          // the first ring's expected bytes are set
+  if (lane != 0) return;
+  const uint64_t policy = sm100::l2_policy_evict_first();   // weights are read once per launch
+  for (long long i = 0; i < n_pre; ++i) issue_a(p, s, mp, wk.unit(p, i), static_cast<int>(i), policy);
+  pdl_wait();
+  long long issued = n_pre;
+  int stage = static_cast<int>(n_pre % p.stages);
+  uint32_t phase = n_pre == p.stages ? 1u : 0u;
+  for (long long v = n_pre; v < nv; ++v) {
+    const long long u = wk.unit(p, v);
+    if (!sm100::mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
+      *abort_flag = 1;
+      set_status(p.status, EAGLE_ERR_TIMEOUT);
+      break;
     }
-    pdl_wait();
-    for (long long i = 0; i < n_pre; ++i) issue_b(wk.unit(p, i), static_cast<int>(i));
-    issued = n_pre;
-    stage = static_cast<int>(n_pre % p.stages);
-    phase = n_pre == p.stages ? 1u : 0u;
-    for (long long v = n_pre; v < nv; ++v) {
-      const long long u = wk.unit(p, v);
-      if (!sm100::mbar_wait(&s.empty[stage], phase ^ 1u, abort_flag)) {
-        *abort_flag = 1;
-        set_status(p.status, EAGLE_ERR_TIMEOUT);
-        break;
-      }
-      sm100::mbar_arrive_expect_tx(&s.full[stage], p.a_stage_bytes + p.b_stage_bytes);
-      issue_a(u, stage);
-      issue_b(u, stage);
-      ++issued;
-      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
-    }
-    if (*abort_flag) {
-      // let copies already in flight land before the CTA exits
-      const long long pending = issued < p.stages ? issued : p.stages;
-      for (long long i = 0; i < pending; ++i) {
-        stage = stage == 0 ? p.stages - 1 : stage - 1;
-        if (stage == p.stages - 1) phase ^= 1u;
-        const uint64_t t0 = globaltimer_ns();
-        while (!sm100::mbar_try_wait(&s.full[stage], phase) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
-        }
+    sm100::mbar_arrive_expect_tx(&s.full[stage], p.a_stage_bytes + p.b_stage_bytes);
+    issue_a(p, s, mp, u, stage, policy);
+    issue_b(p, s, mp, u, stage);
+    ++issued;
+    if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+  }
+  if (*abort_flag) {
+    // let copies already in flight land before the CTA exits
+    const long long pending = issued < p.stages ? issued : p.stages;
+    for (long long i = 0; i < pending; ++i) {
+      stage = stage == 0 ? p.stages - 1 : stage - 1;
+      if (stage == p.stages - 1) phase ^= 1u;
+      const uint64_t t0 = globaltimer_ns();
+      while (!sm100::mbar_try_wait(&s.full[stage], phase) && globaltimer_ns() - t0 < WAIT_LIMIT_NS) {
       }
     }
   }
+}
+
+// Warp 2, before its epilogue work: the activation boxes of the first ring.
+__device__ __forceinline__ void gemm_produce_first_b(const GemmParams& p, const Smem& s, const GemmMaps& mp, int lane,
+                                                     const CtaWork& wk) {
+  sm100::named_barrier(2, 64);                 // warp 0 has set the expected bytes
+  if (lane == 0) {
+    pdl_wait();
+    const long long n_pre = first_ring(p, wk);
+    for (long long i = 0; i < n_pre; ++i) issue_b(p, s, mp, wk.unit(p, i), static_cast<int>(i));
+  }
+  __syncwarp();
 }
 
 // MMA issuer (warp 1, lane 0): one accumulator per tile segment of the
@@ -657,6 +674,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
+    if (warp == 2) gemm_produce_first_b(p, s, maps, lane, wk);
     pdl_wait();                                 // residuals, norms, positions of earlier kernels
     const int et = threadIdx.x - 64;            // 0..127
     const int quarter = warp & 3;               // tensor-memory lanes this warp may read

@@ -201,6 +201,10 @@ __device__ __forceinline__ void tmem_wait_ld() {
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
+// Arrive on named barrier `id` without waiting (every thread of the warp).
+__device__ __forceinline__ void named_barrier_arrive(int id, int threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // ---- thread-block clusters and distributed shared memory -------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
