@@ -62,10 +62,7 @@ eagle_status check_plan(const eagle_ctx* c, const eagle_plan* p) {
   return EAGLE_OK;
 }
 
-int splits_bound(const eagle_ctx* c, int pairs) {
-  int s = ceil_div(2 * c->sm_count, std::max(1, pairs));
-  return std::min(31, std::max(1, s));
-}
+int splits_bound(const eagle_ctx* c, int pairs) { return attn_splits_bound(c, pairs); }
 
 void layout(eagle_ctx* c) {
   const eagle_dims& D = c->dims;

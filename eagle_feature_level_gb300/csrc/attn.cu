@@ -2,10 +2,11 @@
 // verification layer ([B] "Tree Attention 如何一次验证多条路径": node u sees the
 // committed prefix plus the tree nodes that are its ancestors or itself).
 //
-// Split-KV layout: one CTA per (prefix split or tree part, request, kv head).
-// Every query row of the request that maps to this kv head (tree nodes x GQA
-// group) consumes the same shared-memory K/V tile, so prefix KV bytes are
-// read from HBM once per call however many tree nodes there are.  Each CTA
+// Split-KV layout: one CTA per (prefix split or tree part, request, kv head),
+// one wave at four CTAs per SM.  Every query row of the request that maps to
+// this kv head (tree nodes x GQA group) consumes the same shared-memory K/V
+// tile, so prefix KV bytes are read from HBM once per call however many tree
+// nodes there are.  Each CTA
 // writes (max, sum, unnormalised output) partials; the last CTA of a
 // (request, kv head) merges them in split order.  The ancestor mask of each
 // query row lives in a register (one 64-bit word) and is tested per tree key.
@@ -18,18 +19,25 @@
 namespace eagle {
 namespace {
 
-constexpr int TILE = 64;          // KV rows per shared-memory tile
-constexpr int THREADS = 256;
+constexpr int TILE = 64;          // prefix / verify-tree keys per shared-memory tile (bf16)
+constexpr int TILE_F32 = 32;      // draft-tree keys per tile (fp32, same bytes)
+constexpr int THREADS = 128;
 constexpr int WARPS = THREADS / 32;
 constexpr int MAX_DH = 128;
-constexpr int RW = 8;             // query rows a warp owns in one pass
+constexpr int RW = 8;             // query rows a warp owns in one pass, at most
 constexpr int ROWS_PASS = WARPS * RW;
-constexpr int PF = TILE * (MAX_DH / 8) / THREADS;   // 16-byte prefix pieces per thread per K (or V) tile
+constexpr int KLD = MAX_DH + 8;   // bf16 row pitch of a tile in shared memory (elements)
+
+// Shared-memory bytes of one K+V tile buffer: 64 bf16 rows of K and of V,
+// or 32 fp32 rows of each (dh + 4 floats per row).
+constexpr size_t TILE_BYTES = static_cast<size_t>(2) * TILE * KLD * 2;
+static_assert(static_cast<size_t>(2) * TILE_F32 * (MAX_DH + 4) * 4 <= TILE_BYTES, "fp32 half tile fits a buffer");
 
 struct AttnParams {
   int mode;                       // 0 draft, 1 verify
   int B, Hq, Hkv, dh, G;
   int n_splits, chunk;            // prefix splits and rows per split (a multiple of TILE)
+  int n_buf;                      // tile buffers per CTA (2: the next prefix tile streams in)
   int rows_cap;                   // query nodes per request (draft: rows per request; verify: tree stride)
   int rows_pass;                  // query rows staged per pass: min(ROWS_PASS, rows_cap * G)
   const float* q_f32;             // draft: [n][Hq*dh] fp32
@@ -67,262 +75,191 @@ __device__ __forceinline__ uint64_t row_mask(const AttnParams& p, int b, int nod
   return p.anc[static_cast<size_t>(b) * p.tree_cap + node];
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 w, float* dst) {
-  float4 a, b;
-  a.x = __uint_as_float(w.x << 16); a.y = __uint_as_float(w.x & 0xffff0000u);
-  a.z = __uint_as_float(w.y << 16); a.w = __uint_as_float(w.y & 0xffff0000u);
-  b.x = __uint_as_float(w.z << 16); b.y = __uint_as_float(w.z & 0xffff0000u);
-  b.z = __uint_as_float(w.w << 16); b.w = __uint_as_float(w.w & 0xffff0000u);
-  *reinterpret_cast<float4*>(dst) = a;
-  *reinterpret_cast<float4*>(dst + 4) = b;
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(sm100::smem_u32(dst)), "l"(src),
+               "l"(policy)
+               : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// A bf16 prefix tile in flight: piece i of this thread is row (tid + i*THREADS)
-// / (dh/8), 8 columns.  Loads are issued for the next tile before the current
-// one is consumed; rows past the tile's end stay zero.
-struct PrefixTile {
-  uint4 k[PF], v[PF];
-};
-
-// 16-byte read-only load whose L2 line is replaced first (the prefix KV is
-// read once per launch).
-__device__ __forceinline__ uint4 ld_stream16(const void* ptr, uint64_t policy) {
-  uint4 r;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(ptr), "l"(policy));
-  return r;
-}
-
-__device__ __forceinline__ void prefix_load(PrefixTile& t, const uint16_t* kb, const uint16_t* vb, size_t row0,
-                                            size_t row_stride, int nt, int dh) {
-  const uint64_t policy = sm100::l2_policy_evict_first();
+// Copies one bf16 tile (keys t0 .. t0 + nt - 1 of kv head h) into buf as K
+// rows [TILE][KLD] then V rows; rows past nt are zeroed.  Issued by all
+// threads as 16-byte asynchronous copies (one commit group per tile).
+__device__ __forceinline__ void stage_bf16(uint16_t* buf, const uint16_t* kb, const uint16_t* vb, size_t row0,
+                                           size_t row_stride, int nt, int dh, uint64_t policy) {
+  uint16_t* sk = buf;
+  uint16_t* sv = buf + TILE * KLD;
   const int pieces = dh >> 3;
-#pragma unroll
-  for (int i = 0; i < PF; ++i) {
-    const int idx = threadIdx.x + i * THREADS;
+  for (int idx = threadIdx.x; idx < TILE * pieces; idx += THREADS) {
     const int r = idx / pieces, c = idx - r * pieces;
     if (r < nt) {
-      t.k[i] = ld_stream16(reinterpret_cast<const uint4*>(kb + row0 + r * row_stride) + c, policy);
-      t.v[i] = ld_stream16(reinterpret_cast<const uint4*>(vb + row0 + r * row_stride) + c, policy);
+      cp_async16(sk + r * KLD + 8 * c, kb + row0 + r * row_stride + 8 * c, policy);
+      cp_async16(sv + r * KLD + 8 * c, vb + row0 + r * row_stride + 8 * c, policy);
     } else {
-      t.k[i] = make_uint4(0u, 0u, 0u, 0u);
-      t.v[i] = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sk + r * KLD + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sv + r * KLD + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
     }
   }
+  cp_async_commit();
 }
 
-__device__ __forceinline__ void prefix_store(const PrefixTile& t, float* sk, float* sv, int ld, int dh) {
-  const int pieces = dh >> 3;
-#pragma unroll
-  for (int i = 0; i < PF; ++i) {
-    const int idx = threadIdx.x + i * THREADS;
+// Copies draft-tree keys k0 .. k0 + nt - 1 (fp32, at most TILE_F32) into buf
+// as K rows [TILE_F32][dh + 4] then V rows; rows past nt are zeroed.
+__device__ __forceinline__ void stage_f32(float* buf, const float* kf, const float* vf, size_t row0,
+                                          size_t row_stride, int nt, int dh) {
+  const int ld = dh + 4;
+  float* sk = buf;
+  float* sv = buf + TILE_F32 * ld;
+  const int pieces = dh >> 2;
+  const uint64_t policy = sm100::l2_policy_evict_first();
+  for (int idx = threadIdx.x; idx < TILE_F32 * pieces; idx += THREADS) {
     const int r = idx / pieces, c = idx - r * pieces;
-    if (r < TILE) {
-      bf16x8_to_f32(t.k[i], sk + r * ld + c * 8);
-      bf16x8_to_f32(t.v[i], sv + r * ld + c * 8);
+    if (r < nt) {
+      cp_async16(sk + r * ld + 4 * c, kf + row0 + r * row_stride + 4 * c, policy);
+      cp_async16(sv + r * ld + 4 * c, vf + row0 + r * row_stride + 4 * c, policy);
+    } else {
+      *reinterpret_cast<float4*>(sk + r * ld + 4 * c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(sv + r * ld + 4 * c) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
+  cp_async_commit();
 }
 
-// The tree part (at most one tile): fp32 (draft) or bf16 (verify) rows, zero past nt.
-__device__ __forceinline__ void tree_stage(const AttnParams& p, float* sk, float* sv, int ld, size_t row0,
-                                           size_t row_stride, int nt) {
-  const int dh = p.dh;
-  if (p.mode == 0) {
-    const int pieces = dh >> 2;
-    for (int idx = threadIdx.x; idx < TILE * pieces; idx += THREADS) {
-      const int r = idx / pieces, c = idx - r * pieces;
-      float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
-      if (r < nt) {
-        kk = __ldg(reinterpret_cast<const float4*>(p.kt_f32 + row0 + r * row_stride) + c);
-        vv = __ldg(reinterpret_cast<const float4*>(p.vt_f32 + row0 + r * row_stride) + c);
-      }
-      *reinterpret_cast<float4*>(sk + r * ld + c * 4) = kk;
-      *reinterpret_cast<float4*>(sv + r * ld + c * 4) = vv;
-    }
-  } else {
-    const int pieces = dh >> 3;
-    for (int idx = threadIdx.x; idx < TILE * pieces; idx += THREADS) {
-      const int r = idx / pieces, c = idx - r * pieces;
-      uint4 kk = make_uint4(0u, 0u, 0u, 0u), vv = kk;
-      if (r < nt) {
-        kk = __ldg(reinterpret_cast<const uint4*>(p.kt_bf16 + row0 + r * row_stride) + c);
-        vv = __ldg(reinterpret_cast<const uint4*>(p.vt_bf16 + row0 + r * row_stride) + c);
-      }
-      bf16x8_to_f32(kk, sk + r * ld + c * 8);
-      bf16x8_to_f32(vv, sv + r * ld + c * 8);
-    }
-  }
+__device__ __forceinline__ float4 bf16x4(uint2 w) {
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u), __uint_as_float(w.y << 16),
+                     __uint_as_float(w.y & 0xffff0000u));
 }
 
-// Per-CTA constants of one attention launch, shared by the pass bodies.
-struct PassCtx {
-  int b, h, warp, lane, dh, ld, lo, hi, rec, split, dcol;
-  bool is_tree, has_cols;
-  size_t row_stride;
-  float *sk, *sv, *sq, *sp;
-  uint64_t* s_mask;
+// Running softmax state of the rows a warp owns in a pass.
+template <int NR>
+struct RowState {
+  float m[NR], l[NR], acc[NR][4];
 };
 
-// One pass over this CTA's keys for query rows r0 .. r0 + rp - 1; warp w owns
-// rows w + 8 i, i < nr <= NR.  The kernel is instantiated for NR = 1, 2, 4, 8
-// (chosen from the launch's rows per pass) so that a warp issues work only
-// for row slots that can exist: with one query row per warp the unrolled
-// code of eight would cost eight times the issue slots.
-template <int NR>
-__device__ __forceinline__ void attn_pass(const AttnParams& p, const PassCtx& x, int r0, int rp) {
-  const int b = x.b, h = x.h, warp = x.warp, lane = x.lane, dh = x.dh, ld = x.ld, lo = x.lo, hi = x.hi;
-  const int rec = x.rec, split = x.split, dcol = x.dcol;
-  const bool is_tree = x.is_tree, has_cols = x.has_cols;
-  const size_t row_stride = x.row_stride;
-  float *sk = x.sk, *sv = x.sv, *sq = x.sq, *sp = x.sp;
-  uint64_t* s_mask = x.s_mask;
-  const int nr = rp > warp ? (rp - warp + WARPS - 1) / WARPS : 0;   // <= NR
-  // The prefix KV is not written by the kernels of this draft step: its
-  // first tile is requested before waiting on the predecessor.
-  PrefixTile pre;
-  if (!is_tree && lo < hi)
-    prefix_load(pre, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + lo) * p.Hkv + h) * dh, row_stride,
-                min(TILE, hi - lo), dh);
-  if (r0 == 0) pdl_wait();                 // q rows, tree K/V and masks come from the predecessors
-  __syncthreads();                         // previous pass done with sq
-  for (int idx = threadIdx.x; idx < rp * (dh >> 2); idx += THREADS) {
-    const int rr = idx / (dh >> 2), c = idx - rr * (dh >> 2);
-    const int r = r0 + rr, node = r / p.G, hq = h * p.G + r % p.G;
-    const size_t qo = q_index(p, b, node, hq) + 4 * c;
-    float4 v;
-    if (p.mode == 0) {
-      v = *reinterpret_cast<const float4*>(p.q_f32 + qo);
-    } else {
-      const uint2 w = *reinterpret_cast<const uint2*>(p.q_bf16 + qo);
-      v.x = __uint_as_float(w.x << 16); v.y = __uint_as_float(w.x & 0xffff0000u);
-      v.z = __uint_as_float(w.y << 16); v.w = __uint_as_float(w.y & 0xffff0000u);
-    }
-    *reinterpret_cast<float4*>(sq + rr * dh + 4 * c) = v;
-  }
-  if (is_tree && lane < RW && lane < nr)
-    s_mask[warp * RW + lane] = row_mask(p, b, (r0 + warp + WARPS * lane) / p.G);
-  float m_run[NR], l_run[NR], acc[NR][4];
+// One staged tile against the warp's rows: scores of the lane's keys (lane
+// and lane + 32 for a bf16 tile, lane for an fp32 half tile), the online
+// softmax, and acc += P V (lane = 4 output columns).  `tmask` holds bit j of
+// tile key j for the tree part (all ones for prefix tiles).
+template <int NR, bool F32>
+__device__ __forceinline__ void tile_compute(const AttnParams& p, RowState<NR>& st, const void* buf, const float* sq,
+                                             float* sp, const uint64_t* s_mask, int warp, int lane, int nr, int nt,
+                                             int key_base, bool is_tree) {
+  const int dh = p.dh;
+  constexpr int KEYS = F32 ? TILE_F32 : TILE;
+  float s0[NR], s1[NR];
 #pragma unroll
-  for (int i = 0; i < NR; ++i) {
-    m_run[i] = -INFINITY;
-    l_run[i] = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
-  }
-
-  for (int t0 = lo; t0 < hi; t0 += TILE) {
-    const int nt = min(TILE, hi - t0);
-    __syncthreads();                       // all warps done with the previous tile
-    if (!is_tree) {
-      prefix_store(pre, sk, sv, ld, dh);
-      if (t0 + TILE < hi)                  // next tile's loads fly while this one is consumed
-        prefix_load(pre, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + t0 + TILE) * p.Hkv + h) * dh,
-                    row_stride, min(TILE, hi - t0 - TILE), dh);
-    } else {
-      tree_stage(p, sk, sv, ld, ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh, row_stride, nt);
-    }
-    __syncthreads();
-    if (nr == 0) continue;
-
-    // scores of keys lane and lane + 32 for each owned row
-    float s0[NR], s1[NR];
-#pragma unroll
-    for (int i = 0; i < NR; ++i) { s0[i] = 0.f; s1[i] = 0.f; }
-    const float* k0 = sk + lane * ld;
-    const float* k1 = sk + (lane + 32) * ld;
+  for (int i = 0; i < NR; ++i) { s0[i] = 0.f; s1[i] = 0.f; }
+  if (F32) {
+    const int ld = dh + 4;
+    const float* k0 = static_cast<const float*>(buf) + lane * ld;
     for (int d = 0; d < dh; d += 4) {
       const float4 a = *reinterpret_cast<const float4*>(k0 + d);
-      const float4 c = *reinterpret_cast<const float4*>(k1 + d);
 #pragma unroll
       for (int i = 0; i < NR; ++i) {
         if (i < nr) {
           const float4 q = *reinterpret_cast<const float4*>(sq + (warp + WARPS * i) * dh + d);
-          // plain FMA chains: the 2 x NR independent (row, key) sums give the ILP
           s0[i] = fmaf(q.w, a.w, fmaf(q.z, a.z, fmaf(q.y, a.y, fmaf(q.x, a.x, s0[i]))));
-          s1[i] = fmaf(q.w, c.w, fmaf(q.z, c.z, fmaf(q.y, c.y, fmaf(q.x, c.x, s1[i]))));
         }
       }
     }
-    // online softmax per row; probabilities to this warp's shared rows
+  } else {
+    const uint16_t* k0 = static_cast<const uint16_t*>(buf) + lane * KLD;
+    const uint16_t* k1 = k0 + 32 * KLD;
+    for (int d = 0; d < dh; d += 8) {
+      const uint4 wa = *reinterpret_cast<const uint4*>(k0 + d);
+      const uint4 wc = *reinterpret_cast<const uint4*>(k1 + d);
+      const float4 a0 = bf16x4(make_uint2(wa.x, wa.y)), a1 = bf16x4(make_uint2(wa.z, wa.w));
+      const float4 c0 = bf16x4(make_uint2(wc.x, wc.y)), c1 = bf16x4(make_uint2(wc.z, wc.w));
 #pragma unroll
-    for (int i = 0; i < NR; ++i) {
-      if (i < nr) {
-        // tree keys: one tile (t0 == 0), bit j of the row's ancestor mask
-        const uint64_t mask = is_tree ? s_mask[warp * RW + i] : ~0ull;
-        const bool v0 = lane < nt && ((mask >> lane) & 1ull);
-        const bool v1 = lane + 32 < nt && ((mask >> (lane + 32)) & 1ull);
-        const float a = v0 ? s0[i] * p.scale : -INFINITY;
-        const float c = v1 ? s1[i] * p.scale : -INFINITY;
-        const float m_new = fmaxf(m_run[i], warp_max(fmaxf(a, c)));
-        float p0 = 0.f, p1 = 0.f, corr = 1.f;
-        if (m_new != -INFINITY) {
-          p0 = __expf(a - m_new);
-          p1 = __expf(c - m_new);
-          corr = __expf(m_run[i] - m_new);
-        }
-        l_run[i] = l_run[i] * corr + warp_sum(p0 + p1);
-        m_run[i] = m_new;
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) acc[i][c4] *= corr;
-        sp[i * TILE + lane] = p0;
-        sp[i * TILE + lane + 32] = p1;
-      }
-    }
-    __syncwarp();
-    // acc += P V over the tile, 4 keys per step (V rows past nt are zero)
-    if (has_cols) {
-      for (int j = 0; j < nt; j += 4) {
-        float4 vv[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) vv[u] = *reinterpret_cast<const float4*>(sv + (j + u) * ld + dcol);
-#pragma unroll
-        for (int i = 0; i < NR; ++i) {
-          if (i < nr) {
-            const float4 pj = *reinterpret_cast<const float4*>(sp + i * TILE + j);
-            acc[i][0] = fmaf(pj.x, vv[0].x, fmaf(pj.y, vv[1].x, fmaf(pj.z, vv[2].x, fmaf(pj.w, vv[3].x, acc[i][0]))));
-            acc[i][1] = fmaf(pj.x, vv[0].y, fmaf(pj.y, vv[1].y, fmaf(pj.z, vv[2].y, fmaf(pj.w, vv[3].y, acc[i][1]))));
-            acc[i][2] = fmaf(pj.x, vv[0].z, fmaf(pj.y, vv[1].z, fmaf(pj.z, vv[2].z, fmaf(pj.w, vv[3].z, acc[i][2]))));
-            acc[i][3] = fmaf(pj.x, vv[0].w, fmaf(pj.y, vv[1].w, fmaf(pj.z, vv[2].w, fmaf(pj.w, vv[3].w, acc[i][3]))));
-          }
+      for (int i = 0; i < NR; ++i) {
+        if (i < nr) {
+          const float* qr = sq + (warp + WARPS * i) * dh + d;
+          const float4 q0 = *reinterpret_cast<const float4*>(qr);
+          const float4 q1 = *reinterpret_cast<const float4*>(qr + 4);
+          float x = fmaf(q0.w, a0.w, fmaf(q0.z, a0.z, fmaf(q0.y, a0.y, fmaf(q0.x, a0.x, s0[i]))));
+          s0[i] = fmaf(q1.w, a1.w, fmaf(q1.z, a1.z, fmaf(q1.y, a1.y, fmaf(q1.x, a1.x, x))));
+          float y = fmaf(q0.w, c0.w, fmaf(q0.z, c0.z, fmaf(q0.y, c0.y, fmaf(q0.x, c0.x, s1[i]))));
+          s1[i] = fmaf(q1.w, c1.w, fmaf(q1.z, c1.z, fmaf(q1.y, c1.y, fmaf(q1.x, c1.x, y))));
         }
       }
     }
-    __syncwarp();
   }
+  // online softmax per row; probabilities to this warp's shared rows
 #pragma unroll
   for (int i = 0; i < NR; ++i) {
     if (i < nr) {
-      const int r = r0 + warp + WARPS * i;
-      const int node = r / p.G, hq = h * p.G + r % p.G;
-      const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
-      float* dst = p.part + (qi * (p.n_splits + 1) + split) * rec;
-      if (lane == 0) {
-        dst[0] = m_run[i];
-        dst[1] = l_run[i];
+      // tree keys: bit (key_base + j) of the row's ancestor mask (one tile of <= 64 slots)
+      const uint64_t mask = is_tree ? s_mask[warp * RW + i] : ~0ull;
+      const int j0 = lane, j1 = lane + 32;
+      const bool v0 = j0 < nt && ((mask >> (key_base + j0)) & 1ull);
+      const bool v1 = !F32 && j1 < nt && ((mask >> (key_base + (j1 & 63))) & 1ull);
+      const float a = v0 ? s0[i] * p.scale : -INFINITY;
+      const float c = v1 ? s1[i] * p.scale : -INFINITY;
+      const float m_new = fmaxf(st.m[i], warp_max(fmaxf(a, c)));
+      float p0 = 0.f, p1 = 0.f, corr = 1.f;
+      if (m_new != -INFINITY) {
+        p0 = __expf(a - m_new);
+        p1 = __expf(c - m_new);
+        corr = __expf(st.m[i] - m_new);
       }
-      if (has_cols) {
+      st.l[i] = st.l[i] * corr + warp_sum(p0 + p1);
+      st.m[i] = m_new;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) dst[2 + dcol + c] = acc[i][c];
+      for (int c4 = 0; c4 < 4; ++c4) st.acc[i][c4] *= corr;
+      sp[i * TILE + lane] = p0;
+      if (!F32) sp[i * TILE + lane + 32] = p1;
+    }
+  }
+  __syncwarp();
+  // acc += P V over the tile, 4 keys per step (rows past nt are zero)
+  const int dcol = 4 * lane;
+  if (dcol < dh) {
+    for (int j = 0; j < nt; j += 4) {
+      float4 vv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (F32) {
+          vv[u] = *reinterpret_cast<const float4*>(static_cast<const float*>(buf) + (KEYS + j + u) * (dh + 4) + dcol);
+        } else {
+          vv[u] = bf16x4(*reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(buf) + (KEYS + j + u) * KLD +
+                                                         dcol));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < NR; ++i) {
+        if (i < nr) {
+          const float4 pj = *reinterpret_cast<const float4*>(sp + i * TILE + j);
+          st.acc[i][0] = fmaf(pj.x, vv[0].x, fmaf(pj.y, vv[1].x, fmaf(pj.z, vv[2].x, fmaf(pj.w, vv[3].x, st.acc[i][0]))));
+          st.acc[i][1] = fmaf(pj.x, vv[0].y, fmaf(pj.y, vv[1].y, fmaf(pj.z, vv[2].y, fmaf(pj.w, vv[3].y, st.acc[i][1]))));
+          st.acc[i][2] = fmaf(pj.x, vv[0].z, fmaf(pj.y, vv[1].z, fmaf(pj.z, vv[2].z, fmaf(pj.w, vv[3].z, st.acc[i][2]))));
+          st.acc[i][3] = fmaf(pj.x, vv[0].w, fmaf(pj.y, vv[1].w, fmaf(pj.z, vv[2].w, fmaf(pj.w, vv[3].w, st.acc[i][3]))));
+        }
       }
     }
   }
+  __syncwarp();
 }
 
-// Dynamic shared memory: K tile, V tile ([TILE][dh+4] fp32 each; the 4-word
-// pad makes lane-per-row float4 reads conflict-free), the pass's query rows
-// [rows_pass][dh] and each warp's probabilities [WARPS][RW][TILE].
+// Dynamic shared memory: n_buf tile buffers (TILE_BYTES each), the pass's
+// query rows [rows_pass][dh] fp32, and each warp's probabilities
+// [WARPS][RW][TILE].
 //
-// Warp w owns query rows w + 8 i of the pass: it scores them against the tile
-// (lane = keys lane and lane + 32), runs the online softmax and accumulates
-// P V for them (lane = 4 output columns), so after the tile is staged no
-// further block-wide barrier is needed.
+// One CTA per (prefix split or tree part, request, kv head).  Warp w owns
+// query rows w + 4 i of a pass: it scores them against the staged tile,
+// runs the online softmax and accumulates P V for them, so a staged tile
+// needs no further block-wide barrier.  Prefix tiles are bf16 copied by
+// cp.async (the next one streams in while the current one is consumed when a
+// split holds several); the draft's fp32 tree part is consumed as two
+// 32-key halves of the same buffer.  The kernel is instantiated for NR = 1,
+// 2, 4, 8 rows per warp so that a warp issues work only for row slots that
+// can exist.
 template <int NR>
-__global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams p) {
   pdl_trigger();
   if (p.mode == 1) pdl_wait();               // verification reads the tree's size first
-  extern __shared__ __align__(16) float smem_attn[];
+  extern __shared__ __align__(16) uint8_t smem_attn[];
   __shared__ int s_last;
   __shared__ uint64_t s_mask[ROWS_PASS];     // ancestor masks of the tree part's rows
 
@@ -331,14 +268,13 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams 
   const int b = pair / p.Hkv, h = pair % p.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int dh = p.dh;
-  const int ld = dh + 4;
-  float* sk = smem_attn;
-  float* sv = sk + TILE * ld;
-  float* sq = sv + TILE * ld;
+  uint8_t* bufs = smem_attn;
+  float* sq = reinterpret_cast<float*>(smem_attn + p.n_buf * TILE_BYTES);
   float* sp = sq + p.rows_pass * dh + (warp * RW) * TILE;
   const int nodes = n_nodes(p, b);
   const int R = nodes * p.G;
   const bool is_tree = split == p.n_splits;
+  const bool tree_f32 = is_tree && p.mode == 0;
   int lo = 0, hi = 0;
   if (!is_tree) {
     const int L = p.kv_len[b];
@@ -349,16 +285,111 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams 
   }
   const int rec = dh + 2;
   const size_t row_stride = static_cast<size_t>(p.Hkv) * dh;
-  const int dcol = 4 * lane;                 // this lane's output columns
-  const bool has_cols = dcol < dh;
+  const uint64_t policy = sm100::l2_policy_evict_first();
+  const int step = tree_f32 ? TILE_F32 : TILE;
+  const int n_tiles = hi > lo ? (hi - lo + step - 1) / step : 0;
+  // A split whose keys fit one buffer stages them once for every pass.
+  const bool resident = n_tiles <= 1;
 
-  const PassCtx x{b, h, warp, lane, dh, ld, lo, hi, rec, split, dcol, is_tree, has_cols, row_stride,
-                  sk, sv, sq, sp, s_mask};
+  auto stage = [&](int tile, int which) {
+    uint8_t* buf = bufs + which * TILE_BYTES;
+    const int t0 = lo + tile * step, nt = min(step, hi - t0);
+    if (tree_f32)
+      stage_f32(reinterpret_cast<float*>(buf), p.kt_f32, p.vt_f32,
+                ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh, row_stride, nt, dh);
+    else if (is_tree)
+      stage_bf16(reinterpret_cast<uint16_t*>(buf), p.kt_bf16, p.vt_bf16,
+                 ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh, row_stride, nt, dh, policy);
+    else
+      stage_bf16(reinterpret_cast<uint16_t*>(buf), p.kp, p.vp,
+                 ((static_cast<size_t>(b) * p.kv_cap + t0) * p.Hkv + h) * dh, row_stride, nt, dh, policy);
+  };
+  // The prefix KV is not written by the kernels of this draft step: its
+  // first tile is requested before waiting on the predecessor.
+  if (!is_tree && n_tiles > 0) stage(0, 0);
+  pdl_wait();                                // q rows, tree K/V and masks come from the predecessors
+  if (is_tree && n_tiles > 0) stage(0, 0);
+
   for (int r0 = 0; r0 < R; r0 += p.rows_pass) {
-    attn_pass<NR>(p, x, r0, min(p.rows_pass, R - r0));
+    const int rp = min(p.rows_pass, R - r0);
+    const int nr = rp > warp ? (rp - warp + WARPS - 1) / WARPS : 0;   // <= NR
+    if (r0 > 0) __syncthreads();             // the previous pass is done with sq (and the buffers)
+    for (int idx = threadIdx.x; idx < rp * (dh >> 2); idx += THREADS) {
+      const int rr = idx / (dh >> 2), c = idx - rr * (dh >> 2);
+      const int r = r0 + rr, node = r / p.G, hq = h * p.G + r % p.G;
+      const size_t qo = q_index(p, b, node, hq) + 4 * c;
+      float4 v;
+      if (p.mode == 0) {
+        v = *reinterpret_cast<const float4*>(p.q_f32 + qo);
+      } else {
+        const uint2 w = *reinterpret_cast<const uint2*>(p.q_bf16 + qo);
+        v = bf16x4(w);
+      }
+      *reinterpret_cast<float4*>(sq + rr * dh + 4 * c) = v;
+    }
+    if (is_tree && lane < RW && lane < nr)
+      s_mask[warp * RW + lane] = row_mask(p, b, (r0 + warp + WARPS * lane) / p.G);
+    RowState<NR> st;
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      st.m[i] = -INFINITY;
+      st.l[i] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) st.acc[i][c] = 0.f;
+    }
+    for (int tile = 0; tile < n_tiles; ++tile) {
+      const int which = p.n_buf > 1 ? (tile & 1) : 0;
+      if (!resident) {
+        // staged earlier: tile 0 of the first pass (prologue), or by the
+        // previous iteration's prefetch when two buffers alternate
+        const bool staged = (r0 == 0 && tile == 0) || (p.n_buf > 1 && tile > 0);
+        if (!staged) {
+          __syncthreads();                   // every warp is done with this buffer
+          stage(tile, which);
+        }
+        if (p.n_buf > 1 && tile + 1 < n_tiles) {
+          __syncthreads();                   // the other buffer's previous tile is consumed
+          stage(tile + 1, which ^ 1);
+          cp_async_wait<1>();                // this tile's copies have landed
+        } else {
+          cp_async_wait<0>();
+        }
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncthreads();
+      if (nr > 0) {
+        const int t0 = lo + tile * step;
+        const int nt = min(step, hi - t0);
+        const uint8_t* buf = bufs + which * TILE_BYTES;
+        if (tree_f32)
+          tile_compute<NR, true>(p, st, buf, sq, sp, s_mask, warp, lane, nr, nt, t0, true);
+        else
+          tile_compute<NR, false>(p, st, buf, sq, sp, s_mask, warp, lane, nr, nt, is_tree ? t0 : 0, is_tree);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+      if (i < nr) {
+        const int r = r0 + warp + WARPS * i;
+        const int node = r / p.G, hq = h * p.G + r % p.G;
+        const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
+        float* dst = p.part + (qi * (p.n_splits + 1) + split) * rec;
+        if (lane == 0) {
+          dst[0] = st.m[i];
+          dst[1] = st.l[i];
+        }
+        // records are dh + 2 floats: 8-byte aligned at column 4 * lane
+        const int dcol = 4 * lane;
+        if (dcol < dh) {
+          *reinterpret_cast<float2*>(dst + 2 + dcol) = make_float2(st.acc[i][0], st.acc[i][1]);
+          *reinterpret_cast<float2*>(dst + 4 + dcol) = make_float2(st.acc[i][2], st.acc[i][3]);
+        }
+      }
+    }
   }
+  cp_async_wait<0>();                        // nothing may land after the CTA has left
 
-  pdl_wait();                                 // (no-op once waited; a pass-less CTA waits here)
   // the last CTA of this (request, kv head) merges the splits in order
   __threadfence();
   __syncthreads();
@@ -370,7 +401,7 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams 
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int r = warp; r < R; r += 8) {
+  for (int r = warp; r < R; r += WARPS) {
     const int node = r / p.G, hq = h * p.G + r % p.G;
     const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
     const float* src = p.part + qi * (p.n_splits + 1) * rec;
@@ -424,11 +455,9 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_kernel(const AttnParams 
 
 int attn_splits(const eagle_ctx* ctx, int pairs, int cap) {
   const int tiles = ceil_div(cap < 1 ? 1 : cap, TILE);
-  // one wave at two CTAs per SM, the tree part's CTA included
-  int want = 2 * ctx->sm_count / (pairs < 1 ? 1 : pairs) - 1;
+  // one wave at four CTAs per SM, the tree part's CTA included
+  int want = attn_splits_bound(ctx, pairs);
   if (want > tiles) want = tiles;
-  if (want > 31) want = 31;        // n_splits + 1 records fit one warp in the merge
-  if (want < 1) want = 1;
   const int per = ceil_div(tiles, want);
   return ceil_div(tiles, per);     // every split non-empty at full length
 }
@@ -437,8 +466,8 @@ template <int NR>
 static cudaError_t launch_attn_nr(const AttnParams& p, dim3 grid, size_t smem, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    const size_t most = (static_cast<size_t>(2) * TILE * (MAX_DH + 4) + static_cast<size_t>(ROWS_PASS) * MAX_DH +
-                         static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
+    const size_t most = 2 * TILE_BYTES + (static_cast<size_t>(ROWS_PASS) * MAX_DH +
+                                          static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(most));
     if (e != cudaSuccess) return e;
@@ -449,11 +478,13 @@ static cudaError_t launch_attn_nr(const AttnParams& p, dim3 grid, size_t smem, c
 
 static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
   p.n_splits = attn_splits(ctx, p.B * p.Hkv, p.kv_cap);
-  p.chunk = ceil_div(ceil_div(p.kv_cap, TILE), p.n_splits) * TILE;
+  const int tiles_per_split = ceil_div(ceil_div(p.kv_cap, TILE), p.n_splits);
+  p.chunk = tiles_per_split * TILE;
+  p.n_buf = tiles_per_split > 1 ? 2 : 1;
   p.rows_pass = std::min(ROWS_PASS, p.rows_cap * p.G);
   dim3 grid(p.n_splits + 1, p.B * p.Hkv);
-  const size_t smem = (static_cast<size_t>(2) * TILE * (p.dh + 4) + static_cast<size_t>(p.rows_pass) * p.dh +
-                       static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
+  const size_t smem = p.n_buf * TILE_BYTES + (static_cast<size_t>(p.rows_pass) * p.dh +
+                                              static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
   const int per_warp = ceil_div(p.rows_pass, WARPS);
   trace_before(ctx, kernel_id, st);
   cudaError_t e;
