@@ -43,8 +43,8 @@ constexpr int BK = 64;                     // elements per k-block (one 128-byte
 constexpr int KBLK_BYTES = BK * 2;
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
-constexpr int XCH_ROWS = 32;
-constexpr int STG_FLOATS = XCH_ROWS * BM;   // finalize staging: 32 rows of a tile
+constexpr int XCH_ROWS = 16;
+constexpr int STG_FLOATS = XCH_ROWS * BM;   // finalize staging: 16 rows of a tile
 
 struct GemmParams {
   int epi;
@@ -621,7 +621,7 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, const Smem& s, int
   }
 }
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(NUM_THREADS, 2)
     gemm_stream_kernel(const __grid_constant__ CUtensorMap mA0, const __grid_constant__ CUtensorMap mA1,
                        const __grid_constant__ CUtensorMap mA2, const __grid_constant__ CUtensorMap mT0,
                        const __grid_constant__ CUtensorMap mT1, const __grid_constant__ CUtensorMap mT2,
@@ -891,13 +891,6 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   p.two_mma = 2 * p.NP > 256 ? 1 : 0;
   for (int i = 0; i < 3; ++i) p.full_rows[i] = i < p.n_mats ? rows[i] / 8 * 8 : 0;
   p.full_kb = K / BK;
-  // two k-blocks per stage while that still leaves a ring of >= 3 stages
-  const size_t smem_cap = 232448;
-  p.kps = smem_bytes_for(3, BM * KBLK_BYTES * 2, 2 * p.NP * KBLK_BYTES * 2) <= smem_cap ? 2 : 1;
-  p.a_stage_bytes = static_cast<uint32_t>(BM * KBLK_BYTES * p.kps);
-  p.b_stage_bytes = static_cast<uint32_t>(2 * p.NP * KBLK_BYTES * p.kps);
-  p.kb = ceil_div(K, BK * p.kps);
-  p.total_units = static_cast<long long>(p.m_tiles) * p.kb;
   const int acc_cols = 2 * p.NP;
   p.acc_stride = acc_cols < 32 ? 32 : (acc_cols + 31) / 32 * 32;
   p.n_acc = 2 * p.acc_stride <= 512 ? 2 : 1;
@@ -905,13 +898,29 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   int cols = 32;
   while (cols < need) cols <<= 1;
   p.tmem_cols = cols;
+  // Contractions with fewer tiles than SMs (every tile split) run two CTAs
+  // per SM with half-size rings when two fit (shared memory and tensor
+  // memory): a CTA of the next kernel can then start on an SM as soon as one
+  // of the two leaves, instead of waiting for the SM's last finalizing CTA.
+  // The others keep one CTA per SM (whole tiles of their own at the end).
+  const size_t half_cap = static_cast<size_t>(113) * 1024;
+  const int per_sm = p.m_tiles < ctx->sm_count && cols <= 256 &&
+                     smem_bytes_for(2, BM * KBLK_BYTES, 2 * p.NP * KBLK_BYTES) <= half_cap ? 2 : 1;
+  const size_t smem_cap = per_sm == 2 ? half_cap : 232448;
+  const int min_ring = per_sm == 2 ? 2 : 3;
+  // two k-blocks per stage while that still leaves a ring of min_ring stages
+  p.kps = smem_bytes_for(min_ring, BM * KBLK_BYTES * 2, 2 * p.NP * KBLK_BYTES * 2) <= smem_cap ? 2 : 1;
+  p.a_stage_bytes = static_cast<uint32_t>(BM * KBLK_BYTES * p.kps);
+  p.b_stage_bytes = static_cast<uint32_t>(2 * p.NP * KBLK_BYTES * p.kps);
+  p.kb = ceil_div(K, BK * p.kps);
+  p.total_units = static_cast<long long>(p.m_tiles) * p.kb;
 
   int stages = 8;
   while (stages > 2 && smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes) > smem_cap) --stages;
   p.stages = stages;
   size_t smem = smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes);
   if (smem > smem_cap) return cudaErrorInvalidConfiguration;
-  if (smem < 120 * 1024) smem = 120 * 1024;    // one CTA per SM: tensor memory is never contended
+  if (per_sm == 1 && smem < 120 * 1024) smem = 120 * 1024;    // keeps one CTA per SM
 
   CUtensorMap maps[3], tails[3], mb;
   for (int i = 0; i < 3; ++i) {
@@ -924,12 +933,11 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
 
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_cap));
+    cudaError_t e = cudaFuncSetAttribute(gemm_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  int grid = ctx->sm_count;
+  int grid = per_sm * ctx->sm_count;
   if (p.total_units < grid) grid = static_cast<int>(p.total_units);
   // whole waves of tiles go data-parallel at the end of every CTA's work;
   // the remaining tiles are split stream-K and processed first
