@@ -429,15 +429,53 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
 // Final epilogue of tile t: sum the partials of CTAs [c_first, c_last] and
 // apply the contraction's fused elementwise work.  `m` is the tile row this
 // thread owns (its tensor-memory lane).  It runs once per tile, cold, at the
-// end of the stream, so both its instruction footprint and its chain of
-// memory latencies are on the kernel's critical path: every global input of
-// a 32-row chunk is brought into shared memory by asynchronous copies issued
-// from compact loops (many in flight, one wait), then the per-row loops read
-// shared memory only.
+// end of the stream, so its chain of memory latencies is on the kernel's
+// critical path: the partials are brought into shared memory by
+// asynchronous copies issued from compact loops (many in flight, one wait),
+// then the per-row loops read shared memory only.  `area` (cap floats,
+// 16-byte aligned) is the idle pipeline ring when this is the CTA's last
+// tile, else null: the partials of all rows then arrive several CTAs per
+// batch; otherwise they come 16 rows x one CTA at a time through s.stg.
+// Either way every element is summed in CTA order (deterministic, and the
+// same order on both routes).
 __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, const EpiCol& col, int t,
-                                           int c_first, int c_last, int m) {
+                                           int c_first, int c_last, int m, float* area, int cap) {
   const int et = m;                    // epilogue thread index == tile row
   const int C = c_last - c_first + 1;
+  const int blk = p.n * BM;            // one CTA's partial of the tile: n rows
+  const float* part = p.part + static_cast<size_t>(t + c_first) * blk;
+  if (area != nullptr && cap >= 2 * blk) {
+    float* acc = area;
+    float* stage = area + blk;
+    const int cb = min(C, (cap - blk) / blk);
+    sm100::fence_proxy_async_smem();   // the ring's last reads were the tensor cores'
+#pragma unroll 1
+    for (int c0 = 0; c0 < C; c0 += cb) {
+      const int cn = min(cb, C - c0);
+      stage_block(stage, part + static_cast<size_t>(c0) * blk, cn * blk, et);
+      cp_async_wait_all();
+      sm100::named_barrier(1, EPI_THREADS);
+#pragma unroll 1
+      for (int i = 4 * et; i < blk; i += 4 * EPI_THREADS) {
+        float4 a = c0 == 0 ? *reinterpret_cast<const float4*>(stage + i) : *reinterpret_cast<const float4*>(acc + i);
+#pragma unroll 1
+        for (int c = c0 == 0 ? 1 : 0; c < cn; ++c) {
+          const float4 x = *reinterpret_cast<const float4*>(stage + static_cast<size_t>(c) * blk + i);
+          a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+        }
+        *reinterpret_cast<float4*>(acc + i) = a;
+      }
+      sm100::named_barrier(1, EPI_THREADS);
+    }
+    for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
+      const int nj = min(XCH_ROWS, p.n - jc);
+#pragma unroll 1
+      for (int jj = 0; jj < nj; ++jj) s.xch[jj * BM + m] = acc[(jc + jj) * BM + m];
+      sm100::named_barrier(1, EPI_THREADS);
+      epilogue_chunk(p, s, col, t, jc, nj, m, jc == 0);   // chunk 0's row inputs were staged early
+    }
+    return;
+  }
   for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
     const int nj = min(XCH_ROWS, p.n - jc);
     // 1. partials of the contributing CTAs (each one contiguous block of nj
@@ -449,8 +487,7 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
       const int cn = min(cb, C - c0);
 #pragma unroll 1
       for (int c = 0; c < cn; ++c)
-        stage_block(s.stg + c * nj * BM, p.part + (static_cast<size_t>(t + c_first + c0 + c) * p.n + jc) * BM,
-                    nj * BM, et);
+        stage_block(s.stg + c * nj * BM, part + static_cast<size_t>(c0 + c) * blk + jc * BM, nj * BM, et);
       cp_async_wait_all();
       sm100::named_barrier(1, EPI_THREADS);
 #pragma unroll 1
@@ -755,7 +792,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
       sm100::named_barrier(1, EPI_THREADS);
       if (s.flags[1]) {
         __threadfence();
-        finalize_tile(p, s, col, t, c_first, c_last, m);
+        // on the CTA's last tile the pipeline ring is idle: all of its loads
+        // were consumed by MMAs that have completed
+        int t2;
+        long long w0, w1;
+        const bool last_seg = !wk.segment(p, seg + 1, t2, w0, w1);
+        float* area = last_seg ? reinterpret_cast<float*>(s.a) : nullptr;
+        const int cap = static_cast<int>(static_cast<size_t>(p.stages) * (p.a_stage_bytes + p.b_stage_bytes) / 4);
+        finalize_tile(p, s, col, t, c_first, c_last, m, area, cap);
       }
       sm100::named_barrier(1, EPI_THREADS);
     }
