@@ -96,7 +96,8 @@ void layout(eagle_ctx* c) {
   W.ss_o = take(static_cast<size_t>(L.max_rows) * tiles_d * 4);
   W.max_mtiles = std::max({tiles_d, ceil_div((D.n_q_heads + 2 * D.n_kv_heads) * D.head_dim, 128),
                            ceil_div(D.d_ff, 64), ceil_div(D.vocab, 128)});
-  W.gemm_part = take(static_cast<size_t>(W.max_mtiles + c->sm_count) * L.max_rows * 128 * 4);
+  // split-tile partial slots t + cta: t < max_mtiles, cta < grid <= 2 * SMs
+  W.gemm_part = take(static_cast<size_t>(W.max_mtiles + 2 * c->sm_count) * L.max_rows * 128 * 4);
   W.gemm_cnt = take(static_cast<size_t>(6) * W.max_mtiles * 4);
   size_t records = 0;
   for (int b = 1; b <= L.max_batch; ++b) {

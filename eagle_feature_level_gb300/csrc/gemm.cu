@@ -987,6 +987,9 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   // the remaining tiles are split stream-K and processed first
   p.dp_waves = p.m_tiles / grid;
   p.sk_tiles = p.m_tiles - p.dp_waves * grid;
+  // partial slots t + cta of split tiles stay inside the workspace's array
+  if (p.sk_tiles > 0 && p.sk_tiles - 1 + grid - 1 >= W.max_mtiles + 2 * ctx->sm_count)
+    return cudaErrorInvalidConfiguration;
   trace_before(ctx, epi, st);
   const cudaError_t e = launch_pdl(gemm_stream_kernel, dim3(grid), dim3(NUM_THREADS), smem, st, maps[0], maps[1],
                                    maps[2], tails[0], tails[1], tails[2], mb, p);

@@ -36,7 +36,7 @@ struct Workspace {
   size_t h, h2;                  // fp32 [max_rows][d]
   size_t qrow;                   // fp32 [max_rows][Hq*dh]
   size_t ss_fc, ss_o;            // fp32 [max_rows][tiles of d]
-  size_t gemm_part;              // fp32 [(max_mtiles + grid) * max_rows * 128]
+  size_t gemm_part;              // fp32 [(max_mtiles + 2 * SMs) * max_rows * 128]
   size_t gemm_cnt;               // int [6][max_mtiles]
   size_t attn_part;              // fp32 partial (m, l, acc[dh]) records
   size_t attn_cnt;               // int [2][max_batch * Hkv]
