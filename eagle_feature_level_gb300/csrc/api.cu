@@ -106,7 +106,7 @@ void layout(eagle_ctx* c) {
     records = std::max(records, static_cast<size_t>(b) * L.max_tree * D.n_q_heads * s1);
     if (b > 4096) break;   // the bound stops growing once splits reach 1
   }
-  W.attn_part = take(records * (D.head_dim + 2) * 4);
+  W.attn_part = take(records * (D.head_dim + 4) * 4);
   W.attn_cnt = take(static_cast<size_t>(2) * L.max_batch * D.n_kv_heads * 4);
   W.accept_scratch = take(static_cast<size_t>(L.max_batch) * D.vocab * 8);
   W.total = off;

@@ -2,14 +2,19 @@
 // verification layer ([B] "Tree Attention 如何一次验证多条路径": node u sees the
 // committed prefix plus the tree nodes that are its ancestors or itself).
 //
-// Split-KV layout: one CTA per (prefix split or tree part, request, kv head),
-// one wave at four CTAs per SM.  Every query row of the request that maps to
-// this kv head (tree nodes x GQA group) consumes the same shared-memory K/V
-// tile, so prefix KV bytes are read from HBM once per call however many tree
-// nodes there are.  Each CTA
-// writes (max, sum, unnormalised output) partials; the last CTA of a
+// Split-KV layout: one CTA per (prefix split or tree part, request, kv head).
+// Every query row of the request that maps to this kv head (tree nodes x
+// GQA group) consumes the same shared-memory K/V tile, so prefix KV bytes
+// are read from HBM once per call however many tree nodes there are.  Each
+// CTA writes (max, sum, unnormalised output) partials; the last CTA of a
 // (request, kv head) merges them in split order.  The ancestor mask of each
-// query row lives in a register (one 64-bit word) and is tested per tree key.
+// query row is one 64-bit word, tested per tree key.
+//
+// Two kernels share this layout.  The draft layer's (a few fp32 query rows
+// per request and layer) runs on the CUDA cores, one wave at four CTAs per
+// SM.  The verification layer's (every tree node at once, bf16 queries)
+// runs its products on the tensor cores (warp-level bf16 MMA tiles, fp32
+// accumulation), one wave at two CTAs per SM.
 #include <algorithm>
 #include <mutex>
 
@@ -20,18 +25,22 @@ namespace eagle {
 namespace {
 
 constexpr int TILE = 64;          // prefix / verify-tree keys per shared-memory tile (bf16)
-constexpr int TILE_F32 = 32;      // draft-tree keys per tile (fp32, same bytes)
+constexpr int TILE_F32 = 32;      // draft-tree keys per tile (fp32, or bf16 hi + lo: same bytes)
 constexpr int THREADS = 128;
 constexpr int WARPS = THREADS / 32;
 constexpr int MAX_DH = 128;
-constexpr int RW = 8;             // query rows a warp owns in one pass, at most
-constexpr int ROWS_PASS = WARPS * RW;
-constexpr int KLD = MAX_DH + 8;   // bf16 row pitch of a tile in shared memory (elements)
+constexpr int RW = 8;             // CUDA-core kernel: query rows a warp owns in one pass, at most
+constexpr int ROWS_PASS = WARPS * RW;   // query rows per pass (tensor-core kernel: two 16-row tiles)
+constexpr int KLD = MAX_DH + 8;   // bf16 row pitch in shared memory (elements): ldmatrix rows hit distinct banks
+constexpr int MLD = MAX_DH + 4;   // fp32 row pitch of a warp's softmax state in the intra-CTA merge
 
-// Shared-memory bytes of one K+V tile buffer: 64 bf16 rows of K and of V,
-// or 32 fp32 rows of each (dh + 4 floats per row).
+// Shared-memory bytes of one K+V tile buffer: 64 bf16 rows of K then of V,
+// 32 fp32 rows of each, or 32 bf16 rows each of K hi, K lo, V hi, V lo.
 constexpr size_t TILE_BYTES = static_cast<size_t>(2) * TILE * KLD * 2;
 static_assert(static_cast<size_t>(2) * TILE_F32 * (MAX_DH + 4) * 4 <= TILE_BYTES, "fp32 half tile fits a buffer");
+constexpr size_t Q_BYTES = static_cast<size_t>(2) * ROWS_PASS * KLD * 2;     // pass rows, hi and lo
+constexpr size_t MRG_BYTES = static_cast<size_t>(2) * 16 * MLD * 4;          // two warp states of 16 rows
+static_assert(MRG_BYTES <= Q_BYTES, "the merge states reuse the query rows' space");
 
 struct AttnParams {
   int mode;                       // 0 draft, 1 verify
@@ -39,7 +48,7 @@ struct AttnParams {
   int n_splits, chunk;            // prefix splits and rows per split (a multiple of TILE)
   int n_buf;                      // tile buffers per CTA (2: the next prefix tile streams in)
   int rows_cap;                   // query nodes per request (draft: rows per request; verify: tree stride)
-  int rows_pass;                  // query rows staged per pass: min(ROWS_PASS, rows_cap * G)
+  int rows_pass;                  // CUDA-core kernel: query rows staged per pass, min(ROWS_PASS, rows_cap * G)
   const float* q_f32;             // draft: [n][Hq*dh] fp32
   const uint16_t* q_bf16;         // verify: [B][S][Hq][dh] bf16
   const uint16_t* kp;             // prefix KV [B][cap][Hkv][dh] bf16
@@ -58,7 +67,7 @@ struct AttnParams {
   float* out_f32;                 // verify: [B][S][Hq][dh]
   uint16_t* b_o;                  // draft: next GEMM operand (hi/lo), [2NP][bo_ld]
   int NP, bo_ld;
-  float* part;
+  float* part;                    // partial records [query row][split][dh + 4]
   int* counters;
 };
 
@@ -79,6 +88,9 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t 
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(sm100::smem_u32(dst)), "l"(src),
                "l"(policy)
                : "memory");
+}
+__device__ __forceinline__ void cp_async16_cg(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm100::smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -104,6 +116,8 @@ __device__ __forceinline__ void stage_bf16(uint16_t* buf, const uint16_t* kb, co
   }
   cp_async_commit();
 }
+
+// ---- draft layer: CUDA cores -------------------------------------------------
 
 // Copies draft-tree keys k0 .. k0 + nt - 1 (fp32, at most TILE_F32) into buf
 // as K rows [TILE_F32][dh + 4] then V rows; rows past nt are zeroed.
@@ -283,7 +297,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
   } else {
     hi = p.mode == 0 ? p.tree_cap : min(p.tree_size[b], p.tree_cap);
   }
-  const int rec = dh + 2;
+  const int rec = dh + 4;                    // partial record: max, sum, 2 unused, output[dh]
   const size_t row_stride = static_cast<size_t>(p.Hkv) * dh;
   const uint64_t policy = sm100::l2_policy_evict_first();
   const int step = tree_f32 ? TILE_F32 : TILE;
@@ -379,12 +393,9 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
           dst[0] = st.m[i];
           dst[1] = st.l[i];
         }
-        // records are dh + 2 floats: 8-byte aligned at column 4 * lane
         const int dcol = 4 * lane;
-        if (dcol < dh) {
-          *reinterpret_cast<float2*>(dst + 2 + dcol) = make_float2(st.acc[i][0], st.acc[i][1]);
-          *reinterpret_cast<float2*>(dst + 4 + dcol) = make_float2(st.acc[i][2], st.acc[i][3]);
-        }
+        if (dcol < dh)
+          *reinterpret_cast<float4*>(dst + 4 + dcol) = make_float4(st.acc[i][0], st.acc[i][1], st.acc[i][2], st.acc[i][3]);
       }
     }
   }
@@ -421,7 +432,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int d = lane + 32 * c;
-          vals[u][c] = (s < ns && d < dh) ? __ldcg(src + s * rec + 2 + d) : 0.f;
+          vals[u][c] = (s < ns && d < dh) ? __ldcg(src + s * rec + 4 + d) : 0.f;
         }
       }
 #pragma unroll
@@ -451,16 +462,476 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
   }
 }
 
+// ---- verification layer: tensor cores ----------------------------------------
+
+// ---- warp-level bf16 tensor-core tiles (m16n8k16, fp32 accumulate) ---------
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const uint16_t* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(sm100::smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const uint16_t* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(sm100::smem_u32(p)));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// (x, y) -> bf16x2 hi = RN(x, y) and lo = RN of the remainders; x in the low half
+__device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint32_t& lo) {
+  uint16_t xh, xl, yh, yl;
+  split_bf16(x, xh, xl);
+  split_bf16(y, yh, yl);
+  hi = static_cast<uint32_t>(xh) | (static_cast<uint32_t>(yh) << 16);
+  lo = static_cast<uint32_t>(xl) | (static_cast<uint32_t>(yl) << 16);
+}
+
+// Draft-tree keys k0 .. k0 + nt - 1 (fp32, at most TILE_F32) into buf as bf16
+// hi / lo pairs: K hi [TILE_F32][KLD], K lo, then V hi at row TILE (the same
+// place as a bf16 tile's V), V lo; rows past nt are zeroed.
+__device__ __forceinline__ void stage_f32_split(uint16_t* buf, const float* kf, const float* vf, size_t row0,
+                                                size_t row_stride, int nt, int dh) {
+  const int pieces = dh >> 2;
+  for (int idx = threadIdx.x; idx < TILE_F32 * pieces; idx += THREADS) {
+    const int r = idx / pieces, c = idx - r * pieces;
+    float4 k = make_float4(0.f, 0.f, 0.f, 0.f), v = k;
+    if (r < nt) {
+      k = __ldcg(reinterpret_cast<const float4*>(kf + row0 + r * row_stride + 4 * c));
+      v = __ldcg(reinterpret_cast<const float4*>(vf + row0 + r * row_stride + 4 * c));
+    }
+    uint32_t h0, l0, h1, l1;
+    const int o = r * KLD + 4 * c;
+    split_pair(k.x, k.y, h0, l0);
+    split_pair(k.z, k.w, h1, l1);
+    *reinterpret_cast<uint2*>(buf + o) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(buf + TILE_F32 * KLD + o) = make_uint2(l0, l1);
+    split_pair(v.x, v.y, h0, l0);
+    split_pair(v.z, v.w, h1, l1);
+    *reinterpret_cast<uint2*>(buf + TILE * KLD + o) = make_uint2(h0, h1);
+    *reinterpret_cast<uint2*>(buf + (TILE + TILE_F32) * KLD + o) = make_uint2(l0, l1);
+  }
+}
+
+// Online-softmax state of one warp: rows g and g + 8 of its 16-row tile
+// (g = lane / 4), output columns 8 j + 2 (lane % 4) + {0, 1} of each 8-wide
+// column tile j (the m16n8 accumulator layout).
+struct WarpState {
+  float m[2], l[2];
+  float o[MAX_DH / 8][4];
+};
+
+// One warp, one staged tile: rows [16 mt, 16 mt + 16) of the pass against
+// tile keys [k_lo, k_lo + 8 NKT).  S = Q K^T on the tensor cores (Q as bf16
+// hi + lo when it is fp32; K hi + lo for the draft's fp32 tree keys), scale,
+// mask (keys past nt; tree keys outside the row's ancestor set), online
+// softmax in registers, then O += P V with P split into bf16 hi + lo taken
+// straight from the score accumulators.
+template <int NKT>
+__device__ __forceinline__ void tile_mma(const AttnParams& p, WarpState& st, const uint16_t* buf, bool kv_lo,
+                                         const uint16_t* qhi, const uint16_t* qlo, int mt, int k_lo, int nt,
+                                         int key_base, bool is_tree, uint64_t mask_a, uint64_t mask_b, int lane) {
+  const int dh = p.dh;
+  const int tq = lane & 3;
+  const uint16_t* sk = buf;
+  const uint16_t* skl = buf + TILE_F32 * KLD;
+  const uint16_t* sv = buf + TILE * KLD;
+  const uint16_t* svl = buf + (TILE + TILE_F32) * KLD;
+  float s[NKT][4];
+#pragma unroll
+  for (int j = 0; j < NKT; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+  const int qrow = 16 * mt + (lane & 15), qcol = (lane >> 4) * 8;
+  const int krow = k_lo + (lane & 7) + ((lane >> 4) << 3), kcol = ((lane >> 3) & 1) * 8;
+  for (int kk = 0; kk < dh; kk += 16) {
+    uint32_t a[4], al[4];
+    ldsm_x4(a, qhi + qrow * KLD + kk + qcol);
+    if (qlo != nullptr) ldsm_x4(al, qlo + qrow * KLD + kk + qcol);
+#pragma unroll
+    for (int j = 0; j < NKT; j += 2) {
+      uint32_t bk[4];
+      ldsm_x4(bk, sk + (krow + 8 * j) * KLD + kk + kcol);
+      mma_bf16_16816(s[j], a, bk[0], bk[1]);
+      mma_bf16_16816(s[j + 1], a, bk[2], bk[3]);
+      if (qlo != nullptr) {
+        mma_bf16_16816(s[j], al, bk[0], bk[1]);
+        mma_bf16_16816(s[j + 1], al, bk[2], bk[3]);
+      }
+      if (kv_lo) {
+        ldsm_x4(bk, skl + (krow + 8 * j) * KLD + kk + kcol);
+        mma_bf16_16816(s[j], a, bk[0], bk[1]);
+        mma_bf16_16816(s[j + 1], a, bk[2], bk[3]);
+      }
+    }
+  }
+  // scale and mask; the rows' maxima over this warp's keys (a quad shares a row)
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int j = 0; j < NKT; ++j) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int key = k_lo + 8 * j + 2 * tq + (e & 1);
+      const uint64_t mk = e < 2 ? mask_a : mask_b;
+      const bool ok = key < nt && (!is_tree || ((mk >> (key_base + key)) & 1ull));
+      s[j][e] = ok ? s[j][e] * p.scale : -INFINITY;
+      mx[e >> 1] = fmaxf(mx[e >> 1], s[j][e]);
+    }
+  }
+  float corr[2], sum[2] = {0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+    mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+    const float m_new = fmaxf(st.m[r], mx[r]);
+    corr[r] = m_new == -INFINITY ? 1.f : __expf(st.m[r] - m_new);
+    mx[r] = m_new;
+  }
+#pragma unroll
+  for (int j = 0; j < NKT; ++j) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float m_new = mx[e >> 1];
+      const float pe = m_new == -INFINITY ? 0.f : __expf(s[j][e] - m_new);
+      s[j][e] = pe;
+      sum[e >> 1] += pe;
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], 1);
+    sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], 2);
+    st.l[r] = st.l[r] * corr[r] + sum[r];
+    st.m[r] = mx[r];
+  }
+#pragma unroll
+  for (int j = 0; j < MAX_DH / 8; ++j) {
+    st.o[j][0] *= corr[0];
+    st.o[j][1] *= corr[0];
+    st.o[j][2] *= corr[1];
+    st.o[j][3] *= corr[1];
+  }
+  // O += P V, 16 keys per step: the score accumulators of column tiles 2q
+  // and 2q + 1 are the A fragment of keys [16 q, 16 q + 16)
+  const int vrow = k_lo + (lane & 7) + ((lane >> 3) & 1) * 8, vcol = (lane >> 4) * 8;
+#pragma unroll
+  for (int q = 0; q < NKT / 2; ++q) {
+    uint32_t ah[4], alo[4];
+    split_pair(s[2 * q][0], s[2 * q][1], ah[0], alo[0]);
+    split_pair(s[2 * q][2], s[2 * q][3], ah[1], alo[1]);
+    split_pair(s[2 * q + 1][0], s[2 * q + 1][1], ah[2], alo[2]);
+    split_pair(s[2 * q + 1][2], s[2 * q + 1][3], ah[3], alo[3]);
+#pragma unroll
+    for (int j = 0; j < MAX_DH / 8; j += 2) {
+      if (8 * j < dh) {
+        uint32_t bv[4];
+        ldsm_x4_t(bv, sv + (vrow + 16 * q) * KLD + 8 * j + vcol);
+        mma_bf16_16816(st.o[j], ah, bv[0], bv[1]);
+        mma_bf16_16816(st.o[j + 1], ah, bv[2], bv[3]);
+        mma_bf16_16816(st.o[j], alo, bv[0], bv[1]);
+        mma_bf16_16816(st.o[j + 1], alo, bv[2], bv[3]);
+        if (kv_lo) {
+          ldsm_x4_t(bv, svl + (vrow + 16 * q) * KLD + 8 * j + vcol);
+          mma_bf16_16816(st.o[j], ah, bv[0], bv[1]);
+          mma_bf16_16816(st.o[j + 1], ah, bv[2], bv[3]);
+        }
+      }
+    }
+  }
+}
+
+// st <- merge(st, the state stored at slot): the usual rescale to the
+// larger maximum.
+__device__ __forceinline__ void merge_state(WarpState& st, const float* slot, int dh, int lane) {
+  const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const float* row = slot + (g + 8 * r) * MLD;
+    const float mb = row[MAX_DH], lb = row[MAX_DH + 1];
+    const float m = fmaxf(st.m[r], mb);
+    const float wa = m == -INFINITY ? 0.f : __expf(st.m[r] - m);
+    const float wb = m == -INFINITY ? 0.f : __expf(mb - m);
+    st.l[r] = st.l[r] * wa + lb * wb;
+    st.m[r] = m;
+#pragma unroll
+    for (int j = 0; j < MAX_DH / 8; ++j) {
+      if (8 * j < dh) {
+        const float2 ob = *reinterpret_cast<const float2*>(row + 8 * j + 2 * tq);
+        st.o[j][2 * r] = st.o[j][2 * r] * wa + ob.x * wb;
+        st.o[j][2 * r + 1] = st.o[j][2 * r + 1] * wa + ob.y * wb;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void store_state(const WarpState& st, float* slot, int dh, int lane) {
+  const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    float* row = slot + (g + 8 * r) * MLD;
+    if (tq == 0) {
+      row[MAX_DH] = st.m[r];
+      row[MAX_DH + 1] = st.l[r];
+    }
+#pragma unroll
+    for (int j = 0; j < MAX_DH / 8; ++j)
+      if (8 * j < dh) *reinterpret_cast<float2*>(row + 8 * j + 2 * tq) = make_float2(st.o[j][2 * r], st.o[j][2 * r + 1]);
+  }
+}
+
+// Dynamic shared memory: n_buf tile buffers (TILE_BYTES each) and the
+// pass's query rows as bf16 hi [ROWS_PASS][KLD] and lo, whose space holds
+// two warp states for the intra-CTA merge once the pass's tiles are done;
+// at the end, the merging CTA reuses all of it to stage partial records.
+//
+// One CTA per (prefix split or tree part, request, kv head).  A pass covers
+// up to 32 query rows (tree nodes x GQA group) as MT = 1 or 2 tiles of 16;
+// the 4 / MT warps of a row tile split every staged key tile between them,
+// each keeping its own online softmax, and are merged (in a fixed order) at
+// the end of the pass.  Prefix tiles are bf16 copied by cp.async (the next
+// one streams in while the current one is consumed when a split holds
+// several); the draft's fp32 tree keys are split into bf16 hi + lo as they
+// are staged, 32 keys per tile.
+__global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnParams p) {
+  pdl_trigger();
+  if (p.mode == 1) pdl_wait();               // verification reads the tree's size first
+  extern __shared__ __align__(16) uint8_t smem_attn[];
+  __shared__ int s_last;
+  __shared__ uint64_t s_mask[ROWS_PASS];     // ancestor masks of the pass's rows (tree part)
+
+  const int split = blockIdx.x;              // split == n_splits: the tree part
+  const int pair = blockIdx.y;
+  const int b = pair / p.Hkv, h = pair % p.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int dh = p.dh;
+  uint8_t* bufs = smem_attn;
+  uint16_t* qhi = reinterpret_cast<uint16_t*>(smem_attn + p.n_buf * TILE_BYTES);
+  uint16_t* qlo = qhi + ROWS_PASS * KLD;
+  float* mrg = reinterpret_cast<float*>(qhi);   // after a pass's last tile, the query rows are dead
+  const int nodes = n_nodes(p, b);
+  const int R = nodes * p.G;
+  const bool is_tree = split == p.n_splits;
+  const bool tree_f32 = is_tree && p.mode == 0;
+  int lo = 0, hi = 0;
+  if (!is_tree) {
+    const int L = p.kv_len[b];
+    lo = split * p.chunk;
+    hi = min(L, lo + p.chunk);
+  } else {
+    hi = p.mode == 0 ? p.tree_cap : min(p.tree_size[b], p.tree_cap);
+  }
+  const int rec = dh + 4;                    // partial record: max, sum, 2 unused, output[dh]
+  const size_t row_stride = static_cast<size_t>(p.Hkv) * dh;
+  const uint64_t policy = sm100::l2_policy_evict_first();
+  const int step = tree_f32 ? TILE_F32 : TILE;
+  const int n_tiles = hi > lo ? (hi - lo + step - 1) / step : 0;
+  // A split whose keys fit one buffer stages them once for every pass.
+  const bool resident = n_tiles <= 1;
+
+  auto stage = [&](int tile, int which) {
+    uint16_t* buf = reinterpret_cast<uint16_t*>(bufs + which * TILE_BYTES);
+    const int t0 = lo + tile * step, nt = min(step, hi - t0);
+    if (tree_f32)
+      stage_f32_split(buf, p.kt_f32, p.vt_f32, ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh,
+                      row_stride, nt, dh);
+    else if (is_tree)
+      stage_bf16(buf, p.kt_bf16, p.vt_bf16, ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh,
+                 row_stride, nt, dh, policy);
+    else
+      stage_bf16(buf, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + t0) * p.Hkv + h) * dh, row_stride, nt, dh,
+                 policy);
+  };
+  // The prefix KV is not written by the kernels of this draft step: its
+  // first tile is requested before waiting on the predecessor.
+  if (!is_tree && n_tiles > 0) stage(0, 0);
+  pdl_wait();                                // q rows, tree K/V and masks come from the predecessors
+  if (is_tree && n_tiles > 0) stage(0, 0);
+
+  for (int r0 = 0; r0 < R; r0 += ROWS_PASS) {
+    const int rp = min(ROWS_PASS, R - r0);
+    const int MT = rp > 16 ? 2 : 1;
+    const int KS = WARPS / MT;               // warps sharing a row tile
+    const int mt = warp % MT, ks = warp / MT;
+    if (r0 > 0) __syncthreads();             // the previous pass is done with the query rows and buffers
+    // query rows of the pass as bf16 hi (+ lo for fp32 queries); rows past rp are zero
+    for (int idx = threadIdx.x; idx < 16 * MT * (dh >> 2); idx += THREADS) {
+      const int rr = idx / (dh >> 2), c = idx - rr * (dh >> 2);
+      uint2 wh = make_uint2(0u, 0u), wl = make_uint2(0u, 0u);
+      if (rr < rp) {
+        const int r = r0 + rr, node = r / p.G, hq = h * p.G + r % p.G;
+        const size_t qo = q_index(p, b, node, hq) + 4 * c;
+        if (p.mode == 0) {
+          const float4 v = *reinterpret_cast<const float4*>(p.q_f32 + qo);
+          split_pair(v.x, v.y, wh.x, wl.x);
+          split_pair(v.z, v.w, wh.y, wl.y);
+        } else {
+          wh = *reinterpret_cast<const uint2*>(p.q_bf16 + qo);
+        }
+      }
+      *reinterpret_cast<uint2*>(qhi + rr * KLD + 4 * c) = wh;
+      if (p.mode == 0) *reinterpret_cast<uint2*>(qlo + rr * KLD + 4 * c) = wl;
+    }
+    if (is_tree && threadIdx.x < ROWS_PASS)
+      s_mask[threadIdx.x] = threadIdx.x < rp ? row_mask(p, b, (r0 + threadIdx.x) / p.G) : 0ull;
+    WarpState st;
+    st.m[0] = st.m[1] = -INFINITY;
+    st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+    for (int j = 0; j < MAX_DH / 8; ++j) st.o[j][0] = st.o[j][1] = st.o[j][2] = st.o[j][3] = 0.f;
+    for (int tile = 0; tile < n_tiles; ++tile) {
+      const int which = p.n_buf > 1 ? (tile & 1) : 0;
+      if (!resident) {
+        // staged earlier: tile 0 of the first pass (prologue), or by the
+        // previous iteration's prefetch when two buffers alternate
+        const bool staged = (r0 == 0 && tile == 0) || (p.n_buf > 1 && tile > 0);
+        if (!staged) {
+          __syncthreads();                   // every warp is done with this buffer
+          stage(tile, which);
+        }
+        if (p.n_buf > 1 && tile + 1 < n_tiles) {
+          __syncthreads();                   // the other buffer's previous tile is consumed
+          stage(tile + 1, which ^ 1);
+          cp_async_wait<1>();                // this tile's copies have landed
+        } else {
+          cp_async_wait<0>();
+        }
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncthreads();
+      const int t0 = lo + tile * step;
+      const int nt = min(step, hi - t0);
+      const int kpw = max(16, step / KS);    // keys per warp: 16 or 32
+      const int k_lo = ks * kpw;
+      if (k_lo < nt) {
+        const uint16_t* buf = reinterpret_cast<const uint16_t*>(bufs + which * TILE_BYTES);
+        const uint64_t ma = is_tree ? s_mask[16 * mt + (lane >> 2)] : ~0ull;
+        const uint64_t mb = is_tree ? s_mask[16 * mt + (lane >> 2) + 8] : ~0ull;
+        const uint16_t* ql = p.mode == 0 ? qlo : nullptr;
+        const int kb = is_tree ? t0 : 0;
+        if (kpw == 32)
+          tile_mma<4>(p, st, buf, tree_f32, qhi, ql, mt, k_lo, nt, kb, is_tree, ma, mb, lane);
+        else
+          tile_mma<2>(p, st, buf, tree_f32, qhi, ql, mt, k_lo, nt, kb, is_tree, ma, mb, lane);
+      }
+    }
+    // merge the KS warps of each row tile pairwise, in a fixed order
+    for (int d = 1; d < KS; d <<= 1) {
+      __syncthreads();
+      const int slot = mt + MT * (ks / (2 * d));          // < 2
+      if (ks % (2 * d) == d) store_state(st, mrg + slot * 16 * MLD, dh, lane);
+      __syncthreads();
+      if (ks % (2 * d) == 0) merge_state(st, mrg + slot * 16 * MLD, dh, lane);
+    }
+    if (ks == 0) {
+      const int g = lane >> 2, tq = lane & 3;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int rr = 16 * mt + g + 8 * r;
+        if (rr >= rp) continue;
+        const int row = r0 + rr, node = row / p.G, hq = h * p.G + row % p.G;
+        const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
+        float* dst = p.part + (qi * (p.n_splits + 1) + split) * rec;
+        if (tq == 0) {
+          dst[0] = st.m[r];
+          dst[1] = st.l[r];
+        }
+#pragma unroll
+        for (int j = 0; j < MAX_DH / 8; ++j)
+          if (8 * j < dh)
+            *reinterpret_cast<float2*>(dst + 4 + 8 * j + 2 * tq) = make_float2(st.o[j][2 * r], st.o[j][2 * r + 1]);
+      }
+    }
+  }
+  cp_async_wait<0>();                        // nothing may land after the CTA has left
+
+  // the last CTA of this (request, kv head) merges the splits in order
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(&p.counters[pair], 1);
+    s_last = prev == p.n_splits;
+    if (s_last) p.counters[pair] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // Every record of a batch of rows is copied into shared memory at once
+  // (16-byte asynchronous copies: a row's ns records are contiguous), then a
+  // warp per row merges from shared memory: lane s < ns holds split s's
+  // header, lane c sums columns c + 32 i.
+  const int ns = p.n_splits + 1;
+  float* stg = reinterpret_cast<float*>(smem_attn);
+  const int row_floats = ns * rec;
+  const size_t smem_floats = (p.n_buf * TILE_BYTES + Q_BYTES) / sizeof(float);
+  const int batch = max(1, static_cast<int>(smem_floats / row_floats));
+  for (int rb = 0; rb < R; rb += batch) {
+    const int nb = min(batch, R - rb);
+    __syncthreads();                         // the previous batch is merged
+    for (int i = 0; i < nb; ++i) {
+      const int r = rb + i, node = r / p.G, hq = h * p.G + r % p.G;
+      const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
+      const float* src = p.part + qi * ns * rec;
+      for (int k = 4 * threadIdx.x; k < row_floats; k += 4 * THREADS) cp_async16_cg(stg + i * row_floats + k, src + k);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int i = warp; i < nb; i += WARPS) {
+      const int r = rb + i, node = r / p.G, hq = h * p.G + r % p.G;
+      const float* srow = stg + i * row_floats;
+      const float ms = lane < ns ? srow[lane * rec] : -INFINITY;
+      const float ls = lane < ns ? srow[lane * rec + 1] : 0.f;
+      const float M = warp_max(ms);
+      const float wgt = ms == -INFINITY ? 0.f : __expf(ms - M);
+      const float Lsum = warp_sum(wgt * ls);
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < ns; ++s) {
+        const float ws = __shfl_sync(0xffffffffu, wgt, s);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int d = lane + 32 * c;
+          if (d < dh) o[c] = fmaf(ws, srow[s * rec + 4 + d], o[c]);
+        }
+      }
+      const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int d = lane + 32 * c;
+        if (d >= dh) continue;
+        const float v = o[c] * inv;
+        if (p.mode == 1) {
+          p.out_f32[((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * dh + d] = v;
+        } else {
+          const int j = b * p.rows_cap + node;
+          const int col = hq * dh + d;
+          uint16_t hi16, lo16;
+          split_bf16(v, hi16, lo16);
+          p.b_o[static_cast<size_t>(j) * p.bo_ld + col] = hi16;
+          p.b_o[static_cast<size_t>(p.NP + j) * p.bo_ld + col] = lo16;
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+}
+
 }  // namespace
 
-int attn_splits(const eagle_ctx* ctx, int pairs, int cap) {
+int attn_splits(const eagle_ctx* ctx, int pairs, int cap, int per_sm) {
   const int tiles = ceil_div(cap < 1 ? 1 : cap, TILE);
-  // one wave at four CTAs per SM, the tree part's CTA included
-  int want = attn_splits_bound(ctx, pairs);
+  // one wave at per_sm CTAs per SM, the tree part's CTA included
+  int want = attn_splits_bound(ctx, pairs, per_sm);
   if (want > tiles) want = tiles;
   const int per = ceil_div(tiles, want);
   return ceil_div(tiles, per);     // every split non-empty at full length
 }
+
+// CTAs per SM each kernel is sized for (its split count makes one wave).
+constexpr int kDraftPerSm = 4;
+constexpr int kVerifyPerSm = 2;
 
 template <int NR>
 static cudaError_t launch_attn_nr(const AttnParams& p, dim3 grid, size_t smem, cudaStream_t st) {
@@ -477,21 +948,35 @@ static cudaError_t launch_attn_nr(const AttnParams& p, dim3 grid, size_t smem, c
 }
 
 static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
-  p.n_splits = attn_splits(ctx, p.B * p.Hkv, p.kv_cap);
+  if (p.dh % 16 != 0 || p.dh > MAX_DH) return cudaErrorInvalidValue;
+  const bool mma = p.mode == 1;
+  p.n_splits = attn_splits(ctx, p.B * p.Hkv, p.kv_cap, mma ? kVerifyPerSm : kDraftPerSm);
   const int tiles_per_split = ceil_div(ceil_div(p.kv_cap, TILE), p.n_splits);
   p.chunk = tiles_per_split * TILE;
   p.n_buf = tiles_per_split > 1 ? 2 : 1;
   p.rows_pass = std::min(ROWS_PASS, p.rows_cap * p.G);
   dim3 grid(p.n_splits + 1, p.B * p.Hkv);
-  const size_t smem = p.n_buf * TILE_BYTES + (static_cast<size_t>(p.rows_pass) * p.dh +
-                                              static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
-  const int per_warp = ceil_div(p.rows_pass, WARPS);
   trace_before(ctx, kernel_id, st);
   cudaError_t e;
-  if (per_warp <= 1) e = launch_attn_nr<1>(p, grid, smem, st);
-  else if (per_warp <= 2) e = launch_attn_nr<2>(p, grid, smem, st);
-  else if (per_warp <= 4) e = launch_attn_nr<4>(p, grid, smem, st);
-  else e = launch_attn_nr<RW>(p, grid, smem, st);
+  if (mma) {
+    static bool attr_set = false;
+    e = cudaSuccess;
+    if (!attr_set) {
+      e = cudaFuncSetAttribute(tree_attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(2 * TILE_BYTES + Q_BYTES));
+      attr_set = e == cudaSuccess;
+    }
+    if (e == cudaSuccess)
+      e = launch_pdl(tree_attn_mma_kernel, grid, dim3(THREADS), p.n_buf * TILE_BYTES + Q_BYTES, st, p);
+  } else {
+    const size_t smem = p.n_buf * TILE_BYTES + (static_cast<size_t>(p.rows_pass) * p.dh +
+                                                static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
+    const int per_warp = ceil_div(p.rows_pass, WARPS);
+    if (per_warp <= 1) e = launch_attn_nr<1>(p, grid, smem, st);
+    else if (per_warp <= 2) e = launch_attn_nr<2>(p, grid, smem, st);
+    else if (per_warp <= 4) e = launch_attn_nr<4>(p, grid, smem, st);
+    else e = launch_attn_nr<RW>(p, grid, smem, st);
+  }
   ctx->launches++;
   trace_after(ctx, kernel_id, st);
   return e;
@@ -580,9 +1065,9 @@ void* scratch_base[kScratchMaxDevices] = {};
 
 size_t verify_scratch_need(const eagle_ctx* ctx, int batch, const eagle_kv* prefix, const eagle_tree* tree) {
   const eagle_dims& D = ctx->dims;
-  const int splits = attn_splits(ctx, batch * D.n_kv_heads, prefix->cap);
+  const int splits = attn_splits(ctx, batch * D.n_kv_heads, prefix->cap, kVerifyPerSm);
   const size_t records = static_cast<size_t>(batch) * tree->stride * D.n_q_heads * (splits + 1);
-  return records * (D.head_dim + 2) * sizeof(float);
+  return records * (D.head_dim + 4) * sizeof(float);
 }
 
 eagle_status launch_verify_attn_noalloc(eagle_ctx* ctx, int batch, const uint16_t* q, const uint16_t* kt,

@@ -159,13 +159,14 @@ struct CommitLaunch {
 cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st);
 
 // Prefix splits of the split-KV attention for `pairs` (request, kv head)
-// pairs over a cache of `cap` rows.
-int attn_splits(const eagle_ctx* ctx, int pairs, int cap);
+// pairs over a cache of `cap` rows, for a kernel run at per_sm CTAs per SM.
+int attn_splits(const eagle_ctx* ctx, int pairs, int cap, int per_sm);
 // Most prefix splits an attention launch over `pairs` (request, kv head)
-// pairs uses: one wave at four CTAs per SM with the tree part's CTA, at
-// most 31 so that a warp holds every split's record in the merge.
-inline int attn_splits_bound(const eagle_ctx* ctx, int pairs) {
-  int s = 4 * ctx->sm_count / (pairs < 1 ? 1 : pairs) - 1;
+// pairs uses: one wave at per_sm CTAs per SM (four, the most any attention
+// kernel runs at, by default) with the tree part's CTA, at most 31 so that
+// a warp holds every split's record in the merge.
+inline int attn_splits_bound(const eagle_ctx* ctx, int pairs, int per_sm = 4) {
+  int s = per_sm * ctx->sm_count / (pairs < 1 ? 1 : pairs) - 1;
   if (s > 31) s = 31;
   return s < 1 ? 1 : s;
 }

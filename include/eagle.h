@@ -318,12 +318,12 @@ eagle_status eagle_tree_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q
  * inside libeagle, one per device.
  *
  * Limit: batch * n_kv_heads <= 16384 and
- *   batch * tree.stride * n_q_heads * (splits + 1) * (head_dim + 2) * 4 bytes
+ *   batch * tree.stride * n_q_heads * (splits + 1) * (head_dim + 4) * 4 bytes
  *   <= 32 MiB - 64 KiB,
  * splits being the prefix split count the library picks (<= 31 and
- * <= 4 * SMs / (batch * n_kv_heads) - 1, at most one per 64 rows of
- * prefix.cap).  Example: batch 1, 32 query heads of 128, stride 27, 17
- * splits: 8.1 MB.
+ * <= 2 * SMs / (batch * n_kv_heads) - 1, at most one per 64 rows of
+ * prefix.cap).  Example: batch 1, 32 query heads of 128, stride 27, 8
+ * splits: 4.1 MB.
  * Beyond the limit the call returns EAGLE_ERR_CAPACITY and launches nothing;
  * use eagle_tree_verify_attn with a workspace instead.
  *

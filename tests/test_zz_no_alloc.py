@@ -67,7 +67,7 @@ def test_noalloc_matches_workspace_entry(name):
 
 
 def test_noalloc_rejects_oversize():
-    """64 query heads of 128 over 16 requests with 61-slot trees need ~130 MB
+    """64 query heads of 128 over 16 requests with 61-slot trees need ~66 MB
     of partials, beyond the fixed 32 MiB array: EAGLE_ERR_CAPACITY and the
     output untouched (nothing launched)."""
     w = S.variant("70b_x16_eagle2", name="noalloc_oversize", d=256, d_ff=512, vocab=1000, prefix_len=256)
