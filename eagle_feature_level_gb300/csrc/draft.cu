@@ -18,8 +18,11 @@ __global__ void prep_fc_kernel(const float* __restrict__ f_last, const float* __
                                const int32_t* __restrict__ token, const int32_t* __restrict__ parent,
                                const uint16_t* __restrict__ embed, int ld_embed, int d, int E, int rpr, int e0,
                                int NP, int kp, uint16_t* __restrict__ bfc) {
-  pdl_wait();      // predecessor outputs visible from here on
+  // The FC contraction after this kernel may be scheduled now (its CTAs
+  // start streaming weights); triggering before the wait in the kernels
+  // ahead of this one would bring it in while the LM head still streams.
   pdl_trigger();
+  pdl_wait();      // predecessor outputs visible from here on
   const int j = blockIdx.x;
   const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
   if (c0 >= 2 * d) return;
