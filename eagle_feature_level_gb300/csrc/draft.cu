@@ -78,13 +78,25 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
+// Order-preserving unsigned image of a non-NaN float (-0 taken as +0, so
+// equal values tie exactly as they do under ranks_before), and its inverse.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// The warp's best (v, i) under ranks_before, on every lane: two warp-wide
+// integer reductions (largest key, then smallest id among the lanes that
+// hold it).  Ids are non-negative; INT32_MAX marks an empty lane.
 __device__ __forceinline__ void warp_argmax(float& v, int& i) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
-    if (ranks_before(ov, oi, v, i)) { v = ov; i = oi; }
-  }
+  const uint32_t key = order_key(v);
+  const uint32_t best = __reduce_max_sync(0xffffffffu, key);
+  const uint32_t id = __reduce_min_sync(0xffffffffu, key == best ? static_cast<uint32_t>(i) : 0xffffffffu);
+  v = key_value(best);
+  i = static_cast<int>(id);
 }
 
 // One warp: the k best of n <= 128 candidates (z, id, q), in order, to out.
