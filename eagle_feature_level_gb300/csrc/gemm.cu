@@ -310,6 +310,13 @@ __device__ __noinline__ void stage_row_inputs(const GemmParams& p, const Smem& s
 // warps synchronised.
 __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, const EpiCol& col, int t, int jc,
                                             int nj, int m, bool prestaged) {
+  // the shared rows' pointers in registers: the loops' global stores could
+  // otherwise alias the Smem fields, forcing a re-read per row
+  float* const xch = s.xch;
+  const float* const stg2 = s.stg2;
+  const float* const rs = s.rs;
+  const int* const rowi = s.rowi;
+  float* const red = s.red;
   const int gi = col.gi, qd = col.qd, kd = col.kd, head = col.head, di = col.di, partner = col.partner;
   const bool rope = col.rope, is_v = col.is_v, rot_first = col.rot_first, d_col = col.d_col;
   const float f_hi = col.f_hi, f_lo = col.f_lo, col_bias = col.col_bias, col_gain = col.col_gain;
@@ -320,10 +327,10 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
   sm100::named_barrier(1, EPI_THREADS);
   if ((p.epi == EPI_O || p.epi == EPI_DOWN) && d_col) {
 #pragma unroll 1
-    for (int jj = 0; jj < nj; ++jj) s.xch[jj * BM + m] += s.stg2[jj * BM + m];
+    for (int jj = 0; jj < nj; ++jj) xch[jj * BM + m] += stg2[jj * BM + m];
   }
   if ((p.epi == EPI_QKV || p.epi == EPI_GATEUP) && m < nj) {      // RMSNorm scale of input row jc + m
-    const float* ss = s.stg2 + m * tiles;
+    const float* ss = stg2 + m * tiles;
     float acc4[4] = {0.f, 0.f, 0.f, 0.f};
     int i = 0;
 #pragma unroll 1
@@ -344,11 +351,11 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
       const int j = jc + jj;
       float v = 0.f;
       if (d_col) {
-        v = s.xch[jj * BM + m] + col_bias;
+        v = xch[jj * BM + m] + col_bias;
         p.out_f32[static_cast<size_t>(j) * p.d + gi] = v;
         put_split(p.bnext, p.NP, p.kp_next, j, gi, v * col_gain);
       }
-      s.xch[jj * BM + m] = v;
+      xch[jj * BM + m] = v;
     }
     sm100::named_barrier(1, EPI_THREADS);
     // sum of squares of the tile's columns of each row (next RMSNorm): warp
@@ -360,15 +367,15 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
         float sq = 0.f;
 #pragma unroll 8
         for (int k = 0; k < 32; ++k) {
-          const float x = s.xch[r * BM + 32 * w + ((k + r) & 31)];
+          const float x = xch[r * BM + 32 * w + ((k + r) & 31)];
           sq = fmaf(x, x, sq);
         }
-        s.red[w * 32 + r] = sq;
+        red[w * 32 + r] = sq;
       }
       sm100::named_barrier(1, EPI_THREADS);
       if (m < nj)
         p.ss_out[static_cast<size_t>(jc + m) * p.m_tiles + t] =
-            (s.red[m] + s.red[32 + m]) + (s.red[64 + m] + s.red[96 + m]);
+            (red[m] + red[32 + m]) + (red[64 + m] + red[96 + m]);
     }
   } else if (p.epi == EPI_QKV) {
     if (gi < qd + 2 * kd) {
@@ -376,12 +383,12 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
       for (int jj = 0; jj < nj; ++jj) {
         const int j = jc + jj;
         const int b = j / p.rpr, e = p.e0 + j % p.rpr;
-        const float sc = s.rs[jj];
-        float v = s.xch[jj * BM + m] * sc;
+        const float sc = rs[jj];
+        float v = xch[jj * BM + m] * sc;
         if (rope) {
           float sn, cs;
-          sincosf(rope_angle(s.rowi[jj], f_hi, f_lo), &sn, &cs);
-          const float other = s.xch[jj * BM + partner] * sc;
+          sincosf(rope_angle(rowi[jj], f_hi, f_lo), &sn, &cs);
+          const float other = xch[jj * BM + partner] * sc;
           v = rot_first ? v * cs - other * sn : v * cs + other * sn;
         }
         if (gi < qd) {
@@ -397,8 +404,8 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
     if (m < 64 && c < p.F) {
 #pragma unroll 1
       for (int jj = 0; jj < nj; ++jj) {
-        const float sc = s.rs[jj];
-        const float g = s.xch[jj * BM + m] * sc, u = s.xch[jj * BM + m + 64] * sc;
+        const float sc = rs[jj];
+        const float g = xch[jj * BM + m] * sc, u = xch[jj * BM + m + 64] * sc;
         put_split(p.bnext, p.NP, p.kp_next, jc + jj, c, g / (1.0f + expf(-g)) * u);
       }
     }
@@ -408,7 +415,7 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
       for (int jj = 0; jj < nj; ++jj) {
         const int j = jc + jj;
         const int b = j / p.rpr, e = p.e0 + j % p.rpr;
-        const float v = s.xch[jj * BM + m];
+        const float v = xch[jj * BM + m];
         p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.d + gi] = v;
         put_split(p.bnext, p.NP, p.kp_next, j, gi, v);
       }
@@ -419,7 +426,7 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
       for (int jj = 0; jj < nj; ++jj) {
         const int j = jc + jj;
         const int b = j / p.rpr, e = p.e0 + j % p.rpr;
-        p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.V + gi] = s.xch[jj * BM + m];
+        p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.V + gi] = xch[jj * BM + m];
       }
     }
   }
@@ -444,6 +451,8 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
   const int C = c_last - c_first + 1;
   const int blk = p.n * BM;            // one CTA's partial of the tile: n rows
   const float* part = p.part + static_cast<size_t>(t + c_first) * blk;
+  float* const xch = s.xch;            // in registers (see epilogue_chunk)
+  float* const stg = s.stg;
   if (area != nullptr && cap >= 2 * blk) {
     float* acc = area;
     float* stage = area + blk;
@@ -470,7 +479,7 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
     for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
       const int nj = min(XCH_ROWS, p.n - jc);
 #pragma unroll 1
-      for (int jj = 0; jj < nj; ++jj) s.xch[jj * BM + m] = acc[(jc + jj) * BM + m];
+      for (int jj = 0; jj < nj; ++jj) xch[jj * BM + m] = acc[(jc + jj) * BM + m];
       sm100::named_barrier(1, EPI_THREADS);
       epilogue_chunk(p, s, col, t, jc, nj, m, jc == 0);   // chunk 0's row inputs were staged early
     }
@@ -487,15 +496,15 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
       const int cn = min(cb, C - c0);
 #pragma unroll 1
       for (int c = 0; c < cn; ++c)
-        stage_block(s.stg + c * nj * BM, part + static_cast<size_t>(c0 + c) * blk + jc * BM, nj * BM, et);
+        stage_block(stg + c * nj * BM, part + static_cast<size_t>(c0 + c) * blk + jc * BM, nj * BM, et);
       cp_async_wait_all();
       sm100::named_barrier(1, EPI_THREADS);
 #pragma unroll 1
       for (int jj = 0; jj < nj; ++jj) {
-        float a = c0 == 0 ? s.stg[jj * BM + m] : s.xch[jj * BM + m] + s.stg[jj * BM + m];
+        float a = c0 == 0 ? stg[jj * BM + m] : xch[jj * BM + m] + stg[jj * BM + m];
 #pragma unroll 1
-        for (int c = 1; c < cn; ++c) a += s.stg[(c * nj + jj) * BM + m];
-        s.xch[jj * BM + m] = a;
+        for (int c = 1; c < cn; ++c) a += stg[(c * nj + jj) * BM + m];
+        xch[jj * BM + m] = a;
       }
       sm100::named_barrier(1, EPI_THREADS);
     }
