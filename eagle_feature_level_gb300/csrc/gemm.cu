@@ -346,14 +346,17 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
   sm100::named_barrier(1, EPI_THREADS);
   // 3. the contraction's elementwise epilogue, one activation row at a time
   if (p.epi == EPI_FC || p.epi == EPI_O) {
+    float* const out = p.out_f32;
+    uint16_t* const bn = p.bnext;
+    const int NP = p.NP, kpn = p.kp_next, d = p.d;
 #pragma unroll 1
     for (int jj = 0; jj < nj; ++jj) {
       const int j = jc + jj;
       float v = 0.f;
       if (d_col) {
         v = xch[jj * BM + m] + col_bias;
-        p.out_f32[static_cast<size_t>(j) * p.d + gi] = v;
-        put_split(p.bnext, p.NP, p.kp_next, j, gi, v * col_gain);
+        out[static_cast<size_t>(j) * d + gi] = v;
+        put_split(bn, NP, kpn, j, gi, v * col_gain);
       }
       xch[jj * BM + m] = v;
     }
@@ -379,10 +382,13 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
     }
   } else if (p.epi == EPI_QKV) {
     if (gi < qd + 2 * kd) {
+      float* const qrow = p.qrow;
+      float* const dst = is_v ? p.v_tree : p.k_tree;
+      const int rpr = p.rpr, e0 = p.e0, E = p.E, Hkv = p.Hkv, dh = p.dh;
 #pragma unroll 1
       for (int jj = 0; jj < nj; ++jj) {
         const int j = jc + jj;
-        const int b = j / p.rpr, e = p.e0 + j % p.rpr;
+        const int b = j / rpr, e = e0 + j % rpr;
         const float sc = rs[jj];
         float v = xch[jj * BM + m] * sc;
         if (rope) {
@@ -391,42 +397,47 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
           const float other = xch[jj * BM + partner] * sc;
           v = rot_first ? v * cs - other * sn : v * cs + other * sn;
         }
-        if (gi < qd) {
-          p.qrow[static_cast<size_t>(j) * qd + gi] = v;
-        } else {
-          float* dst = is_v ? p.v_tree : p.k_tree;
-          dst[((static_cast<size_t>(b) * p.E + e) * p.Hkv + head) * p.dh + di] = v;
-        }
+        if (gi < qd)
+          qrow[static_cast<size_t>(j) * qd + gi] = v;
+        else
+          dst[((static_cast<size_t>(b) * E + e) * Hkv + head) * dh + di] = v;
       }
     }
   } else if (p.epi == EPI_GATEUP) {
     const int c = t * 64 + m;
     if (m < 64 && c < p.F) {
+      uint16_t* const bn = p.bnext;
+      const int NP = p.NP, kpn = p.kp_next;
 #pragma unroll 1
       for (int jj = 0; jj < nj; ++jj) {
         const float sc = rs[jj];
         const float g = xch[jj * BM + m] * sc, u = xch[jj * BM + m + 64] * sc;
-        put_split(p.bnext, p.NP, p.kp_next, jc + jj, c, g / (1.0f + expf(-g)) * u);
+        put_split(bn, NP, kpn, jc + jj, c, g / (1.0f + expf(-g)) * u);
       }
     }
   } else if (p.epi == EPI_DOWN) {
     if (d_col) {
+      float* const out = p.out_f32;
+      uint16_t* const bn = p.bnext;
+      const int NP = p.NP, kpn = p.kp_next, d = p.d, rpr = p.rpr, e0 = p.e0, E = p.E;
 #pragma unroll 1
       for (int jj = 0; jj < nj; ++jj) {
         const int j = jc + jj;
-        const int b = j / p.rpr, e = p.e0 + j % p.rpr;
+        const int b = j / rpr, e = e0 + j % rpr;
         const float v = xch[jj * BM + m];
-        p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.d + gi] = v;
-        put_split(p.bnext, p.NP, p.kp_next, j, gi, v);
+        out[(static_cast<size_t>(b) * E + e) * d + gi] = v;
+        put_split(bn, NP, kpn, j, gi, v);
       }
     }
   } else {  // EPI_LM
     if (gi < p.V) {
+      float* const out = p.out_f32;
+      const int rpr = p.rpr, e0 = p.e0, E = p.E, V = p.V;
 #pragma unroll 1
       for (int jj = 0; jj < nj; ++jj) {
         const int j = jc + jj;
-        const int b = j / p.rpr, e = p.e0 + j % p.rpr;
-        p.out_f32[(static_cast<size_t>(b) * p.E + e) * p.V + gi] = xch[jj * BM + m];
+        const int b = j / rpr, e = e0 + j % rpr;
+        out[(static_cast<size_t>(b) * E + e) * V + gi] = xch[jj * BM + m];
       }
     }
   }
