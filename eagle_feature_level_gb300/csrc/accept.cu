@@ -48,24 +48,14 @@ __global__ void __launch_bounds__(SM_THREADS)
     if (ranks_before(x, v, bv, bi)) { bv = x; bi = v; }
   }
   if (bad) set_status(status, EAGLE_ERR_NUMERIC);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-  }
+  warp_argmax(bv, bi);
   if (lane == 0) { red_f[wid] = bv; red_i[wid] = bi; }
   __syncthreads();
   if (wid == 0) {
     const int nw = SM_THREADS / 32;
     bv = lane < nw ? red_f[lane] : -INFINITY;
     bi = lane < nw ? red_i[lane] : INT32_MAX;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
+    warp_argmax(bv, bi);
     if (lane == 0) { red_f[0] = bv; red_i[0] = bi; }
   }
   __syncthreads();

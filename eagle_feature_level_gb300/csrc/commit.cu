@@ -2,8 +2,9 @@
 // §12 item 3): the root and the accepted path become authoritative, rejected
 // branches are dropped by not copying them.  One CTA per (request, path
 // position): it copies that slot's K/V row of every target layer into the
-// cache at position L_b + i and gathers its true feature; position 0 also
-// writes the next round's state and appends the root's draft K/V row.
+// cache at position L_b + i and gathers its true feature.  One more CTA per
+// request, running beside them, writes the next round's state and appends
+// the root's draft K/V row.
 #include "internal.h"
 #include "common.cuh"
 
@@ -48,9 +49,40 @@ __global__ void commit_kernel(const CommitParams p) {
   pdl_trigger();
   const int b = blockIdx.x, i = blockIdx.y;
   const int a = p.accept_len[b];
+  const int L = p.kv_len[b];
+  if (i == p.path_cap) {
+    // next round's state: the last accepted slot's true feature, the bonus
+    // token, the new prefix length; the root's draft K/V row (fp32 -> bf16,
+    // four elements per load) appended to the draft cache
+    const int last = p.last_slot[b];
+    const float4* fl = reinterpret_cast<const float4*>(p.f_true + (static_cast<size_t>(b) * p.S + last) * p.d);
+    float4* fo = reinterpret_cast<float4*>(p.f_last + static_cast<size_t>(b) * p.d);
+    for (int c = threadIdx.x; c < p.d / 4; c += blockDim.x) fo[c] = fl[c];
+    if (threadIdx.x == 0) {
+      p.t_next[b] = p.final_token[b];
+      p.prefix_len_out[b] = L + 1 + a;
+    }
+    if (p.dk) {
+      const int Ld = p.draft_len[b];
+      const size_t src = (static_cast<size_t>(b) * p.E + 0) * p.row_elems;
+      const size_t dst = (static_cast<size_t>(b) * p.draft_cap + Ld) * p.row_elems;
+      const float4* ks = reinterpret_cast<const float4*>(p.dk_tree + src);
+      const float4* vs = reinterpret_cast<const float4*>(p.dv_tree + src);
+      uint2* kd = reinterpret_cast<uint2*>(p.dk + dst);
+      uint2* vd = reinterpret_cast<uint2*>(p.dv + dst);
+      for (int c = threadIdx.x; c < p.row_elems / 4; c += blockDim.x) {
+        const float4 k = ks[c], v = vs[c];
+        kd[c] = make_uint2(f32_to_bf16(k.x) | (static_cast<uint32_t>(f32_to_bf16(k.y)) << 16),
+                           f32_to_bf16(k.z) | (static_cast<uint32_t>(f32_to_bf16(k.w)) << 16));
+        vd[c] = make_uint2(f32_to_bf16(v.x) | (static_cast<uint32_t>(f32_to_bf16(v.y)) << 16),
+                           f32_to_bf16(v.z) | (static_cast<uint32_t>(f32_to_bf16(v.w)) << 16));
+      }
+      if (threadIdx.x == 0) p.draft_len_out[b] = Ld + 1;
+    }
+    return;
+  }
   if (i > a) return;
   const int slot = p.path[static_cast<size_t>(b) * p.path_cap + i];
-  const int L = p.kv_len[b];
   for (int l = 0; l < p.n_layers; ++l) {
     const size_t src = (static_cast<size_t>(b) * p.S + slot) * p.row_elems;
     const size_t dst = (static_cast<size_t>(b) * p.kv_cap + L + i) * p.row_elems;
@@ -64,26 +96,6 @@ __global__ void commit_kernel(const CommitParams p) {
     int32_t* tc = p.tok_commit + static_cast<size_t>(b) * (p.path_cap + 1);
     tc[i] = p.t_token[static_cast<size_t>(b) * p.S + slot];
     if (i == a) tc[a + 1] = p.final_token[b];
-  }
-  if (i == 0) {
-    const int last = p.last_slot[b];
-    const float4* fl = reinterpret_cast<const float4*>(p.f_true + (static_cast<size_t>(b) * p.S + last) * p.d);
-    float4* fo = reinterpret_cast<float4*>(p.f_last + static_cast<size_t>(b) * p.d);
-    for (int c = threadIdx.x; c < p.d / 4; c += blockDim.x) fo[c] = fl[c];
-    if (threadIdx.x == 0) {
-      p.t_next[b] = p.final_token[b];
-      p.prefix_len_out[b] = L + 1 + a;
-    }
-    if (p.dk) {
-      const int Ld = p.draft_len[b];
-      const size_t src = (static_cast<size_t>(b) * p.E + 0) * p.row_elems;
-      const size_t dst = (static_cast<size_t>(b) * p.draft_cap + Ld) * p.row_elems;
-      for (int c = threadIdx.x; c < p.row_elems; c += blockDim.x) {
-        p.dk[dst + c] = f32_to_bf16(p.dk_tree[src + c]);
-        p.dv[dst + c] = f32_to_bf16(p.dv_tree[src + c]);
-      }
-      if (threadIdx.x == 0) p.draft_len_out[b] = Ld + 1;
-    }
   }
 }
 
@@ -125,7 +137,7 @@ cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st
   p.t_next = C.out->t_next;
   p.prefix_len_out = C.out->prefix_len;
   p.draft_len_out = C.out->draft_len;
-  dim3 grid(C.batch, C.acc->path_cap);
+  dim3 grid(C.batch, C.acc->path_cap + 1);
   trace_before(ctx, EAGLE_K_COMMIT, st);
   const cudaError_t e = launch_pdl(commit_kernel, grid, dim3(512), 0, st, p);
   ctx->launches++;

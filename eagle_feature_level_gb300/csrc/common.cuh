@@ -143,6 +143,27 @@ __device__ __forceinline__ int block_max_i(int v, int* scratch) {
   return warp_max_i(r);
 }
 
+// Order-preserving unsigned image of a non-NaN float (-0 taken as +0, so
+// equal values tie exactly as they do under ranks_before), and its inverse.
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t u = __float_as_uint(v + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// The warp's best (v, i) -- larger v first, then smaller i -- on every lane: two warp-wide
+// integer reductions (largest key, then smallest id among the lanes that
+// hold it).  Ids are non-negative; INT32_MAX marks an empty lane.
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+  const uint32_t key = order_key(v);
+  const uint32_t best = __reduce_max_sync(0xffffffffu, key);
+  const uint32_t id = __reduce_min_sync(0xffffffffu, key == best ? static_cast<uint32_t>(i) : 0xffffffffu);
+  v = key_value(best);
+  i = static_cast<int>(id);
+}
+
 // ---- device status word -----------------------------------------------------
 // First int of the workspace.  The first error wins; later ones are dropped.
 __device__ __forceinline__ void set_status(int* status, int code) {

@@ -78,27 +78,6 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
   return va > vb || (va == vb && ia < ib);
 }
 
-// Order-preserving unsigned image of a non-NaN float (-0 taken as +0, so
-// equal values tie exactly as they do under ranks_before), and its inverse.
-__device__ __forceinline__ uint32_t order_key(float v) {
-  const uint32_t u = __float_as_uint(v + 0.0f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
-// The warp's best (v, i) under ranks_before, on every lane: two warp-wide
-// integer reductions (largest key, then smallest id among the lanes that
-// hold it).  Ids are non-negative; INT32_MAX marks an empty lane.
-__device__ __forceinline__ void warp_argmax(float& v, int& i) {
-  const uint32_t key = order_key(v);
-  const uint32_t best = __reduce_max_sync(0xffffffffu, key);
-  const uint32_t id = __reduce_min_sync(0xffffffffu, key == best ? static_cast<uint32_t>(i) : 0xffffffffu);
-  v = key_value(best);
-  i = static_cast<int>(id);
-}
-
 // One warp: the k best of n <= 128 candidates (z, id, q), in order, to out.
 // Lane l holds candidates l, l + 32, l + 64, l + 96.
 __device__ __forceinline__ void warp_merge_topk(const float* cz, const int* ci, const float* cq, int n, int k,
