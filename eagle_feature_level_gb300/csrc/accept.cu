@@ -117,20 +117,27 @@ __global__ void __launch_bounds__(SM_THREADS) accept_walk_kernel(const WalkParam
   const float T = p.temperature[b];
   int32_t* path = p.path + static_cast<size_t>(b) * p.path_cap;
 
-  if (!(T > 0.f)) {  // greedy walk
+  if (!(T > 0.f)) {  // greedy walk, over the tree staged in shared memory
+    __shared__ int s_par[EAGLE_MAX_NODES], s_tok[EAGLE_MAX_NODES], s_am[EAGLE_MAX_NODES];
+    const int size = min(p.t_size[b], EAGLE_MAX_NODES);
+    for (int c = tid; c < size; c += blockDim.x) {
+      s_par[c] = p.t_parent[tb + c];
+      s_tok[c] = p.t_token[tb + c];
+      s_am[c] = p.argmax[tb + c];
+    }
+    __syncthreads();
     if (tid == 0) {
-      const int size = p.t_size[b];
       int u = 0, a = 0;
       path[0] = 0;
-      int g = p.argmax[tb];
+      int g = s_am[0];
       while (true) {
         int nxt = -1;
         for (int c = 1; c < size; ++c)
-          if (p.t_parent[tb + c] == u && p.t_token[tb + c] == g) { nxt = c; break; }
+          if (s_par[c] == u && s_tok[c] == g) { nxt = c; break; }
         if (nxt < 0 || a + 1 >= p.path_cap) break;
         u = nxt;
         path[++a] = u;
-        g = p.argmax[tb + u];
+        g = s_am[u];
       }
       p.accept_len[b] = a;
       p.final_token[b] = g;
