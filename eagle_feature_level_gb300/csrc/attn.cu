@@ -402,16 +402,14 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
   cp_async_wait<0>();                        // nothing may land after the CTA has left
 
   // the last CTA of this (request, kv head) merges the splits in order
-  __threadfence();
-  __syncthreads();
+  __syncthreads();                           // every thread's partial records come first
   if (threadIdx.x == 0) {
-    const int prev = atomicAdd(&p.counters[pair], 1);
+    const int prev = arrive_acq_rel(&p.counters[pair]);
     s_last = prev == p.n_splits;
     if (s_last) p.counters[pair] = 0;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   for (int r = warp; r < R; r += WARPS) {
     const int node = r / p.G, hq = h * p.G + r % p.G;
     const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
@@ -848,16 +846,14 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
   cp_async_wait<0>();                        // nothing may land after the CTA has left
 
   // the last CTA of this (request, kv head) merges the splits in order
-  __threadfence();
-  __syncthreads();
+  __syncthreads();                           // every thread's partial records come first
   if (threadIdx.x == 0) {
-    const int prev = atomicAdd(&p.counters[pair], 1);
+    const int prev = arrive_acq_rel(&p.counters[pair]);
     s_last = prev == p.n_splits;
     if (s_last) p.counters[pair] = 0;
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   // Every record of a batch of rows is copied into shared memory at once
   // (16-byte asynchronous copies: a row's ns records are contiguous), then a
   // warp per row merges from shared memory: lane s < ns holds split s's

@@ -164,6 +164,19 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
   i = static_cast<int>(id);
 }
 
+// ---- last-arriver counters ------------------------------------------------
+// One thread's arrival on a per-tile (or per-pair) counter, issued after a
+// CTA barrier that follows the CTA's partial-result stores.  Release is
+// cumulative over the barrier, so the CTA that observes the final count sees
+// those stores; acquire makes the earlier arrivals' stores visible here (the
+// rest of the CTA reads them after the next barrier).  Takes the place of a
+// full fence on every thread before and after a relaxed atomic.
+__device__ __forceinline__ int arrive_acq_rel(int* counter) {
+  int prev;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(prev) : "l"(counter) : "memory");
+  return prev;
+}
+
 // ---- device status word -----------------------------------------------------
 // First int of the workspace.  The first error wins; later ones are dropped.
 __device__ __forceinline__ void set_status(int* status, int code) {

@@ -801,17 +801,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
       sm100::tc_fence_before();
       __syncwarp();
       if (lane == 0) sm100::mbar_arrive(&s.tempty[buf]);
-      __threadfence();
-      sm100::named_barrier(1, EPI_THREADS);
+      sm100::named_barrier(1, EPI_THREADS);     // every epilogue thread's partial stores come first
       if (et == 0) {
-        const int prev = atomicAdd(&p.counters[t], 1);
+        const int prev = arrive_acq_rel(&p.counters[t]);
         const int last = prev == c_last - c_first;
         if (last) p.counters[t] = 0;
         s.flags[1] = last;
       }
       sm100::named_barrier(1, EPI_THREADS);
       if (s.flags[1]) {
-        __threadfence();
         // on the CTA's last tile the pipeline ring is idle: all of its loads
         // were consumed by MMAs that have completed
         int t2;
