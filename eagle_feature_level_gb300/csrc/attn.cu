@@ -414,15 +414,31 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
     const int node = r / p.G, hq = h * p.G + r % p.G;
     const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
     const float* src = p.part + qi * (p.n_splits + 1) * rec;
-    // lane s holds split s (n_splits + 1 <= 32): all partial headers load at once
+    // lane s holds split s (n_splits + 1 <= 32): all partial headers, and
+    // the outputs of the first 16 splits, are requested at once
     const int ns = p.n_splits + 1;
     const float ms = lane < ns ? __ldcg(src + lane * rec) : -INFINITY;
     const float ls = lane < ns ? __ldcg(src + lane * rec + 1) : 0.f;
+    float first[16][4];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int d = lane + 32 * c;
+        first[u][c] = (u < ns && d < dh) ? __ldcg(src + u * rec + 4 + d) : 0.f;
+      }
+    }
     const float M = warp_max(ms);
     const float wgt = ms == -INFINITY ? 0.f : __expf(ms - M);
     const float Lsum = warp_sum(wgt * ls);
     float o[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s0 = 0; s0 < ns; s0 += 8) {
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float ws = __shfl_sync(0xffffffffu, wgt, u);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) o[c] = fmaf(ws, first[u][c], o[c]);
+    }
+    for (int s0 = 16; s0 < ns; s0 += 8) {
       float vals[8][4];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {

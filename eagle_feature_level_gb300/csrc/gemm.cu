@@ -478,7 +478,7 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
 #pragma unroll 1
       for (int i = 4 * et; i < blk; i += 4 * EPI_THREADS) {
         float4 a = c0 == 0 ? *reinterpret_cast<const float4*>(stage + i) : *reinterpret_cast<const float4*>(acc + i);
-#pragma unroll 1
+#pragma unroll 4
         for (int c = c0 == 0 ? 1 : 0; c < cn; ++c) {
           const float4 x = *reinterpret_cast<const float4*>(stage + static_cast<size_t>(c) * blk + i);
           a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
