@@ -188,6 +188,38 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
     }
   }
   if (bad) set_status(p.status, EAGLE_ERR_NUMERIC);
+  if (greedy) {
+    // each warp's k best (logit desc, id asc): no softmax statistic is needed,
+    // so they are ranked before the cluster exchanges (probabilities later)
+    uint32_t taken = 0;
+    float bv = -INFINITY;
+    int bi = INT32_MAX, bs = -1;
+#pragma unroll
+    for (int u = 0; u < SEL_PER; ++u)
+      if (v0 + u < V && ranks_before(x[u], v0 + u, bv, bi)) { bv = x[u]; bi = v0 + u; bs = u; }
+    for (int r = 0; r < k; ++r) {
+      float wv = bv;
+      int wi = bi;
+      warp_argmax(wv, wi);
+      if (bs >= 0 && wi == bi && bi != INT32_MAX) {
+        s_wz[wid * k + r] = bv;
+        s_wi[wid * k + r] = bi;
+        s_wq[wid * k + r] = 0.f;
+        taken |= 1u << bs;
+        bv = -INFINITY; bi = INT32_MAX; bs = -1;
+#pragma unroll
+        for (int u = 0; u < SEL_PER; ++u)
+          if (!((taken >> u) & 1u) && v0 + u < V && ranks_before(x[u], v0 + u, bv, bi)) {
+            bv = x[u]; bi = v0 + u; bs = u;
+          }
+      }
+      if (wi == INT32_MAX && lane == 0) {
+        s_wz[wid * k + r] = -INFINITY;
+        s_wi[wid * k + r] = INT32_MAX;
+        s_wq[wid * k + r] = 0.f;
+      }
+    }
+  }
   lmax = warp_max(lmax);
   if (lane == 0) s_red[wid] = lmax;
   __syncthreads();
@@ -201,6 +233,16 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
   sm100::cluster_sync();
   float m = s_cmax[0];
   for (int c = 1; c < SEL_CL; ++c) m = fmaxf(m, s_cmax[c]);
+  if (greedy && wid == 0) {
+    // the CTA's list (from the warps' lists, complete since the barrier
+    // before the max push) goes straight into rank 0's candidate table
+    warp_merge_topk(s_wz, s_wi, s_wq, SEL_WARPS * k, k, s_cz + rank * k, s_ci + rank * k, s_cq + rank * k);
+    if (lane < k) {
+      const int c = rank * k + lane;
+      sm100::dsmem_st_f32(sm100::dsmem_addr(&s_cz[c], 0), s_cz[c]);
+      sm100::dsmem_st_s32(sm100::dsmem_addr(&s_ci[c], 0), s_ci[c]);
+    }
+  }
 
   // exponentials, slice sum in a fixed order, cluster sum in rank order
   float ex[SEL_PER];
@@ -237,57 +279,14 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
   }
 
   if (greedy) {
-    // each warp's k best (logit desc, id asc), then the CTA's, then rank 0 merges the cluster's
-    uint32_t taken = 0;
-    float bv = -INFINITY;
-    int bi = INT32_MAX, bs = -1;
-#pragma unroll
-    for (int u = 0; u < SEL_PER; ++u)
-      if (v0 + u < V && ranks_before(x[u], v0 + u, bv, bi)) { bv = x[u]; bi = v0 + u; bs = u; }
-    for (int r = 0; r < k; ++r) {
-      float wv = bv;
-      int wi = bi;
-      warp_argmax(wv, wi);
-      if (bs >= 0 && wi == bi && bi != INT32_MAX) {
-        float qv = 0.f;
-#pragma unroll
-        for (int u = 0; u < SEL_PER; ++u)
-          if (u == bs) qv = q[u];
-        s_wz[wid * k + r] = bv;
-        s_wi[wid * k + r] = bi;
-        s_wq[wid * k + r] = qv;
-        taken |= 1u << bs;
-        bv = -INFINITY; bi = INT32_MAX; bs = -1;
-#pragma unroll
-        for (int u = 0; u < SEL_PER; ++u)
-          if (!((taken >> u) & 1u) && v0 + u < V && ranks_before(x[u], v0 + u, bv, bi)) {
-            bv = x[u]; bi = v0 + u; bs = u;
-          }
-      }
-      if (wi == INT32_MAX && lane == 0) {
-        s_wz[wid * k + r] = -INFINITY;
-        s_wi[wid * k + r] = INT32_MAX;
-        s_wq[wid * k + r] = 0.f;
-      }
-    }
-    __syncthreads();
-    if (wid == 0) {
-      // the CTA's list goes straight into rank 0's candidate table
-      warp_merge_topk(s_wz, s_wi, s_wq, SEL_WARPS * k, k, s_cz + rank * k, s_ci + rank * k, s_cq + rank * k);
-      if (lane < k) {
-        const int c = rank * k + lane;
-        sm100::dsmem_st_f32(sm100::dsmem_addr(&s_cz[c], 0), s_cz[c]);
-        sm100::dsmem_st_s32(sm100::dsmem_addr(&s_ci[c], 0), s_ci[c]);
-        sm100::dsmem_st_f32(sm100::dsmem_addr(&s_cq[c], 0), s_cq[c]);
-      }
-    }
-    sm100::cluster_sync();
+    // rank 0 merges the cluster's lists (complete since the second barrier);
+    // a child's probability is its q entry, recomputed by the same expression
     if (rank != 0 || wid != 0) return;
-    warp_merge_topk(s_cz, s_ci, s_cq, SEL_CL * k, k, nullptr, s_wi, s_wq);
+    warp_merge_topk(s_cz, s_ci, s_cq, SEL_CL * k, k, s_wz, s_wi, s_wq);
     if (lane < p.K) {
       const bool ok = lane < k && s_wi[lane] != INT32_MAX && s_wi[lane] < V;
       ct[lane] = ok ? s_wi[lane] : -1;
-      cp[lane] = ok ? s_wq[lane] : 0.f;
+      cp[lane] = ok ? expf((s_wz[lane] - m) * inv_t) * invS : 0.f;
     }
     return;
   }
