@@ -211,7 +211,7 @@ __device__ __forceinline__ void tile_compute(const AttnParams& p, RowState<NR>& 
       const bool v1 = !F32 && j1 < nt && ((mask >> (key_base + (j1 & 63))) & 1ull);
       const float a = v0 ? s0[i] * p.scale : -INFINITY;
       const float c = v1 ? s1[i] * p.scale : -INFINITY;
-      const float m_new = fmaxf(st.m[i], warp_max(fmaxf(a, c)));
+      const float m_new = fmaxf(st.m[i], warp_max_redux(fmaxf(a, c)));
       float p0 = 0.f, p1 = 0.f, corr = 1.f;
       if (m_new != -INFINITY) {
         p0 = __expf(a - m_new);

@@ -153,6 +153,12 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
+// The warp's largest non-NaN value on every lane, in one reduction (-0 and
+// +0 compare equal; the result is then +0).
+__device__ __forceinline__ float warp_max_redux(float v) {
+  return key_value(__reduce_max_sync(0xffffffffu, order_key(v)));
+}
+
 // The warp's best (v, i) -- larger v first, then smaller i -- on every lane: two warp-wide
 // integer reductions (largest key, then smallest id among the lanes that
 // hold it).  Ids are non-negative; INT32_MAX marks an empty lane.

@@ -220,7 +220,7 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
       }
     }
   }
-  lmax = warp_max(lmax);
+  lmax = warp_max_redux(lmax);
   if (lane == 0) s_red[wid] = lmax;
   __syncthreads();
   if (tid < SEL_CL) {                        // push this CTA's max to every rank
