@@ -280,28 +280,20 @@ def run_ours(args):
     kernel_us = {n: round(1e3 * c[1] / k_tr, 2) for n, c in sorted(by_class.items())}
 
     # ---- end to end through the public API with host buffers ----
-    pin = lambda t: t.detach().to("cpu").pin_memory()
-    host_in = {"t_next": pin(rd.t_next), "f_last": pin(rd.f_last), "pos0": pin(rd.pos0),
-               "temps": pin(rd.temps), "target_logits": pin(rd.target_logits), "f_true": pin(rd.f_true),
-               "tree_q": pin(rd.tree_q), "tree_k": pin(rd.tree_k[0]), "tree_v": pin(rd.tree_v[0])}
-    dev_in = {"t_next": rd.t_next, "f_last": rd.f_last, "pos0": rd.pos0, "temps": rd.temps,
-              "target_logits": rd.target_logits, "f_true": rd.f_true, "tree_q": rd.tree_q,
-              "tree_k": rd.tree_k[0], "tree_v": rd.tree_v[0]}
-    dev_out = {"accept_len": rd.accept_len, "path": rd.path, "final_token": rd.final_token,
-               "tok_commit": rd.tok_commit, "f_last_out": rd.f_last_out, "prefix_len_out": rd.prefix_len_out}
-    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in dev_out.items()}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    # the round's host-facing tensors live in one device allocation per
+    # direction (runtime.Round.io_in / io_out): one copy each way per step
+    host_in = rd.io_in.detach().to("cpu").pin_memory()
+    host_out = torch.empty(rd.io_out.shape, dtype=rd.io_out.dtype, pin_memory=True)
+    h2d = host_in.numel() * host_in.element_size()
+    d2h = host_out.numel() * host_out.element_size()
     k_e2e = max(1, min(args.steps, 200))
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     for _ in range(k_e2e):
-        for k, t in host_in.items():
-            dev_in[k].copy_(t, non_blocking=True)
+        rd.io_in.copy_(host_in, non_blocking=True)
         graph.replay()
-        for k, t in dev_out.items():
-            host_out[k].copy_(t, non_blocking=True)
+        host_out.copy_(rd.io_out, non_blocking=True)
         stream.synchronize()
     el = max_over_ranks(time.perf_counter() - t0, world, dev)
     e2e_value = world * nodes_per_round * k_e2e / el

@@ -88,6 +88,20 @@ class Engine:
             ld(W["embed"]), _p(W["w_lm"]), ld(W["w_lm"]))
 
 
+def _packed(specs, device):
+    """One zeroed device allocation holding several tensors at 256-byte
+    aligned offsets: a host buffer of the same layout moves all of them in
+    one copy.  specs: [(shape, dtype)]; returns (flat uint8 tensor, views)."""
+    offs, total = [], 0
+    for shape, dtype in specs:
+        n = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+        offs.append((total, n))
+        total += (n + 255) // 256 * 256
+    flat = torch.zeros(max(total, 256), dtype=torch.uint8, device=device)
+    views = [flat[o:o + n].view(dtype).view(shape) for (o, n), (shape, dtype) in zip(offs, specs)]
+    return flat, views
+
+
 class Round:
     """Caller-side buffers and ABI structs of one round (batch B, plan fixed)."""
 
@@ -104,11 +118,21 @@ class Round:
         f32 = dict(dtype=torch.float32, device=dev)
         bf = dict(dtype=torch.bfloat16, device=dev)
         z = torch.zeros
-        # request state
-        self.t_next = z(batch, **i32)
-        self.f_last = z(batch, d, **f32)
-        self.pos0 = z(batch, **i32)
-        self.temps = z(batch, **f32)
+        # What a round takes from the host (request state, the target's
+        # verification-layer inputs and outputs) and gives back (acceptance
+        # and commit results) sits in one allocation each way: `io_in` and
+        # `io_out`, one copy per direction and round.
+        self.io_in, (self.t_next, self.f_last, self.pos0, self.temps, self.target_logits, self.f_true,
+                     self.tree_q, tree_k0, tree_v0) = _packed(
+            [((batch,), torch.int32), ((batch, d), torch.float32), ((batch,), torch.int32),
+             ((batch,), torch.float32), ((batch, S, V), torch.float32), ((batch, S, d), torch.float32),
+             ((batch, S, Hq, dh), torch.bfloat16), ((batch, S, Hkv, dh), torch.bfloat16),
+             ((batch, S, Hkv, dh), torch.bfloat16)], dev)
+        self.io_out, (self.accept_len, self.path, self.final_token, self.tok_commit, self.f_last_out,
+                      self.prefix_len_out) = _packed(
+            [((batch,), torch.int32), ((batch, self.path_cap), torch.int32), ((batch,), torch.int32),
+             ((batch, self.path_cap + 1), torch.int32), ((batch, d), torch.float32), ((batch,), torch.int32)],
+            dev)
         self.draft_k = z(batch, kv_cap, Hkv, dh, **bf)
         self.draft_v = z(batch, kv_cap, Hkv, dh, **bf)
         self.draft_len = z(batch, **i32)
@@ -138,27 +162,18 @@ class Round:
         self.t_size = z(batch, **i32)
         # verification layer(s) and the target's outputs
         self.n_layers = n_target_layers
-        self.tree_q = z(batch, S, Hq, dh, **bf)
-        self.tree_k = [z(batch, S, Hkv, dh, **bf) for _ in range(n_target_layers)]
-        self.tree_v = [z(batch, S, Hkv, dh, **bf) for _ in range(n_target_layers)]
+        self.tree_k = [tree_k0] + [z(batch, S, Hkv, dh, **bf) for _ in range(n_target_layers - 1)]
+        self.tree_v = [tree_v0] + [z(batch, S, Hkv, dh, **bf) for _ in range(n_target_layers - 1)]
         self.tgt_k = [z(batch, kv_cap, Hkv, dh, **bf) for _ in range(n_target_layers)]
         self.tgt_v = [z(batch, kv_cap, Hkv, dh, **bf) for _ in range(n_target_layers)]
         self.tgt_len = z(batch, **i32)
         self.attn_out = z(batch, S, Hq, dh, **f32)
-        self.target_logits = z(batch, S, V, **f32)
         self.target_probs = z(batch, S, V, **f32)
         self.target_argmax = z(batch, S, **i32)
-        self.f_true = z(batch, S, d, **f32)
         # accept + commit outputs
-        self.accept_len = z(batch, **i32)
-        self.path = z(batch, self.path_cap, **i32)
-        self.final_token = z(batch, **i32)
         self.last_slot = z(batch, **i32)
         self.f_commit = z(batch, self.path_cap, d, **f32)
-        self.tok_commit = z(batch, self.path_cap + 1, **i32)
-        self.f_last_out = z(batch, d, **f32)
         self.t_next_out = z(batch, **i32)
-        self.prefix_len_out = z(batch, **i32)
         self.draft_len_out = z(batch, **i32)
         self.seed, self.round_id = 0, 0
         self._structs()
