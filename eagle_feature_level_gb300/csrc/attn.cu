@@ -710,7 +710,6 @@ __device__ __forceinline__ void store_state(const WarpState& st, float* slot, in
 // are staged, 32 keys per tile.
 __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnParams p) {
   pdl_trigger();
-  if (p.mode == 1) pdl_wait();               // verification reads the tree's size first
   extern __shared__ __align__(16) uint8_t smem_attn[];
   __shared__ int s_last;
   __shared__ uint64_t s_mask[ROWS_PASS];     // ancestor masks of the pass's rows (tree part)
@@ -724,25 +723,22 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
   uint16_t* qhi = reinterpret_cast<uint16_t*>(smem_attn + p.n_buf * TILE_BYTES);
   uint16_t* qlo = qhi + ROWS_PASS * KLD;
   float* mrg = reinterpret_cast<float*>(qhi);   // after a pass's last tile, the query rows are dead
-  const int nodes = n_nodes(p, b);
-  const int R = nodes * p.G;
   const bool is_tree = split == p.n_splits;
   const bool tree_f32 = is_tree && p.mode == 0;
+  // The prefix and its length are this round's inputs, written by no kernel
+  // of the round: a prefix split's range and tiles are known (and its tiles
+  // requested) before the dependency wait.  The tree part's size, the query
+  // rows and the tree K/V come from the predecessors.
   int lo = 0, hi = 0;
   if (!is_tree) {
     const int L = p.kv_len[b];
     lo = split * p.chunk;
     hi = min(L, lo + p.chunk);
-  } else {
-    hi = p.mode == 0 ? p.tree_cap : min(p.tree_size[b], p.tree_cap);
   }
   const int rec = dh + 4;                    // partial record: max, sum, 2 unused, output[dh]
   const size_t row_stride = static_cast<size_t>(p.Hkv) * dh;
   const uint64_t policy = sm100::l2_policy_evict_first();
   const int step = tree_f32 ? TILE_F32 : TILE;
-  const int n_tiles = hi > lo ? (hi - lo + step - 1) / step : 0;
-  // A split whose keys fit one buffer stages them once for every pass.
-  const bool resident = n_tiles <= 1;
 
   auto stage = [&](int tile, int which) {
     uint16_t* buf = reinterpret_cast<uint16_t*>(bufs + which * TILE_BYTES);
@@ -757,18 +753,32 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
       stage_bf16(buf, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + t0) * p.Hkv + h) * dh, row_stride, nt, dh,
                  policy);
   };
-  // The prefix KV is not written by the kernels of this draft step: its
-  // first tile is requested before waiting on the predecessor.
-  if (!is_tree && n_tiles > 0) stage(0, 0);
-  pdl_wait();                                // q rows, tree K/V and masks come from the predecessors
-  if (is_tree && n_tiles > 0) stage(0, 0);
+  // tiles [0, staged) of the current pass have been requested; a split
+  // whose tiles all fit the buffers stages them once for every pass
+  int n_tiles = hi > lo ? (hi - lo + step - 1) / step : 0;
+  int staged = 0;
+  if (!is_tree) {
+    for (; staged < n_tiles && staged < p.n_buf; ++staged) stage(staged, staged);
+  }
+  pdl_wait();                                // q rows, tree K/V, masks and the tree's size
+  const int nodes = n_nodes(p, b);
+  const int R = nodes * p.G;
+  if (is_tree) {
+    hi = p.mode == 0 ? p.tree_cap : min(p.tree_size[b], p.tree_cap);
+    n_tiles = hi > lo ? (hi - lo + step - 1) / step : 0;
+    for (; staged < n_tiles && staged < p.n_buf; ++staged) stage(staged, staged);
+  }
+  const bool resident = n_tiles <= p.n_buf;
 
   for (int r0 = 0; r0 < R; r0 += ROWS_PASS) {
     const int rp = min(ROWS_PASS, R - r0);
     const int MT = rp > 16 ? 2 : 1;
     const int KS = WARPS / MT;               // warps sharing a row tile
     const int mt = warp % MT, ks = warp / MT;
-    if (r0 > 0) __syncthreads();             // the previous pass is done with the query rows and buffers
+    if (r0 > 0) {
+      __syncthreads();                       // the previous pass is done with the query rows and buffers
+      if (!resident) staged = 0;
+    }
     // query rows of the pass as bf16 hi (+ lo for fp32 queries); rows past rp are zero
     for (int idx = threadIdx.x; idx < 16 * MT * (dh >> 2); idx += THREADS) {
       const int rr = idx / (dh >> 2), c = idx - rr * (dh >> 2);
@@ -796,24 +806,18 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
     for (int j = 0; j < MAX_DH / 8; ++j) st.o[j][0] = st.o[j][1] = st.o[j][2] = st.o[j][3] = 0.f;
     for (int tile = 0; tile < n_tiles; ++tile) {
       const int which = p.n_buf > 1 ? (tile & 1) : 0;
-      if (!resident) {
-        // staged earlier: tile 0 of the first pass (prologue), or by the
-        // previous iteration's prefetch when two buffers alternate
-        const bool staged = (r0 == 0 && tile == 0) || (p.n_buf > 1 && tile > 0);
-        if (!staged) {
-          __syncthreads();                   // every warp is done with this buffer
-          stage(tile, which);
-        }
-        if (p.n_buf > 1 && tile + 1 < n_tiles) {
-          __syncthreads();                   // the other buffer's previous tile is consumed
-          stage(tile + 1, which ^ 1);
-          cp_async_wait<1>();                // this tile's copies have landed
-        } else {
-          cp_async_wait<0>();
-        }
-      } else {
-        cp_async_wait<0>();
+      if (tile >= staged) {
+        __syncthreads();                     // every warp is done with this buffer
+        stage(tile, which);
+        staged = tile + 1;
       }
+      if (p.n_buf > 1 && tile + 1 < n_tiles && tile + 1 >= staged) {
+        __syncthreads();                     // the other buffer's previous tile is consumed
+        stage(tile + 1, which ^ 1);
+        staged = tile + 2;
+      }
+      if (staged > tile + 1) cp_async_wait<1>();   // this tile's copies have landed (the next may fly)
+      else cp_async_wait<0>();
       __syncthreads();
       const int t0 = lo + tile * step;
       const int nt = min(step, hi - t0);
