@@ -40,9 +40,9 @@ ALPHA = (0.9, 0.7, 0.6, 0.6, 0.6, 0.6)   # injected per-layer acceptance profile
 # DRAM bytes (read + write) per gemm_stream_kernel launch from one ncu capture
 # (profiles/gemm_stream_7b_static26.md).  Reported only while the kernel's
 # sources are the ones the counters were taken on.
-GEMM_TRAFFIC = {"workload": "7b_static26", "bytes_per_launch": 125183394,
+GEMM_TRAFFIC = {"workload": "7b_static26", "bytes_per_launch": 125171209,
                 "sources": ("gemm.cu", "sm100.cuh", "common.cuh"),
-                "sha256": "c0dd60f624c0a688d1fbd978853b6ad037aeb04ff3c64740e8daea56b07ec996"}
+                "sha256": "0981a4b227111620be844b01977a5b32b1662865f0ec0c1c49243b8b636a9a10"}
 
 
 def gemm_traffic(workload: str):
