@@ -159,13 +159,18 @@ def algorithmic_bytes(w, inp) -> float:
     return n_fwd * weight_bytes_per_forward(w) + n_fwd * draft_kv + verify_kv
 
 
-def cpu_baseline(w, seed, W, inp, budget_s=20.0, max_rounds=None):
-    """The oracle as it stands, on the host cores: full rounds of request 0."""
+def cpu_baseline(w, seed, W, inp, budget_s=20.0, max_rounds=None, warmup=0):
+    """The oracle as it stands, on the host cores: full rounds of request 0
+    (after up to `warmup` untimed rounds, at most ~30 s of them)."""
     from oracle.layer import DraftWeights
     from oracle.round import numpy_inputs, run_round
     Wc = {k: v.detach().cpu() for k, v in W.items()}
     ic = numpy_inputs({k: (v.detach().cpu() if torch.is_tensor(v) else v) for k, v in inp.items()})
     Wd = DraftWeights(Wc, w)
+    warm, t_w = 0, time.perf_counter()
+    while warm < warmup and time.perf_counter() - t_w < 30.0:
+        run_round(Wd, w, ic, requests=[0])
+        warm += 1
     rounds, t0 = 0, time.perf_counter()
     while True:
         run_round(Wd, w, ic, requests=[0])
@@ -176,7 +181,7 @@ def cpu_baseline(w, seed, W, inp, budget_s=20.0, max_rounds=None):
     nodes = w.top_m
     return {"value": nodes * rounds / el, "unit": "tree nodes/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{rounds} full rounds of request 0 of {w.name} ({el:.1f} s, numpy fp64, BLAS threads "
-                      f"= host cores)"}, rounds, el
+                      f"= host cores)", "warmup_rounds": warm}, rounds, el
 
 
 def run_reference(args):
@@ -187,10 +192,12 @@ def run_reference(args):
     seed = S.WORKLOAD_SEEDS[args.workload]
     W = S.draft_weights(w, seed, device="cpu")
     inp = S.round_inputs(w, seed, device="cpu")
-    base, rounds, el = cpu_baseline(w, seed, W, inp, budget_s=90.0, max_rounds=max(1, args.steps))
+    base, rounds, el = cpu_baseline(w, seed, W, inp, budget_s=90.0, max_rounds=max(1, args.steps),
+                                    warmup=args.warmup)
+    warm = base.pop("warmup_rounds")
     ms = 1000.0 * el / rounds
     line = {"metric": METRIC, "value": base["value"], "unit": "tree nodes/s", "n_gpus": args.gpus,
-            "steps": rounds, "warmup": 0, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "steps": rounds, "warmup": warm, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": describe(w), "sample": base["sample"]},
             "cpu_baseline": base,
@@ -302,6 +309,7 @@ def run_ours(args):
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         base, _, _ = cpu_baseline(w, seed, W, inp, budget_s=args.cpu_budget)
+        base.pop("warmup_rounds", None)
 
     alg = algorithmic_bytes(w, {"draft_len": inp["draft_len"], "prefix_len": inp["prefix_len"]})
     clocks = clk.summary()
