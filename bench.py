@@ -42,7 +42,7 @@ ALPHA = (0.9, 0.7, 0.6, 0.6, 0.6, 0.6)   # injected per-layer acceptance profile
 # sources are the ones the counters were taken on.
 GEMM_TRAFFIC = {"workload": "7b_static26", "bytes_per_launch": 125171209,
                 "sources": ("gemm.cu", "sm100.cuh", "common.cuh"),
-                "sha256": "0981a4b227111620be844b01977a5b32b1662865f0ec0c1c49243b8b636a9a10"}
+                "sha256": "72df5f1ad9bb4e47661dfe7af21dec0d955cc36dbf6e5c6172130195c0421339"}
 
 
 def gemm_traffic(workload: str):

@@ -21,11 +21,14 @@
 //    ring slot;
 //  * activations enter as two bf16 halves (x = hi + lo), stacked along N, so
 //    the fp32 activation keeps ~16 mantissa bits while the weights stay bf16;
-//  * work is split stream-K style: the (tile, k-block) units of the whole
-//    matrix are divided evenly over one CTA per SM, so every SM streams the
-//    same number of bytes; each CTA writes its fp32 partial of a tile and the
-//    last CTA to finish the tile sums the partials in CTA order
-//    (deterministic);
+//  * work is split stream-K style: the (tile, k-block) units are divided
+//    evenly over the CTAs, so every SM streams the same number of bytes.
+//    Contractions with fewer 128-row tiles than SMs run two CTAs per SM with
+//    half-size rings (every tile split); the others run one CTA per SM, the
+//    stream-K share of the leftover tiles first, then whole tiles of their
+//    own with the epilogue straight from tensor memory.  For a split tile
+//    each CTA writes its fp32 partial and arrives on the tile's counter; the
+//    last to arrive sums the partials in CTA order (deterministic);
 //  * the epilogue of that last CTA fuses the layer's elementwise work: bias,
 //    residual adds, RMSNorm scaling (sum of squares carried as per-tile
 //    partials), RoPE, SiLU-gating, the bf16 hi/lo split of the next
