@@ -64,8 +64,11 @@ def select_children(z: np.ndarray, q: np.ndarray, temperature: float, k: int,
 
 def draft_step(W: DraftWeights, dims, st: RequestDraft, rows: List[int], f_last: np.ndarray,
                pos0: int, draft_k: np.ndarray, draft_v: np.ndarray, draft_len: int,
-               temperature: float, k: int, seed: int, request: int, round_id: int):
-    """Run the draft head on expanded nodes ``rows`` of one request."""
+               temperature: float, k: int, seed: int, request: int, round_id: int, guide=None):
+    """Run the draft head on expanded nodes ``rows`` of one request.  A
+    ``guide`` (see run_round) may substitute another implementation's child
+    choice for a row; the row's confidences are then this oracle's q at the
+    substituted tokens."""
     ex = st.ex
     feats = np.stack([f_last if e == 0 else st.f_hat[ex.parent[e]] for e in rows])
     toks = [ex.token[e] for e in rows]
@@ -89,11 +92,20 @@ def draft_step(W: DraftWeights, dims, st: RequestDraft, rows: List[int], f_last:
         st.f_hat[e], st.z[e], st.q[e] = f_hat[i], z[i], qp[i]
         st.child_tok[e], st.child_q[e] = select_children(z[i], qp[i], temperature, k, seed,
                                                          request, e, round_id)
+        if guide is not None:
+            toks = guide.children(request, e, st)
+            if toks is not None:
+                st.child_tok[e] = [int(t) for t in toks]
+                st.child_q[e] = [float(qp[i][t]) if t >= 0 else 0.0 for t in toks]
     st.layers.append(list(rows))
 
 
-def draft_tree(W, w, b: int, inp: dict) -> (RequestDraft, T.Tree):
-    """Draft phase + tree construction for request b."""
+def _follow(choice, own):
+    return own if choice is None else choice
+
+
+def draft_tree(W, w, b: int, inp: dict, guide=None) -> (RequestDraft, T.Tree):
+    """Draft phase + tree construction for request b (``guide``: see run_round)."""
     t_next = int(inp["t_next"][b])
     st = RequestDraft(T.root(t_next))
     temp = float(inp["temps"][b])
@@ -101,14 +113,20 @@ def draft_tree(W, w, b: int, inp: dict) -> (RequestDraft, T.Tree):
     L, Ld = inp["prefix_len"][b], inp["draft_len"][b]
     args = dict(f_last=inp["f_last"][b], pos0=L, draft_k=inp["draft_k"][b],
                 draft_v=inp["draft_v"][b], draft_len=Ld, temperature=temp, seed=seed,
-                request=b, round_id=rid)
+                request=b, round_id=rid, guide=guide)
     if w.tree == "eagle2":
         draft_step(W, w, st, [0], k=w.top_k, **args)
         prev = [0]
         for _ in range(1, w.depth):
-            prev = T.eagle2_frontier(st.ex, st.child_tok, st.child_q, prev, w.top_k)
+            keys = T.eagle2_frontier_keys(st.ex, st.child_tok, st.child_q, prev, w.top_k)
+            if guide is not None:
+                keys = _follow(guide.frontier(b, st, prev, keys), keys)
+            prev = T.expand_keys(st.ex, st.child_tok, st.child_q, keys, width=w.top_k)
             draft_step(W, w, st, prev, k=w.top_k, **args)
-        tr = T.eagle2_final(st.ex, st.child_tok, st.child_q, w.top_m)
+        keys = T.eagle2_final_keys(st.ex, st.child_tok, st.child_q, w.top_m)
+        if guide is not None:
+            keys = _follow(guide.final(b, st, keys), keys)
+        tr = T.tree_from_keys(st.ex, st.child_tok, st.child_q, keys)
     else:
         tpl = T.template(w.tree)
         draft_step(W, w, st, [0], k=tpl.k_max, **args)
@@ -154,13 +172,23 @@ def numpy_inputs(inp: dict) -> dict:
     return out
 
 
-def run_round(W: DraftWeights, w, inp: dict, requests: Optional[List[int]] = None) -> List[dict]:
-    """The whole round for the listed requests (all by default)."""
+def run_round(W: DraftWeights, w, inp: dict, requests: Optional[List[int]] = None,
+              guide=None) -> List[dict]:
+    """The whole round for the listed requests (all by default).
+
+    ``guide`` (test harness use) lets the round follow another
+    implementation's discrete choices: at each decision -- a row's children,
+    an EAGLE-2 frontier, the rerank, the acceptance walk -- this oracle first
+    makes its own choice, then calls guide.children(b, e, st) /
+    guide.frontier(b, st, prev, keys) / guide.final(b, st, keys) /
+    guide.accept(b, tree, result), which return the choice to continue with
+    (None or the given value keeps this oracle's own).  The arithmetic of
+    every step is unchanged; only which branch is followed."""
     if "f_last" in inp and not isinstance(inp["f_last"], np.ndarray):
         inp = numpy_inputs(inp)
     res = []
     for b in (range(w.batch) if requests is None else requests):
-        st, tr = draft_tree(W, w, b, inp)
+        st, tr = draft_tree(W, w, b, inp, guide=guide)
         S = tr.size
         L = inp["prefix_len"][b]
         tl = synthetic_target_logits(st, tr, inp["tgt_noise"][b], inp["tgt_fresh"][b])
@@ -175,6 +203,8 @@ def run_round(W: DraftWeights, w, inp: dict, requests: Optional[List[int]] = Non
             p = softmax(tl, temp)
             a, path, final = accept_sampling(tr, p, st.q, st.child_tok, b,
                                              inp["philox_seed"], inp["round_id"])
+        if guide is not None:
+            a, path, final = _follow(guide.accept(b, tr, (a, path, final)), (a, path, final))
         cm = commit(tr, path, final, L, inp["tree_k"][b], inp["tree_v"][b], inp["f_true"][b])
         cm["draft_root_k"], cm["draft_root_v"] = st.k_tree[0], st.v_tree[0]
         cm["draft_len"] = inp["draft_len"][b] + 1

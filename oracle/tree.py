@@ -3,6 +3,11 @@
 Bookkeeping used throughout (our layout; the pages fix only the rules):
   * expanded nodes -- nodes the draft head runs on -- get slots e = 0, 1, ...
     in creation order; e = 0 is the root (the already-committed token t_next);
+    an EAGLE-2 expansion layer always occupies k consecutive slots (layer l
+    at 1 + (l - 1) k .. l k): when fewer than k candidates exist (rows whose
+    distribution ran out of mass draw fewer children), the layer's last
+    slots stay inactive (token -1).  Slot numbers matter beyond bookkeeping:
+    they key the uniforms of each node's draws;
   * every expanded node e has k drawn children (e, r), r = draw rank;
   * the verified tree has slot 0 = root and slots 1..m sorted by
     (depth asc, rank in the selection order asc);
@@ -93,6 +98,17 @@ class Expanded:
     value: List[float] = dataclasses.field(default_factory=list)
     anc: List[int] = dataclasses.field(default_factory=list)     # bitmask over e
 
+    def add_inactive(self, depth) -> int:
+        """An unused slot of an expansion layer (token -1)."""
+        e = len(self.token)
+        self.token.append(-1)
+        self.parent.append(-1)
+        self.rank.append(0)
+        self.depth.append(depth)
+        self.value.append(-1.0)
+        self.anc.append(0)
+        return e
+
     def add(self, token, parent, rank, depth, value) -> int:
         e = len(self.token)
         self.token.append(int(token))
@@ -110,21 +126,44 @@ def root(t_next: int) -> Expanded:
     return ex
 
 
-def eagle2_frontier(ex: Expanded, child_tok, child_q, prev: Sequence[int], k: int) -> List[int]:
-    """Expansion step: among the children of the previous frontier, keep the top-k
-    by (value desc, parent slot asc, draw rank asc) and append them as expanded
-    nodes.  Returns the new slots in selection order."""
+def eagle2_frontier_keys(ex: Expanded, child_tok, child_q, prev: Sequence[int], k: int) -> List[Tuple[int, int]]:
+    """The expansion step's choice: among the children of the previous
+    frontier, the top-k drawn children (e, r) by (value desc, parent slot asc,
+    draw rank asc), in selection order."""
     cands = []
     for e in prev:
         for r, tok in enumerate(child_tok[e]):
             if tok < 0:
                 continue
-            cands.append((ex.value[e] * float(child_q[e][r]), e, r, tok))
+            cands.append((ex.value[e] * float(child_q[e][r]), e, r))
     cands.sort(key=lambda c: (-c[0], c[1], c[2]))
+    return [(e, r) for _, e, r in cands[:k]]
+
+
+def expand_keys(ex: Expanded, child_tok, child_q, keys: Sequence[Tuple[int, int]],
+                width: Optional[int] = None) -> List[int]:
+    """Append the drawn children ``keys`` = [(e, r)], in the given order, as
+    expanded nodes with value(child) = value(e) * c; with ``width``, pad the
+    layer with inactive slots to that many.  Returns the new active slots."""
     new = []
-    for v, e, r, tok in cands[:k]:
-        new.append(ex.add(tok, e, r, ex.depth[e] + 1, v))
+    depth = None
+    for e, r in keys:
+        v = ex.value[e] * float(child_q[e][r])
+        depth = ex.depth[e] + 1
+        new.append(ex.add(child_tok[e][r], e, r, depth, v))
+    if width is not None:
+        if depth is None:
+            depth = 1 + max(d for d, t in zip(ex.depth, ex.token) if t >= 0)
+        for _ in range(width - len(keys)):
+            ex.add_inactive(depth)
     return new
+
+
+def eagle2_frontier(ex: Expanded, child_tok, child_q, prev: Sequence[int], k: int) -> List[int]:
+    """Expansion step: among the children of the previous frontier, keep the top-k
+    by (value desc, parent slot asc, draw rank asc) and append them as expanded
+    nodes.  Returns the new slots in selection order."""
+    return expand_keys(ex, child_tok, child_q, eagle2_frontier_keys(ex, child_tok, child_q, prev, k), width=k)
 
 
 def static_frontier(ex: Expanded, child_tok, tpl: Template, depth: int, child_q=None) -> List[int]:
@@ -173,7 +212,7 @@ def _flatten(ex: Expanded, chosen: List[Tuple[int, int]], child_tok, values) -> 
     keys = [chosen[i] for i in order]
     slot_of_key = {key: 1 + j for j, key in enumerate(keys)}
     # expanded slot -> pool key it came from
-    key_of_exp = {e: (ex.parent[e], ex.rank[e]) for e in range(1, len(ex.token))}
+    key_of_exp = {e: (ex.parent[e], ex.rank[e]) for e in range(1, len(ex.token)) if ex.token[e] >= 0}
     exp_of_key = {v: e for e, v in key_of_exp.items()}
     token, parent, depth, exp_, value = [ex.token[0]], [-1], [0], [0], [1.0]
     for key in keys:
@@ -195,20 +234,34 @@ def _flatten(ex: Expanded, chosen: List[Tuple[int, int]], child_tok, values) -> 
     return Tree(token, parent, depth, exp_, anc, dict(slot_of_key), value)
 
 
+def _pool_values(ex: Expanded, child_tok, child_q) -> Dict[Tuple[int, int], float]:
+    values = {}
+    for e in range(len(ex.token)):
+        if ex.token[e] < 0:
+            continue
+        for r, tok in enumerate(child_tok[e]):
+            if tok >= 0:
+                values[(e, r)] = ex.value[e] * float(child_q[e][r])
+    return values
+
+
+def eagle2_final_keys(ex: Expanded, child_tok, child_q, m: int) -> List[Tuple[int, int]]:
+    """The rerank's choice: the top-m drawn children (e, r) of every expanded
+    node by (value desc, depth asc, parent slot asc, draw rank asc)."""
+    values = _pool_values(ex, child_tok, child_q)
+    pool = sorted(values, key=lambda key: (-values[key], ex.depth[key[0]] + 1, key[0], key[1]))
+    return pool[:m]
+
+
+def tree_from_keys(ex: Expanded, child_tok, child_q, keys: Sequence[Tuple[int, int]]) -> Tree:
+    """Flatten the retained drawn children ``keys`` (selection order)."""
+    return _flatten(ex, list(keys), child_tok, _pool_values(ex, child_tok, child_q))
+
+
 def eagle2_final(ex: Expanded, child_tok, child_q, m: int) -> Tree:
     """Rerank: top-m of every drawn child of every expanded node by
     (value desc, depth asc, parent slot asc, draw rank asc), then flatten."""
-    pool, values = [], {}
-    for e in range(len(ex.token)):
-        for r, tok in enumerate(child_tok[e]):
-            if tok < 0:
-                continue
-            v = ex.value[e] * float(child_q[e][r])
-            pool.append((v, ex.depth[e] + 1, e, r))
-            values[(e, r)] = v
-    pool.sort(key=lambda c: (-c[0], c[1], c[2], c[3]))
-    chosen = [(e, r) for _, _, e, r in pool[:m]]
-    return _flatten(ex, chosen, child_tok, values)
+    return tree_from_keys(ex, child_tok, child_q, eagle2_final_keys(ex, child_tok, child_q, m))
 
 
 def static_final(ex: Expanded, child_tok, tpl: Template) -> Tree:

@@ -69,12 +69,15 @@ def _bitlen(x: int) -> int:
     return int(x).bit_length()
 
 
-def accept_sampling(tree, p_rows, q_rows, child_tok, request, seed, round_id):
+def accept_sampling(tree, p_rows, q_rows, child_tok, request, seed, round_id, margins=None):
     """Recursive multi-candidate rejection sampling on the flattened tree.
 
     p_rows[s]: target probabilities at tree slot s; q_rows[e]: draft
     probabilities of expanded node e; child_tok[e]: drawn children in draw
-    order.  Returns (accept_len, path, final token)."""
+    order.  Returns (accept_len, path, final token).  If ``margins`` is a
+    list, each decision appends how far it was from going the other way,
+    relative: |r Q ΣP - P ΣQ 2^32| / (P ΣQ 2^32) for a test, and the distance
+    of r from the nearest CDF boundary for the final draw."""
     u, path = 0, [0]
     while True:
         P = [int(w) for w in quantize(p_rows[u])]
@@ -90,6 +93,9 @@ def accept_sampling(tree, p_rows, q_rows, child_tok, request, seed, round_id):
                 sum_qi = sum_q - sum(Wq[t] for t in taken)
                 sum_p = sum(P)
                 r = philox.uniform_u32(seed, i, u, philox.PURPOSE_ACCEPT, request, round_id)
+                if margins is not None:
+                    rhs = P[x] * sum_qi * (1 << 32)
+                    margins.append(abs(r * Wq[x] * sum_p - rhs) / rhs if rhs else float("inf"))
                 if r * Wq[x] * sum_p < P[x] * sum_qi * (1 << 32):
                     slot = tree.child_slot.get((e, i), -1)
                     if slot < 0:
@@ -106,6 +112,10 @@ def accept_sampling(tree, p_rows, q_rows, child_tok, request, seed, round_id):
         if descended:
             continue
         r = philox.uniform_u32(seed, 0, u, philox.PURPOSE_FINAL, request, round_id)
+        if margins is not None:
+            total = sum(P)
+            cum = np.cumsum(np.array(P, dtype=np.float64)) / max(total, 1)
+            margins.append(float(np.min(np.abs(cum - r / 2.0 ** 32))) if total else float("inf"))
         return len(path) - 1, path, draw_one(np.array(P, dtype=np.int64), r)
 
 
