@@ -1,20 +1,34 @@
 """GPU-vs-oracle round harness used by the parity tests and smoke().
 
 run_gpu_round: seeded inputs -> one round through libeagle's C ABI on cuda:0.
-run_oracle_round: the same inputs (copied to the host) through the CPU oracle.
-compare_round: element-wise comparison.  Discrete results (children, tree,
-accept length, path, tokens) must be identical; a mismatch is tolerated only
-as a flagged near-tie, when the oracle's own margin for that decision is
-below the floating-point tolerance (a logit gap, a sampling CDF margin, or
-for EAGLE-2 two node values -- products of draft confidences -- closer than
-the confidences' observed error can reorder), and the request's later
-comparisons are then skipped.  Floating point: features, logits and attention outputs within
-max-abs 1e-4 (fp32 workload) or 2e-2 (bf16 workloads), applied to values in
-units of the row's RMS when that exceeds 1 (random draft weights grow the
-residual stream layer by layer, to RMS ~10^2 at depth 5 of the 70B shape,
-while the bound presumes unit-scale features); probabilities within 1e-3.
+run_oracle_round: the same inputs (copied to the host) through the CPU oracle,
+following the GPU's discrete choices (GpuGuide) so that every request is
+compared through to the commit.
+compare_round: element-wise comparison of everything the round produced.
+
+Discrete decisions (children, EAGLE-2 frontier and rerank, the acceptance
+walk) are checked in two ways at every decision point:
+
+  * replay -- the oracle's own selection function, fed the GPU's fp32 inputs
+    for that decision (its logits or probabilities, its confidences and node
+    values, its target probabilities), must reproduce the GPU's choice
+    exactly.  A difference here is a failure: the two sides implement the
+    same exact integer / total-order rules;
+  * own -- the oracle's choice from its own fp64 values.  A difference is
+    allowed only as a near-tie: the oracle's margin for that decision (a
+    logit gap, a CDF distance, a node-value gap, an accept-test distance) is
+    within what the measured floating-point difference of the inputs can
+    move.  It is logged with its margin, and the oracle then continues from
+    the GPU's choice, so the request's later stages are still compared.
+
+Floating point: features, logits, draft K and attention outputs within
+max-abs 1e-4 (fp32 workload) or 2e-2 (bf16 workloads); probabilities within
+1e-3.  The report also carries each tensor's error in units of the oracle
+row's RMS, for reference.
 """
 from __future__ import annotations
+
+import copy
 
 import numpy as np
 import torch
@@ -30,11 +44,11 @@ def feature_tol(w) -> float:
     return 1e-4 if w.name.startswith("tiny") else 2e-2
 
 
-GPU_FIELDS = ["p_token", "p_parent", "p_depth", "p_value", "c_token", "c_prob", "f_hat", "logits", "probs",
-              "dk_tree", "t_token", "t_parent", "t_depth", "t_pos", "t_exp", "t_anc", "t_size", "attn_out",
-              "target_logits", "target_probs", "target_argmax", "accept_len", "path", "final_token", "last_slot",
-              "f_commit", "tok_commit", "f_last_out", "t_next_out", "prefix_len_out", "draft_len_out",
-              "draft_k", "draft_v"]
+GPU_FIELDS = ["p_token", "p_parent", "p_rank", "p_depth", "p_value", "c_token", "c_prob", "f_hat", "logits",
+              "probs", "dk_tree", "t_token", "t_parent", "t_depth", "t_pos", "t_exp", "t_anc", "t_size",
+              "t_child_slot", "attn_out", "target_logits", "target_probs", "target_argmax", "accept_len", "path",
+              "final_token", "last_slot", "f_commit", "tok_commit", "f_last_out", "t_next_out", "prefix_len_out",
+              "draft_len_out", "draft_k", "draft_v"]
 
 
 def run_gpu_round(w, seed, device="cuda", weights=None, inputs=None):
@@ -54,11 +68,8 @@ def run_gpu_round(w, seed, device="cuda", weights=None, inputs=None):
     return out
 
 
-def run_oracle_round(w, seed, inputs_cpu, weights_cpu, requests=None):
-    from oracle.layer import DraftWeights
-    from oracle.round import run_round
-    Wd = DraftWeights(weights_cpu, w)
-    return run_round(Wd, w, inputs_cpu, requests=requests)
+def _f64(t):
+    return t.to(torch.float64).numpy() if torch.is_tensor(t) else np.asarray(t, dtype=np.float64)
 
 
 def _maxerr(a, b) -> float:
@@ -67,79 +78,266 @@ def _maxerr(a, b) -> float:
     return float(np.max(np.abs(a - b))) if a.size else 0.0
 
 
-def _maxerr_scaled(a, b) -> float:
-    """max |a - b| in units of max(1, RMS of the oracle row b)."""
+def _rms(b) -> float:
     b = np.asarray(b, dtype=np.float64)
-    scale = max(1.0, float(np.sqrt(np.mean(b * b)))) if b.size else 1.0
-    return _maxerr(a, b) / scale
+    return float(np.sqrt(np.mean(b * b))) if b.size else 0.0
 
 
-def _f64(t):
-    return t.to(torch.float64).numpy() if torch.is_tensor(t) else np.asarray(t, dtype=np.float64)
+class GpuGuide:
+    """Makes the oracle round follow the GPU's discrete choices (see the
+    module docstring): replay checks, near-tie checks and logging."""
+
+    def __init__(self, w, gpu):
+        from oracle import philox
+        self.w, self.gpu, self.philox = w, gpu, philox
+        self.inp = gpu["inputs_cpu"]
+        self.temps = [float(t) for t in self.inp["temps"]]
+        self.near_ties = []      # dicts: request, stage, where, margin, bound
+        self.errors = []
+        self._st, self._tl = {}, {}   # per request: the oracle's draft state, target logits
+        # per request: expected number of sampling draws that land between the
+        # two sides' CDF boundaries (each draw's flip probability is the
+        # measure of those gaps, sum over boundaries of |C_oracle - C_gpu|)
+        self.expected_flips = {}
+
+    # -- helpers ---------------------------------------------------------------
+    def _tie(self, b, stage, where, margin, bound):
+        rec = {"request": b, "stage": stage, "where": where, "margin": float(margin), "bound": float(bound)}
+        if margin <= bound:
+            self.near_ties.append(rec)
+        else:
+            self.errors.append(f"b{b} {stage} {where}: oracle margin {margin:.3g} exceeds the fp bound "
+                               f"{bound:.3g}")
+
+    def _u(self, b, i, slot, purpose):
+        return self.philox.uniform_u32(self.inp["philox_seed"], i, slot, purpose, b, self.inp["round_id"])
+
+    def _conf_rel_err(self, b, st):
+        """Largest relative error of a GPU draft confidence against the
+        oracle's confidence of the same token."""
+        rho = 0.0
+        for e, toks in st.child_tok.items():
+            for r, t in enumerate(toks):
+                if t < 0:
+                    continue
+                want = float(st.q[e][t])
+                got = float(self.gpu["c_prob"][b, e, r])
+                if want > 0:
+                    rho = max(rho, abs(got - want) / want)
+        return rho
+
+    # -- children of one expanded node ------------------------------------------
+    def children(self, b, e, st):
+        from oracle.sampling import draw_one, greedy_top_k, quantize
+        self._st[b] = st
+        own = list(st.child_tok[e])
+        k = len(own)
+        g = [int(x) for x in self.gpu["c_token"][b, e, :k]]
+        temp = self.temps[b]
+        z_gpu = _f64(self.gpu["logits"][b, e])
+        if temp <= 0:
+            replay = greedy_top_k(z_gpu, k)
+        else:
+            from oracle.sampling import draws_without_replacement
+            u = [self._u(b, i, e, self.philox.PURPOSE_DRAW) for i in range(k)]
+            replay = draws_without_replacement(quantize(_f64(self.gpu["probs"][b, e])), u)
+        if replay != g:
+            self.errors.append(f"b{b} children e{e}: GPU {g} but its own row selects {replay}")
+            return g
+        if temp > 0:
+            wo = quantize(np.asarray(st.q[e], dtype=np.float64)).astype(np.float64)
+            wg = quantize(_f64(self.gpu["probs"][b, e])).astype(np.float64)
+            gap = float(np.abs(np.cumsum(wo) / max(wo.sum(), 1.0) - np.cumsum(wg) / max(wg.sum(), 1.0)).sum())
+            self.expected_flips[b] = self.expected_flips.get(b, 0.0) + k * gap
+        if own == g:
+            return None
+        z_or = np.asarray(st.z[e], dtype=np.float64)
+        if temp <= 0:
+            # rank by rank: the oracle's best among the tokens the GPU has not taken yet
+            taken = set()
+            for i in range(k):
+                rest = [v for v in np.lexsort((np.arange(z_or.size), -z_or)) if int(v) not in taken][0]
+                a, gt = int(rest), g[i]
+                if a != gt and gt >= 0:
+                    margin = z_or[a] - z_or[gt]
+                    bound = abs(z_gpu[a] - z_or[a]) + abs(z_gpu[gt] - z_or[gt]) + 2.0 ** -22 * abs(z_or[a])
+                    self._tie(b, "children", f"e{e} rank{i}: oracle {a} / GPU {gt}", margin, bound)
+                taken.add(gt)
+        else:
+            wq_or = quantize(np.asarray(st.q[e], dtype=np.float64))
+            wq_gpu = quantize(_f64(self.gpu["probs"][b, e]))
+            for i in range(k):
+                u = self._u(b, i, e, self.philox.PURPOSE_DRAW)
+                a, gt = draw_one(wq_or, u), g[i]
+                if a != gt:
+                    c_or = np.cumsum(wq_or.astype(np.float64)) / max(float(wq_or.sum()), 1.0)
+                    c_gpu = np.cumsum(wq_gpu.astype(np.float64)) / max(float(wq_gpu.sum()), 1.0)
+                    margin = float(np.min(np.abs(c_or - u / 2.0 ** 32)))
+                    bound = float(np.max(np.abs(c_or - c_gpu))) + 2.0 ** -32
+                    self._tie(b, "children", f"e{e} draw{i}: oracle {a} / GPU {gt}", margin, bound)
+                if gt >= 0:            # both sides continue with the GPU's draw removed
+                    wq_or[gt] = 0
+                    wq_gpu[gt] = 0
+        return g
+
+    # -- EAGLE-2 frontier and rerank ----------------------------------------------
+    def _gpu_pool(self, b, st):
+        """A copy of the oracle's expanded nodes carrying the GPU's fp64 values,
+        and the GPU's confidences per drawn child."""
+        ex_g = copy.deepcopy(st.ex)
+        n = len(ex_g.token)
+        ex_g.value = [float(x) for x in self.gpu["p_value"][b, :n]]
+        cq_g = {e: [float(x) for x in self.gpu["c_prob"][b, e, :len(toks)]] for e, toks in st.child_tok.items()}
+        return ex_g, cq_g
+
+    def _value_bound(self, b, st, v):
+        return 2.0 * self.w.depth * (self._conf_rel_err(b, st) + 2.0 ** -23) * v
+
+    def frontier(self, b, st, prev, own):
+        from oracle import tree as T
+        n0 = len(st.ex.token)
+        cnt = sum(1 for t in self.gpu["p_token"][b, n0:n0 + self.w.top_k] if int(t) >= 0)
+        g = [(int(self.gpu["p_parent"][b, n0 + i]), int(self.gpu["p_rank"][b, n0 + i])) for i in range(cnt)]
+        ex_g, cq_g = self._gpu_pool(b, st)
+        replay = T.eagle2_frontier_keys(ex_g, st.child_tok, cq_g, prev, self.w.top_k)
+        if replay != g:
+            self.errors.append(f"b{b} frontier at e{n0}: GPU {g} but its own values select {replay}")
+            return g
+        vals = [ex_g.value[e] * cq_g[e][r] for e, r in g]
+        got = [float(x) for x in self.gpu["p_value"][b, n0:n0 + cnt]]
+        if vals != got:
+            self.errors.append(f"b{b} frontier values at e{n0}: GPU {got} vs its own products {vals}")
+        if own != g:
+            v = lambda key: st.ex.value[key[0]] * float(st.child_q[key[0]][key[1]])
+            i = next((j for j in range(min(len(own), len(g))) if own[j] != g[j]), None)
+            if i is None:
+                self.errors.append(f"b{b} frontier at e{n0}: {len(g)} GPU nodes vs {len(own)} oracle nodes")
+            else:
+                margin = abs(v(own[i]) - v(g[i]))
+                self._tie(b, "frontier", f"e{n0 + i}: oracle {own[i]} / GPU {g[i]}", margin,
+                          self._value_bound(b, st, max(v(own[i]), v(g[i]))))
+        return g
+
+    def final(self, b, st, own):
+        from oracle import tree as T
+        ex_g, cq_g = self._gpu_pool(b, st)
+        replay = T.eagle2_final_keys(ex_g, st.child_tok, cq_g, self.w.top_m)
+        cs = self.gpu["t_child_slot"][b]
+        g_set = {(e, r) for e in range(cs.shape[0]) for r in range(cs.shape[1]) if int(cs[e, r]) >= 1}
+        if set(replay) != g_set:
+            self.errors.append(f"b{b} rerank: GPU kept {sorted(g_set)} but its own values keep {sorted(replay)}")
+        if own != replay:
+            v = lambda key: st.ex.value[key[0]] * float(st.child_q[key[0]][key[1]])
+            i = next((j for j in range(min(len(own), len(replay))) if own[j] != replay[j]), None)
+            if i is None:
+                self.errors.append(f"b{b} rerank: {len(replay)} GPU nodes vs {len(own)} oracle nodes")
+            else:
+                margin = abs(v(own[i]) - v(replay[i]))
+                self._tie(b, "rerank", f"rank{i}: oracle {own[i]} / GPU {replay[i]}", margin,
+                          self._value_bound(b, st, max(v(own[i]), v(replay[i]))))
+        return replay
+
+    # -- acceptance ---------------------------------------------------------------
+    def accept(self, b, tr, own):
+        from oracle import verify as Vf
+        from oracle.layer import softmax
+        from oracle.round import synthetic_target_logits
+        st = self._st[b]
+        self._tl[b] = synthetic_target_logits(st, tr, np.asarray(self.inp["tgt_noise"][b], dtype=np.float64),
+                                              np.asarray(self.inp["tgt_fresh"][b], dtype=np.float64))
+        a = int(self.gpu["accept_len"][b])
+        g = (a, [int(x) for x in self.gpu["path"][b, :a + 1]], int(self.gpu["final_token"][b]))
+        temp = self.temps[b]
+        size = tr.size
+        seed, rid = self.inp["philox_seed"], self.inp["round_id"]
+        if temp <= 0:
+            tl_gpu = _f64(self.gpu["target_logits"][b, :size])
+            replay = Vf.accept_greedy(tr, tl_gpu)
+        else:
+            replay = Vf.accept_sampling(tr, _f64(self.gpu["target_probs"][b, :size]), _f64(self.gpu["probs"][b]),
+                                        st.child_tok, b, seed, rid)
+        replay = (replay[0], list(replay[1]), int(replay[2]))
+        if replay != g:
+            self.errors.append(f"b{b} accept: GPU {g} but its own inputs walk {replay}")
+            return g
+        own = (own[0], list(own[1]), int(own[2]))
+        if own == g:
+            return None
+        tl_or = self._tl[b]
+        if temp <= 0:
+            # first node where the two walks part: the oracle's argmax there vs the GPU's
+            c = 1
+            while c < min(len(own[1]), len(g[1])) and own[1][c] == g[1][c]:
+                c += 1
+            node = g[1][c - 1]
+            z = np.asarray(tl_or[node], dtype=np.float64)
+            tl_gpu = _f64(self.gpu["target_logits"][b, node])
+            oa, ga = int(np.argmax(z)), int(np.argmax(tl_gpu))
+            if oa == ga:
+                self.errors.append(f"b{b} accept: walks part at slot {node} although both argmaxes are {oa}")
+            else:
+                margin = z[oa] - z[ga]
+                bound = abs(tl_gpu[oa] - z[oa]) + abs(tl_gpu[ga] - z[ga]) + 2.0 ** -22 * abs(z[oa])
+                self._tie(b, "accept", f"slot {node}: oracle argmax {oa} / GPU {ga}", margin, bound)
+        else:
+            margins = []
+            p_or = softmax(tl_or, temp)
+            Vf.accept_sampling(tr, p_or, st.q, st.child_tok, b, seed, rid, margins=margins)
+            # relative discrepancy of the probabilities the walk used
+            p_gpu = _f64(self.gpu["target_probs"][b, :size])
+            q_gpu = _f64(self.gpu["probs"][b])
+            rel = 0.0
+            for s_ in range(size):
+                m = p_or[s_] > 1e-12
+                rel = max(rel, float(np.max(np.abs(p_gpu[s_][m] - p_or[s_][m]) / p_or[s_][m])))
+            for e in st.q:
+                qo = np.asarray(st.q[e], dtype=np.float64)
+                m = qo > 1e-12
+                rel = max(rel, float(np.max(np.abs(q_gpu[e][m] - qo[m]) / qo[m])))
+            self._tie(b, "accept", f"oracle {own} / GPU {g}", min(margins) if margins else float("inf"),
+                      4.0 * rel + 2.0 ** -30)
+        return g
 
 
-def _conf_rel_err(gpu, b, st):
-    """Largest relative error of a GPU draft confidence against the oracle's."""
-    rho = 0.0
-    for e in range(len(st.ex.token)):
-        k = len(st.child_tok[e])
-        want = np.asarray(st.child_q[e], dtype=np.float64)
-        got = np.asarray(gpu["c_prob"][b, e, :k], dtype=np.float64)
-        ok = want > 0
-        if ok.any():
-            rho = max(rho, float(np.max(np.abs(got[ok] - want[ok]) / want[ok])))
-    return rho
-
-
-def _value_tie(gpu, b, st, e_par, tok, v_ref, depth):
-    """EAGLE-2 value near-tie: the GPU kept (child `tok` of expanded node
-    `e_par`) where the oracle kept a node of value v_ref.  Values are products
-    of at most `depth` draft confidences, so two values closer than twice
-    depth x (the confidences' observed relative error + fp32 rounding) may
-    order either way.  Returns a description, or None."""
-    ex = st.ex
-    if not 0 <= e_par < len(ex.token):
-        return None
-    ranks = [r for r, t in enumerate(st.child_tok[e_par]) if t == tok]
-    if not ranks:
-        return None
-    v_gpu = ex.value[e_par] * float(st.child_q[e_par][ranks[0]])
-    bound = 2.0 * depth * (_conf_rel_err(gpu, b, st) + 2.0 ** -23) * max(v_gpu, v_ref)
-    gap = abs(v_gpu - v_ref)
-    if gap <= bound:
-        return f"values {v_ref:.9g} vs {v_gpu:.9g} (gap {gap:.2e} <= {bound:.2e})"
-    return None
-
-
-def _rerank_near_tie(gpu, b, st, tr, depth):
-    """The final trees first differ at a slot whose two candidates are an
-    EAGLE-2 value near-tie (see _value_tie)."""
-    size = tr.size
-    g_tok = [int(x) for x in gpu["t_token"][b, :size]]
-    g_par = [int(x) for x in gpu["t_parent"][b, :size]]
-    s = next((j for j in range(size) if (g_tok[j], g_par[j]) != (tr.token[j], tr.parent[j])), None)
-    if s is None or s == 0:
-        return None
-    p = g_par[s]
-    if not 0 <= p < s or tr.exp[p] < 0:
-        return None
-    tie = _value_tie(gpu, b, st, tr.exp[p], g_tok[s], tr.value[s], depth)
-    return None if tie is None else f"slot {s}: {tie}"
+def run_oracle_round(w, seed, inputs_cpu, weights_cpu, requests=None, gpu=None):
+    """The oracle's round for the listed requests.  With ``gpu`` (a
+    run_gpu_round result) it follows the GPU's discrete choices through a
+    GpuGuide, kept in every result dict under 'guide'."""
+    from oracle.layer import DraftWeights
+    from oracle.round import run_round
+    Wd = DraftWeights(weights_cpu, w)
+    if gpu is None:
+        return run_round(Wd, w, inputs_cpu, requests=requests)
+    guide = GpuGuide(w, gpu)
+    res = run_round(Wd, w, inputs_cpu, requests=requests, guide=guide)
+    for r in res:
+        r["guide"] = guide
+    return res
 
 
 def compare_round(w, gpu, ref, requests=None):
-    """Returns a report dict; report['ok'] is False on any non-near-tie mismatch."""
-    from oracle import philox
-    from oracle.sampling import quantize
+    """Returns a report: 'ok' is False on any failure; 'reached' gives, per
+    compared request, the last stage compared ('commit' when complete);
+    'near_ties' lists the logged near-ties; 'max_err' the plain max-abs error
+    per tensor and 'max_err_rms' the same in units of the oracle row's RMS."""
     tol = feature_tol(w)
     reqs = list(range(w.batch)) if requests is None else list(requests)
-    rep = {"ok": True, "near_ties": [], "errors": [], "max_err": {}}
+    guide = ref[0].get("guide") if ref else None
+    rep = {"ok": True, "near_ties": list(guide.near_ties) if guide else [], "errors": [],
+           "max_err": {}, "max_err_rms": {}, "reached": {}, "f_hat_by_depth": {},
+           "expected_flips": dict(guide.expected_flips) if guide else {}}
+    if guide is not None and guide.errors:
+        rep["ok"] = False
+        rep["errors"].extend(guide.errors)
 
-    def err(name, val, lim):
-        rep["max_err"][name] = max(rep["max_err"].get(name, 0.0), val)
-        if not val <= lim:
+    def err(name, got, want, lim):
+        e = _maxerr(got, want)
+        rep["max_err"][name] = max(rep["max_err"].get(name, 0.0), e)
+        scale = max(1.0, _rms(want))
+        rep["max_err_rms"][name] = max(rep["max_err_rms"].get(name, 0.0), e / scale)
+        if not e <= lim:
             rep["ok"] = False
-            rep["errors"].append(f"{name}: {val:.3g} > {lim:g}")
+            rep["errors"].append(f"{name}: {e:.3g} > {lim:g}")
 
     def fail(msg):
         rep["ok"] = False
@@ -153,111 +351,87 @@ def compare_round(w, gpu, ref, requests=None):
         st, tr = r["draft"], r["tree"]
         ex = st.ex
         temp = float(inp["temps"][b])
-        diverged = False
+        reached = "draft"
         # draft head outputs, per expanded node in creation order
-        for e in range(len(ex.token)):
-            if int(gpu["p_token"][b, e]) != ex.token[e] or int(gpu["p_parent"][b, e]) != ex.parent[e]:
-                tie = None
-                if e > 0 and w.tree == "eagle2":
-                    tie = _value_tie(gpu, b, st, int(gpu["p_parent"][b, e]), int(gpu["p_token"][b, e]),
-                                     ex.value[e], w.depth)
-                if tie is not None:
-                    rep["near_ties"].append(f"b{b} frontier e{e}: {tie}")
-                else:
-                    fail(f"b{b} pool token e{e}: {int(gpu['p_token'][b, e])} vs {ex.token[e]}")
-                diverged = True
-                break
-            err("f_hat", _maxerr_scaled(gpu["f_hat"][b, e], st.f_hat[e]), tol)
-            err("logits", _maxerr_scaled(gpu["logits"][b, e], st.z[e]), tol)
-            err("probs", _maxerr(gpu["probs"][b, e], st.q[e]), TOL_PROB)
-            err("draft_k", _maxerr(gpu["dk_tree"][b, e], st.k_tree[e]), tol)
+        n = len(ex.token)
+        pool_ok = ([int(x) for x in gpu["p_token"][b, :n]] == ex.token and
+                   [int(x) for x in gpu["p_parent"][b, :n]] == ex.parent and
+                   [int(x) for x in gpu["p_depth"][b, :n]] == ex.depth)
+        if not pool_ok:
+            fail(f"b{b} pool differs from the followed oracle pool")
+        for e in range(n):
+            if ex.token[e] < 0:           # an unused slot of a short expansion layer
+                continue
+            err("f_hat", gpu["f_hat"][b, e], st.f_hat[e], tol)
+            dd = rep["f_hat_by_depth"].setdefault(ex.depth[e], [0.0, 0.0])
+            dd[0] = max(dd[0], _maxerr(gpu["f_hat"][b, e], st.f_hat[e]))
+            dd[1] = max(dd[1], _rms(st.f_hat[e]))
+            err("logits", gpu["logits"][b, e], st.z[e], tol)
+            err("probs", gpu["probs"][b, e], st.q[e], TOL_PROB)
+            err("draft_k", gpu["dk_tree"][b, e], st.k_tree[e], tol)
             k = len(st.child_tok[e])
-            g_ch = [int(x) for x in gpu["c_token"][b, e, :k]]
-            if g_ch != list(st.child_tok[e]):
-                rank = next(j for j in range(k) if g_ch[j] != st.child_tok[e][j])
-                a_tok, g_tok = st.child_tok[e][rank], g_ch[rank]
-                if temp <= 0:
-                    # two logits closer than twice the row's measured logit error
-                    # (plus fp32 rounding of the logits themselves) may order either way
-                    margin = abs(st.z[e][a_tok] - st.z[e][g_tok]) if g_tok >= 0 else np.inf
-                    dz = _maxerr(gpu["logits"][b, e], st.z[e])
-                    near = margin <= 2.0 * dz + 2.0 ** -22 * abs(st.z[e][a_tok])
-                else:
-                    u = philox.uniform_u32(inp["philox_seed"], rank, e, philox.PURPOSE_DRAW, b, inp["round_id"])
-                    wq = quantize(st.q[e]).astype(np.float64)
-                    for t in st.child_tok[e][:rank]:
-                        wq[t] = 0.0
-                    cdf = np.cumsum(wq) / wq.sum()
-                    margin = float(np.min(np.abs(cdf - u / 2.0 ** 32)))
-                    # q = softmax(z / T): a logit error dz moves every CDF point by at
-                    # most 2 max|dz| / T (relative to the remaining mass)
-                    dz = _maxerr(gpu["logits"][b, e], st.z[e])
-                    rem = wq.sum() / max(1.0, float(quantize(st.q[e]).sum()))
-                    near = margin < 2.0 * dz / temp / max(rem, 1e-12) + 1e-6
-                if near:
-                    rep["near_ties"].append(f"b{b} children e{e} rank{rank} margin {margin:.2e}")
-                    diverged = True
-                    break
-                fail(f"b{b} children of e{e}: {g_ch} vs {list(st.child_tok[e])}")
-                diverged = True
-                break
-            err("child_prob", _maxerr(gpu["c_prob"][b, e, :k], st.child_q[e]), TOL_PROB)
-        if diverged:
-            continue
+            if [int(x) for x in gpu["c_token"][b, e, :k]] != list(st.child_tok[e]):
+                fail(f"b{b} children of e{e} differ from the followed oracle children")
+            err("child_prob", gpu["c_prob"][b, e, :k], st.child_q[e], TOL_PROB)
         # tree
         size = tr.size
         if int(gpu["t_size"][b]) != size:
             fail(f"b{b} tree size {int(gpu['t_size'][b])} vs {size}")
+            rep["reached"][b] = reached
             continue
-        tie = _rerank_near_tie(gpu, b, st, tr, w.depth)
-        if tie is not None:
-            rep["near_ties"].append(f"b{b} rerank {tie}")
-            continue
+        reached = "tree"
+        tree_ok = True
         for name, mine, want in (("token", gpu["t_token"], tr.token), ("parent", gpu["t_parent"], tr.parent),
                                  ("depth", gpu["t_depth"], tr.depth), ("exp", gpu["t_exp"], tr.exp)):
             got = [int(x) for x in mine[b, :size]]
             if got != list(want):
                 fail(f"b{b} tree {name}: {got} vs {list(want)}")
-                diverged = True
+                tree_ok = False
         anc = [int(x) & 0xFFFFFFFFFFFFFFFF for x in gpu["t_anc"][b, :size]]
         if anc != list(tr.anc):
             fail(f"b{b} tree anc differs")
-            diverged = True
+            tree_ok = False
         pos = [int(x) for x in gpu["t_pos"][b, :size]]
         if pos != [inp["prefix_len"][b] + dd for dd in tr.depth]:
             fail(f"b{b} tree pos differs")
-        if diverged:
+        if not tree_ok:
+            rep["reached"][b] = reached
             continue
         # verification attention, target distribution
-        err("verify_out", _maxerr(gpu["attn_out"][b, :size], r["verify_out"]), tol)
+        reached = "verify"
+        err("verify_out", gpu["attn_out"][b, :size], r["verify_out"], tol)
         for s_ in range(size):
-            err("target_logits", _maxerr_scaled(gpu["target_logits"][b, s_], r["target_logits"][s_]), tol)
+            err("target_logits", gpu["target_logits"][b, s_], r["target_logits"][s_], tol)
         if temp > 0:
-            err("target_probs", _maxerr(gpu["target_probs"][b, :size], r["target_probs"]), TOL_PROB)
+            err("target_probs", gpu["target_probs"][b, :size], r["target_probs"], TOL_PROB)
         # acceptance
+        reached = "accept"
         a = int(gpu["accept_len"][b])
         path = [int(x) for x in gpu["path"][b, :a + 1]]
         final = int(gpu["final_token"][b])
         if (a, path, final) != (r["accept_len"], list(r["path"]), r["final"]):
             fail(f"b{b} accept: gpu ({a}, {path}, {final}) vs oracle ({r['accept_len']}, {r['path']}, {r['final']})")
+            rep["reached"][b] = reached
             continue
+        if int(gpu["last_slot"][b]) != path[-1]:
+            fail(f"b{b} last slot {int(gpu['last_slot'][b])} vs {path[-1]}")
         # commit
         cm = r["commit"]
         toks = [int(x) for x in gpu["tok_commit"][b, :a + 2]]
         if toks != cm["tok_commit"]:
             fail(f"b{b} tok_commit {toks} vs {cm['tok_commit']}")
-        err("f_commit", _maxerr(gpu["f_commit"][b, :a + 1], cm["f_commit"]), 0.0)
-        err("f_last", _maxerr(gpu["f_last_out"][b], cm["f_last"]), 0.0)
+        err("f_commit", gpu["f_commit"][b, :a + 1], cm["f_commit"], 0.0)
+        err("f_last", gpu["f_last_out"][b], cm["f_last"], 0.0)
         if int(gpu["t_next_out"][b]) != cm["t_next"] or int(gpu["prefix_len_out"][b]) != cm["prefix_len"]:
             fail(f"b{b} next-round state differs")
         if int(gpu["draft_len_out"][b]) != cm["draft_len"]:
             fail(f"b{b} draft_len differs")
         L = inp["prefix_len"][b]
-        got_kv = _f64(gpu["tgt_k_after"][b, L:L + a + 1])
-        err("kv_commit", _maxerr(got_kv, cm["kv_rows_k"]), 0.0)
+        err("kv_commit", _f64(gpu["tgt_k_after"][b, L:L + a + 1]), cm["kv_rows_k"], 0.0)
         Ld = inp["draft_len"][b]
         root_k = np.asarray(cm["draft_root_k"])
         # the cache is bf16: the appended row carries one bf16 rounding (2^-9 relative)
-        err("draft_kv_append", _maxerr(_f64(gpu["draft_k"][b, Ld]), root_k),
+        err("draft_kv_append", _f64(gpu["draft_k"][b, Ld]), root_k,
             tol + 2.0 ** -8 * float(np.max(np.abs(root_k))))
+        rep["reached"][b] = "commit"
     return rep

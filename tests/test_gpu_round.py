@@ -31,21 +31,39 @@ SMALL = {
 }
 
 
+def _check(w, rep, reqs):
+    """Every compared request reaches the commit.  Near-ties are logged with
+    their margins; each one is within the measured floating-point difference
+    of its inputs (else compare_round fails).  Sampling draws: their count
+    per request stays within what the measured CDF differences predict (the
+    expected count is the sum over draws of the gaps between the two sides'
+    CDF boundaries); every other kind of decision: at most one per request.
+    The report is printed so the log carries every tensor's plain max-abs
+    error."""
+    print(w.name, json.dumps({k: rep[k] for k in ("max_err", "max_err_rms", "f_hat_by_depth", "near_ties",
+                                                   "expected_flips")}))
+    if not rep["ok"]:
+        pytest.fail(json.dumps({k: v for k, v in rep.items() if k != "ok"}, indent=1, default=str))
+    assert rep["reached"] == {b: "commit" for b in reqs}, rep["reached"]
+    draws, other = {}, {}
+    for t in rep["near_ties"]:
+        kind = draws if (t["stage"] == "children" and " draw" in t["where"]) else other
+        kind[t["request"]] = kind.get(t["request"], 0) + 1
+    assert all(n <= 1 for n in other.values()), rep["near_ties"]
+    for b, n in draws.items():
+        mu = rep["expected_flips"].get(b, 0.0)
+        assert n <= 2 + 3 * mu + 4 * mu ** 0.5, (b, n, mu, rep["near_ties"])
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", list(SMALL))
 def test_round_parity_small(name):
     w = SMALL[name]
     seed = 77
     gpu = run_gpu_round(w, seed)
-    ref = run_oracle_round(w, seed, gpu["inputs_cpu"], gpu["weights_cpu"])
+    ref = run_oracle_round(w, seed, gpu["inputs_cpu"], gpu["weights_cpu"], gpu=gpu)
     rep = compare_round(w, gpu, ref)
-    if not rep["ok"]:
-        pytest.fail(json.dumps(rep, indent=1))
-    # A decision between two candidates closer than the measured fp32 error
-    # (two logits 2.8e-8 apart in small_eagle2_ragged_k10; two EAGLE-2 node
-    # values 2.4e-6 apart relative in small_rows160_two_mma) is flagged and
-    # skips only that request's later stages; at most one request in eight.
-    assert len(rep["near_ties"]) <= max(1, w.batch // 8), rep
+    _check(w, rep, list(range(w.batch)))
 
 
 FULL = {"7b_static26": None, "7b_eagle2": None, "13b_x8_eagle2": [0, 3, 7], "70b_x16_eagle2": [0, 1]}
@@ -60,16 +78,9 @@ def test_round_parity_full_size(name):
     seed = S.WORKLOAD_SEEDS[name]
     gpu = run_gpu_round(w, seed)
     reqs = FULL[name]
-    ref = run_oracle_round(w, seed, gpu["inputs_cpu"], gpu["weights_cpu"], requests=reqs)
+    ref = run_oracle_round(w, seed, gpu["inputs_cpu"], gpu["weights_cpu"], requests=reqs, gpu=gpu)
     rep = compare_round(w, gpu, ref, requests=reqs)
-    if not rep["ok"]:
-        pytest.fail(json.dumps(rep, indent=1))
-    # sampling at T > 0 over V = 32000 nearly flat draft distributions: a draw can
-    # land within the fp32-vs-fp64 CDF difference of a boundary; such draws are
-    # flagged (not failed) and the request's later stages are compared only
-    # when no flag was raised.  Greedy requests must never flag a child choice.
-    greedy = [b for b in (reqs or range(w.batch)) if w.temps_for_batch()[b] <= 0]
-    assert not any(f"b{b} children " in t for t in rep["near_ties"] for b in greedy), rep
+    _check(w, rep, list(range(w.batch)) if reqs is None else reqs)
 
 
 @pytest.mark.gpu
