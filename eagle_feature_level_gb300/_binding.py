@@ -144,10 +144,12 @@ def _declare(L):
                                     C.POINTER(eagle_children), P, P, P, C.POINTER(eagle_sampling),
                                     C.POINTER(eagle_accept_out), P, P],
         "eagle_commit": [P, I, C.POINTER(eagle_accept_out), C.POINTER(eagle_tree), P, I, P, P, P, P, I, P,
-                         C.POINTER(eagle_draft_out), C.POINTER(eagle_kv), C.POINTER(eagle_commit_out), P],
+                         C.POINTER(eagle_draft_out), C.POINTER(eagle_kv), C.POINTER(eagle_commit_out), P, P],
         "eagle_trace_enable": [P, I, I],
         "eagle_trace_read": [P, C.POINTER(C.c_float), C.POINTER(I), I, C.POINTER(I)],
         "eagle_trace_disable": [P],
+        "eagle_stamps_enable": [P, P, I],
+        "eagle_stamps_disable": [P, C.POINTER(I), I, C.POINTER(I)],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -164,7 +166,7 @@ EXPORTED = ["eagle_create", "eagle_destroy", "eagle_workspace_init", "eagle_read
             "eagle_tree_expand_rerank", "eagle_tree_verify_attn", "eagle_tree_verify_attn_noalloc",
             "eagle_accept", "eagle_accept_from_probs",
             "eagle_commit", "eagle_trace_enable", "eagle_trace_read", "eagle_trace_disable",
-            "eagle_launch_count"]
+            "eagle_stamps_enable", "eagle_stamps_disable", "eagle_launch_count"]
 
 
 def _check(name: str, code: int):
@@ -259,14 +261,14 @@ def eagle_accept_from_probs(ctx, plan, batch, tree, children, target_probs, targ
 
 
 def eagle_commit(ctx, batch, acc, tree, f_true, k_tree_layers, v_tree_layers, k_cache_layers, v_cache_layers,
-                 kv_cap, target_kv_len, draft, draft_kv, out, stream):
+                 kv_cap, target_kv_len, draft, draft_kv, out, ws_ptr, stream):
     n = len(k_tree_layers)
     arr = lambda xs: (P * max(n, 1))(*xs)
     _check("eagle_commit",
            lib().eagle_commit(ctx, batch, C.byref(acc), C.byref(tree), f_true, n, C.cast(arr(k_tree_layers), P),
                               C.cast(arr(v_tree_layers), P), C.cast(arr(k_cache_layers), P),
                               C.cast(arr(v_cache_layers), P), kv_cap, target_kv_len, _ref(draft), _ref(draft_kv),
-                              C.byref(out), stream))
+                              C.byref(out), ws_ptr, stream))
 
 
 def eagle_trace_enable(ctx, kernel: str, capacity: int):
@@ -285,6 +287,19 @@ def eagle_trace_read(ctx, cap: int):
 
 def eagle_trace_disable(ctx):
     _check("eagle_trace_disable", lib().eagle_trace_disable(ctx))
+
+
+def eagle_stamps_enable(ctx, stamps_ptr: int, capacity: int):
+    _check("eagle_stamps_enable", lib().eagle_stamps_enable(ctx, stamps_ptr, capacity))
+
+
+def eagle_stamps_disable(ctx, cap: int = 4096):
+    """Kernel class names of the stamped launches, in launch order."""
+    ids = (I * cap)()
+    n = I()
+    _check("eagle_stamps_disable", lib().eagle_stamps_disable(ctx, ids, cap, C.byref(n)))
+    names = {v: k for k, v in KERNEL_ID.items()}
+    return [names.get(ids[i], str(ids[i])) for i in range(min(n.value, cap))]
 
 
 def eagle_launch_count(ctx) -> int:

@@ -29,8 +29,10 @@ __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
 __global__ void __launch_bounds__(SM_THREADS)
     target_softmax_kernel(const float* __restrict__ logits, const float* __restrict__ temperature,
                           const int32_t* __restrict__ tree_size, int S, int V, float* __restrict__ probs,
-                          int32_t* __restrict__ argmax, int* status) {
+                          int32_t* __restrict__ argmax, int* status, uint64_t* stamp) {
+  const LaunchStamp lstamp(stamp);
   pdl_wait();      // predecessor outputs visible from here on
+  lstamp.waited();
   pdl_trigger();
   __shared__ float red_f[32];
   __shared__ int red_i[32];
@@ -60,7 +62,7 @@ __global__ void __launch_bounds__(SM_THREADS)
   }
   __syncthreads();
   const float m = red_f[0];
-  if (tid == 0) argmax[row] = red_i[0];
+  if (tid == 0) argmax[row] = red_i[0] == INT32_MAX ? -1 : red_i[0];   // -1: no finite logit
   const float T = temperature[b];
   if (!(T > 0.f)) return;
   const float inv_t = 1.0f / T;
@@ -101,10 +103,13 @@ struct WalkParams {
   int32_t* final_token;
   int32_t* last_slot;
   int* status;
+  uint64_t* stamp;
 };
 
 __global__ void __launch_bounds__(SM_THREADS) accept_walk_kernel(const WalkParams p) {
+  const LaunchStamp ls(p.stamp);
   pdl_wait();      // predecessor outputs visible from here on
+  ls.waited();
   pdl_trigger();
   __shared__ uint64_t red_u[32];
   __shared__ int red_i[32];
@@ -119,7 +124,7 @@ __global__ void __launch_bounds__(SM_THREADS) accept_walk_kernel(const WalkParam
 
   if (!(T > 0.f)) {  // greedy walk, over the tree staged in shared memory
     __shared__ int s_par[EAGLE_MAX_NODES], s_tok[EAGLE_MAX_NODES], s_am[EAGLE_MAX_NODES];
-    const int size = min(p.t_size[b], EAGLE_MAX_NODES);
+    const int size = min(p.t_size[b], min(p.S, EAGLE_MAX_NODES));
     for (int c = tid; c < size; c += blockDim.x) {
       s_par[c] = p.t_parent[tb + c];
       s_tok[c] = p.t_token[tb + c];
@@ -162,7 +167,11 @@ __global__ void __launch_bounds__(SM_THREADS) accept_walk_kernel(const WalkParam
       ls += w;
     }
     uint64_t SP = block_sum_u64(ls, red_u);
-    const int e = p.t_exp[tb + u];
+    int e = p.t_exp[tb + u];
+    if (e >= p.E) {                   // not an expanded slot of this layout
+      if (tid == 0) set_status(p.status, EAGLE_ERR_INVALID_TREE);
+      e = -1;
+    }
     bool descended = false;
     if (e >= 0) {
       const float* qe = p.q + (static_cast<size_t>(b) * p.E + e) * p.V;
@@ -174,6 +183,10 @@ __global__ void __launch_bounds__(SM_THREADS) accept_walk_kernel(const WalkParam
       for (int i = 0; i < p.k; ++i) {
         const int x = p.ctok[(static_cast<size_t>(b) * p.E + e) * p.K + i];
         if (x < 0) break;
+        if (x >= p.V) {                 // not a token: the node's candidates end here
+          if (tid == 0) set_status(p.status, EAGLE_ERR_INVALID_ARG);
+          break;
+        }
         const uint64_t SQi = SQ - taken_w;
         __syncthreads();
         if (x >= v0 && x < v1) s_px = P[x];
@@ -188,7 +201,11 @@ __global__ void __launch_bounds__(SM_THREADS) accept_walk_kernel(const WalkParam
         }
         __syncthreads();
         if (s_flag) {
-          const int slot = s_u;
+          int slot = s_u;
+          if (slot >= p.S) {            // outside the tree: treated as pruned
+            if (tid == 0) set_status(p.status, EAGLE_ERR_INVALID_TREE);
+            slot = -1;
+          }
           if (slot >= 0 && a + 1 < p.path_cap) {
             u = slot;
             ++a;
@@ -286,10 +303,11 @@ cudaError_t launch_target_softmax(eagle_ctx* ctx, int batch, const eagle_tree* t
                                   const float* temperature, float* probs, int32_t* argmax, void* ws,
                                   cudaStream_t st) {
   dim3 grid(tree->stride, batch);
+  uint64_t* stamp = stamp_slot(ctx, EAGLE_K_ACCEPT);
   trace_before(ctx, EAGLE_K_ACCEPT, st);
   const cudaError_t e = launch_pdl(target_softmax_kernel, grid, dim3(SM_THREADS), 0, st, logits, temperature,
                                    tree->size, tree->stride, ctx->dims.vocab, probs, argmax,
-                                   ws_ptr<int>(ws, ctx->ws.status));
+                                   ws_ptr<int>(ws, ctx->ws.status), stamp);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_ACCEPT, st);
   return e;
@@ -324,6 +342,7 @@ cudaError_t launch_accept_walk(eagle_ctx* ctx, const eagle_plan* plan, int batch
   p.final_token = out->final_token;
   p.last_slot = out->last_slot;
   p.status = ws_ptr<int>(ws, ctx->ws.status);
+  p.stamp = stamp_slot(ctx, EAGLE_K_ACCEPT);
   trace_before(ctx, EAGLE_K_ACCEPT, st);
   const cudaError_t e = launch_pdl(accept_walk_kernel, dim3(batch), dim3(SM_THREADS), 0, st, p);
   ctx->launches++;

@@ -3,6 +3,9 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <mutex>
+#include <set>
+#include <tuple>
 
 #include "internal.h"
 
@@ -62,7 +65,7 @@ eagle_status check_plan(const eagle_ctx* c, const eagle_plan* p) {
   return EAGLE_OK;
 }
 
-int splits_bound(const eagle_ctx* c, int pairs) { return attn_splits_bound(c, pairs); }
+int splits_bound(const eagle_ctx* c, int pairs) { return attn_splits_bound(c, pairs, c->lim.max_prefix); }
 
 void layout(eagle_ctx* c) {
   const eagle_dims& D = c->dims;
@@ -99,12 +102,17 @@ void layout(eagle_ctx* c) {
   // split-tile partial slots t + cta: t < max_mtiles, cta < grid <= 2 * SMs
   W.gemm_part = take(static_cast<size_t>(W.max_mtiles + 2 * c->sm_count) * L.max_rows * 128 * 4);
   W.gemm_cnt = take(static_cast<size_t>(6) * W.max_mtiles * 4);
+  // partial records of the widest attention launch: b requests use
+  // splits_bound(b * Hkv) + 1 records per query row; past the batch where
+  // the splits reach 1 the count grows as 2b, so the largest batch covers
+  // every batch beyond the scanned ones
   size_t records = 0;
-  for (int b = 1; b <= L.max_batch; ++b) {
+  const int scan = std::min(L.max_batch, 4096);
+  for (int i = 0; i <= scan; ++i) {
+    const int b = i < scan ? i + 1 : L.max_batch;
     const size_t s1 = static_cast<size_t>(splits_bound(c, b * D.n_kv_heads) + 1);
     records = std::max(records, static_cast<size_t>(L.max_rows) * D.n_q_heads * s1);
     records = std::max(records, static_cast<size_t>(b) * L.max_tree * D.n_q_heads * s1);
-    if (b > 4096) break;   // the bound stops growing once splits reach 1
   }
   W.attn_part = take(records * (D.head_dim + 4) * 4);
   W.attn_cnt = take(static_cast<size_t>(2) * L.max_batch * D.n_kv_heads * 4);
@@ -158,7 +166,8 @@ eagle_status check_kv(const eagle_ctx* c, const eagle_kv* kv) {
   EAGLE_REQUIRE(kv, EAGLE_ERR_INVALID_ARG);
   EAGLE_PTR(kv->k); EAGLE_PTR(kv->v); EAGLE_PTR(kv->len);
   EAGLE_REQUIRE(kv->cap >= 1, EAGLE_ERR_SHAPE);
-  (void)c;
+  // the workspace's attention records are sized for caches up to max_prefix
+  EAGLE_REQUIRE(kv->cap <= c->lim.max_prefix, EAGLE_ERR_CAPACITY);
   return EAGLE_OK;
 }
 
@@ -171,6 +180,56 @@ eagle_status check_ws(const void* ws) {
 }  // namespace
 
 namespace eagle {
+
+namespace {
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+struct CtxQuery {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+  CtxQuery() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(fn);
+  }
+};
+
+std::mutex once_mu;
+std::set<std::tuple<unsigned long long, const void*, int>> once_done;
+}  // namespace
+
+bool current_context_id(unsigned long long* id) {
+  static const CtxQuery q;
+  if (!q.get_current || !q.get_id) return false;
+  CUcontext c = nullptr;
+  if (q.get_current(&c) != CUDA_SUCCESS) return false;
+  if (c == nullptr) {
+    // no current context yet: select the device, which makes its primary
+    // context current (the runtime initialises it there)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return false;
+    if (q.get_current(&c) != CUDA_SUCCESS || c == nullptr) return false;
+  }
+  return q.get_id(c, id) == CUDA_SUCCESS;
+}
+
+cudaError_t smem_limit_once(const void* kernel, int bytes) {
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  const auto key = std::make_tuple(id, kernel, bytes);
+  std::lock_guard<std::mutex> lock(once_mu);
+  if (once_done.count(key)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) once_done.insert(key);
+  return e;
+}
 
 void trace_before(eagle_ctx* ctx, int kernel_id, cudaStream_t s) {
   TraceState& t = ctx->trace;
@@ -502,7 +561,7 @@ eagle_status eagle_commit(eagle_ctx* ctx, int batch, const eagle_accept_out* acc
                           const uint16_t* const* v_tree_layers, uint16_t* const* k_cache_layers,
                           uint16_t* const* v_cache_layers, int kv_cap, const int32_t* target_kv_len,
                           const eagle_draft_out* draft, const eagle_kv* draft_kv, const eagle_commit_out* out,
-                          cudaStream_t stream) {
+                          void* workspace, cudaStream_t stream) {
   EAGLE_REQUIRE(ctx, EAGLE_ERR_INVALID_ARG);
   EAGLE_REQUIRE(batch >= 1 && batch <= ctx->lim.max_batch, EAGLE_ERR_CAPACITY);
   EAGLE_REQUIRE(acc, EAGLE_ERR_INVALID_ARG);
@@ -530,6 +589,7 @@ eagle_status eagle_commit(eagle_ctx* ctx, int batch, const eagle_accept_out* acc
     if ((st = check_kv(ctx, draft_kv)) != EAGLE_OK) return st;
     EAGLE_PTR(out->draft_len);
   }
+  if ((st = check_ws(workspace)) != EAGLE_OK) return st;
   CommitLaunch C{};
   C.batch = batch;
   C.n_layers = n_layers;
@@ -545,6 +605,7 @@ eagle_status eagle_commit(eagle_ctx* ctx, int batch, const eagle_accept_out* acc
   C.draft = draft;
   C.draft_kv = draft_kv;
   C.out = out;
+  C.status = ws_ptr<int>(workspace, ctx->ws.status);
   EAGLE_CUDA(launch_commit(ctx, C, stream));
   return EAGLE_OK;
 }
@@ -583,6 +644,26 @@ eagle_status eagle_trace_disable(eagle_ctx* ctx) {
   EAGLE_REQUIRE(ctx, EAGLE_ERR_INVALID_ARG);
   ctx->trace.kernel_id = -2;
   ctx->trace.n = 0;
+  return EAGLE_OK;
+}
+
+eagle_status eagle_stamps_enable(eagle_ctx* ctx, uint64_t* stamps, int capacity) {
+  EAGLE_REQUIRE(ctx && capacity >= 1, EAGLE_ERR_INVALID_ARG);
+  EAGLE_PTR(stamps);
+  ctx->stamps = stamps;
+  ctx->stamp_cap = capacity;
+  ctx->stamp_ids.clear();
+  return EAGLE_OK;
+}
+
+eagle_status eagle_stamps_disable(eagle_ctx* ctx, int* ids_out, int cap, int* n_out) {
+  EAGLE_REQUIRE(ctx && n_out && (ids_out || cap == 0), EAGLE_ERR_INVALID_ARG);
+  const int n = static_cast<int>(ctx->stamp_ids.size());
+  for (int i = 0; i < n && i < cap; ++i) ids_out[i] = ctx->stamp_ids[i];
+  *n_out = n;
+  ctx->stamps = nullptr;
+  ctx->stamp_cap = 0;
+  ctx->stamp_ids.clear();
   return EAGLE_OK;
 }
 

@@ -17,6 +17,7 @@
 // accumulation), one wave at two CTAs per SM.
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "sm100.cuh"
@@ -69,7 +70,20 @@ struct AttnParams {
   int NP, bo_ld;
   float* part;                    // partial records [query row][split][dh + 4]
   int* counters;
+  int* status;                    // device status word (null: not reported)
+  uint64_t* stamp;                // launch timestamps (null: off)
 };
+
+// Prefix rows of request b that exist: a length beyond the cache is read as
+// the whole cache and reported once per (request, kv head) pair.
+__device__ __forceinline__ int prefix_rows(const AttnParams& p, int b, bool report) {
+  const int L = p.kv_len[b];
+  if (L > p.kv_cap) {
+    if (report) set_status(p.status, EAGLE_ERR_CAPACITY);
+    return p.kv_cap;
+  }
+  return L;
+}
 
 __device__ __forceinline__ int n_nodes(const AttnParams& p, int b) {
   return p.mode == 0 ? p.rows_cap : min(p.tree_size[b], p.rows_cap);
@@ -271,8 +285,12 @@ __device__ __forceinline__ void tile_compute(const AttnParams& p, RowState<NR>& 
 // can exist.
 template <int NR>
 __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams p) {
+  const LaunchStamp ls(p.stamp);
   pdl_trigger();
-  if (p.mode == 1) pdl_wait();               // verification reads the tree's size first
+  if (p.mode == 1) {
+    pdl_wait();                              // verification reads the tree's size first
+    ls.waited();
+  }
   extern __shared__ __align__(16) uint8_t smem_attn[];
   __shared__ int s_last;
   __shared__ uint64_t s_mask[ROWS_PASS];     // ancestor masks of the tree part's rows
@@ -291,7 +309,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
   const bool tree_f32 = is_tree && p.mode == 0;
   int lo = 0, hi = 0;
   if (!is_tree) {
-    const int L = p.kv_len[b];
+    const int L = prefix_rows(p, b, split == 0 && threadIdx.x == 0);
     lo = split * p.chunk;
     hi = min(L, lo + p.chunk);
   } else {
@@ -322,6 +340,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
   // first tile is requested before waiting on the predecessor.
   if (!is_tree && n_tiles > 0) stage(0, 0);
   pdl_wait();                                // q rows, tree K/V and masks come from the predecessors
+  ls.waited();
   if (is_tree && n_tiles > 0) stage(0, 0);
 
   for (int r0 = 0; r0 < R; r0 += p.rows_pass) {
@@ -709,6 +728,7 @@ __device__ __forceinline__ void store_state(const WarpState& st, float* slot, in
 // several); the draft's fp32 tree keys are split into bf16 hi + lo as they
 // are staged, 32 keys per tile.
 __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnParams p) {
+  const LaunchStamp ls(p.stamp);
   pdl_trigger();
   extern __shared__ __align__(16) uint8_t smem_attn[];
   __shared__ int s_last;
@@ -731,7 +751,7 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
   // rows and the tree K/V come from the predecessors.
   int lo = 0, hi = 0;
   if (!is_tree) {
-    const int L = p.kv_len[b];
+    const int L = prefix_rows(p, b, split == 0 && threadIdx.x == 0);
     lo = split * p.chunk;
     hi = min(L, lo + p.chunk);
   }
@@ -761,6 +781,7 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
     for (; staged < n_tiles && staged < p.n_buf; ++staged) stage(staged, staged);
   }
   pdl_wait();                                // q rows, tree K/V, masks and the tree's size
+  ls.waited();
   const int nodes = n_nodes(p, b);
   const int R = nodes * p.G;
   if (is_tree) {
@@ -939,7 +960,7 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
 int attn_splits(const eagle_ctx* ctx, int pairs, int cap, int per_sm) {
   const int tiles = ceil_div(cap < 1 ? 1 : cap, TILE);
   // one wave at per_sm CTAs per SM, the tree part's CTA included
-  int want = attn_splits_bound(ctx, pairs, per_sm);
+  int want = attn_splits_bound(ctx, pairs, cap, per_sm);
   if (want > tiles) want = tiles;
   const int per = ceil_div(tiles, want);
   return ceil_div(tiles, per);     // every split non-empty at full length
@@ -951,37 +972,32 @@ constexpr int kVerifyPerSm = 2;
 
 template <int NR>
 static cudaError_t launch_attn_nr(const AttnParams& p, dim3 grid, size_t smem, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    const size_t most = 2 * TILE_BYTES + (static_cast<size_t>(ROWS_PASS) * MAX_DH +
-                                          static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(tree_attn_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(most));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const size_t most = 2 * TILE_BYTES + (static_cast<size_t>(ROWS_PASS) * MAX_DH +
+                                        static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
+  const cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(tree_attn_kernel<NR>), static_cast<int>(most));
+  if (e != cudaSuccess) return e;
   return launch_pdl(tree_attn_kernel<NR>, grid, dim3(THREADS), smem, st, p);
 }
 
+// Query rows per (request, kv head) from which the draft layer's attention
+// runs on the tensor cores too: below it most of a 16-row tile would be
+// padding, and the CUDA-core kernel is faster.
+constexpr int kDraftMmaRows = 16;
+
 static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
   if (p.dh % 16 != 0 || p.dh > MAX_DH) return cudaErrorInvalidValue;
-  const bool mma = p.mode == 1;
+  const bool mma = p.mode == 1 || p.rows_cap * p.G >= kDraftMmaRows;
   p.n_splits = attn_splits(ctx, p.B * p.Hkv, p.kv_cap, mma ? kVerifyPerSm : kDraftPerSm);
   const int tiles_per_split = ceil_div(ceil_div(p.kv_cap, TILE), p.n_splits);
   p.chunk = tiles_per_split * TILE;
   p.n_buf = tiles_per_split > 1 ? 2 : 1;
   p.rows_pass = std::min(ROWS_PASS, p.rows_cap * p.G);
   dim3 grid(p.n_splits + 1, p.B * p.Hkv);
+  p.stamp = stamp_slot(ctx, kernel_id);
   trace_before(ctx, kernel_id, st);
   cudaError_t e;
   if (mma) {
-    static bool attr_set = false;
-    e = cudaSuccess;
-    if (!attr_set) {
-      e = cudaFuncSetAttribute(tree_attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(2 * TILE_BYTES + Q_BYTES));
-      attr_set = e == cudaSuccess;
-    }
+    e = smem_limit_once(reinterpret_cast<const void*>(tree_attn_mma_kernel), static_cast<int>(2 * TILE_BYTES + Q_BYTES));
     if (e == cudaSuccess)
       e = launch_pdl(tree_attn_mma_kernel, grid, dim3(THREADS), p.n_buf * TILE_BYTES + Q_BYTES, st, p);
   } else {
@@ -1025,6 +1041,7 @@ cudaError_t launch_draft_attn(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t
   p.bo_ld = W.kp_o;
   p.part = ws_ptr<float>(L.ws, W.attn_part);
   p.counters = ws_ptr<int>(L.ws, W.attn_cnt);
+  p.status = ws_ptr<int>(L.ws, W.status);
   return run_attn(ctx, p, EAGLE_K_DRAFT_ATTN, st);
 }
 
@@ -1055,6 +1072,7 @@ cudaError_t launch_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, con
   p.out_f32 = out;
   p.part = ws_ptr<float>(ws, W.attn_part);
   p.counters = ws_ptr<int>(ws, W.attn_cnt) + ctx->lim.max_batch * D.n_kv_heads;
+  p.status = ws_ptr<int>(ws, W.status);
   return run_attn(ctx, p, EAGLE_K_VERIFY_ATTN, st);
 }
 
@@ -1070,13 +1088,15 @@ cudaError_t launch_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, con
 constexpr size_t kScratchBytes = static_cast<size_t>(32) << 20;
 constexpr size_t kScratchCounterBytes = static_cast<size_t>(64) << 10;
 constexpr int kScratchMaxPairs = static_cast<int>(kScratchCounterBytes / sizeof(int));
-constexpr int kScratchMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char verify_scratch[kScratchBytes];
 
 namespace {
+// The array's address in each CUDA context that has used it, keyed by the
+// context's id: a context re-created after cudaDeviceReset has a new id, so
+// its array is looked up and its counters zeroed again.
 std::mutex scratch_mu;
-void* scratch_base[kScratchMaxDevices] = {};
+std::vector<std::pair<unsigned long long, void*>> scratch_base;
 }  // namespace
 
 size_t verify_scratch_need(const eagle_ctx* ctx, int batch, const eagle_kv* prefix, const eagle_tree* tree) {
@@ -1093,19 +1113,26 @@ eagle_status launch_verify_attn_noalloc(eagle_ctx* ctx, int batch, const uint16_
   if (batch * D.n_kv_heads > kScratchMaxPairs ||
       verify_scratch_need(ctx, batch, prefix, tree) > kScratchBytes - kScratchCounterBytes)
     return EAGLE_ERR_CAPACITY;                 // nothing launched
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kScratchMaxDevices) return EAGLE_ERR_CUDA;
+  unsigned long long cid = 0;
+  if (!current_context_id(&cid)) return EAGLE_ERR_CUDA;
   void* base = nullptr;
   {
     std::lock_guard<std::mutex> lock(scratch_mu);
-    base = scratch_base[dev];
+    for (const auto& kv : scratch_base)
+      if (kv.first == cid) base = kv.second;
     if (base == nullptr) {
-      // first call on this device: the array's address, then zeroed counters
+      // first call in this context: the set-up below would synchronise the
+      // stream, which a capture does not allow -- refuse before touching it
+      cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+      if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return EAGLE_ERR_CUDA;
+      if (cap != cudaStreamCaptureStatusNone) return EAGLE_ERR_INVALID_ARG;
+      // the array's address, then zeroed counters
       void* ptr = nullptr;
       if (cudaGetSymbolAddress(&ptr, verify_scratch) != cudaSuccess) return EAGLE_ERR_CUDA;
       if (cudaMemsetAsync(ptr, 0, kScratchCounterBytes, st) != cudaSuccess) return EAGLE_ERR_CUDA;
       if (cudaStreamSynchronize(st) != cudaSuccess) return EAGLE_ERR_CUDA;
-      scratch_base[dev] = base = ptr;
+      scratch_base.emplace_back(cid, ptr);
+      base = ptr;
     }
   }
   AttnParams p{};

@@ -35,6 +35,8 @@ struct CommitParams {
   int32_t* t_next;
   int32_t* prefix_len_out;
   int32_t* draft_len_out;
+  int* status;
+  uint64_t* stamp;
 };
 
 // rows are whole multiples of 8 bf16 (16 bytes)
@@ -45,12 +47,26 @@ __device__ __forceinline__ void copy_row(uint16_t* dst, const uint16_t* src, int
 }
 
 __global__ void commit_kernel(const CommitParams p) {
+  const LaunchStamp ls(p.stamp);
   pdl_wait();      // predecessor outputs visible from here on
+  ls.waited();
   pdl_trigger();
   const int b = blockIdx.x, i = blockIdx.y;
   const int a = p.accept_len[b];
   const int L = p.kv_len[b];
+  // a request whose cache cannot take the path commits nothing (checked
+  // alike by every CTA of the request; the state CTA reports it)
+  const bool room = L >= 0 && static_cast<long long>(L) + 1 + a <= p.kv_cap;
+  const bool draft_room = p.dk == nullptr || (p.draft_len[b] >= 0 && p.draft_len[b] < p.draft_cap);
   if (i == p.path_cap) {
+    if (!room || !draft_room) {
+      if (threadIdx.x == 0) {
+        p.prefix_len_out[b] = L;
+        if (p.dk) p.draft_len_out[b] = p.draft_len[b];
+        set_status(p.status, EAGLE_ERR_CAPACITY);
+      }
+      return;
+    }
     // next round's state: the last accepted slot's true feature, the bonus
     // token, the new prefix length; the root's draft K/V row (fp32 -> bf16,
     // four elements per load) appended to the draft cache
@@ -81,7 +97,7 @@ __global__ void commit_kernel(const CommitParams p) {
     }
     return;
   }
-  if (i > a) return;
+  if (i > a || !room || !draft_room) return;
   const int slot = p.path[static_cast<size_t>(b) * p.path_cap + i];
   for (int l = 0; l < p.n_layers; ++l) {
     const size_t src = (static_cast<size_t>(b) * p.S + slot) * p.row_elems;
@@ -137,6 +153,8 @@ cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st
   p.t_next = C.out->t_next;
   p.prefix_len_out = C.out->prefix_len;
   p.draft_len_out = C.out->draft_len;
+  p.status = C.status;
+  p.stamp = stamp_slot(ctx, EAGLE_K_COMMIT);
   dim3 grid(C.batch, C.acc->path_cap + 1);
   trace_before(ctx, EAGLE_K_COMMIT, st);
   const cudaError_t e = launch_pdl(commit_kernel, grid, dim3(512), 0, st, p);

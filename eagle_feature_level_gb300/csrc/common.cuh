@@ -74,10 +74,19 @@ __device__ __forceinline__ uint64_t scale_uniform(uint32_t u, uint64_t S) {
 
 constexpr int QBITS = 40;
 
-// W = floor(p * 2^40) for p in [0, 1] (exact: power-of-two scale).
+// W = floor(p * 2^40) for p in [0, 2^24), exactly, in integer arithmetic
+// (no fp64 pipe, which GB300 runs at a small fraction of its integer rate):
+// a finite positive fp32 p is m * 2^(E - 150) with the significand m (hidden
+// bit included; E the biased exponent, E = 1 for subnormals), so
+// p * 2^40 = m * 2^(E - 110), a shift of m.  Zero, negative, infinite and
+// NaN inputs carry no mass (0).
 __device__ __forceinline__ uint64_t quantize_prob(float p) {
-  const double x = static_cast<double>(p) * 1099511627776.0;
-  return x > 0.0 ? static_cast<uint64_t>(x) : 0ull;  // truncation == floor for x >= 0
+  const uint32_t u = __float_as_uint(p);
+  const uint32_t E = (u >> 23) & 0xffu;
+  if ((u >> 31) != 0u || E == 0xffu || E > 150u) return 0ull;
+  const uint64_t m = E != 0u ? ((u & 0x7fffffu) | 0x800000u) : (u & 0x7fffffu);
+  const int sh = static_cast<int>(E != 0u ? E : 1u) - 110;
+  return sh >= 0 ? (m << sh) : (sh > -32 ? (m >> -sh) : 0ull);
 }
 
 // ---- reductions -----------------------------------------------------------
@@ -194,6 +203,24 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// ---- launch timestamps (measurement) ---------------------------------------
+// With a non-null slot, thread 0 of every CTA records %globaltimer twice:
+// when it has passed the dependency wait (atomic min into slot[0]: the
+// earliest moment a CTA of this launch could use its predecessors' outputs)
+// and when it leaves the kernel (atomic max into slot[1]).  A null slot
+// costs one test.
+struct LaunchStamp {
+  unsigned long long* slot;
+  __device__ explicit LaunchStamp(uint64_t* s)
+      : slot(threadIdx.x == 0 ? reinterpret_cast<unsigned long long*>(s) : nullptr) {}
+  __device__ void waited() const {
+    if (slot) atomicMin(slot, static_cast<unsigned long long>(globaltimer_ns()));
+  }
+  __device__ ~LaunchStamp() {
+    if (slot) atomicMax(slot + 1, static_cast<unsigned long long>(globaltimer_ns()));
+  }
+};
 
 // A device-side wait gives up after this long and reports EAGLE_ERR_TIMEOUT.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;

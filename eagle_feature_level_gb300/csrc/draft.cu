@@ -17,12 +17,14 @@ namespace {
 __global__ void prep_fc_kernel(const float* __restrict__ f_last, const float* __restrict__ f_hat,
                                const int32_t* __restrict__ token, const int32_t* __restrict__ parent,
                                const uint16_t* __restrict__ embed, int ld_embed, int d, int E, int rpr, int e0,
-                               int NP, int kp, uint16_t* __restrict__ bfc) {
+                               int NP, int kp, uint16_t* __restrict__ bfc, uint64_t* stamp) {
+  const LaunchStamp ls(stamp);
   // The FC contraction after this kernel may be scheduled now (its CTAs
   // start streaming weights); triggering before the wait in the kernels
   // ahead of this one would bring it in while the LM head still streams.
   pdl_trigger();
   pdl_wait();      // predecessor outputs visible from here on
+  ls.waited();
   const int j = blockIdx.x;
   const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
   if (c0 >= 2 * d) return;
@@ -128,10 +130,13 @@ struct SelParams {
   int V, E, K, k, rpr, e0;
   uint32_t seed, round_id;
   int* status;
+  uint64_t* stamp;
 };
 
 __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) select_kernel(const SelParams p) {
+  const LaunchStamp ls(p.stamp);
   pdl_wait();      // predecessor outputs visible from here on
+  ls.waited();
   pdl_trigger();
   __shared__ float s_red[SEL_WARPS];
   __shared__ float s_cmax[SEL_CL], s_csum[SEL_CL];         // per-rank partials (pushed)
@@ -374,10 +379,11 @@ cudaError_t launch_prep_fc(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st
   const eagle_dims& D = ctx->dims;
   trace_before(ctx, EAGLE_K_PREP, st);
   const dim3 grid(L.n, ceil_div(2 * D.d / 8, 128));
+  uint64_t* stamp = stamp_slot(ctx, EAGLE_K_PREP);
   const cudaError_t e =
       launch_pdl(prep_fc_kernel, grid, dim3(128), 0, st, L.req->f_last, L.out->f_hat, L.pool->token, L.pool->parent,
                  L.w->embed, L.w->ld_embed, D.d, ctx->lim.max_expanded, L.rpr, L.e0, L.NP, ctx->ws.kp_fc,
-                 ws_ptr<uint16_t>(L.ws, ctx->ws.b_fc));
+                 ws_ptr<uint16_t>(L.ws, ctx->ws.b_fc), stamp);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_PREP, st);
   return e;
@@ -400,6 +406,7 @@ cudaError_t launch_select(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st)
   p.seed = L.s->seed;
   p.round_id = L.s->round_id;
   p.status = ws_ptr<int>(L.ws, ctx->ws.status);
+  p.stamp = stamp_slot(ctx, EAGLE_K_SELECT);
   trace_before(ctx, EAGLE_K_SELECT, st);
   const cudaError_t e = launch_pdl(select_kernel, dim3(L.n * SEL_CL), dim3(SEL_THREADS), 0, st, p);
   ctx->launches++;

@@ -84,6 +84,7 @@ struct GemmParams {
   float* part;
   int* counters;
   int* status;
+  uint64_t* stamp;
 };
 
 struct Smem {
@@ -573,7 +574,7 @@ __device__ __forceinline__ long long first_ring(const GemmParams& p, const CtaWo
 // (gemm_produce_first_b) as soon as the previous kernel has completed, so a
 // CTA that starts late is not held up behind its own weight requests.
 __device__ __forceinline__ void gemm_produce(const GemmParams& p, const Smem& s, const GemmMaps& mp, int lane,
-                                             const CtaWork& wk, volatile int* abort_flag) {
+                                             const CtaWork& wk, volatile int* abort_flag, const LaunchStamp& ls) {
   const long long nv = wk.n_units(p);
   const long long n_pre = first_ring(p, wk);
   if (lane == 0)
@@ -585,6 +586,7 @@ __device__ __forceinline__ void gemm_produce(const GemmParams& p, const Smem& s,
   const uint64_t policy = sm100::l2_policy_evict_first();   // weights are read once per launch
   for (long long i = 0; i < n_pre; ++i) issue_a(p, s, mp, wk.unit(p, i), static_cast<int>(i), policy);
   pdl_wait();
+  ls.waited();
   long long issued = n_pre;
   int stage = static_cast<int>(n_pre % p.stages);
   uint32_t phase = n_pre == p.stages ? 1u : 0u;
@@ -694,6 +696,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
   const long long U_sk = static_cast<long long>(p.sk_tiles) * p.kb;
   volatile int* abort_flag = s.flags;
   const GemmMaps maps{&mA0, &mA1, &mA2, &mT0, &mT1, &mT2, &mB};
+  const LaunchStamp ls(p.stamp);
   pdl_trigger();
 
   if (threadIdx.x == 0) {
@@ -727,7 +730,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
   const uint32_t tmem_base = *s.tmem_holder;
 
   if (warp == 0) {
-    gemm_produce(p, s, maps, lane, wk, abort_flag);
+    gemm_produce(p, s, maps, lane, wk, abort_flag, ls);
     __syncwarp();
   } else if (warp == 1) {
     gemm_mma(p, s, lane, tmem_base, wk, abort_flag);
@@ -996,11 +999,9 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   if (!encode_grouped(ctx, &mb, ws_ptr<uint16_t>(L.ws, b_in), kp_in, 2 * p.NP, kp_in, p.kps, 2 * p.NP / 8))
     return cudaErrorInvalidValue;
 
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+  {
+    const cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(gemm_stream_kernel), 232448);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   int grid = per_sm * ctx->sm_count;
   if (p.total_units < grid) grid = static_cast<int>(p.total_units);
@@ -1011,6 +1012,7 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   // partial slots t + cta of split tiles stay inside the workspace's array
   if (p.sk_tiles > 0 && p.sk_tiles - 1 + grid - 1 >= W.max_mtiles + 2 * ctx->sm_count)
     return cudaErrorInvalidConfiguration;
+  p.stamp = stamp_slot(ctx, epi);
   trace_before(ctx, epi, st);
   const cudaError_t e = launch_pdl(gemm_stream_kernel, dim3(grid), dim3(NUM_THREADS), smem, st, maps[0], maps[1],
                                    maps[2], tails[0], tails[1], tails[2], mb, p);

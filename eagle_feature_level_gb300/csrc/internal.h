@@ -69,6 +69,10 @@ struct eagle_ctx {
   eagle::TraceState trace;
   long long launches = 0;
   eagle::EncodeTiledFn encode = nullptr;
+  // launch timestamps (eagle_stamps_enable): caller-owned device pairs
+  uint64_t* stamps = nullptr;
+  int stamp_cap = 0;
+  std::vector<int> stamp_ids;        // kernel class of each stamped launch
 };
 
 namespace eagle {
@@ -91,6 +95,27 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// The calling thread's current CUDA context as a process-unique id (the
+// driver never reuses one, so a context re-created after cudaDeviceReset gets
+// a new id).  Makes the device's primary context current if none is.  False
+// if the id cannot be determined.
+bool current_context_id(unsigned long long* id);
+
+// cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+// bytes), done once per (current context, kernel, bytes): function
+// attributes belong to a context, so every device and every re-created
+// context gets its own.
+cudaError_t smem_limit_once(const void* kernel, int bytes);
+
+// The timestamp pair of the next launch (of kernel class `kernel_id`) while
+// stamps are enabled, else null.
+inline uint64_t* stamp_slot(eagle_ctx* ctx, int kernel_id) {
+  if (!ctx->stamps || static_cast<int>(ctx->stamp_ids.size()) >= ctx->stamp_cap) return nullptr;
+  uint64_t* s = ctx->stamps + 2 * ctx->stamp_ids.size();
+  ctx->stamp_ids.push_back(kernel_id);
+  return s;
 }
 
 // Launch bookkeeping: optional CUDA-event trace around kernels of one class.
@@ -155,6 +180,7 @@ struct CommitLaunch {
   const eagle_draft_out* draft;
   const eagle_kv* draft_kv;
   const eagle_commit_out* out;
+  int* status;
 };
 cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st);
 
@@ -162,11 +188,15 @@ cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st
 // pairs over a cache of `cap` rows, for a kernel run at per_sm CTAs per SM.
 int attn_splits(const eagle_ctx* ctx, int pairs, int cap, int per_sm);
 // Most prefix splits an attention launch over `pairs` (request, kv head)
-// pairs uses: one wave at per_sm CTAs per SM (four, the most any attention
-// kernel runs at, by default) with the tree part's CTA, at most 31 so that
-// a warp holds every split's record in the merge.
-inline int attn_splits_bound(const eagle_ctx* ctx, int pairs, int per_sm = 4) {
+// pairs and a cache of `cap` rows uses: enough for one wave at per_sm CTAs
+// per SM (four, the most any attention kernel runs at, by default) with the
+// tree part's CTA, and at least enough that no split holds more than 8 key
+// tiles of 64 (long or ragged prefixes: many short CTAs, not a few long
+// ones); at most 31, so that a warp holds every split's record in the merge.
+inline int attn_splits_bound(const eagle_ctx* ctx, int pairs, int cap, int per_sm = 4) {
   int s = per_sm * ctx->sm_count / (pairs < 1 ? 1 : pairs) - 1;
+  const int tiles = ((cap < 1 ? 1 : cap) + 63) / 64;
+  if (s < (tiles + 7) / 8) s = (tiles + 7) / 8;
   if (s > 31) s = 31;
   return s < 1 ? 1 : s;
 }

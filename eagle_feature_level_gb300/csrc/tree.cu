@@ -13,7 +13,10 @@
 //             Then flatten: slots 1..m by (depth asc, selection rank asc),
 //             parent slots, positions, ancestor bitmasks.
 // Ranks come from counting (each thread compares its key with every other
-// valid key), which is exact and independent of thread order.
+// valid key), which is exact and independent of thread order.  Node values
+// are non-negative fp64 products, whose bit patterns order like the values
+// as unsigned integers: the counting loops compare those (GB300 runs fp64
+// comparisons at a small fraction of the integer rate).
 #include "internal.h"
 #include "common.cuh"
 
@@ -47,19 +50,28 @@ struct TreeParams {
   int32_t* t_child_slot;
   int32_t* t_size;
   int* status;
+  uint64_t* stamp;
 };
 
-// key order: true if entry a ranks before entry b
-__device__ __forceinline__ bool before(double va, int da, int ca, double vb, int db, int cb) {
+// key order: true if entry a ranks before entry b (value keys: the bits of
+// non-negative doubles, larger first; then depth, then creation order)
+__device__ __forceinline__ bool before(uint64_t va, int da, int ca, uint64_t vb, int db, int cb) {
   if (va != vb) return va > vb;
   if (da != db) return da < db;
   return ca < cb;
 }
 
+__device__ __forceinline__ uint64_t value_key(double v) {
+  return static_cast<uint64_t>(__double_as_longlong(v));
+}
+
 __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) {
+  const LaunchStamp ls(p.stamp);
   pdl_wait();      // predecessor outputs visible from here on
+  ls.waited();
   pdl_trigger();
   __shared__ double s_val[MAX_POOL];
+  __shared__ uint64_t s_key[MAX_POOL];
   __shared__ int s_dep[MAX_POOL];
   __shared__ int s_rank[MAX_POOL];
   __shared__ int s_slot[MAX_POOL];
@@ -118,6 +130,7 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
       const int tok = p.ctok[(pb + e) * K + r];
       const bool valid = p.p_token[pb + e] >= 0 && tok >= 0;
       s_val[c] = valid ? p.p_value[pb + e] * static_cast<double>(p.cprob[(pb + e) * K + r]) : -1.0;
+      s_key[c] = valid ? value_key(s_val[c]) : 0ull;
       s_dep[c] = valid ? 1 : 0;
       if (valid) atomicAdd(&s_count, 1);
     }
@@ -126,7 +139,7 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
       if (!s_dep[c]) continue;
       int rank = 0;
       for (int o = 0; o < n_c; ++o)
-        if (s_dep[o] && before(s_val[o], 0, o, s_val[c], 0, c)) ++rank;
+        if (s_dep[o] && before(s_key[o], 0, o, s_key[c], 0, c)) ++rank;
       if (rank >= n_new) continue;
       const int e = e_prev + c / k, r = c % k;
       const int e_new = e_new0 + rank;
@@ -183,6 +196,7 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
       const int tok = p.ctok[(pb + e) * K + r];
       const bool valid = p.p_token[pb + e] >= 0 && tok >= 0;
       s_val[c] = valid ? p.p_value[pb + e] * static_cast<double>(p.cprob[(pb + e) * K + r]) : -1.0;
+      s_key[c] = valid ? value_key(s_val[c]) : 0ull;
       s_dep[c] = valid ? p.p_depth[pb + e] + 1 : -1;
       s_slot[c] = -1;
       if (valid) atomicAdd(&s_count, 1);
@@ -193,7 +207,7 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
       if (s_dep[c] >= 0) {
         rank = 0;
         for (int o = 0; o < n_c; ++o)
-          if (s_dep[o] >= 0 && before(s_val[o], s_dep[o], o, s_val[c], s_dep[c], c)) ++rank;
+          if (s_dep[o] >= 0 && before(s_key[o], s_dep[o], o, s_key[c], s_dep[c], c)) ++rank;
       }
       s_rank[c] = rank;
     }
@@ -296,6 +310,7 @@ cudaError_t launch_tree(eagle_ctx* ctx, const eagle_plan* plan, int phase, int l
     p.t_size = tree->size;
   }
   p.status = status;
+  p.stamp = stamp_slot(ctx, EAGLE_K_TREE);
   trace_before(ctx, EAGLE_K_TREE, st);
   const cudaError_t e = launch_pdl(tree_kernel, dim3(batch), dim3(TREE_THREADS), 0, st, p);
   ctx->launches++;

@@ -232,7 +232,7 @@ class Round:
         B.eagle_commit(e.ctx, self.B, self.acc_c, self.tree_c, _p(self.f_true),
                        [_p(t) for t in self.tree_k], [_p(t) for t in self.tree_v],
                        [_p(t) for t in self.tgt_k], [_p(t) for t in self.tgt_v], self.kv_cap, _p(self.tgt_len),
-                       self.out_c, self.draft_kv_c, self.commit_c, e.stream())
+                       self.out_c, self.draft_kv_c, self.commit_c, e.ws.data_ptr(), e.stream())
 
     def capture(self, w_c: B.eagle_draft_weights) -> "torch.cuda.CUDAGraph":
         """Capture one whole round (target logits already in place) as a CUDA

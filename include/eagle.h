@@ -297,7 +297,9 @@ eagle_status eagle_tree_expand_rerank(eagle_ctx* ctx, const eagle_plan* plan, in
  * ([B] "Tree Attention 如何一次验证多条路径"; [A] §12 item 5):
  *   out[b][s][h] = softmax(scale * q[b][s][h] . K^T) V over prefix rows
  *   0..prefix.len[b]-1 and tree slots j < tree.size[b] with bit j of
- *   tree.anc[b][s]; kv head = h / (Hq / Hkv).
+ *   tree.anc[b][s]; kv head = h / (Hq / Hkv).  A length beyond the cache
+ *   (prefix.len[b] > prefix.cap) is read as prefix.cap rows and sets
+ *   EAGLE_ERR_CAPACITY in the status word.
  * q: [B][S][Hq][dh] bf16; k_tree, v_tree: [B][S][Hkv][dh] bf16; out: [B][S][Hq][dh] fp32,
  * S = tree.stride.  Slots s >= tree.size[b] are not written. */
 eagle_status eagle_tree_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q,
@@ -394,14 +396,20 @@ typedef struct {
  * are simply not copied.
  * k_tree_layers / v_tree_layers / k_cache_layers / v_cache_layers are HOST
  * arrays of n_layers device pointers ([B][S][Hkv][dh] and [B][kv_cap][Hkv][dh]).
- * f_true: [B][S][d] fp32.  Output buffers must not alias inputs. */
+ * f_true: [B][S][d] fp32.  Output buffers must not alias inputs.
+ * Capacity (checked on the device, where the lengths live): a request whose
+ * target cache cannot take its 1 + a rows (L_b + 1 + a > kv_cap), or whose
+ * draft cache is full (draft_kv.len[b] >= draft_kv.cap), is not committed:
+ * no cache row of it is written, prefix_len / draft_len keep the old
+ * lengths, its other outputs are unspecified, and EAGLE_ERR_CAPACITY is set
+ * in the workspace's status word. */
 eagle_status eagle_commit(eagle_ctx* ctx, int batch, const eagle_accept_out* acc,
                           const eagle_tree* tree, const float* f_true, int n_layers,
                           const uint16_t* const* k_tree_layers, const uint16_t* const* v_tree_layers,
                           uint16_t* const* k_cache_layers, uint16_t* const* v_cache_layers,
                           int kv_cap, const int32_t* target_kv_len,
                           const eagle_draft_out* draft, const eagle_kv* draft_kv,
-                          const eagle_commit_out* out, cudaStream_t stream);
+                          const eagle_commit_out* out, void* workspace, cudaStream_t stream);
 
 /* ---- measurement --------------------------------------------------------- */
 
@@ -420,6 +428,22 @@ eagle_status eagle_trace_enable(eagle_ctx* ctx, int kernel_id, int capacity);
  * kernel class of each (ids_out may be NULL) and the count. */
 eagle_status eagle_trace_read(eagle_ctx* ctx, float* ms_out, int* ids_out, int cap, int* n_out);
 eagle_status eagle_trace_disable(eagle_ctx* ctx);
+
+/* Launch timestamps, for measuring kernels inside an untraced round (a CUDA
+ * graph replay keeps the programmatic overlap between kernels, which event
+ * pairs around each launch would break).  While enabled, the i-th launch
+ * issued through this context (counted from enable; launches captured into a
+ * graph keep their slot on every replay) has thread 0 of each CTA record
+ * %globaltimer nanoseconds into stamps[2i] (atomic min, taken when the CTA
+ * has passed its wait for the preceding kernels' results) and stamps[2i+1]
+ * (atomic max, taken when the thread leaves the kernel).  `stamps` is a
+ * caller-owned device buffer of 2 * capacity uint64_t that the caller sets
+ * to (UINT64_MAX, 0) pairs before each run it measures; launches beyond
+ * `capacity` are not recorded.  Costs one atomic per CTA and stamp. */
+eagle_status eagle_stamps_enable(eagle_ctx* ctx, uint64_t* stamps, int capacity);
+/* Stops assigning stamp slots; writes the kernel class (eagle_kernel_id) of
+ * each stamped launch, in order, to ids_out (up to cap) and their count. */
+eagle_status eagle_stamps_disable(eagle_ctx* ctx, int* ids_out, int cap, int* n_out);
 
 /* Kernels this context has launched so far (host-side count). */
 long long eagle_launch_count(const eagle_ctx* ctx);
