@@ -37,9 +37,9 @@ import eagle_synth as S  # noqa: E402
 METRIC = "EAGLE draft+verify round µs and tree nodes/s at 7B shape; % of HBM roofline"
 ALPHA = (0.9, 0.7, 0.6, 0.6, 0.6, 0.6)   # injected per-layer acceptance profile
 
-# DRAM bytes (read + write) per gemm_stream_kernel launch from one ncu capture
-# (profiles/gemm_stream_7b_static26.md).  Reported only while the kernel's
-# sources are the ones the counters were taken on.
+# DRAM bytes (read + write) per gemm_stream_kernel launch at 7b_static26,
+# averaged over the 30 launches of one round in one ncu capture.  Reported
+# only while the kernel's sources hash to the ones the counters were taken on.
 GEMM_TRAFFIC = {"workload": "7b_static26", "bytes_per_launch": 125171209,
                 "sources": ("gemm.cu", "sm100.cuh", "common.cuh"),
                 "sha256": "72df5f1ad9bb4e47661dfe7af21dec0d955cc36dbf6e5c6172130195c0421339"}
@@ -184,6 +184,34 @@ def cpu_baseline(w, seed, W, inp, budget_s=20.0, max_rounds=None, warmup=0):
                       f"= host cores)", "warmup_rounds": warm}, rounds, el
 
 
+def cpu_single_thread(workload: str, budget_s: float):
+    """The oracle's bounded sample on one host thread: a child process (its
+    BLAS limited to one thread from start-up) that rebuilds the inputs from
+    the seeds.  Bounded; returns its result dict, or a reason."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-oracle-sample", "--workload", workload,
+                            "--cpu-budget", str(budget_s)], env=env, capture_output=True, text=True,
+                           timeout=budget_s * 6 + 120)
+        line = [x for x in r.stdout.splitlines() if x.startswith("{")]
+        return json.loads(line[-1]) if line else {"unavailable": (r.stderr or "no output").strip()[-200:]}
+    except Exception as exc:                               # reported, not fatal
+        return {"unavailable": str(exc)[:200]}
+
+
+def run_cpu_sample(args):
+    w = S.WORKLOADS[args.workload]
+    seed = S.WORKLOAD_SEEDS[args.workload]
+    W = S.draft_weights(w, seed, device="cpu")
+    inp = S.round_inputs(w, seed, device="cpu")
+    base, _, _ = cpu_baseline(w, seed, W, inp, budget_s=args.cpu_budget)
+    base.pop("warmup_rounds", None)
+    base["cores"] = 1
+    base["sample"] = base["sample"].replace("BLAS threads = host cores", "BLAS threads = 1")
+    print(json.dumps(base), flush=True)
+
+
 def run_reference(args):
     rank, world, local = dist_setup(args.gpus)
     if rank != 0:
@@ -253,38 +281,66 @@ def run_ours(args):
     nodes_per_round = w.batch * w.top_m
     value = world * nodes_per_round * args.steps / (ms_total / 1e3)
 
-    # ---- per-kernel durations: the same graph with an event pair around every kernel ----
-    k_tr = min(args.steps, 50)
-    B.eagle_trace_enable(eng.ctx, "all", per_round + 8)
-    tgraph = rd.capture(wc)
-    by_class = {}
-    for _ in range(k_tr):
-        tgraph.replay()
+    # ---- per-kernel durations inside the untraced round ----
+    # The same round captured with launch timestamps: every kernel records
+    # (%globaltimer) when its first CTA passed the wait for its predecessors
+    # and when its last CTA left.  Kernel i's exclusive window runs from its
+    # own release to the next kernel's release (the last one's to its exit):
+    # the windows tile the round, so they sum to the round's device time and
+    # keep the programmatic overlap between kernels intact.
+    cap = per_round + 8
+    stamps = torch.empty(2 * cap, dtype=torch.int64, device=dev)
+    B.eagle_stamps_enable(eng.ctx, stamps.data_ptr(), cap)
+    sgraph = rd.capture(wc)
+    names = B.eagle_stamps_disable(eng.ctx)
+    k_st = min(max(args.steps, 5), 50)
+    n = len(names)
+    excl = [0.0] * n
+    span = [0.0] * n
+    stamped_round = 0.0
+    tick = None
+    for _ in range(k_st):
+        stamps.view(-1, 2)[:, 0].fill_(-1)          # UINT64_MAX: no release seen yet
+        stamps.view(-1, 2)[:, 1].fill_(0)
+        sgraph.replay()
         torch.cuda.synchronize()
-        for name, ms in B.eagle_trace_read(eng.ctx, per_round + 8):
-            c = by_class.setdefault(name, [0, 0.0])
-            c[0] += 1
-            c[1] += ms
-    B.eagle_trace_disable(eng.ctx)
-    del tgraph
+        t = [int(x) & 0xFFFFFFFFFFFFFFFF for x in stamps[:2 * n].cpu().tolist()]
+        w_, e_ = t[0::2], t[1::2]
+        for i in range(n):
+            nxt = w_[i + 1] if i + 1 < n else e_[i]
+            excl[i] += (nxt - w_[i]) / 1e3
+            span[i] += (e_[i] - w_[i]) / 1e3
+        stamped_round += (e_[n - 1] - w_[0]) / 1e3
+        d = sorted({abs(a - b) for a, b in zip(w_[1:], w_[:-1]) if a != b})
+        if d:
+            tick = d[0] if tick is None else min(tick, d[0])
+    del sgraph
+    by_class = {}
+    for i, name in enumerate(names):
+        c = by_class.setdefault(name, [0, 0.0, 0.0])
+        c[0] += 1
+        c[1] += excl[i] / k_st
+        c[2] += span[i] / k_st
     gb = gemm_weight_bytes(w)
-    g_bytes = sum(gb[n] * by_class[n][0] for n in gb if n in by_class)
-    g_ms = sum(by_class[n][1] for n in gb if n in by_class)
-    g_launch = sum(by_class[n][0] for n in gb if n in by_class)
+    g_cls = [c for c in gb if c in by_class]
+    g_bytes = sum(gb[c] * by_class[c][0] for c in g_cls)                  # per round
+    g_us = sum(by_class[c][1] for c in g_cls)
+    g_launch = sum(by_class[c][0] for c in g_cls)
     peak, peak_kind = peaks()
-    achieved = g_bytes / (g_ms / 1e3) / 1e9
-    lm = by_class.get("gemm_lm", [1, 0.0])
-    lm_gbs = gb["gemm_lm"] * lm[0] / (lm[1] / 1e3) / 1e9 if lm[1] > 0 else None
+    achieved = g_bytes / (g_us / 1e6) / 1e9
+    per_contraction = {c: {"us_per_launch": round(by_class[c][1] / by_class[c][0], 2),
+                           "gbs": round(gb[c] / (by_class[c][1] / by_class[c][0] / 1e6) / 1e9, 1)}
+                       for c in g_cls}
     stage = {
-        "draft_us": 1e3 * sum(by_class.get(n, [0, 0.0])[1] for n in
-                              ("prep", "gemm_fc", "gemm_qkv", "draft_attn", "gemm_o", "gemm_gateup", "gemm_down",
-                               "gemm_lm", "select")) / k_tr,
-        "tree_us": 1e3 * by_class.get("tree", [0, 0.0])[1] / k_tr,
-        "verify_us": 1e3 * by_class.get("verify_attn", [0, 0.0])[1] / k_tr,
-        "accept_us": 1e3 * by_class.get("accept", [0, 0.0])[1] / k_tr,
-        "commit_us": 1e3 * by_class.get("commit", [0, 0.0])[1] / k_tr,
+        "draft_us": sum(by_class.get(c, [0, 0.0])[1] for c in
+                        ("prep", "gemm_fc", "gemm_qkv", "draft_attn", "gemm_o", "gemm_gateup", "gemm_down",
+                         "gemm_lm", "select")),
+        "tree_us": by_class.get("tree", [0, 0.0])[1],
+        "verify_us": by_class.get("verify_attn", [0, 0.0])[1],
+        "accept_us": by_class.get("accept", [0, 0.0])[1],
+        "commit_us": by_class.get("commit", [0, 0.0])[1],
     }
-    kernel_us = {n: round(1e3 * c[1] / k_tr, 2) for n, c in sorted(by_class.items())}
+    kernel_us = {c: round(v[1], 2) for c, v in sorted(by_class.items())}
 
     # ---- end to end through the public API with host buffers ----
     # the round's host-facing tensors live in one device allocation per
@@ -310,6 +366,10 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         base, _, _ = cpu_baseline(w, seed, W, inp, budget_s=args.cpu_budget)
         base.pop("warmup_rounds", None)
+        if args.workload in ("tiny_fp32", "7b_static26", "7b_eagle2"):
+            base["single_thread"] = cpu_single_thread(args.workload, args.cpu_budget)
+        else:
+            base["single_thread"] = {"unavailable": "not run: one round of this shape takes minutes on one thread"}
 
     alg = algorithmic_bytes(w, {"draft_len": inp["draft_len"], "prefix_len": inp["prefix_len"]})
     clocks = clk.summary()
@@ -329,13 +389,22 @@ def run_ours(args):
         "algorithmic_bytes_per_round": alg,
         "hbm_frac": alg / (ms_step / 1e3) / (peak * 1e9),
         "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
+        "hbm_frac_of_nominal_8tbs": alg / (ms_step / 1e3) / 8.0e12,
+        "timing": "stages_us / kernel_us_per_round: exclusive windows of each kernel inside the untraced "
+                  "graph replay (kernel-written %globaltimer stamps, mean of "
+                  f"{k_st} replays); they sum to stamped_round_us",
+        "stamped_round_us": round(stamped_round / k_st, 2),
+        "stamp_tick_ns": tick,
         "stages_us": {k: round(v, 2) for k, v in stage.items()},
         "kernel_us_per_round": kernel_us,
+        "kernel_span_us_per_round": {c: round(v[2], 2) for c, v in sorted(by_class.items())},
         "roofline": {"kernel": "gemm_stream_kernel (all six draft-layer contractions)", "bound": "hbm",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": gemm_traffic(w.name), "launches": g_launch,
+                     "peak_kind": peak_kind, "traffic": gemm_traffic(w.name), "launches_per_round": g_launch,
                      "bytes_per_launch": g_bytes / max(g_launch, 1),
-                     "lm_head_gbs": lm_gbs},
+                     "us_per_round": round(g_us, 2),
+                     "duration": "exclusive window per launch from launch timestamps in the untraced round",
+                     "per_contraction": per_contraction},
         "e2e": {"value": e2e_value, "unit": "tree nodes/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": k_e2e},
         "gpu_launches": launches,
@@ -358,7 +427,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-oracle-sample", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_oracle_sample:
+        run_cpu_sample(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -32,6 +32,10 @@ CASES = {
     "static26": S.variant("7b_static26", name="stage_static26", temps=(0.0, 1.0), **_SMALL),
     "chain4": S.variant("7b_static26", name="stage_chain4", tree="chain4", top_k=1, depth=4, top_m=4,
                         temps=(0.0, 1.0), **_SMALL),
+    # six requests, some roots cut to fewer children than k: short expansion
+    # layers, whose unused slots stay inactive
+    "eagle2_short_layers": S.variant("7b_eagle2", name="stage_outcomes", temps=(0.0, 0.0, 0.0, 1.0, 1.0, 0.7),
+                                     **dict(_SMALL, batch=6)),
 }
 
 
@@ -92,7 +96,7 @@ def _oracle_tree(w, t_next, tok_b, q_b, n_layers):
 
 def _build(name):
     w = CASES[name]
-    seed = 5150 + sorted(CASES).index(name)
+    seed = 5200 if name == "eagle2_short_layers" else 5150 + sorted(CASES).index(name)
     inp = S.round_inputs(w, seed, device="cuda")
     eng, rd = make_round(w, inp)
     tok, q = _children(w, seed, rd.B, rd.E, rd.K, w.vocab)
@@ -189,3 +193,103 @@ def test_accept_stage_bit_exact(name):
         descended += a
     # the inputs make walks descend: the comparison covers more than the root
     assert descended > 0, name
+
+
+OUTCOME_CASE = S.variant("7b_eagle2", name="stage_outcomes", temps=(0.0, 0.0, 0.0, 1.0, 1.0, 0.7),
+                         **dict(_SMALL, batch=6))
+
+
+def _peak(V, tok):
+    row = np.zeros(V, dtype=np.float32)
+    row[tok] = 1.0
+    return row
+
+
+def _path_to(tr, s):
+    path = []
+    while s >= 0:
+        path.append(s)
+        s = tr.parent[s]
+    return path[::-1]
+
+
+def test_accept_outcomes_on_gpu():
+    """Acceptance outcomes of [B] "正确性与状态边界" each made to happen on the
+    GPU by target rows that put all their mass on one token (so every test's
+    result is fixed by construction), and each compared with the oracle:
+    greedy rejection at the root, rejection in the middle of a path, a path
+    accepted to a deepest leaf with the bonus token; under sampling a drawn
+    child that rerank pruned accepted as the final token, every candidate of
+    the root rejected with the final token from the residual, and a path
+    accepted to a deepest leaf."""
+    w = OUTCOME_CASE
+    seed = 5200
+    inp = S.round_inputs(w, seed, device="cuda")
+    eng, rd = make_round(w, inp)
+    tok, q = _children(w, seed, rd.B, rd.E, rd.K, w.vocab)
+    _gpu_tree(eng, rd, tok, q)
+    t_next = inp["t_next"].cpu().numpy()
+    refs = [_oracle_tree(w, t_next[b], tok[b], q[b], rd.plan.n_layers) for b in range(rd.B)]
+    V, Sn = w.vocab, rd.S
+    qrows, p_rand, _ = _accept_inputs(w, seed, rd, refs, tok)
+    p = p_rand.copy()
+    expect = {}
+    for b, (ex, tr, child_tok) in enumerate(refs):
+        kids = {s: [c for c in range(tr.size) if tr.parent[c] == s] for s in range(tr.size)}
+        drawn_tokens = lambda s: set(child_tok[tr.exp[s]]) if tr.exp[s] >= 0 else set()
+        not_child = lambda s: next(t for t in range(V) if t not in drawn_tokens(s))
+        deepest = max(range(tr.size), key=lambda s: (tr.depth[s], -s))
+        if b in (0, 4):                         # root rejection (greedy / every sampled candidate)
+            t = not_child(0)
+            p[b, 0] = _peak(V, t)
+            expect[b] = (0, [0], t)
+        elif b == 1:                            # middle rejection after two accepted nodes
+            mid = next(s for s in range(tr.size) if tr.depth[s] == 2 and kids[s])
+            path = _path_to(tr, mid)
+            for u, c in zip(path[:-1], path[1:]):
+                p[b, u] = _peak(V, tr.token[c])
+            t = not_child(mid)
+            p[b, mid] = _peak(V, t)
+            expect[b] = (2, path, t)
+        elif b in (2, 5):                       # all accepted down to a deepest leaf, bonus token there
+            path = _path_to(tr, deepest)
+            for u, c in zip(path[:-1], path[1:]):
+                p[b, u] = _peak(V, tr.token[c])
+            p[b, deepest] = _peak(V, 11)
+            expect[b] = (tr.depth[deepest], path, 11)
+        else:                                   # b == 3: an accepted candidate that rerank pruned
+            u, y = next((s, t) for s in range(tr.size) if tr.exp[s] >= 0
+                        for r, t in enumerate(child_tok[tr.exp[s]])
+                        if t >= 0 and tr.child_slot.get((tr.exp[s], r), -1) < 0)
+            path = _path_to(tr, u)
+            for a_, c in zip(path[:-1], path[1:]):
+                p[b, a_] = _peak(V, tr.token[c])
+            p[b, u] = _peak(V, y)
+            expect[b] = (tr.depth[u], path, y)
+    argmax = np.argmax(p, axis=-1).astype(np.int32)
+    temps = w.temps_for_batch()
+    rd.temps.copy_(torch.tensor(temps, dtype=torch.float32))
+    rd.set_sampling(inp["philox_seed"], inp["round_id"])
+    rd.probs.copy_(torch.from_numpy(qrows))
+    rd.target_probs.copy_(torch.from_numpy(p))
+    rd.target_argmax.copy_(torch.from_numpy(argmax))
+    st, ws = eng.stream(), eng.ws.data_ptr()
+    B.eagle_accept_from_probs(eng.ctx, rd.plan, rd.B, rd.tree_c, rd.children_c, _p(rd.target_probs),
+                              _p(rd.target_argmax), _p(rd.probs), rd.sampling_c, rd.acc_c, ws, st)
+    torch.cuda.synchronize()
+    assert B.eagle_read_device_status(eng.ctx, ws, st) == 0
+    for b, (_ex, tr, child_tok) in enumerate(refs):
+        if temps[b] <= 0:
+            want = Vf.accept_greedy(tr, p[b].astype(np.float64))
+        else:
+            want = Vf.accept_sampling(tr, p[b], qrows[b], child_tok, b, inp["philox_seed"], inp["round_id"])
+        got_a = int(rd.accept_len[b])
+        got = (got_a, rd.path[b, :got_a + 1].tolist(), int(rd.final_token[b]))
+        assert got == (want[0], list(want[1]), int(want[2])), (b, got, want)
+        assert got == (expect[b][0], list(expect[b][1]), expect[b][2]), (b, got, expect[b])
+        assert int(rd.last_slot[b]) == got[1][-1]
+    # the five outcomes all happened, under greedy and under sampling
+    assert expect[0][0] == 0 and expect[4][0] == 0
+    assert 0 < expect[1][0] and refs[1][1].children(expect[1][1][-1])
+    assert expect[2][0] == max(refs[2][1].depth) and not refs[2][1].children(expect[2][1][-1])
+    assert all(t != expect[3][2] for t in (refs[3][1].token[c] for c in refs[3][1].children(expect[3][1][-1])))

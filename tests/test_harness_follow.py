@@ -153,3 +153,18 @@ def test_follow_continues_after_a_flagged_choice():
     rep = compare_round(w, gpu, ref)
     assert not rep["ok"] and any("its own row selects" in e for e in rep["errors"]), rep["errors"]
     assert np.isfinite(rep["max_err"]["f_hat"])
+
+
+def test_flip_measure_matches_brute_force():
+    """The expected sampling flips per draw: the measure of uniforms on which
+    inverse-CDF draws over two nearby distributions differ."""
+    from tests.gpu_harness import _flip_measure
+    assert _flip_measure(np.array([0.2, 0.5, 1.0]), np.array([0.21, 0.5, 1.0])) == pytest.approx(0.01)
+    assert _flip_measure(np.array([0.2, 0.5, 1.0]), np.array([0.25, 0.45, 1.0])) == pytest.approx(0.1)
+    rng = np.random.default_rng(0)
+    q = rng.dirichlet(np.ones(50))
+    q2 = q * np.exp(rng.normal(0, 0.01, 50))
+    ca, cb = np.cumsum(q), np.cumsum(q2 / q2.sum())
+    u = rng.random(400000)
+    brute = np.mean(np.searchsorted(ca, u, side="right") != np.searchsorted(cb, u, side="right"))
+    assert _flip_measure(ca, cb) == pytest.approx(brute, abs=1e-3)
