@@ -27,7 +27,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 KERNEL_ID = {"all": -1, "gemm_fc": 0, "gemm_qkv": 1, "gemm_o": 2, "gemm_gateup": 3, "gemm_down": 4,
              "gemm_lm": 5, "draft_attn": 6, "select": 7, "tree": 8, "verify_attn": 9, "accept": 10,
-             "commit": 11, "prep": 12}
+             "commit": 11, "prep": 12, "refresh": 13}
 
 P = C.c_void_p
 I = C.c_int
@@ -149,6 +149,8 @@ def _declare(L):
         "eagle_trace_read": [P, C.POINTER(C.c_float), C.POINTER(I), I, C.POINTER(I)],
         "eagle_trace_disable": [P],
         "eagle_stamps_enable": [P, P, I],
+        "eagle_draft_refresh": [P, I, C.POINTER(eagle_draft_weights), C.POINTER(eagle_accept_out),
+                                C.POINTER(eagle_commit_out), P, C.POINTER(eagle_kv), P, P, P],
         "eagle_stamps_disable": [P, C.POINTER(I), I, C.POINTER(I)],
     }
     for name, args in sig.items():
@@ -166,7 +168,7 @@ EXPORTED = ["eagle_create", "eagle_destroy", "eagle_workspace_init", "eagle_read
             "eagle_tree_expand_rerank", "eagle_tree_verify_attn", "eagle_tree_verify_attn_noalloc",
             "eagle_accept", "eagle_accept_from_probs",
             "eagle_commit", "eagle_trace_enable", "eagle_trace_read", "eagle_trace_disable",
-            "eagle_stamps_enable", "eagle_stamps_disable", "eagle_launch_count"]
+            "eagle_stamps_enable", "eagle_stamps_disable", "eagle_draft_refresh", "eagle_launch_count"]
 
 
 def _check(name: str, code: int):
@@ -269,6 +271,12 @@ def eagle_commit(ctx, batch, acc, tree, f_true, k_tree_layers, v_tree_layers, k_
                               C.cast(arr(v_tree_layers), P), C.cast(arr(k_cache_layers), P),
                               C.cast(arr(v_cache_layers), P), kv_cap, target_kv_len, _ref(draft), _ref(draft_kv),
                               C.byref(out), ws_ptr, stream))
+
+
+def eagle_draft_refresh(ctx, batch, w, acc, cm, pos0, draft_kv, len_out, ws_ptr, stream):
+    _check("eagle_draft_refresh",
+           lib().eagle_draft_refresh(ctx, batch, C.byref(w), C.byref(acc), C.byref(cm), pos0, C.byref(draft_kv),
+                                     len_out, ws_ptr, stream))
 
 
 def eagle_trace_enable(ctx, kernel: str, capacity: int):

@@ -101,7 +101,7 @@ void layout(eagle_ctx* c) {
                            ceil_div(D.d_ff, 64), ceil_div(D.vocab, 128)});
   // split-tile partial slots t + cta: t < max_mtiles, cta < grid <= 2 * SMs
   W.gemm_part = take(static_cast<size_t>(W.max_mtiles + 2 * c->sm_count) * L.max_rows * 128 * 4);
-  W.gemm_cnt = take(static_cast<size_t>(6) * W.max_mtiles * 4);
+  W.gemm_cnt = take(static_cast<size_t>(N_EPI) * W.max_mtiles * 4);
   // partial records of the widest attention launch: b requests use
   // splits_bound(b * Hkv) + 1 records per query row; past the batch where
   // the splits reach 1 the count grows as 2b, so the largest batch covers
@@ -454,6 +454,44 @@ eagle_status eagle_draft_step(eagle_ctx* ctx, const eagle_plan* plan, int layer,
   return EAGLE_OK;
 }
 
+eagle_status eagle_draft_refresh(eagle_ctx* ctx, int batch, const eagle_draft_weights* w, const eagle_accept_out* acc,
+                                 const eagle_commit_out* cm, const int32_t* pos0, const eagle_kv* draft_kv,
+                                 int32_t* len_out, void* workspace, cudaStream_t stream) {
+  EAGLE_REQUIRE(ctx, EAGLE_ERR_INVALID_ARG);
+  EAGLE_REQUIRE(batch >= 1 && batch <= ctx->lim.max_batch, EAGLE_ERR_CAPACITY);
+  eagle_status st = check_weights(ctx, w);
+  if (st != EAGLE_OK) return st;
+  EAGLE_REQUIRE(acc && cm, EAGLE_ERR_INVALID_ARG);
+  EAGLE_PTR(acc->accept_len);
+  EAGLE_REQUIRE(acc->path_cap >= 2, EAGLE_ERR_SHAPE);
+  EAGLE_PTR(cm->f_commit); EAGLE_PTR(cm->tok_commit);
+  EAGLE_PTR(pos0);
+  if ((st = check_kv(ctx, draft_kv)) != EAGLE_OK) return st;
+  EAGLE_PTR(len_out);
+  EAGLE_REQUIRE(len_out != draft_kv->len, EAGLE_ERR_INVALID_ARG);
+  if ((st = check_ws(workspace)) != EAGLE_OK) return st;
+  const int R = acc->path_cap - 1;
+  EAGLE_REQUIRE(static_cast<long long>(batch) * R <= ctx->lim.max_rows, EAGLE_ERR_CAPACITY);
+  eagle_requests req{};
+  req.pos0 = pos0;
+  DraftLaunch L{};
+  L.batch = batch;
+  L.rpr = R;
+  L.e0 = 0;
+  L.n = batch * R;
+  L.NP = padded_rows(L.n);
+  L.k = 1;
+  L.w = w;
+  L.req = &req;
+  L.ws = workspace;
+  L.refresh_kv = draft_kv;
+  L.refresh_n = acc->accept_len;
+  EAGLE_CUDA(launch_prep_refresh(ctx, L, cm->f_commit, cm->tok_commit, acc->path_cap, len_out, stream));
+  EAGLE_CUDA(launch_gemm(ctx, EPI_FC, L, stream));
+  EAGLE_CUDA(launch_gemm(ctx, EPI_KV, L, stream));
+  return EAGLE_OK;
+}
+
 eagle_status eagle_tree_expand_rerank(eagle_ctx* ctx, const eagle_plan* plan, int phase, int layer, int batch,
                                       const eagle_requests* req, const eagle_children* children,
                                       const eagle_pool* pool, const eagle_tree* tree, void* workspace,
@@ -611,7 +649,7 @@ eagle_status eagle_commit(eagle_ctx* ctx, int batch, const eagle_accept_out* acc
 }
 
 eagle_status eagle_trace_enable(eagle_ctx* ctx, int kernel_id, int capacity) {
-  EAGLE_REQUIRE(ctx && capacity >= 1 && kernel_id >= -1 && kernel_id <= EAGLE_K_PREP, EAGLE_ERR_INVALID_ARG);
+  EAGLE_REQUIRE(ctx && capacity >= 1 && kernel_id >= -1 && kernel_id <= EAGLE_K_REFRESH, EAGLE_ERR_INVALID_ARG);
   TraceState& t = ctx->trace;
   while (static_cast<int>(t.events.size()) < 2 * capacity) {
     cudaEvent_t e;

@@ -61,6 +61,69 @@ __global__ void prep_fc_kernel(const float* __restrict__ f_last, const float* __
   *reinterpret_cast<uint4*>(bfc + static_cast<size_t>(NP + j) * kp + c0) = lv;
 }
 
+// Draft-cache refresh rows ([B] "KV Cache 必须按事务提交": the drafter
+// continues from the committed path; [A] §6.2 closing remark): row
+// j = b * R + i - 1 (i = 1 .. R) is x = [f_commit[b][i-1] ; E[tok_commit[b][i]]]
+// -- the true feature of accepted position i - 1 and the token at position
+// i -- when i <= accept_len[b], else zero.  Same operand layout as
+// prep_fc_kernel.  The first thread of each request also writes its new
+// cache length (len + a when the cache takes all a rows, else len, with
+// EAGLE_ERR_CAPACITY).
+__global__ void prep_refresh_kernel(const float* __restrict__ f_commit, const int32_t* __restrict__ tok_commit,
+                                    const int32_t* __restrict__ n_act, const int32_t* __restrict__ kv_len, int kv_cap,
+                                    int32_t* __restrict__ len_out, int path_cap, int R,
+                                    const uint16_t* __restrict__ embed, int ld_embed, int d, int V, int NP, int kp,
+                                    uint16_t* __restrict__ bfc, int* status, uint64_t* stamp) {
+  const LaunchStamp ls(stamp);
+  pdl_trigger();
+  pdl_wait();      // the acceptance and commit outputs are visible from here on
+  ls.waited();
+  const int j = blockIdx.x;
+  const int b = j / R, i = j % R + 1;
+  const int a = min(max(n_act[b], 0), R);
+  if (i == 1 && blockIdx.y == 0 && threadIdx.x == 0) {
+    const int len = kv_len[b];
+    const bool room = len >= 0 && len + a <= kv_cap;
+    len_out[b] = room ? len + a : len;
+    if (!room) set_status(status, EAGLE_ERR_CAPACITY);
+  }
+  const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
+  if (c0 >= 2 * d) return;
+  int tok = i <= a ? tok_commit[static_cast<size_t>(b) * (path_cap + 1) + i] : -1;
+  if (tok >= V) {
+    if (c0 == 0) set_status(status, EAGLE_ERR_INVALID_ARG);
+    tok = -1;
+  }
+  float x[8];
+  if (tok < 0) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u) x[u] = 0.f;
+  } else if (c0 < d) {
+    const float* feat = f_commit + (static_cast<size_t>(b) * path_cap + (i - 1)) * d;
+    const float4 f0 = *reinterpret_cast<const float4*>(feat + c0);
+    const float4 f1 = *reinterpret_cast<const float4*>(feat + c0 + 4);
+    x[0] = f0.x; x[1] = f0.y; x[2] = f0.z; x[3] = f0.w; x[4] = f1.x; x[5] = f1.y; x[6] = f1.z; x[7] = f1.w;
+  } else {
+    const uint4 r = *reinterpret_cast<const uint4*>(embed + static_cast<size_t>(tok) * ld_embed + (c0 - d));
+    const uint32_t wv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      x[2 * u] = __uint_as_float(wv[u] << 16);
+      x[2 * u + 1] = __uint_as_float(wv[u] & 0xffff0000u);
+    }
+  }
+  uint16_t h[8], l[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) split_bf16(x[u], h[u], l[u]);
+  uint4 hv, lv;
+  hv.x = h[0] | (uint32_t(h[1]) << 16); hv.y = h[2] | (uint32_t(h[3]) << 16);
+  hv.z = h[4] | (uint32_t(h[5]) << 16); hv.w = h[6] | (uint32_t(h[7]) << 16);
+  lv.x = l[0] | (uint32_t(l[1]) << 16); lv.y = l[2] | (uint32_t(l[3]) << 16);
+  lv.z = l[4] | (uint32_t(l[5]) << 16); lv.w = l[6] | (uint32_t(l[7]) << 16);
+  *reinterpret_cast<uint4*>(bfc + static_cast<size_t>(j) * kp + c0) = hv;
+  *reinterpret_cast<uint4*>(bfc + static_cast<size_t>(NP + j) * kp + c0) = lv;
+}
+
 // select: a cluster of SEL_CL CTAs per row, each CTA one contiguous
 // SEL_THREADS * SEL_PER slice of the vocabulary, SEL_PER consecutive logits
 // per thread held in registers.  Row max, sum, top-k candidates and sampling
@@ -386,6 +449,21 @@ cudaError_t launch_prep_fc(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st
                  ws_ptr<uint16_t>(L.ws, ctx->ws.b_fc), stamp);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_PREP, st);
+  return e;
+}
+
+cudaError_t launch_prep_refresh(eagle_ctx* ctx, const DraftLaunch& L, const float* f_commit,
+                                const int32_t* tok_commit, int path_cap, int32_t* len_out, cudaStream_t st) {
+  const eagle_dims& D = ctx->dims;
+  const dim3 grid(L.n, ceil_div(2 * D.d / 8, 128));
+  uint64_t* stamp = stamp_slot(ctx, EAGLE_K_REFRESH);
+  trace_before(ctx, EAGLE_K_REFRESH, st);
+  const cudaError_t e =
+      launch_pdl(prep_refresh_kernel, grid, dim3(128), 0, st, f_commit, tok_commit, L.refresh_n, L.refresh_kv->len,
+                 L.refresh_kv->cap, len_out, path_cap, L.rpr, L.w->embed, L.w->ld_embed, D.d, D.vocab, L.NP,
+                 ctx->ws.kp_fc, ws_ptr<uint16_t>(L.ws, ctx->ws.b_fc), ws_ptr<int>(L.ws, ctx->ws.status), stamp);
+  ctx->launches++;
+  trace_after(ctx, EAGLE_K_REFRESH, st);
   return e;
 }
 

@@ -85,6 +85,12 @@ struct GemmParams {
   int* counters;
   int* status;
   uint64_t* stamp;
+  // EPI_KV (draft-cache refresh): bf16 cache [B][kv_cap_rows][Hkv][dh]
+  uint16_t* kc;
+  uint16_t* vc;
+  int kv_cap_rows;
+  const int32_t* kv_len;
+  const int32_t* n_act;
 };
 
 struct Smem {
@@ -256,13 +262,13 @@ struct EpiCol {
 __device__ __noinline__ EpiCol epi_column(const GemmParams& p, int t, int m) {
   EpiCol c;
   c.gi = t * BM + m;
-  c.qd = p.Hq * p.dh;
+  c.qd = p.epi == EPI_KV ? 0 : p.Hq * p.dh;   // the refresh projects K and V only
   c.kd = p.Hkv * p.dh;
   const int half = p.dh >> 1;
   c.rope = false; c.is_v = false; c.rot_first = false;
   c.head = 0; c.di = 0; c.partner = m;
   c.f_hi = 0.f; c.f_lo = 0.f;          // inverse frequency as an unevaluated float pair
-  if (p.epi == EPI_QKV && c.gi < c.qd + 2 * c.kd) {
+  if ((p.epi == EPI_QKV || p.epi == EPI_KV) && c.gi < c.qd + 2 * c.kd) {
     c.is_v = c.gi >= c.qd + c.kd;
     const int base = c.gi < c.qd ? 0 : (c.gi < c.qd + c.kd ? c.qd : c.qd + c.kd);
     c.head = (c.gi - base) / p.dh;
@@ -294,7 +300,7 @@ __device__ __noinline__ void stage_row_inputs(const GemmParams& p, const Smem& s
       const int r = i / (BM / 4), q = 4 * (i % (BM / 4));
       if (q < ncol) cp_async16(s.stg2 + r * BM + q, p.resid + static_cast<size_t>(jc + r) * p.d + t * BM + q);
     }
-  } else if (p.epi == EPI_QKV || p.epi == EPI_GATEUP) {           // norm partials of rows jc..jc+nj-1
+  } else if (p.epi == EPI_QKV || p.epi == EPI_GATEUP || p.epi == EPI_KV) {   // norm partials of rows jc..jc+nj-1
     const float* ss = p.ss_in + static_cast<size_t>(jc) * tiles;
     if (tiles % 4 == 0) {
       stage_block(s.stg2, ss, nj * tiles, et);
@@ -304,6 +310,15 @@ __device__ __noinline__ void stage_row_inputs(const GemmParams& p, const Smem& s
     if (p.epi == EPI_QKV && m < nj) {
       const int j = jc + m, b = j / p.rpr, e = p.e0 + j % p.rpr;
       s.rowi[m] = p.pos0[b] + p.depth[static_cast<size_t>(b) * p.E + e];
+    }
+    if (p.epi == EPI_KV && m < nj) {
+      // refresh row (b, i): position pos0[b] + i, cache row len[b] + i - 1;
+      // all of a request's rows or none (the cache must take them all)
+      const int j = jc + m, b = j / p.rpr, i = j % p.rpr + 1;
+      const int len = p.kv_len[b], a = min(max(p.n_act[b], 0), p.rpr);
+      const bool room = len >= 0 && len + a <= p.kv_cap_rows;
+      s.rowi[m] = p.pos0[b] + i;
+      s.rowi[XCH_ROWS + m] = (i <= a && room) ? len + i - 1 : -1;
     }
   }
 }
@@ -333,7 +348,7 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
 #pragma unroll 1
     for (int jj = 0; jj < nj; ++jj) xch[jj * BM + m] += stg2[jj * BM + m];
   }
-  if ((p.epi == EPI_QKV || p.epi == EPI_GATEUP) && m < nj) {      // RMSNorm scale of input row jc + m
+  if ((p.epi == EPI_QKV || p.epi == EPI_GATEUP || p.epi == EPI_KV) && m < nj) {   // RMSNorm scale of input row jc + m
     const float* ss = stg2 + m * tiles;
     float acc4[4] = {0.f, 0.f, 0.f, 0.f};
     int i = 0;
@@ -405,6 +420,26 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
           qrow[static_cast<size_t>(j) * qd + gi] = v;
         else
           dst[((static_cast<size_t>(b) * E + e) * Hkv + head) * dh + di] = v;
+      }
+    }
+  } else if (p.epi == EPI_KV) {
+    if (gi < 2 * kd) {
+      uint16_t* const dst = is_v ? p.vc : p.kc;
+      const int rpr = p.rpr, Hkv = p.Hkv, dh = p.dh, cap = p.kv_cap_rows;
+#pragma unroll 1
+      for (int jj = 0; jj < nj; ++jj) {
+        const int row = rowi[XCH_ROWS + jj];
+        if (row < 0) continue;                 // inactive row, or the cache cannot take the request's rows
+        const int b = (jc + jj) / rpr;
+        const float sc = rs[jj];
+        float v = xch[jj * BM + m] * sc;
+        if (rope) {
+          float sn, cs;
+          sincosf(rope_angle(rowi[jj], f_hi, f_lo), &sn, &cs);
+          const float other = xch[jj * BM + partner] * sc;
+          v = rot_first ? v * cs - other * sn : v * cs + other * sn;
+        }
+        dst[((static_cast<size_t>(b) * cap + row) * Hkv + head) * dh + di] = f32_to_bf16(v);
       }
     }
   } else if (p.epi == EPI_GATEUP) {
@@ -943,13 +978,23 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
       p.out_f32 = L.out->f_hat;
       p.bnext = ws_ptr<uint16_t>(L.ws, W.b_lm); p.kp_next = W.kp_lm;
       break;
+    case EPI_KV:
+      mats[0] = w->wk; rows[0] = kd; lds[0] = w->ld_k;
+      mats[1] = w->wv; rows[1] = kd; lds[1] = w->ld_v;
+      K = D.d; b_in = W.b_qkv; kp_in = W.kp_qkv; n_out = 2 * kd;
+      p.ss_in = ws_ptr<float>(L.ws, W.ss_fc); p.ss_in_tiles = tiles_d;
+      p.pos0 = L.req->pos0;
+      p.kc = L.refresh_kv->k; p.vc = L.refresh_kv->v;
+      p.kv_cap_rows = L.refresh_kv->cap; p.kv_len = L.refresh_kv->len;
+      p.n_act = L.refresh_n;
+      break;
     default:  // EPI_LM
       mats[0] = w->w_lm; rows[0] = D.vocab; lds[0] = w->ld_lm; K = D.d;
       b_in = W.b_lm; kp_in = W.kp_lm; n_out = D.vocab;
       p.out_f32 = L.out->logits;
       break;
   }
-  p.n_mats = epi == EPI_QKV ? 3 : (epi == EPI_GATEUP ? 2 : 1);
+  p.n_mats = epi == EPI_QKV ? 3 : (epi == EPI_GATEUP || epi == EPI_KV ? 2 : 1);
   int cum = 0;
   for (int i = 0; i < p.n_mats; ++i) {
     cum += ceil_div(rows[i], 64);
@@ -1012,12 +1057,13 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   // partial slots t + cta of split tiles stay inside the workspace's array
   if (p.sk_tiles > 0 && p.sk_tiles - 1 + grid - 1 >= W.max_mtiles + 2 * ctx->sm_count)
     return cudaErrorInvalidConfiguration;
-  p.stamp = stamp_slot(ctx, epi);
-  trace_before(ctx, epi, st);
+  const int kid = epi == EPI_KV ? static_cast<int>(EAGLE_K_REFRESH) : epi;
+  p.stamp = stamp_slot(ctx, kid);
+  trace_before(ctx, kid, st);
   const cudaError_t e = launch_pdl(gemm_stream_kernel, dim3(grid), dim3(NUM_THREADS), smem, st, maps[0], maps[1],
                                    maps[2], tails[0], tails[1], tails[2], mb, p);
   ctx->launches++;
-  trace_after(ctx, epi, st);
+  trace_after(ctx, kid, st);
   return e;
 }
 

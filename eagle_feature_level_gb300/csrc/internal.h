@@ -16,8 +16,10 @@ namespace eagle {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// GEMM epilogue kinds (one per contraction of the draft step).
-enum Epi : int { EPI_FC = 0, EPI_QKV = 1, EPI_O = 2, EPI_GATEUP = 3, EPI_DOWN = 4, EPI_LM = 5 };
+// GEMM epilogue kinds (one per contraction of the draft step, and the K/V
+// projection of the draft-cache refresh).
+enum Epi : int { EPI_FC = 0, EPI_QKV = 1, EPI_O = 2, EPI_GATEUP = 3, EPI_DOWN = 4, EPI_LM = 5, EPI_KV = 6 };
+constexpr int N_EPI = 7;
 
 // Activation rows are padded to NP; the GEMM's B operand holds the bf16 "hi"
 // parts in rows [0, NP) and the "lo" parts in rows [NP, 2NP).  NP is a
@@ -37,7 +39,7 @@ struct Workspace {
   size_t qrow;                   // fp32 [max_rows][Hq*dh]
   size_t ss_fc, ss_o;            // fp32 [max_rows][tiles of d]
   size_t gemm_part;              // fp32 [(max_mtiles + 2 * SMs) * max_rows * 128]
-  size_t gemm_cnt;               // int [6][max_mtiles]
+  size_t gemm_cnt;               // int [N_EPI][max_mtiles]
   size_t attn_part;              // fp32 partial (m, l, acc[dh]) records
   size_t attn_cnt;               // int [2][max_batch * Hkv]
   size_t accept_scratch;         // u64 [max_batch][V] current acceptance weights
@@ -138,12 +140,19 @@ struct DraftLaunch {
   const eagle_children* children;
   const eagle_sampling* s;
   void* ws;
+  // draft-cache refresh (EPI_KV): rows j = b * rpr + i - 1 for i = 1 .. rpr
+  const eagle_kv* refresh_kv;     // cache; row of (b, i) = len[b] + i - 1
+  const int32_t* refresh_n;       // [B] active rows of request b
 };
 
 cudaError_t launch_prep_fc(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st);
 cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStream_t st);
 cudaError_t launch_draft_attn(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st);
 cudaError_t launch_select(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st);
+// Gathers the refresh rows [f_commit[b][i-1] ; E[tok_commit[b][i]]] into the
+// FC operand and writes len_out = len + active rows.
+cudaError_t launch_prep_refresh(eagle_ctx* ctx, const DraftLaunch& L, const float* f_commit,
+                                const int32_t* tok_commit, int path_cap, int32_t* len_out, cudaStream_t st);
 
 cudaError_t launch_tree(eagle_ctx* ctx, const eagle_plan* plan, int phase, int layer, int batch,
                         const eagle_requests* req, const eagle_children* ch, const eagle_pool* pool,

@@ -175,6 +175,7 @@ class Round:
         self.f_commit = z(batch, self.path_cap, d, **f32)
         self.t_next_out = z(batch, **i32)
         self.draft_len_out = z(batch, **i32)
+        self.draft_len_next = z(batch, **i32)    # after the draft-cache refresh
         self.seed, self.round_id = 0, 0
         self._structs()
 
@@ -233,6 +234,28 @@ class Round:
                        [_p(t) for t in self.tree_k], [_p(t) for t in self.tree_v],
                        [_p(t) for t in self.tgt_k], [_p(t) for t in self.tgt_v], self.kv_cap, _p(self.tgt_len),
                        self.out_c, self.draft_kv_c, self.commit_c, e.ws.data_ptr(), e.stream())
+
+    def refresh(self, w_c: B.eagle_draft_weights):
+        """Append the draft layer's K/V of the accepted path (from the
+        committed true features) after the root row commit appended:
+        draft_len_next = draft_len_out + accept_len."""
+        e = self.eng
+        kv = B.eagle_kv(_p(self.draft_k), _p(self.draft_v), self.kv_cap, _p(self.draft_len_out))
+        B.eagle_draft_refresh(e.ctx, self.B, w_c, self.acc_c, self.commit_c, _p(self.pos0), kv,
+                              _p(self.draft_len_next), e.ws.data_ptr(), e.stream())
+
+    def advance(self):
+        """Make the committed state the next round's input by exchanging
+        buffers (nothing is copied): t_next <- final token, f_last <- the
+        last accepted slot's true feature, root position and target cache
+        length <- the new prefix length, draft cache length <- the length
+        after the refresh."""
+        self.t_next, self.t_next_out = self.t_next_out, self.t_next
+        self.f_last, self.f_last_out = self.f_last_out, self.f_last
+        self.pos0, self.prefix_len_out = self.prefix_len_out, self.pos0
+        self.tgt_len = self.pos0                 # both equal the prefix length
+        self.draft_len, self.draft_len_next = self.draft_len_next, self.draft_len
+        self._structs()
 
     def capture(self, w_c: B.eagle_draft_weights) -> "torch.cuda.CUDAGraph":
         """Capture one whole round (target logits already in place) as a CUDA

@@ -17,6 +17,7 @@ def limits_for(w):
     else:
         plan = R.plan_for(w.tree)
         rows = w.batch * max(plan.layer_rows[l] for l in range(plan.n_layers))
+    rows = max(rows, w.batch * w.depth)     # the draft-cache refresh of a whole accepted path
     return dict(max_batch=w.batch, max_rows=rows, max_expanded=S.max_expanded(w), max_children=w.top_k,
                 max_tree=1 + w.top_m)
 

@@ -411,6 +411,34 @@ eagle_status eagle_commit(eagle_ctx* ctx, int batch, const eagle_accept_out* acc
                           const eagle_draft_out* draft, const eagle_kv* draft_kv,
                           const eagle_commit_out* out, void* workspace, cudaStream_t stream);
 
+/* eagle_draft_refresh -- the draft layer's K/V of the accepted path's
+ * positions, computed from the target's true features, appended to the
+ * draft cache: after a round the drafter continues from the committed path,
+ * not from its own drafted features ([B] "KV Cache 必须按事务提交"; [A] §6.2
+ * closing remark; [C] "工程落地时真正要看什么").  With the round's root at
+ * position L_b = pos0[b] and a = acc.accept_len[b] accepted nodes, for
+ * i = 1 .. a (at most acc.path_cap - 1):
+ *   x = [cm.f_commit[b][i-1] ; E[cm.tok_commit[b][i]]]   (true feature of
+ *       position L_b + i - 1, token at position L_b + i)
+ *   k, v = RoPE(W_{k,v} RMSNorm(W_fc x + b_fc; g1)) at position L_b + i
+ * go (bf16) to draft_kv rows draft_kv.len[b] + i - 1, and
+ * len_out[b] = draft_kv.len[b] + a.  The root's own row (position L_b) was
+ * appended by eagle_commit, so pass draft_kv.len = that call's
+ * cm.draft_len; the next round's root row (the final token at L_b + a + 1)
+ * comes from its own first draft step.  Run once over a prompt (f_commit =
+ * the prompt's features, tok_commit = its tokens, accept_len = rows) it
+ * fills the draft cache for a new request.
+ * Layouts: cm.f_commit [B][acc.path_cap][d] fp32, cm.tok_commit
+ * [B][acc.path_cap + 1]; batch * (acc.path_cap - 1) <= max_rows
+ * (EAGLE_ERR_CAPACITY).  A request whose cache cannot take its a rows
+ * writes none and keeps its length (EAGLE_ERR_CAPACITY in the status word).
+ * len_out must not alias draft_kv.len (EAGLE_ERR_INVALID_ARG).  Streams the
+ * FC and the K / V projection weights once. */
+eagle_status eagle_draft_refresh(eagle_ctx* ctx, int batch, const eagle_draft_weights* w,
+                                 const eagle_accept_out* acc, const eagle_commit_out* cm, const int32_t* pos0,
+                                 const eagle_kv* draft_kv, int32_t* len_out, void* workspace,
+                                 cudaStream_t stream);
+
 /* ---- measurement --------------------------------------------------------- */
 
 /* Kernel timing hook: while enabled, the library records a CUDA event before
@@ -421,7 +449,7 @@ typedef enum {
   EAGLE_K_ALL = -1, EAGLE_K_GEMM_FC = 0, EAGLE_K_GEMM_QKV = 1, EAGLE_K_GEMM_O = 2,
   EAGLE_K_GEMM_GATEUP = 3, EAGLE_K_GEMM_DOWN = 4, EAGLE_K_GEMM_LM = 5, EAGLE_K_DRAFT_ATTN = 6,
   EAGLE_K_SELECT = 7, EAGLE_K_TREE = 8, EAGLE_K_VERIFY_ATTN = 9, EAGLE_K_ACCEPT = 10,
-  EAGLE_K_COMMIT = 11, EAGLE_K_PREP = 12
+  EAGLE_K_COMMIT = 11, EAGLE_K_PREP = 12, EAGLE_K_REFRESH = 13
 } eagle_kernel_id;
 eagle_status eagle_trace_enable(eagle_ctx* ctx, int kernel_id, int capacity);
 /* Synchronises the recorded events; writes up to `cap` durations in ms, the

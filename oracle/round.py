@@ -137,6 +137,19 @@ def draft_tree(W, w, b: int, inp: dict, guide=None) -> (RequestDraft, T.Tree):
     return st, tr
 
 
+def draft_refresh_rows(W: DraftWeights, dims, feats: np.ndarray, tokens, positions):
+    """The draft layer's K/V of committed positions, from true features (Page
+    B "KV Cache 必须按事务提交": after a round the drafter continues from the
+    committed path; Page A §6.2 closing remark: the accepted path's true
+    features replace the drafted ones).  Row i: x = [f_{p-1} ; e(t_p)] at
+    position p; returns k, v [n, Hkv, dh] after RoPE, as the draft layer
+    would store them for those positions."""
+    h = fc_rows(W, np.asarray(feats, dtype=np.float64), list(tokens))
+    a = rmsnorm(h, W.g1, dims.rms_eps)
+    _, k, v = qkv_rows(W, a, list(positions), dims)
+    return k, v
+
+
 def synthetic_target_logits(st: RequestDraft, tr: T.Tree, noise: np.ndarray,
                             fresh: np.ndarray) -> np.ndarray:
     rows = []

@@ -64,16 +64,25 @@ def run_gpu_round(w, seed, device="cuda", weights=None, inputs=None):
     W = weights if weights is not None else S.draft_weights(w, seed, device=device)
     inp = inputs if inputs is not None else S.round_inputs(w, seed, device=device)
     eng, rd = make_round(w, inp, device)
-    rd.run(eng.weights(W), target_fn=standin(inp))
+    inputs_cpu = {k: (v.detach().to("cpu") if torch.is_tensor(v) else v) for k, v in inp.items()}
+    out = round_on(eng, rd, eng.weights(W), inp, inputs_cpu)
+    out["weights_cpu"] = {k: v.detach().to("cpu") for k, v in W.items()}
+    eng.close()
+    return out
+
+
+def round_on(eng, rd, w_c, inp, inputs_cpu):
+    """One round on an existing Round (the synthetic target built from the
+    round's own draft logits); returns the GPU fields, the status and the
+    given host copy of the round's inputs."""
+    rd.run(w_c, target_fn=standin(inp))
     torch.cuda.synchronize()
     status = eng.status()
     out = {k: getattr(rd, k).detach().to("cpu") for k in GPU_FIELDS}
     out["tgt_k_after"] = rd.tgt_k[0].detach().to("cpu")
     out["status"] = status
     out["launches"] = R.B.eagle_launch_count(eng.ctx)
-    out["inputs_cpu"] = {k: (v.detach().to("cpu") if torch.is_tensor(v) else v) for k, v in inp.items()}
-    out["weights_cpu"] = {k: v.detach().to("cpu") for k, v in W.items()}
-    eng.close()
+    out["inputs_cpu"] = inputs_cpu
     return out
 
 

@@ -44,3 +44,19 @@ def test_round_state_is_consistent(name):
         # q rows are distributions
         for e, q in r["draft"].q.items():
             assert abs(q.sum() - 1.0) < 1e-12
+
+
+def test_refresh_rows_are_the_draft_layers_kv_of_those_rows():
+    """draft_refresh_rows gives, for a row (feature, token, position), the
+    K/V the draft step computes for a node with that parent feature, token
+    and position: the root row of a round is one."""
+    import eagle_synth as S
+    from oracle.layer import DraftWeights
+    from oracle.round import draft_refresh_rows, draft_tree, numpy_inputs
+    w = S.WORKLOADS["tiny_fp32"]
+    seed = S.WORKLOAD_SEEDS["tiny_fp32"]
+    Wd = DraftWeights(S.draft_weights(w, seed), w)
+    inp = numpy_inputs(S.round_inputs(w, seed))
+    st, _ = draft_tree(Wd, w, 0, inp)
+    k, v = draft_refresh_rows(Wd, w, inp["f_last"][:1], [inp["t_next"][0]], [inp["prefix_len"][0]])
+    assert np.array_equal(k[0], st.k_tree[0]) and np.array_equal(v[0], st.v_tree[0])
