@@ -257,6 +257,30 @@ class Round:
         self.draft_len, self.draft_len_next = self.draft_len_next, self.draft_len
         self._structs()
 
+    def set_plan(self, plan: B.eagle_plan):
+        """Switch to another tree budget whose shapes fit this round's buffers
+        (depth, retained nodes, expanded slots, children per node)."""
+        if (plan.depth + 1 > self.path_cap or plan.top_m + 1 > self.S or plan.n_expanded > self.E
+                or plan.top_k > self.K):
+            raise ValueError("plan does not fit the round's buffers")
+        self.plan = plan
+
+    def capture_segments(self, w_c: B.eagle_draft_weights, refresh: bool = False):
+        """The round as two CUDA graphs around the target model: (draft,
+        tree, verification attention) and (acceptance, commit[, refresh]).
+        A server replays the first, runs its target over the tree, then the
+        second.  Run the round eagerly once first."""
+        pre, post = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pre):
+            self.draft_and_tree(w_c)
+            self.verify()
+        with torch.cuda.graph(post):
+            self.accept()
+            self.commit()
+            if refresh:
+                self.refresh(w_c)
+        return pre, post
+
     def capture(self, w_c: B.eagle_draft_weights) -> "torch.cuda.CUDAGraph":
         """Capture one whole round (target logits already in place) as a CUDA
         graph; replaying it re-issues the same kernels with no host work.
