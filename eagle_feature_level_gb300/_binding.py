@@ -27,7 +27,7 @@ STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 KERNEL_ID = {"all": -1, "gemm_fc": 0, "gemm_qkv": 1, "gemm_o": 2, "gemm_gateup": 3, "gemm_down": 4,
              "gemm_lm": 5, "draft_attn": 6, "select": 7, "tree": 8, "verify_attn": 9, "accept": 10,
-             "commit": 11, "prep": 12, "refresh": 13}
+             "commit": 11, "prep": 12, "refresh": 13, "fuse": 14}
 
 P = C.c_void_p
 I = C.c_int
@@ -149,6 +149,7 @@ def _declare(L):
         "eagle_trace_read": [P, C.POINTER(C.c_float), C.POINTER(I), I, C.POINTER(I)],
         "eagle_trace_disable": [P],
         "eagle_stamps_enable": [P, P, I],
+        "eagle_fuse_features": [P, P, I, P, I, P, P, P, P],
         "eagle_draft_refresh": [P, I, C.POINTER(eagle_draft_weights), C.POINTER(eagle_accept_out),
                                 C.POINTER(eagle_commit_out), P, C.POINTER(eagle_kv), P, P, P],
         "eagle_stamps_disable": [P, C.POINTER(I), I, C.POINTER(I)],
@@ -168,7 +169,8 @@ EXPORTED = ["eagle_create", "eagle_destroy", "eagle_workspace_init", "eagle_read
             "eagle_tree_expand_rerank", "eagle_tree_verify_attn", "eagle_tree_verify_attn_noalloc",
             "eagle_accept", "eagle_accept_from_probs",
             "eagle_commit", "eagle_trace_enable", "eagle_trace_read", "eagle_trace_disable",
-            "eagle_stamps_enable", "eagle_stamps_disable", "eagle_draft_refresh", "eagle_launch_count"]
+            "eagle_stamps_enable", "eagle_stamps_disable", "eagle_draft_refresh", "eagle_fuse_features",
+            "eagle_launch_count"]
 
 
 def _check(name: str, code: int):
@@ -271,6 +273,11 @@ def eagle_commit(ctx, batch, acc, tree, f_true, k_tree_layers, v_tree_layers, k_
                               C.cast(arr(v_tree_layers), P), C.cast(arr(k_cache_layers), P),
                               C.cast(arr(v_cache_layers), P), kv_cap, target_kv_len, _ref(draft), _ref(draft_kv),
                               C.byref(out), ws_ptr, stream))
+
+
+def eagle_fuse_features(ctx, w_fuse, ld_fuse, b_fuse, n_rows, lmh, g_out, ws_ptr, stream):
+    _check("eagle_fuse_features",
+           lib().eagle_fuse_features(ctx, w_fuse, ld_fuse, b_fuse or None, n_rows, lmh, g_out, ws_ptr, stream))
 
 
 def eagle_draft_refresh(ctx, batch, w, acc, cm, pos0, draft_kv, len_out, ws_ptr, stream):

@@ -77,6 +77,7 @@ void layout(eagle_ctx* c) {
   W.kp_qkv = W.kp_gu = W.kp_lm = r64(D.d);
   W.kp_o = r64(D.n_q_heads * D.head_dim);
   W.kp_down = r64(D.d_ff);
+  W.kp_fuse = r64(3 * D.d);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -91,6 +92,7 @@ void layout(eagle_ctx* c) {
   W.b_gu = take(np2 * W.kp_gu * 2);
   W.b_down = take(np2 * W.kp_down * 2);
   W.b_lm = take(np2 * W.kp_lm * 2);
+  W.b_fuse = take(np2 * W.kp_fuse * 2);
   W.h = take(static_cast<size_t>(L.max_rows) * D.d * 4);
   W.h2 = take(static_cast<size_t>(L.max_rows) * D.d * 4);
   W.qrow = take(static_cast<size_t>(L.max_rows) * D.n_q_heads * D.head_dim * 4);
@@ -492,6 +494,33 @@ eagle_status eagle_draft_refresh(eagle_ctx* ctx, int batch, const eagle_draft_we
   return EAGLE_OK;
 }
 
+eagle_status eagle_fuse_features(eagle_ctx* ctx, const uint16_t* w_fuse, int ld_fuse, const float* b_fuse, int n_rows,
+                                 const float* lmh, float* g_out, void* workspace, cudaStream_t stream) {
+  EAGLE_REQUIRE(ctx, EAGLE_ERR_INVALID_ARG);
+  EAGLE_PTR(w_fuse);
+  EAGLE_REQUIRE(ld_fuse >= 3 * ctx->dims.d, EAGLE_ERR_SHAPE);
+  EAGLE_REQUIRE(ld_fuse % 8 == 0, EAGLE_ERR_ALIGN);
+  if (b_fuse) EAGLE_PTR(b_fuse);
+  EAGLE_REQUIRE(n_rows >= 1 && n_rows <= ctx->lim.max_rows, EAGLE_ERR_CAPACITY);
+  EAGLE_PTR(lmh); EAGLE_PTR(g_out);
+  eagle_status st = check_ws(workspace);
+  if (st != EAGLE_OK) return st;
+  DraftLaunch L{};
+  L.batch = 1;
+  L.rpr = n_rows;
+  L.n = n_rows;
+  L.NP = padded_rows(n_rows);
+  L.k = 1;
+  L.ws = workspace;
+  L.w_fuse = w_fuse;
+  L.ld_fuse = ld_fuse;
+  L.b_fuse = b_fuse;
+  L.g_out = g_out;
+  EAGLE_CUDA(launch_prep_fuse(ctx, L, lmh, stream));
+  EAGLE_CUDA(launch_gemm(ctx, EPI_FUSE, L, stream));
+  return EAGLE_OK;
+}
+
 eagle_status eagle_tree_expand_rerank(eagle_ctx* ctx, const eagle_plan* plan, int phase, int layer, int batch,
                                       const eagle_requests* req, const eagle_children* children,
                                       const eagle_pool* pool, const eagle_tree* tree, void* workspace,
@@ -649,7 +678,7 @@ eagle_status eagle_commit(eagle_ctx* ctx, int batch, const eagle_accept_out* acc
 }
 
 eagle_status eagle_trace_enable(eagle_ctx* ctx, int kernel_id, int capacity) {
-  EAGLE_REQUIRE(ctx && capacity >= 1 && kernel_id >= -1 && kernel_id <= EAGLE_K_REFRESH, EAGLE_ERR_INVALID_ARG);
+  EAGLE_REQUIRE(ctx && capacity >= 1 && kernel_id >= -1 && kernel_id <= EAGLE_K_FUSE, EAGLE_ERR_INVALID_ARG);
   TraceState& t = ctx->trace;
   while (static_cast<int>(t.events.size()) < 2 * capacity) {
     cudaEvent_t e;

@@ -61,6 +61,34 @@ __global__ void prep_fc_kernel(const float* __restrict__ f_last, const float* __
   *reinterpret_cast<uint4*>(bfc + static_cast<size_t>(NP + j) * kp + c0) = lv;
 }
 
+// EAGLE-3 feature fusion input ([C] "EAGLE-3：放弃 feature prediction，改成多层
+// 特征融合与 training-time test": g = FC([l; m; h])): row j of [l ; m ; h]
+// (fp32 [n][3d]) into the fusion contraction's bf16 hi/lo operand.
+__global__ void prep_fuse_kernel(const float* __restrict__ lmh, int d3, int NP, int kp, uint16_t* __restrict__ bop,
+                                 uint64_t* stamp) {
+  const LaunchStamp ls(stamp);
+  pdl_trigger();
+  pdl_wait();
+  ls.waited();
+  const int j = blockIdx.x;
+  const int c0 = (blockIdx.y * blockDim.x + threadIdx.x) * 8;
+  if (c0 >= d3) return;
+  const float* row = lmh + static_cast<size_t>(j) * d3 + c0;
+  const float4 a = *reinterpret_cast<const float4*>(row);
+  const float4 c = *reinterpret_cast<const float4*>(row + 4);
+  const float x[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+  uint16_t h[8], l[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) split_bf16(x[u], h[u], l[u]);
+  uint4 hv, lv;
+  hv.x = h[0] | (uint32_t(h[1]) << 16); hv.y = h[2] | (uint32_t(h[3]) << 16);
+  hv.z = h[4] | (uint32_t(h[5]) << 16); hv.w = h[6] | (uint32_t(h[7]) << 16);
+  lv.x = l[0] | (uint32_t(l[1]) << 16); lv.y = l[2] | (uint32_t(l[3]) << 16);
+  lv.z = l[4] | (uint32_t(l[5]) << 16); lv.w = l[6] | (uint32_t(l[7]) << 16);
+  *reinterpret_cast<uint4*>(bop + static_cast<size_t>(j) * kp + c0) = hv;
+  *reinterpret_cast<uint4*>(bop + static_cast<size_t>(NP + j) * kp + c0) = lv;
+}
+
 // Draft-cache refresh rows ([B] "KV Cache 必须按事务提交": the drafter
 // continues from the committed path; [A] §6.2 closing remark): row
 // j = b * R + i - 1 (i = 1 .. R) is x = [f_commit[b][i-1] ; E[tok_commit[b][i]]]
@@ -449,6 +477,18 @@ cudaError_t launch_prep_fc(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st
                  ws_ptr<uint16_t>(L.ws, ctx->ws.b_fc), stamp);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_PREP, st);
+  return e;
+}
+
+cudaError_t launch_prep_fuse(eagle_ctx* ctx, const DraftLaunch& L, const float* lmh, cudaStream_t st) {
+  const int d3 = 3 * ctx->dims.d;
+  const dim3 grid(L.n, ceil_div(d3 / 8, 128));
+  uint64_t* stamp = stamp_slot(ctx, EAGLE_K_FUSE);
+  trace_before(ctx, EAGLE_K_FUSE, st);
+  const cudaError_t e = launch_pdl(prep_fuse_kernel, grid, dim3(128), 0, st, lmh, d3, L.NP, ctx->ws.kp_fuse,
+                                   ws_ptr<uint16_t>(L.ws, ctx->ws.b_fuse), stamp);
+  ctx->launches++;
+  trace_after(ctx, EAGLE_K_FUSE, st);
   return e;
 }
 

@@ -283,6 +283,7 @@ __device__ __noinline__ EpiCol epi_column(const GemmParams& p, int t, int m) {
   c.d_col = c.gi < p.d;
   c.col_bias = 0.f; c.col_gain = 0.f;
   if (p.epi == EPI_FC && c.d_col) { c.col_bias = p.bias[c.gi]; c.col_gain = p.gain[c.gi]; }
+  if (p.epi == EPI_FUSE && c.d_col && p.bias != nullptr) c.col_bias = p.bias[c.gi];
   if (p.epi == EPI_O && c.d_col) c.col_gain = p.gain[c.gi];
   return c;
 }
@@ -441,6 +442,13 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
         }
         dst[((static_cast<size_t>(b) * cap + row) * Hkv + head) * dh + di] = f32_to_bf16(v);
       }
+    }
+  } else if (p.epi == EPI_FUSE) {
+    if (d_col) {
+      float* const out = p.out_f32;
+      const int d = p.d;
+#pragma unroll 1
+      for (int jj = 0; jj < nj; ++jj) out[static_cast<size_t>(jc + jj) * d + gi] = xch[jj * BM + m] + col_bias;
     }
   } else if (p.epi == EPI_GATEUP) {
     const int c = t * 64 + m;
@@ -988,6 +996,12 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
       p.kv_cap_rows = L.refresh_kv->cap; p.kv_len = L.refresh_kv->len;
       p.n_act = L.refresh_n;
       break;
+    case EPI_FUSE:
+      mats[0] = L.w_fuse; rows[0] = D.d; lds[0] = L.ld_fuse; K = 3 * D.d;
+      b_in = W.b_fuse; kp_in = W.kp_fuse; n_out = D.d;
+      p.bias = L.b_fuse;
+      p.out_f32 = L.g_out;
+      break;
     default:  // EPI_LM
       mats[0] = w->w_lm; rows[0] = D.vocab; lds[0] = w->ld_lm; K = D.d;
       b_in = W.b_lm; kp_in = W.kp_lm; n_out = D.vocab;
@@ -1057,7 +1071,8 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   // partial slots t + cta of split tiles stay inside the workspace's array
   if (p.sk_tiles > 0 && p.sk_tiles - 1 + grid - 1 >= W.max_mtiles + 2 * ctx->sm_count)
     return cudaErrorInvalidConfiguration;
-  const int kid = epi == EPI_KV ? static_cast<int>(EAGLE_K_REFRESH) : epi;
+  const int kid = epi == EPI_KV ? static_cast<int>(EAGLE_K_REFRESH)
+                                 : (epi == EPI_FUSE ? static_cast<int>(EAGLE_K_FUSE) : epi);
   p.stamp = stamp_slot(ctx, kid);
   trace_before(ctx, kid, st);
   const cudaError_t e = launch_pdl(gemm_stream_kernel, dim3(grid), dim3(NUM_THREADS), smem, st, maps[0], maps[1],

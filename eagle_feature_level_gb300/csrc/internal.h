@@ -18,8 +18,9 @@ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // GEMM epilogue kinds (one per contraction of the draft step, and the K/V
 // projection of the draft-cache refresh).
-enum Epi : int { EPI_FC = 0, EPI_QKV = 1, EPI_O = 2, EPI_GATEUP = 3, EPI_DOWN = 4, EPI_LM = 5, EPI_KV = 6 };
-constexpr int N_EPI = 7;
+enum Epi : int { EPI_FC = 0, EPI_QKV = 1, EPI_O = 2, EPI_GATEUP = 3, EPI_DOWN = 4, EPI_LM = 5, EPI_KV = 6,
+                 EPI_FUSE = 7 };
+constexpr int N_EPI = 8;
 
 // Activation rows are padded to NP; the GEMM's B operand holds the bf16 "hi"
 // parts in rows [0, NP) and the "lo" parts in rows [NP, 2NP).  NP is a
@@ -33,8 +34,8 @@ inline int padded_rows(int n) {
 
 struct Workspace {
   size_t status;                 // int status word
-  size_t b_fc, b_qkv, b_o, b_gu, b_down, b_lm;   // bf16 [2*NPmax][Kpad]
-  int kp_fc, kp_qkv, kp_o, kp_gu, kp_down, kp_lm;
+  size_t b_fc, b_qkv, b_o, b_gu, b_down, b_lm, b_fuse;   // bf16 [2*NPmax][Kpad]
+  int kp_fc, kp_qkv, kp_o, kp_gu, kp_down, kp_lm, kp_fuse;
   size_t h, h2;                  // fp32 [max_rows][d]
   size_t qrow;                   // fp32 [max_rows][Hq*dh]
   size_t ss_fc, ss_o;            // fp32 [max_rows][tiles of d]
@@ -143,6 +144,11 @@ struct DraftLaunch {
   // draft-cache refresh (EPI_KV): rows j = b * rpr + i - 1 for i = 1 .. rpr
   const eagle_kv* refresh_kv;     // cache; row of (b, i) = len[b] + i - 1
   const int32_t* refresh_n;       // [B] active rows of request b
+  // feature fusion (EPI_FUSE): g[j] = W_fuse [l; m; h]_j (+ b_fuse)
+  const uint16_t* w_fuse;
+  int ld_fuse;
+  const float* b_fuse;
+  float* g_out;
 };
 
 cudaError_t launch_prep_fc(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st);
@@ -151,6 +157,8 @@ cudaError_t launch_draft_attn(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t
 cudaError_t launch_select(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t st);
 // Gathers the refresh rows [f_commit[b][i-1] ; E[tok_commit[b][i]]] into the
 // FC operand and writes len_out = len + active rows.
+// Gathers rows of [l ; m ; h] (fp32 [n][3d]) into the fusion operand.
+cudaError_t launch_prep_fuse(eagle_ctx* ctx, const DraftLaunch& L, const float* lmh, cudaStream_t st);
 cudaError_t launch_prep_refresh(eagle_ctx* ctx, const DraftLaunch& L, const float* f_commit,
                                 const int32_t* tok_commit, int path_cap, int32_t* len_out, cudaStream_t st);
 

@@ -207,6 +207,12 @@ def round_inputs(w: Workload, seed: int, device="cpu") -> Dict[str, object]:
     return out
 
 
+def fuse_weights(w: Workload, seed: int, device="cpu") -> Dict[str, torch.Tensor]:
+    """EAGLE-3 feature fusion FC (3d -> d): weights and bias N(0, std)."""
+    return {"w_fuse": _bf16_matrix(w.d, 3 * w.d, w.weight_std, seed, "w_fuse", device),
+            "b_fuse": (_randn((w.d,), seed, "b_fuse", device) * w.weight_std).contiguous()}
+
+
 def random_probs(rows: int, V: int, seed: int, name: str, sigma: float = 1.0,
                  device="cpu") -> torch.Tensor:
     """fp32 random probability rows for stage tests: log-normal weights

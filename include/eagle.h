@@ -439,6 +439,24 @@ eagle_status eagle_draft_refresh(eagle_ctx* ctx, int batch, const eagle_draft_we
                                  const eagle_kv* draft_kv, int32_t* len_out, void* workspace,
                                  cudaStream_t stream);
 
+/* eagle_fuse_features -- the EAGLE-3 input ([C] "EAGLE-3：放弃 feature
+ * prediction，改成多层特征融合与 training-time test"): the target's low-, middle-
+ * and high-layer features of a position, each of dimension d, concatenated
+ * and compressed back to d,
+ *   g[j] = W_fuse [l_j ; m_j ; h_j] (+ b_fuse),
+ * for n_rows rows.  g then takes the place of the feature f everywhere the
+ * round reads a target feature: the round's f_last, and the true features
+ * of the tree slots (f_true) that eagle_commit gathers and
+ * eagle_draft_refresh reads; drafted rows still carry the draft's own
+ * outputs, as in EAGLE-1 and EAGLE-2.
+ * w_fuse [d][ld_fuse] bf16 (ld_fuse >= 3d, % 8 == 0), columns 0..d-1 take
+ * l, d..2d-1 m, 2d..3d-1 h; b_fuse [d] fp32 or NULL (no bias); lmh
+ * [n_rows][3d] fp32; g_out [n_rows][d] fp32; n_rows <= max_rows
+ * (EAGLE_ERR_CAPACITY).  Streams W_fuse once. */
+eagle_status eagle_fuse_features(eagle_ctx* ctx, const uint16_t* w_fuse, int ld_fuse, const float* b_fuse,
+                                 int n_rows, const float* lmh, float* g_out, void* workspace,
+                                 cudaStream_t stream);
+
 /* ---- measurement --------------------------------------------------------- */
 
 /* Kernel timing hook: while enabled, the library records a CUDA event before
@@ -449,7 +467,7 @@ typedef enum {
   EAGLE_K_ALL = -1, EAGLE_K_GEMM_FC = 0, EAGLE_K_GEMM_QKV = 1, EAGLE_K_GEMM_O = 2,
   EAGLE_K_GEMM_GATEUP = 3, EAGLE_K_GEMM_DOWN = 4, EAGLE_K_GEMM_LM = 5, EAGLE_K_DRAFT_ATTN = 6,
   EAGLE_K_SELECT = 7, EAGLE_K_TREE = 8, EAGLE_K_VERIFY_ATTN = 9, EAGLE_K_ACCEPT = 10,
-  EAGLE_K_COMMIT = 11, EAGLE_K_PREP = 12, EAGLE_K_REFRESH = 13
+  EAGLE_K_COMMIT = 11, EAGLE_K_PREP = 12, EAGLE_K_REFRESH = 13, EAGLE_K_FUSE = 14
 } eagle_kernel_id;
 eagle_status eagle_trace_enable(eagle_ctx* ctx, int kernel_id, int capacity);
 /* Synchronises the recorded events; writes up to `cap` durations in ms, the

@@ -123,6 +123,19 @@ def fc_rows(W: DraftWeights, feats: np.ndarray, tokens) -> np.ndarray:
     return x @ W.w_fc.T + W.b_fc
 
 
+def fuse_rows(w_fuse, b_fuse, l, m, h) -> np.ndarray:
+    """EAGLE-3's fused feature (Page C "EAGLE-3：放弃 feature prediction，改成
+    多层特征融合与 training-time test"): the target's low-, middle- and
+    high-layer features concatenated, [l; m; h] (3k), compressed back to k by
+    a fully connected layer, g = FC([l; m; h]).  Rows [n, d] each; the FC's
+    bias is optional (None), as the page leaves it unstated."""
+    d = np.asarray(l).shape[-1]
+    W = to_f64(w_fuse)[:, :3 * d]
+    x = np.concatenate([to_f64(l), to_f64(m), to_f64(h)], axis=-1)
+    g = x @ W.T
+    return g if b_fuse is None else g + to_f64(b_fuse)
+
+
 def finish_rows(W, h: np.ndarray, o: np.ndarray, dims) -> np.ndarray:
     """h2 = h + Wo o;  f^ = h2 + W_down(SiLU(W_gate b) * W_up b), b = RMSNorm(h2)."""
     h2 = h + o.reshape(o.shape[0], -1) @ W.wo.T

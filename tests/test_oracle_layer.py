@@ -175,3 +175,28 @@ def test_expected_tokens_worked_examples():
         assert abs(expected_tokens(alphas) - float(printed)) <= half_ulp + 1e-12
         n += 1
     assert n == 4
+
+
+def test_fuse_rows_input_order_is_low_middle_high():
+    """g = FC([l; m; h]): each third of the FC's input columns reads its own
+    layer's feature, in the order low, middle, high."""
+    from oracle.layer import fuse_rows
+    w = S.variant("tiny_fp32", name="fuse_pin")
+    F = S.fuse_weights(w, 7)
+    rng = np.random.default_rng(5)
+    l, m, h = (rng.standard_normal((2, w.d)) for _ in range(3))
+    d = w.d
+    for blk, feat in enumerate((l, m, h)):
+        Wb = F["w_fuse"].clone()
+        keep = slice(blk * d, (blk + 1) * d)
+        mask = torch.zeros_like(Wb)
+        mask[:, keep] = 1
+        Wb = Wb * mask
+        g = fuse_rows(Wb, None, l, m, h)
+        # only this block's feature matters: the others can change freely
+        others = [np.zeros_like(l) if i != blk else feat for i in range(3)]
+        np.testing.assert_array_equal(g, fuse_rows(Wb, None, *others))
+        np.testing.assert_allclose(g, feat @ Wb.double().numpy()[:, keep].T, rtol=1e-12, atol=1e-12)
+    g0 = fuse_rows(F["w_fuse"], None, l, m, h)
+    np.testing.assert_allclose(fuse_rows(F["w_fuse"], F["b_fuse"], l, m, h) - g0,
+                               np.broadcast_to(F["b_fuse"].double().numpy(), g0.shape), rtol=0, atol=1e-12)
