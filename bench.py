@@ -289,7 +289,7 @@ def run_ours(args):
     # the windows tile the round, so they sum to the round's device time and
     # keep the programmatic overlap between kernels intact.
     cap = per_round + 8
-    stamps = torch.empty(2 * cap, dtype=torch.int64, device=dev)
+    stamps = torch.empty(3 * cap, dtype=torch.int64, device=dev)
     B.eagle_stamps_enable(eng.ctx, stamps.data_ptr(), cap)
     sgraph = rd.capture(wc)
     names = B.eagle_stamps_disable(eng.ctx)
@@ -299,13 +299,17 @@ def run_ours(args):
     span = [0.0] * n
     stamped_round = 0.0
     tick = None
-    for _ in range(k_st):
-        stamps.view(-1, 2)[:, 0].fill_(-1)          # UINT64_MAX: no release seen yet
-        stamps.view(-1, 2)[:, 1].fill_(0)
+    dump = []
+    for rep in range(k_st):
+        stamps.view(-1, 3)[:, :2].fill_(-1)         # UINT64_MAX: no start / release seen yet
+        stamps.view(-1, 3)[:, 2].fill_(0)
         sgraph.replay()
         torch.cuda.synchronize()
-        t = [int(x) & 0xFFFFFFFFFFFFFFFF for x in stamps[:2 * n].cpu().tolist()]
-        w_, e_ = t[0::2], t[1::2]
+        t = [int(x) & 0xFFFFFFFFFFFFFFFF for x in stamps[:3 * n].cpu().tolist()]
+        s_, w_, e_ = t[0::3], t[1::3], t[2::3]
+        if rep == k_st - 1 and args.dump_stamps:
+            dump = [{"kernel": names[i], "start_us": (s_[i] - w_[0]) / 1e3, "release_us": (w_[i] - w_[0]) / 1e3,
+                     "exit_us": (e_[i] - w_[0]) / 1e3} for i in range(n)]
         for i in range(n):
             nxt = w_[i + 1] if i + 1 < n else e_[i]
             excl[i] += (nxt - w_[i]) / 1e3
@@ -315,6 +319,9 @@ def run_ours(args):
         if d:
             tick = d[0] if tick is None else min(tick, d[0])
     del sgraph
+    if dump:
+        with open(args.dump_stamps, "w") as fh:
+            json.dump(dump, fh, indent=0)
     by_class = {}
     for i, name in enumerate(names):
         c = by_class.setdefault(name, [0, 0.0, 0.0])
@@ -428,6 +435,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-oracle-sample", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--dump-stamps", default=None, help="write the last stamped replay's per-launch times (JSON)")
     args = ap.parse_args()
     if args.cpu_oracle_sample:
         run_cpu_sample(args)

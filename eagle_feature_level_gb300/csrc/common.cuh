@@ -205,20 +205,22 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // ---- launch timestamps (measurement) ---------------------------------------
-// With a non-null slot, thread 0 of every CTA records %globaltimer twice:
-// when it has passed the dependency wait (atomic min into slot[0]: the
-// earliest moment a CTA of this launch could use its predecessors' outputs)
-// and when it leaves the kernel (atomic max into slot[1]).  A null slot
-// costs one test.
+// With a non-null slot, thread 0 of every CTA records %globaltimer three
+// times: when it starts (atomic min into slot[0]), when it has passed the
+// dependency wait (atomic min into slot[1]: the earliest moment a CTA of this
+// launch could use its predecessors' outputs) and when it leaves the kernel
+// (atomic max into slot[2]).  A null slot costs one test.
 struct LaunchStamp {
   unsigned long long* slot;
   __device__ explicit LaunchStamp(uint64_t* s)
-      : slot(threadIdx.x == 0 ? reinterpret_cast<unsigned long long*>(s) : nullptr) {}
-  __device__ void waited() const {
+      : slot(threadIdx.x == 0 ? reinterpret_cast<unsigned long long*>(s) : nullptr) {
     if (slot) atomicMin(slot, static_cast<unsigned long long>(globaltimer_ns()));
   }
+  __device__ void waited() const {
+    if (slot) atomicMin(slot + 1, static_cast<unsigned long long>(globaltimer_ns()));
+  }
   __device__ ~LaunchStamp() {
-    if (slot) atomicMax(slot + 1, static_cast<unsigned long long>(globaltimer_ns()));
+    if (slot) atomicMax(slot + 2, static_cast<unsigned long long>(globaltimer_ns()));
   }
 };
 

@@ -116,7 +116,7 @@ cudaError_t smem_limit_once(const void* kernel, int bytes);
 // stamps are enabled, else null.
 inline uint64_t* stamp_slot(eagle_ctx* ctx, int kernel_id) {
   if (!ctx->stamps || static_cast<int>(ctx->stamp_ids.size()) >= ctx->stamp_cap) return nullptr;
-  uint64_t* s = ctx->stamps + 2 * ctx->stamp_ids.size();
+  uint64_t* s = ctx->stamps + 3 * ctx->stamp_ids.size();
   ctx->stamp_ids.push_back(kernel_id);
   return s;
 }

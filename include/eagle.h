@@ -480,12 +480,13 @@ eagle_status eagle_trace_disable(eagle_ctx* ctx);
  * pairs around each launch would break).  While enabled, the i-th launch
  * issued through this context (counted from enable; launches captured into a
  * graph keep their slot on every replay) has thread 0 of each CTA record
- * %globaltimer nanoseconds into stamps[2i] (atomic min, taken when the CTA
- * has passed its wait for the preceding kernels' results) and stamps[2i+1]
- * (atomic max, taken when the thread leaves the kernel).  `stamps` is a
- * caller-owned device buffer of 2 * capacity uint64_t that the caller sets
- * to (UINT64_MAX, 0) pairs before each run it measures; launches beyond
- * `capacity` are not recorded.  Costs one atomic per CTA and stamp. */
+ * %globaltimer nanoseconds into stamps[3i] (atomic min, when the CTA
+ * starts), stamps[3i+1] (atomic min, when it has passed its wait for the
+ * preceding kernels' results) and stamps[3i+2] (atomic max, when the thread
+ * leaves the kernel).  `stamps` is a caller-owned device buffer of
+ * 3 * capacity uint64_t that the caller sets to (UINT64_MAX, UINT64_MAX, 0)
+ * triples before each run it measures; launches beyond `capacity` are not
+ * recorded.  Costs one atomic per CTA and stamp. */
 eagle_status eagle_stamps_enable(eagle_ctx* ctx, uint64_t* stamps, int capacity);
 /* Stops assigning stamp slots; writes the kernel class (eagle_kernel_id) of
  * each stamped launch, in order, to ids_out (up to cap) and their count. */
