@@ -82,3 +82,40 @@ def test_noalloc_rejects_oversize():
     assert ei.value.code == 4                     # EAGLE_ERR_CAPACITY
     torch.cuda.synchronize()
     assert torch.isnan(out).all()
+
+
+def test_first_call_refused_on_a_capturing_stream():
+    """The first call in a CUDA context sets the array up (zeroing and a
+    stream synchronisation, which a capture does not allow): on a capturing
+    stream it returns EAGLE_ERR_INVALID_ARG without touching the stream, so
+    the caller's capture stays valid.  Runs in a fresh process, where no call
+    has set the array up yet."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = r"""
+import math, sys, torch
+sys.path.insert(0, %r)
+import eagle_synth as S
+from eagle_feature_level_gb300 import _binding as B
+from eagle_feature_level_gb300.workload import make_round
+w = S.variant("70b_x16_eagle2", name="noalloc_capture", d=256, n_q_heads=8, n_kv_heads=2, head_dim=32, d_ff=688,
+              vocab=1000, batch=2, prefix_len=64, top_k=4, depth=3, top_m=8, weight_std=0.05)
+inp = S.round_inputs(w, 4245, device="cuda")
+eng, rd = make_round(w, inp)
+torch.cuda.synchronize()
+g = torch.cuda.CUDAGraph()
+code = 0
+with torch.cuda.graph(g):
+    try:
+        B.eagle_tree_verify_attn_noalloc(eng.ctx, rd.B, rd.tree_q.data_ptr(), rd.tree_k[0].data_ptr(),
+                                         rd.tree_v[0].data_ptr(), rd.prefix_c, rd.tree_c, 1.0 / math.sqrt(32),
+                                         rd.attn_out.data_ptr(), eng.stream())
+    except B.EagleError as e:
+        code = e.code
+torch.cuda.synchronize()
+print("CODE", code)
+""" % root
+    r = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True, timeout=600)
+    assert "CODE 1" in r.stdout, (r.stdout[-2000:], r.stderr[-2000:])
