@@ -64,8 +64,12 @@ class eagle_draft_weights(C.Structure):
                 ("ld_embed", I), ("w_lm", P), ("ld_lm", I)]
 
 
+class eagle_paging(C.Structure):
+    _fields_ = [("block_table", P), ("block_size", I), ("n_blocks", I)]
+
+
 class eagle_kv(C.Structure):
-    _fields_ = [("k", P), ("v", P), ("cap", I), ("len", P)]
+    _fields_ = [("k", P), ("v", P), ("cap", I), ("len", P), ("paging", eagle_paging)]
 
 
 class eagle_requests(C.Structure):
@@ -144,7 +148,8 @@ def _declare(L):
                                     C.POINTER(eagle_children), P, P, P, C.POINTER(eagle_sampling),
                                     C.POINTER(eagle_accept_out), P, P],
         "eagle_commit": [P, I, C.POINTER(eagle_accept_out), C.POINTER(eagle_tree), P, I, P, P, P, P, I, P,
-                         C.POINTER(eagle_draft_out), C.POINTER(eagle_kv), C.POINTER(eagle_commit_out), P, P],
+                         C.POINTER(eagle_paging), C.POINTER(eagle_draft_out), C.POINTER(eagle_kv),
+                         C.POINTER(eagle_commit_out), P, P],
         "eagle_trace_enable": [P, I, I],
         "eagle_trace_read": [P, C.POINTER(C.c_float), C.POINTER(I), I, C.POINTER(I)],
         "eagle_trace_disable": [P],
@@ -265,14 +270,14 @@ def eagle_accept_from_probs(ctx, plan, batch, tree, children, target_probs, targ
 
 
 def eagle_commit(ctx, batch, acc, tree, f_true, k_tree_layers, v_tree_layers, k_cache_layers, v_cache_layers,
-                 kv_cap, target_kv_len, draft, draft_kv, out, ws_ptr, stream):
+                 kv_cap, target_kv_len, draft, draft_kv, out, ws_ptr, stream, target_paging=None):
     n = len(k_tree_layers)
     arr = lambda xs: (P * max(n, 1))(*xs)
     _check("eagle_commit",
            lib().eagle_commit(ctx, batch, C.byref(acc), C.byref(tree), f_true, n, C.cast(arr(k_tree_layers), P),
                               C.cast(arr(v_tree_layers), P), C.cast(arr(k_cache_layers), P),
-                              C.cast(arr(v_cache_layers), P), kv_cap, target_kv_len, _ref(draft), _ref(draft_kv),
-                              C.byref(out), ws_ptr, stream))
+                              C.cast(arr(v_cache_layers), P), kv_cap, target_kv_len, _ref(target_paging),
+                              _ref(draft), _ref(draft_kv), C.byref(out), ws_ptr, stream))
 
 
 def eagle_fuse_features(ctx, w_fuse, ld_fuse, b_fuse, n_rows, lmh, g_out, ws_ptr, stream):

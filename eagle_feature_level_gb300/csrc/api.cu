@@ -164,13 +164,27 @@ eagle_status check_children(const eagle_children* ch) {
   return EAGLE_OK;
 }
 
-eagle_status check_kv(const eagle_ctx* c, const eagle_kv* kv) {
+// A block table (if any) over a cache of cap rows per request: block_size a
+// power of two dividing cap, at least one block in the pools.
+eagle_status check_paging(const eagle_paging* pg, int cap) {
+  if (pg == nullptr || pg->block_table == nullptr) return EAGLE_OK;
+  EAGLE_PTR(pg->block_table);
+  const int bs = pg->block_size;
+  EAGLE_REQUIRE(bs >= 1 && (bs & (bs - 1)) == 0 && cap % bs == 0, EAGLE_ERR_INVALID_ARG);
+  EAGLE_REQUIRE(pg->n_blocks >= 1, EAGLE_ERR_INVALID_ARG);
+  return EAGLE_OK;
+}
+
+// paged: the cache may be addressed through a block table (target caches);
+// the draft cache is always contiguous
+eagle_status check_kv(const eagle_ctx* c, const eagle_kv* kv, bool paged = false) {
   EAGLE_REQUIRE(kv, EAGLE_ERR_INVALID_ARG);
   EAGLE_PTR(kv->k); EAGLE_PTR(kv->v); EAGLE_PTR(kv->len);
   EAGLE_REQUIRE(kv->cap >= 1, EAGLE_ERR_SHAPE);
   // the workspace's attention records are sized for caches up to max_prefix
   EAGLE_REQUIRE(kv->cap <= c->lim.max_prefix, EAGLE_ERR_CAPACITY);
-  return EAGLE_OK;
+  EAGLE_REQUIRE(paged || kv->paging.block_table == nullptr, EAGLE_ERR_INVALID_ARG);
+  return check_paging(&kv->paging, kv->cap);
 }
 
 eagle_status check_ws(const void* ws) {
@@ -557,7 +571,7 @@ eagle_status eagle_tree_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q
   EAGLE_REQUIRE(ctx, EAGLE_ERR_INVALID_ARG);
   EAGLE_REQUIRE(batch >= 1 && batch <= ctx->lim.max_batch, EAGLE_ERR_CAPACITY);
   EAGLE_PTR(q); EAGLE_PTR(k_tree); EAGLE_PTR(v_tree); EAGLE_PTR(out);
-  eagle_status st = check_kv(ctx, prefix);
+  eagle_status st = check_kv(ctx, prefix, true);
   if (st != EAGLE_OK) return st;
   if ((st = check_tree(ctx, tree)) != EAGLE_OK) return st;
   if ((st = check_ws(workspace)) != EAGLE_OK) return st;
@@ -572,7 +586,7 @@ eagle_status eagle_tree_verify_attn_noalloc(eagle_ctx* ctx, int batch, const uin
   EAGLE_REQUIRE(ctx, EAGLE_ERR_INVALID_ARG);
   EAGLE_REQUIRE(batch >= 1 && batch <= ctx->lim.max_batch, EAGLE_ERR_CAPACITY);
   EAGLE_PTR(q); EAGLE_PTR(k_tree); EAGLE_PTR(v_tree); EAGLE_PTR(out);
-  eagle_status st = check_kv(ctx, prefix);
+  eagle_status st = check_kv(ctx, prefix, true);
   if (st != EAGLE_OK) return st;
   if ((st = check_tree(ctx, tree)) != EAGLE_OK) return st;
   EAGLE_REQUIRE(std::isfinite(scale) && scale > 0.f, EAGLE_ERR_INVALID_ARG);
@@ -627,8 +641,9 @@ eagle_status eagle_commit(eagle_ctx* ctx, int batch, const eagle_accept_out* acc
                           const float* f_true, int n_layers, const uint16_t* const* k_tree_layers,
                           const uint16_t* const* v_tree_layers, uint16_t* const* k_cache_layers,
                           uint16_t* const* v_cache_layers, int kv_cap, const int32_t* target_kv_len,
-                          const eagle_draft_out* draft, const eagle_kv* draft_kv, const eagle_commit_out* out,
-                          void* workspace, cudaStream_t stream) {
+                          const eagle_paging* target_paging, const eagle_draft_out* draft,
+                          const eagle_kv* draft_kv, const eagle_commit_out* out, void* workspace,
+                          cudaStream_t stream) {
   EAGLE_REQUIRE(ctx, EAGLE_ERR_INVALID_ARG);
   EAGLE_REQUIRE(batch >= 1 && batch <= ctx->lim.max_batch, EAGLE_ERR_CAPACITY);
   EAGLE_REQUIRE(acc, EAGLE_ERR_INVALID_ARG);
@@ -647,6 +662,7 @@ eagle_status eagle_commit(eagle_ctx* ctx, int batch, const eagle_accept_out* acc
   }
   EAGLE_REQUIRE(kv_cap >= 1, EAGLE_ERR_SHAPE);
   EAGLE_PTR(target_kv_len);
+  if ((st = check_paging(target_paging, kv_cap)) != EAGLE_OK) return st;
   EAGLE_REQUIRE(out, EAGLE_ERR_INVALID_ARG);
   EAGLE_PTR(out->f_commit); EAGLE_PTR(out->tok_commit); EAGLE_PTR(out->f_last); EAGLE_PTR(out->t_next);
   EAGLE_PTR(out->prefix_len);
@@ -661,6 +677,7 @@ eagle_status eagle_commit(eagle_ctx* ctx, int batch, const eagle_accept_out* acc
   C.batch = batch;
   C.n_layers = n_layers;
   C.kv_cap = kv_cap;
+  C.paged = paged_of(target_paging, kv_cap);
   C.acc = acc;
   C.tree = tree;
   C.f_true = f_true;

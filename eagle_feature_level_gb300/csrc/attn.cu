@@ -52,9 +52,10 @@ struct AttnParams {
   int rows_pass;                  // CUDA-core kernel: query rows staged per pass, min(ROWS_PASS, rows_cap * G)
   const float* q_f32;             // draft: [n][Hq*dh] fp32
   const uint16_t* q_bf16;         // verify: [B][S][Hq][dh] bf16
-  const uint16_t* kp;             // prefix KV [B][cap][Hkv][dh] bf16
+  const uint16_t* kp;             // prefix KV [B][cap][Hkv][dh] bf16, or block pools (paged)
   const uint16_t* vp;
   int kv_cap;
+  PagedKv paged;                  // verify: the prefix through a block table (table null: contiguous)
   const int32_t* kv_len;
   const float* kt_f32;            // draft: tree K/V [B][E][Hkv][dh] fp32
   const float* vt_f32;
@@ -124,6 +125,36 @@ __device__ __forceinline__ void stage_bf16(uint16_t* buf, const uint16_t* kb, co
       cp_async16(sk + r * KLD + 8 * c, kb + row0 + r * row_stride + 8 * c, policy);
       cp_async16(sv + r * KLD + 8 * c, vb + row0 + r * row_stride + 8 * c, policy);
     } else {
+      *reinterpret_cast<uint4*>(sk + r * KLD + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sv + r * KLD + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  cp_async_commit();
+}
+
+// Prefix keys t0 .. t0 + nt - 1 of request b, kv head h, staged like
+// stage_bf16 but read through the block table; rows of an unallocated block
+// are zero and reported.
+__device__ __forceinline__ void stage_bf16_paged(uint16_t* buf, const AttnParams& p, int b, int h, int t0, int nt,
+                                                 uint64_t policy) {
+  uint16_t* sk = buf;
+  uint16_t* sv = buf + TILE * KLD;
+  const int dh = p.dh, pieces = dh >> 3;
+  for (int idx = threadIdx.x; idx < TILE * pieces; idx += THREADS) {
+    const int r = idx / pieces, c = idx - r * pieces;
+    bool loaded = false;
+    if (r < nt) {
+      const long long row = paged_row(p.paged, b, t0 + r);
+      if (row >= 0) {
+        const size_t off = (static_cast<size_t>(row) * p.Hkv + h) * dh + 8 * c;
+        cp_async16(sk + r * KLD + 8 * c, p.kp + off, policy);
+        cp_async16(sv + r * KLD + 8 * c, p.vp + off, policy);
+        loaded = true;
+      } else if (c == 0) {
+        set_status(p.status, EAGLE_ERR_INVALID_ARG);
+      }
+    }
+    if (!loaded) {
       *reinterpret_cast<uint4*>(sk + r * KLD + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
       *reinterpret_cast<uint4*>(sv + r * KLD + 8 * c) = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -332,6 +363,8 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
     else if (is_tree)
       stage_bf16(reinterpret_cast<uint16_t*>(buf), p.kt_bf16, p.vt_bf16,
                  ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh, row_stride, nt, dh, policy);
+    else if (p.paged.table)
+      stage_bf16_paged(reinterpret_cast<uint16_t*>(buf), p, b, h, t0, nt, policy);
     else
       stage_bf16(reinterpret_cast<uint16_t*>(buf), p.kp, p.vp,
                  ((static_cast<size_t>(b) * p.kv_cap + t0) * p.Hkv + h) * dh, row_stride, nt, dh, policy);
@@ -769,6 +802,8 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
     else if (is_tree)
       stage_bf16(buf, p.kt_bf16, p.vt_bf16, ((static_cast<size_t>(b) * p.tree_cap + t0) * p.Hkv + h) * dh,
                  row_stride, nt, dh, policy);
+    else if (p.paged.table)
+      stage_bf16_paged(buf, p, b, h, t0, nt, policy);
     else
       stage_bf16(buf, p.kp, p.vp, ((static_cast<size_t>(b) * p.kv_cap + t0) * p.Hkv + h) * dh, row_stride, nt, dh,
                  policy);
@@ -1062,6 +1097,7 @@ cudaError_t launch_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, con
   p.kp = prefix->k;
   p.vp = prefix->v;
   p.kv_cap = prefix->cap;
+  p.paged = paged_of(&prefix->paging, prefix->cap);
   p.kv_len = prefix->len;
   p.kt_bf16 = kt;
   p.vt_bf16 = vt;
@@ -1147,6 +1183,7 @@ eagle_status launch_verify_attn_noalloc(eagle_ctx* ctx, int batch, const uint16_
   p.kp = prefix->k;
   p.vp = prefix->v;
   p.kv_cap = prefix->cap;
+  p.paged = paged_of(&prefix->paging, prefix->cap);
   p.kv_len = prefix->len;
   p.kt_bf16 = kt;
   p.vt_bf16 = vt;

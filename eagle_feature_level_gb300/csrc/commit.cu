@@ -13,6 +13,7 @@ namespace {
 
 struct CommitParams {
   int n_layers, kv_cap, S, E, d, row_elems, path_cap, draft_cap;
+  PagedKv paged;                  // target caches through a block table (table null: contiguous)
   const uint16_t* kt[EAGLE_MAX_LAYERS];
   const uint16_t* vt[EAGLE_MAX_LAYERS];
   uint16_t* kc[EAGLE_MAX_LAYERS];
@@ -55,8 +56,12 @@ __global__ void commit_kernel(const CommitParams p) {
   const int a = p.accept_len[b];
   const int L = p.kv_len[b];
   // a request whose cache cannot take the path commits nothing (checked
-  // alike by every CTA of the request; the state CTA reports it)
-  const bool room = L >= 0 && static_cast<long long>(L) + 1 + a <= p.kv_cap;
+  // alike by every CTA of the request; the state CTA reports it): the rows
+  // L .. L + a must exist and, in a paged cache, lie in allocated blocks
+  bool room = L >= 0 && static_cast<long long>(L) + 1 + a <= p.kv_cap;
+  if (room && p.paged.table)
+    for (int pos = L; room && pos <= L + a; pos = ((pos >> p.paged.shift) + 1) << p.paged.shift)
+      room = paged_row(p.paged, b, pos) >= 0;
   const bool draft_room = p.dk == nullptr || (p.draft_len[b] >= 0 && p.draft_len[b] < p.draft_cap);
   if (i == p.path_cap) {
     if (!room || !draft_room) {
@@ -99,9 +104,11 @@ __global__ void commit_kernel(const CommitParams p) {
   }
   if (i > a || !room || !draft_room) return;
   const int slot = p.path[static_cast<size_t>(b) * p.path_cap + i];
+  const size_t row = p.paged.table ? static_cast<size_t>(paged_row(p.paged, b, L + i))
+                                    : static_cast<size_t>(b) * p.kv_cap + L + i;
   for (int l = 0; l < p.n_layers; ++l) {
     const size_t src = (static_cast<size_t>(b) * p.S + slot) * p.row_elems;
-    const size_t dst = (static_cast<size_t>(b) * p.kv_cap + L + i) * p.row_elems;
+    const size_t dst = row * p.row_elems;
     copy_row(p.kc[l] + dst, p.kt[l] + src, p.row_elems);
     copy_row(p.vc[l] + dst, p.vt[l] + src, p.row_elems);
   }
@@ -121,6 +128,7 @@ cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st
   CommitParams p{};
   p.n_layers = C.n_layers;
   p.kv_cap = C.kv_cap;
+  p.paged = C.paged;
   p.S = C.tree->stride;
   p.E = ctx->lim.max_expanded;
   p.d = ctx->dims.d;

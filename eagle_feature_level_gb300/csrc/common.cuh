@@ -198,6 +198,14 @@ __device__ __forceinline__ void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Block-table addressing of a paged KV cache (PagedKv): the pool row of
+// position pos of request b, or -1 when that block is not allocated.
+__device__ __forceinline__ long long paged_row(const PagedKv& pg, int b, int pos) {
+  const int blk = pg.table[static_cast<size_t>(b) * pg.per_req + (pos >> pg.shift)];
+  if (blk < 0 || blk >= pg.n_blocks) return -1;
+  return (static_cast<long long>(blk) << pg.shift) + (pos & ((1 << pg.shift) - 1));
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

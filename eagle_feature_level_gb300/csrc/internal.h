@@ -184,8 +184,29 @@ cudaError_t launch_accept_walk(eagle_ctx* ctx, const eagle_plan* plan, int batch
                                const float* q_probs, const eagle_sampling* s, const eagle_accept_out* out,
                                void* ws, cudaStream_t st);
 
+// Block-table addressing of a paged KV cache: position pos of request b is
+// row pos % 2^shift of block table[b * per_req + pos / 2^shift] of the pool
+// (eagle_paging); table == nullptr: contiguous [B][cap] rows.
+struct PagedKv {
+  const int32_t* table;
+  int shift;              // log2(block_size)
+  int per_req;            // table entries per request (cap / block_size)
+  int n_blocks;
+};
+
+inline PagedKv paged_of(const eagle_paging* pg, int cap) {
+  PagedKv k{};
+  if (pg == nullptr || pg->block_table == nullptr) return k;
+  k.table = pg->block_table;
+  while ((1 << k.shift) < pg->block_size) ++k.shift;
+  k.per_req = cap / pg->block_size;
+  k.n_blocks = pg->n_blocks;
+  return k;
+}
+
 struct CommitLaunch {
   int batch, n_layers, kv_cap;
+  PagedKv paged;          // target caches
   const eagle_accept_out* acc;
   const eagle_tree* tree;
   const float* f_true;

@@ -80,12 +80,17 @@ class Engine:
             self.ctx = None
 
     def weights(self, W: Dict[str, torch.Tensor]) -> B.eagle_draft_weights:
+        """The ABI struct of the draft weights W.  The struct holds raw device
+        pointers, so it keeps a reference to W: the tensors live as long as
+        the struct does."""
         ld = lambda t: t.shape[1]
-        return B.eagle_draft_weights(
+        w_c = B.eagle_draft_weights(
             _p(W["w_fc"]), ld(W["w_fc"]), _p(W["b_fc"]), _p(W["g1"]), _p(W["wq"]), ld(W["wq"]), _p(W["wk"]),
             ld(W["wk"]), _p(W["wv"]), ld(W["wv"]), _p(W["wo"]), ld(W["wo"]), _p(W["g2"]), _p(W["w_gate"]),
             ld(W["w_gate"]), _p(W["w_up"]), ld(W["w_up"]), _p(W["w_down"]), ld(W["w_down"]), _p(W["embed"]),
             ld(W["embed"]), _p(W["w_lm"]), ld(W["w_lm"]))
+        w_c.tensors = dict(W)
+        return w_c
 
 
 def _packed(specs, device):

@@ -141,12 +141,34 @@ typedef struct {
   const uint16_t* w_lm;   int ld_lm;    /* [V][ld] frozen target LM head, in = d */
 } eagle_draft_weights;
 
-/* A KV cache of one attention layer: [B][cap][Hkv][dh] bf16. */
+/* Block-table (paged) addressing of a KV cache ([C] "工程落地时真正要看什么":
+ * the authoritative KV of accepted tokens lives in blocks that the serving
+ * system's cache manager allocates; [B] "KV Cache 必须按事务提交": the commit
+ * may land through block-table remapping, the logical state being the same).
+ * With block_table == NULL the cache is contiguous, [B][cap][Hkv][dh].
+ * Otherwise its k and v are block pools [n_blocks][block_size][Hkv][dh] and
+ * position p < cap of request b is row p % block_size of block
+ * block_table[b * (cap / block_size) + p / block_size]; a table entry < 0 (or
+ * >= n_blocks) marks a block that is not allocated.  block_size is a power of
+ * two that divides cap (EAGLE_ERR_INVALID_ARG otherwise).  The caller owns
+ * the table and the blocks: the library reads the table and never changes it.
+ * Rows of an unallocated block inside a request's length read as zeros and set
+ * EAGLE_ERR_INVALID_ARG in the status word; a commit whose rows would land in
+ * an unallocated block is refused (EAGLE_ERR_CAPACITY, see eagle_commit). */
+typedef struct {
+  const int32_t* block_table;  /* [B][cap / block_size] block ids (device), NULL: contiguous */
+  int block_size;              /* rows per block */
+  int n_blocks;                /* blocks in each pool */
+} eagle_paging;
+
+/* A KV cache of one attention layer: [B][cap][Hkv][dh] bf16, or block pools
+ * addressed through `paging` (all zero: contiguous). */
 typedef struct {
   uint16_t* k;
   uint16_t* v;
   int cap;                 /* rows per request */
   const int32_t* len;      /* [B] valid rows per request (device) */
+  eagle_paging paging;     /* target caches only: the draft cache stays contiguous */
 } eagle_kv;
 
 /* Per-round request inputs. */
@@ -299,7 +321,8 @@ eagle_status eagle_tree_expand_rerank(eagle_ctx* ctx, const eagle_plan* plan, in
  *   0..prefix.len[b]-1 and tree slots j < tree.size[b] with bit j of
  *   tree.anc[b][s]; kv head = h / (Hq / Hkv).  A length beyond the cache
  *   (prefix.len[b] > prefix.cap) is read as prefix.cap rows and sets
- *   EAGLE_ERR_CAPACITY in the status word.
+ *   EAGLE_ERR_CAPACITY in the status word.  The prefix may be paged
+ *   (prefix.paging): its rows are then read through the block table.
  * q: [B][S][Hq][dh] bf16; k_tree, v_tree: [B][S][Hkv][dh] bf16; out: [B][S][Hq][dh] fp32,
  * S = tree.stride.  Slots s >= tree.size[b] are not written. */
 eagle_status eagle_tree_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q,
@@ -396,18 +419,23 @@ typedef struct {
  * are simply not copied.
  * k_tree_layers / v_tree_layers / k_cache_layers / v_cache_layers are HOST
  * arrays of n_layers device pointers ([B][S][Hkv][dh] and [B][kv_cap][Hkv][dh]).
+ * target_paging (host pointer, NULL: contiguous caches) pages every target
+ * layer's cache through one block table: k_cache_layers[l] / v_cache_layers[l]
+ * are then layer l's block pools and row L_b + i lands in the block that the
+ * table maps position L_b + i to (eagle_paging).
  * f_true: [B][S][d] fp32.  Output buffers must not alias inputs.
  * Capacity (checked on the device, where the lengths live): a request whose
  * target cache cannot take its 1 + a rows (L_b + 1 + a > kv_cap), or whose
  * draft cache is full (draft_kv.len[b] >= draft_kv.cap), is not committed:
  * no cache row of it is written, prefix_len / draft_len keep the old
  * lengths, its other outputs are unspecified, and EAGLE_ERR_CAPACITY is set
- * in the workspace's status word. */
+ * in the workspace's status word.  With target_paging, a request any of whose
+ * 1 + a rows maps to an unallocated block is refused the same way. */
 eagle_status eagle_commit(eagle_ctx* ctx, int batch, const eagle_accept_out* acc,
                           const eagle_tree* tree, const float* f_true, int n_layers,
                           const uint16_t* const* k_tree_layers, const uint16_t* const* v_tree_layers,
                           uint16_t* const* k_cache_layers, uint16_t* const* v_cache_layers,
-                          int kv_cap, const int32_t* target_kv_len,
+                          int kv_cap, const int32_t* target_kv_len, const eagle_paging* target_paging,
                           const eagle_draft_out* draft, const eagle_kv* draft_kv,
                           const eagle_commit_out* out, void* workspace, cudaStream_t stream);
 
