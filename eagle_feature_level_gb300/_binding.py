@@ -13,7 +13,7 @@ import os
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libeagle.so")
 
-EAGLE_MAX_NODES = 64
+EAGLE_MAX_NODES = 256
 EAGLE_MAX_CHILDREN = 16
 EAGLE_MAX_LAYERS = 128
 EAGLE_MAX_VOCAB = 32768
@@ -53,8 +53,8 @@ class eagle_limits(C.Structure):
 class eagle_plan(C.Structure):
     _fields_ = [("kind", I), ("top_k", I), ("depth", I), ("top_m", I), ("n_expanded", I), ("n_layers", I),
                 ("layer_e0", I * EAGLE_MAX_NODES), ("layer_rows", I * EAGLE_MAX_NODES), ("n_nodes", I),
-                ("node_parent", C.c_int8 * EAGLE_MAX_NODES), ("node_rank", C.c_int8 * EAGLE_MAX_NODES),
-                ("node_depth", C.c_int8 * EAGLE_MAX_NODES), ("node_exp", C.c_int8 * EAGLE_MAX_NODES)]
+                ("node_parent", C.c_int16 * EAGLE_MAX_NODES), ("node_rank", C.c_int16 * EAGLE_MAX_NODES),
+                ("node_depth", C.c_int16 * EAGLE_MAX_NODES), ("node_exp", C.c_int16 * EAGLE_MAX_NODES)]
 
 
 class eagle_draft_weights(C.Structure):
@@ -222,8 +222,8 @@ def eagle_plan_eagle2(top_k: int, depth: int, top_m: int) -> eagle_plan:
 
 def eagle_plan_static(parents, ranks) -> eagle_plan:
     n = len(parents)
-    par = (C.c_int8 * max(n, 1))(*parents)
-    rk = (C.c_int8 * max(n, 1))(*ranks)
+    par = (C.c_int16 * max(n, 1))(*parents)
+    rk = (C.c_int16 * max(n, 1))(*ranks)
     p = eagle_plan()
     _check("eagle_plan_static", lib().eagle_plan_static(C.byref(p), n, C.cast(par, P), C.cast(rk, P)))
     return p

@@ -368,7 +368,8 @@ eagle_status eagle_plan_eagle2(eagle_plan* out, int top_k, int depth, int top_m)
   return EAGLE_OK;
 }
 
-eagle_status eagle_plan_static(eagle_plan* out, int n_nodes, const int8_t* node_parent, const int8_t* node_rank) {
+eagle_status eagle_plan_static(eagle_plan* out, int n_nodes, const int16_t* node_parent,
+                               const int16_t* node_rank) {
   EAGLE_REQUIRE(out && node_parent && node_rank, EAGLE_ERR_INVALID_ARG);
   EAGLE_REQUIRE(n_nodes >= 1 && n_nodes + 1 <= EAGLE_MAX_NODES, EAGLE_ERR_CAPACITY);
   eagle_plan p;
@@ -383,17 +384,17 @@ eagle_status eagle_plan_static(eagle_plan* out, int n_nodes, const int8_t* node_
     EAGLE_REQUIRE(r >= 0 && r < EAGLE_MAX_CHILDREN, EAGLE_ERR_INVALID_TREE);
     for (int j = 0; j < i; ++j)
       EAGLE_REQUIRE(!(node_parent[j] == par && node_rank[j] == r), EAGLE_ERR_INVALID_TREE);
-    p.node_parent[i] = static_cast<int8_t>(par);
-    p.node_rank[i] = static_cast<int8_t>(r);
+    p.node_parent[i] = static_cast<int16_t>(par);
+    p.node_rank[i] = static_cast<int16_t>(r);
     const int dep = par < 0 ? 1 : p.node_depth[par] + 1;
     EAGLE_REQUIRE(i == 0 || dep >= p.node_depth[i - 1], EAGLE_ERR_INVALID_TREE);   // listed by depth
-    p.node_depth[i] = static_cast<int8_t>(dep);
+    p.node_depth[i] = static_cast<int16_t>(dep);
     if (par >= 0) has_child[par] = true;
     kmax = std::max(kmax, r + 1);
     dmax = std::max(dmax, dep);
   }
   int e = 1;
-  for (int i = 0; i < n_nodes; ++i) p.node_exp[i] = has_child[i] ? static_cast<int8_t>(e++) : -1;
+  for (int i = 0; i < n_nodes; ++i) p.node_exp[i] = has_child[i] ? static_cast<int16_t>(e++) : -1;
   EAGLE_REQUIRE(e <= EAGLE_MAX_NODES, EAGLE_ERR_CAPACITY);
   p.top_k = kmax;
   p.depth = dmax;

@@ -32,6 +32,7 @@ constexpr int WARPS = THREADS / 32;
 constexpr int MAX_DH = 128;
 constexpr int RW = 8;             // CUDA-core kernel: query rows a warp owns in one pass, at most
 constexpr int ROWS_PASS = WARPS * RW;   // query rows per pass (tensor-core kernel: two 16-row tiles)
+constexpr int MASKW = EAGLE_MASK_WORDS(EAGLE_MAX_NODES);   // ancestor-mask words a row can have
 constexpr int KLD = MAX_DH + 8;   // bf16 row pitch in shared memory (elements): ldmatrix rows hit distinct banks
 constexpr int MLD = MAX_DH + 4;   // fp32 row pitch of a warp's softmax state in the intra-CTA merge
 
@@ -62,7 +63,8 @@ struct AttnParams {
   const uint16_t* kt_bf16;        // verify: tree K/V [B][S][Hkv][dh] bf16
   const uint16_t* vt_bf16;
   int tree_cap;                   // E or S
-  const uint64_t* anc;            // draft: pool.anc [B][E]; verify: tree.anc [B][S]
+  const uint64_t* anc;            // draft: pool.anc [B][E][W]; verify: tree.anc [B][S][W]
+  int mask_words;                 // W = EAGLE_MASK_WORDS(tree_cap)
   const int32_t* tree_size;       // verify: [B]
   int e0;                         // draft: first expanded slot of this layer
   float scale;
@@ -94,9 +96,17 @@ __device__ __forceinline__ size_t q_index(const AttnParams& p, int b, int node, 
   return ((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * p.dh;
 }
 
-__device__ __forceinline__ uint64_t row_mask(const AttnParams& p, int b, int node) {
-  if (p.mode == 0) return p.anc[static_cast<size_t>(b) * p.tree_cap + p.e0 + node];
-  return p.anc[static_cast<size_t>(b) * p.tree_cap + node];
+// Word w of a query row's ancestor mask (tree keys j with bit j % 64 of
+// word j / 64 set are visible to the row).
+__device__ __forceinline__ uint64_t row_mask(const AttnParams& p, int b, int node, int w) {
+  const size_t slot = static_cast<size_t>(b) * p.tree_cap + (p.mode == 0 ? p.e0 + node : node);
+  return p.anc[slot * p.mask_words + w];
+}
+
+// A query row's mask words into shared memory (MASKW per row, unused ones zero).
+__device__ __forceinline__ void load_row_mask(const AttnParams& p, uint64_t* dst, int b, int node) {
+#pragma unroll
+  for (int w = 0; w < MASKW; ++w) dst[w] = w < p.mask_words ? row_mask(p, b, node, w) : 0ull;
 }
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t policy) {
@@ -249,11 +259,14 @@ __device__ __forceinline__ void tile_compute(const AttnParams& p, RowState<NR>& 
 #pragma unroll
   for (int i = 0; i < NR; ++i) {
     if (i < nr) {
-      // tree keys: bit (key_base + j) of the row's ancestor mask (one tile of <= 64 slots)
-      const uint64_t mask = is_tree ? s_mask[warp * RW + i] : ~0ull;
+      // tree keys: bit key_base + j of the row's ancestor mask; a tile (64
+      // bf16 or 32 fp32 keys, starting at a multiple of its size) lies in
+      // one mask word
+      const uint64_t mask = is_tree ? s_mask[(warp * RW + i) * MASKW + (key_base >> 6)] : ~0ull;
+      const int kb = key_base & 63;
       const int j0 = lane, j1 = lane + 32;
-      const bool v0 = j0 < nt && ((mask >> (key_base + j0)) & 1ull);
-      const bool v1 = !F32 && j1 < nt && ((mask >> (key_base + (j1 & 63))) & 1ull);
+      const bool v0 = j0 < nt && ((mask >> (kb + j0)) & 1ull);
+      const bool v1 = !F32 && j1 < nt && ((mask >> (kb + (j1 & 63))) & 1ull);
       const float a = v0 ? s0[i] * p.scale : -INFINITY;
       const float c = v1 ? s1[i] * p.scale : -INFINITY;
       const float m_new = fmaxf(st.m[i], warp_max_redux(fmaxf(a, c)));
@@ -324,7 +337,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
   }
   extern __shared__ __align__(16) uint8_t smem_attn[];
   __shared__ int s_last;
-  __shared__ uint64_t s_mask[ROWS_PASS];     // ancestor masks of the tree part's rows
+  __shared__ uint64_t s_mask[ROWS_PASS * MASKW];   // ancestor masks of the tree part's rows
 
   const int split = blockIdx.x;              // split == n_splits: the tree part
   const int pair = blockIdx.y;
@@ -394,7 +407,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
       *reinterpret_cast<float4*>(sq + rr * dh + 4 * c) = v;
     }
     if (is_tree && lane < RW && lane < nr)
-      s_mask[warp * RW + lane] = row_mask(p, b, (r0 + warp + WARPS * lane) / p.G);
+      load_row_mask(p, s_mask + (warp * RW + lane) * MASKW, b, (r0 + warp + WARPS * lane) / p.G);
     RowState<NR> st;
 #pragma unroll
     for (int i = 0; i < NR; ++i) {
@@ -765,7 +778,7 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
   pdl_trigger();
   extern __shared__ __align__(16) uint8_t smem_attn[];
   __shared__ int s_last;
-  __shared__ uint64_t s_mask[ROWS_PASS];     // ancestor masks of the pass's rows (tree part)
+  __shared__ uint64_t s_mask[ROWS_PASS * MASKW];   // ancestor masks of the pass's rows (tree part)
 
   const int split = blockIdx.x;              // split == n_splits: the tree part
   const int pair = blockIdx.y;
@@ -853,8 +866,14 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
       *reinterpret_cast<uint2*>(qhi + rr * KLD + 4 * c) = wh;
       if (p.mode == 0) *reinterpret_cast<uint2*>(qlo + rr * KLD + 4 * c) = wl;
     }
-    if (is_tree && threadIdx.x < ROWS_PASS)
-      s_mask[threadIdx.x] = threadIdx.x < rp ? row_mask(p, b, (r0 + threadIdx.x) / p.G) : 0ull;
+    if (is_tree && threadIdx.x < ROWS_PASS) {
+      if (threadIdx.x < rp) {
+        load_row_mask(p, s_mask + threadIdx.x * MASKW, b, (r0 + threadIdx.x) / p.G);
+      } else {
+#pragma unroll
+        for (int w = 0; w < MASKW; ++w) s_mask[threadIdx.x * MASKW + w] = 0ull;
+      }
+    }
     WarpState st;
     st.m[0] = st.m[1] = -INFINITY;
     st.l[0] = st.l[1] = 0.f;
@@ -881,10 +900,12 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
       const int k_lo = ks * kpw;
       if (k_lo < nt) {
         const uint16_t* buf = reinterpret_cast<const uint16_t*>(bufs + which * TILE_BYTES);
-        const uint64_t ma = is_tree ? s_mask[16 * mt + (lane >> 2)] : ~0ull;
-        const uint64_t mb = is_tree ? s_mask[16 * mt + (lane >> 2) + 8] : ~0ull;
+        // a tree tile lies in one mask word (it starts at a multiple of its size)
+        const int mw = is_tree ? (t0 >> 6) : 0;
+        const uint64_t ma = is_tree ? s_mask[(16 * mt + (lane >> 2)) * MASKW + mw] : ~0ull;
+        const uint64_t mb = is_tree ? s_mask[(16 * mt + (lane >> 2) + 8) * MASKW + mw] : ~0ull;
         const uint16_t* ql = p.mode == 0 ? qlo : nullptr;
-        const int kb = is_tree ? t0 : 0;
+        const int kb = is_tree ? (t0 & 63) : 0;
         if (kpw == 32)
           tile_mma<4>(p, st, buf, tree_f32, qhi, ql, mt, k_lo, nt, kb, is_tree, ma, mb, lane);
         else
@@ -1069,6 +1090,7 @@ cudaError_t launch_draft_attn(eagle_ctx* ctx, const DraftLaunch& L, cudaStream_t
   p.vt_f32 = L.out->v_tree;
   p.tree_cap = ctx->lim.max_expanded;
   p.anc = L.pool->anc;
+  p.mask_words = EAGLE_MASK_WORDS(p.tree_cap);
   p.e0 = L.e0;
   p.scale = 1.0f / sqrtf(static_cast<float>(D.head_dim));
   p.b_o = ws_ptr<uint16_t>(L.ws, W.b_o);
@@ -1103,6 +1125,7 @@ cudaError_t launch_verify_attn(eagle_ctx* ctx, int batch, const uint16_t* q, con
   p.vt_bf16 = vt;
   p.tree_cap = tree->stride;
   p.anc = tree->anc;
+  p.mask_words = EAGLE_MASK_WORDS(p.tree_cap);
   p.tree_size = tree->size;
   p.scale = scale;
   p.out_f32 = out;
@@ -1189,6 +1212,7 @@ eagle_status launch_verify_attn_noalloc(eagle_ctx* ctx, int batch, const uint16_
   p.vt_bf16 = vt;
   p.tree_cap = tree->stride;
   p.anc = tree->anc;
+  p.mask_words = EAGLE_MASK_WORDS(p.tree_cap);
   p.tree_size = tree->size;
   p.scale = scale;
   p.out_f32 = out;

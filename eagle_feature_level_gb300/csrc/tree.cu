@@ -12,6 +12,10 @@
 //             kept set is a connected tree.  Static -- every template node.
 //             Then flatten: slots 1..m by (depth asc, selection rank asc),
 //             parent slots, positions, ancestor bitmasks.
+// Ancestor masks take EAGLE_MASK_WORDS(n) words per slot (n = expanded
+// slots for the pool, tree slots for the tree): bit j is bit j % 64 of word
+// j / 64.  A tree slot's mask is built by its own thread walking the parent
+// chain to the root, every word in registers.
 // Ranks come from counting (each thread compares its key with every other
 // valid key), which is exact and independent of thread order.  Node values
 // are non-negative fp64 products, whose bit patterns order like the values
@@ -24,12 +28,13 @@ namespace eagle {
 namespace {
 
 constexpr int TREE_THREADS = 1024;
-constexpr int MAX_POOL = EAGLE_MAX_NODES * EAGLE_MAX_CHILDREN;
+constexpr int MAX_WORDS = EAGLE_MASK_WORDS(EAGLE_MAX_NODES);
 
 struct TreeParams {
   eagle_plan plan;
   int phase, layer;
   int E, K, S;
+  int WE, WS;                     // mask words per pool slot, per tree slot
   const int32_t* t_next;
   const int32_t* pos0;
   const int32_t* ctok;
@@ -65,17 +70,31 @@ __device__ __forceinline__ uint64_t value_key(double v) {
   return static_cast<uint64_t>(__double_as_longlong(v));
 }
 
+// Mask word w of the pool slot e of request b (pb = b * E).
+__device__ __forceinline__ uint64_t& pool_anc(const TreeParams& p, size_t pb, int e, int w) {
+  return p.p_anc[(pb + e) * p.WE + w];
+}
+
+// Dynamic shared memory of the kernel: the E * K drawn candidates of a
+// request and the parent slot of every tree slot.
+size_t tree_smem_bytes(int E, int K, int S) {
+  const size_t n = static_cast<size_t>(E) * K;
+  return n * (sizeof(double) + sizeof(uint64_t) + 3 * sizeof(int)) + static_cast<size_t>(S) * sizeof(int);
+}
+
 __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) {
   const LaunchStamp ls(p.stamp);
   pdl_wait();      // predecessor outputs visible from here on
   ls.waited();
   pdl_trigger();
-  __shared__ double s_val[MAX_POOL];
-  __shared__ uint64_t s_key[MAX_POOL];
-  __shared__ int s_dep[MAX_POOL];
-  __shared__ int s_rank[MAX_POOL];
-  __shared__ int s_slot[MAX_POOL];
-  __shared__ int s_parent_slot[EAGLE_MAX_NODES];
+  extern __shared__ __align__(16) uint8_t smem_tree[];
+  const int n_pool = p.E * p.K;
+  double* s_val = reinterpret_cast<double*>(smem_tree);
+  uint64_t* s_key = reinterpret_cast<uint64_t*>(s_val + n_pool);
+  int* s_dep = reinterpret_cast<int*>(s_key + n_pool);
+  int* s_rank = s_dep + n_pool;
+  int* s_slot = s_rank + n_pool;
+  int* s_parent_slot = s_slot + n_pool;
   __shared__ int s_count;
 
   const int b = blockIdx.x;
@@ -93,7 +112,7 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
       p.p_rank[pb + e] = 0;
       p.p_depth[pb + e] = 0;
       p.p_value[pb + e] = root ? 1.0 : -1.0;
-      p.p_anc[pb + e] = root ? 1ull : 0ull;
+      for (int w = 0; w < p.WE; ++w) pool_anc(p, pb, e, w) = root && w == 0 ? 1ull : 0ull;
     }
     return;
   }
@@ -114,7 +133,9 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
         p.p_depth[pb + e_new] = l;
         p.p_value[pb + e_new] =
             ok ? p.p_value[pb + par_e] * static_cast<double>(p.cprob[(pb + par_e) * K + r]) : -1.0;
-        p.p_anc[pb + e_new] = ok ? (p.p_anc[pb + par_e] | (1ull << e_new)) : 0ull;
+        for (int w = 0; w < p.WE; ++w)
+          pool_anc(p, pb, e_new, w) =
+              ok ? (pool_anc(p, pb, par_e, w) | (w == (e_new >> 6) ? 1ull << (e_new & 63) : 0ull)) : 0ull;
         if (ok) p.p_child_exp[(pb + par_e) * K + r] = e_new;
       }
       return;
@@ -148,7 +169,8 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
       p.p_rank[pb + e_new] = r;
       p.p_depth[pb + e_new] = p.p_depth[pb + e] + 1;
       p.p_value[pb + e_new] = s_val[c];
-      p.p_anc[pb + e_new] = p.p_anc[pb + e] | (1ull << e_new);
+      for (int w = 0; w < p.WE; ++w)
+        pool_anc(p, pb, e_new, w) = pool_anc(p, pb, e, w) | (w == (e_new >> 6) ? 1ull << (e_new & 63) : 0ull);
       p.p_child_exp[(pb + e) * K + r] = e_new;
     }
     for (int i = tid; i < n_new; i += TREE_THREADS) {
@@ -159,7 +181,7 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
       p.p_rank[pb + e_new] = 0;
       p.p_depth[pb + e_new] = l;
       p.p_value[pb + e_new] = -1.0;
-      p.p_anc[pb + e_new] = 0ull;
+      for (int w = 0; w < p.WE; ++w) pool_anc(p, pb, e_new, w) = 0ull;
     }
     return;
   }
@@ -246,33 +268,46 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
       p.t_child_slot[(pb + e) * K + r] = s;
     }
   }
+  if (tid == 0) s_parent_slot[0] = -1;
   __syncthreads();
+  const int size = 1 + n_sel;
   if (tid == 0) {
-    const int size = 1 + n_sel;
     p.t_size[b] = size;
     p.t_token[tb] = p.p_token[pb];
     p.t_parent[tb] = -1;
     p.t_depth[tb] = 0;
     p.t_pos[tb] = p.pos0[b];
     p.t_exp[tb] = 0;
-    uint64_t anc[EAGLE_MAX_NODES];
-    anc[0] = 1ull;
-    p.t_anc[tb] = 1ull;
-    for (int s = 1; s < size; ++s) {
-      const int ps = s_parent_slot[s];
-      const bool ok = ps >= 0 && ps < s;
-      anc[s] = (ok ? anc[ps] : 0ull) | (1ull << s);
-      if (!ok) set_status(p.status, EAGLE_ERR_INVALID_TREE);
-      p.t_anc[tb + s] = anc[s];
-    }
-    for (int s = size; s < S; ++s) {
+  }
+  // ancestor-or-self masks: slot s walks its parent chain (parents precede
+  // their children, so the walk ends at the root within s steps)
+  for (int s = tid; s < S; s += TREE_THREADS) {
+    uint64_t m[MAX_WORDS];
+#pragma unroll
+    for (int w = 0; w < MAX_WORDS; ++w) m[w] = 0ull;
+    if (s < size) {
+      int u = s;
+      for (int steps = 0; u >= 0 && steps <= s; ++steps) {
+#pragma unroll
+        for (int w = 0; w < MAX_WORDS; ++w)
+          if (w == (u >> 6)) m[w] |= 1ull << (u & 63);
+        const int pu = u == 0 ? -1 : s_parent_slot[u];
+        if (u != 0 && !(pu >= 0 && pu < u)) {
+          set_status(p.status, EAGLE_ERR_INVALID_TREE);
+          break;
+        }
+        u = pu;
+      }
+    } else {
       p.t_token[tb + s] = -1;
       p.t_parent[tb + s] = -1;
       p.t_depth[tb + s] = 0;
       p.t_pos[tb + s] = 0;
       p.t_exp[tb + s] = -1;
-      p.t_anc[tb + s] = 0ull;
     }
+#pragma unroll
+    for (int w = 0; w < MAX_WORDS; ++w)
+      if (w < p.WS) p.t_anc[(tb + s) * p.WS + w] = m[w];
   }
 }
 
@@ -287,6 +322,7 @@ cudaError_t launch_tree(eagle_ctx* ctx, const eagle_plan* plan, int phase, int l
   p.layer = layer;
   p.E = ctx->lim.max_expanded;
   p.K = ctx->lim.max_children;
+  p.WE = EAGLE_MASK_WORDS(p.E);
   p.t_next = req ? req->t_next : nullptr;
   p.pos0 = req ? req->pos0 : nullptr;
   p.ctok = ch ? ch->token : nullptr;
@@ -300,6 +336,7 @@ cudaError_t launch_tree(eagle_ctx* ctx, const eagle_plan* plan, int phase, int l
   p.p_child_exp = pool->child_exp;
   if (tree) {
     p.S = tree->stride;
+    p.WS = EAGLE_MASK_WORDS(p.S);
     p.t_token = tree->token;
     p.t_parent = tree->parent;
     p.t_depth = tree->depth;
@@ -311,8 +348,15 @@ cudaError_t launch_tree(eagle_ctx* ctx, const eagle_plan* plan, int phase, int l
   }
   p.status = status;
   p.stamp = stamp_slot(ctx, EAGLE_K_TREE);
+  const size_t smem = tree_smem_bytes(p.E, p.K, tree ? p.S : 1);
+  {
+    // the attribute is set once per context, to what the largest limits need
+    const size_t most = tree_smem_bytes(EAGLE_MAX_NODES, EAGLE_MAX_CHILDREN, EAGLE_MAX_NODES);
+    const cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(tree_kernel), static_cast<int>(most));
+    if (e != cudaSuccess) return e;
+  }
   trace_before(ctx, EAGLE_K_TREE, st);
-  const cudaError_t e = launch_pdl(tree_kernel, dim3(batch), dim3(TREE_THREADS), 0, st, p);
+  const cudaError_t e = launch_pdl(tree_kernel, dim3(batch), dim3(TREE_THREADS), smem, st, p);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_TREE, st);
   return e;

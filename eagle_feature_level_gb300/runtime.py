@@ -12,6 +12,7 @@ from __future__ import annotations
 import math
 from typing import Dict, List, Optional
 
+import numpy as np
 import torch
 
 from . import _binding as B
@@ -38,6 +39,8 @@ STATIC_TEMPLATES = {
         (0, 0, 0, 0), (0, 0, 0, 1), (0, 0, 1, 0), (0, 1, 0, 0), (1, 0, 0, 0),
         (0, 0, 0, 0, 0), (0, 0, 0, 0, 1),
     ],
+    # complete ternary tree, depths 1..4 (120 nodes, 40 of them expanded)
+    "ternary4": [tuple(int(c) for c in np.base_repr(i, 3).zfill(n)) for n in range(1, 5) for i in range(3 ** n)],
 }
 
 
@@ -91,6 +94,11 @@ class Engine:
             ld(W["embed"]), _p(W["w_lm"]), ld(W["w_lm"]))
         w_c.tensors = dict(W)
         return w_c
+
+
+def mask_words(n: int) -> int:
+    """64-bit words per slot of an ancestor mask over n slots (EAGLE_MASK_WORDS)."""
+    return (n + 63) // 64
 
 
 def _packed(specs, device):
@@ -147,7 +155,7 @@ class Round:
         self.p_rank = z(batch, E, **i32)
         self.p_depth = z(batch, E, **i32)
         self.p_value = z(batch, E, dtype=torch.float64, device=dev)
-        self.p_anc = z(batch, E, dtype=torch.int64, device=dev)
+        self.p_anc = z(batch, E, mask_words(E), dtype=torch.int64, device=dev)
         self.p_child_exp = z(batch, E, K, **i32)
         self.c_token = z(batch, E, K, **i32)
         self.c_prob = z(batch, E, K, **f32)
@@ -162,7 +170,7 @@ class Round:
         self.t_depth = z(batch, S, **i32)
         self.t_pos = z(batch, S, **i32)
         self.t_exp = z(batch, S, **i32)
-        self.t_anc = z(batch, S, dtype=torch.int64, device=dev)
+        self.t_anc = z(batch, S, mask_words(S), dtype=torch.int64, device=dev)
         self.t_child_slot = z(batch, E, K, **i32)
         self.t_size = z(batch, **i32)
         # verification layer(s) and the target's outputs

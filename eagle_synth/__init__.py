@@ -170,7 +170,7 @@ def max_expanded(w: Workload) -> int:
     if w.tree == "eagle2":
         return 1 + w.top_k * (w.depth - 1)
     # static templates: fixed by name
-    return {"chain4": 4, "static8": 4, "static26": 14}[w.tree]
+    return {"chain4": 4, "static8": 4, "static26": 14, "ternary4": 40}[w.tree]
 
 
 def round_inputs(w: Workload, seed: int, device="cpu") -> Dict[str, object]:

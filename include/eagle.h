@@ -41,7 +41,7 @@
  *    children (e, r), r = draw rank.  Layer l of the plan runs the draft head
  *    on slots [layer_e0[l], layer_e0[l] + layer_rows[l]) of every request.
  *  - The verified tree has S = 1 + m slots per request: slot 0 = root, slots
- *    1..m sorted by (depth, selection rank).  anc[s] bit j is set iff slot j
+ *    1..m sorted by (depth, selection rank).  anc[s] bit j (word j / 64) is set iff slot j
  *    is an ancestor of s or j == s ([B] "Tree Attention": M_uv = 0 iff v is
  *    an ancestor of u or v = u).  A node at depth delta sits at position
  *    L_b + delta.
@@ -70,7 +70,11 @@ typedef enum {
   EAGLE_ERR_CUDA = 9           /* a CUDA runtime call failed */
 } eagle_status;
 
-#define EAGLE_MAX_NODES 64     /* tree slots and expanded slots per request (u64 masks) */
+#define EAGLE_MAX_NODES 256    /* tree slots and expanded slots per request */
+/* Ancestor masks over n slots take EAGLE_MASK_WORDS(n) 64-bit words per
+ * slot: bit j of a mask is bit j % 64 of word j / 64.  Up to 64 slots that is
+ * one word, so trees of up to 63 retained nodes keep one u64 per slot. */
+#define EAGLE_MASK_WORDS(n) (((n) + 63) / 64)
 #define EAGLE_MAX_CHILDREN 16  /* drawn children per expanded node */
 #define EAGLE_MAX_LAYERS 128   /* target layers one commit can append */
 #define EAGLE_MAX_VOCAB 32768  /* keeps every exact sampling product below 2^128 */
@@ -118,10 +122,10 @@ typedef struct {
   int layer_e0[EAGLE_MAX_NODES];        /* first expanded slot of draft layer l */
   int layer_rows[EAGLE_MAX_NODES];      /* expanded slots of draft layer l */
   int n_nodes;                          /* kind 1: template nodes */
-  int8_t node_parent[EAGLE_MAX_NODES];  /* kind 1: template index of the parent, -1 root */
-  int8_t node_rank[EAGLE_MAX_NODES];    /* kind 1: child number under the parent */
-  int8_t node_depth[EAGLE_MAX_NODES];   /* filled by eagle_plan_static */
-  int8_t node_exp[EAGLE_MAX_NODES];     /* filled: expanded slot of the node or -1 */
+  int16_t node_parent[EAGLE_MAX_NODES]; /* kind 1: template index of the parent, -1 root */
+  int16_t node_rank[EAGLE_MAX_NODES];   /* kind 1: child number under the parent */
+  int16_t node_depth[EAGLE_MAX_NODES];  /* filled by eagle_plan_static */
+  int16_t node_exp[EAGLE_MAX_NODES];    /* filled: expanded slot of the node or -1 */
 } eagle_plan;
 
 /* Draft head weights.  bf16 matrices [out][ld]; fp32 vectors. */
@@ -189,7 +193,8 @@ typedef struct {
   uint32_t round_id;
 } eagle_sampling;
 
-/* Expanded-node pool ([A] §10.3: the EAGLE-2 candidate set), [B][E] arrays. */
+/* Expanded-node pool ([A] §10.3: the EAGLE-2 candidate set), [B][E] arrays
+ * with E = max_expanded; anc is [B][E][EAGLE_MASK_WORDS(E)]. */
 typedef struct {
   int32_t* token;       /* -1 marks an inactive slot */
   int32_t* parent;      /* expanded slot of the parent, -1 for the root */
@@ -215,7 +220,8 @@ typedef struct {
   float* v_tree;        /* [B][E][Hkv][dh] fp32 */
 } eagle_draft_out;
 
-/* Flattened verification tree, [B][S] arrays with S = tree stride. */
+/* Flattened verification tree, [B][S] arrays with S = tree stride; anc is
+ * [B][S][EAGLE_MASK_WORDS(S)]. */
 typedef struct {
   int32_t* token;
   int32_t* parent;      /* tree slot of the parent, -1 for slot 0 */
@@ -270,8 +276,8 @@ eagle_status eagle_plan_eagle2(eagle_plan* out, int top_k, int depth, int top_m)
 
 /* Static plan from a template given as (parent, rank) per node, listed by
  * depth; every node's parent must precede it.  top_k = 1 + max rank. */
-eagle_status eagle_plan_static(eagle_plan* out, int n_nodes, const int8_t* node_parent,
-                               const int8_t* node_rank);
+eagle_status eagle_plan_static(eagle_plan* out, int n_nodes, const int16_t* node_parent,
+                               const int16_t* node_rank);
 
 /* ---- the round ------------------------------------------------------------ */
 

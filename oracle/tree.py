@@ -26,6 +26,7 @@ EAGLE-2 (Page A Â§10.3; Page C "EAGLE-2ï¼šå›ºå®šæ ‘å˜æˆä¸Šä¸‹æ–‡æ„ŸçŸ¥åŠ¨æ€æ 
 from __future__ import annotations
 
 import dataclasses
+import itertools
 from typing import Dict, List, Optional, Sequence, Tuple
 
 # Static templates: rank paths below the root (reading: the pages give no
@@ -41,6 +42,9 @@ STATIC_TEMPLATES: Dict[str, List[Tuple[int, ...]]] = {
         (0, 0, 0, 0), (0, 0, 0, 1), (0, 0, 1, 0), (0, 1, 0, 0), (1, 0, 0, 0),
         (0, 0, 0, 0, 0), (0, 0, 0, 0, 1),
     ],
+    # the complete ternary tree of depth 4: 3 + 9 + 27 + 81 = 120 nodes, a
+    # template beyond the 63 nodes one 64-bit ancestor mask can cover
+    "ternary4": [path for depth in range(1, 5) for path in itertools.product(range(3), repeat=depth)],
 }
 
 

@@ -86,6 +86,18 @@ def round_on(eng, rd, w_c, inp, inputs_cpu):
     return out
 
 
+def mask_ints(words) -> list:
+    """Ancestor masks stored as [n][W] int64 words -> n Python ints (bit j of
+    a mask is bit j % 64 of word j / 64)."""
+    out = []
+    for row in words.tolist():
+        v = 0
+        for w, x in enumerate(row):
+            v |= (int(x) & 0xFFFFFFFFFFFFFFFF) << (64 * w)
+        out.append(v)
+    return out
+
+
 def _f64(t):
     return t.to(torch.float64).numpy() if torch.is_tensor(t) else np.asarray(t, dtype=np.float64)
 
@@ -422,7 +434,7 @@ def compare_round(w, gpu, ref, requests=None):
             if got != list(want):
                 fail(f"b{b} tree {name}: {got} vs {list(want)}")
                 tree_ok = False
-        anc = [int(x) & 0xFFFFFFFFFFFFFFFF for x in gpu["t_anc"][b, :size]]
+        anc = mask_ints(gpu["t_anc"][b, :size])
         if anc != list(tr.anc):
             fail(f"b{b} tree anc differs")
             tree_ok = False

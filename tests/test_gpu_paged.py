@@ -28,7 +28,7 @@ from eagle_feature_level_gb300 import runtime as R
 from eagle_feature_level_gb300.runtime import _p
 from eagle_feature_level_gb300.workload import dims_of, limits_for, load_round, standin
 from oracle.verify import tree_attention
-from tests.gpu_harness import feature_tol
+from tests.gpu_harness import feature_tol, mask_ints
 
 pytestmark = pytest.mark.gpu
 
@@ -125,7 +125,7 @@ def test_paged_verify_equals_contiguous_and_oracle(bs):
         assert torch.equal(got[b, :n], want[b, :n]), b
         assert torch.isnan(got[b, n:]).all()               # slots past the tree are not written
         L = int(rd.tgt_len[b])
-        anc = [int(x) & 0xFFFFFFFFFFFFFFFF for x in rd.t_anc[b, :n].tolist()]
+        anc = mask_ints(rd.t_anc[b, :n])
         f = lambda t: t.double().cpu().numpy()
         ref = tree_attention(f(rd.tree_q[b, :n]), f(rd.tree_k[0][b, :n]), f(rd.tree_v[0][b, :n]),
                              f(rd.tgt_k[0][b, :L]), f(rd.tgt_v[0][b, :L]), anc, 1.0 / math.sqrt(W.head_dim))

@@ -28,6 +28,18 @@ SMALL = {
     "small_rows160_two_mma": S.variant("70b_x16_eagle2", name="small_rows160_two_mma", d=128, n_q_heads=4,
                                        n_kv_heads=2, head_dim=32, d_ff=256, vocab=700, prefix_len=64,
                                        weight_std=0.05),
+    # trees past 63 nodes (multi-word ancestor masks): EAGLE-2 pools of 73 and
+    # 71 expanded slots (two mask words) with trees of 121 and 256 slots (two
+    # and four words), and a 120-node static template
+    "small_eagle2_m120_k8_d10": S.variant("70b_x16_eagle2", name="small_eagle2_m120_k8_d10", d=128, n_q_heads=4,
+                                          n_kv_heads=2, head_dim=32, d_ff=256, vocab=700, batch=2, prefix_len=64,
+                                          top_k=8, depth=10, top_m=120, weight_std=0.05),
+    "small_eagle2_m255_k10_d8": S.variant("70b_x16_eagle2", name="small_eagle2_m255_k10_d8", d=128, n_q_heads=4,
+                                          n_kv_heads=2, head_dim=32, d_ff=256, vocab=1500, batch=2, prefix_len=90,
+                                          top_k=10, depth=8, top_m=255, weight_std=0.05),
+    "small_ternary4_m120": S.variant("7b_static26", name="small_ternary4_m120", tree="ternary4", top_k=3, depth=4,
+                                     top_m=120, d=128, n_q_heads=2, n_kv_heads=2, head_dim=64, d_ff=344, vocab=900,
+                                     prefix_len=70, weight_std=0.05),
 }
 
 

@@ -20,6 +20,7 @@ from eagle_feature_level_gb300.runtime import _p
 from eagle_feature_level_gb300.workload import make_round
 from oracle import tree as T
 from oracle import verify as Vf
+from tests.gpu_harness import mask_ints
 
 pytestmark = pytest.mark.gpu
 
@@ -122,7 +123,7 @@ def test_tree_stage_bit_exact(name):
         assert rd.t_parent[b, :s].tolist() == tr.parent, (name, b)
         assert rd.t_depth[b, :s].tolist() == tr.depth, (name, b)
         assert rd.t_exp[b, :s].tolist() == tr.exp, (name, b)
-        assert [int(x) & 0xFFFFFFFFFFFFFFFF for x in rd.t_anc[b, :s].tolist()] == tr.anc, (name, b)
+        assert mask_ints(rd.t_anc[b, :s]) == tr.anc, (name, b)
         assert rd.t_pos[b, :s].tolist() == [L[b] + dd for dd in tr.depth], (name, b)
         cs = rd.t_child_slot[b].cpu().numpy()
         for e in range(n):

@@ -60,7 +60,7 @@ def _standin_gpu(w, seed, guide=None):
          "p_value": torch.zeros(Bn, E, dtype=torch.float64), "c_token": i32(Bn, E, K), "c_prob": f32(Bn, E, K),
          "f_hat": f32(Bn, E, d), "logits": f32(Bn, E, V), "probs": f32(Bn, E, V), "dk_tree": f32(Bn, E, Hkv, dh),
          "t_token": i32(Bn, Sn), "t_parent": i32(Bn, Sn), "t_depth": i32(Bn, Sn), "t_pos": i32(Bn, Sn),
-         "t_exp": i32(Bn, Sn), "t_anc": torch.zeros(Bn, Sn, dtype=torch.int64), "t_size": i32(Bn),
+         "t_exp": i32(Bn, Sn), "t_anc": torch.zeros(Bn, Sn, (Sn + 63) // 64, dtype=torch.int64), "t_size": i32(Bn),
          "t_child_slot": i32(Bn, E, K), "attn_out": f32(Bn, Sn, w.n_q_heads, dh),
          "target_logits": f32(Bn, Sn, V), "target_probs": f32(Bn, Sn, V), "target_argmax": i32(Bn, Sn),
          "accept_len": i32(Bn), "path": i32(Bn, w.depth + 1), "final_token": i32(Bn), "last_slot": i32(Bn),
@@ -92,7 +92,9 @@ def _standin_gpu(w, seed, guide=None):
                            ("t_exp", tr.exp)):
             g[name][b, :s] = torch.tensor(vals)
         g["t_pos"][b, :s] = torch.tensor([inp["prefix_len"][b] + dd for dd in tr.depth])
-        g["t_anc"][b, :s] = torch.tensor([a - (1 << 64) if a >= (1 << 63) else a for a in tr.anc])
+        for w_ in range(g["t_anc"].shape[2]):            # mask words: bits 64 w .. 64 w + 63
+            words = [(a >> (64 * w_)) & 0xFFFFFFFFFFFFFFFF for a in tr.anc]
+            g["t_anc"][b, :s, w_] = torch.tensor([x - (1 << 64) if x >= (1 << 63) else x for x in words])
         for (e, rr), slot in tr.child_slot.items():
             g["t_child_slot"][b, e, rr] = slot
         g["attn_out"][b, :s] = torch.from_numpy(r["verify_out"])

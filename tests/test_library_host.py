@@ -44,9 +44,13 @@ def test_plan_eagle2_layout(lib):
     assert (p.kind, p.top_k, p.depth, p.top_m, p.n_expanded, p.n_layers) == (0, 10, 6, 60, 51, 6)
     assert list(p.layer_e0[:6]) == [0, 1, 11, 21, 31, 41]
     assert list(p.layer_rows[:6]) == [1, 10, 10, 10, 10, 10]
-    with pytest.raises(lib.EagleError) as e:
-        lib.eagle_plan_eagle2(10, 8, 60)        # 71 expanded slots > 64
-    assert e.value.name == "EAGLE_ERR_CAPACITY"
+    big = lib.eagle_plan_eagle2(10, 8, 255)      # 71 expanded slots, 256 tree slots
+    assert (big.n_expanded, big.top_m, big.layer_e0[7]) == (71, 255, 61)
+    for args in ((16, 18, 60),                    # 273 expanded slots > 256
+                 (10, 8, 256)):                   # 257 tree slots > 256
+        with pytest.raises(lib.EagleError) as e:
+            lib.eagle_plan_eagle2(*args)
+        assert e.value.name == "EAGLE_ERR_CAPACITY"
 
 
 def test_plan_static_matches_template_shape(lib):
@@ -57,6 +61,10 @@ def test_plan_static_matches_template_shape(lib):
     assert list(p.layer_e0[:5]) == [0, 1, 5, 9, 13]
     p8 = plan_for("static8")
     assert (p8.top_k, p8.n_expanded, list(p8.layer_rows[:3])) == (3, 4, [1, 2, 1])
+    t4 = plan_for("ternary4")                    # 120 nodes: template indices past int8
+    assert (t4.top_k, t4.depth, t4.top_m, t4.n_expanded) == (3, 4, 120, 40)
+    assert list(t4.layer_rows[:4]) == [1, 3, 9, 27] and list(t4.layer_e0[:4]) == [0, 1, 4, 13]
+    assert t4.node_parent[119] == 38 and t4.node_exp[38] == 39
 
 
 def test_plan_static_rejects_bad_templates(lib):
