@@ -73,6 +73,9 @@ struct AttnParams {
   int NP, bo_ld;
   float* part;                    // partial records [query row][split][dh + 4]
   int* counters;
+  int cluster;                    // tensor-core kernel: the splits of a (request, kv head) form a cluster
+                                  // and merge through distributed shared memory (part, counters unused)
+  int recs_off;                   // with cluster: byte offset of the CTA's records [rows][dh + 4] in shared memory
   int* status;                    // device status word (null: not reported)
   uint64_t* stamp;                // launch timestamps (null: off)
 };
@@ -773,6 +776,30 @@ __device__ __forceinline__ void store_state(const WarpState& st, float* slot, in
 // one streams in while the current one is consumed when a split holds
 // several); the draft's fp32 tree keys are split into bf16 hi + lo as they
 // are staged, 32 keys per tile.
+// Final output of one query row from the merged split states: o / L, as
+// fp32 (verification) or as the next GEMM's hi / lo bf16 operand (draft).
+__device__ __forceinline__ void write_merged_row(const AttnParams& p, int b, int node, int hq, const float (&o)[4],
+                                                 float Lsum, int lane) {
+  const int dh = p.dh;
+  const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int d = lane + 32 * c;
+    if (d >= dh) continue;
+    const float v = o[c] * inv;
+    if (p.mode == 1) {
+      p.out_f32[((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * dh + d] = v;
+    } else {
+      const int j = b * p.rows_cap + node;
+      const int col = hq * dh + d;
+      uint16_t hi16, lo16;
+      split_bf16(v, hi16, lo16);
+      p.b_o[static_cast<size_t>(j) * p.bo_ld + col] = hi16;
+      p.b_o[static_cast<size_t>(p.NP + j) * p.bo_ld + col] = lo16;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnParams p) {
   const LaunchStamp ls(p.stamp);
   pdl_trigger();
@@ -928,7 +955,8 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
         if (rr >= rp) continue;
         const int row = r0 + rr, node = row / p.G, hq = h * p.G + row % p.G;
         const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
-        float* dst = p.part + (qi * (p.n_splits + 1) + split) * rec;
+        float* dst = p.cluster ? reinterpret_cast<float*>(smem_attn + p.recs_off) + static_cast<size_t>(row) * rec
+                               : p.part + (qi * (p.n_splits + 1) + split) * rec;
         if (tq == 0) {
           dst[0] = st.m[r];
           dst[1] = st.l[r];
@@ -941,6 +969,40 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
     }
   }
   cp_async_wait<0>();                        // nothing may land after the CTA has left
+
+  if (p.cluster) {
+    // The splits of this (request, kv head) are one cluster: every CTA
+    // merges the rows r = rank (mod splits + 1), reading each split's record
+    // of the row from that CTA's shared memory.  Same arithmetic, in the same
+    // order, as the merge through global memory below.
+    __syncthreads();
+    sm100::cluster_sync();                   // every CTA's records are complete
+    const int ns = p.n_splits + 1;
+    const int rank = static_cast<int>(sm100::cluster_rank());
+    const float* recs = reinterpret_cast<const float*>(smem_attn + p.recs_off);
+    for (int r = rank + ns * warp; r < R; r += ns * WARPS) {
+      const int node = r / p.G, hq = h * p.G + r % p.G;
+      const float* mine = recs + static_cast<size_t>(r) * rec;
+      const float ms = lane < ns ? sm100::dsmem_ld_f32(sm100::dsmem_addr(mine, lane)) : -INFINITY;
+      const float ls = lane < ns ? sm100::dsmem_ld_f32(sm100::dsmem_addr(mine + 1, lane)) : 0.f;
+      const float M = warp_max(ms);
+      const float wgt = ms == -INFINITY ? 0.f : __expf(ms - M);
+      const float Lsum = warp_sum(wgt * ls);
+      float o[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int sp = 0; sp < ns; ++sp) {
+        const float ws = __shfl_sync(0xffffffffu, wgt, sp);
+        const uint32_t rs = sm100::dsmem_addr(mine + 4, sp);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int d = lane + 32 * c;
+          if (d < dh) o[c] = fmaf(ws, sm100::dsmem_ld_f32(rs + 4u * static_cast<uint32_t>(d)), o[c]);
+        }
+      }
+      write_merged_row(p, b, node, hq, o, Lsum, lane);
+    }
+    sm100::cluster_sync();                   // no CTA leaves while a peer still reads its records
+    return;
+  }
 
   // the last CTA of this (request, kv head) merges the splits in order
   __syncthreads();                           // every thread's partial records come first
@@ -989,23 +1051,7 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
           if (d < dh) o[c] = fmaf(ws, srow[s * rec + 4 + d], o[c]);
         }
       }
-      const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int d = lane + 32 * c;
-        if (d >= dh) continue;
-        const float v = o[c] * inv;
-        if (p.mode == 1) {
-          p.out_f32[((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * dh + d] = v;
-        } else {
-          const int j = b * p.rows_cap + node;
-          const int col = hq * dh + d;
-          uint16_t hi16, lo16;
-          split_bf16(v, hi16, lo16);
-          p.b_o[static_cast<size_t>(j) * p.bo_ld + col] = hi16;
-          p.b_o[static_cast<size_t>(p.NP + j) * p.bo_ld + col] = lo16;
-        }
-      }
+      write_merged_row(p, b, node, hq, o, Lsum, lane);
     }
   }
   cp_async_wait<0>();
@@ -1025,6 +1071,8 @@ int attn_splits(const eagle_ctx* ctx, int pairs, int cap, int per_sm) {
 // CTAs per SM each kernel is sized for (its split count makes one wave).
 constexpr int kDraftPerSm = 4;
 constexpr int kVerifyPerSm = 2;
+// Dynamic shared memory of the tensor-core kernel at two CTAs per SM.
+constexpr size_t kMmaSmemMost = static_cast<size_t>(112) << 10;
 
 template <int NR>
 static cudaError_t launch_attn_nr(const AttnParams& p, dim3 grid, size_t smem, cudaStream_t st) {
@@ -1053,9 +1101,20 @@ static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaSt
   trace_before(ctx, kernel_id, st);
   cudaError_t e;
   if (mma) {
-    e = smem_limit_once(reinterpret_cast<const void*>(tree_attn_mma_kernel), static_cast<int>(2 * TILE_BYTES + Q_BYTES));
+    // The splits of a (request, kv head) merge inside a cluster when they fit
+    // one (portable size) and every row's record fits beside the tiles at
+    // two CTAs per SM; otherwise the last CTA to finish merges them through
+    // global memory.
+    const int ns = p.n_splits + 1;
+    const size_t base = p.n_buf * TILE_BYTES + Q_BYTES;
+    const size_t recs = static_cast<size_t>(p.rows_cap) * p.G * (p.dh + 4) * sizeof(float);
+    p.cluster = ns <= 8 && base + recs <= kMmaSmemMost ? 1 : 0;
+    p.recs_off = static_cast<int>(base);
+    const size_t smem = p.cluster ? base + recs : base;
+    e = smem_limit_once(reinterpret_cast<const void*>(tree_attn_mma_kernel), static_cast<int>(kMmaSmemMost));
     if (e == cudaSuccess)
-      e = launch_pdl(tree_attn_mma_kernel, grid, dim3(THREADS), p.n_buf * TILE_BYTES + Q_BYTES, st, p);
+      e = p.cluster ? launch_pdl_cluster(tree_attn_mma_kernel, grid, dim3(THREADS), smem, st, ns, p)
+                    : launch_pdl(tree_attn_mma_kernel, grid, dim3(THREADS), smem, st, p);
   } else {
     const size_t smem = p.n_buf * TILE_BYTES + (static_cast<size_t>(p.rows_pass) * p.dh +
                                                 static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
