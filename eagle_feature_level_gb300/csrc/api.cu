@@ -236,6 +236,17 @@ bool current_context_id(unsigned long long* id) {
   return q.get_id(c, id) == CUDA_SUCCESS;
 }
 
+cudaError_t cluster_nonportable_once(const void* kernel) {
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) return cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  const auto key = std::make_tuple(id, kernel, -1);
+  std::lock_guard<std::mutex> lock(once_mu);
+  if (once_done.count(key)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) once_done.insert(key);
+  return e;
+}
+
 cudaError_t smem_limit_once(const void* kernel, int bytes) {
   unsigned long long id = 0;
   if (!current_context_id(&id)) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);

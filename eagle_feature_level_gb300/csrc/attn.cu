@@ -175,6 +175,67 @@ __device__ __forceinline__ void stage_bf16_paged(uint16_t* buf, const AttnParams
   cp_async_commit();
 }
 
+// Final output of one query row from the merged split states: o / L, as
+// fp32 (verification) or as the next GEMM's hi / lo bf16 operand (draft).
+__device__ __forceinline__ void write_merged_row(const AttnParams& p, int b, int node, int hq, const float (&o)[4],
+                                                 float Lsum, int lane) {
+  const int dh = p.dh;
+  const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int d = lane + 32 * c;
+    if (d >= dh) continue;
+    const float v = o[c] * inv;
+    if (p.mode == 1) {
+      p.out_f32[((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * dh + d] = v;
+    } else {
+      const int j = b * p.rows_cap + node;
+      const int col = hq * dh + d;
+      uint16_t hi16, lo16;
+      split_bf16(v, hi16, lo16);
+      p.b_o[static_cast<size_t>(j) * p.bo_ld + col] = hi16;
+      p.b_o[static_cast<size_t>(p.NP + j) * p.bo_ld + col] = lo16;
+    }
+  }
+}
+
+// The splits of one (request, kv head) as one thread-block cluster: each
+// CTA has left its records [row][dh + 4] (max, sum, 2 unused, output) in its
+// own shared memory at `recs`; CTA `rank` merges the rows r = rank (mod
+// splits + 1), warp by warp, reading every split's record of the row from
+// that split's CTA.  The arithmetic and its order are those of the merge
+// through global memory (the splits' weights in a warp, then the outputs
+// summed split by split).  Every thread of every CTA of the cluster calls it.
+__device__ __noinline__ void cluster_merge(const AttnParams& p, const float* recs, int R, int b, int h, int warp,
+                                           int lane) {
+  const int dh = p.dh, rec = dh + 4;
+  __syncthreads();
+  sm100::cluster_sync();                     // every CTA's records are complete
+  const int ns = p.n_splits + 1;
+  const int rank = static_cast<int>(sm100::cluster_rank());
+  for (int r = rank + ns * warp; r < R; r += ns * WARPS) {
+    const int node = r / p.G, hq = h * p.G + r % p.G;
+    const float* mine = recs + static_cast<size_t>(r) * rec;
+    const float ms = lane < ns ? sm100::dsmem_ld_f32(sm100::dsmem_addr(mine, lane)) : -INFINITY;
+    const float ls = lane < ns ? sm100::dsmem_ld_f32(sm100::dsmem_addr(mine + 1, lane)) : 0.f;
+    const float M = warp_max(ms);
+    const float wgt = ms == -INFINITY ? 0.f : __expf(ms - M);
+    const float Lsum = warp_sum(wgt * ls);
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int sp = 0; sp < ns; ++sp) {
+      const float ws = __shfl_sync(0xffffffffu, wgt, sp);
+      const uint32_t rs = sm100::dsmem_addr(mine + 4, sp);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int d = lane + 32 * c;
+        if (d < dh) o[c] = fmaf(ws, sm100::dsmem_ld_f32(rs + 4u * static_cast<uint32_t>(d)), o[c]);
+      }
+    }
+    write_merged_row(p, b, node, hq, o, Lsum, lane);
+  }
+  sm100::cluster_sync();                     // no CTA leaves while a peer still reads its records
+}
+
 // ---- draft layer: CUDA cores -------------------------------------------------
 
 // Copies draft-tree keys k0 .. k0 + nt - 1 (fp32, at most TILE_F32) into buf
@@ -456,7 +517,8 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
         const int r = r0 + warp + WARPS * i;
         const int node = r / p.G, hq = h * p.G + r % p.G;
         const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
-        float* dst = p.part + (qi * (p.n_splits + 1) + split) * rec;
+        float* dst = p.cluster ? reinterpret_cast<float*>(smem_attn + p.recs_off) + static_cast<size_t>(r) * rec
+                               : p.part + (qi * (p.n_splits + 1) + split) * rec;
         if (lane == 0) {
           dst[0] = st.m[i];
           dst[1] = st.l[i];
@@ -468,6 +530,11 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
     }
   }
   cp_async_wait<0>();                        // nothing may land after the CTA has left
+
+  if (p.cluster) {
+    cluster_merge(p, reinterpret_cast<const float*>(smem_attn + p.recs_off), R, b, h, warp, lane);
+    return;
+  }
 
   // the last CTA of this (request, kv head) merges the splits in order
   __syncthreads();                           // every thread's partial records come first
@@ -524,23 +591,7 @@ __global__ void __launch_bounds__(THREADS, 4) tree_attn_kernel(const AttnParams 
         for (int c = 0; c < 4; ++c) o[c] = fmaf(ws, vals[u][c], o[c]);
       }
     }
-    const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int d = lane + 32 * c;
-      if (d >= dh) continue;
-      const float v = o[c] * inv;
-      if (p.mode == 1) {
-        p.out_f32[((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * dh + d] = v;
-      } else {
-        const int j = b * p.rows_cap + node;
-        const int col = hq * dh + d;
-        uint16_t hi16, lo16;
-        split_bf16(v, hi16, lo16);
-        p.b_o[static_cast<size_t>(j) * p.bo_ld + col] = hi16;
-        p.b_o[static_cast<size_t>(p.NP + j) * p.bo_ld + col] = lo16;
-      }
-    }
+    write_merged_row(p, b, node, hq, o, Lsum, lane);
   }
 }
 
@@ -776,30 +827,6 @@ __device__ __forceinline__ void store_state(const WarpState& st, float* slot, in
 // one streams in while the current one is consumed when a split holds
 // several); the draft's fp32 tree keys are split into bf16 hi + lo as they
 // are staged, 32 keys per tile.
-// Final output of one query row from the merged split states: o / L, as
-// fp32 (verification) or as the next GEMM's hi / lo bf16 operand (draft).
-__device__ __forceinline__ void write_merged_row(const AttnParams& p, int b, int node, int hq, const float (&o)[4],
-                                                 float Lsum, int lane) {
-  const int dh = p.dh;
-  const float inv = Lsum > 0.f ? 1.0f / Lsum : 0.f;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const int d = lane + 32 * c;
-    if (d >= dh) continue;
-    const float v = o[c] * inv;
-    if (p.mode == 1) {
-      p.out_f32[((static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq) * dh + d] = v;
-    } else {
-      const int j = b * p.rows_cap + node;
-      const int col = hq * dh + d;
-      uint16_t hi16, lo16;
-      split_bf16(v, hi16, lo16);
-      p.b_o[static_cast<size_t>(j) * p.bo_ld + col] = hi16;
-      p.b_o[static_cast<size_t>(p.NP + j) * p.bo_ld + col] = lo16;
-    }
-  }
-}
-
 __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnParams p) {
   const LaunchStamp ls(p.stamp);
   pdl_trigger();
@@ -971,36 +998,7 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
   cp_async_wait<0>();                        // nothing may land after the CTA has left
 
   if (p.cluster) {
-    // The splits of this (request, kv head) are one cluster: every CTA
-    // merges the rows r = rank (mod splits + 1), reading each split's record
-    // of the row from that CTA's shared memory.  Same arithmetic, in the same
-    // order, as the merge through global memory below.
-    __syncthreads();
-    sm100::cluster_sync();                   // every CTA's records are complete
-    const int ns = p.n_splits + 1;
-    const int rank = static_cast<int>(sm100::cluster_rank());
-    const float* recs = reinterpret_cast<const float*>(smem_attn + p.recs_off);
-    for (int r = rank + ns * warp; r < R; r += ns * WARPS) {
-      const int node = r / p.G, hq = h * p.G + r % p.G;
-      const float* mine = recs + static_cast<size_t>(r) * rec;
-      const float ms = lane < ns ? sm100::dsmem_ld_f32(sm100::dsmem_addr(mine, lane)) : -INFINITY;
-      const float ls = lane < ns ? sm100::dsmem_ld_f32(sm100::dsmem_addr(mine + 1, lane)) : 0.f;
-      const float M = warp_max(ms);
-      const float wgt = ms == -INFINITY ? 0.f : __expf(ms - M);
-      const float Lsum = warp_sum(wgt * ls);
-      float o[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int sp = 0; sp < ns; ++sp) {
-        const float ws = __shfl_sync(0xffffffffu, wgt, sp);
-        const uint32_t rs = sm100::dsmem_addr(mine + 4, sp);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int d = lane + 32 * c;
-          if (d < dh) o[c] = fmaf(ws, sm100::dsmem_ld_f32(rs + 4u * static_cast<uint32_t>(d)), o[c]);
-        }
-      }
-      write_merged_row(p, b, node, hq, o, Lsum, lane);
-    }
-    sm100::cluster_sync();                   // no CTA leaves while a peer still reads its records
+    cluster_merge(p, reinterpret_cast<const float*>(smem_attn + p.recs_off), R, b, h, warp, lane);
     return;
   }
 
@@ -1073,14 +1071,25 @@ constexpr int kDraftPerSm = 4;
 constexpr int kVerifyPerSm = 2;
 // Dynamic shared memory of the tensor-core kernel at two CTAs per SM.
 constexpr size_t kMmaSmemMost = static_cast<size_t>(112) << 10;
+// Dynamic shared memory the CUDA-core kernel may use: two tile buffers, a
+// full pass of query rows and score rows, and the records of up to 16 rows.
+constexpr size_t kCoreSmemMost = 2 * TILE_BYTES + (static_cast<size_t>(ROWS_PASS) * MAX_DH +
+                                                   static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float) +
+                                 static_cast<size_t>(16) * (MAX_DH + 4) * sizeof(float);
+// CTAs of one cluster at most (above 8 the size is not portable).
+constexpr int kClusterMost = 16;
+// Shared memory of an SM, and what each resident CTA costs beyond its
+// dynamic shared memory (static arrays and the reserved kilobyte).
+constexpr size_t kSmemPerSm = static_cast<size_t>(228) << 10;
+constexpr size_t kSmemPerCta = static_cast<size_t>(3) << 10;
 
 template <int NR>
 static cudaError_t launch_attn_nr(const AttnParams& p, dim3 grid, size_t smem, cudaStream_t st) {
-  const size_t most = 2 * TILE_BYTES + (static_cast<size_t>(ROWS_PASS) * MAX_DH +
-                                        static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
-  const cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(tree_attn_kernel<NR>), static_cast<int>(most));
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(tree_attn_kernel<NR>), static_cast<int>(kCoreSmemMost));
+  if (e == cudaSuccess && p.cluster) e = cluster_nonportable_once(reinterpret_cast<const void*>(tree_attn_kernel<NR>));
   if (e != cudaSuccess) return e;
-  return launch_pdl(tree_attn_kernel<NR>, grid, dim3(THREADS), smem, st, p);
+  return p.cluster ? launch_pdl_cluster(tree_attn_kernel<NR>, grid, dim3(THREADS), smem, st, p.n_splits + 1, p)
+                   : launch_pdl(tree_attn_kernel<NR>, grid, dim3(THREADS), smem, st, p);
 }
 
 // Query rows per (request, kv head) from which the draft layer's attention
@@ -1091,33 +1100,60 @@ constexpr int kDraftMmaRows = 16;
 static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
   if (p.dh % 16 != 0 || p.dh > MAX_DH) return cudaErrorInvalidValue;
   const bool mma = p.mode == 1 || p.rows_cap * p.G >= kDraftMmaRows;
+  const int tiles = ceil_div(p.kv_cap, TILE);
+  const int rows = p.rows_cap * p.G;
+  p.rows_pass = std::min(ROWS_PASS, rows);
   p.n_splits = attn_splits(ctx, p.B * p.Hkv, p.kv_cap, mma ? kVerifyPerSm : kDraftPerSm);
-  const int tiles_per_split = ceil_div(ceil_div(p.kv_cap, TILE), p.n_splits);
+  // Dynamic shared memory of a launch whose splits hold tps key tiles each.
+  auto smem_for = [&](int tps) {
+    const size_t bufs = (tps > 1 ? 2 : 1) * TILE_BYTES;
+    return mma ? bufs + Q_BYTES
+               : bufs + (static_cast<size_t>(p.rows_pass) * p.dh + static_cast<size_t>(WARPS) * RW * TILE) *
+                            sizeof(float);
+  };
+  // Waves of a launch of `splits` prefix splits whose CTAs take `smem`
+  // bytes of dynamic shared memory each.
+  const int pairs = p.B * p.Hkv;
+  const int per_sm_most = mma ? kVerifyPerSm : kDraftPerSm;
+  auto waves = [&](int splits, size_t smem) {
+    int per_sm = static_cast<int>(kSmemPerSm / (smem + kSmemPerCta));
+    per_sm = std::max(1, std::min(per_sm, per_sm_most));
+    return ceil_div((splits + 1) * pairs, per_sm * ctx->sm_count);
+  };
+  // The splits of a (request, kv head) merge inside one cluster when they
+  // fit one (at most kClusterMost CTAs, the tree part's included), every
+  // row's record fits beside the tiles and the launch is one wave;
+  // otherwise the last CTA to finish merges them through global memory.
+  // Measured: fewer, longer splits to fit a cluster are slower (the tiles
+  // of a split load one after another), and so are clusters over several
+  // waves (whole clusters wait for room in one GPC: 13B draft attention
+  // 1.8 -> 3.8 ms).
+  if (p.n_splits + 1 <= kClusterMost) {
+    const size_t recs = static_cast<size_t>(rows) * (p.dh + 4) * sizeof(float);
+    const size_t base = smem_for(ceil_div(tiles, p.n_splits));
+    if (base + recs <= (mma ? kMmaSmemMost : kCoreSmemMost) && waves(p.n_splits, base + recs) == 1) {
+      p.cluster = 1;
+      p.recs_off = static_cast<int>(base);
+    }
+  }
+  const int tiles_per_split = ceil_div(tiles, p.n_splits);
   p.chunk = tiles_per_split * TILE;
   p.n_buf = tiles_per_split > 1 ? 2 : 1;
-  p.rows_pass = std::min(ROWS_PASS, p.rows_cap * p.G);
-  dim3 grid(p.n_splits + 1, p.B * p.Hkv);
+  const size_t smem = smem_for(tiles_per_split) +
+                      (p.cluster ? static_cast<size_t>(rows) * (p.dh + 4) * sizeof(float) : 0);
+  const int ns = p.n_splits + 1;
+  dim3 grid(ns, p.B * p.Hkv);
   p.stamp = stamp_slot(ctx, kernel_id);
   trace_before(ctx, kernel_id, st);
   cudaError_t e;
   if (mma) {
-    // The splits of a (request, kv head) merge inside a cluster when they fit
-    // one (portable size) and every row's record fits beside the tiles at
-    // two CTAs per SM; otherwise the last CTA to finish merges them through
-    // global memory.
-    const int ns = p.n_splits + 1;
-    const size_t base = p.n_buf * TILE_BYTES + Q_BYTES;
-    const size_t recs = static_cast<size_t>(p.rows_cap) * p.G * (p.dh + 4) * sizeof(float);
-    p.cluster = ns <= 8 && base + recs <= kMmaSmemMost ? 1 : 0;
-    p.recs_off = static_cast<int>(base);
-    const size_t smem = p.cluster ? base + recs : base;
     e = smem_limit_once(reinterpret_cast<const void*>(tree_attn_mma_kernel), static_cast<int>(kMmaSmemMost));
+    if (e == cudaSuccess && p.cluster)
+      e = cluster_nonportable_once(reinterpret_cast<const void*>(tree_attn_mma_kernel));
     if (e == cudaSuccess)
       e = p.cluster ? launch_pdl_cluster(tree_attn_mma_kernel, grid, dim3(THREADS), smem, st, ns, p)
                     : launch_pdl(tree_attn_mma_kernel, grid, dim3(THREADS), smem, st, p);
   } else {
-    const size_t smem = p.n_buf * TILE_BYTES + (static_cast<size_t>(p.rows_pass) * p.dh +
-                                                static_cast<size_t>(WARPS) * RW * TILE) * sizeof(float);
     const int per_warp = ceil_div(p.rows_pass, WARPS);
     if (per_warp <= 1) e = launch_attn_nr<1>(p, grid, smem, st);
     else if (per_warp <= 2) e = launch_attn_nr<2>(p, grid, smem, st);

@@ -132,6 +132,9 @@ bool current_context_id(unsigned long long* id);
 // attributes belong to a context, so every device and every re-created
 // context gets its own.
 cudaError_t smem_limit_once(const void* kernel, int bytes);
+// cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed,
+// 1) (clusters of up to 16 CTAs), once per (current context, kernel).
+cudaError_t cluster_nonportable_once(const void* kernel);
 
 // The timestamp pair of the next launch (of kernel class `kernel_id`) while
 // stamps are enabled, else null.
