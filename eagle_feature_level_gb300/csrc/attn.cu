@@ -1093,9 +1093,11 @@ static cudaError_t launch_attn_nr(const AttnParams& p, dim3 grid, size_t smem, c
 }
 
 // Query rows per (request, kv head) from which the draft layer's attention
-// runs on the tensor cores too: below it most of a 16-row tile would be
-// padding, and the CUDA-core kernel is faster.
-constexpr int kDraftMmaRows = 16;
+// runs on the tensor cores too.  Measured: 10 rows (EAGLE-2, k = 10) take
+// 25 us per launch there against 46 on the CUDA cores at the 7B shape (13B:
+// 217 against 368); 1 to 4 rows (the static tree) are faster on the CUDA
+// cores (10 against 15 us), most of a 16-row tile being padding.
+constexpr int kDraftMmaRows = 8;
 
 static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
   if (p.dh % 16 != 0 || p.dh > MAX_DH) return cudaErrorInvalidValue;
