@@ -40,9 +40,14 @@ constexpr int MLD = MAX_DH + 4;   // fp32 row pitch of a warp's softmax state in
 // 32 fp32 rows of each, or 32 bf16 rows each of K hi, K lo, V hi, V lo.
 constexpr size_t TILE_BYTES = static_cast<size_t>(2) * TILE * KLD * 2;
 static_assert(static_cast<size_t>(2) * TILE_F32 * (MAX_DH + 4) * 4 <= TILE_BYTES, "fp32 half tile fits a buffer");
-constexpr size_t Q_BYTES = static_cast<size_t>(2) * ROWS_PASS * KLD * 2;     // pass rows, hi and lo
-constexpr size_t MRG_BYTES = static_cast<size_t>(2) * 16 * MLD * 4;          // two warp states of 16 rows
-static_assert(MRG_BYTES <= Q_BYTES, "the merge states reuse the query rows' space");
+// Tensor-core kernel with nw warps: query rows per pass (32 with four warps,
+// 16 per warp with eight), their bf16 hi and lo copies, and the nw / 2 warp
+// states of 16 rows that reuse that space in the intra-CTA merge.
+__host__ __device__ constexpr int mma_rows(int nw) { return nw == 4 ? 32 : 16 * nw; }
+__host__ __device__ constexpr size_t q_bytes(int nw) { return static_cast<size_t>(2) * mma_rows(nw) * KLD * 2; }
+__host__ __device__ constexpr size_t mrg_bytes(int nw) { return static_cast<size_t>(nw / 2) * 16 * MLD * 4; }
+static_assert(mrg_bytes(4) <= q_bytes(4) && mrg_bytes(8) <= q_bytes(8), "the merge states reuse the query rows' space");
+constexpr size_t Q_BYTES = q_bytes(4);
 
 struct AttnParams {
   int mode;                       // 0 draft, 1 verify
@@ -123,6 +128,13 @@ __device__ __forceinline__ void cp_async16_cg(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// Waits until at most n (0..3, larger taken as 3) copy groups are pending.
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+  if (n <= 0) cp_async_wait<0>();
+  else if (n == 1) cp_async_wait<1>();
+  else if (n == 2) cp_async_wait<2>();
+  else cp_async_wait<3>();
+}
 
 // Copies one bf16 tile (keys t0 .. t0 + nt - 1 of kv head h) into buf as K
 // rows [TILE][KLD] then V rows; rows past nt are zeroed.  Issued by all
@@ -132,7 +144,7 @@ __device__ __forceinline__ void stage_bf16(uint16_t* buf, const uint16_t* kb, co
   uint16_t* sk = buf;
   uint16_t* sv = buf + TILE * KLD;
   const int pieces = dh >> 3;
-  for (int idx = threadIdx.x; idx < TILE * pieces; idx += THREADS) {
+  for (int idx = threadIdx.x; idx < TILE * pieces; idx += blockDim.x) {
     const int r = idx / pieces, c = idx - r * pieces;
     if (r < nt) {
       cp_async16(sk + r * KLD + 8 * c, kb + row0 + r * row_stride + 8 * c, policy);
@@ -153,7 +165,7 @@ __device__ __forceinline__ void stage_bf16_paged(uint16_t* buf, const AttnParams
   uint16_t* sk = buf;
   uint16_t* sv = buf + TILE * KLD;
   const int dh = p.dh, pieces = dh >> 3;
-  for (int idx = threadIdx.x; idx < TILE * pieces; idx += THREADS) {
+  for (int idx = threadIdx.x; idx < TILE * pieces; idx += blockDim.x) {
     const int r = idx / pieces, c = idx - r * pieces;
     bool loaded = false;
     if (r < nt) {
@@ -213,7 +225,8 @@ __device__ __noinline__ void cluster_merge(const AttnParams& p, const float* rec
   sm100::cluster_sync();                     // every CTA's records are complete
   const int ns = p.n_splits + 1;
   const int rank = static_cast<int>(sm100::cluster_rank());
-  for (int r = rank + ns * warp; r < R; r += ns * WARPS) {
+  const int nwarps = static_cast<int>(blockDim.x >> 5);
+  for (int r = rank + ns * warp; r < R; r += ns * nwarps) {
     const int node = r / p.G, hq = h * p.G + r % p.G;
     const float* mine = recs + static_cast<size_t>(r) * rec;
     const float ms = lane < ns ? sm100::dsmem_ld_f32(sm100::dsmem_addr(mine, lane)) : -INFINITY;
@@ -247,7 +260,7 @@ __device__ __forceinline__ void stage_f32(float* buf, const float* kf, const flo
   float* sv = buf + TILE_F32 * ld;
   const int pieces = dh >> 2;
   const uint64_t policy = sm100::l2_policy_evict_first();
-  for (int idx = threadIdx.x; idx < TILE_F32 * pieces; idx += THREADS) {
+  for (int idx = threadIdx.x; idx < TILE_F32 * pieces; idx += blockDim.x) {
     const int r = idx / pieces, c = idx - r * pieces;
     if (r < nt) {
       cp_async16(sk + r * ld + 4 * c, kf + row0 + r * row_stride + 4 * c, policy);
@@ -630,7 +643,7 @@ __device__ __forceinline__ void split_pair(float x, float y, uint32_t& hi, uint3
 __device__ __forceinline__ void stage_f32_split(uint16_t* buf, const float* kf, const float* vf, size_t row0,
                                                 size_t row_stride, int nt, int dh) {
   const int pieces = dh >> 2;
-  for (int idx = threadIdx.x; idx < TILE_F32 * pieces; idx += THREADS) {
+  for (int idx = threadIdx.x; idx < TILE_F32 * pieces; idx += blockDim.x) {
     const int r = idx / pieces, c = idx - r * pieces;
     float4 k = make_float4(0.f, 0.f, 0.f, 0.f), v = k;
     if (r < nt) {
@@ -648,6 +661,7 @@ __device__ __forceinline__ void stage_f32_split(uint16_t* buf, const float* kf, 
     *reinterpret_cast<uint2*>(buf + TILE * KLD + o) = make_uint2(h0, h1);
     *reinterpret_cast<uint2*>(buf + (TILE + TILE_F32) * KLD + o) = make_uint2(l0, l1);
   }
+  cp_async_commit();                         // an empty group: one group per staged tile, as the others
 }
 
 // Online-softmax state of one warp: rows g and g + 8 of its 16-row tile
@@ -815,24 +829,30 @@ __device__ __forceinline__ void store_state(const WarpState& st, float* slot, in
 }
 
 // Dynamic shared memory: n_buf tile buffers (TILE_BYTES each) and the
-// pass's query rows as bf16 hi [ROWS_PASS][KLD] and lo, whose space holds
-// two warp states for the intra-CTA merge once the pass's tiles are done;
-// at the end, the merging CTA reuses all of it to stage partial records.
+// pass's query rows as bf16 hi [16 NW][KLD] and lo, whose space holds the
+// warp states of the intra-CTA merge once the pass's tiles are done; at the
+// end, the merging CTA reuses all of it to stage partial records.
 //
-// One CTA per (prefix split or tree part, request, kv head).  A pass covers
-// up to 32 query rows (tree nodes x GQA group) as MT = 1 or 2 tiles of 16;
-// the 4 / MT warps of a row tile split every staged key tile between them,
+// One CTA of NW warps per (prefix split or tree part, request, kv head):
+// four warps at two CTAs per SM, or eight at one when a kv head has more
+// than 32 query rows (fewer passes, each re-reading the split's tiles).  A
+// pass covers up to 16 NW query rows (tree nodes x GQA group) as MT tiles of
+// 16 (a power of two); the NW / MT warps of a row tile split every staged
+// key tile between them,
 // each keeping its own online softmax, and are merged (in a fixed order) at
 // the end of the pass.  Prefix tiles are bf16 copied by cp.async (the next
 // one streams in while the current one is consumed when a split holds
 // several); the draft's fp32 tree keys are split into bf16 hi + lo as they
 // are staged, 32 keys per tile.
-__global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnParams p) {
+template <int NW>
+__global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1) tree_attn_mma_kernel(const AttnParams p) {
+  constexpr int kThreads = 32 * NW;
+  constexpr int kRows = mma_rows(NW);        // query rows per pass
   const LaunchStamp ls(p.stamp);
   pdl_trigger();
   extern __shared__ __align__(16) uint8_t smem_attn[];
   __shared__ int s_last;
-  __shared__ uint64_t s_mask[ROWS_PASS * MASKW];   // ancestor masks of the pass's rows (tree part)
+  __shared__ uint64_t s_mask[kRows * MASKW];   // ancestor masks of the pass's rows (tree part)
 
   const int split = blockIdx.x;              // split == n_splits: the tree part
   const int pair = blockIdx.y;
@@ -841,7 +861,7 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
   const int dh = p.dh;
   uint8_t* bufs = smem_attn;
   uint16_t* qhi = reinterpret_cast<uint16_t*>(smem_attn + p.n_buf * TILE_BYTES);
-  uint16_t* qlo = qhi + ROWS_PASS * KLD;
+  uint16_t* qlo = qhi + kRows * KLD;
   float* mrg = reinterpret_cast<float*>(qhi);   // after a pass's last tile, the query rows are dead
   const bool is_tree = split == p.n_splits;
   const bool tree_f32 = is_tree && p.mode == 0;
@@ -893,17 +913,18 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
   }
   const bool resident = n_tiles <= p.n_buf;
 
-  for (int r0 = 0; r0 < R; r0 += ROWS_PASS) {
-    const int rp = min(ROWS_PASS, R - r0);
-    const int MT = rp > 16 ? 2 : 1;
-    const int KS = WARPS / MT;               // warps sharing a row tile
+  for (int r0 = 0; r0 < R; r0 += kRows) {
+    const int rp = min(kRows, R - r0);
+    int MT = 1;                              // 16-row tiles of the pass (a power of two)
+    while (16 * MT < rp && MT < kRows / 16) MT <<= 1;
+    const int KS = NW / MT;                  // warps sharing a row tile
     const int mt = warp % MT, ks = warp / MT;
     if (r0 > 0) {
       __syncthreads();                       // the previous pass is done with the query rows and buffers
       if (!resident) staged = 0;
     }
     // query rows of the pass as bf16 hi (+ lo for fp32 queries); rows past rp are zero
-    for (int idx = threadIdx.x; idx < 16 * MT * (dh >> 2); idx += THREADS) {
+    for (int idx = threadIdx.x; idx < 16 * MT * (dh >> 2); idx += kThreads) {
       const int rr = idx / (dh >> 2), c = idx - rr * (dh >> 2);
       uint2 wh = make_uint2(0u, 0u), wl = make_uint2(0u, 0u);
       if (rr < rp) {
@@ -920,7 +941,7 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
       *reinterpret_cast<uint2*>(qhi + rr * KLD + 4 * c) = wh;
       if (p.mode == 0) *reinterpret_cast<uint2*>(qlo + rr * KLD + 4 * c) = wl;
     }
-    if (is_tree && threadIdx.x < ROWS_PASS) {
+    if (is_tree && threadIdx.x < kRows) {
       if (threadIdx.x < rp) {
         load_row_mask(p, s_mask + threadIdx.x * MASKW, b, (r0 + threadIdx.x) / p.G);
       } else {
@@ -934,23 +955,19 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
 #pragma unroll
     for (int j = 0; j < MAX_DH / 8; ++j) st.o[j][0] = st.o[j][1] = st.o[j][2] = st.o[j][3] = 0.f;
     for (int tile = 0; tile < n_tiles; ++tile) {
-      const int which = p.n_buf > 1 ? (tile & 1) : 0;
-      if (tile >= staged) {
-        __syncthreads();                     // every warp is done with this buffer
-        stage(tile, which);
-        staged = tile + 1;
+      // a ring of n_buf buffers: tile t in buffer t % n_buf, up to n_buf
+      // tiles requested ahead; the buffer refilled here held the tile that
+      // the previous iteration consumed
+      const int which = tile % p.n_buf;
+      if (staged < n_tiles && staged < tile + p.n_buf) {
+        __syncthreads();                     // every warp is done with the buffers being refilled
+        for (; staged < n_tiles && staged < tile + p.n_buf; ++staged) stage(staged, staged % p.n_buf);
       }
-      if (p.n_buf > 1 && tile + 1 < n_tiles && tile + 1 >= staged) {
-        __syncthreads();                     // the other buffer's previous tile is consumed
-        stage(tile + 1, which ^ 1);
-        staged = tile + 2;
-      }
-      if (staged > tile + 1) cp_async_wait<1>();   // this tile's copies have landed (the next may fly)
-      else cp_async_wait<0>();
+      cp_async_wait_upto(staged - tile - 1);   // this tile's copies have landed (later ones may fly)
       __syncthreads();
       const int t0 = lo + tile * step;
       const int nt = min(step, hi - t0);
-      const int kpw = max(16, step / KS);    // keys per warp: 16 or 32
+      const int kpw = max(16, step / KS);    // keys per warp: 16, 32 or 64
       const int k_lo = ks * kpw;
       if (k_lo < nt) {
         const uint16_t* buf = reinterpret_cast<const uint16_t*>(bufs + which * TILE_BYTES);
@@ -960,16 +977,22 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
         const uint64_t mb = is_tree ? s_mask[(16 * mt + (lane >> 2) + 8) * MASKW + mw] : ~0ull;
         const uint16_t* ql = p.mode == 0 ? qlo : nullptr;
         const int kb = is_tree ? (t0 & 63) : 0;
-        if (kpw == 32)
-          tile_mma<4>(p, st, buf, tree_f32, qhi, ql, mt, k_lo, nt, kb, is_tree, ma, mb, lane);
-        else
+        if (kpw == 16) {
           tile_mma<2>(p, st, buf, tree_f32, qhi, ql, mt, k_lo, nt, kb, is_tree, ma, mb, lane);
+        } else if (kpw == 32) {
+          tile_mma<4>(p, st, buf, tree_f32, qhi, ql, mt, k_lo, nt, kb, is_tree, ma, mb, lane);
+        } else {
+          // 64 keys per warp: one warp per row tile, which only the
+          // eight-warp kernel's 128-row passes produce
+          if constexpr (kRows / 16 == NW)
+            tile_mma<8>(p, st, buf, tree_f32, qhi, ql, mt, k_lo, nt, kb, is_tree, ma, mb, lane);
+        }
       }
     }
     // merge the KS warps of each row tile pairwise, in a fixed order
     for (int d = 1; d < KS; d <<= 1) {
       __syncthreads();
-      const int slot = mt + MT * (ks / (2 * d));          // < 2
+      const int slot = mt + MT * (ks / (2 * d));          // < NW / 2
       if (ks % (2 * d) == d) store_state(st, mrg + slot * 16 * MLD, dh, lane);
       __syncthreads();
       if (ks % (2 * d) == 0) merge_state(st, mrg + slot * 16 * MLD, dh, lane);
@@ -1018,7 +1041,7 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
   const int ns = p.n_splits + 1;
   float* stg = reinterpret_cast<float*>(smem_attn);
   const int row_floats = ns * rec;
-  const size_t smem_floats = (p.n_buf * TILE_BYTES + Q_BYTES) / sizeof(float);
+  const size_t smem_floats = (p.n_buf * TILE_BYTES + q_bytes(NW)) / sizeof(float);
   const int batch = max(1, static_cast<int>(smem_floats / row_floats));
   for (int rb = 0; rb < R; rb += batch) {
     const int nb = min(batch, R - rb);
@@ -1027,12 +1050,12 @@ __global__ void __launch_bounds__(THREADS, 2) tree_attn_mma_kernel(const AttnPar
       const int r = rb + i, node = r / p.G, hq = h * p.G + r % p.G;
       const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
       const float* src = p.part + qi * ns * rec;
-      for (int k = 4 * threadIdx.x; k < row_floats; k += 4 * THREADS) cp_async16_cg(stg + i * row_floats + k, src + k);
+      for (int k = 4 * threadIdx.x; k < row_floats; k += 4 * kThreads) cp_async16_cg(stg + i * row_floats + k, src + k);
     }
     cp_async_commit();
     cp_async_wait<0>();
     __syncthreads();
-    for (int i = warp; i < nb; i += WARPS) {
+    for (int i = warp; i < nb; i += NW) {
       const int r = rb + i, node = r / p.G, hq = h * p.G + r % p.G;
       const float* srow = stg + i * row_floats;
       const float ms = lane < ns ? srow[lane * rec] : -INFINITY;
@@ -1069,8 +1092,10 @@ int attn_splits(const eagle_ctx* ctx, int pairs, int cap, int per_sm) {
 // CTAs per SM each kernel is sized for (its split count makes one wave).
 constexpr int kDraftPerSm = 4;
 constexpr int kVerifyPerSm = 2;
-// Dynamic shared memory of the tensor-core kernel at two CTAs per SM.
+// Dynamic shared memory of the tensor-core kernel: four warps at two CTAs
+// per SM, eight warps at one.
 constexpr size_t kMmaSmemMost = static_cast<size_t>(112) << 10;
+constexpr size_t kMma8SmemMost = static_cast<size_t>(216) << 10;
 // Dynamic shared memory the CUDA-core kernel may use: two tile buffers, a
 // full pass of query rows and score rows, and the records of up to 16 rows.
 constexpr size_t kCoreSmemMost = 2 * TILE_BYTES + (static_cast<size_t>(ROWS_PASS) * MAX_DH +
@@ -1092,6 +1117,16 @@ static cudaError_t launch_attn_nr(const AttnParams& p, dim3 grid, size_t smem, c
                    : launch_pdl(tree_attn_kernel<NR>, grid, dim3(THREADS), smem, st, p);
 }
 
+template <int NW>
+static cudaError_t launch_mma(const AttnParams& p, dim3 grid, size_t smem, cudaStream_t st, size_t most) {
+  const void* k = reinterpret_cast<const void*>(tree_attn_mma_kernel<NW>);
+  cudaError_t e = smem_limit_once(k, static_cast<int>(most));
+  if (e == cudaSuccess && p.cluster) e = cluster_nonportable_once(k);
+  if (e != cudaSuccess) return e;
+  return p.cluster ? launch_pdl_cluster(tree_attn_mma_kernel<NW>, grid, dim3(32 * NW), smem, st, p.n_splits + 1, p)
+                   : launch_pdl(tree_attn_mma_kernel<NW>, grid, dim3(32 * NW), smem, st, p);
+}
+
 // Query rows per (request, kv head) from which the draft layer's attention
 // runs on the tensor cores too.  Measured: 10 rows (EAGLE-2, k = 10) take
 // 25 us per launch there against 46 on the CUDA cores at the 7B shape (13B:
@@ -1105,18 +1140,26 @@ static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaSt
   const int tiles = ceil_div(p.kv_cap, TILE);
   const int rows = p.rows_cap * p.G;
   p.rows_pass = std::min(ROWS_PASS, rows);
-  p.n_splits = attn_splits(ctx, p.B * p.Hkv, p.kv_cap, mma ? kVerifyPerSm : kDraftPerSm);
-  // Dynamic shared memory of a launch whose splits hold tps key tiles each.
+  // tensor cores: eight warps per CTA (one CTA per SM, 128-row passes) when
+  // a kv head has more query rows than four four-warp passes take.
+  // Measured at the 70B shape: 488 verification rows 4.7 -> 4.0 ms; 80
+  // draft rows 4.5 -> 5.1 ms (slower: a CTA per SM); 61 rows about even.
+  const int nw = mma && rows > 4 * ROWS_PASS ? 8 : 4;
+  const int per_sm_most = mma ? (nw == 8 ? 1 : kVerifyPerSm) : kDraftPerSm;
+  p.n_splits = attn_splits(ctx, p.B * p.Hkv, p.kv_cap, per_sm_most);
+  // Tile buffers of a split of tps key tiles (two: the next tile streams in
+  // while the current one is consumed; a deeper ring measured no faster at
+  // the 70B shape), and the dynamic shared memory of such a launch.
+  auto nbuf_for = [&](int tps) { return std::min(tps, 2); };
   auto smem_for = [&](int tps) {
-    const size_t bufs = (tps > 1 ? 2 : 1) * TILE_BYTES;
-    return mma ? bufs + Q_BYTES
+    const size_t bufs = static_cast<size_t>(nbuf_for(tps)) * TILE_BYTES;
+    return mma ? bufs + q_bytes(nw)
                : bufs + (static_cast<size_t>(p.rows_pass) * p.dh + static_cast<size_t>(WARPS) * RW * TILE) *
                             sizeof(float);
   };
   // Waves of a launch of `splits` prefix splits whose CTAs take `smem`
   // bytes of dynamic shared memory each.
   const int pairs = p.B * p.Hkv;
-  const int per_sm_most = mma ? kVerifyPerSm : kDraftPerSm;
   auto waves = [&](int splits, size_t smem) {
     int per_sm = static_cast<int>(kSmemPerSm / (smem + kSmemPerCta));
     per_sm = std::max(1, std::min(per_sm, per_sm_most));
@@ -1133,14 +1176,15 @@ static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaSt
   if (p.n_splits + 1 <= kClusterMost) {
     const size_t recs = static_cast<size_t>(rows) * (p.dh + 4) * sizeof(float);
     const size_t base = smem_for(ceil_div(tiles, p.n_splits));
-    if (base + recs <= (mma ? kMmaSmemMost : kCoreSmemMost) && waves(p.n_splits, base + recs) == 1) {
+    const size_t most = mma ? (nw == 8 ? kMma8SmemMost : kMmaSmemMost) : kCoreSmemMost;
+    if (base + recs <= most && waves(p.n_splits, base + recs) == 1) {
       p.cluster = 1;
       p.recs_off = static_cast<int>(base);
     }
   }
   const int tiles_per_split = ceil_div(tiles, p.n_splits);
   p.chunk = tiles_per_split * TILE;
-  p.n_buf = tiles_per_split > 1 ? 2 : 1;
+  p.n_buf = nbuf_for(tiles_per_split);
   const size_t smem = smem_for(tiles_per_split) +
                       (p.cluster ? static_cast<size_t>(rows) * (p.dh + 4) * sizeof(float) : 0);
   const int ns = p.n_splits + 1;
@@ -1149,12 +1193,7 @@ static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaSt
   trace_before(ctx, kernel_id, st);
   cudaError_t e;
   if (mma) {
-    e = smem_limit_once(reinterpret_cast<const void*>(tree_attn_mma_kernel), static_cast<int>(kMmaSmemMost));
-    if (e == cudaSuccess && p.cluster)
-      e = cluster_nonportable_once(reinterpret_cast<const void*>(tree_attn_mma_kernel));
-    if (e == cudaSuccess)
-      e = p.cluster ? launch_pdl_cluster(tree_attn_mma_kernel, grid, dim3(THREADS), smem, st, ns, p)
-                    : launch_pdl(tree_attn_mma_kernel, grid, dim3(THREADS), smem, st, p);
+    e = nw == 8 ? launch_mma<8>(p, grid, smem, st, kMma8SmemMost) : launch_mma<4>(p, grid, smem, st, kMmaSmemMost);
   } else {
     const int per_warp = ceil_div(p.rows_pass, WARPS);
     if (per_warp <= 1) e = launch_attn_nr<1>(p, grid, smem, st);
