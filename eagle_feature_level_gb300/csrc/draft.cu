@@ -165,6 +165,7 @@ constexpr int SEL_SLICE = SEL_THREADS * SEL_PER;
 static_assert(SEL_CL * SEL_SLICE >= EAGLE_MAX_VOCAB, "one cluster covers the largest vocabulary");
 static_assert(SEL_CL * EAGLE_MAX_CHILDREN <= 128 && SEL_WARPS * EAGLE_MAX_CHILDREN <= 128,
               "candidate lists fit four per lane");
+static_assert(SEL_WARPS == SEL_CL, "rank 0 merges the lists of CTA w in its warp w");
 
 // (value desc, id asc) total order: true if a ranks before b.
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
@@ -226,6 +227,10 @@ struct SelParams {
 
 __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) select_kernel(const SelParams p) {
   const LaunchStamp ls(p.stamp);
+  // Phase 0 of the cluster barrier: every CTA arrives as it starts and waits
+  // just before its first access to another CTA's shared memory, which is
+  // then known to have started.
+  sm100::cluster_arrive_relaxed();
   pdl_wait();      // predecessor outputs visible from here on
   ls.waited();
   pdl_trigger();
@@ -235,7 +240,10 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
   __shared__ uint64_t s_wscan[SEL_WARPS];
   __shared__ float s_wz[SEL_WARPS * EAGLE_MAX_CHILDREN], s_wq[SEL_WARPS * EAGLE_MAX_CHILDREN];
   __shared__ int s_wi[SEL_WARPS * EAGLE_MAX_CHILDREN];
-  __shared__ float s_cz[SEL_CL * EAGLE_MAX_CHILDREN], s_cq[SEL_CL * EAGLE_MAX_CHILDREN];  // rank 0: per-CTA lists
+  // rank 0: every warp's list of every CTA (pushed), then each CTA's merged list
+  __shared__ float s_gz[SEL_CL * SEL_WARPS * EAGLE_MAX_CHILDREN];
+  __shared__ int s_gi[SEL_CL * SEL_WARPS * EAGLE_MAX_CHILDREN];
+  __shared__ float s_cz[SEL_CL * EAGLE_MAX_CHILDREN], s_cq[SEL_CL * EAGLE_MAX_CHILDREN];
   __shared__ int s_ci[SEL_CL * EAGLE_MAX_CHILDREN];
   __shared__ int s_pick[EAGLE_MAX_CHILDREN];                // sampling: drawn token of each round (pushed)
   __shared__ uint64_t s_pw[EAGLE_MAX_CHILDREN];
@@ -248,7 +256,7 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
   int32_t* ct = p.child_tok + node * p.K;
   float* cp = p.child_prob + node * p.K;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (p.token[node] < 0) {                   // uniform over the cluster: no barrier is reached
+  if (p.token[node] < 0) {                   // uniform over the cluster: no barrier is waited on
     if (rank == 0 && tid < p.K) { ct[tid] = -1; cp[tid] = 0.f; }
     return;
   }
@@ -284,23 +292,34 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
     }
   }
   if (bad) set_status(p.status, EAGLE_ERR_NUMERIC);
+  lmax = warp_max_redux(lmax);
+  if (lane == 0) s_red[wid] = lmax;
+  __syncthreads();
+  sm100::cluster_wait();                     // phase 0: every CTA of the cluster has started
+  if (tid < SEL_CL) {                        // push this CTA's max to every rank
+    float m = s_red[0];
+    for (int w = 1; w < SEL_WARPS; ++w) m = fmaxf(m, s_red[w]);
+    sm100::dsmem_st_f32(sm100::dsmem_addr(&s_cmax[rank], tid), m);
+  }
+  sm100::cluster_arrive();                   // phase 1: the maxima
   if (greedy) {
-    // each warp's k best (logit desc, id asc): no softmax statistic is needed,
-    // so they are ranked before the cluster exchanges (probabilities later)
+    // each warp's k best (logit desc, id asc) go straight into rank 0's
+    // table while the maxima travel (no softmax statistic is needed to rank
+    // them; the probabilities come later)
     uint32_t taken = 0;
     float bv = -INFINITY;
     int bi = INT32_MAX, bs = -1;
 #pragma unroll
     for (int u = 0; u < SEL_PER; ++u)
       if (v0 + u < V && ranks_before(x[u], v0 + u, bv, bi)) { bv = x[u]; bi = v0 + u; bs = u; }
+    const int gbase = (static_cast<int>(rank) * SEL_WARPS + wid) * k;
     for (int r = 0; r < k; ++r) {
       float wv = bv;
       int wi = bi;
       warp_argmax(wv, wi);
       if (bs >= 0 && wi == bi && bi != INT32_MAX) {
-        s_wz[wid * k + r] = bv;
-        s_wi[wid * k + r] = bi;
-        s_wq[wid * k + r] = 0.f;
+        sm100::dsmem_st_f32(sm100::dsmem_addr(&s_gz[gbase + r], 0), bv);
+        sm100::dsmem_st_s32(sm100::dsmem_addr(&s_gi[gbase + r], 0), bi);
         taken |= 1u << bs;
         bv = -INFINITY; bi = INT32_MAX; bs = -1;
 #pragma unroll
@@ -310,35 +329,14 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
           }
       }
       if (wi == INT32_MAX && lane == 0) {
-        s_wz[wid * k + r] = -INFINITY;
-        s_wi[wid * k + r] = INT32_MAX;
-        s_wq[wid * k + r] = 0.f;
+        sm100::dsmem_st_f32(sm100::dsmem_addr(&s_gz[gbase + r], 0), -INFINITY);
+        sm100::dsmem_st_s32(sm100::dsmem_addr(&s_gi[gbase + r], 0), INT32_MAX);
       }
     }
   }
-  lmax = warp_max_redux(lmax);
-  if (lane == 0) s_red[wid] = lmax;
-  __syncthreads();
-  if (tid < SEL_CL) {                        // push this CTA's max to every rank
-    float m = s_red[0];
-    for (int w = 1; w < SEL_WARPS; ++w) m = fmaxf(m, s_red[w]);
-    sm100::dsmem_st_f32(sm100::dsmem_addr(&s_cmax[rank], tid), m);
-  }
-  // The first cluster barrier also orders every later remote write after
-  // every CTA of the cluster has started.
-  sm100::cluster_sync();
+  sm100::cluster_wait();
   float m = s_cmax[0];
   for (int c = 1; c < SEL_CL; ++c) m = fmaxf(m, s_cmax[c]);
-  if (greedy && wid == 0) {
-    // the CTA's list (from the warps' lists, complete since the barrier
-    // before the max push) goes straight into rank 0's candidate table
-    warp_merge_topk(s_wz, s_wi, s_wq, SEL_WARPS * k, k, s_cz + rank * k, s_ci + rank * k, s_cq + rank * k);
-    if (lane < k) {
-      const int c = rank * k + lane;
-      sm100::dsmem_st_f32(sm100::dsmem_addr(&s_cz[c], 0), s_cz[c]);
-      sm100::dsmem_st_s32(sm100::dsmem_addr(&s_ci[c], 0), s_ci[c]);
-    }
-  }
 
   // exponentials, slice sum in a fixed order, cluster sum in rank order
   float ex[SEL_PER];
@@ -375,9 +373,14 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
   }
 
   if (greedy) {
-    // rank 0 merges the cluster's lists (complete since the second barrier);
-    // a child's probability is its q entry, recomputed by the same expression
-    if (rank != 0 || wid != 0) return;
+    // rank 0 merges the cluster's lists (complete since the second barrier):
+    // warp w the lists of CTA w, then warp 0 the CTAs' lists; a child's
+    // probability is its q entry, recomputed by the same expression
+    if (rank != 0) return;
+    warp_merge_topk(s_gz + wid * SEL_WARPS * k, s_gi + wid * SEL_WARPS * k, s_gz + wid * SEL_WARPS * k,
+                    SEL_WARPS * k, k, s_cz + wid * k, s_ci + wid * k, s_cq + wid * k);
+    __syncthreads();
+    if (wid != 0) return;
     warp_merge_topk(s_cz, s_ci, s_cq, SEL_CL * k, k, s_wz, s_wi, s_wq);
     if (lane < p.K) {
       const bool ok = lane < k && s_wi[lane] != INT32_MAX && s_wi[lane] < V;
