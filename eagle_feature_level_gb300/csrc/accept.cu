@@ -2,7 +2,7 @@
 // [C] "为什么普通草稿模型不够理想").
 //  target_softmax: per (request, tree slot): argmax of the target logits
 //    (ties to the lower id) and, for sampling requests, p = softmax(z / T).
-//  accept_walk: one CTA per request walks from the root.
+//  accept_walk: one cluster per request walks from the root.
 //    greedy   -- descend while a retained child carries the target argmax;
 //                the argmax at the last node is the correction/bonus token.
 //    sampling -- recursive multi-candidate rejection sampling in exact
@@ -16,6 +16,7 @@
 //                final token; no candidate left -> final = one draw from P.
 #include "internal.h"
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace eagle {
 namespace {
@@ -97,7 +98,6 @@ struct WalkParams {
   const float* q;          // [B][E][V]
   const float* temperature;
   uint32_t seed, round_id;
-  uint64_t* scratch;       // [B][V] current weights P
   int32_t* accept_len;
   int32_t* path;
   int32_t* final_token;
@@ -106,23 +106,41 @@ struct WalkParams {
   uint64_t* stamp;
 };
 
-__global__ void __launch_bounds__(SM_THREADS) accept_walk_kernel(const WalkParams p) {
+// The walk: one cluster of WALK_CL CTAs per request.  The sampling walk
+// spreads the vocabulary over the cluster, WALK_PER consecutive entries per
+// thread (the weights P of the current node and the taken-candidate marks
+// stay in registers); sums and maxima are CTA reductions whose per-CTA
+// values every CTA pushes to every other through distributed shared memory
+// before a cluster barrier, so every CTA holds the same totals and takes the
+// same decisions.  A candidate's weight P[x] is read from the CTA that owns
+// x.  A value published by the n-th barrier sits in slot n % 2, rewritten
+// only two barriers later, after every CTA has read it.  The greedy walk is
+// rank 0's alone.
+constexpr int WALK_CL = 8;
+constexpr int WALK_THREADS = 512;
+constexpr int WALK_PER = 8;
+static_assert(WALK_CL * WALK_THREADS * WALK_PER >= EAGLE_MAX_VOCAB, "one cluster covers the largest vocabulary");
+
+__global__ void __cluster_dims__(WALK_CL, 1, 1) __launch_bounds__(WALK_THREADS)
+    accept_walk_kernel(const WalkParams p) {
   const LaunchStamp ls(p.stamp);
   pdl_wait();      // predecessor outputs visible from here on
   ls.waited();
   pdl_trigger();
   __shared__ uint64_t red_u[32];
   __shared__ int red_i[32];
-  __shared__ uint64_t tprefix[SM_THREADS];
-  __shared__ int s_taken[EAGLE_MAX_CHILDREN];
-  __shared__ uint64_t s_px;
-  __shared__ int s_flag, s_u, s_final;
-  const int b = blockIdx.x, tid = threadIdx.x;
+  __shared__ uint64_t x_a[2][WALK_CL], x_b[2][WALK_CL];   // per-CTA values, by barrier parity
+  __shared__ uint64_t x_px[2];                            // P at the next candidate (its owner CTA)
+  __shared__ int x_pick[2];                               // the final draw (rank 0)
+  const int b = blockIdx.x / WALK_CL;
+  const uint32_t rank = sm100::cluster_rank();
+  const int tid = threadIdx.x;
   const size_t tb = static_cast<size_t>(b) * p.S;
   const float T = p.temperature[b];
   int32_t* path = p.path + static_cast<size_t>(b) * p.path_cap;
 
   if (!(T > 0.f)) {  // greedy walk, over the tree staged in shared memory
+    if (rank != 0) return;
     __shared__ int s_par[EAGLE_MAX_NODES], s_tok[EAGLE_MAX_NODES], s_am[EAGLE_MAX_NODES];
     const int size = min(p.t_size[b], min(p.S, EAGLE_MAX_NODES));
     for (int c = tid; c < size; c += blockDim.x) {
@@ -151,146 +169,185 @@ __global__ void __launch_bounds__(SM_THREADS) accept_walk_kernel(const WalkParam
     return;
   }
 
-  const int per = (p.V + SM_THREADS - 1) / SM_THREADS;
-  const int v0 = tid * per, v1 = min(p.V, v0 + per);
-  uint64_t* P = p.scratch + static_cast<size_t>(b) * p.V;
-  int u = 0, a = 0;
-  if (tid == 0) path[0] = 0;
-  int final_tok = -1;
+  sm100::cluster_sync();                     // every CTA of the cluster has started
+  int ph = 0;                                // cluster barriers passed since
+  const bool lead = rank == 0 && tid == 0;
+  const int V = p.V;
+  const int v0 = (static_cast<int>(rank) * WALK_THREADS + tid) * WALK_PER;
+  auto owner = [](int v) { return static_cast<uint32_t>(v / (WALK_THREADS * WALK_PER)); };
+  // this CTA's value v (held by every thread) into slot ph % 2 of every CTA
+  auto publish = [&](uint64_t (*xs)[WALK_CL], uint64_t v) {
+    if (tid < WALK_CL) sm100::dsmem_st_u64(sm100::dsmem_addr(&xs[ph & 1][rank], tid), v);
+  };
+  auto barrier = [&]() {
+    sm100::cluster_sync();
+    ++ph;
+  };
+  auto total = [&](uint64_t (*xs)[WALK_CL]) {  // the published values' sum, in rank order
+    uint64_t t = 0;
+    for (int c = 0; c < WALK_CL; ++c) t += xs[(ph - 1) & 1][c];
+    return t;
+  };
+  const int32_t* ctok_b = p.ctok + static_cast<size_t>(b) * p.E * p.K;
+
+  int u = 0, a = 0, final_tok = -1;
+  if (lead) path[0] = 0;
+  uint64_t P[WALK_PER];
   while (true) {
-    // P = target weights of node u
-    const float* pu = p.probs + (tb + u) * p.V;
-    uint64_t ls = 0;
-    for (int v = v0; v < v1; ++v) {
-      const uint64_t w = quantize_prob(pu[v]);
-      P[v] = w;
-      ls += w;
+    // P = target weights of node u; Q = draft weights of its expanded slot
+    const float* pu = p.probs + (tb + u) * V;
+    uint64_t lp = 0;
+#pragma unroll
+    for (int j = 0; j < WALK_PER; ++j) {
+      P[j] = v0 + j < V ? quantize_prob(pu[v0 + j]) : 0ull;
+      lp += P[j];
     }
-    uint64_t SP = block_sum_u64(ls, red_u);
     int e = p.t_exp[tb + u];
     if (e >= p.E) {                   // not an expanded slot of this layout
-      if (tid == 0) set_status(p.status, EAGLE_ERR_INVALID_TREE);
+      if (lead) set_status(p.status, EAGLE_ERR_INVALID_TREE);
       e = -1;
     }
+    const float* qe = e >= 0 ? p.q + (static_cast<size_t>(b) * p.E + e) * V : nullptr;
+    uint64_t lq = 0;
+    if (qe) {
+#pragma unroll
+      for (int j = 0; j < WALK_PER; ++j) lq += v0 + j < V ? quantize_prob(qe[v0 + j]) : 0ull;
+    }
+    const uint64_t cp = block_sum_u64(lp, red_u);
+    const uint64_t cq = block_sum_u64(lq, red_u);
+    publish(x_a, cp);
+    publish(x_b, cq);
+    if (e >= 0 && p.k > 0) {          // P at the first candidate, from its owner
+      const int x0 = ctok_b[e * p.K];
+      if (x0 >= v0 && x0 < v0 + WALK_PER && x0 < V) x_px[ph & 1] = P[x0 - v0];
+    }
+    barrier();
+    uint64_t SP = total(x_a);
+    const uint64_t SQ = total(x_b);
     bool descended = false;
     if (e >= 0) {
-      const float* qe = p.q + (static_cast<size_t>(b) * p.E + e) * p.V;
-      uint64_t lq = 0;
-      for (int v = v0; v < v1; ++v) lq += quantize_prob(qe[v]);
-      const uint64_t SQ = block_sum_u64(lq, red_u);
       uint64_t taken_w = 0;
-      int n_taken = 0;
+      uint32_t tmask = 0;             // this thread's entries drawn as earlier candidates
       for (int i = 0; i < p.k; ++i) {
-        const int x = p.ctok[(static_cast<size_t>(b) * p.E + e) * p.K + i];
+        const int x = ctok_b[e * p.K + i];
         if (x < 0) break;
-        if (x >= p.V) {                 // not a token: the node's candidates end here
-          if (tid == 0) set_status(p.status, EAGLE_ERR_INVALID_ARG);
+        if (x >= V) {                 // not a token: the node's candidates end here
+          if (lead) set_status(p.status, EAGLE_ERR_INVALID_ARG);
           break;
         }
         const uint64_t SQi = SQ - taken_w;
-        __syncthreads();
-        if (x >= v0 && x < v1) s_px = P[x];
-        __syncthreads();
-        if (tid == 0) {
-          const uint64_t Qx = quantize_prob(qe[x]);
-          const uint32_t r = round_uniform(p.seed, i, u, PURPOSE_ACCEPT, b, p.round_id);
-          const u128 lhs = static_cast<u128>(r) * Qx * SP;
-          const u128 rhs = (static_cast<u128>(s_px) * SQi) << 32;
-          s_flag = lhs < rhs ? 1 : 0;
-          if (s_flag) s_u = p.t_child_slot[(static_cast<size_t>(b) * p.E + e) * p.K + i];
-        }
-        __syncthreads();
-        if (s_flag) {
-          int slot = s_u;
-          if (slot >= p.S) {            // outside the tree: treated as pruned
-            if (tid == 0) set_status(p.status, EAGLE_ERR_INVALID_TREE);
+        const uint64_t px = sm100::dsmem_ld_u64(sm100::dsmem_addr(&x_px[(ph - 1) & 1], owner(x)));
+        const uint64_t Qx = quantize_prob(qe[x]);
+        const uint32_t r = round_uniform(p.seed, i, u, PURPOSE_ACCEPT, b, p.round_id);
+        const u128 lhs = static_cast<u128>(r) * Qx * SP;
+        const u128 rhs = (static_cast<u128>(px) * SQi) << 32;
+        if (lhs < rhs) {
+          int slot = p.t_child_slot[(static_cast<size_t>(b) * p.E + e) * p.K + i];
+          if (slot >= p.S) {          // outside the tree: treated as pruned
+            if (lead) set_status(p.status, EAGLE_ERR_INVALID_TREE);
             slot = -1;
           }
           if (slot >= 0 && a + 1 < p.path_cap) {
             u = slot;
             ++a;
-            if (tid == 0) path[a] = u;
+            if (lead) path[a] = u;
             descended = true;
           } else {
             // accepted but pruned: x is the final token (a full path cannot
             // occur: path_cap >= depth + 1 is checked on the host)
-            if (slot >= 0) set_status(p.status, EAGLE_ERR_CAPACITY);
+            if (slot >= 0 && lead) set_status(p.status, EAGLE_ERR_CAPACITY);
             final_tok = x;
           }
           break;
         }
         // rejection: residual max(0, P sum(Q_i) - Q_i sum(P)), rescaled below 2^40
         int lbits = 0;
-        for (int v = v0; v < v1; ++v) {
-          bool tk = false;
-          for (int t = 0; t < n_taken; ++t) tk |= s_taken[t] == v;
-          const uint64_t qv = tk ? 0ull : quantize_prob(qe[v]);
-          const u128 A = static_cast<u128>(P[v]) * SQi, Bq = static_cast<u128>(qv) * SP;
-          const u128 rr = A > Bq ? A - Bq : static_cast<u128>(0);
-          lbits = max(lbits, bitlen128(rr));
+#pragma unroll
+        for (int j = 0; j < WALK_PER; ++j) {
+          if (v0 + j >= V) continue;
+          const uint64_t qv = ((tmask >> j) & 1u) ? 0ull : quantize_prob(qe[v0 + j]);
+          const u128 A = static_cast<u128>(P[j]) * SQi, Bq = static_cast<u128>(qv) * SP;
+          lbits = max(lbits, bitlen128(A > Bq ? A - Bq : static_cast<u128>(0)));
         }
-        const int bits = block_max_i(lbits, red_i);
+        publish(x_a, static_cast<uint64_t>(block_max_i(lbits, red_i)));
+        barrier();
+        int bits = 0;
+        for (int c = 0; c < WALK_CL; ++c) bits = max(bits, static_cast<int>(x_a[(ph - 1) & 1][c]));
         const int shift = bits > QBITS ? bits - QBITS : 0;
-        uint64_t ls2 = 0;
-        for (int v = v0; v < v1; ++v) {
-          bool tk = false;
-          for (int t = 0; t < n_taken; ++t) tk |= s_taken[t] == v;
-          const uint64_t qv = tk ? 0ull : quantize_prob(qe[v]);
-          const u128 A = static_cast<u128>(P[v]) * SQi, Bq = static_cast<u128>(qv) * SP;
-          const u128 rr = A > Bq ? A - Bq : static_cast<u128>(0);
-          const uint64_t w = static_cast<uint64_t>(rr >> shift);
-          P[v] = w;
-          ls2 += w;
+        uint64_t l2 = 0;
+#pragma unroll
+        for (int j = 0; j < WALK_PER; ++j) {
+          if (v0 + j >= V) continue;
+          const uint64_t qv = ((tmask >> j) & 1u) ? 0ull : quantize_prob(qe[v0 + j]);
+          const u128 A = static_cast<u128>(P[j]) * SQi, Bq = static_cast<u128>(qv) * SP;
+          P[j] = static_cast<uint64_t>((A > Bq ? A - Bq : static_cast<u128>(0)) >> shift);
+          l2 += P[j];
         }
-        SP = block_sum_u64(ls2, red_u);
-        __syncthreads();
-        if (tid == 0) s_taken[n_taken] = x;
-        taken_w += quantize_prob(qe[x]);
-        ++n_taken;
-        __syncthreads();
+        publish(x_b, block_sum_u64(l2, red_u));
+        if (i + 1 < p.k) {            // the next candidate's new weight, from its owner
+          const int xn = ctok_b[e * p.K + i + 1];
+          if (xn >= v0 && xn < v0 + WALK_PER && xn < V) x_px[ph & 1] = P[xn - v0];
+        }
+        barrier();
+        SP = total(x_b);
+        if (x >= v0 && x < v0 + WALK_PER) tmask |= 1u << (x - v0);
+        taken_w += Qx;
       }
     }
     if (descended) continue;          // reload P for the accepted child
     if (final_tok < 0) {
-      // one draw from P: thread slices, inclusive scan, search
-      uint64_t ls3 = 0;
-      for (int v = v0; v < v1; ++v) ls3 += P[v];
-      __syncthreads();
-      tprefix[tid] = ls3;
-      __syncthreads();
-      for (int off = 1; off < SM_THREADS; off <<= 1) {
-        const uint64_t add = tid >= off ? tprefix[tid - off] : 0ull;
-        __syncthreads();
-        tprefix[tid] += add;
-        __syncthreads();
+      // one draw from P: the entry whose inclusive prefix first exceeds
+      // t = floor(u32 * sum / 2^32), scanning entries in vocabulary order
+      uint64_t l3 = 0;
+#pragma unroll
+      for (int j = 0; j < WALK_PER; ++j) l3 += P[j];
+      const int lane = tid & 31, wid = tid >> 5;
+      uint64_t incl = l3;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-      if (tid == 0) {
-        const uint64_t tot = tprefix[SM_THREADS - 1];
-        int pick = -1;
-        if (tot > 0) {
-          const uint32_t r = round_uniform(p.seed, 0, u, PURPOSE_FINAL, b, p.round_id);
-          const uint64_t t = scale_uniform(r, tot);
-          int lo = 0, hi = SM_THREADS - 1;
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (tprefix[mid] > t) hi = mid; else lo = mid + 1;
+      __syncthreads();
+      if (lane == 31) red_u[wid] = incl;
+      __syncthreads();
+      uint64_t before = incl - l3, cta = 0;
+      for (int w = 0; w < WALK_THREADS / 32; ++w) {
+        if (w < wid) before += red_u[w];
+        cta += red_u[w];
+      }
+      publish(x_a, cta);
+      barrier();
+      uint64_t tot = 0;
+      for (int c = 0; c < WALK_CL; ++c) {
+        const uint64_t tc = x_a[(ph - 1) & 1][c];
+        if (c < static_cast<int>(rank)) before += tc;
+        tot += tc;
+      }
+      if (tot > 0) {
+        const uint32_t r = round_uniform(p.seed, 0, u, PURPOSE_FINAL, b, p.round_id);
+        const uint64_t t = scale_uniform(r, tot);
+        if (l3 > 0 && before <= t && t - before < l3) {
+          uint64_t run = before;
+          int pick = -1;
+#pragma unroll
+          for (int j = 0; j < WALK_PER; ++j) {
+            run += P[j];
+            if (pick < 0 && run > t) pick = v0 + j;
           }
-          uint64_t run = lo > 0 ? tprefix[lo - 1] : 0ull;
-          const int s0 = lo * per, s1 = min(p.V, s0 + per);
-          for (int v = s0; v < s1; ++v) {
-            run += P[v];
-            if (run > t) { pick = v; break; }
-          }
+          sm100::dsmem_st_s32(sm100::dsmem_addr(&x_pick[ph & 1], 0), pick);
         }
-        if (pick < 0) set_status(p.status, EAGLE_ERR_NUMERIC);
-        s_final = pick;
+        barrier();
+        final_tok = rank == 0 ? x_pick[(ph - 1) & 1] : 0;
+        if (final_tok < 0 && lead) set_status(p.status, EAGLE_ERR_NUMERIC);
+      } else {
+        if (lead) set_status(p.status, EAGLE_ERR_NUMERIC);
+        final_tok = -1;
       }
-      __syncthreads();
-      final_tok = s_final;
     }
     break;
   }
-  if (tid == 0) {
+  if (lead) {
     p.accept_len[b] = a;
     p.final_token[b] = final_tok;
     p.last_slot[b] = u;
@@ -336,7 +393,6 @@ cudaError_t launch_accept_walk(eagle_ctx* ctx, const eagle_plan* plan, int batch
   p.temperature = s->temperature;
   p.seed = s->seed;
   p.round_id = s->round_id;
-  p.scratch = ws_ptr<uint64_t>(ws, ctx->ws.accept_scratch);
   p.accept_len = out->accept_len;
   p.path = out->path;
   p.final_token = out->final_token;
@@ -344,7 +400,7 @@ cudaError_t launch_accept_walk(eagle_ctx* ctx, const eagle_plan* plan, int batch
   p.status = ws_ptr<int>(ws, ctx->ws.status);
   p.stamp = stamp_slot(ctx, EAGLE_K_ACCEPT);
   trace_before(ctx, EAGLE_K_ACCEPT, st);
-  const cudaError_t e = launch_pdl(accept_walk_kernel, dim3(batch), dim3(SM_THREADS), 0, st, p);
+  const cudaError_t e = launch_pdl(accept_walk_kernel, dim3(batch * WALK_CL), dim3(WALK_THREADS), 0, st, p);
   ctx->launches++;
   trace_after(ctx, EAGLE_K_ACCEPT, st);
   return e;

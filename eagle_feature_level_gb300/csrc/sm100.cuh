@@ -231,6 +231,11 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank)
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
   return a;
 }
+__device__ __forceinline__ uint64_t dsmem_ld_u64(uint32_t a) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
+}
 __device__ __forceinline__ void dsmem_st_f32(uint32_t a, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
 }
