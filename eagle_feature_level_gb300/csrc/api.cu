@@ -118,7 +118,6 @@ void layout(eagle_ctx* c) {
   }
   W.attn_part = take(records * (D.head_dim + 4) * 4);
   W.attn_cnt = take(static_cast<size_t>(2) * L.max_batch * D.n_kv_heads * 4);
-  W.accept_scratch = take(static_cast<size_t>(L.max_batch) * D.vocab * 8);
   W.total = off;
 }
 

@@ -1078,6 +1078,367 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1) tree_attn_mma_kernel
   cp_async_wait<0>();
 }
 
+
+// ---- verification layer, many query rows per kv head: tcgen05 ---------------
+//
+// One CTA of 256 threads per (request, kv head, block of 128 query rows,
+// prefix split); the last split also takes the tree part, its online softmax
+// continuing over the tree keys.  Per tile of 64 keys:
+//   S   = Q K^T      tcgen05.mma, M 128 x N 64 over dh, into tensor memory
+//   softmax          thread (warp % 4) * 32 + lane owns query row = its TMEM
+//                    lane: mask, scale, running max and sum, P = exp(S - m)
+//                    as bf16 hi + lo (both warpgroups compute the same row
+//                    statistics; warps 0-3 write keys 0-31 of P, 4-7 keys
+//                    32-63)
+//   O_t = P V        tcgen05.mma, M 128 x N dh over the 64 keys (P hi, then
+//                    P lo), into tensor memory
+//   O = O c + O_t    in registers: warps 0-3 hold output columns 0-63 of
+//                    their rows, warps 4-7 columns 64-127
+// Operands sit in shared memory in the 128-byte swizzled K-major layout the
+// weight stream uses: Q [128 rows][dh], the K tile [64 keys][dh], V
+// transposed to [dh][64 keys] as it is staged, P [128 rows][64 keys].  The
+// next tile's K and V are loaded into registers while the current one is
+// computed.  bf16 queries and keys (verification), dh = 128.  With one
+// split per (request, kv head, row block) the CTA writes the output rows;
+// with several, records like the other kernels' and the last CTA of the
+// (request, kv head) merges them.
+constexpr int TC_THREADS = 256;
+constexpr int TC_ROWS = 128;
+constexpr int TC_KEYS = 64;
+constexpr int TC_DH = 128;
+constexpr uint32_t TC_Q_OFF = 0;                   // 2 k-blocks x 16 row groups x 1024 B
+constexpr uint32_t TC_K_OFF = TC_Q_OFF + 32768;    // 2 k-blocks x 8 key groups
+constexpr uint32_t TC_VT_OFF = TC_K_OFF + 16384;   // 1 k-block x 16 dh groups
+constexpr uint32_t TC_PH_OFF = TC_VT_OFF + 16384;  // 1 k-block x 16 row groups
+constexpr uint32_t TC_PL_OFF = TC_PH_OFF + 16384;
+constexpr size_t TC_SMEM = TC_PL_OFF + 16384 + 1024;   // + room to align the base to 1024 bytes
+constexpr int TC_MAX_SPLITS = 8;
+
+// Byte offset of the 16-byte chunk holding elements [k, k + 8) (k a multiple
+// of 8) of row `row` in a K-major 128-byte-swizzled operand of kb k-blocks
+// of 64 elements: 8-row groups of kb 1024-byte atoms, chunk j of row r of an
+// atom stored at chunk j ^ r.
+__device__ __forceinline__ uint32_t sw128_off(int row, int k, int kb) {
+  const int r = row & 7;
+  return static_cast<uint32_t>(((row >> 3) * kb + (k >> 6)) * 1024 + r * 128 + ((((k & 63) >> 3) ^ r) << 4));
+}
+
+// Key rows of a tile as 16-byte chunks: this thread's share (4 chunks of K
+// and 4 of V), zero past the tile's keys.  K chunk i of thread t is chunk
+// (t + 256 i) % 16 of key (t + 256 i) / 16 (a warp reads two whole key
+// rows); V chunk i is chunk ((t + 256 i) / 64) % 16 of key (t + 256 i) % 64
+// (a warp covers 32 consecutive keys of one 8-dim chunk, so that its
+// transposed 2-byte stores fall on distinct banks).  A prefix row in an
+// unallocated block reads as zero and is reported.
+struct TcChunks {
+  uint4 k[4], v[4];
+};
+// Global element offset of key kk of the tile, dims c8.., or -1 (no row).
+__device__ __forceinline__ long long tc_row_off(const AttnParams& p, int b, int h, bool tree, int k0, int kk,
+                                                int c8) {
+  if (tree) return ((static_cast<long long>(b) * p.tree_cap + k0 + kk) * p.Hkv + h) * TC_DH + c8;
+  long long row = static_cast<long long>(b) * p.kv_cap + k0 + kk;
+  if (p.paged.table) {
+    row = paged_row(p.paged, b, k0 + kk);
+    if (row < 0) {
+      if (c8 == 0) set_status(p.status, EAGLE_ERR_INVALID_ARG);
+      return -1;
+    }
+  }
+  return (row * p.Hkv + h) * TC_DH + c8;
+}
+__device__ __forceinline__ void tc_load(const AttnParams& p, TcChunks& c, int b, int h, bool tree, int k0, int nk) {
+  const uint16_t* kb = tree ? p.kt_bf16 : p.kp;
+  const uint16_t* vb = tree ? p.vt_bf16 : p.vp;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = threadIdx.x + TC_THREADS * i;
+    c.k[i] = make_uint4(0u, 0u, 0u, 0u);
+    c.v[i] = c.k[i];
+    {
+      const int kk = idx >> 4, c8 = (idx & 15) * 8;
+      const long long off = kk < nk ? tc_row_off(p, b, h, tree, k0, kk, c8) : -1;
+      if (off >= 0) c.k[i] = __ldcg(reinterpret_cast<const uint4*>(kb + off));
+    }
+    {
+      const int kk = idx & 63, c8 = ((idx >> 6) & 15) * 8;
+      const long long off = kk < nk ? tc_row_off(p, b, h, tree, k0, kk, c8) : -1;
+      if (off >= 0) c.v[i] = __ldcg(reinterpret_cast<const uint4*>(vb + off));
+    }
+  }
+}
+__device__ __forceinline__ void tc_store(uint8_t* sm, const TcChunks& c) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = threadIdx.x + TC_THREADS * i;
+    {
+      const int kk = idx >> 4, c8 = (idx & 15) * 8;
+      *reinterpret_cast<uint4*>(sm + TC_K_OFF + sw128_off(kk, c8, 2)) = c.k[i];
+    }
+    {
+      const int kk = idx & 63, c8 = ((idx >> 6) & 15) * 8;
+      const uint16_t* ve = reinterpret_cast<const uint16_t*>(&c.v[i]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)          // V[key kk][dim c8 + j] -> Vt[dim c8 + j][key kk]
+        *reinterpret_cast<uint16_t*>(sm + TC_VT_OFF + sw128_off(c8 + j, kk & ~7, 1) + (kk & 7) * 2) = ve[j];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1) tree_attn_tc_kernel(const AttnParams p) {
+  const LaunchStamp ls(p.stamp);
+  extern __shared__ uint8_t smem_tc_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_tc_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t s_bar[2];          // S complete, O_t complete
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_ok, s_last;
+  __shared__ uint64_t s_mask[TC_ROWS * MASKW];
+
+  const int split = blockIdx.x, rb = blockIdx.y, pair = blockIdx.z;
+  const int b = pair / p.Hkv, h = pair % p.Hkv;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int row = quarter * 32 + lane;                 // query row of the block = tensor-memory lane
+  const bool last_split = split == p.n_splits - 1;
+  int lo = 0, hi = 0;
+  {
+    const int L = prefix_rows(p, b, split == 0 && rb == 0 && tid == 0);
+    lo = split * p.chunk;
+    hi = min(L, lo + p.chunk);
+  }
+  const int n_pre = hi > lo ? (hi - lo + TC_KEYS - 1) / TC_KEYS : 0;
+  if (tid == 0) {
+    sm100::mbar_init(&s_bar[0], 1);
+    sm100::mbar_init(&s_bar[1], 1);
+    sm100::fence_barrier_init();
+  }
+  // The prefix is this round's input, written by no kernel of the round:
+  // the split's first tile is loaded before the dependency wait.
+  TcChunks next;
+  if (n_pre > 0) tc_load(p, next, b, h, false, lo, min(TC_KEYS, hi - lo));
+  pdl_wait();                                // q rows, tree K/V, masks and the tree's size
+  ls.waited();
+  const int R = n_nodes(p, b) * p.G;
+  const int r0 = rb * TC_ROWS;
+  const int rows_here = max(0, min(TC_ROWS, R - r0));
+  const int tree_keys = last_split ? min(p.tree_size[b], p.tree_cap) : 0;
+  const int n_tree = (tree_keys + TC_KEYS - 1) / TC_KEYS;
+  const int n_tiles = rows_here > 0 ? n_pre + n_tree : 0;
+  if (n_pre == 0 && n_tiles > 0) tc_load(p, next, b, h, true, 0, min(TC_KEYS, tree_keys));
+  // Tensor memory only after the wait (every kernel this one waits for has
+  // finished), and dependents start only once every CTA holds its columns
+  // (the trigger follows the barrier after the allocation): no kernel that
+  // waits for this one can hold the columns it waits for.
+  if (warp == 0) {
+    sm100::tmem_alloc(&s_tmem, 256);
+    sm100::tmem_relinquish();
+  }
+  // the block's query rows (bf16), swizzled; rows past the block's zero
+  for (int idx = tid; idx < TC_ROWS * (TC_DH / 8); idx += TC_THREADS) {
+    const int rr = idx / (TC_DH / 8), c8 = (idx % (TC_DH / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (rr < rows_here) {
+      const int r = r0 + rr, node = r / p.G, hq = h * p.G + r % p.G;
+      v = *reinterpret_cast<const uint4*>(p.q_bf16 + q_index(p, b, node, hq) + c8);
+    }
+    *reinterpret_cast<uint4*>(sm + TC_Q_OFF + sw128_off(rr, c8, 2)) = v;
+  }
+  if (n_tree > 0 && tid < TC_ROWS) {
+    if (tid < rows_here) {
+      load_row_mask(p, s_mask + tid * MASKW, b, (r0 + tid) / p.G);
+    } else {
+#pragma unroll
+      for (int w = 0; w < MASKW; ++w) s_mask[tid * MASKW + w] = 0ull;
+    }
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::tc_fence_after();
+  pdl_trigger();
+  const uint32_t tmem = s_tmem;
+  const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t t_s = tmem, t_o = tmem + 128;           // S: columns 0-63, O_t: 128-255
+  const uint32_t id_s = sm100::idesc_bf16_f32(TC_ROWS, TC_KEYS), id_o = sm100::idesc_bf16_f32(TC_ROWS, TC_DH);
+  const uint32_t sbase = sm100::smem_u32(sm);
+  volatile int* abort_flag = &s_ok;
+  if (tid == 0) s_ok = 0;
+  float o[64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j) o[j] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;
+  bool alive = true;
+  for (int t = 0; t < n_tiles && alive; ++t) {
+    const bool tree = t >= n_pre;
+    const int k0 = tree ? (t - n_pre) * TC_KEYS : lo + t * TC_KEYS;
+    const int nk = tree ? min(TC_KEYS, tree_keys - k0) : min(TC_KEYS, hi - k0);
+    tc_store(sm, next);
+    if (t + 1 < n_tiles) {                 // the next tile's rows travel while this one is computed
+      const bool tn = t + 1 >= n_pre;
+      const int kn = tn ? (t + 1 - n_pre) * TC_KEYS : lo + (t + 1) * TC_KEYS;
+      tc_load(p, next, b, h, tn, kn, tn ? min(TC_KEYS, tree_keys - kn) : min(TC_KEYS, hi - kn));
+    }
+    sm100::fence_proxy_async_smem();       // generic-proxy stores -> tensor-core reads
+    __syncthreads();
+    if (tid == 0) {
+      sm100::tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < TC_DH / 16; ++kk) {
+        const uint32_t off = static_cast<uint32_t>(kk >> 2) * 1024u + static_cast<uint32_t>(kk & 3) * 32u;
+        sm100::mma_bf16(t_s, sm100::smem_desc_sw128_sbo(sbase + TC_Q_OFF + off, 2048),
+                        sm100::smem_desc_sw128_sbo(sbase + TC_K_OFF + off, 2048), id_s, kk > 0 ? 1u : 0u);
+      }
+      sm100::mma_commit(&s_bar[0]);
+      s_ok = sm100::mbar_wait(&s_bar[0], static_cast<uint32_t>(t & 1), abort_flag) ? 0 : 1;
+    }
+    __syncthreads();
+    if (s_ok) {
+      if (tid == 0) set_status(p.status, EAGLE_ERR_TIMEOUT);
+      alive = false;
+      break;
+    }
+    sm100::tc_fence_after();
+    // softmax of this thread's row over the tile
+    float sv[TC_KEYS];
+#pragma unroll
+    for (int c = 0; c < TC_KEYS / 8; ++c) {
+      float v8[8];
+      sm100::tmem_ld8(t_s + lane_base + 8 * c, v8);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sv[8 * c + j] = v8[j];
+    }
+    sm100::tmem_wait_ld();
+    const uint64_t mk = tree ? s_mask[row * MASKW + (k0 >> 6)] : ~0ull;   // a tree tile lies in one mask word
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < TC_KEYS; ++j) {
+      const bool ok = j < nk && ((mk >> j) & 1ull);
+      sv[j] = ok ? sv[j] * p.scale : -INFINITY;
+      mx = fmaxf(mx, sv[j]);
+    }
+    const float m_new = fmaxf(m_run, mx);
+    const float corr = m_new == -INFINITY ? 1.f : __expf(m_run - m_new);
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < TC_KEYS; ++j) {
+      sv[j] = m_new == -INFINITY ? 0.f : __expf(sv[j] - m_new);
+      sum += sv[j];
+    }
+    l_run = l_run * corr + sum;
+    m_run = m_new;
+    // this warpgroup's half of P: keys 32 half .. 32 half + 31, hi and lo
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {          // constant indices: sv stays in registers
+        const float x0 = half ? sv[32 + 8 * c + 2 * q] : sv[8 * c + 2 * q];
+        const float x1 = half ? sv[33 + 8 * c + 2 * q] : sv[8 * c + 2 * q + 1];
+        split_pair(x0, x1, hw[q], lw[q]);
+      }
+      const uint32_t off = sw128_off(row, 32 * half + 8 * c, 1);
+      *reinterpret_cast<uint4*>(sm + TC_PH_OFF + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      *reinterpret_cast<uint4*>(sm + TC_PL_OFF + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+    sm100::fence_proxy_async_smem();
+    sm100::tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      sm100::tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < TC_KEYS / 16; ++kk)
+        sm100::mma_bf16(t_o, sm100::smem_desc_sw128_sbo(sbase + TC_PH_OFF + kk * 32, 1024),
+                        sm100::smem_desc_sw128_sbo(sbase + TC_VT_OFF + kk * 32, 1024), id_o, kk > 0 ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < TC_KEYS / 16; ++kk)
+        sm100::mma_bf16(t_o, sm100::smem_desc_sw128_sbo(sbase + TC_PL_OFF + kk * 32, 1024),
+                        sm100::smem_desc_sw128_sbo(sbase + TC_VT_OFF + kk * 32, 1024), id_o, 1u);
+      sm100::mma_commit(&s_bar[1]);
+      s_ok = sm100::mbar_wait(&s_bar[1], static_cast<uint32_t>(t & 1), abort_flag) ? 0 : 1;
+    }
+    __syncthreads();
+    if (s_ok) {
+      if (tid == 0) set_status(p.status, EAGLE_ERR_TIMEOUT);
+      alive = false;
+      break;
+    }
+    sm100::tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float v8[8];
+      sm100::tmem_ld8(t_o + lane_base + 64 * half + 8 * c, v8);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[8 * c + j] = fmaf(o[8 * c + j], corr, v8[j]);
+    }
+    sm100::tmem_wait_ld();
+    sm100::tc_fence_before();
+  }
+  __syncthreads();
+  if (warp == 0) {
+    sm100::tc_fence_after();
+    sm100::tmem_dealloc(tmem, 256);
+  }
+  if (!alive) return;
+  // this thread's output columns 64 half .. 64 half + 63 of its row
+  const int r = r0 + row;
+  const bool has_row = row < rows_here;
+  const int node = r / p.G, hq = h * p.G + r % p.G;
+  const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
+  if (p.n_splits == 1) {
+    if (has_row) {
+      const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+      float* dst = p.out_f32 + qi * TC_DH + 64 * half;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<float4*>(dst + 4 * c) =
+            make_float4(o[4 * c] * inv, o[4 * c + 1] * inv, o[4 * c + 2] * inv, o[4 * c + 3] * inv);
+    }
+    return;
+  }
+  const int rec = TC_DH + 4;
+  const int ns = p.n_splits;
+  if (has_row) {
+    float* dst = p.part + (qi * ns + split) * rec;
+    if (half == 0) {
+      dst[0] = m_run;
+      dst[1] = l_run;
+    }
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      *reinterpret_cast<float4*>(dst + 4 + 64 * half + 4 * c) = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+  }
+  // the last CTA of this (request, kv head) merges the splits of every row
+  __syncthreads();                           // every thread's records come first
+  if (tid == 0) {
+    const int prev = arrive_acq_rel(&p.counters[pair]);
+    s_last = prev == ns * static_cast<int>(gridDim.y) - 1;
+    if (s_last) p.counters[pair] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  for (int rr = warp; rr < R; rr += TC_THREADS / 32) {
+    const int nd = rr / p.G, hh = h * p.G + rr % p.G;
+    const float* src = p.part + ((static_cast<size_t>(b) * p.rows_cap + nd) * p.Hq + hh) * ns * rec;
+    const float ms = lane < ns ? __ldcg(src + lane * rec) : -INFINITY;
+    const float lsv = lane < ns ? __ldcg(src + lane * rec + 1) : 0.f;
+    float vals[TC_MAX_SPLITS][4];
+#pragma unroll
+    for (int u = 0; u < TC_MAX_SPLITS; ++u)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) vals[u][c] = u < ns ? __ldcg(src + u * rec + 4 + lane + 32 * c) : 0.f;
+    const float M = warp_max(ms);
+    const float wgt = ms == -INFINITY ? 0.f : __expf(ms - M);
+    const float Lsum = warp_sum(wgt * lsv);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < TC_MAX_SPLITS; ++u) {
+      const float ws = __shfl_sync(0xffffffffu, wgt, u);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[c] = fmaf(ws, vals[u][c], acc[c]);
+    }
+    write_merged_row(p, b, nd, hh, acc, Lsum, lane);
+  }
+}
+
 }  // namespace
 
 int attn_splits(const eagle_ctx* ctx, int pairs, int cap, int per_sm) {
@@ -1134,8 +1495,35 @@ static cudaError_t launch_mma(const AttnParams& p, dim3 grid, size_t smem, cudaS
 // cores (10 against 15 us), most of a 16-row tile being padding.
 constexpr int kDraftMmaRows = 8;
 
+// Verification with more query rows per kv head than a four-warp pass takes
+// (dh 128): the tcgen05 kernel, with as many prefix splits (at most
+// TC_MAX_SPLITS, and never more records per row than the workspace and the
+// no-allocation scratch hold) as one wave of CTAs needs.
+static cudaError_t run_attn_tc(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
+  const int rows = p.rows_cap * p.G;
+  const int row_blocks = ceil_div(rows, TC_ROWS);
+  const int pairs = p.B * p.Hkv;
+  const int tiles = ceil_div(p.kv_cap, TILE);
+  int want = ceil_div(ctx->sm_count, pairs * row_blocks);
+  want = std::min(want, std::min(TC_MAX_SPLITS, tiles));
+  want = std::min(want, attn_splits(ctx, pairs, p.kv_cap, kVerifyPerSm) + 1);
+  want = std::max(want, 1);
+  const int per = ceil_div(tiles, want);
+  p.n_splits = ceil_div(tiles, per);         // every split non-empty at full length
+  p.chunk = per * TILE;
+  dim3 grid(p.n_splits, row_blocks, pairs);
+  p.stamp = stamp_slot(ctx, kernel_id);
+  trace_before(ctx, kernel_id, st);
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(tree_attn_tc_kernel), static_cast<int>(TC_SMEM));
+  if (e == cudaSuccess) e = launch_pdl(tree_attn_tc_kernel, grid, dim3(TC_THREADS), TC_SMEM, st, p);
+  ctx->launches++;
+  trace_after(ctx, kernel_id, st);
+  return e;
+}
+
 static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
   if (p.dh % 16 != 0 || p.dh > MAX_DH) return cudaErrorInvalidValue;
+  if (p.mode == 1 && p.dh == TC_DH && p.rows_cap * p.G > ROWS_PASS) return run_attn_tc(ctx, p, kernel_id, st);
   const bool mma = p.mode == 1 || p.rows_cap * p.G >= kDraftMmaRows;
   const int tiles = ceil_div(p.kv_cap, TILE);
   const int rows = p.rows_cap * p.G;

@@ -43,7 +43,6 @@ struct Workspace {
   size_t gemm_cnt;               // int [N_EPI][max_mtiles]
   size_t attn_part;              // fp32 partial (m, l, acc[dh]) records
   size_t attn_cnt;               // int [2][max_batch * Hkv]
-  size_t accept_scratch;         // u64 [max_batch][V] current acceptance weights
   size_t total;
   int max_mtiles;
   int npmax;

@@ -40,6 +40,16 @@ SMALL = {
     "small_ternary4_m120": S.variant("7b_static26", name="small_ternary4_m120", tree="ternary4", top_k=3, depth=4,
                                      top_m=120, d=128, n_q_heads=2, n_kv_heads=2, head_dim=64, d_ff=344, vocab=900,
                                      prefix_len=70, weight_std=0.05),
+    # verification with more than 32 query rows per kv head at head_dim 128
+    # (the tensor-memory kernel): 164 rows in two row blocks over a
+    # five-split prefix (partials merged), and 42 rows for 160 (request, kv
+    # head) pairs (one split each, written directly)
+    "small_tc_merge_dh128": S.variant("70b_x16_eagle2", name="small_tc_merge_dh128", d=256, n_q_heads=8,
+                                      n_kv_heads=2, head_dim=128, d_ff=512, vocab=1000, batch=3, prefix_len=300,
+                                      top_k=4, depth=4, top_m=40, weight_std=0.05),
+    "small_tc_direct_dh128": S.variant("70b_x16_eagle2", name="small_tc_direct_dh128", d=512, n_q_heads=16,
+                                       n_kv_heads=8, head_dim=128, d_ff=512, vocab=500, batch=20, prefix_len=100,
+                                       top_k=3, depth=3, top_m=20, weight_std=0.05),
 }
 
 
