@@ -1086,32 +1086,39 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1) tree_attn_mma_kernel
 // continuing over the tree keys.  Per tile of 64 keys:
 //   S   = Q K^T      tcgen05.mma, M 128 x N 64 over dh, into tensor memory
 //   softmax          thread (warp % 4) * 32 + lane owns query row = its TMEM
-//                    lane: mask, scale, running max and sum, P = exp(S - m)
-//                    as bf16 hi + lo (both warpgroups compute the same row
-//                    statistics; warps 0-3 write keys 0-31 of P, 4-7 keys
-//                    32-63)
-//   O_t = P V        tcgen05.mma, M 128 x N dh over the 64 keys (P hi, then
-//                    P lo), into tensor memory
-//   O = O c + O_t    in registers: warps 0-3 hold output columns 0-63 of
-//                    their rows, warps 4-7 columns 64-127
-// Operands sit in shared memory in the 128-byte swizzled K-major layout the
-// weight stream uses: Q [128 rows][dh], the K tile [64 keys][dh], V
-// transposed to [dh][64 keys] as it is staged, P [128 rows][64 keys].  The
-// next tile's K and V are loaded into registers while the current one is
-// computed.  bf16 queries and keys (verification), dh = 128.  With one
-// split per (request, kv head, row block) the CTA writes the output rows;
-// with several, records like the other kernels' and the last CTA of the
-// (request, kv head) merges them.
+//                    lane: mask, scale, the row maximum (both warpgroups,
+//                    alike), then warps 0-3 take keys 0-31 and warps 4-7
+//                    keys 32-63: P = exp(S - m) as bf16 hi + lo and their
+//                    share of the row sum (added at the end)
+//   O += P V         tcgen05.mma, M 128 x N dh over the 64 keys (P hi, then
+//                    P lo), accumulating in tensor memory across the tiles
+// P is taken relative to a per-row reference maximum, raised (and O, l
+// rescaled in place) only when a tile's maximum exceeds it by more than
+// TC_RESCALE: P stays below e^TC_RESCALE, O / l is unchanged.  Tiles are
+// double-buffered (K, V, P in shared memory, S in tensor memory): the MMAs
+// of tile t's P V and tile t + 1's S are issued together, and one wait for
+// both precedes tile t + 1's softmax.  Operands sit in shared memory in the
+// 128-byte swizzled K-major layout the weight stream uses: Q [128 rows][dh],
+// K tiles [64 keys][dh], V transposed to [dh][64 keys] as it is staged, P
+// [128 rows][64 keys].  The tile after next is loaded into registers while
+// the current one is computed.  bf16 queries and keys (verification), dh =
+// 128.  At the end warps 0-3 read output columns 0-63 of their rows from
+// tensor memory, warps 4-7 columns 64-127.  With one split per (request, kv
+// head, row block) the CTA writes the output rows; with several, records
+// like the other kernels' and the last CTA of the (request, kv head) merges
+// them.
 constexpr int TC_THREADS = 256;
 constexpr int TC_ROWS = 128;
 constexpr int TC_KEYS = 64;
 constexpr int TC_DH = 128;
 constexpr uint32_t TC_Q_OFF = 0;                   // 2 k-blocks x 16 row groups x 1024 B
-constexpr uint32_t TC_K_OFF = TC_Q_OFF + 32768;    // 2 k-blocks x 8 key groups
-constexpr uint32_t TC_VT_OFF = TC_K_OFF + 16384;   // 1 k-block x 16 dh groups
-constexpr uint32_t TC_PH_OFF = TC_VT_OFF + 16384;  // 1 k-block x 16 row groups
-constexpr uint32_t TC_PL_OFF = TC_PH_OFF + 16384;
-constexpr size_t TC_SMEM = TC_PL_OFF + 16384 + 1024;   // + room to align the base to 1024 bytes
+constexpr uint32_t TC_K_OFF = TC_Q_OFF + 32768;    // two buffers: 2 k-blocks x 8 key groups
+constexpr uint32_t TC_VT_OFF = TC_K_OFF + 32768;   // two buffers: 1 k-block x 16 dh groups
+constexpr uint32_t TC_PH_OFF = TC_VT_OFF + 32768;  // two buffers: 1 k-block x 16 row groups
+constexpr uint32_t TC_PL_OFF = TC_PH_OFF + 32768;
+constexpr uint32_t TC_BUF = 16384;                 // one buffer of K, V^T, P hi or P lo
+constexpr size_t TC_SMEM = TC_PL_OFF + 32768 + 1024;   // + room to align the base to 1024 bytes
+constexpr float TC_RESCALE = 8.0f;                 // reference maximum raised past this margin
 constexpr int TC_MAX_SPLITS = 8;
 
 // Byte offset of the 16-byte chunk holding elements [k, k + 8) (k a multiple
@@ -1167,20 +1174,22 @@ __device__ __forceinline__ void tc_load(const AttnParams& p, TcChunks& c, int b,
     }
   }
 }
-__device__ __forceinline__ void tc_store(uint8_t* sm, const TcChunks& c) {
+__device__ __forceinline__ void tc_store(uint8_t* sm, const TcChunks& c, int buf) {
+  uint8_t* kt = sm + TC_K_OFF + buf * TC_BUF;
+  uint8_t* vt = sm + TC_VT_OFF + buf * TC_BUF;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int idx = threadIdx.x + TC_THREADS * i;
     {
       const int kk = idx >> 4, c8 = (idx & 15) * 8;
-      *reinterpret_cast<uint4*>(sm + TC_K_OFF + sw128_off(kk, c8, 2)) = c.k[i];
+      *reinterpret_cast<uint4*>(kt + sw128_off(kk, c8, 2)) = c.k[i];
     }
     {
       const int kk = idx & 63, c8 = ((idx >> 6) & 15) * 8;
       const uint16_t* ve = reinterpret_cast<const uint16_t*>(&c.v[i]);
 #pragma unroll
       for (int j = 0; j < 8; ++j)          // V[key kk][dim c8 + j] -> Vt[dim c8 + j][key kk]
-        *reinterpret_cast<uint16_t*>(sm + TC_VT_OFF + sw128_off(c8 + j, kk & ~7, 1) + (kk & 7) * 2) = ve[j];
+        *reinterpret_cast<uint16_t*>(vt + sw128_off(c8 + j, kk & ~7, 1) + (kk & 7) * 2) = ve[j];
     }
   }
 }
@@ -1189,10 +1198,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tree_attn_tc_kernel(const AttnP
   const LaunchStamp ls(p.stamp);
   extern __shared__ uint8_t smem_tc_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_tc_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t s_bar[2];          // S complete, O_t complete
+  __shared__ uint64_t s_bar[4];          // S of buffer 0 / 1 complete, P V of buffer 0 / 1 complete
   __shared__ uint32_t s_tmem;
   __shared__ int s_ok, s_last;
   __shared__ uint64_t s_mask[TC_ROWS * MASKW];
+  __shared__ float s_lpart[2][TC_ROWS];    // each warpgroup's share of the row sums
 
   const int split = blockIdx.x, rb = blockIdx.y, pair = blockIdx.z;
   const int b = pair / p.Hkv, h = pair % p.Hkv;
@@ -1208,8 +1218,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tree_attn_tc_kernel(const AttnP
   }
   const int n_pre = hi > lo ? (hi - lo + TC_KEYS - 1) / TC_KEYS : 0;
   if (tid == 0) {
-    sm100::mbar_init(&s_bar[0], 1);
-    sm100::mbar_init(&s_bar[1], 1);
+    for (int k = 0; k < 4; ++k) sm100::mbar_init(&s_bar[k], 1);
     sm100::fence_barrier_init();
   }
   // The prefix is this round's input, written by no kernel of the round:
@@ -1257,38 +1266,49 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tree_attn_tc_kernel(const AttnP
   pdl_trigger();
   const uint32_t tmem = s_tmem;
   const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-  const uint32_t t_s = tmem, t_o = tmem + 128;           // S: columns 0-63, O_t: 128-255
+  const uint32_t t_o = tmem + 128;                       // S buffers: columns 0 and 64; O: 128-255
   const uint32_t id_s = sm100::idesc_bf16_f32(TC_ROWS, TC_KEYS), id_o = sm100::idesc_bf16_f32(TC_ROWS, TC_DH);
   const uint32_t sbase = sm100::smem_u32(sm);
   volatile int* abort_flag = &s_ok;
   if (tid == 0) s_ok = 0;
-  float o[64];
+  // S(t) = Q K(t)^T into S buffer t % 2 (issued by thread 0)
+  auto issue_s = [&](int buf) {
 #pragma unroll
-  for (int j = 0; j < 64; ++j) o[j] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
+    for (int kk = 0; kk < TC_DH / 16; ++kk) {
+      const uint32_t off = static_cast<uint32_t>(kk >> 2) * 1024u + static_cast<uint32_t>(kk & 3) * 32u;
+      sm100::mma_bf16(tmem + 64u * buf, sm100::smem_desc_sw128_sbo(sbase + TC_Q_OFF + off, 2048),
+                      sm100::smem_desc_sw128_sbo(sbase + TC_K_OFF + buf * TC_BUF + off, 2048), id_s,
+                      kk > 0 ? 1u : 0u);
+    }
+    sm100::mma_commit(&s_bar[buf]);
+  };
+  float m_ref = -INFINITY, l_run = 0.f;
   bool alive = true;
-  for (int t = 0; t < n_tiles && alive; ++t) {
-    const bool tree = t >= n_pre;
-    const int k0 = tree ? (t - n_pre) * TC_KEYS : lo + t * TC_KEYS;
-    const int nk = tree ? min(TC_KEYS, tree_keys - k0) : min(TC_KEYS, hi - k0);
-    tc_store(sm, next);
-    if (t + 1 < n_tiles) {                 // the next tile's rows travel while this one is computed
-      const bool tn = t + 1 >= n_pre;
-      const int kn = tn ? (t + 1 - n_pre) * TC_KEYS : lo + (t + 1) * TC_KEYS;
+  if (n_tiles > 0) {
+    tc_store(sm, next, 0);
+    if (n_tiles > 1) {
+      const bool tn = 1 >= n_pre;
+      const int kn = tn ? (1 - n_pre) * TC_KEYS : lo + TC_KEYS;
       tc_load(p, next, b, h, tn, kn, tn ? min(TC_KEYS, tree_keys - kn) : min(TC_KEYS, hi - kn));
     }
     sm100::fence_proxy_async_smem();       // generic-proxy stores -> tensor-core reads
     __syncthreads();
     if (tid == 0) {
       sm100::tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < TC_DH / 16; ++kk) {
-        const uint32_t off = static_cast<uint32_t>(kk >> 2) * 1024u + static_cast<uint32_t>(kk & 3) * 32u;
-        sm100::mma_bf16(t_s, sm100::smem_desc_sw128_sbo(sbase + TC_Q_OFF + off, 2048),
-                        sm100::smem_desc_sw128_sbo(sbase + TC_K_OFF + off, 2048), id_s, kk > 0 ? 1u : 0u);
-      }
-      sm100::mma_commit(&s_bar[0]);
-      s_ok = sm100::mbar_wait(&s_bar[0], static_cast<uint32_t>(t & 1), abort_flag) ? 0 : 1;
+      issue_s(0);
+    }
+  }
+  for (int t = 0; t < n_tiles; ++t) {
+    const int buf = t & 1;
+    const bool tree = t >= n_pre;
+    const int k0 = tree ? (t - n_pre) * TC_KEYS : lo + t * TC_KEYS;
+    const int nk = tree ? min(TC_KEYS, tree_keys - k0) : min(TC_KEYS, hi - k0);
+    // one wait: P V of tile t - 1 (its buffers and O) and S of tile t
+    if (tid == 0) {
+      bool ok = true;
+      if (t >= 1) ok = sm100::mbar_wait(&s_bar[2 + ((t - 1) & 1)], static_cast<uint32_t>(((t - 1) >> 1) & 1), abort_flag);
+      if (ok) ok = sm100::mbar_wait(&s_bar[buf], static_cast<uint32_t>((t >> 1) & 1), abort_flag);
+      s_ok = ok ? 0 : 1;
     }
     __syncthreads();
     if (s_ok) {
@@ -1297,12 +1317,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tree_attn_tc_kernel(const AttnP
       break;
     }
     sm100::tc_fence_after();
+    if (t + 1 < n_tiles) {                 // tile t + 1 into the other buffers, tile t + 2 into registers
+      tc_store(sm, next, buf ^ 1);
+      if (t + 2 < n_tiles) {
+        const bool tn = t + 2 >= n_pre;
+        const int kn = tn ? (t + 2 - n_pre) * TC_KEYS : lo + (t + 2) * TC_KEYS;
+        tc_load(p, next, b, h, tn, kn, tn ? min(TC_KEYS, tree_keys - kn) : min(TC_KEYS, hi - kn));
+      }
+    }
     // softmax of this thread's row over the tile
     float sv[TC_KEYS];
 #pragma unroll
     for (int c = 0; c < TC_KEYS / 8; ++c) {
       float v8[8];
-      sm100::tmem_ld8(t_s + lane_base + 8 * c, v8);
+      sm100::tmem_ld8(tmem + 64u * buf + lane_base + 8 * c, v8);
 #pragma unroll
       for (int j = 0; j < 8; ++j) sv[8 * c + j] = v8[j];
     }
@@ -1315,27 +1343,45 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tree_attn_tc_kernel(const AttnP
       sv[j] = ok ? sv[j] * p.scale : -INFINITY;
       mx = fmaxf(mx, sv[j]);
     }
-    const float m_new = fmaxf(m_run, mx);
-    const float corr = m_new == -INFINITY ? 1.f : __expf(m_run - m_new);
+    // raise the reference maximum when the tile's exceeds it by the margin
+    // (O holds nothing yet while the reference is -inf)
+    const bool raise = mx > m_ref + TC_RESCALE || (m_ref == -INFINITY && mx != -INFINITY);
+    const bool rescale = raise && m_ref != -INFINITY;
+    const float factor = rescale ? __expf(m_ref - mx) : 1.f;
+    if (raise) {
+      l_run *= factor;                     // this warpgroup's share of the sum scales alike
+      m_ref = mx;
+    }
+    if (__any_sync(0xffffffffu, rescale)) {  // this warp's O rows times factor (1 where unchanged)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float v8[8];
+        const uint32_t ta = t_o + lane_base + 64 * half + 8 * c;
+        sm100::tmem_ld8(ta, v8);
+        sm100::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v8[j] *= factor;
+        sm100::tmem_st8(ta, v8);
+      }
+      sm100::tmem_wait_st();
+    }
+    // this warpgroup's half of the keys: 32 half .. 32 half + 31 (its share
+    // of the row sum, and of P as hi and lo)
+    float pe[TC_KEYS / 2];
     float sum = 0.f;
 #pragma unroll
-    for (int j = 0; j < TC_KEYS; ++j) {
-      sv[j] = m_new == -INFINITY ? 0.f : __expf(sv[j] - m_new);
-      sum += sv[j];
+    for (int jj = 0; jj < TC_KEYS / 2; ++jj) {    // constant indices: sv stays in registers
+      const float x = half ? sv[32 + jj] : sv[jj];
+      pe[jj] = m_ref == -INFINITY ? 0.f : __expf(x - m_ref);
+      sum += pe[jj];
     }
-    l_run = l_run * corr + sum;
-    m_run = m_new;
-    // this warpgroup's half of P: keys 32 half .. 32 half + 31, hi and lo
+    l_run += sum;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t hw[4], lw[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {          // constant indices: sv stays in registers
-        const float x0 = half ? sv[32 + 8 * c + 2 * q] : sv[8 * c + 2 * q];
-        const float x1 = half ? sv[33 + 8 * c + 2 * q] : sv[8 * c + 2 * q + 1];
-        split_pair(x0, x1, hw[q], lw[q]);
-      }
-      const uint32_t off = sw128_off(row, 32 * half + 8 * c, 1);
+      for (int q = 0; q < 4; ++q) split_pair(pe[8 * c + 2 * q], pe[8 * c + 2 * q + 1], hw[q], lw[q]);
+      const uint32_t off = sw128_off(row, 32 * half + 8 * c, 1) + buf * TC_BUF;
       *reinterpret_cast<uint4*>(sm + TC_PH_OFF + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       *reinterpret_cast<uint4*>(sm + TC_PL_OFF + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
@@ -1344,35 +1390,49 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tree_attn_tc_kernel(const AttnP
     __syncthreads();
     if (tid == 0) {
       sm100::tc_fence_after();
+      if (t + 1 < n_tiles) issue_s(buf ^ 1);
+      const uint32_t ph = sbase + TC_PH_OFF + buf * TC_BUF, pl = sbase + TC_PL_OFF + buf * TC_BUF;
+      const uint32_t vt = sbase + TC_VT_OFF + buf * TC_BUF;
 #pragma unroll
       for (int kk = 0; kk < TC_KEYS / 16; ++kk)
-        sm100::mma_bf16(t_o, sm100::smem_desc_sw128_sbo(sbase + TC_PH_OFF + kk * 32, 1024),
-                        sm100::smem_desc_sw128_sbo(sbase + TC_VT_OFF + kk * 32, 1024), id_o, kk > 0 ? 1u : 0u);
+        sm100::mma_bf16(t_o, sm100::smem_desc_sw128_sbo(ph + kk * 32, 1024), sm100::smem_desc_sw128_sbo(vt + kk * 32, 1024),
+                        id_o, (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
       for (int kk = 0; kk < TC_KEYS / 16; ++kk)
-        sm100::mma_bf16(t_o, sm100::smem_desc_sw128_sbo(sbase + TC_PL_OFF + kk * 32, 1024),
-                        sm100::smem_desc_sw128_sbo(sbase + TC_VT_OFF + kk * 32, 1024), id_o, 1u);
-      sm100::mma_commit(&s_bar[1]);
-      s_ok = sm100::mbar_wait(&s_bar[1], static_cast<uint32_t>(t & 1), abort_flag) ? 0 : 1;
+        sm100::mma_bf16(t_o, sm100::smem_desc_sw128_sbo(pl + kk * 32, 1024), sm100::smem_desc_sw128_sbo(vt + kk * 32, 1024),
+                        id_o, 1u);
+      sm100::mma_commit(&s_bar[2 + buf]);
     }
+  }
+  // the last P V, then this thread's output columns from tensor memory
+  float o[64];
+#pragma unroll
+  for (int j = 0; j < 64; ++j) o[j] = 0.f;
+  if (alive && n_tiles > 0) {
+    if (tid == 0)
+      s_ok = sm100::mbar_wait(&s_bar[2 + ((n_tiles - 1) & 1)], static_cast<uint32_t>(((n_tiles - 1) >> 1) & 1),
+                              abort_flag) ? 0 : 1;
     __syncthreads();
     if (s_ok) {
       if (tid == 0) set_status(p.status, EAGLE_ERR_TIMEOUT);
       alive = false;
-      break;
-    }
-    sm100::tc_fence_after();
+    } else {
+      sm100::tc_fence_after();
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float v8[8];
-      sm100::tmem_ld8(t_o + lane_base + 64 * half + 8 * c, v8);
+      for (int c = 0; c < 8; ++c) {
+        float v8[8];
+        sm100::tmem_ld8(t_o + lane_base + 64 * half + 8 * c, v8);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) o[8 * c + j] = fmaf(o[8 * c + j], corr, v8[j]);
+        for (int j = 0; j < 8; ++j) o[8 * c + j] = v8[j];
+      }
+      sm100::tmem_wait_ld();
     }
-    sm100::tmem_wait_ld();
-    sm100::tc_fence_before();
   }
+  const float m_run = m_ref;
+  s_lpart[half][row] = l_run;
+  sm100::tc_fence_before();
   __syncthreads();
+  l_run = s_lpart[0][row] + s_lpart[1][row];     // the row sum, in the same order in both warpgroups
   if (warp == 0) {
     sm100::tc_fence_after();
     sm100::tmem_dealloc(tmem, 256);
