@@ -237,7 +237,7 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
   __shared__ float s_red[SEL_WARPS];
   __shared__ float s_cmax[SEL_CL], s_csum[SEL_CL];         // per-rank partials (pushed)
   __shared__ uint64_t s_ctot[SEL_CL];
-  __shared__ uint64_t s_wscan[SEL_WARPS];
+  __shared__ uint64_t s_tt[SEL_THREADS], s_wt[SEL_WARPS];    // sampling: integer weight totals per thread, warp
   __shared__ float s_wz[SEL_WARPS * EAGLE_MAX_CHILDREN], s_wq[SEL_WARPS * EAGLE_MAX_CHILDREN];
   __shared__ int s_wi[SEL_WARPS * EAGLE_MAX_CHILDREN];
   // rank 0: every warp's list of every CTA (pushed), then each CTA's merged list
@@ -245,9 +245,6 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
   __shared__ int s_gi[SEL_CL * SEL_WARPS * EAGLE_MAX_CHILDREN];
   __shared__ float s_cz[SEL_CL * EAGLE_MAX_CHILDREN], s_cq[SEL_CL * EAGLE_MAX_CHILDREN];
   __shared__ int s_ci[SEL_CL * EAGLE_MAX_CHILDREN];
-  __shared__ int s_pick[EAGLE_MAX_CHILDREN];                // sampling: drawn token of each round (pushed)
-  __shared__ uint64_t s_pw[EAGLE_MAX_CHILDREN];
-  __shared__ float s_pq[EAGLE_MAX_CHILDREN];
 
   const int row = blockIdx.x / SEL_CL;
   const uint32_t rank = sm100::cluster_rank();
@@ -268,7 +265,6 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
   const float* zrow = p.logits + node * V;
   float* qrow = p.probs + node * V;
   const bool vec = (V & 3) == 0 && v0 + SEL_PER <= V;
-  if (tid < EAGLE_MAX_CHILDREN) s_pick[tid] = -1;
 
   // logits, finiteness, slice max
   float x[SEL_PER];
@@ -390,81 +386,104 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
     return;
   }
 
-  // sampling: exact integer weights, this thread's chunk sum, its exclusive
-  // prefix within the cluster (CTA scan + earlier ranks' totals)
-  uint64_t W[SEL_PER];
+  // sampling: exact integer weights floor(q 2^40).  Every CTA leaves its
+  // per-thread and per-warp weight totals in shared memory; one warp of rank
+  // 0 then makes the k draws without replacement, each by descending from
+  // the CTAs' totals to a warp's and a thread's (reading the other CTAs'
+  // shared memory) and to that thread's entries (their weights again from
+  // q, which every CTA wrote before the barrier), the weights already drawn
+  // taken out at every level: the token is the first one, in vocabulary
+  // order, at which the running sum of the remaining weights exceeds
+  // t = floor(u32 * remaining / 2^32).
   uint64_t wsum = 0;
 #pragma unroll
-  for (int u = 0; u < SEL_PER; ++u) {
-    W[u] = v0 + u < V ? quantize_prob(q[u]) : 0ull;
-    wsum += W[u];
-  }
-  uint64_t incl = wsum;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) s_wscan[wid] = incl;
+  for (int u = 0; u < SEL_PER; ++u) wsum += v0 + u < V ? quantize_prob(q[u]) : 0ull;
+  s_tt[tid] = wsum;
+  const uint64_t wtot = warp_sum_u64(wsum);
+  if (lane == 0) s_wt[wid] = wtot;
   __syncthreads();
-  uint64_t before = incl - wsum, cta_total = 0;
-  for (int w = 0; w < SEL_WARPS; ++w) {
-    if (w < wid) before += s_wscan[w];
-    cta_total += s_wscan[w];
+  if (tid < SEL_CL) {                        // this CTA's total, to every rank
+    uint64_t cta_total = 0;
+    for (int w = 0; w < SEL_WARPS; ++w) cta_total += s_wt[w];
+    sm100::dsmem_st_u64(sm100::dsmem_addr(&s_ctot[rank], tid), cta_total);
   }
-  if (tid < SEL_CL) sm100::dsmem_st_u64(sm100::dsmem_addr(&s_ctot[rank], tid), cta_total);
-  sm100::cluster_sync();
-  uint64_t remaining = 0;
-  for (int c = 0; c < SEL_CL; ++c) {
-    if (c < static_cast<int>(rank)) before += s_ctot[c];
-    remaining += s_ctot[c];
-  }
-  const int v1 = v0 + SEL_PER;
-  bool lost = false;
-  for (int r = 0; r < k; ++r) {
-    if (remaining == 0) break;               // uniform: every CTA tracks the same total
-    const uint32_t u32 = round_uniform(p.seed, r, e, PURPOSE_DRAW, b, p.round_id);
-    const uint64_t t = scale_uniform(u32, remaining);
-    // this thread's range of the remaining (not yet drawn) mass
-    uint64_t start = before, own = wsum;
-    for (int x2 = 0; x2 < r; ++x2) {
-      const int y = s_pick[x2];
-      if (y < 0) continue;
-      if (y < v0) start -= s_pw[x2];
-      else if (y < v1) own -= s_pw[x2];
-    }
-    if (own > 0 && start <= t && t - start < own) {
-      uint64_t run = start;
-      int pick = -1;
-      uint64_t wp = 0;
-      float qp = 0.f;
+  sm100::cluster_sync();                     // every CTA's weights and totals are in place
+  if (rank == 0 && wid == 0) {
+    uint64_t total = 0;
+    for (int c = 0; c < SEL_CL; ++c) total += s_ctot[c];
+    int pk_tok = -1;                         // lane r: the r-th drawn token, its weight and q
+    uint64_t pk_w = 0;
+    float pk_q = 0.f;
+    uint64_t picked = 0;
+    int n_drawn = 0;
+    bool lost = false;
+    // the first lane whose inclusive running sum of adj exceeds t (-1: none);
+    // t becomes the offset inside that lane's range
+    auto descend = [&](uint64_t adj, uint64_t& t) {
+      uint64_t incl = adj;
 #pragma unroll
-      for (int u = 0; u < SEL_PER; ++u) {
-        bool drawn = false;
-        for (int x2 = 0; x2 < r; ++x2) drawn |= s_pick[x2] == v0 + u;
-        if (pick < 0 && !drawn && W[u] > 0) {
-          run += W[u];
-          if (run > t) { pick = v0 + u; wp = W[u]; qp = q[u]; }
-        }
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-      if (pick >= 0) {
-        for (int c = 0; c < SEL_CL; ++c) {
-          sm100::dsmem_st_s32(sm100::dsmem_addr(&s_pick[r], c), pick);
-          sm100::dsmem_st_u64(sm100::dsmem_addr(&s_pw[r], c), wp);
-          sm100::dsmem_st_f32(sm100::dsmem_addr(&s_pq[r], c), qp);
-        }
+      const unsigned m = __ballot_sync(0xffffffffu, incl > t);
+      if (m == 0u) return -1;
+      const int f = __ffs(m) - 1;
+      t -= __shfl_sync(0xffffffffu, incl - adj, f);
+      return f;
+    };
+    // adj minus the weights of the earlier draws that fall in [lo_v, hi_v)
+    auto minus_drawn = [&](uint64_t adj, int lo_v, int hi_v, int r) {
+      for (int s2 = 0; s2 < r; ++s2) {
+        const int tk = __shfl_sync(0xffffffffu, pk_tok, s2);
+        const uint64_t wk = __shfl_sync(0xffffffffu, pk_w, s2);
+        if (tk >= lo_v && tk < hi_v) adj -= wk;
       }
+      return adj;
+    };
+    for (int r = 0; r < k; ++r) {
+      const uint64_t remaining = total - picked;
+      if (remaining == 0) break;             // the distribution ran out of mass
+      const uint32_t u32 = round_uniform(p.seed, r, e, PURPOSE_DRAW, b, p.round_id);
+      uint64_t t = scale_uniform(u32, remaining);
+      // CTA, warp, thread, entry
+      uint64_t adj = lane < SEL_CL ? s_ctot[lane] : 0ull;
+      adj = minus_drawn(adj, lane * SEL_SLICE, (lane + 1) * SEL_SLICE, r);
+      const int c = descend(lane < SEL_CL ? adj : 0ull, t);
+      if (c < 0) { lost = true; break; }
+      const int cb = c * SEL_SLICE;
+      adj = lane < SEL_WARPS ? sm100::dsmem_ld_u64(sm100::dsmem_addr(&s_wt[lane], c)) : 0ull;
+      adj = minus_drawn(adj, cb + lane * 32 * SEL_PER, cb + (lane + 1) * 32 * SEL_PER, r);
+      const int w = descend(lane < SEL_WARPS ? adj : 0ull, t);
+      if (w < 0) { lost = true; break; }
+      const int th = w * 32 + lane;
+      adj = sm100::dsmem_ld_u64(sm100::dsmem_addr(&s_tt[th], c));
+      adj = minus_drawn(adj, cb + th * SEL_PER, cb + (th + 1) * SEL_PER, r);
+      const int j = descend(adj, t);
+      if (j < 0) { lost = true; break; }
+      const int tb = cb + (w * 32 + j) * SEL_PER;
+      const uint64_t wraw = lane < SEL_PER && tb + lane < V ? quantize_prob(qrow[tb + lane]) : 0ull;
+      adj = minus_drawn(wraw, tb + lane, tb + lane + 1, r);
+      const int u = descend(lane < SEL_PER ? adj : 0ull, t);
+      if (u < 0) { lost = true; break; }
+      const int tok = tb + u;
+      const uint64_t wt = __shfl_sync(0xffffffffu, wraw, u);
+      if (lane == r) {
+        pk_tok = tok;
+        pk_w = wt;
+        pk_q = qrow[tok];                    // written by its CTA before the barrier
+      }
+      picked += wt;
+      ++n_drawn;
     }
-    sm100::cluster_sync();
-    if (s_pick[r] < 0) { lost = true; break; }   // cannot happen with consistent prefix sums
-    remaining -= s_pw[r];
+    if (lane < p.K) {
+      const bool ok = lane < k && lane < n_drawn;
+      ct[lane] = ok ? pk_tok : -1;
+      cp[lane] = ok ? pk_q : 0.f;
+    }
+    if (lost && lane == 0) set_status(p.status, EAGLE_ERR_NUMERIC);
   }
-  if (rank == 0 && tid < p.K) {
-    const bool ok = tid < k && s_pick[tid] >= 0;
-    ct[tid] = ok ? s_pick[tid] : -1;
-    cp[tid] = ok ? s_pq[tid] : 0.f;
-  }
-  if (lost && rank == 0 && tid == 0) set_status(p.status, EAGLE_ERR_NUMERIC);
+  sm100::cluster_sync();                     // no CTA leaves while rank 0 still reads its shared memory
 }
 
 }  // namespace
