@@ -16,6 +16,7 @@
 // runs its products on the tensor cores (warp-level bf16 MMA tiles, fp32
 // accumulation), one wave at two CTAs per SM.
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 #include <vector>
 
@@ -81,6 +82,9 @@ struct AttnParams {
   int cluster;                    // tensor-core kernel: the splits of a (request, kv head) form a cluster
                                   // and merge through distributed shared memory (part, counters unused)
   int recs_off;                   // with cluster: byte offset of the CTA's records [rows][dh + 4] in shared memory
+  int tma;                        // tcgen05 kernel: whole prefix tiles by TMA through the launch's tensor maps
+  int box_rows;                   // keys per TMA box: 64, or the block size of a paged prefix
+  int stages;                     // tcgen05 kernel: K/V ring stages
   int* status;                    // device status word (null: not reported)
   uint64_t* stamp;                // launch timestamps (null: off)
 };
@@ -1079,394 +1083,765 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1) tree_attn_mma_kernel
 }
 
 
-// ---- verification layer, many query rows per kv head: tcgen05 ---------------
+// ---- tcgen05 attention with warp roles (dh 128) -------------------------------
 //
-// One CTA of 256 threads per (request, kv head, block of 128 query rows,
-// prefix split); the last split also takes the tree part, its online softmax
-// continuing over the tree keys.  Per tile of 64 keys:
-//   S   = Q K^T      tcgen05.mma, M 128 x N 64 over dh, into tensor memory
-//   softmax          thread (warp % 4) * 32 + lane owns query row = its TMEM
-//                    lane: mask, scale, the row maximum (both warpgroups,
-//                    alike), then warps 0-3 take keys 0-31 and warps 4-7
-//                    keys 32-63: P = exp(S - m) as bf16 hi + lo and their
-//                    share of the row sum (added at the end)
-//   O += P V         tcgen05.mma, M 128 x N dh over the 64 keys (P hi, then
-//                    P lo), accumulating in tensor memory across the tiles
-// P is taken relative to a per-row reference maximum, raised (and O, l
-// rescaled in place) only when a tile's maximum exceeds it by more than
-// TC_RESCALE: P stays below e^TC_RESCALE, O / l is unchanged.  Tiles are
-// double-buffered (K, V, P in shared memory, S in tensor memory): the MMAs
-// of tile t's P V and tile t + 1's S are issued together, and one wait for
-// both precedes tile t + 1's softmax.  Operands sit in shared memory in the
-// 128-byte swizzled K-major layout the weight stream uses: Q [128 rows][dh],
-// K tiles [64 keys][dh], V transposed to [dh][64 keys] as it is staged, P
-// [128 rows][64 keys].  The tile after next is loaded into registers while
-// the current one is computed.  bf16 queries and keys (verification), dh =
-// 128.  At the end warps 0-3 read output columns 0-63 of their rows from
-// tensor memory, warps 4-7 columns 64-127.  With one split per (request, kv
-// head, row block) the CTA writes the output rows; with several, records
-// like the other kernels' and the last CTA of the (request, kv head) merges
-// them.
-constexpr int TC_THREADS = 256;
-constexpr int TC_ROWS = 128;
-constexpr int TC_KEYS = 64;
-constexpr int TC_DH = 128;
-constexpr uint32_t TC_Q_OFF = 0;                   // 2 k-blocks x 16 row groups x 1024 B
-constexpr uint32_t TC_K_OFF = TC_Q_OFF + 32768;    // two buffers: 2 k-blocks x 8 key groups
-constexpr uint32_t TC_VT_OFF = TC_K_OFF + 32768;   // two buffers: 1 k-block x 16 dh groups
-constexpr uint32_t TC_PH_OFF = TC_VT_OFF + 32768;  // two buffers: 1 k-block x 16 row groups
-constexpr uint32_t TC_PL_OFF = TC_PH_OFF + 32768;
-constexpr uint32_t TC_BUF = 16384;                 // one buffer of K, V^T, P hi or P lo
-constexpr size_t TC_SMEM = TC_PL_OFF + 32768 + 1024;   // + room to align the base to 1024 bytes
-constexpr float TC_RESCALE = 8.0f;                 // reference maximum raised past this margin
-constexpr int TC_MAX_SPLITS = 8;
+// One CTA of 640 threads per (prefix split, block of 128 query rows, request
+// and kv head); the last split also takes the tree part, its online softmax
+// continuing over the tree keys.  Roles:
+//   warps 0-1   loaders, warp 0 of every tile's K and warp 1 of its V, each
+//               with its own ring barriers: K is released when S has been
+//               computed, V when P V has, so the K stream runs a whole ring
+//               ahead of S (one ring for both measured load-latency bound).
+//               A whole prefix tile comes by TMA (boxes of 64 dims x 64 keys,
+//               or x one block of a paged prefix); a partial tile, a tile
+//               with an unallocated block and the verification tree's tiles
+//               by 16-byte asynchronous copies with the missing rows zeroed;
+//               the draft tree's fp32 keys and values as bf16 hi + lo pairs,
+//               32 keys a tile.
+//   warp 2      MMA issuer (one thread): S = Q K^T into one of two S buffers
+//               in tensor memory, O += P V with P read from tensor memory.
+//   warps 4-19  softmax, four warpgroups: thread = query row = its tensor-
+//               memory lane (warp % 4 selects the 32-lane quarter), and
+//               warpgroup g takes quarter g of each tile's keys: its partial
+//               row maximum, exchanged with the other three through shared
+//               memory (one barrier of the softmax warps a tile); P = 2^(s c
+//               - m) (c = scale log2 e) of its keys as bf16 hi + lo into
+//               tensor memory; its share of the row sum; quarter g of O's
+//               columns when O is rescaled and at the end.
+// The four warpgroups (rather than two taking all of a row's keys each) hide
+// the latency of the per-tile chain -- tensor-memory load, maximum,
+// exponentials, hi / lo split, tensor-memory store -- measured as the limit.
+// P is relative to a per-row reference maximum m (log2 units), raised -- O
+// and the sums rescaled in place -- only when a tile's maximum passes it by
+// more than WS_RESCALE (natural units): P stays below e^WS_RESCALE and O / l
+// does not depend on when m was raised.  Pipelining: K / V stages in a ring
+// (kv_full / kv_empty barriers); S double-buffered, so S(t + 1) is ready
+// while the softmax of tile t runs, and S(t + 2) is issued as soon as that
+// softmax has loaded S(t) (s_free), before P(t) V(t); P double-buffered; O
+// accumulating in tensor memory over all tiles.  Draft rows (fp32 queries) enter S as hi + lo: S = Qhi K +
+// Qlo K; the draft tree's keys as hi + lo too: S = Qhi Khi + Qlo Khi + Qhi
+// Klo and O += Phi Vhi + Plo Vhi + Phi Vlo.
+// Shared-memory operands use the 128-byte swizzle (1024-byte atoms of 8 rows
+// x 128 bytes, 16-byte chunk j of row r at chunk j ^ (r % 8)): Q as two
+// k-blocks [128 rows][64 dims] (draft: hi, then lo); a ring stage as K [64
+// keys][64 dims] x 2 halves, then V alike -- what TMA writes for boxes of 64
+// dims x 64 keys -- K being the K-major B operand of Q K^T and V the MN-major
+// B operand of P V; a draft-tree stage as K hi, K lo, V hi, V lo of 32 keys.
+constexpr int WS_LOAD_WARPS = 2;
+constexpr int WS_MMA_WARP = 2;                      // (warp 3 has no role)
+constexpr int WS_SOFT_WARP0 = 4;
+constexpr int WS_SOFT_WGS = 4;                      // softmax warpgroups: a quarter of each tile's keys each
+constexpr int WS_THREADS = 32 * (WS_SOFT_WARP0 + 4 * WS_SOFT_WGS);
+constexpr int WS_SOFT_THREADS = 128 * WS_SOFT_WGS;
+constexpr int WS_ROWS = 128;
+constexpr int WS_KEYS = 64;                         // keys per prefix / verification-tree tile
+constexpr int WS_FKEYS = 32;                        // keys per draft-tree tile
+constexpr int WS_DH = 128;
+constexpr uint32_t WS_STAGE = 32768;                // one ring stage: K then V
+constexpr uint32_t WS_HALF = 8192;                  // 64 keys x 64 dims of bf16
+constexpr uint32_t WS_FHALF = 4096;                 // 32 keys x 64 dims of bf16
+constexpr uint32_t WS_QHALF = 16384;                // 128 rows x 64 dims of bf16
+constexpr uint32_t WS_BUDGET = 196608;              // Q + ring stages
+constexpr int WS_MAX_STAGES = 5;
+constexpr size_t WS_SMEM = WS_BUDGET + 1024;        // + room to align the base to 1024 bytes
+constexpr float WS_RESCALE = 8.0f;
+constexpr float WS_LOG2E = 1.4426950408889634f;
+constexpr int WS_MAX_RECS = 16;                     // prefix splits of a (request, kv head) at most
+constexpr uint32_t WS_TM_S = 0;                     // S buffers: columns 0 and 64
+constexpr uint32_t WS_TM_O = 128;                   // O: columns 128-255
+constexpr uint32_t WS_TM_P = 256;                   // P buffers: 256 and 320 (hi, then lo 32 columns on)
+constexpr uint32_t WS_TM_COLS = 512;
+constexpr int WS_BAR_SOFT = 2;                      // named barrier of the softmax warps
 
-// Byte offset of the 16-byte chunk holding elements [k, k + 8) (k a multiple
-// of 8) of row `row` in a K-major 128-byte-swizzled operand of kb k-blocks
-// of 64 elements: 8-row groups of kb 1024-byte atoms, chunk j of row r of an
-// atom stored at chunk j ^ r.
-__device__ __forceinline__ uint32_t sw128_off(int row, int k, int kb) {
-  const int r = row & 7;
-  return static_cast<uint32_t>(((row >> 3) * kb + (k >> 6)) * 1024 + r * 128 + ((((k & 63) >> 3) ^ r) << 4));
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a swizzled
+// block of 128-byte rows.
+__device__ __forceinline__ uint32_t ws_sw(int row, int chunk) {
+  return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
+}
+// 32 lanes x 32 consecutive 32-bit columns (thread i: lane quarter * 32 + i).
+__device__ __forceinline__ void ws_tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void ws_tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 32 lanes x 4 consecutive 32-bit columns, stored.
+__device__ __forceinline__ void ws_tmem_st4(uint32_t taddr, const uint32_t (&w)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3])
+               : "memory");
+}
+// 32 lanes x 8 consecutive 32-bit columns, stored.
+__device__ __forceinline__ void ws_tmem_st8(uint32_t taddr, const uint32_t (&w)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns, stored.
+__device__ __forceinline__ void ws_tmem_st16(uint32_t taddr, const uint32_t (&w)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+               : "memory");
+}
+// Shared-memory descriptors as two 32-bit words.  The high word (8-row group
+// stride 1024 bytes, version 1, 128-byte swizzle) is the same for every
+// operand here; the low word is (address >> 4) | (leading byte offset >> 4)
+// << 16, so an operand that many bytes on is the low word plus (bytes >> 4)
+// (the address field never carries: operands end below 256 KB).
+constexpr uint32_t WS_DESC_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t ws_desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr >> 4) & 0x3FFFu) | ((lbo >> 4) << 16);
+}
+// The two MMA forms from 32-bit descriptor words; `acc` false only for the
+// first MMA of an accumulation.
+__device__ __forceinline__ void ws_mma_ss32(uint32_t d_tmem, uint32_t alo, uint32_t blo, uint32_t hi, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 a, b;\n setp.ne.b32 p, %5, 0;\n mov.b64 a, {%1, %3};\n mov.b64 b, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(alo), "r"(blo), "r"(hi), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void ws_mma_ts32(uint32_t d_tmem, uint32_t a_tmem, uint32_t blo, uint32_t hi, uint32_t idesc,
+                                            uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 b;\n setp.ne.b32 p, %5, 0;\n mov.b64 b, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(blo), "r"(hi), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ float ws_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// (x, y) -> bf16x2 hi = RN(x, y) and lo = RN of the remainders, x in the low
+// half (the same values as split_pair, two conversions per pair).
+__device__ __forceinline__ void ws_split2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// Key rows of a tile as 16-byte chunks: this thread's share (4 chunks of K
-// and 4 of V), zero past the tile's keys.  K chunk i of thread t is chunk
-// (t + 256 i) % 16 of key (t + 256 i) / 16 (a warp reads two whole key
-// rows); V chunk i is chunk ((t + 256 i) / 64) % 16 of key (t + 256 i) % 64
-// (a warp covers 32 consecutive keys of one 8-dim chunk, so that its
-// transposed 2-byte stores fall on distinct banks).  A prefix row in an
-// unallocated block reads as zero and is reported.
-struct TcChunks {
-  uint4 k[4], v[4];
+// Tile t of a CTA: prefix tiles of the split first, then (last split) the
+// tree's.  k0 = its first key (prefix position or tree slot), nk = its keys.
+struct WsTiles {
+  int lo, hi, n_pre, tree_keys, n;
+  bool draft;
+  __device__ __forceinline__ void at(int t, bool& tree, bool& f32, int& k0, int& nk) const {
+    tree = t >= n_pre;
+    f32 = draft && tree;
+    if (tree) {
+      const int kt = draft ? WS_FKEYS : WS_KEYS;
+      k0 = (t - n_pre) * kt;
+      nk = min(kt, tree_keys - k0);
+    } else {
+      k0 = lo + t * WS_KEYS;
+      nk = min(WS_KEYS, hi - k0);
+    }
+  }
 };
-// Global element offset of key kk of the tile, dims c8.., or -1 (no row).
-__device__ __forceinline__ long long tc_row_off(const AttnParams& p, int b, int h, bool tree, int k0, int kk,
-                                                int c8) {
-  if (tree) return ((static_cast<long long>(b) * p.tree_cap + k0 + kk) * p.Hkv + h) * TC_DH + c8;
-  long long row = static_cast<long long>(b) * p.kv_cap + k0 + kk;
-  if (p.paged.table) {
-    row = paged_row(p.paged, b, k0 + kk);
-    if (row < 0) {
-      if (c8 == 0) set_status(p.status, EAGLE_ERR_INVALID_ARG);
-      return -1;
-    }
+
+// Whether prefix tile [k0, k0 + 64) may come by TMA: the launch has tensor
+// maps, the tile is whole, and every block of a paged prefix it spans exists.
+__device__ __forceinline__ bool ws_tma_ok(const AttnParams& p, int b, int k0, int nk) {
+  if (!p.tma || nk != WS_KEYS) return false;
+  if (!p.paged.table) return true;
+  for (int r = 0; r < WS_KEYS; r += p.box_rows) {
+    const int blk = p.paged.table[static_cast<size_t>(b) * p.paged.per_req + ((k0 + r) >> p.paged.shift)];
+    if (blk < 0 || blk >= p.paged.n_blocks) return false;
   }
-  return (row * p.Hkv + h) * TC_DH + c8;
+  return true;
 }
-__device__ __forceinline__ void tc_load(const AttnParams& p, TcChunks& c, int b, int h, bool tree, int k0, int nk) {
-  const uint16_t* kb = tree ? p.kt_bf16 : p.kp;
-  const uint16_t* vb = tree ? p.vt_bf16 : p.vp;
+// Requests half `m` (0: K, 1: V) of prefix tile [k0, k0 + 64) of kv head h
+// into its place in stage `st` (one thread).
+__device__ __forceinline__ void ws_tma_half(const AttnParams& p, const CUtensorMap* map, uint8_t* st, uint64_t* bar,
+                                            int m, int b, int h, int k0) {
+  sm100::mbar_arrive_expect_tx(bar, WS_STAGE / 2);
+  for (int r = 0; r < WS_KEYS; r += p.box_rows) {
+    const int row = p.paged.table ? static_cast<int>(paged_row(p.paged, b, k0 + r)) : b * p.kv_cap + k0 + r;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = threadIdx.x + TC_THREADS * i;
-    c.k[i] = make_uint4(0u, 0u, 0u, 0u);
-    c.v[i] = c.k[i];
-    {
-      const int kk = idx >> 4, c8 = (idx & 15) * 8;
-      const long long off = kk < nk ? tc_row_off(p, b, h, tree, k0, kk, c8) : -1;
-      if (off >= 0) c.k[i] = __ldcg(reinterpret_cast<const uint4*>(kb + off));
-    }
-    {
-      const int kk = idx & 63, c8 = ((idx >> 6) & 15) * 8;
-      const long long off = kk < nk ? tc_row_off(p, b, h, tree, k0, kk, c8) : -1;
-      if (off >= 0) c.v[i] = __ldcg(reinterpret_cast<const uint4*>(vb + off));
-    }
+    for (int half = 0; half < 2; ++half)
+      sm100::tma_load_3d(st + m * 2 * WS_HALF + half * WS_HALF + r * 128, map, 64 * half, h, row, bar);
   }
 }
-__device__ __forceinline__ void tc_store(uint8_t* sm, const TcChunks& c, int buf) {
-  uint8_t* kt = sm + TC_K_OFF + buf * TC_BUF;
-  uint8_t* vt = sm + TC_VT_OFF + buf * TC_BUF;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int idx = threadIdx.x + TC_THREADS * i;
-    {
-      const int kk = idx >> 4, c8 = (idx & 15) * 8;
-      *reinterpret_cast<uint4*>(kt + sw128_off(kk, c8, 2)) = c.k[i];
+// Half m (0: K, 1: V) of a bf16 tile by 16-byte asynchronous copies (one
+// warp): prefix keys (through the block table when paged; a row of an
+// unallocated block is zero and reported) or verification-tree keys; rows
+// past nk are zero.  Returns once the copies have landed.
+__device__ __forceinline__ void ws_copy_half(const AttnParams& p, uint8_t* st, int m, int b, int h, bool tree, int k0,
+                                             int nk, int lane) {
+  const uint16_t* src_base = m == 0 ? (tree ? p.kt_bf16 : p.kp) : (tree ? p.vt_bf16 : p.vp);
+  uint8_t* dst = st + m * 2 * WS_HALF;
+  for (int idx = lane; idx < WS_KEYS * 16; idx += 32) {
+    const int key = idx >> 4, c = idx & 15;
+    const uint32_t off = (c >> 3) * WS_HALF + ws_sw(key, c & 7);
+    long long row = -1;
+    if (key < nk) {
+      if (tree) {
+        row = static_cast<long long>(b) * p.tree_cap + k0 + key;
+      } else if (p.paged.table) {
+        row = paged_row(p.paged, b, k0 + key);
+        if (row < 0 && c == 0 && m == 0) set_status(p.status, EAGLE_ERR_INVALID_ARG);
+      } else {
+        row = static_cast<long long>(b) * p.kv_cap + k0 + key;
+      }
     }
-    {
-      const int kk = idx & 63, c8 = ((idx >> 6) & 15) * 8;
-      const uint16_t* ve = reinterpret_cast<const uint16_t*>(&c.v[i]);
+    if (row >= 0)
+      cp_async16_cg(dst + off, src_base + (static_cast<size_t>(row) * p.Hkv + h) * WS_DH + 8 * c);
+    else
+      *reinterpret_cast<uint4*>(dst + off) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+}
+// Half m (0: K, 1: V) of a draft-tree tile (one warp): fp32 rows k0 .. k0 +
+// nk - 1 (nk <= 32) as bf16 hi then lo, each two 4 KB dim halves of 32 rows.
+__device__ __forceinline__ void ws_split_half(const AttnParams& p, uint8_t* st, int m, int b, int h, int k0, int nk,
+                                              int lane) {
+  constexpr int PER = WS_FKEYS * 16 / 32;    // 8-dim chunks per lane
+  constexpr int BATCH = 4;
+  static_assert(PER % BATCH == 0, "whole batches");
+  const float* src_base = m == 0 ? p.kt_f32 : p.vt_f32;
+  uint8_t* dst = st + m * 2 * WS_HALF;
+  for (int i0 = 0; i0 < PER; i0 += BATCH) {
+    float4 x[BATCH][2];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)          // V[key kk][dim c8 + j] -> Vt[dim c8 + j][key kk]
-        *reinterpret_cast<uint16_t*>(vt + sw128_off(c8 + j, kk & ~7, 1) + (kk & 7) * 2) = ve[j];
+    for (int i = 0; i < BATCH; ++i) {
+      const int idx = lane + 32 * (i0 + i);
+      const int key = idx >> 4, c = idx & 15;
+      x[i][0] = x[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (key < nk) {
+        const size_t src = ((static_cast<size_t>(b) * p.tree_cap + k0 + key) * p.Hkv + h) * WS_DH + 8 * c;
+        x[i][0] = __ldcg(reinterpret_cast<const float4*>(src_base + src));
+        x[i][1] = __ldcg(reinterpret_cast<const float4*>(src_base + src + 4));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i) {
+      const int idx = lane + 32 * (i0 + i);
+      const int key = idx >> 4, c = idx & 15;
+      const uint32_t off = (c >> 3) * WS_FHALF + ws_sw(key, c & 7);
+      const float4 a = x[i][0], z = x[i][1];
+      uint4 hi, lo;
+      ws_split2(a.x, a.y, hi.x, lo.x);
+      ws_split2(a.z, a.w, hi.y, lo.y);
+      ws_split2(z.x, z.y, hi.z, lo.z);
+      ws_split2(z.z, z.w, hi.w, lo.w);
+      *reinterpret_cast<uint4*>(dst + off) = hi;
+      *reinterpret_cast<uint4*>(dst + WS_HALF + off) = lo;
     }
   }
 }
 
-__global__ void __launch_bounds__(TC_THREADS, 1) tree_attn_tc_kernel(const AttnParams p) {
+// Waits (every lane of the warp) for the phase of `bar` with the given
+// parity; the result is the same in every lane.
+__device__ __forceinline__ bool ws_warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const bool ok = sm100::mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// The softmax of one tile (KT keys) for this thread's row and its
+// warpgroup's quarter g of the keys: see the kernel's description.  `full`:
+// every key visible (a whole prefix tile); otherwise key j is visible when
+// j < nk and bit j of mk is set.  The row maximum is the maximum of the four
+// warpgroups' partial maxima, exchanged through s_pmax [2][4][128] with one
+// barrier of the softmax warps; every softmax thread calls this once per
+// tile, `work` false after an abort (the barrier is still passed, nothing
+// else done).  Returns false when a wait gave up.
+template <int KT>
+__device__ __forceinline__ bool ws_softmax_tile(bool work, uint32_t tmem, uint32_t lane_base, int t, int g, int row,
+                                                bool full, uint64_t mk, int nk, float c, float& m_ref, float& l_part,
+                                                uint64_t* o_done, uint64_t* s_free, float* s_pmax,
+                                                volatile int* abort) {
+  constexpr int KPT = KT / WS_SOFT_WGS;      // this thread's keys: 16 of 64 or 8 of 32
+  const int buf = t & 1;
+  const int j0 = KPT * g;
+  float sv[KPT];
+  // With c > 0 the maximum is taken over the raw scores and the scale enters
+  // with the exponent (one FFMA per key); otherwise the scores are scaled
+  // first.  Invisible keys are -inf.
+  const bool pos = c > 0.f;
+  const float ec = pos ? c : 1.f;
+  float pm = -INFINITY;
+  if (work) {
+    if constexpr (KPT == 16) {
+      ws_tmem_ld16(tmem + WS_TM_S + 64u * buf + lane_base + j0, sv);
+    } else {
+      sm100::tmem_ld8(tmem + WS_TM_S + 64u * buf + lane_base + j0, sv);
+    }
+    sm100::tmem_wait_ld();
+    // this warp is done with S buffer t % 2: S(t + 2) may be issued into it
+    sm100::tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) sm100::mbar_arrive(&s_free[buf]);
+    if (!pos) {
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) sv[j] *= c;
+    }
+    if (!full) {
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) sv[j] = (j0 + j < nk && ((mk >> (j0 + j)) & 1ull)) ? sv[j] : -INFINITY;
+    }
+    float mx[4];                             // four independent chains
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mx[i] = sv[i];
+#pragma unroll
+    for (int j = 4; j < KPT; ++j) mx[j & 3] = fmaxf(mx[j & 3], sv[j]);
+    pm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+  }
+  s_pmax[(buf * WS_SOFT_WGS + g) * WS_ROWS + row] = pm;
+  sm100::named_barrier(WS_BAR_SOFT, WS_SOFT_THREADS);
+  if (!work) return true;
+  float mxr = s_pmax[(buf * WS_SOFT_WGS) * WS_ROWS + row];
+#pragma unroll
+  for (int q = 1; q < WS_SOFT_WGS; ++q) mxr = fmaxf(mxr, s_pmax[(buf * WS_SOFT_WGS + q) * WS_ROWS + row]);
+  const float mt = mxr * ec;                 // the tile's maximum, log2 units
+  const bool raise = mt > m_ref + WS_RESCALE * WS_LOG2E || (m_ref == -INFINITY && mt != -INFINITY);
+  const bool rescale = raise && m_ref != -INFINITY;
+  if (__any_sync(0xffffffffu, rescale)) {
+    // O of the warp's rows times 2^(m_old - m_new) once P V of tile t - 1
+    // (t >= 1: a finite reference comes from an earlier tile) is done with it;
+    // this warpgroup's quarter of the columns
+    if (!ws_warp_wait(&o_done[(t - 1) & 1], static_cast<uint32_t>(((t - 1) >> 1) & 1), abort)) return false;
+    sm100::tc_fence_after();
+    const float f = rescale ? ws_exp2(m_ref - mt) : 1.f;
+    float v32[32];
+    const uint32_t ta = tmem + WS_TM_O + lane_base + 32 * g;
+    ws_tmem_ld32(ta, v32);
+    sm100::tmem_wait_ld();
+    uint32_t w[16];
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(v32[16 * hlf + j] * f);
+      ws_tmem_st16(ta + 16 * hlf, w);
+    }
+    sm100::tmem_wait_st();
+    if (rescale) l_part *= f;
+  }
+  if (raise) m_ref = mt;
+  const float nm = m_ref == -INFINITY ? 0.f : -m_ref;   // (with m = -inf every key is -inf: P = 0)
+  float pe[KPT];
+  float part[2] = {0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    pe[j] = ws_exp2(fmaf(sv[j], ec, nm));
+    part[j & 1] += pe[j];
+  }
+  l_part += part[0] + part[1];
+  // the P buffer: P V of tile t - 2 is done with it
+  if (t >= 2 && !ws_warp_wait(&o_done[buf], static_cast<uint32_t>(((t - 2) >> 1) & 1), abort)) return false;
+  // keys j0 .. j0 + KPT - 1 are P columns j0 / 2 .. (two bf16 a column), hi then lo 32 columns on
+  const uint32_t pcol = tmem + WS_TM_P + 64u * buf + lane_base + j0 / 2;
+  if constexpr (KPT == 16) {
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ws_split2(pe[2 * i], pe[2 * i + 1], hw[i], lw[i]);
+    ws_tmem_st8(pcol, hw);
+    ws_tmem_st8(pcol + 32, lw);
+  } else {
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ws_split2(pe[2 * i], pe[2 * i + 1], hw[i], lw[i]);
+    ws_tmem_st4(pcol, hw);
+    ws_tmem_st4(pcol + 32, lw);
+  }
+  sm100::tmem_wait_st();
+  return true;
+}
+
+__global__ void __launch_bounds__(WS_THREADS, 1)
+    tree_attn_ws_kernel(const AttnParams p, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap) {
   const LaunchStamp ls(p.stamp);
-  extern __shared__ uint8_t smem_tc_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_tc_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t s_bar[4];          // S of buffer 0 / 1 complete, P V of buffer 0 / 1 complete
+  extern __shared__ uint8_t smem_ws_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_ws_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  // per stage and half (0: K, 1: V): loaded / released by its MMAs
+  __shared__ uint64_t s_full[2][WS_MAX_STAGES], s_empty[2][WS_MAX_STAGES];
+  __shared__ uint64_t s_s_full[2], s_s_free[2], s_p_full[2], s_o_done[2], s_mma_done;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_ok, s_last;
-  __shared__ uint64_t s_mask[TC_ROWS * MASKW];
-  __shared__ float s_lpart[2][TC_ROWS];    // each warpgroup's share of the row sums
+  __shared__ int s_abort, s_never, s_pre, s_last;
+  __shared__ uint64_t s_mask[WS_ROWS * MASKW];
+  __shared__ float s_lsum[WS_SOFT_WGS][WS_ROWS];
+  __shared__ float s_pmax[2 * WS_SOFT_WGS * WS_ROWS];
 
   const int split = blockIdx.x, rb = blockIdx.y, pair = blockIdx.z;
   const int b = pair / p.Hkv, h = pair % p.Hkv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, half = warp >> 2;
-  const int row = quarter * 32 + lane;                 // query row of the block = tensor-memory lane
-  const bool last_split = split == p.n_splits - 1;
-  int lo = 0, hi = 0;
+  const bool draft = p.mode == 0;
+  const int NST = p.stages;
+  const uint32_t q_bytes = draft ? 4 * WS_QHALF : 2 * WS_QHALF;
+  uint8_t* ring = sm + q_bytes;
+  volatile int* abort_flag = &s_abort;
+  volatile int* never = &s_never;
+
+  WsTiles T;
+  T.draft = draft;
   {
     const int L = prefix_rows(p, b, split == 0 && rb == 0 && tid == 0);
-    lo = split * p.chunk;
-    hi = min(L, lo + p.chunk);
+    T.lo = split * p.chunk;
+    T.hi = min(L, T.lo + p.chunk);
   }
-  const int n_pre = hi > lo ? (hi - lo + TC_KEYS - 1) / TC_KEYS : 0;
+  T.n_pre = T.hi > T.lo ? (T.hi - T.lo + WS_KEYS - 1) / WS_KEYS : 0;
   if (tid == 0) {
-    for (int k = 0; k < 4; ++k) sm100::mbar_init(&s_bar[k], 1);
+    for (int s = 0; s < NST; ++s) {
+      for (int m = 0; m < 2; ++m) {
+        sm100::mbar_init(&s_full[m][s], 1);
+        sm100::mbar_init(&s_empty[m][s], 1);
+      }
+    }
+    for (int i = 0; i < 2; ++i) {
+      sm100::mbar_init(&s_s_full[i], 1);
+      sm100::mbar_init(&s_s_free[i], 4 * WS_SOFT_WGS);   // one arrival per softmax warp
+      sm100::mbar_init(&s_p_full[i], 4 * WS_SOFT_WGS);
+      sm100::mbar_init(&s_o_done[i], 1);
+    }
+    sm100::mbar_init(&s_mma_done, 1);
+    s_abort = 0;
+    s_never = 0;
     sm100::fence_barrier_init();
+    // The prefix is this round's input, written by no kernel of the round:
+    // the split's first whole tiles are requested before the dependency wait.
+    int pre = 0;
+    for (; pre < min(NST, T.n_pre); ++pre) {
+      const int k0 = T.lo + pre * WS_KEYS;
+      if (!ws_tma_ok(p, b, k0, min(WS_KEYS, T.hi - k0))) break;
+      ws_tma_half(p, &kmap, ring + pre * WS_STAGE, &s_full[0][pre], 0, b, h, k0);
+      ws_tma_half(p, &vmap, ring + pre * WS_STAGE, &s_full[1][pre], 1, b, h, k0);
+    }
+    s_pre = pre;
   }
-  // The prefix is this round's input, written by no kernel of the round:
-  // the split's first tile is loaded before the dependency wait.
-  TcChunks next;
-  if (n_pre > 0) tc_load(p, next, b, h, false, lo, min(TC_KEYS, hi - lo));
   pdl_wait();                                // q rows, tree K/V, masks and the tree's size
   ls.waited();
   const int R = n_nodes(p, b) * p.G;
-  const int r0 = rb * TC_ROWS;
-  const int rows_here = max(0, min(TC_ROWS, R - r0));
-  const int tree_keys = last_split ? min(p.tree_size[b], p.tree_cap) : 0;
-  const int n_tree = (tree_keys + TC_KEYS - 1) / TC_KEYS;
-  const int n_tiles = rows_here > 0 ? n_pre + n_tree : 0;
-  if (n_pre == 0 && n_tiles > 0) tc_load(p, next, b, h, true, 0, min(TC_KEYS, tree_keys));
+  const int r0 = rb * WS_ROWS;
+  const int rows_here = max(0, min(WS_ROWS, R - r0));
+  const bool last_split = split == p.n_splits - 1;
+  T.tree_keys = !last_split ? 0
+                            : (draft ? min(p.e0 + p.rows_cap, p.tree_cap) : min(p.tree_size[b], p.tree_cap));
+  const int n_tree = (T.tree_keys + (draft ? WS_FKEYS : WS_KEYS) - 1) / (draft ? WS_FKEYS : WS_KEYS);
+  T.n = rows_here > 0 ? T.n_pre + n_tree : 0;
+  const int n_tiles = T.n;
+
   // Tensor memory only after the wait (every kernel this one waits for has
-  // finished), and dependents start only once every CTA holds its columns
-  // (the trigger follows the barrier after the allocation): no kernel that
-  // waits for this one can hold the columns it waits for.
-  if (warp == 0) {
-    sm100::tmem_alloc(&s_tmem, 256);
+  // finished), and dependents start only once every CTA holds its columns.
+  if (warp == WS_MMA_WARP) {
+    sm100::tmem_alloc(&s_tmem, WS_TM_COLS);
     sm100::tmem_relinquish();
   }
-  // the block's query rows (bf16), swizzled; rows past the block's zero
-  for (int idx = tid; idx < TC_ROWS * (TC_DH / 8); idx += TC_THREADS) {
-    const int rr = idx / (TC_DH / 8), c8 = (idx % (TC_DH / 8)) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (rr < rows_here) {
-      const int r = r0 + rr, node = r / p.G, hq = h * p.G + r % p.G;
-      v = *reinterpret_cast<const uint4*>(p.q_bf16 + q_index(p, b, node, hq) + c8);
+  if (warp >= WS_SOFT_WARP0 && n_tiles > 0) {
+    // the block's query rows (rows past the block's: zero), then the masks
+    const int st = tid - 32 * WS_SOFT_WARP0;
+    for (int idx = st; idx < WS_ROWS * 16; idx += WS_SOFT_THREADS) {
+      const int rr = idx >> 4, c = idx & 15;
+      const uint32_t off = (c >> 3) * WS_QHALF + ws_sw(rr, c & 7);
+      uint4 vh = make_uint4(0u, 0u, 0u, 0u), vl = vh;
+      if (rr < rows_here) {
+        const int r = r0 + rr, node = r / p.G, hq = h * p.G + r % p.G;
+        const size_t qo = q_index(p, b, node, hq) + 8 * c;
+        if (draft) {
+          const float4 a = *reinterpret_cast<const float4*>(p.q_f32 + qo);
+          const float4 z = *reinterpret_cast<const float4*>(p.q_f32 + qo + 4);
+          ws_split2(a.x, a.y, vh.x, vl.x);
+          ws_split2(a.z, a.w, vh.y, vl.y);
+          ws_split2(z.x, z.y, vh.z, vl.z);
+          ws_split2(z.z, z.w, vh.w, vl.w);
+        } else {
+          vh = *reinterpret_cast<const uint4*>(p.q_bf16 + qo);
+        }
+      }
+      *reinterpret_cast<uint4*>(sm + off) = vh;
+      if (draft) *reinterpret_cast<uint4*>(sm + 2 * WS_QHALF + off) = vl;
     }
-    *reinterpret_cast<uint4*>(sm + TC_Q_OFF + sw128_off(rr, c8, 2)) = v;
-  }
-  if (n_tree > 0 && tid < TC_ROWS) {
-    if (tid < rows_here) {
-      load_row_mask(p, s_mask + tid * MASKW, b, (r0 + tid) / p.G);
-    } else {
+    if (n_tree > 0 && st < WS_ROWS) {
+      if (st < rows_here) {
+        load_row_mask(p, s_mask + st * MASKW, b, (r0 + st) / p.G);
+      } else {
 #pragma unroll
-      for (int w = 0; w < MASKW; ++w) s_mask[tid * MASKW + w] = 0ull;
+        for (int w = 0; w < MASKW; ++w) s_mask[st * MASKW + w] = 0ull;
+      }
     }
+    sm100::fence_proxy_async_smem();         // generic-proxy stores -> tensor-core reads
   }
   sm100::tc_fence_before();
   __syncthreads();
   sm100::tc_fence_after();
   pdl_trigger();
   const uint32_t tmem = s_tmem;
-  const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-  const uint32_t t_o = tmem + 128;                       // S buffers: columns 0 and 64; O: 128-255
-  const uint32_t id_s = sm100::idesc_bf16_f32(TC_ROWS, TC_KEYS), id_o = sm100::idesc_bf16_f32(TC_ROWS, TC_DH);
   const uint32_t sbase = sm100::smem_u32(sm);
-  volatile int* abort_flag = &s_ok;
-  if (tid == 0) s_ok = 0;
-  // S(t) = Q K(t)^T into S buffer t % 2 (issued by thread 0)
-  auto issue_s = [&](int buf) {
+  const uint32_t rbase = sbase + q_bytes;
+
+  constexpr int OC = WS_DH / WS_SOFT_WGS;     // output columns per softmax thread
+  float o[OC];
 #pragma unroll
-    for (int kk = 0; kk < TC_DH / 16; ++kk) {
-      const uint32_t off = static_cast<uint32_t>(kk >> 2) * 1024u + static_cast<uint32_t>(kk & 3) * 32u;
-      sm100::mma_bf16(tmem + 64u * buf, sm100::smem_desc_sw128_sbo(sbase + TC_Q_OFF + off, 2048),
-                      sm100::smem_desc_sw128_sbo(sbase + TC_K_OFF + buf * TC_BUF + off, 2048), id_s,
-                      kk > 0 ? 1u : 0u);
-    }
-    sm100::mma_commit(&s_bar[buf]);
-  };
-  float m_ref = -INFINITY, l_run = 0.f;
-  bool alive = true;
-  if (n_tiles > 0) {
-    tc_store(sm, next, 0);
-    if (n_tiles > 1) {
-      const bool tn = 1 >= n_pre;
-      const int kn = tn ? (1 - n_pre) * TC_KEYS : lo + TC_KEYS;
-      tc_load(p, next, b, h, tn, kn, tn ? min(TC_KEYS, tree_keys - kn) : min(TC_KEYS, hi - kn));
-    }
-    sm100::fence_proxy_async_smem();       // generic-proxy stores -> tensor-core reads
-    __syncthreads();
-    if (tid == 0) {
-      sm100::tc_fence_after();
-      issue_s(0);
-    }
-  }
-  for (int t = 0; t < n_tiles; ++t) {
-    const int buf = t & 1;
-    const bool tree = t >= n_pre;
-    const int k0 = tree ? (t - n_pre) * TC_KEYS : lo + t * TC_KEYS;
-    const int nk = tree ? min(TC_KEYS, tree_keys - k0) : min(TC_KEYS, hi - k0);
-    // one wait: P V of tile t - 1 (its buffers and O) and S of tile t
-    if (tid == 0) {
+  for (int j = 0; j < OC; ++j) o[j] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;
+  const int sw = warp - WS_SOFT_WARP0;       // softmax warp
+  const int g = sw >> 2, quarter = warp & 3;
+  const int row = quarter * 32 + lane;
+
+  if (warp < WS_LOAD_WARPS) {
+    // ---- loaders: warp 0 the K halves, warp 1 the V halves, each a ring ahead ----
+    const int m = warp;
+    const CUtensorMap* map = m == 0 ? &kmap : &vmap;
+    int t = s_pre;
+    for (; t < n_tiles; ++t) {
+      const int s = t % NST;
       bool ok = true;
-      if (t >= 1) ok = sm100::mbar_wait(&s_bar[2 + ((t - 1) & 1)], static_cast<uint32_t>(((t - 1) >> 1) & 1), abort_flag);
-      if (ok) ok = sm100::mbar_wait(&s_bar[buf], static_cast<uint32_t>((t >> 1) & 1), abort_flag);
-      s_ok = ok ? 0 : 1;
-    }
-    __syncthreads();
-    if (s_ok) {
-      if (tid == 0) set_status(p.status, EAGLE_ERR_TIMEOUT);
-      alive = false;
-      break;
-    }
-    sm100::tc_fence_after();
-    if (t + 1 < n_tiles) {                 // tile t + 1 into the other buffers, tile t + 2 into registers
-      tc_store(sm, next, buf ^ 1);
-      if (t + 2 < n_tiles) {
-        const bool tn = t + 2 >= n_pre;
-        const int kn = tn ? (t + 2 - n_pre) * TC_KEYS : lo + (t + 2) * TC_KEYS;
-        tc_load(p, next, b, h, tn, kn, tn ? min(TC_KEYS, tree_keys - kn) : min(TC_KEYS, hi - kn));
+      if (lane == 0 && t >= NST)
+        ok = sm100::mbar_wait(&s_empty[m][s], static_cast<uint32_t>((t / NST - 1) & 1), abort_flag);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+        if (lane == 0) {
+          set_status(p.status, EAGLE_ERR_TIMEOUT);
+          s_abort = 1;
+        }
+        break;
+      }
+      bool tree, f32;
+      int k0, nk;
+      T.at(t, tree, f32, k0, nk);
+      if (!tree && ws_tma_ok(p, b, k0, nk)) {          // the same decision in every lane
+        if (lane == 0) ws_tma_half(p, map, ring + s * WS_STAGE, &s_full[m][s], m, b, h, k0);
+      } else {
+        if (f32) ws_split_half(p, ring + s * WS_STAGE, m, b, h, k0, nk, lane);
+        else ws_copy_half(p, ring + s * WS_STAGE, m, b, h, tree, k0, nk, lane);
+        sm100::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) sm100::mbar_arrive(&s_full[m][s]);
       }
     }
-    // softmax of this thread's row over the tile
-    float sv[TC_KEYS];
+    // no TMA copy may still be landing when the CTA leaves
+    const int issued = max(t, s_pre);
+    if (lane == 0)
+      for (int u = max(0, issued - NST); u < issued; ++u)
+        sm100::mbar_wait(&s_full[m][u % NST], static_cast<uint32_t>((u / NST) & 1), never);
+  } else if (warp == WS_MMA_WARP) {
+    // ---- MMA issuer ----
+    if (lane == 0 && n_tiles > 0) {
+      const uint32_t id_s64 = sm100::idesc_bf16_f32(WS_ROWS, WS_KEYS);
+      const uint32_t id_s32 = sm100::idesc_bf16_f32(WS_ROWS, WS_FKEYS);
+      const uint32_t id_pv = sm100::idesc_bf16_f32(WS_ROWS, WS_DH) | (1u << 16);   // B (V) MN-major
+      // S(t) = Q K(t)^T and O += P(t) V(t), each issued as one run of MMAs
+      // (alternating the two measured 2.4x slower).  The issuing loop is kept
+      // lean -- descriptors formed once per tile, every MMA's offset a
+      // constant -- since a dependent MMA chain issues at the rate this
+      // thread reaches it.
+      const uint32_t hi = WS_DESC_HI;
+      const uint32_t qlo = ws_desc_lo(sbase, 16);                 // Q hi, k-block 0
+      // stage base of tile t's K and V; stage and phase tracked incrementally
+      auto issue_s = [&](int t, int st) {
+        sm100::tc_fence_after();
+        const uint32_t stg = rbase + static_cast<uint32_t>(st) * WS_STAGE;
+        const uint32_t d = tmem + WS_TM_S + 64u * static_cast<uint32_t>(t & 1);
+        const uint32_t klo = ws_desc_lo(stg, 16);
+        if (!(draft && t >= T.n_pre)) {
 #pragma unroll
-    for (int c = 0; c < TC_KEYS / 8; ++c) {
-      float v8[8];
-      sm100::tmem_ld8(tmem + 64u * buf + lane_base + 8 * c, v8);
+          for (int kk = 0; kk < 8; ++kk)                 // Q hi against K
+            ws_mma_ss32(d, qlo + (((kk >> 2) * WS_QHALF + (kk & 3) * 32) >> 4),
+                        klo + (((kk >> 2) * WS_HALF + (kk & 3) * 32) >> 4), hi, id_s64, kk > 0 ? 1u : 0u);
+          if (draft) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sv[8 * c + j] = v8[j];
+            for (int kk = 0; kk < 8; ++kk)               // Q lo against K
+              ws_mma_ss32(d, qlo + ((2 * WS_QHALF + (kk >> 2) * WS_QHALF + (kk & 3) * 32) >> 4),
+                          klo + (((kk >> 2) * WS_HALF + (kk & 3) * 32) >> 4), hi, id_s64, 1u);
+          }
+        } else {
+#pragma unroll
+          for (int pr = 0; pr < 3; ++pr)                 // Qhi Khi, Qlo Khi, Qhi Klo
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              ws_mma_ss32(d, qlo + (((pr == 1 ? 2 * WS_QHALF : 0u) + (kk >> 2) * WS_QHALF + (kk & 3) * 32) >> 4),
+                          klo + (((pr == 2 ? WS_HALF : 0u) + (kk >> 2) * WS_FHALF + (kk & 3) * 32) >> 4), hi, id_s32,
+                          (pr | kk) != 0 ? 1u : 0u);
+        }
+        sm100::mma_commit(&s_s_full[t & 1]);
+        sm100::mma_commit(&s_empty[0][st]);
+      };
+      auto issue_pv = [&](int t, int st) {
+        const uint32_t stg = rbase + static_cast<uint32_t>(st) * WS_STAGE;
+        const uint32_t pt = tmem + WS_TM_P + 64u * static_cast<uint32_t>(t & 1);
+        const uint32_t od = tmem + WS_TM_O;
+        const uint32_t first = t > 0 ? 1u : 0u;
+        if (!(draft && t >= T.n_pre)) {
+          const uint32_t vlo = ws_desc_lo(stg + 2 * WS_HALF, WS_HALF);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)                    // P hi, then P lo, against V
+            ws_mma_ts32(od, pt + 32u * (i >> 2) + 8u * (i & 3), vlo + (((i & 3) * 2048) >> 4), hi, id_pv,
+                        i > 0 ? 1u : first);
+        } else {
+          const uint32_t vlo = ws_desc_lo(stg + 2 * WS_HALF, WS_FHALF);
+#pragma unroll
+          for (int i = 0; i < 6; ++i) {                  // Phi Vhi, Plo Vhi, Phi Vlo
+            const int pr = i >> 1, kk = i & 1;
+            ws_mma_ts32(od, pt + (pr == 1 ? 32u : 0u) + 8u * kk,
+                        vlo + (((pr == 2 ? WS_HALF : 0u) + kk * 2048) >> 4), hi, id_pv, i > 0 ? 1u : first);
+          }
+        }
+        sm100::mma_commit(&s_o_done[t & 1]);
+        sm100::mma_commit(&s_empty[1][st]);
+      };
+      auto advance = [&](int& st, uint32_t& ph) {
+        if (++st == NST) {
+          st = 0;
+          ph ^= 1u;
+        }
+      };
+      int ss = 0, sp = 0;                       // stages of the next S and the next P V
+      uint32_t ps = 0, pp = 0;                  // their fill phases
+      bool ok = sm100::mbar_wait(&s_full[0][ss], ps, abort_flag);
+      if (ok) {
+        issue_s(0, ss);
+        advance(ss, ps);
+      }
+      if (ok && n_tiles > 1) {
+        ok = sm100::mbar_wait(&s_full[0][ss], ps, abort_flag);
+        if (ok) {
+          issue_s(1, ss);
+          advance(ss, ps);
+        }
+      }
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        // S(t + 2) into S buffer t % 2 as soon as the softmax of tile t has
+        // read S(t) from it (it then runs while that softmax does), then
+        // O += P(t) V(t) once P(t) is written
+        if (t + 2 < n_tiles) {
+          ok = sm100::mbar_wait(&s_s_free[t & 1], static_cast<uint32_t>((t >> 1) & 1), abort_flag) &&
+               sm100::mbar_wait(&s_full[0][ss], ps, abort_flag);
+          if (!ok) break;
+          issue_s(t + 2, ss);
+          advance(ss, ps);
+        }
+        ok = sm100::mbar_wait(&s_p_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), abort_flag) &&
+             sm100::mbar_wait(&s_full[1][sp], pp, abort_flag);
+        if (!ok) break;
+        sm100::tc_fence_after();
+        issue_pv(t, sp);
+        advance(sp, pp);
+      }
+      if (!ok) {
+        set_status(p.status, EAGLE_ERR_TIMEOUT);
+        s_abort = 1;
+      }
+      // every MMA issued here has completed before the tensor memory goes
+      sm100::mma_commit(&s_mma_done);
+      sm100::mbar_wait(&s_mma_done, 0u, never);
     }
-    sm100::tmem_wait_ld();
-    const uint64_t mk = tree ? s_mask[row * MASKW + (k0 >> 6)] : ~0ull;   // a tree tile lies in one mask word
-    float mx = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < TC_KEYS; ++j) {
-      const bool ok = j < nk && ((mk >> j) & 1ull);
-      sv[j] = ok ? sv[j] * p.scale : -INFINITY;
-      mx = fmaxf(mx, sv[j]);
+  } else if (warp >= WS_SOFT_WARP0) {
+    // ---- softmax ----
+    // Every softmax warp takes part in every tile (rows past the block's
+    // have zero queries: finite, never written out) and passes the tile's
+    // barrier once, also after an abort.
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c = p.scale * WS_LOG2E;
+    float m_ref = -INFINITY, l_part = 0.f;
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      bool work = ok && !*abort_flag;
+      if (work) {
+        work = ws_warp_wait(&s_s_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), abort_flag);
+        ok = work;
+        sm100::tc_fence_after();
+      }
+      bool tree, f32;
+      int k0, nk;
+      T.at(t, tree, f32, k0, nk);
+      const bool full = !tree && nk == WS_KEYS;
+      const uint64_t mk = tree ? (s_mask[row * MASKW + (k0 >> 6)] >> (k0 & 63)) : ~0ull;
+      const bool done = f32 ? ws_softmax_tile<WS_FKEYS>(work, tmem, lane_base, t, g, row, full, mk, nk, c, m_ref,
+                                                        l_part, s_o_done, s_s_free, s_pmax, abort_flag)
+                            : ws_softmax_tile<WS_KEYS>(work, tmem, lane_base, t, g, row, full, mk, nk, c, m_ref,
+                                                       l_part, s_o_done, s_s_free, s_pmax, abort_flag);
+      if (work && !done) ok = false;
+      sm100::tc_fence_before();
+      __syncwarp();
+      if (work && ok && lane == 0) sm100::mbar_arrive(&s_p_full[t & 1]);
     }
-    // raise the reference maximum when the tile's exceeds it by the margin
-    // (O holds nothing yet while the reference is -inf)
-    const bool raise = mx > m_ref + TC_RESCALE || (m_ref == -INFINITY && mx != -INFINITY);
-    const bool rescale = raise && m_ref != -INFINITY;
-    const float factor = rescale ? __expf(m_ref - mx) : 1.f;
-    if (raise) {
-      l_run *= factor;                     // this warpgroup's share of the sum scales alike
-      m_ref = mx;
-    }
-    if (__any_sync(0xffffffffu, rescale)) {  // this warp's O rows times factor (1 where unchanged)
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float v8[8];
-        const uint32_t ta = t_o + lane_base + 64 * half + 8 * c;
-        sm100::tmem_ld8(ta, v8);
+    if (ok && n_tiles > 0) {
+      const int tl = n_tiles - 1;
+      ok = ws_warp_wait(&s_o_done[tl & 1], static_cast<uint32_t>((tl >> 1) & 1), abort_flag);
+      if (ok) {
+        sm100::tc_fence_after();
+        ws_tmem_ld32(tmem + WS_TM_O + lane_base + OC * g, o);
         sm100::tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v8[j] *= factor;
-        sm100::tmem_st8(ta, v8);
       }
-      sm100::tmem_wait_st();
     }
-    // this warpgroup's half of the keys: 32 half .. 32 half + 31 (its share
-    // of the row sum, and of P as hi and lo)
-    float pe[TC_KEYS / 2];
-    float sum = 0.f;
-#pragma unroll
-    for (int jj = 0; jj < TC_KEYS / 2; ++jj) {    // constant indices: sv stays in registers
-      const float x = half ? sv[32 + jj] : sv[jj];
-      pe[jj] = m_ref == -INFINITY ? 0.f : __expf(x - m_ref);
-      sum += pe[jj];
+    if (!ok) {
+      if (lane == 0) set_status(p.status, EAGLE_ERR_TIMEOUT);
+      s_abort = 1;
     }
-    l_run += sum;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) split_pair(pe[8 * c + 2 * q], pe[8 * c + 2 * q + 1], hw[q], lw[q]);
-      const uint32_t off = sw128_off(row, 32 * half + 8 * c, 1) + buf * TC_BUF;
-      *reinterpret_cast<uint4*>(sm + TC_PH_OFF + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      *reinterpret_cast<uint4*>(sm + TC_PL_OFF + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    }
-    sm100::fence_proxy_async_smem();
-    sm100::tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      sm100::tc_fence_after();
-      if (t + 1 < n_tiles) issue_s(buf ^ 1);
-      const uint32_t ph = sbase + TC_PH_OFF + buf * TC_BUF, pl = sbase + TC_PL_OFF + buf * TC_BUF;
-      const uint32_t vt = sbase + TC_VT_OFF + buf * TC_BUF;
-#pragma unroll
-      for (int kk = 0; kk < TC_KEYS / 16; ++kk)
-        sm100::mma_bf16(t_o, sm100::smem_desc_sw128_sbo(ph + kk * 32, 1024), sm100::smem_desc_sw128_sbo(vt + kk * 32, 1024),
-                        id_o, (t > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < TC_KEYS / 16; ++kk)
-        sm100::mma_bf16(t_o, sm100::smem_desc_sw128_sbo(pl + kk * 32, 1024), sm100::smem_desc_sw128_sbo(vt + kk * 32, 1024),
-                        id_o, 1u);
-      sm100::mma_commit(&s_bar[2 + buf]);
-    }
+    s_lsum[g][row] = l_part;
+    sm100::named_barrier(WS_BAR_SOFT, WS_SOFT_THREADS);
+    m_run = m_ref;
+    // the row sum, in the same order in every warpgroup
+    l_run = (s_lsum[0][row] + s_lsum[1][row]) + (s_lsum[2][row] + s_lsum[3][row]);
   }
-  // the last P V, then this thread's output columns from tensor memory
-  float o[64];
-#pragma unroll
-  for (int j = 0; j < 64; ++j) o[j] = 0.f;
-  if (alive && n_tiles > 0) {
-    if (tid == 0)
-      s_ok = sm100::mbar_wait(&s_bar[2 + ((n_tiles - 1) & 1)], static_cast<uint32_t>(((n_tiles - 1) >> 1) & 1),
-                              abort_flag) ? 0 : 1;
-    __syncthreads();
-    if (s_ok) {
-      if (tid == 0) set_status(p.status, EAGLE_ERR_TIMEOUT);
-      alive = false;
-    } else {
-      sm100::tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float v8[8];
-        sm100::tmem_ld8(t_o + lane_base + 64 * half + 8 * c, v8);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) o[8 * c + j] = v8[j];
-      }
-      sm100::tmem_wait_ld();
-    }
-  }
-  const float m_run = m_ref;
-  s_lpart[half][row] = l_run;
   sm100::tc_fence_before();
   __syncthreads();
-  l_run = s_lpart[0][row] + s_lpart[1][row];     // the row sum, in the same order in both warpgroups
-  if (warp == 0) {
+  if (warp == WS_MMA_WARP) {
     sm100::tc_fence_after();
-    sm100::tmem_dealloc(tmem, 256);
+    sm100::tmem_dealloc(tmem, WS_TM_COLS);
   }
-  if (!alive) return;
-  // this thread's output columns 64 half .. 64 half + 63 of its row
+  if (s_abort) return;
+
+  // this thread's output columns OC g .. OC g + OC - 1 of its row
+  // (a row with no key in this split keeps max -inf, sum 0, output 0)
+  const bool has_row = warp >= WS_SOFT_WARP0 && row < rows_here;
   const int r = r0 + row;
-  const bool has_row = row < rows_here;
   const int node = r / p.G, hq = h * p.G + r % p.G;
   const size_t qi = (static_cast<size_t>(b) * p.rows_cap + node) * p.Hq + hq;
   if (p.n_splits == 1) {
-    if (has_row) {
-      const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-      float* dst = p.out_f32 + qi * TC_DH + 64 * half;
+    if (!has_row) return;
+    const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
+    if (!draft) {
+      float* dst = p.out_f32 + qi * WS_DH + OC * g;
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        *reinterpret_cast<float4*>(dst + 4 * c) =
-            make_float4(o[4 * c] * inv, o[4 * c + 1] * inv, o[4 * c + 2] * inv, o[4 * c + 3] * inv);
+      for (int q = 0; q < OC / 4; ++q)
+        *reinterpret_cast<float4*>(dst + 4 * q) =
+            make_float4(o[4 * q] * inv, o[4 * q + 1] * inv, o[4 * q + 2] * inv, o[4 * q + 3] * inv);
+    } else {
+      const size_t j = static_cast<size_t>(b) * p.rows_cap + node;
+      uint16_t* dh = p.b_o + j * p.bo_ld + hq * WS_DH + OC * g;
+      uint16_t* dl = p.b_o + (static_cast<size_t>(p.NP) + j) * p.bo_ld + hq * WS_DH + OC * g;
+#pragma unroll
+      for (int q = 0; q < OC / 8; ++q) {
+        uint4 hi, lo;
+        ws_split2(o[8 * q] * inv, o[8 * q + 1] * inv, hi.x, lo.x);
+        ws_split2(o[8 * q + 2] * inv, o[8 * q + 3] * inv, hi.y, lo.y);
+        ws_split2(o[8 * q + 4] * inv, o[8 * q + 5] * inv, hi.z, lo.z);
+        ws_split2(o[8 * q + 6] * inv, o[8 * q + 7] * inv, hi.w, lo.w);
+        *reinterpret_cast<uint4*>(dh + 8 * q) = hi;
+        *reinterpret_cast<uint4*>(dl + 8 * q) = lo;
+      }
     }
     return;
   }
-  const int rec = TC_DH + 4;
+  // several splits: records [query row][split][dh + 4] (max in log2 units,
+  // sum, 2 unused, output), then the last CTA of the (request, kv head)
+  // merges every row in split order
+  const int rec = WS_DH + 4;
   const int ns = p.n_splits;
   if (has_row) {
     float* dst = p.part + (qi * ns + split) * rec;
-    if (half == 0) {
+    if (g == 0) {
       dst[0] = m_run;
       dst[1] = l_run;
     }
 #pragma unroll
-    for (int c = 0; c < 16; ++c)
-      *reinterpret_cast<float4*>(dst + 4 + 64 * half + 4 * c) = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+    for (int q = 0; q < OC / 4; ++q)
+      *reinterpret_cast<float4*>(dst + 4 + OC * g + 4 * q) = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
   }
-  // the last CTA of this (request, kv head) merges the splits of every row
   __syncthreads();                           // every thread's records come first
   if (tid == 0) {
     const int prev = arrive_acq_rel(&p.counters[pair]);
@@ -1475,25 +1850,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tree_attn_tc_kernel(const AttnP
   }
   __syncthreads();
   if (!s_last) return;
-  for (int rr = warp; rr < R; rr += TC_THREADS / 32) {
+  for (int rr = warp; rr < R; rr += WS_THREADS / 32) {
     const int nd = rr / p.G, hh = h * p.G + rr % p.G;
     const float* src = p.part + ((static_cast<size_t>(b) * p.rows_cap + nd) * p.Hq + hh) * ns * rec;
     const float ms = lane < ns ? __ldcg(src + lane * rec) : -INFINITY;
     const float lsv = lane < ns ? __ldcg(src + lane * rec + 1) : 0.f;
-    float vals[TC_MAX_SPLITS][4];
+    float vals[WS_MAX_RECS][4];
 #pragma unroll
-    for (int u = 0; u < TC_MAX_SPLITS; ++u)
+    for (int u = 0; u < WS_MAX_RECS; ++u)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) vals[u][c] = u < ns ? __ldcg(src + u * rec + 4 + lane + 32 * c) : 0.f;
+      for (int q = 0; q < 4; ++q) vals[u][q] = u < ns ? __ldcg(src + u * rec + 4 + lane + 32 * q) : 0.f;
     const float M = warp_max(ms);
-    const float wgt = ms == -INFINITY ? 0.f : __expf(ms - M);
+    const float wgt = ms == -INFINITY ? 0.f : ws_exp2(ms - M);
     const float Lsum = warp_sum(wgt * lsv);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int u = 0; u < TC_MAX_SPLITS; ++u) {
+    for (int u = 0; u < WS_MAX_RECS; ++u) {
       const float ws = __shfl_sync(0xffffffffu, wgt, u);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) acc[c] = fmaf(ws, vals[u][c], acc[c]);
+      for (int q = 0; q < 4; ++q) acc[q] = fmaf(ws, vals[u][q], acc[q]);
     }
     write_merged_row(p, b, nd, hh, acc, Lsum, lane);
   }
@@ -1555,27 +1930,59 @@ static cudaError_t launch_mma(const AttnParams& p, dim3 grid, size_t smem, cudaS
 // cores (10 against 15 us), most of a 16-row tile being padding.
 constexpr int kDraftMmaRows = 8;
 
-// Verification with more query rows per kv head than a four-warp pass takes
-// (dh 128): the tcgen05 kernel, with as many prefix splits (at most
-// TC_MAX_SPLITS, and never more records per row than the workspace and the
-// no-allocation scratch hold) as one wave of CTAs needs.
-static cudaError_t run_attn_tc(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
+// Query rows per (request, kv head) from which the draft layer's attention
+// (dh 128) runs on the tcgen05 kernel.
+constexpr int kDraftTcRows = 8;
+
+// A bf16 KV array [rows][Hkv][dh 128] as a 3-D tensor map {dh, kv head, row}
+// with boxes of 64 dims x 1 head x box_rows rows in the 128-byte swizzle.
+static bool encode_kv_map(eagle_ctx* ctx, CUtensorMap* map, const void* ptr, int Hkv, long long rows, int box_rows) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(WS_DH), static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(WS_DH) * 2, static_cast<cuuint64_t>(Hkv) * WS_DH * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tcgen05 kernel (dh 128): as many prefix splits (at most WS_MAX_RECS,
+// and never more records per row than the workspace and the no-allocation
+// scratch hold) as one wave of CTAs, one per SM, needs.  Whole prefix tiles
+// come by TMA when the caches allow it (16-byte aligned, a paged block of at
+// least 8 rows, rows addressable with 32-bit coordinates); otherwise every
+// tile is copied by the loader warps.
+static cudaError_t run_attn_ws(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
   const int rows = p.rows_cap * p.G;
-  const int row_blocks = ceil_div(rows, TC_ROWS);
+  const int row_blocks = ceil_div(rows, WS_ROWS);
   const int pairs = p.B * p.Hkv;
   const int tiles = ceil_div(p.kv_cap, TILE);
-  int want = ceil_div(ctx->sm_count, pairs * row_blocks);
-  want = std::min(want, std::min(TC_MAX_SPLITS, tiles));
+  int want = ctx->sm_count / (pairs * row_blocks);     // whole waves only
+  want = std::min(want, std::min(WS_MAX_RECS, tiles));
   want = std::min(want, attn_splits(ctx, pairs, p.kv_cap, kVerifyPerSm) + 1);
   want = std::max(want, 1);
   const int per = ceil_div(tiles, want);
   p.n_splits = ceil_div(tiles, per);         // every split non-empty at full length
   p.chunk = per * TILE;
+  p.stages = static_cast<int>((WS_BUDGET - (p.mode == 0 ? 4u : 2u) * WS_QHALF) / WS_STAGE);
+  const bool paged = p.paged.table != nullptr;
+  const int bs = paged ? (1 << p.paged.shift) : WS_KEYS;
+  const long long rows_total =
+      paged ? (static_cast<long long>(p.paged.n_blocks) << p.paged.shift) : static_cast<long long>(p.B) * p.kv_cap;
+  auto aligned16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  p.box_rows = std::min(WS_KEYS, bs);
+  p.tma = bs >= 8 && rows_total < (1ll << 31) && aligned16(p.kp) && aligned16(p.vp);
+  CUtensorMap km, vm;
+  std::memset(&km, 0, sizeof(km));
+  std::memset(&vm, 0, sizeof(vm));
+  if (p.tma && !(encode_kv_map(ctx, &km, p.kp, p.Hkv, rows_total, p.box_rows) &&
+                 encode_kv_map(ctx, &vm, p.vp, p.Hkv, rows_total, p.box_rows)))
+    p.tma = 0;
   dim3 grid(p.n_splits, row_blocks, pairs);
   p.stamp = stamp_slot(ctx, kernel_id);
   trace_before(ctx, kernel_id, st);
-  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(tree_attn_tc_kernel), static_cast<int>(TC_SMEM));
-  if (e == cudaSuccess) e = launch_pdl(tree_attn_tc_kernel, grid, dim3(TC_THREADS), TC_SMEM, st, p);
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(tree_attn_ws_kernel), static_cast<int>(WS_SMEM));
+  if (e == cudaSuccess) e = launch_pdl(tree_attn_ws_kernel, grid, dim3(WS_THREADS), WS_SMEM, st, p, km, vm);
   ctx->launches++;
   trace_after(ctx, kernel_id, st);
   return e;
@@ -1583,7 +1990,8 @@ static cudaError_t run_attn_tc(eagle_ctx* ctx, AttnParams& p, int kernel_id, cud
 
 static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
   if (p.dh % 16 != 0 || p.dh > MAX_DH) return cudaErrorInvalidValue;
-  if (p.mode == 1 && p.dh == TC_DH && p.rows_cap * p.G > ROWS_PASS) return run_attn_tc(ctx, p, kernel_id, st);
+  if (p.dh == WS_DH && ((p.mode == 1 && p.rows_cap * p.G > ROWS_PASS) || (p.mode == 0 && p.rows_cap * p.G >= kDraftTcRows)))
+    return run_attn_ws(ctx, p, kernel_id, st);
   const bool mma = p.mode == 1 || p.rows_cap * p.G >= kDraftMmaRows;
   const int tiles = ceil_div(p.kv_cap, TILE);
   const int rows = p.rows_cap * p.G;

@@ -37,6 +37,11 @@ W = S.variant("13b_x8_eagle2", name="paged_small", d=128, n_q_heads=4, n_kv_head
 # the commit cases run greedy: paging is independent of how tokens are drawn
 W_GREEDY = S.variant("13b_x8_eagle2", name="paged_small_greedy", d=128, n_q_heads=4, n_kv_heads=2, head_dim=64,
                      d_ff=344, vocab=1000, batch=4, prefix_range=(50, 400), weight_std=0.05, temps=(0.0,))
+# head_dim 128 with 164 query rows per kv head: the tensor-memory kernel,
+# whose whole prefix tiles come by TMA (per block when paged, from a block
+# size of 8) and the rest by copies
+W128 = S.variant("13b_x8_eagle2", name="paged_dh128", d=256, n_q_heads=8, n_kv_heads=2, head_dim=128, d_ff=512,
+                 vocab=1000, batch=3, prefix_range=(50, 700), top_k=4, depth=4, top_m=40, weight_std=0.05)
 INVALID_ARG, CAPACITY = 1, 4
 BF16_NAN = 0x7FC0
 
@@ -99,24 +104,25 @@ def _gather(pool, table, bs, cap):
     return out
 
 
-def _verify(eng, rd, prefix):
+def _verify(eng, rd, prefix, w=W):
     out = torch.full_like(rd.attn_out, float("nan"))
     B.eagle_tree_verify_attn(eng.ctx, rd.B, _p(rd.tree_q), _p(rd.tree_k[0]), _p(rd.tree_v[0]), prefix, rd.tree_c,
-                             1.0 / math.sqrt(W.head_dim), _p(out), eng.ws.data_ptr(), eng.stream())
+                             1.0 / math.sqrt(w.head_dim), _p(out), eng.ws.data_ptr(), eng.stream())
     return out
 
 
+@pytest.mark.parametrize("w", [W, W128], ids=["dh64", "dh128"])
 @pytest.mark.parametrize("bs", [1, 16, 64, 256])
-def test_paged_verify_equals_contiguous_and_oracle(bs):
+def test_paged_verify_equals_contiguous_and_oracle(bs, w):
     seed = 1201
-    eng, rd, wc, inp = _round(seed)
+    eng, rd, wc, inp = _round(seed, w=w)
     rd.draft_and_tree(wc)
     cap = -(-rd.kv_cap // bs) * bs
     kc, vc = _widen(rd.tgt_k[0], cap), _widen(rd.tgt_v[0], cap)
-    want = _verify(eng, rd, B.eagle_kv(_p(kc), _p(vc), cap, _p(rd.tgt_len)))
+    want = _verify(eng, rd, B.eagle_kv(_p(kc), _p(vc), cap, _p(rd.tgt_len)), w)
     kp, vp, table, nb = _paged(kc, vc, bs, seed + bs, lens=rd.tgt_len.tolist())
     paging = B.eagle_paging(_p(table), bs, nb)
-    got = _verify(eng, rd, B.eagle_kv(_p(kp), _p(vp), cap, _p(rd.tgt_len), paging))
+    got = _verify(eng, rd, B.eagle_kv(_p(kp), _p(vp), cap, _p(rd.tgt_len), paging), w)
     torch.cuda.synchronize()
     assert eng.status() == 0
     sizes = rd.t_size.tolist()
@@ -128,8 +134,8 @@ def test_paged_verify_equals_contiguous_and_oracle(bs):
         anc = mask_ints(rd.t_anc[b, :n])
         f = lambda t: t.double().cpu().numpy()
         ref = tree_attention(f(rd.tree_q[b, :n]), f(rd.tree_k[0][b, :n]), f(rd.tree_v[0][b, :n]),
-                             f(rd.tgt_k[0][b, :L]), f(rd.tgt_v[0][b, :L]), anc, 1.0 / math.sqrt(W.head_dim))
-        assert np.max(np.abs(f(got[b, :n]) - ref)) <= feature_tol(W), b
+                             f(rd.tgt_k[0][b, :L]), f(rd.tgt_v[0][b, :L]), anc, 1.0 / math.sqrt(w.head_dim))
+        assert np.max(np.abs(f(got[b, :n]) - ref)) <= feature_tol(w), b
     eng.close()
 
 
@@ -218,15 +224,16 @@ def test_paged_commit_refused_on_unallocated_block():
     eng.close()
 
 
-def test_unallocated_block_inside_prefix_is_reported():
+@pytest.mark.parametrize("w", [W, W128], ids=["dh64", "dh128"])
+def test_unallocated_block_inside_prefix_is_reported(w):
     seed, bs = 1501, 16
-    eng, rd, wc, inp = _round(seed)
+    eng, rd, wc, inp = _round(seed, w=w)
     rd.draft_and_tree(wc)
     cap = -(-rd.kv_cap // bs) * bs
     kc, vc = _widen(rd.tgt_k[0], cap), _widen(rd.tgt_v[0], cap)
     kp, vp, table, nb = _paged(kc, vc, bs, seed, lens=rd.tgt_len.tolist())
     table[2, 1] = -1                                 # request 2: positions 16..31 lost
-    got = _verify(eng, rd, B.eagle_kv(_p(kp), _p(vp), cap, _p(rd.tgt_len), B.eagle_paging(_p(table), bs, nb)))
+    got = _verify(eng, rd, B.eagle_kv(_p(kp), _p(vp), cap, _p(rd.tgt_len), B.eagle_paging(_p(table), bs, nb)), w)
     torch.cuda.synchronize()
     assert eng.status() == INVALID_ARG
     n = int(rd.t_size[2])

@@ -50,6 +50,18 @@ SMALL = {
     "small_tc_direct_dh128": S.variant("70b_x16_eagle2", name="small_tc_direct_dh128", d=512, n_q_heads=16,
                                        n_kv_heads=8, head_dim=128, d_ff=512, vocab=500, batch=20, prefix_len=100,
                                        top_k=3, depth=3, top_m=20, weight_std=0.05),
+    # the draft layer on the tensor-memory kernel (head_dim 128, 8 or more
+    # query rows per kv head): 80 rows per kv head (8 query heads of one kv
+    # head, k = 10) over a 700-key prefix with a 60-key partial tile, 248
+    # verification rows in two row blocks; and 10 rows per kv head (MHA,
+    # k = 10, depth 6: a 51-slot draft tree in two 32-key tiles) over ragged
+    # prefixes split one 64-key tile per CTA, 61 verification rows
+    "small_ws_g8_k10_dh128": S.variant("70b_x16_eagle2", name="small_ws_g8_k10_dh128", d=256, n_q_heads=8,
+                                       n_kv_heads=1, head_dim=128, d_ff=512, vocab=1000, batch=2, prefix_len=700,
+                                       top_k=10, depth=4, top_m=30, weight_std=0.05),
+    "small_ws_mha_k10_dh128": S.variant("13b_x8_eagle2", name="small_ws_mha_k10_dh128", d=256, n_q_heads=2,
+                                        n_kv_heads=2, head_dim=128, d_ff=512, vocab=1500, batch=3,
+                                        prefix_range=(50, 900), top_k=10, depth=6, top_m=60, weight_std=0.05),
 }
 
 

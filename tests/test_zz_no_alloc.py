@@ -23,6 +23,11 @@ CASES = {
                                   top_k=4, depth=4, top_m=12, weight_std=0.05),
     # the bench's shape: 32 heads of 128, prefix 1024, static 26-node tree
     "7b_static26": S.WORKLOADS["7b_static26"],
+    # head_dim 128 with 164 query rows per kv head (the tensor-memory kernel),
+    # ragged prefixes over several splits
+    "tc_gqa_dh128": S.variant("13b_x8_eagle2", name="noalloc_tc_gqa_dh128", d=256, n_q_heads=8, n_kv_heads=2,
+                              head_dim=128, d_ff=512, vocab=1000, batch=3, prefix_range=(50, 700), top_k=4,
+                              depth=4, top_m=40, weight_std=0.05),
 }
 
 # Same kernel, same split count, same merge order: the two entry points are
