@@ -1098,8 +1098,11 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1) tree_attn_mma_kernel
 //               by 16-byte asynchronous copies with the missing rows zeroed;
 //               the draft tree's fp32 keys and values as bf16 hi + lo pairs,
 //               32 keys a tile.
-//   warp 2      MMA issuer (one thread): S = Q K^T into one of two S buffers
-//               in tensor memory, O += P V with P read from tensor memory.
+//   warps 2-3   MMA issuers, one thread each (warp 2 for the even tiles,
+//               warp 3 for the odd ones -- one issuer measured starved of
+//               issue slots by the busy softmax warps): S = Q K^T into the
+//               group's S buffer in tensor memory, O += P V with P read from
+//               tensor memory.
 //   warps 4-19  softmax, four warpgroups: thread = query row = its tensor-
 //               memory lane (warp % 4 selects the 32-lane quarter), and
 //               warpgroup g takes quarter g of each tile's keys: its partial
@@ -1128,9 +1131,11 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1) tree_attn_mma_kernel
 // dims x 64 keys -- K being the K-major B operand of Q K^T and V the MN-major
 // B operand of P V; a draft-tree stage as K hi, K lo, V hi, V lo of 32 keys.
 constexpr int WS_LOAD_WARPS = 2;
-constexpr int WS_MMA_WARP = 2;                      // (warp 3 has no role)
+constexpr int WS_MMA_WARP = 2;                      // and 3
 constexpr int WS_SOFT_WARP0 = 4;
-constexpr int WS_SOFT_WGS = 4;                      // softmax warpgroups: a quarter of each tile's keys each
+constexpr int WS_SOFT_WGS = 4;                      // softmax warpgroups
+constexpr int WS_GROUP_WGS = 2;                     // ... in two groups of two, a group for every other tile
+constexpr int WS_GROUP_THREADS = 128 * WS_GROUP_WGS;
 constexpr int WS_THREADS = 32 * (WS_SOFT_WARP0 + 4 * WS_SOFT_WGS);
 constexpr int WS_SOFT_THREADS = 128 * WS_SOFT_WGS;
 constexpr int WS_ROWS = 128;
@@ -1147,11 +1152,13 @@ constexpr size_t WS_SMEM = WS_BUDGET + 1024;        // + room to align the base 
 constexpr float WS_RESCALE = 8.0f;
 constexpr float WS_LOG2E = 1.4426950408889634f;
 constexpr int WS_MAX_RECS = 16;                     // prefix splits of a (request, kv head) at most
-constexpr uint32_t WS_TM_S = 0;                     // S buffers: columns 0 and 64
-constexpr uint32_t WS_TM_O = 128;                   // O: columns 128-255
-constexpr uint32_t WS_TM_P = 256;                   // P buffers: 256 and 320 (hi, then lo 32 columns on)
+constexpr uint32_t WS_TM_S = 0;                     // S of group 0 / 1: columns 0 / 64
+constexpr uint32_t WS_TM_O = 128;                   // O of group 0 / 1: columns 128-255 / 384-511
+constexpr uint32_t WS_TM_O_STEP = 256;
+constexpr uint32_t WS_TM_P = 256;                   // P of group 0 / 1: 256 / 320 (hi, then lo 32 columns on)
 constexpr uint32_t WS_TM_COLS = 512;
-constexpr int WS_BAR_SOFT = 2;                      // named barrier of the softmax warps
+constexpr int WS_BAR_SOFT = 1;                      // named barriers: all softmax warps, then one per group
+constexpr int WS_BAR_GROUP = 2;
 
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a swizzled
 // block of 128-byte rows.
@@ -1351,22 +1358,23 @@ __device__ __forceinline__ bool ws_warp_wait(uint64_t* bar, uint32_t parity, vol
   return __all_sync(0xffffffffu, ok);
 }
 
-// The softmax of one tile (KT keys) for this thread's row and its
-// warpgroup's quarter g of the keys: see the kernel's description.  `full`:
-// every key visible (a whole prefix tile); otherwise key j is visible when
-// j < nk and bit j of mk is set.  The row maximum is the maximum of the four
-// warpgroups' partial maxima, exchanged through s_pmax [2][4][128] with one
-// barrier of the softmax warps; every softmax thread calls this once per
-// tile, `work` false after an abort (the barrier is still passed, nothing
-// else done).  Returns false when a wait gave up.
+// The softmax of one tile t (KT keys) of group G = t % 2 for this thread's
+// row and its warpgroup's half w of the keys: see the kernel's description.
+// `full`: every key visible (a whole prefix tile); otherwise key j is
+// visible when j < nk and bit j of mk is set.  The row maximum is the larger
+// of the group's two warpgroups' partial maxima, exchanged through s_pmax
+// [group][2][2][128] with one barrier of the group's warps; every thread of
+// the group calls this once per tile of the group, `work` false after an
+// abort (the barrier is still passed, nothing else done).  Returns false
+// when a wait gave up.
 template <int KT>
-__device__ __forceinline__ bool ws_softmax_tile(bool work, uint32_t tmem, uint32_t lane_base, int t, int g, int row,
+__device__ __forceinline__ bool ws_softmax_tile(bool work, uint32_t tmem, uint32_t lane_base, int t, int w, int row,
                                                 bool full, uint64_t mk, int nk, float c, float& m_ref, float& l_part,
                                                 uint64_t* o_done, uint64_t* s_free, float* s_pmax,
                                                 volatile int* abort) {
-  constexpr int KPT = KT / WS_SOFT_WGS;      // this thread's keys: 16 of 64 or 8 of 32
-  const int buf = t & 1;
-  const int j0 = KPT * g;
+  constexpr int KPT = KT / WS_GROUP_WGS;     // this thread's keys: 32 of 64 or 16 of 32
+  const int G = t & 1, u = t >> 1;           // the group and its own tile count
+  const int j0 = KPT * w;
   float sv[KPT];
   // With c > 0 the maximum is taken over the raw scores and the scale enters
   // with the exponent (one FFMA per key); otherwise the scores are scaled
@@ -1375,16 +1383,16 @@ __device__ __forceinline__ bool ws_softmax_tile(bool work, uint32_t tmem, uint32
   const float ec = pos ? c : 1.f;
   float pm = -INFINITY;
   if (work) {
-    if constexpr (KPT == 16) {
-      ws_tmem_ld16(tmem + WS_TM_S + 64u * buf + lane_base + j0, sv);
+    if constexpr (KPT == 32) {
+      ws_tmem_ld32(tmem + WS_TM_S + 64u * G + lane_base + j0, sv);
     } else {
-      sm100::tmem_ld8(tmem + WS_TM_S + 64u * buf + lane_base + j0, sv);
+      ws_tmem_ld16(tmem + WS_TM_S + 64u * G + lane_base + j0, sv);
     }
     sm100::tmem_wait_ld();
-    // this warp is done with S buffer t % 2: S(t + 2) may be issued into it
+    // this warp is done with S buffer G: S(t + 2) may be issued into it
     sm100::tc_fence_before();
     __syncwarp();
-    if ((threadIdx.x & 31) == 0) sm100::mbar_arrive(&s_free[buf]);
+    if ((threadIdx.x & 31) == 0) sm100::mbar_arrive(&s_free[G]);
     if (!pos) {
 #pragma unroll
       for (int j = 0; j < KPT; ++j) sv[j] *= c;
@@ -1400,62 +1408,55 @@ __device__ __forceinline__ bool ws_softmax_tile(bool work, uint32_t tmem, uint32
     for (int j = 4; j < KPT; ++j) mx[j & 3] = fmaxf(mx[j & 3], sv[j]);
     pm = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
   }
-  s_pmax[(buf * WS_SOFT_WGS + g) * WS_ROWS + row] = pm;
-  sm100::named_barrier(WS_BAR_SOFT, WS_SOFT_THREADS);
+  float* pmx = s_pmax + ((G * 2 + (u & 1)) * WS_GROUP_WGS) * WS_ROWS;
+  pmx[w * WS_ROWS + row] = pm;
+  if (G) sm100::named_barrier(WS_BAR_GROUP + 1, WS_GROUP_THREADS);
+  else sm100::named_barrier(WS_BAR_GROUP, WS_GROUP_THREADS);
   if (!work) return true;
-  float mxr = s_pmax[(buf * WS_SOFT_WGS) * WS_ROWS + row];
-#pragma unroll
-  for (int q = 1; q < WS_SOFT_WGS; ++q) mxr = fmaxf(mxr, s_pmax[(buf * WS_SOFT_WGS + q) * WS_ROWS + row]);
-  const float mt = mxr * ec;                 // the tile's maximum, log2 units
+  const float mt = fmaxf(pmx[row], pmx[WS_ROWS + row]) * ec;   // the tile's maximum, log2 units
   const bool raise = mt > m_ref + WS_RESCALE * WS_LOG2E || (m_ref == -INFINITY && mt != -INFINITY);
   const bool rescale = raise && m_ref != -INFINITY;
+  // P V of the group's previous tile t - 2 is done with O_G and with P buffer G
+  if (t >= 2 && !ws_warp_wait(&o_done[G], static_cast<uint32_t>((u - 1) & 1), abort)) return false;
   if (__any_sync(0xffffffffu, rescale)) {
-    // O of the warp's rows times 2^(m_old - m_new) once P V of tile t - 1
-    // (t >= 1: a finite reference comes from an earlier tile) is done with it;
-    // this warpgroup's quarter of the columns
-    if (!ws_warp_wait(&o_done[(t - 1) & 1], static_cast<uint32_t>(((t - 1) >> 1) & 1), abort)) return false;
+    // O_G of the warp's rows times 2^(m_old - m_new) (a finite reference
+    // comes from an earlier tile of the group); this warpgroup's half of the columns
     sm100::tc_fence_after();
     const float f = rescale ? ws_exp2(m_ref - mt) : 1.f;
-    float v32[32];
-    const uint32_t ta = tmem + WS_TM_O + lane_base + 32 * g;
-    ws_tmem_ld32(ta, v32);
-    sm100::tmem_wait_ld();
-    uint32_t w[16];
 #pragma unroll
-    for (int hlf = 0; hlf < 2; ++hlf) {
+    for (int q = 0; q < 4; ++q) {
+      float v16[16];
+      const uint32_t ta = tmem + WS_TM_O + WS_TM_O_STEP * G + lane_base + 64 * w + 16 * q;
+      ws_tmem_ld16(ta, v16);
+      sm100::tmem_wait_ld();
+      uint32_t x[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(v32[16 * hlf + j] * f);
-      ws_tmem_st16(ta + 16 * hlf, w);
+      for (int j = 0; j < 16; ++j) x[j] = __float_as_uint(v16[j] * f);
+      ws_tmem_st16(ta, x);
     }
     sm100::tmem_wait_st();
     if (rescale) l_part *= f;
   }
   if (raise) m_ref = mt;
   const float nm = m_ref == -INFINITY ? 0.f : -m_ref;   // (with m = -inf every key is -inf: P = 0)
-  float pe[KPT];
   float part[2] = {0.f, 0.f};
+  // keys j0 .. j0 + KPT - 1 are P columns j0 / 2 .. (two bf16 a column), hi then lo 32 columns on
+  const uint32_t pcol = tmem + WS_TM_P + 64u * G + lane_base + j0 / 2;
+  uint32_t hw[KPT / 2], lw[KPT / 2];
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    pe[j] = ws_exp2(fmaf(sv[j], ec, nm));
-    part[j & 1] += pe[j];
+  for (int i = 0; i < KPT / 2; ++i) {
+    const float e0 = ws_exp2(fmaf(sv[2 * i], ec, nm)), e1 = ws_exp2(fmaf(sv[2 * i + 1], ec, nm));
+    part[0] += e0;
+    part[1] += e1;
+    ws_split2(e0, e1, hw[i], lw[i]);
   }
   l_part += part[0] + part[1];
-  // the P buffer: P V of tile t - 2 is done with it
-  if (t >= 2 && !ws_warp_wait(&o_done[buf], static_cast<uint32_t>(((t - 2) >> 1) & 1), abort)) return false;
-  // keys j0 .. j0 + KPT - 1 are P columns j0 / 2 .. (two bf16 a column), hi then lo 32 columns on
-  const uint32_t pcol = tmem + WS_TM_P + 64u * buf + lane_base + j0 / 2;
-  if constexpr (KPT == 16) {
-    uint32_t hw[8], lw[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ws_split2(pe[2 * i], pe[2 * i + 1], hw[i], lw[i]);
+  if constexpr (KPT == 32) {
+    ws_tmem_st16(pcol, hw);
+    ws_tmem_st16(pcol + 32, lw);
+  } else {
     ws_tmem_st8(pcol, hw);
     ws_tmem_st8(pcol + 32, lw);
-  } else {
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) ws_split2(pe[2 * i], pe[2 * i + 1], hw[i], lw[i]);
-    ws_tmem_st4(pcol, hw);
-    ws_tmem_st4(pcol + 32, lw);
   }
   sm100::tmem_wait_st();
   return true;
@@ -1470,12 +1471,12 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
                                            ~static_cast<uintptr_t>(1023));
   // per stage and half (0: K, 1: V): loaded / released by its MMAs
   __shared__ uint64_t s_full[2][WS_MAX_STAGES], s_empty[2][WS_MAX_STAGES];
-  __shared__ uint64_t s_s_full[2], s_s_free[2], s_p_full[2], s_o_done[2], s_mma_done;
+  __shared__ uint64_t s_s_full[2], s_s_free[2], s_p_full[2], s_o_done[2], s_mma_done[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort, s_never, s_pre, s_last;
   __shared__ uint64_t s_mask[WS_ROWS * MASKW];
-  __shared__ float s_lsum[WS_SOFT_WGS][WS_ROWS];
-  __shared__ float s_pmax[2 * WS_SOFT_WGS * WS_ROWS];
+  __shared__ float s_m[2][WS_ROWS], s_l[2][WS_GROUP_WGS][WS_ROWS];
+  __shared__ float s_pmax[2 * 2 * WS_GROUP_WGS * WS_ROWS];
 
   const int split = blockIdx.x, rb = blockIdx.y, pair = blockIdx.z;
   const int b = pair / p.Hkv, h = pair % p.Hkv;
@@ -1504,11 +1505,12 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       sm100::mbar_init(&s_s_full[i], 1);
-      sm100::mbar_init(&s_s_free[i], 4 * WS_SOFT_WGS);   // one arrival per softmax warp
-      sm100::mbar_init(&s_p_full[i], 4 * WS_SOFT_WGS);
+      sm100::mbar_init(&s_s_free[i], 4 * WS_GROUP_WGS);   // one arrival per warp of group i
+      sm100::mbar_init(&s_p_full[i], 4 * WS_GROUP_WGS);
       sm100::mbar_init(&s_o_done[i], 1);
     }
-    sm100::mbar_init(&s_mma_done, 1);
+    sm100::mbar_init(&s_mma_done[0], 1);
+    sm100::mbar_init(&s_mma_done[1], 1);
     s_abort = 0;
     s_never = 0;
     sm100::fence_barrier_init();
@@ -1589,7 +1591,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   for (int j = 0; j < OC; ++j) o[j] = 0.f;
   float m_run = -INFINITY, l_run = 0.f;
   const int sw = warp - WS_SOFT_WARP0;       // softmax warp
-  const int g = sw >> 2, quarter = warp & 3;
+  const int grp = sw >> 3, w = (sw >> 2) & 1, quarter = warp & 3;
+  const int c0 = OC * (2 * w + grp);          // this thread's output columns
   const int row = quarter * 32 + lane;
 
   if (warp < WS_LOAD_WARPS) {
@@ -1627,9 +1630,11 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     if (lane == 0)
       for (int u = max(0, issued - NST); u < issued; ++u)
         sm100::mbar_wait(&s_full[m][u % NST], static_cast<uint32_t>((u / NST) & 1), never);
-  } else if (warp == WS_MMA_WARP) {
-    // ---- MMA issuer ----
-    if (lane == 0 && n_tiles > 0) {
+  } else if (warp == WS_MMA_WARP || warp == WS_MMA_WARP + 1) {
+    // ---- MMA issuers: lane 0 of warp 2 for the even tiles (softmax group 0),
+    // of warp 3 for the odd ones (group 1) ----
+    const int G = warp - WS_MMA_WARP;
+    if (lane == 0 && n_tiles > G) {
       const uint32_t id_s64 = sm100::idesc_bf16_f32(WS_ROWS, WS_KEYS);
       const uint32_t id_s32 = sm100::idesc_bf16_f32(WS_ROWS, WS_FKEYS);
       const uint32_t id_pv = sm100::idesc_bf16_f32(WS_ROWS, WS_DH) | (1u << 16);   // B (V) MN-major
@@ -1672,8 +1677,8 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       auto issue_pv = [&](int t, int st) {
         const uint32_t stg = rbase + static_cast<uint32_t>(st) * WS_STAGE;
         const uint32_t pt = tmem + WS_TM_P + 64u * static_cast<uint32_t>(t & 1);
-        const uint32_t od = tmem + WS_TM_O;
-        const uint32_t first = t > 0 ? 1u : 0u;
+        const uint32_t od = tmem + WS_TM_O + WS_TM_O_STEP * static_cast<uint32_t>(t & 1);
+        const uint32_t first = t >= 2 ? 1u : 0u;            // the first tile of each group starts its O
         if (!(draft && t >= T.n_pre)) {
           const uint32_t vlo = ws_desc_lo(stg + 2 * WS_HALF, WS_HALF);
 #pragma unroll
@@ -1692,65 +1697,50 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
         sm100::mma_commit(&s_o_done[t & 1]);
         sm100::mma_commit(&s_empty[1][st]);
       };
-      auto advance = [&](int& st, uint32_t& ph) {
-        if (++st == NST) {
-          st = 0;
-          ph ^= 1u;
-        }
-      };
-      int ss = 0, sp = 0;                       // stages of the next S and the next P V
-      uint32_t ps = 0, pp = 0;                  // their fill phases
-      bool ok = sm100::mbar_wait(&s_full[0][ss], ps, abort_flag);
-      if (ok) {
-        issue_s(0, ss);
-        advance(ss, ps);
-      }
-      if (ok && n_tiles > 1) {
-        ok = sm100::mbar_wait(&s_full[0][ss], ps, abort_flag);
-        if (ok) {
-          issue_s(1, ss);
-          advance(ss, ps);
-        }
-      }
-      for (int t = 0; ok && t < n_tiles; ++t) {
-        // S(t + 2) into S buffer t % 2 as soon as the softmax of tile t has
-        // read S(t) from it (it then runs while that softmax does), then
-        // O += P(t) V(t) once P(t) is written
+      // stage and fill phase of tile t
+      auto stage_of = [&](int t) { return t % NST; };
+      auto phase_of = [&](int t) { return static_cast<uint32_t>((t / NST) & 1); };
+      bool ok = sm100::mbar_wait(&s_full[0][stage_of(G)], phase_of(G), abort_flag);
+      if (ok) issue_s(G, stage_of(G));
+      for (int t = G; ok && t < n_tiles; t += 2) {
+        // S(t + 2) into this group's S buffer as soon as the group's softmax
+        // of tile t has read S(t) from it (it then runs while that softmax
+        // does), then O += P(t) V(t) once P(t) is written
         if (t + 2 < n_tiles) {
-          ok = sm100::mbar_wait(&s_s_free[t & 1], static_cast<uint32_t>((t >> 1) & 1), abort_flag) &&
-               sm100::mbar_wait(&s_full[0][ss], ps, abort_flag);
+          const int st = stage_of(t + 2);
+          ok = sm100::mbar_wait(&s_s_free[G], static_cast<uint32_t>((t >> 1) & 1), abort_flag) &&
+               sm100::mbar_wait(&s_full[0][st], phase_of(t + 2), abort_flag);
           if (!ok) break;
-          issue_s(t + 2, ss);
-          advance(ss, ps);
+          issue_s(t + 2, st);
         }
-        ok = sm100::mbar_wait(&s_p_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), abort_flag) &&
-             sm100::mbar_wait(&s_full[1][sp], pp, abort_flag);
+        const int sv = stage_of(t);
+        ok = sm100::mbar_wait(&s_p_full[G], static_cast<uint32_t>((t >> 1) & 1), abort_flag) &&
+             sm100::mbar_wait(&s_full[1][sv], phase_of(t), abort_flag);
         if (!ok) break;
         sm100::tc_fence_after();
-        issue_pv(t, sp);
-        advance(sp, pp);
+        issue_pv(t, sv);
       }
       if (!ok) {
         set_status(p.status, EAGLE_ERR_TIMEOUT);
         s_abort = 1;
       }
       // every MMA issued here has completed before the tensor memory goes
-      sm100::mma_commit(&s_mma_done);
-      sm100::mbar_wait(&s_mma_done, 0u, never);
+      sm100::mma_commit(&s_mma_done[G]);
+      sm100::mbar_wait(&s_mma_done[G], 0u, never);
     }
   } else if (warp >= WS_SOFT_WARP0) {
-    // ---- softmax ----
-    // Every softmax warp takes part in every tile (rows past the block's
-    // have zero queries: finite, never written out) and passes the tile's
-    // barrier once, also after an abort.
+    // ---- softmax: group grp takes the tiles t = grp (mod 2) ----
+    // Every warp of the group takes part in each of the group's tiles (rows
+    // past the block's have zero queries: finite, never written out) and
+    // passes the tile's barrier once, also after an abort.
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = p.scale * WS_LOG2E;
     float m_ref = -INFINITY, l_part = 0.f;
     bool ok = true;
-    for (int t = 0; t < n_tiles; ++t) {
+    for (int t = grp; t < n_tiles; t += 2) {
       bool work = ok && !*abort_flag;
       if (work) {
-        work = ws_warp_wait(&s_s_full[t & 1], static_cast<uint32_t>((t >> 1) & 1), abort_flag);
+        work = ws_warp_wait(&s_s_full[grp], static_cast<uint32_t>((t >> 1) & 1), abort_flag);
         ok = work;
         sm100::tc_fence_after();
       }
@@ -1759,33 +1749,50 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       T.at(t, tree, f32, k0, nk);
       const bool full = !tree && nk == WS_KEYS;
       const uint64_t mk = tree ? (s_mask[row * MASKW + (k0 >> 6)] >> (k0 & 63)) : ~0ull;
-      const bool done = f32 ? ws_softmax_tile<WS_FKEYS>(work, tmem, lane_base, t, g, row, full, mk, nk, c, m_ref,
+      const bool done = f32 ? ws_softmax_tile<WS_FKEYS>(work, tmem, lane_base, t, w, row, full, mk, nk, c, m_ref,
                                                         l_part, s_o_done, s_s_free, s_pmax, abort_flag)
-                            : ws_softmax_tile<WS_KEYS>(work, tmem, lane_base, t, g, row, full, mk, nk, c, m_ref,
+                            : ws_softmax_tile<WS_KEYS>(work, tmem, lane_base, t, w, row, full, mk, nk, c, m_ref,
                                                        l_part, s_o_done, s_s_free, s_pmax, abort_flag);
       if (work && !done) ok = false;
       sm100::tc_fence_before();
       __syncwarp();
-      if (work && ok && lane == 0) sm100::mbar_arrive(&s_p_full[t & 1]);
+      if (work && ok && lane == 0) sm100::mbar_arrive(&s_p_full[grp]);
     }
-    if (ok && n_tiles > 0) {
-      const int tl = n_tiles - 1;
-      ok = ws_warp_wait(&s_o_done[tl & 1], static_cast<uint32_t>((tl >> 1) & 1), abort_flag);
-      if (ok) {
-        sm100::tc_fence_after();
-        ws_tmem_ld32(tmem + WS_TM_O + lane_base + OC * g, o);
-        sm100::tmem_wait_ld();
-      }
+    // the group's last P V
+    if (ok && n_tiles > grp) {
+      const int tl = grp + 2 * ((n_tiles - 1 - grp) / 2);
+      ok = ws_warp_wait(&s_o_done[grp], static_cast<uint32_t>((tl >> 1) & 1), abort_flag);
     }
     if (!ok) {
       if (lane == 0) set_status(p.status, EAGLE_ERR_TIMEOUT);
       s_abort = 1;
     }
-    s_lsum[g][row] = l_part;
+    // the two groups' states of the row: m (alike in a group's warpgroups), l in parts
+    if (w == 0) s_m[grp][row] = m_ref;
+    s_l[grp][w][row] = l_part;
     sm100::named_barrier(WS_BAR_SOFT, WS_SOFT_THREADS);
-    m_run = m_ref;
-    // the row sum, in the same order in every warpgroup
-    l_run = (s_lsum[0][row] + s_lsum[1][row]) + (s_lsum[2][row] + s_lsum[3][row]);
+    const float m0 = s_m[0][row], m1 = s_m[1][row];
+    const float M = fmaxf(m0, m1);
+    const float a0 = m0 == -INFINITY ? 0.f : ws_exp2(m0 - M), a1 = m1 == -INFINITY ? 0.f : ws_exp2(m1 - M);
+    m_run = M;
+    l_run = a0 * (s_l[0][0][row] + s_l[0][1][row]) + a1 * (s_l[1][0][row] + s_l[1][1][row]);
+    // output columns c0 .. c0 + OC - 1: a0 O_0 + a1 O_1 (an O with weight 0 is not read: it may never have been written)
+    if (ok && !*abort_flag) {
+      sm100::tc_fence_after();
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi) {
+        const float a = gi ? a1 : a0;
+        if (__any_sync(0xffffffffu, a != 0.f)) {
+          float v[OC];
+          ws_tmem_ld32(tmem + WS_TM_O + WS_TM_O_STEP * gi + lane_base + c0, v);
+          sm100::tmem_wait_ld();
+          if (a != 0.f) {
+#pragma unroll
+            for (int j = 0; j < OC; ++j) o[j] = fmaf(a, v[j], o[j]);
+          }
+        }
+      }
+    }
   }
   sm100::tc_fence_before();
   __syncthreads();
@@ -1795,7 +1802,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   }
   if (s_abort) return;
 
-  // this thread's output columns OC g .. OC g + OC - 1 of its row
+  // this thread's output columns c0 .. c0 + OC - 1 of its row
   // (a row with no key in this split keeps max -inf, sum 0, output 0)
   const bool has_row = warp >= WS_SOFT_WARP0 && row < rows_here;
   const int r = r0 + row;
@@ -1805,15 +1812,15 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     if (!has_row) return;
     const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
     if (!draft) {
-      float* dst = p.out_f32 + qi * WS_DH + OC * g;
+      float* dst = p.out_f32 + qi * WS_DH + c0;
 #pragma unroll
       for (int q = 0; q < OC / 4; ++q)
         *reinterpret_cast<float4*>(dst + 4 * q) =
             make_float4(o[4 * q] * inv, o[4 * q + 1] * inv, o[4 * q + 2] * inv, o[4 * q + 3] * inv);
     } else {
       const size_t j = static_cast<size_t>(b) * p.rows_cap + node;
-      uint16_t* dh = p.b_o + j * p.bo_ld + hq * WS_DH + OC * g;
-      uint16_t* dl = p.b_o + (static_cast<size_t>(p.NP) + j) * p.bo_ld + hq * WS_DH + OC * g;
+      uint16_t* dh = p.b_o + j * p.bo_ld + hq * WS_DH + c0;
+      uint16_t* dl = p.b_o + (static_cast<size_t>(p.NP) + j) * p.bo_ld + hq * WS_DH + c0;
 #pragma unroll
       for (int q = 0; q < OC / 8; ++q) {
         uint4 hi, lo;
@@ -1834,13 +1841,13 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
   const int ns = p.n_splits;
   if (has_row) {
     float* dst = p.part + (qi * ns + split) * rec;
-    if (g == 0) {
+    if (c0 == 0) {
       dst[0] = m_run;
       dst[1] = l_run;
     }
 #pragma unroll
     for (int q = 0; q < OC / 4; ++q)
-      *reinterpret_cast<float4*>(dst + 4 + OC * g + 4 * q) = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+      *reinterpret_cast<float4*>(dst + 4 + c0 + 4 * q) = make_float4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
   }
   __syncthreads();                           // every thread's records come first
   if (tid == 0) {
