@@ -671,13 +671,36 @@ __device__ __forceinline__ void gemm_produce_first_b(const GemmParams& p, const 
   __syncwarp();
 }
 
+// One MMA from 32-bit shared-memory descriptor words: lo = (address >> 4) |
+// (leading byte offset >> 4) << 16, hi = the stride / version / swizzle word
+// shared by both operands (an operand that many bytes on is lo + bytes >> 4:
+// the 14-bit address field never carries, shared memory ending below 256 KB).
+__device__ __forceinline__ void mma_lo_hi(uint32_t d_tmem, uint32_t alo, uint32_t blo, uint32_t hi, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 a, b;\n setp.ne.b32 p, %5, 0;\n mov.b64 a, {%1, %3};\n mov.b64 b, {%2, %3};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, p;\n}\n" ::"r"(d_tmem),
+      "r"(alo), "r"(blo), "r"(hi), "r"(idesc), "r"(acc));
+}
+
 // MMA issuer (warp 1, lane 0): one accumulator per tile segment of the
-// CTA's work, double-buffered in tensor memory when two fit.
+// CTA's work, double-buffered in tensor memory when two fit.  The issuing
+// loop is kept lean -- descriptor words advanced by adds, every MMA's offset
+// within a stage a constant -- since the MMAs issue only as fast as this
+// thread reaches them.
 __device__ __forceinline__ void gemm_mma(const GemmParams& p, const Smem& s, int lane, uint32_t tmem_base,
                                          const CtaWork& wk, volatile int* abort_flag) {
   if (lane == 0) {
     const uint32_t n_total = 2u * p.NP;
     const uint32_t idesc = p.two_mma ? sm100::idesc_bf16_f32(BM, p.NP) : sm100::idesc_bf16_f32(BM, n_total);
+    const uint32_t sbo = static_cast<uint32_t>(p.kps) * 1024u;
+    const uint32_t hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+    const uint32_t a_lo0 = ((sm100::smem_u32(s.a) >> 4) & 0x3FFFu) | (1u << 16);   // stage 0; leading byte offset 16
+    const uint32_t b_lo0 = ((sm100::smem_u32(s.b) >> 4) & 0x3FFFu) | (1u << 16);
+    const uint32_t a_step = p.a_stage_bytes >> 4, b_step = p.b_stage_bytes >> 4;
+    const uint32_t b2 = (static_cast<uint32_t>(p.NP >> 3) * sbo) >> 4;          // second activation half
+    const bool two = p.two_mma != 0, kps2 = p.kps == 2;
+    uint32_t a_lo = a_lo0, b_lo = b_lo0;                                           // the current stage's words
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -701,24 +724,29 @@ __device__ __forceinline__ void gemm_mma(const GemmParams& p, const Smem& s, int
           break;
         }
         sm100::tc_fence_after();
-        const uint32_t a_addr = sm100::smem_u32(s.a + static_cast<size_t>(stage) * p.a_stage_bytes);
-        const uint32_t b_addr = sm100::smem_u32(s.b + static_cast<size_t>(stage) * p.b_stage_bytes);
-        const uint32_t sbo = static_cast<uint32_t>(p.kps) * 1024u;
-        const uint32_t b2 = static_cast<uint32_t>(p.NP >> 3) * sbo;   // second activation half
-        for (int c = 0; c < p.kps; ++c) {
+        const uint32_t first = v != v0 ? 1u : 0u;        // only the segment's first MMA starts the sum
+        // k-block c, step kk: offset c * 1024 + kk * 32 bytes in both operands
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          if (c == 1 && !kps2) break;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint32_t off = static_cast<uint32_t>(c) * 1024u + kk * 32;
-            const uint64_t ad = sm100::smem_desc_sw128_sbo(a_addr + off, sbo);
-            const uint32_t accum = (v != v0 || c > 0 || kk > 0) ? 1u : 0u;
-            sm100::mma_bf16(d_tmem, ad, sm100::smem_desc_sw128_sbo(b_addr + off, sbo), idesc, accum);
-            if (p.two_mma)
-              sm100::mma_bf16(d_tmem + p.NP, ad, sm100::smem_desc_sw128_sbo(b_addr + b2 + off, sbo), idesc,
-                              accum);
+            const uint32_t off = static_cast<uint32_t>((c * 1024 + kk * 32) >> 4);
+            const uint32_t acc = (c > 0 || kk > 0) ? 1u : first;
+            mma_lo_hi(d_tmem, a_lo + off, b_lo + off, hi, idesc, acc);
+            if (two) mma_lo_hi(d_tmem + p.NP, a_lo + off, b_lo + b2 + off, hi, idesc, acc);
           }
         }
         sm100::mma_commit(&s.empty[stage]);
-        if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+          a_lo = a_lo0;
+          b_lo = b_lo0;
+        } else {
+          a_lo += a_step;
+          b_lo += b_step;
+        }
       }
       if (!ok) break;
       sm100::mma_commit(&s.tfull[buf]);
