@@ -1111,6 +1111,8 @@ __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1) tree_attn_mma_kernel
 //               - m) (c = scale log2 e) of its keys as bf16 hi + lo into
 //               tensor memory; its share of the row sum; quarter g of O's
 //               columns when O is rescaled and at the end.
+// Warps whose 32 rows all lie past a block's rows (a few-row draft layer)
+// only keep the barrier protocol.
 // The four warpgroups (rather than two taking all of a row's keys each) hide
 // the latency of the per-tile chain -- tensor-memory load, maximum,
 // exponentials, hi / lo split, tensor-memory store -- measured as the limit.
@@ -1365,12 +1367,13 @@ __device__ __forceinline__ bool ws_warp_wait(uint64_t* bar, uint32_t parity, vol
 // of the group's two warpgroups' partial maxima, exchanged through s_pmax
 // [group][2][2][128] with one barrier of the group's warps; every thread of
 // the group calls this once per tile of the group, `work` false after an
-// abort (the barrier is still passed, nothing else done).  Returns false
-// when a wait gave up.
+// abort (the barrier is still passed, nothing else done) and `rows` false
+// for a warp none of whose rows the block has (barrier and arrivals only).
+// Returns false when a wait gave up.
 template <int KT>
-__device__ __forceinline__ bool ws_softmax_tile(bool work, uint32_t tmem, uint32_t lane_base, int t, int w, int row,
-                                                bool full, uint64_t mk, int nk, float c, float& m_ref, float& l_part,
-                                                uint64_t* o_done, uint64_t* s_free, float* s_pmax,
+__device__ __forceinline__ bool ws_softmax_tile(bool work, bool rows, uint32_t tmem, uint32_t lane_base, int t, int w,
+                                                int row, bool full, uint64_t mk, int nk, float c, float& m_ref,
+                                                float& l_part, uint64_t* o_done, uint64_t* s_free, float* s_pmax,
                                                 volatile int* abort) {
   constexpr int KPT = KT / WS_GROUP_WGS;     // this thread's keys: 32 of 64 or 16 of 32
   const int G = t & 1, u = t >> 1;           // the group and its own tile count
@@ -1382,7 +1385,13 @@ __device__ __forceinline__ bool ws_softmax_tile(bool work, uint32_t tmem, uint32
   const bool pos = c > 0.f;
   const float ec = pos ? c : 1.f;
   float pm = -INFINITY;
-  if (work) {
+  if (work && !rows) {
+    // a warp whose 32 rows all lie past the block's: it only keeps the
+    // barrier protocol (its P stays unwritten: those O rows are never read)
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) sm100::mbar_arrive(&s_free[G]);
+  }
+  if (work && rows) {
     if constexpr (KPT == 32) {
       ws_tmem_ld32(tmem + WS_TM_S + 64u * G + lane_base + j0, sv);
     } else {
@@ -1412,7 +1421,7 @@ __device__ __forceinline__ bool ws_softmax_tile(bool work, uint32_t tmem, uint32
   pmx[w * WS_ROWS + row] = pm;
   if (G) sm100::named_barrier(WS_BAR_GROUP + 1, WS_GROUP_THREADS);
   else sm100::named_barrier(WS_BAR_GROUP, WS_GROUP_THREADS);
-  if (!work) return true;
+  if (!work || !rows) return true;
   const float mt = fmaxf(pmx[row], pmx[WS_ROWS + row]) * ec;   // the tile's maximum, log2 units
   const bool raise = mt > m_ref + WS_RESCALE * WS_LOG2E || (m_ref == -INFINITY && mt != -INFINITY);
   const bool rescale = raise && m_ref != -INFINITY;
@@ -1730,10 +1739,11 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     }
   } else if (warp >= WS_SOFT_WARP0) {
     // ---- softmax: group grp takes the tiles t = grp (mod 2) ----
-    // Every warp of the group takes part in each of the group's tiles (rows
-    // past the block's have zero queries: finite, never written out) and
-    // passes the tile's barrier once, also after an abort.
+    // Every warp of the group passes each of the group's tile barriers once,
+    // also after an abort or with no rows of the block (in a warp that has
+    // some, rows past the block's have zero queries: finite, never written out).
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const bool warp_rows = quarter * 32 < rows_here;   // (the rest of a few-row block is padding)
     const float c = p.scale * WS_LOG2E;
     float m_ref = -INFINITY, l_part = 0.f;
     bool ok = true;
@@ -1749,10 +1759,10 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
       T.at(t, tree, f32, k0, nk);
       const bool full = !tree && nk == WS_KEYS;
       const uint64_t mk = tree ? (s_mask[row * MASKW + (k0 >> 6)] >> (k0 & 63)) : ~0ull;
-      const bool done = f32 ? ws_softmax_tile<WS_FKEYS>(work, tmem, lane_base, t, w, row, full, mk, nk, c, m_ref,
-                                                        l_part, s_o_done, s_s_free, s_pmax, abort_flag)
-                            : ws_softmax_tile<WS_KEYS>(work, tmem, lane_base, t, w, row, full, mk, nk, c, m_ref,
-                                                       l_part, s_o_done, s_s_free, s_pmax, abort_flag);
+      const bool done = f32 ? ws_softmax_tile<WS_FKEYS>(work, warp_rows, tmem, lane_base, t, w, row, full, mk, nk, c,
+                                                        m_ref, l_part, s_o_done, s_s_free, s_pmax, abort_flag)
+                            : ws_softmax_tile<WS_KEYS>(work, warp_rows, tmem, lane_base, t, w, row, full, mk, nk, c,
+                                                       m_ref, l_part, s_o_done, s_s_free, s_pmax, abort_flag);
       if (work && !done) ok = false;
       sm100::tc_fence_before();
       __syncwarp();
@@ -1777,7 +1787,7 @@ __global__ void __launch_bounds__(WS_THREADS, 1)
     m_run = M;
     l_run = a0 * (s_l[0][0][row] + s_l[0][1][row]) + a1 * (s_l[1][0][row] + s_l[1][1][row]);
     // output columns c0 .. c0 + OC - 1: a0 O_0 + a1 O_1 (an O with weight 0 is not read: it may never have been written)
-    if (ok && !*abort_flag) {
+    if (ok && !*abort_flag && warp_rows) {
       sm100::tc_fence_after();
 #pragma unroll
       for (int gi = 0; gi < 2; ++gi) {
