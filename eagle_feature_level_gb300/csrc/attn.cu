@@ -1947,9 +1947,12 @@ static cudaError_t launch_mma(const AttnParams& p, dim3 grid, size_t smem, cudaS
 // cores (10 against 15 us), most of a 16-row tile being padding.
 constexpr int kDraftMmaRows = 8;
 
-// Query rows per (request, kv head) from which the draft layer's attention
-// (dh 128) runs on the tcgen05 kernel.
+// Query rows per (request, kv head) from which the attention (dh 128) runs
+// on the tcgen05 kernel.  Measured at the 7B shape: the static tree's 26
+// verification rows 20 -> 16 us per round against warp-level MMA; the draft
+// layer's 1-4 rows 48 -> 72 us (slower: a 128-row block of padding).
 constexpr int kDraftTcRows = 8;
+constexpr int kVerifyTcRows = 16;
 
 // A bf16 KV array [rows][Hkv][dh 128] as a 3-D tensor map {dh, kv head, row}
 // with boxes of 64 dims x 1 head x box_rows rows in the 128-byte swizzle.
@@ -2007,7 +2010,8 @@ static cudaError_t run_attn_ws(eagle_ctx* ctx, AttnParams& p, int kernel_id, cud
 
 static cudaError_t run_attn(eagle_ctx* ctx, AttnParams& p, int kernel_id, cudaStream_t st) {
   if (p.dh % 16 != 0 || p.dh > MAX_DH) return cudaErrorInvalidValue;
-  if (p.dh == WS_DH && ((p.mode == 1 && p.rows_cap * p.G > ROWS_PASS) || (p.mode == 0 && p.rows_cap * p.G >= kDraftTcRows)))
+  if (p.dh == WS_DH && ((p.mode == 1 && p.rows_cap * p.G >= kVerifyTcRows) ||
+                        (p.mode == 0 && p.rows_cap * p.G >= kDraftTcRows)))
     return run_attn_ws(ctx, p, kernel_id, st);
   const bool mma = p.mode == 1 || p.rows_cap * p.G >= kDraftMmaRows;
   const int tiles = ceil_div(p.kv_cap, TILE);
