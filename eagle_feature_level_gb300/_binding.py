@@ -158,6 +158,7 @@ def _declare(L):
         "eagle_draft_refresh": [P, I, C.POINTER(eagle_draft_weights), C.POINTER(eagle_accept_out),
                                 C.POINTER(eagle_commit_out), P, C.POINTER(eagle_kv), P, P, P],
         "eagle_stamps_disable": [P, C.POINTER(I), I, C.POINTER(I)],
+        "eagle_wait_selftest": [P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -175,7 +176,7 @@ EXPORTED = ["eagle_create", "eagle_destroy", "eagle_workspace_init", "eagle_read
             "eagle_accept", "eagle_accept_from_probs",
             "eagle_commit", "eagle_trace_enable", "eagle_trace_read", "eagle_trace_disable",
             "eagle_stamps_enable", "eagle_stamps_disable", "eagle_draft_refresh", "eagle_fuse_features",
-            "eagle_launch_count"]
+            "eagle_launch_count", "eagle_wait_selftest"]
 
 
 def _check(name: str, code: int):
@@ -208,6 +209,10 @@ def eagle_read_device_status(ctx, ws_ptr: int, stream: int) -> int:
     v = I()
     _check("eagle_read_device_status", lib().eagle_read_device_status(ctx, ws_ptr, stream, C.byref(v)))
     return v.value
+
+
+def eagle_wait_selftest(ctx, ws_ptr: int, stream: int):
+    _check("eagle_wait_selftest", lib().eagle_wait_selftest(ctx, ws_ptr, stream))
 
 
 def eagle_status_string(code: int) -> str:

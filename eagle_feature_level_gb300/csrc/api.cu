@@ -762,6 +762,14 @@ eagle_status eagle_stamps_disable(eagle_ctx* ctx, int* ids_out, int cap, int* n_
   return EAGLE_OK;
 }
 
+eagle_status eagle_wait_selftest(eagle_ctx* ctx, void* workspace, cudaStream_t stream) {
+  EAGLE_REQUIRE(ctx, EAGLE_ERR_INVALID_ARG);
+  eagle_status st = check_ws(workspace);
+  if (st != EAGLE_OK) return st;
+  EAGLE_CUDA(eagle::launch_wait_selftest(ctx, workspace, stream));
+  return EAGLE_OK;
+}
+
 long long eagle_launch_count(const eagle_ctx* ctx) { return ctx ? ctx->launches : -1; }
 
 }  // extern "C"

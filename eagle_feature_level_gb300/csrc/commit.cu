@@ -7,6 +7,7 @@
 // the root's draft K/V row.
 #include "internal.h"
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace eagle {
 namespace {
@@ -169,6 +170,32 @@ cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st
   ctx->launches++;
   trace_after(ctx, EAGLE_K_COMMIT, st);
   return e;
+}
+
+// ---- the bounded wait, checked ------------------------------------------------
+//
+// One CTA whose only wait is the library's bounded barrier wait on a barrier
+// nothing arrives at: it gives up after the device wait limit and reports
+// EAGLE_ERR_TIMEOUT in the status word, as every kernel's barrier wait does,
+// and returns (nothing is in flight when it leaves).
+namespace {
+__global__ void wait_selftest_kernel(int* status) {
+  __shared__ uint64_t s_bar;
+  __shared__ int s_abort;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    sm100::mbar_init(&s_bar, 1);
+    sm100::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !sm100::mbar_wait(&s_bar, 0u, &s_abort)) set_status(status, EAGLE_ERR_TIMEOUT);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(eagle_ctx* ctx, void* ws, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(ws_ptr<int>(ws, ctx->ws.status));
+  ctx->launches++;
+  return cudaGetLastError();
 }
 
 }  // namespace eagle

@@ -244,6 +244,7 @@ struct CommitLaunch {
   int* status;
 };
 cudaError_t launch_commit(eagle_ctx* ctx, const CommitLaunch& C, cudaStream_t st);
+cudaError_t launch_wait_selftest(eagle_ctx* ctx, void* ws, cudaStream_t st);
 
 // Prefix splits of the split-KV attention for `pairs` (request, kv head)
 // pairs over a cache of `cap` rows, for a kernel run at per_sm CTAs per SM.

@@ -267,6 +267,19 @@ eagle_status eagle_read_device_status(eagle_ctx* ctx, void* workspace, cudaStrea
 
 const char* eagle_status_string(eagle_status s);
 
+/* Checks the device-side failure path of the kernels' waits.  Every wait of
+ * the library's kernels on a barrier (a tile landing, a tensor-core result,
+ * another warp's hand-off) is bounded: after 2 s it gives up, sets
+ * EAGLE_ERR_TIMEOUT in the status word and returns, so a lost arrival ends
+ * the launch with an error instead of a hang and the context stays usable.
+ * This launches one CTA whose only wait, that same bounded wait, is on a
+ * barrier nothing arrives at: about 2 s later the status word holds
+ * EAGLE_ERR_TIMEOUT (read and clear it with eagle_read_device_status).
+ * Asynchronous on `stream`; returns EAGLE_OK once launched (EAGLE_ERR_CUDA on
+ * a launch failure, EAGLE_ERR_INVALID_ARG / EAGLE_ERR_ALIGN for the context
+ * or workspace). */
+eagle_status eagle_wait_selftest(eagle_ctx* ctx, void* workspace, cudaStream_t stream);
+
 /* ---- plans (host only) ---------------------------------------------------- */
 
 /* EAGLE-2 plan: layers 0..depth-1 run on 1, top_k, ..., top_k rows per request;

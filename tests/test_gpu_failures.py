@@ -4,8 +4,10 @@ EAGLE_ERR_NUMERIC in the device status word and the calls still return; a
 misaligned pointer is refused with EAGLE_ERR_ALIGN before anything is
 launched; a cache that cannot take the accepted path refuses the commit
 (EAGLE_ERR_CAPACITY, nothing written for that request), and a prefix length
-beyond its cache is read as the cache and reported."""
+beyond its cache is read as the cache and reported; a barrier wait that
+nothing ends gives up after the device limit with EAGLE_ERR_TIMEOUT."""
 import math
+import time
 
 import numpy as np
 import pytest
@@ -21,6 +23,7 @@ pytestmark = pytest.mark.gpu
 W = S.variant("70b_x16_eagle2", name="failures_small", d=128, n_q_heads=4, n_kv_heads=2, head_dim=32, d_ff=256,
               vocab=700, batch=2, prefix_len=80, top_k=3, depth=3, top_m=6, weight_std=0.05, temps=(0.0, 1.0))
 NUMERIC, ALIGN, CAPACITY = 6, 3, 4
+TIMEOUT = 7
 
 
 def _round(seed=31):
@@ -148,4 +151,25 @@ def test_prefix_longer_than_its_cache_is_read_as_the_cache():
         n = int(rd.t_size[b])
         assert torch.equal(rd.attn_out[b, :n], ref[b, :n])
     assert np.isfinite(rd.attn_out.cpu().numpy()).all()
+    eng.close()
+
+
+def test_bounded_wait_gives_up_with_timeout_and_the_context_stays_usable():
+    """The kernels' barrier waits are bounded: the self-test's one CTA waits
+    on a barrier nothing arrives at, gives up after the 2 s device limit and
+    reports EAGLE_ERR_TIMEOUT; the same context then runs a whole round with
+    a clean status."""
+    eng, rd, wc, inp = _round(seed=71)
+    st, ws = eng.stream(), eng.ws.data_ptr()
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    B.eagle_wait_selftest(eng.ctx, ws, st)
+    torch.cuda.synchronize()
+    waited = time.monotonic() - t0
+    assert eng.status() == TIMEOUT
+    assert 1.5 <= waited <= 30.0, waited
+    rd.run(wc, target_fn=standin(inp))
+    torch.cuda.synchronize()
+    assert eng.status() == 0
+    assert (rd.accept_len >= 0).all()
     eng.close()
