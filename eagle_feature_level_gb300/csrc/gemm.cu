@@ -686,71 +686,84 @@ __device__ __forceinline__ void mma_lo_hi(uint32_t d_tmem, uint32_t alo, uint32_
 // MMA issuer (warp 1, lane 0): one accumulator per tile segment of the
 // CTA's work, double-buffered in tensor memory when two fit.  The issuing
 // loop is kept lean -- descriptor words advanced by adds, every MMA's offset
-// within a stage a constant -- since the MMAs issue only as fast as this
-// thread reaches them.
-__device__ __forceinline__ void gemm_mma(const GemmParams& p, const Smem& s, int lane, uint32_t tmem_base,
-                                         const CtaWork& wk, volatile int* abort_flag) {
-  if (lane == 0) {
-    const uint32_t n_total = 2u * p.NP;
-    const uint32_t idesc = p.two_mma ? sm100::idesc_bf16_f32(BM, p.NP) : sm100::idesc_bf16_f32(BM, n_total);
-    const uint32_t sbo = static_cast<uint32_t>(p.kps) * 1024u;
-    const uint32_t hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
-    const uint32_t a_lo0 = ((sm100::smem_u32(s.a) >> 4) & 0x3FFFu) | (1u << 16);   // stage 0; leading byte offset 16
-    const uint32_t b_lo0 = ((sm100::smem_u32(s.b) >> 4) & 0x3FFFu) | (1u << 16);
-    const uint32_t a_step = p.a_stage_bytes >> 4, b_step = p.b_stage_bytes >> 4;
-    const uint32_t b2 = (static_cast<uint32_t>(p.NP >> 3) * sbo) >> 4;          // second activation half
-    const bool two = p.two_mma != 0, kps2 = p.kps == 2;
-    uint32_t a_lo = a_lo0, b_lo = b_lo0;                                           // the current stage's words
-    int stage = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    int t;
-    long long v0, v1;
-    for (int seg = 0; ok && wk.segment(p, seg, t, v0, v1); ++seg) {
-      const int buf = seg % p.n_acc;
-      const uint32_t aph = static_cast<uint32_t>(seg / p.n_acc) & 1u;
-      if (!sm100::mbar_wait(&s.tempty[buf], aph ^ 1u, abort_flag)) {
+// within a stage a constant, the stage shape (KPS2: two k-blocks per stage;
+// TWO: the hi and lo halves as separate MMAs) a template parameter with no
+// branch between MMAs -- since the MMAs issue only as fast as this thread
+// reaches them (a runtime test of either flag between the MMAs doubled the
+// issue time per MMA).
+template <bool KPS2, bool TWO>
+__device__ __forceinline__ void gemm_mma_loop(const GemmParams& p, const Smem& s, uint32_t tmem_base,
+                                              const CtaWork& wk, volatile int* abort_flag) {
+  const uint32_t n_total = 2u * p.NP;
+  const uint32_t idesc = TWO ? sm100::idesc_bf16_f32(BM, p.NP) : sm100::idesc_bf16_f32(BM, n_total);
+  const uint32_t sbo = static_cast<uint32_t>(p.kps) * 1024u;
+  const uint32_t hi = ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+  const uint32_t a_lo0 = ((sm100::smem_u32(s.a) >> 4) & 0x3FFFu) | (1u << 16);   // stage 0; leading byte offset 16
+  const uint32_t b_lo0 = ((sm100::smem_u32(s.b) >> 4) & 0x3FFFu) | (1u << 16);
+  const uint32_t a_step = p.a_stage_bytes >> 4, b_step = p.b_stage_bytes >> 4;
+  const uint32_t b2 = (static_cast<uint32_t>(p.NP >> 3) * sbo) >> 4;          // second activation half
+  uint32_t a_lo = a_lo0, b_lo = b_lo0;                                           // the current stage's words
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+  int t;
+  long long v0, v1;
+  for (int seg = 0; ok && wk.segment(p, seg, t, v0, v1); ++seg) {
+    const int buf = seg % p.n_acc;
+    const uint32_t aph = static_cast<uint32_t>(seg / p.n_acc) & 1u;
+    if (!sm100::mbar_wait(&s.tempty[buf], aph ^ 1u, abort_flag)) {
+      *abort_flag = 1;
+      set_status(p.status, EAGLE_ERR_TIMEOUT);
+      break;
+    }
+    sm100::tc_fence_after();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
+    for (long long v = v0; v < v1; ++v) {
+      if (!sm100::mbar_wait(&s.full[stage], phase, abort_flag)) {
         *abort_flag = 1;
         set_status(p.status, EAGLE_ERR_TIMEOUT);
+        ok = false;
         break;
       }
       sm100::tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * p.acc_stride);
-      for (long long v = v0; v < v1; ++v) {
-        if (!sm100::mbar_wait(&s.full[stage], phase, abort_flag)) {
-          *abort_flag = 1;
-          set_status(p.status, EAGLE_ERR_TIMEOUT);
-          ok = false;
-          break;
-        }
-        sm100::tc_fence_after();
-        const uint32_t first = v != v0 ? 1u : 0u;        // only the segment's first MMA starts the sum
-        // k-block c, step kk: offset c * 1024 + kk * 32 bytes in both operands
+      const uint32_t first = v != v0 ? 1u : 0u;        // only the segment's first MMA starts the sum
+      // k-block c, step kk: offset c * 1024 + kk * 32 bytes in both operands
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          if (c == 1 && !kps2) break;
+      for (int c = 0; c < 2; ++c) {
+        if (c == 1 && !KPS2) break;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint32_t off = static_cast<uint32_t>((c * 1024 + kk * 32) >> 4);
-            const uint32_t acc = (c > 0 || kk > 0) ? 1u : first;
-            mma_lo_hi(d_tmem, a_lo + off, b_lo + off, hi, idesc, acc);
-            if (two) mma_lo_hi(d_tmem + p.NP, a_lo + off, b_lo + b2 + off, hi, idesc, acc);
-          }
-        }
-        sm100::mma_commit(&s.empty[stage]);
-        if (++stage == p.stages) {
-          stage = 0;
-          phase ^= 1u;
-          a_lo = a_lo0;
-          b_lo = b_lo0;
-        } else {
-          a_lo += a_step;
-          b_lo += b_step;
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint32_t off = static_cast<uint32_t>((c * 1024 + kk * 32) >> 4);
+          const uint32_t acc = (c > 0 || kk > 0) ? 1u : first;
+          mma_lo_hi(d_tmem, a_lo + off, b_lo + off, hi, idesc, acc);
+          if (TWO) mma_lo_hi(d_tmem + p.NP, a_lo + off, b_lo + b2 + off, hi, idesc, acc);
         }
       }
-      if (!ok) break;
-      sm100::mma_commit(&s.tfull[buf]);
+      sm100::mma_commit(&s.empty[stage]);
+      if (++stage == p.stages) {
+        stage = 0;
+        phase ^= 1u;
+        a_lo = a_lo0;
+        b_lo = b_lo0;
+      } else {
+        a_lo += a_step;
+        b_lo += b_step;
+      }
     }
+    if (!ok) break;
+    sm100::mma_commit(&s.tfull[buf]);
+  }
+}
+
+__device__ __forceinline__ void gemm_mma(const GemmParams& p, const Smem& s, int lane, uint32_t tmem_base,
+                                         const CtaWork& wk, volatile int* abort_flag) {
+  if (lane != 0) return;
+  if (p.kps == 2) {
+    if (p.two_mma) gemm_mma_loop<true, true>(p, s, tmem_base, wk, abort_flag);
+    else gemm_mma_loop<true, false>(p, s, tmem_base, wk, abort_flag);
+  } else {
+    if (p.two_mma) gemm_mma_loop<false, true>(p, s, tmem_base, wk, abort_flag);
+    else gemm_mma_loop<false, false>(p, s, tmem_base, wk, abort_flag);
   }
 }
 
