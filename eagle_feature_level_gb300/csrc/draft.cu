@@ -166,6 +166,11 @@ static_assert(SEL_CL * SEL_SLICE >= EAGLE_MAX_VOCAB, "one cluster covers the lar
 static_assert(SEL_CL * EAGLE_MAX_CHILDREN <= 128 && SEL_WARPS * EAGLE_MAX_CHILDREN <= 128,
               "candidate lists fit four per lane");
 static_assert(SEL_WARPS == SEL_CL, "rank 0 merges the lists of CTA w in its warp w");
+// 32-bit words of the select kernel's shared buffer: the greedy lists or the
+// sampling per-thread totals, whichever is larger
+constexpr int SEL_GREEDY_WORDS = (2 * SEL_CL * SEL_WARPS + 3 * SEL_CL + 3 * SEL_WARPS) * EAGLE_MAX_CHILDREN;
+constexpr int SEL_SAMPLE_WORDS = 2 * SEL_CL * SEL_THREADS;
+constexpr int SEL_UNION_WORDS = SEL_GREEDY_WORDS > SEL_SAMPLE_WORDS ? SEL_GREEDY_WORDS : SEL_SAMPLE_WORDS;
 
 // (value desc, id asc) total order: true if a ranks before b.
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib) {
@@ -237,14 +242,28 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
   __shared__ float s_red[SEL_WARPS];
   __shared__ float s_cmax[SEL_CL], s_csum[SEL_CL];         // per-rank partials (pushed)
   __shared__ uint64_t s_ctot[SEL_CL];
-  __shared__ uint64_t s_tt[SEL_THREADS], s_wt[SEL_WARPS];    // sampling: integer weight totals per thread, warp
-  __shared__ float s_wz[SEL_WARPS * EAGLE_MAX_CHILDREN], s_wq[SEL_WARPS * EAGLE_MAX_CHILDREN];
-  __shared__ int s_wi[SEL_WARPS * EAGLE_MAX_CHILDREN];
-  // rank 0: every warp's list of every CTA (pushed), then each CTA's merged list
-  __shared__ float s_gz[SEL_CL * SEL_WARPS * EAGLE_MAX_CHILDREN];
-  __shared__ int s_gi[SEL_CL * SEL_WARPS * EAGLE_MAX_CHILDREN];
-  __shared__ float s_cz[SEL_CL * EAGLE_MAX_CHILDREN], s_cq[SEL_CL * EAGLE_MAX_CHILDREN];
-  __shared__ int s_ci[SEL_CL * EAGLE_MAX_CHILDREN];
+  __shared__ uint64_t s_wt[SEL_WARPS];                       // sampling: integer weight totals per warp
+  // sampling, rank 0: every CTA's per-warp weight totals (pushed), and the
+  // draws so far (token, weight)
+  __shared__ uint64_t s_gwt[SEL_CL * SEL_WARPS];
+  __shared__ int s_dtok[EAGLE_MAX_CHILDREN];
+  __shared__ uint64_t s_dw[EAGLE_MAX_CHILDREN];
+  // One buffer serves either path (a cluster's row is greedy or sampled in
+  // every CTA), which keeps the kernel's shared memory small enough for its
+  // CTAs to be resident beside the LM-head contraction they follow, so that
+  // they start before it ends.  Greedy, rank 0: every warp's list of every
+  // CTA (pushed), each CTA's merged list, the final list.  Sampling, rank 0:
+  // every CTA's per-thread weight totals (pushed).
+  __shared__ __align__(16) uint32_t s_un[SEL_UNION_WORDS];
+  float* s_gz = reinterpret_cast<float*>(s_un);
+  int* s_gi = reinterpret_cast<int*>(s_gz + SEL_CL * SEL_WARPS * EAGLE_MAX_CHILDREN);
+  float* s_cz = reinterpret_cast<float*>(s_gi + SEL_CL * SEL_WARPS * EAGLE_MAX_CHILDREN);
+  float* s_cq = s_cz + SEL_CL * EAGLE_MAX_CHILDREN;
+  int* s_ci = reinterpret_cast<int*>(s_cq + SEL_CL * EAGLE_MAX_CHILDREN);
+  float* s_wz = reinterpret_cast<float*>(s_ci + SEL_CL * EAGLE_MAX_CHILDREN);
+  float* s_wq = s_wz + SEL_WARPS * EAGLE_MAX_CHILDREN;
+  int* s_wi = reinterpret_cast<int*>(s_wq + SEL_WARPS * EAGLE_MAX_CHILDREN);
+  uint64_t* s_gtt = reinterpret_cast<uint64_t*>(s_un);
 
   const int row = blockIdx.x / SEL_CL;
   const uint32_t rank = sm100::cluster_rank();
@@ -386,21 +405,27 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
     return;
   }
 
-  // sampling: exact integer weights floor(q 2^40).  Every CTA leaves its
-  // per-thread and per-warp weight totals in shared memory; one warp of rank
-  // 0 then makes the k draws without replacement, each by descending from
-  // the CTAs' totals to a warp's and a thread's (reading the other CTAs'
-  // shared memory) and to that thread's entries (their weights again from
-  // q, which every CTA wrote before the barrier), the weights already drawn
-  // taken out at every level: the token is the first one, in vocabulary
-  // order, at which the running sum of the remaining weights exceeds
-  // t = floor(u32 * remaining / 2^32).
+  // sampling: exact integer weights floor(q 2^40).  Every CTA pushes its
+  // per-thread and per-warp weight totals into rank 0's shared memory; one
+  // warp of rank 0 then makes the k draws without replacement, each by
+  // descending from the CTAs' totals to a warp's and a thread's (local
+  // reads) and to that thread's entries (their weights again from q, which
+  // every CTA wrote before the barrier), the weights already drawn taken out
+  // at every level: the token is the first one, in vocabulary order, at
+  // which the running sum of the remaining weights exceeds
+  // t = floor(u32 * remaining / 2^32).  After the barrier no CTA touches
+  // another's shared memory, so the CTAs other than rank 0 leave at once
+  // (with many rows, later clusters take their SMs: 13B batch 8, 270 ->
+  // 199 us of selection per round).
   uint64_t wsum = 0;
 #pragma unroll
   for (int u = 0; u < SEL_PER; ++u) wsum += v0 + u < V ? quantize_prob(q[u]) : 0ull;
-  s_tt[tid] = wsum;
+  sm100::dsmem_st_u64(sm100::dsmem_addr(&s_gtt[rank * SEL_THREADS + tid], 0), wsum);
   const uint64_t wtot = warp_sum_u64(wsum);
-  if (lane == 0) s_wt[wid] = wtot;
+  if (lane == 0) {
+    s_wt[wid] = wtot;
+    sm100::dsmem_st_u64(sm100::dsmem_addr(&s_gwt[rank * SEL_WARPS + wid], 0), wtot);
+  }
   __syncthreads();
   if (tid < SEL_CL) {                        // this CTA's total, to every rank
     uint64_t cta_total = 0;
@@ -412,7 +437,6 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
     uint64_t total = 0;
     for (int c = 0; c < SEL_CL; ++c) total += s_ctot[c];
     int pk_tok = -1;                         // lane r: the r-th drawn token, its weight and q
-    uint64_t pk_w = 0;
     float pk_q = 0.f;
     uint64_t picked = 0;
     int n_drawn = 0;
@@ -433,11 +457,11 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
       return f;
     };
     // adj minus the weights of the earlier draws that fall in [lo_v, hi_v)
+    // (each lane reads the draws from shared memory: no chain of shuffles)
     auto minus_drawn = [&](uint64_t adj, int lo_v, int hi_v, int r) {
       for (int s2 = 0; s2 < r; ++s2) {
-        const int tk = __shfl_sync(0xffffffffu, pk_tok, s2);
-        const uint64_t wk = __shfl_sync(0xffffffffu, pk_w, s2);
-        if (tk >= lo_v && tk < hi_v) adj -= wk;
+        const int tk = s_dtok[s2];
+        if (tk >= lo_v && tk < hi_v) adj -= s_dw[s2];
       }
       return adj;
     };
@@ -452,12 +476,12 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
       const int c = descend(lane < SEL_CL ? adj : 0ull, t);
       if (c < 0) { lost = true; break; }
       const int cb = c * SEL_SLICE;
-      adj = lane < SEL_WARPS ? sm100::dsmem_ld_u64(sm100::dsmem_addr(&s_wt[lane], c)) : 0ull;
+      adj = lane < SEL_WARPS ? s_gwt[c * SEL_WARPS + lane] : 0ull;
       adj = minus_drawn(adj, cb + lane * 32 * SEL_PER, cb + (lane + 1) * 32 * SEL_PER, r);
       const int w = descend(lane < SEL_WARPS ? adj : 0ull, t);
       if (w < 0) { lost = true; break; }
       const int th = w * 32 + lane;
-      adj = sm100::dsmem_ld_u64(sm100::dsmem_addr(&s_tt[th], c));
+      adj = s_gtt[c * SEL_THREADS + th];
       adj = minus_drawn(adj, cb + th * SEL_PER, cb + (th + 1) * SEL_PER, r);
       const int j = descend(adj, t);
       if (j < 0) { lost = true; break; }
@@ -470,9 +494,11 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
       const uint64_t wt = __shfl_sync(0xffffffffu, wraw, u);
       if (lane == r) {
         pk_tok = tok;
-        pk_w = wt;
         pk_q = qrow[tok];                    // written by its CTA before the barrier
+        s_dtok[r] = tok;
+        s_dw[r] = wt;
       }
+      __syncwarp();                          // the next draw's lanes read this one
       picked += wt;
       ++n_drawn;
     }
@@ -483,7 +509,6 @@ __global__ void __cluster_dims__(SEL_CL, 1, 1) __launch_bounds__(SEL_THREADS) se
     }
     if (lost && lane == 0) set_status(p.status, EAGLE_ERR_NUMERIC);
   }
-  sm100::cluster_sync();                     // no CTA leaves while rank 0 still reads its shared memory
 }
 
 }  // namespace

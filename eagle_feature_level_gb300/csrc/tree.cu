@@ -16,8 +16,9 @@
 // slots for the pool, tree slots for the tree): bit j is bit j % 64 of word
 // j / 64.  A tree slot's mask is built by its own thread walking the parent
 // chain to the root, every word in registers.
-// Ranks come from counting (each thread compares its key with every other
-// valid key), which is exact and independent of thread order.  Node values
+// Ranks come from counting (one warp per candidate, its lanes comparing the
+// candidate's key with every other valid key in turn and summing the
+// counts), which is exact and independent of thread order.  Node values
 // are non-negative fp64 products, whose bit patterns order like the values
 // as unsigned integers: the counting loops compare those (GB300 runs fp64
 // comparisons at a small fraction of the integer rate).
@@ -28,6 +29,7 @@ namespace eagle {
 namespace {
 
 constexpr int TREE_THREADS = 1024;
+constexpr int TREE_WARPS = TREE_THREADS / 32;
 constexpr int MAX_WORDS = EAGLE_MASK_WORDS(EAGLE_MAX_NODES);
 
 struct TreeParams {
@@ -156,22 +158,27 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
       if (valid) atomicAdd(&s_count, 1);
     }
     __syncthreads();
-    for (int c = tid; c < n_c; c += TREE_THREADS) {
-      if (!s_dep[c]) continue;
-      int rank = 0;
-      for (int o = 0; o < n_c; ++o)
-        if (s_dep[o] && before(s_key[o], 0, o, s_key[c], 0, c)) ++rank;
+    const int lane = tid & 31;
+    for (int c = tid >> 5; c < n_c; c += TREE_WARPS) {
+      if (!s_dep[c]) continue;                 // the same for the whole warp
+      const uint64_t kc = s_key[c];
+      int cnt = 0;
+      for (int o = lane; o < n_c; o += 32)
+        if (s_dep[o] && before(s_key[o], 0, o, kc, 0, c)) ++cnt;
+      const int rank = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt)));
       if (rank >= n_new) continue;
       const int e = e_prev + c / k, r = c % k;
       const int e_new = e_new0 + rank;
-      p.p_token[pb + e_new] = p.ctok[(pb + e) * K + r];
-      p.p_parent[pb + e_new] = e;
-      p.p_rank[pb + e_new] = r;
-      p.p_depth[pb + e_new] = p.p_depth[pb + e] + 1;
-      p.p_value[pb + e_new] = s_val[c];
-      for (int w = 0; w < p.WE; ++w)
+      if (lane == 0) {
+        p.p_token[pb + e_new] = p.ctok[(pb + e) * K + r];
+        p.p_parent[pb + e_new] = e;
+        p.p_rank[pb + e_new] = r;
+        p.p_depth[pb + e_new] = p.p_depth[pb + e] + 1;
+        p.p_value[pb + e_new] = s_val[c];
+        p.p_child_exp[(pb + e) * K + r] = e_new;
+      }
+      for (int w = lane; w < p.WE; w += 32)
         pool_anc(p, pb, e_new, w) = pool_anc(p, pb, e, w) | (w == (e_new >> 6) ? 1ull << (e_new & 63) : 0ull);
-      p.p_child_exp[(pb + e) * K + r] = e_new;
     }
     for (int i = tid; i < n_new; i += TREE_THREADS) {
       if (i < s_count) continue;
@@ -224,26 +231,32 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
       if (valid) atomicAdd(&s_count, 1);
     }
     __syncthreads();
-    for (int c = tid; c < n_c; c += TREE_THREADS) {
+    const int lane = tid & 31;
+    for (int c = tid >> 5; c < n_c; c += TREE_WARPS) {
       int rank = INT32_MAX;
-      if (s_dep[c] >= 0) {
-        rank = 0;
-        for (int o = 0; o < n_c; ++o)
-          if (s_dep[o] >= 0 && before(s_key[o], s_dep[o], o, s_key[c], s_dep[c], c)) ++rank;
+      if (s_dep[c] >= 0) {                     // the same for the whole warp
+        const uint64_t kc = s_key[c];
+        const int dc = s_dep[c];
+        int cnt = 0;
+        for (int o = lane; o < n_c; o += 32)
+          if (s_dep[o] >= 0 && before(s_key[o], s_dep[o], o, kc, dc, c)) ++cnt;
+        rank = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt)));
       }
-      s_rank[c] = rank;
+      if (lane == 0) s_rank[c] = rank;
     }
     __syncthreads();
     n_sel = min(m, s_count);
-    for (int c = tid; c < n_c; c += TREE_THREADS) {
+    for (int c = tid >> 5; c < n_c; c += TREE_WARPS) {
       const int rk = s_rank[c];
-      if (rk >= n_sel) continue;
-      int pos = 0;
-      for (int o = 0; o < n_c; ++o) {
+      if (rk >= n_sel) continue;               // the same for the whole warp
+      const int dc = s_dep[c];
+      int cnt = 0;
+      for (int o = lane; o < n_c; o += 32) {
         const int ro = s_rank[o];
-        if (ro < n_sel && (s_dep[o] < s_dep[c] || (s_dep[o] == s_dep[c] && ro < rk))) ++pos;
+        if (ro < n_sel && (s_dep[o] < dc || (s_dep[o] == dc && ro < rk))) ++cnt;
       }
-      s_slot[c] = 1 + pos;
+      const int pos = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt)));
+      if (lane == 0) s_slot[c] = 1 + pos;
     }
     __syncthreads();
     for (int c = tid; c < n_c; c += TREE_THREADS) {
