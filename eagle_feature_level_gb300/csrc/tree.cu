@@ -16,9 +16,12 @@
 // slots for the pool, tree slots for the tree): bit j is bit j % 64 of word
 // j / 64.  A tree slot's mask is built by its own thread walking the parent
 // chain to the root, every word in registers.
-// Ranks come from counting (one warp per candidate, its lanes comparing the
-// candidate's key with every other valid key in turn and summing the
-// counts), which is exact and independent of thread order.  Node values
+// A frontier layer's ranks come from counting (one warp per candidate, its
+// lanes comparing the candidate's key with every other valid key in turn
+// and summing the counts); the final selection's from a bitonic sort of the
+// whole pool's candidates by the same total order (a few hundred keys: the
+// counting's n^2 comparisons took ~30 us on one SM).  Both are exact and
+// independent of thread order.  Node values
 // are non-negative fp64 products, whose bit patterns order like the values
 // as unsigned integers: the counting loops compare those (GB300 runs fp64
 // comparisons at a small fraction of the integer rate).
@@ -77,11 +80,47 @@ __device__ __forceinline__ uint64_t& pool_anc(const TreeParams& p, size_t pb, in
   return p.p_anc[(pb + e) * p.WE + w];
 }
 
+__host__ __device__ inline int pow2_at_least(int n) {
+  int v = 1;
+  while (v < n) v <<= 1;
+  return v;
+}
+
 // Dynamic shared memory of the kernel: the E * K drawn candidates of a
-// request and the parent slot of every tree slot.
+// request, their sort order (padded to a power of two) and the parent slot
+// of every tree slot.
 size_t tree_smem_bytes(int E, int K, int S) {
   const size_t n = static_cast<size_t>(E) * K;
-  return n * (sizeof(double) + sizeof(uint64_t) + 3 * sizeof(int)) + static_cast<size_t>(S) * sizeof(int);
+  return n * (sizeof(double) + sizeof(uint64_t) + 3 * sizeof(int)) +
+         static_cast<size_t>(pow2_at_least(static_cast<int>(n))) * sizeof(int) + static_cast<size_t>(S) * sizeof(int);
+}
+
+// Candidate a goes before candidate b in the final order: valid ones first
+// by the selection order, then invalid and padding entries by index.
+__device__ __forceinline__ bool cand_before(int a, int b, const uint64_t* key, const int* dep, int n) {
+  const bool va = a < n && dep[a] >= 0, vb = b < n && dep[b] >= 0;
+  if (va != vb) return va;
+  if (!va) return a < b;
+  return before(key[a], dep[a], a, key[b], dep[b], b);
+}
+
+// Block-wide bitonic sort of order[0, n2) (n2 a power of two) by cand_before.
+__device__ void sort_candidates(int* order, int n2, const uint64_t* key, const int* dep, int n) {
+  for (int k2 = 2; k2 <= n2; k2 <<= 1)
+    for (int j = k2 >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += TREE_THREADS) {
+        const int l = i ^ j;
+        if (l > i) {
+          const int a = order[i], b = order[l];
+          const bool swap = (i & k2) == 0 ? cand_before(b, a, key, dep, n) : cand_before(a, b, key, dep, n);
+          if (swap) {
+            order[i] = b;
+            order[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
 }
 
 __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) {
@@ -96,7 +135,8 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
   int* s_dep = reinterpret_cast<int*>(s_key + n_pool);
   int* s_rank = s_dep + n_pool;
   int* s_slot = s_rank + n_pool;
-  int* s_parent_slot = s_slot + n_pool;
+  int* s_order = s_slot + n_pool;
+  int* s_parent_slot = s_order + pow2_at_least(n_pool);
   __shared__ int s_count;
 
   const int b = blockIdx.x;
@@ -231,32 +271,26 @@ __global__ void __launch_bounds__(TREE_THREADS) tree_kernel(const TreeParams p) 
       if (valid) atomicAdd(&s_count, 1);
     }
     __syncthreads();
-    const int lane = tid & 31;
-    for (int c = tid >> 5; c < n_c; c += TREE_WARPS) {
-      int rank = INT32_MAX;
-      if (s_dep[c] >= 0) {                     // the same for the whole warp
-        const uint64_t kc = s_key[c];
-        const int dc = s_dep[c];
-        int cnt = 0;
-        for (int o = lane; o < n_c; o += 32)
-          if (s_dep[o] >= 0 && before(s_key[o], s_dep[o], o, kc, dc, c)) ++cnt;
-        rank = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt)));
-      }
-      if (lane == 0) s_rank[c] = rank;
-    }
+    // every candidate's rank (its position in the sorted order; the
+    // s_count valid ones come first)
+    const int n2 = pow2_at_least(n_c);
+    for (int i = tid; i < n2; i += TREE_THREADS) s_order[i] = i;
     __syncthreads();
+    sort_candidates(s_order, n2, s_key, s_dep, n_c);
+    for (int i = tid; i < n_c; i += TREE_THREADS) {
+      const int c = s_order[i];
+      s_rank[c] = s_dep[c] >= 0 ? i : INT32_MAX;
+    }
     n_sel = min(m, s_count);
-    for (int c = tid >> 5; c < n_c; c += TREE_WARPS) {
-      const int rk = s_rank[c];
-      if (rk >= n_sel) continue;               // the same for the whole warp
-      const int dc = s_dep[c];
-      int cnt = 0;
-      for (int o = lane; o < n_c; o += 32) {
-        const int ro = s_rank[o];
-        if (ro < n_sel && (s_dep[o] < dc || (s_dep[o] == dc && ro < rk))) ++cnt;
+    // slots of the kept ones, s_order[0, n_sel): by (depth, rank)
+    for (int i = tid; i < n_sel; i += TREE_THREADS) {
+      const int c = s_order[i], dc = s_dep[c];
+      int pos = 0;
+      for (int j = 0; j < n_sel; ++j) {
+        const int dj = s_dep[s_order[j]];
+        if (dj < dc || (dj == dc && j < i)) ++pos;
       }
-      const int pos = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt)));
-      if (lane == 0) s_slot[c] = 1 + pos;
+      s_slot[c] = 1 + pos;
     }
     __syncthreads();
     for (int c = tid; c < n_c; c += TREE_THREADS) {
