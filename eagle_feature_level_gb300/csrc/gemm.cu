@@ -510,7 +510,6 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
   const int blk = p.n * BM;            // one CTA's partial of the tile: n rows
   const float* part = p.part + static_cast<size_t>(t + c_first) * blk;
   float* const xch = s.xch;            // in registers (see epilogue_chunk)
-  float* const stg = s.stg;
   if (area != nullptr && cap >= 2 * blk) {
     float* acc = area;
     float* stage = area + blk;
@@ -546,26 +545,24 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
   for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
     const int nj = min(XCH_ROWS, p.n - jc);
     // 1. partials of the contributing CTAs (each one contiguous block of nj
-    //    rows), as many CTAs per batch as the staging area holds; summed in
-    //    CTA order
-    const int cb = max(1, XCH_ROWS / nj);
-#pragma unroll 1
-    for (int c0 = 0; c0 < C; c0 += cb) {
-      const int cn = min(cb, C - c0);
-#pragma unroll 1
-      for (int c = 0; c < cn; ++c)
-        stage_block(stg + c * nj * BM, part + static_cast<size_t>(c0 + c) * blk + jc * BM, nj * BM, et);
-      cp_async_wait_all();
-      sm100::named_barrier(1, EPI_THREADS);
-#pragma unroll 1
-      for (int jj = 0; jj < nj; ++jj) {
-        float a = c0 == 0 ? stg[jj * BM + m] : xch[jj * BM + m] + stg[jj * BM + m];
-#pragma unroll 1
-        for (int c = 1; c < cn; ++c) a += stg[(c * nj + jj) * BM + m];
-        xch[jj * BM + m] = a;
-      }
-      sm100::named_barrier(1, EPI_THREADS);
+    //    rows), read straight from L2 four CTAs at a time (64 independent
+    //    loads in flight per thread, where staging them CTA by CTA cost one
+    //    round trip and a barrier each) and summed in CTA order
+    const float* src = part + static_cast<size_t>(jc) * BM + m;
+    float a[XCH_ROWS];
+#pragma unroll
+    for (int jj = 0; jj < XCH_ROWS; ++jj) a[jj] = jj < nj ? __ldcg(src + jj * BM) : 0.f;
+#pragma unroll 4
+    for (int c = 1; c < C; ++c) {
+      const float* sc = src + static_cast<size_t>(c) * blk;
+#pragma unroll
+      for (int jj = 0; jj < XCH_ROWS; ++jj)
+        if (jj < nj) a[jj] += __ldcg(sc + jj * BM);
     }
+#pragma unroll
+    for (int jj = 0; jj < XCH_ROWS; ++jj)
+      if (jj < nj) xch[jj * BM + m] = a[jj];
+    sm100::named_barrier(1, EPI_THREADS);
     epilogue_chunk(p, s, col, t, jc, nj, m, jc == 0);   // chunk 0's row inputs were staged early
   }
 }
