@@ -46,8 +46,11 @@ constexpr int BK = 64;                     // elements per k-block (one 128-byte
 constexpr int KBLK_BYTES = BK * 2;
 constexpr int NUM_THREADS = 192;
 constexpr int EPI_THREADS = 128;
-constexpr int XCH_ROWS = 16;
-constexpr int STG_FLOATS = XCH_ROWS * BM;   // finalize staging: 16 rows of a tile
+// Activation rows per epilogue chunk: 16, or 32 when a launch has more than
+// 16 rows (each chunk's row inputs and split partials cost a round trip to
+// L2, which the finalizing CTA waits for; the smaller chunk keeps the shared
+// memory of few-row launches as it was).
+constexpr int XCH_MAX = 32;
 
 struct GemmParams {
   int epi;
@@ -58,6 +61,7 @@ struct GemmParams {
   int two_mma;
   int tmem_cols, acc_stride, n_acc, stages;
   int kps;                  // k-blocks per stage
+  int xr;                   // activation rows per epilogue chunk (16 or XCH_MAX)
   uint32_t a_stage_bytes, b_stage_bytes;
   int full_rows[3];         // rows of each matrix in whole 8-row groups
   int full_kb;              // whole 64-wide k-blocks of K
@@ -102,19 +106,18 @@ struct Smem {
   uint64_t* tempty; // [2]
   uint32_t* tmem_holder;
   int* flags;       // [0] abort, [1] last-arriver, [2] wait ok
-  float* xch;       // [32][128]
+  float* xch;       // [xr][128]
   float* red;       // [4][32]
   float* rs;        // [32]
-  int* rowi;        // [32]
-  float* stg;       // [STG_FLOATS], 16-byte aligned: partial tiles of other CTAs
-  float* stg2;      // [STG_FLOATS]: the tile's row inputs from earlier kernels
+  int* rowi;        // [2 * XCH_MAX]
+  float* stg2;      // [xr][128], 16-byte aligned: the tile's row inputs from earlier kernels
 };
 
-__host__ __device__ inline size_t smem_bytes_for(int stages, uint32_t a_stage, uint32_t b_stage) {
+__host__ __device__ inline size_t smem_bytes_for(int stages, uint32_t a_stage, uint32_t b_stage, int xr) {
   size_t s = 1024;                                  // alignment slack
   s += static_cast<size_t>(stages) * (a_stage + b_stage);
   s += (2 * stages + 4) * 8 + 64;
-  s += XCH_ROWS * BM * 4 + 4 * 32 * 4 + 32 * 4 + 32 * 4 + 2 * STG_FLOATS * 4;
+  s += static_cast<size_t>(xr) * BM * 4 + 4 * 32 * 4 + 32 * 4 + 2 * XCH_MAX * 4 + static_cast<size_t>(xr) * BM * 4;
   return s;
 }
 
@@ -133,11 +136,10 @@ __device__ inline Smem carve(uint8_t* raw, const GemmParams& p) {
   s.tmem_holder = reinterpret_cast<uint32_t*>(s.tempty + 2);
   s.flags = reinterpret_cast<int*>(s.tmem_holder + 4);
   s.xch = reinterpret_cast<float*>(s.flags + 12);
-  s.red = s.xch + XCH_ROWS * BM;
+  s.red = s.xch + p.xr * BM;
   s.rs = s.red + 4 * 32;
   s.rowi = reinterpret_cast<int*>(s.rs + 32);
-  s.stg = reinterpret_cast<float*>(s.rowi + 32);
-  s.stg2 = s.stg + STG_FLOATS;
+  s.stg2 = reinterpret_cast<float*>(s.rowi + 2 * XCH_MAX);
   return s;
 }
 
@@ -319,7 +321,7 @@ __device__ __noinline__ void stage_row_inputs(const GemmParams& p, const Smem& s
       const int len = p.kv_len[b], a = min(max(p.n_act[b], 0), p.rpr);
       const bool room = len >= 0 && len + a <= p.kv_cap_rows;
       s.rowi[m] = p.pos0[b] + i;
-      s.rowi[XCH_ROWS + m] = (i <= a && room) ? len + i - 1 : -1;
+      s.rowi[XCH_MAX + m] = (i <= a && room) ? len + i - 1 : -1;
     }
   }
 }
@@ -429,7 +431,7 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
       const int rpr = p.rpr, Hkv = p.Hkv, dh = p.dh, cap = p.kv_cap_rows;
 #pragma unroll 1
       for (int jj = 0; jj < nj; ++jj) {
-        const int row = rowi[XCH_ROWS + jj];
+        const int row = rowi[XCH_MAX + jj];
         if (row < 0) continue;                 // inactive row, or the cache cannot take the request's rows
         const int b = (jc + jj) / rpr;
         const float sc = rs[jj];
@@ -495,14 +497,13 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
 // apply the contraction's fused elementwise work.  `m` is the tile row this
 // thread owns (its tensor-memory lane).  It runs once per tile, cold, at the
 // end of the stream, so its chain of memory latencies is on the kernel's
-// critical path: the partials are brought into shared memory by
-// asynchronous copies issued from compact loops (many in flight, one wait),
-// then the per-row loops read shared memory only.  `area` (cap floats,
-// 16-byte aligned) is the idle pipeline ring when this is the CTA's last
-// tile, else null: the partials of all rows then arrive several CTAs per
-// batch; otherwise they come 16 rows x one CTA at a time through s.stg.
-// Either way every element is summed in CTA order (deterministic, and the
-// same order on both routes).
+// critical path.  `area` (cap floats, 16-byte aligned) is the idle pipeline
+// ring when this is the CTA's last tile, else null: the partials of all rows
+// then arrive several CTAs per batch by asynchronous copies issued from
+// compact loops (many in flight, one wait); otherwise each chunk of xr rows
+// is loaded straight from L2, 16 rows x four CTAs' loads in flight at a time.  Either
+// way every element is summed in CTA order (deterministic, and the same
+// order on both routes).
 __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, const EpiCol& col, int t,
                                            int c_first, int c_last, int m, float* area, int cap) {
   const int et = m;                    // epilogue thread index == tile row
@@ -533,8 +534,8 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
       }
       sm100::named_barrier(1, EPI_THREADS);
     }
-    for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
-      const int nj = min(XCH_ROWS, p.n - jc);
+    for (int jc = 0; jc < p.n; jc += p.xr) {
+      const int nj = min(p.xr, p.n - jc);
 #pragma unroll 1
       for (int jj = 0; jj < nj; ++jj) xch[jj * BM + m] = acc[(jc + jj) * BM + m];
       sm100::named_barrier(1, EPI_THREADS);
@@ -542,26 +543,30 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
     }
     return;
   }
-  for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
-    const int nj = min(XCH_ROWS, p.n - jc);
+  for (int jc = 0; jc < p.n; jc += p.xr) {
+    const int nj = min(p.xr, p.n - jc);
     // 1. partials of the contributing CTAs (each one contiguous block of nj
-    //    rows), read straight from L2 four CTAs at a time (64 independent
-    //    loads in flight per thread, where staging them CTA by CTA cost one
-    //    round trip and a barrier each) and summed in CTA order
-    const float* src = part + static_cast<size_t>(jc) * BM + m;
-    float a[XCH_ROWS];
+    //    rows), read straight from L2 16 rows x four CTAs at a time (64
+    //    independent loads in flight per thread, where staging them CTA by
+    //    CTA cost one round trip and a barrier each) and summed in CTA order
+#pragma unroll 1
+    for (int h = 0; h < nj; h += 16) {
+      const int nh = min(16, nj - h);
+      const float* src = part + static_cast<size_t>(jc + h) * BM + m;
+      float a[16];
 #pragma unroll
-    for (int jj = 0; jj < XCH_ROWS; ++jj) a[jj] = jj < nj ? __ldcg(src + jj * BM) : 0.f;
+      for (int jj = 0; jj < 16; ++jj) a[jj] = jj < nh ? __ldcg(src + jj * BM) : 0.f;
 #pragma unroll 4
-    for (int c = 1; c < C; ++c) {
-      const float* sc = src + static_cast<size_t>(c) * blk;
+      for (int c = 1; c < C; ++c) {
+        const float* sc = src + static_cast<size_t>(c) * blk;
 #pragma unroll
-      for (int jj = 0; jj < XCH_ROWS; ++jj)
-        if (jj < nj) a[jj] += __ldcg(sc + jj * BM);
+        for (int jj = 0; jj < 16; ++jj)
+          if (jj < nh) a[jj] += __ldcg(sc + jj * BM);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj)
+        if (jj < nh) xch[(h + jj) * BM + m] = a[jj];
     }
-#pragma unroll
-    for (int jj = 0; jj < XCH_ROWS; ++jj)
-      if (jj < nj) xch[jj * BM + m] = a[jj];
     sm100::named_barrier(1, EPI_THREADS);
     epilogue_chunk(p, s, col, t, jc, nj, m, jc == 0);   // chunk 0's row inputs were staged early
   }
@@ -833,7 +838,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
       const EpiCol col = epi_column(p, t, m);
       cp_async_wait_all();                      // the previous segment's copies into s.stg2 have landed
       sm100::named_barrier(1, EPI_THREADS);
-      stage_row_inputs(p, s, t, 0, min(XCH_ROWS, p.n), m);
+      stage_row_inputs(p, s, t, 0, min(p.xr, p.n), m);
       if (et == 0) s.flags[2] = sm100::mbar_wait(&s.tfull[buf], aph, abort_flag) ? 1 : 0;
       sm100::named_barrier(1, EPI_THREADS);
       if (!s.flags[2]) {
@@ -854,8 +859,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
       }
       if (c_first == c_last) {
         // the whole tile is this CTA's: epilogue straight from tensor memory
-        for (int jc = 0; jc < p.n; jc += XCH_ROWS) {
-          const int nj = min(XCH_ROWS, p.n - jc);
+        for (int jc = 0; jc < p.n; jc += p.xr) {
+          const int nj = min(p.xr, p.n - jc);
           for (int c0 = 0; c0 < nj; c0 += 8) {
             float hi[8], lo[8];
             sm100::tmem_ld8(lane_addr + jc + c0, hi);
@@ -1056,6 +1061,7 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   p.two_mma = 2 * p.NP > 256 ? 1 : 0;
   for (int i = 0; i < 3; ++i) p.full_rows[i] = i < p.n_mats ? rows[i] / 8 * 8 : 0;
   p.full_kb = K / BK;
+  p.xr = p.n > 16 ? XCH_MAX : 16;
   const int acc_cols = 2 * p.NP;
   p.acc_stride = acc_cols < 32 ? 32 : (acc_cols + 31) / 32 * 32;
   p.n_acc = 2 * p.acc_stride <= 512 ? 2 : 1;
@@ -1070,20 +1076,20 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   // The others keep one CTA per SM (whole tiles of their own at the end).
   const size_t half_cap = static_cast<size_t>(113) * 1024;
   const int per_sm = p.m_tiles < ctx->sm_count && cols <= 256 &&
-                     smem_bytes_for(2, BM * KBLK_BYTES, 2 * p.NP * KBLK_BYTES) <= half_cap ? 2 : 1;
+                     smem_bytes_for(2, BM * KBLK_BYTES, 2 * p.NP * KBLK_BYTES, p.xr) <= half_cap ? 2 : 1;
   const size_t smem_cap = per_sm == 2 ? half_cap : 232448;
   const int min_ring = per_sm == 2 ? 2 : 3;
   // two k-blocks per stage while that still leaves a ring of min_ring stages
-  p.kps = smem_bytes_for(min_ring, BM * KBLK_BYTES * 2, 2 * p.NP * KBLK_BYTES * 2) <= smem_cap ? 2 : 1;
+  p.kps = smem_bytes_for(min_ring, BM * KBLK_BYTES * 2, 2 * p.NP * KBLK_BYTES * 2, p.xr) <= smem_cap ? 2 : 1;
   p.a_stage_bytes = static_cast<uint32_t>(BM * KBLK_BYTES * p.kps);
   p.b_stage_bytes = static_cast<uint32_t>(2 * p.NP * KBLK_BYTES * p.kps);
   p.kb = ceil_div(K, BK * p.kps);
   p.total_units = static_cast<long long>(p.m_tiles) * p.kb;
 
   int stages = 8;
-  while (stages > 2 && smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes) > smem_cap) --stages;
+  while (stages > 2 && smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes, p.xr) > smem_cap) --stages;
   p.stages = stages;
-  size_t smem = smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes);
+  size_t smem = smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes, p.xr);
   if (smem > smem_cap) return cudaErrorInvalidConfiguration;
   if (per_sm == 1 && smem < 120 * 1024) smem = 120 * 1024;    // keeps one CTA per SM
 
