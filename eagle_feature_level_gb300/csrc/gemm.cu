@@ -327,11 +327,12 @@ __device__ __noinline__ void stage_row_inputs(const GemmParams& p, const Smem& s
 }
 
 // Steps 2-3 of a tile's epilogue for rows jc .. jc + nj - 1, whose summed
-// accumulators are in s.xch: stage the rows' inputs written by earlier
-// kernels, then the contraction's elementwise work.  Ends with the epilogue
-// warps synchronised.
+// accumulators are in s.xch: wait for the rows' inputs written by earlier
+// kernels (the caller has issued their copies into s.stg2), then the
+// contraction's elementwise work.  Ends with the epilogue warps
+// synchronised.
 __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, const EpiCol& col, int t, int jc,
-                                            int nj, int m, bool prestaged) {
+                                            int nj, int m) {
   // the shared rows' pointers in registers: the loops' global stores could
   // otherwise alias the Smem fields, forcing a re-read per row
   float* const xch = s.xch;
@@ -344,7 +345,6 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
   const float f_hi = col.f_hi, f_lo = col.f_lo, col_bias = col.col_bias, col_gain = col.col_gain;
   // 2. row inputs written by earlier kernels (staged in s.stg2)
   const int tiles = p.ss_in_tiles;
-  if (!prestaged) stage_row_inputs(p, s, t, jc, nj, m);
   cp_async_wait_all();
   sm100::named_barrier(1, EPI_THREADS);
   if ((p.epi == EPI_O || p.epi == EPI_DOWN) && d_col) {
@@ -536,15 +536,19 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
     }
     for (int jc = 0; jc < p.n; jc += p.xr) {
       const int nj = min(p.xr, p.n - jc);
+      if (jc > 0) stage_row_inputs(p, s, t, jc, nj, m);   // chunk 0's row inputs were staged early
 #pragma unroll 1
       for (int jj = 0; jj < nj; ++jj) xch[jj * BM + m] = acc[(jc + jj) * BM + m];
       sm100::named_barrier(1, EPI_THREADS);
-      epilogue_chunk(p, s, col, t, jc, nj, m, jc == 0);   // chunk 0's row inputs were staged early
+      epilogue_chunk(p, s, col, t, jc, nj, m);
     }
     return;
   }
   for (int jc = 0; jc < p.n; jc += p.xr) {
     const int nj = min(p.xr, p.n - jc);
+    // 0. the chunk's row inputs, by asynchronous copies that land while the
+    //    partials below are read (chunk 0's were staged early)
+    if (jc > 0) stage_row_inputs(p, s, t, jc, nj, m);
     // 1. partials of the contributing CTAs (each one contiguous block of nj
     //    rows), read straight from L2 16 rows x four CTAs at a time (64
     //    independent loads in flight per thread, where staging them CTA by
@@ -568,7 +572,7 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
         if (jj < nh) xch[(h + jj) * BM + m] = a[jj];
     }
     sm100::named_barrier(1, EPI_THREADS);
-    epilogue_chunk(p, s, col, t, jc, nj, m, jc == 0);   // chunk 0's row inputs were staged early
+    epilogue_chunk(p, s, col, t, jc, nj, m);
   }
 }
 
@@ -861,6 +865,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
         // the whole tile is this CTA's: epilogue straight from tensor memory
         for (int jc = 0; jc < p.n; jc += p.xr) {
           const int nj = min(p.xr, p.n - jc);
+          // this chunk's row inputs stream in while its accumulators are read
+          // (chunk 0's were staged before the accumulators were ready)
+          if (jc > 0) stage_row_inputs(p, s, t, jc, nj, m);
           for (int c0 = 0; c0 < nj; c0 += 8) {
             float hi[8], lo[8];
             sm100::tmem_ld8(lane_addr + jc + c0, hi);
@@ -871,7 +878,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
               if (c0 + i < nj) s.xch[(c0 + i) * BM + m] = hi[i] + lo[i];
           }
           sm100::named_barrier(1, EPI_THREADS);
-          epilogue_chunk(p, s, col, t, jc, nj, m, jc == 0);
+          epilogue_chunk(p, s, col, t, jc, nj, m);
         }
         sm100::tc_fence_before();
         __syncwarp();
