@@ -498,10 +498,12 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
 // thread owns (its tensor-memory lane).  It runs once per tile, cold, at the
 // end of the stream, so its chain of memory latencies is on the kernel's
 // critical path.  `area` (cap floats, 16-byte aligned) is the idle pipeline
-// ring when this is the CTA's last tile, else null: the partials of all rows
-// then arrive several CTAs per batch by asynchronous copies issued from
-// compact loops (many in flight, one wait); otherwise each chunk of xr rows
-// is loaded straight from L2, 16 rows x four CTAs' loads in flight at a time.  Either
+// ring when this is the CTA's last tile, else null: when every contributor's
+// partial fits in it beside their sum, the partials of all rows arrive in
+// one batch of asynchronous copies issued from compact loops (many in
+// flight, one wait); otherwise each chunk of xr rows is loaded straight from
+// L2, 16 rows x four CTAs' loads in flight at a time (staging one
+// contributor's 160 rows at a time through the ring took ~7 us a batch).  Either
 // way every element is summed in CTA order (deterministic, and the same
 // order on both routes).
 __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, const EpiCol& col, int t,
@@ -511,7 +513,7 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
   const int blk = p.n * BM;            // one CTA's partial of the tile: n rows
   const float* part = p.part + static_cast<size_t>(t + c_first) * blk;
   float* const xch = s.xch;            // in registers (see epilogue_chunk)
-  if (area != nullptr && cap >= 2 * blk) {
+  if (area != nullptr && cap - blk >= C * blk) {   // every contributor's partial in one batch
     float* acc = area;
     float* stage = area + blk;
     const int cb = min(C, (cap - blk) / blk);
