@@ -192,6 +192,15 @@ __device__ __forceinline__ int arrive_acq_rel(int* counter) {
   return prev;
 }
 
+// A counter's value with acquire semantics at GPU scope: once it shows every
+// arrival, the stores the arrivals released are visible to this thread (and,
+// after a CTA barrier, to the rest of its CTA).
+__device__ __forceinline__ int ld_acquire(const int* counter) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+  return v;
+}
+
 // ---- device status word -----------------------------------------------------
 // First int of the workspace.  The first error wins; later ones are dropped.
 __device__ __forceinline__ void set_status(int* status, int code) {

@@ -62,6 +62,7 @@ struct GemmParams {
   int tmem_cols, acc_stride, n_acc, stages;
   int kps;                  // k-blocks per stage
   int xr;                   // activation rows per epilogue chunk (16 or XCH_MAX)
+  int coop;                 // every CTA resident at once: split tiles finalized by all their contributors
   uint32_t a_stage_bytes, b_stage_bytes;
   int full_rows[3];         // rows of each matrix in whole 8-row groups
   int full_kb;              // whole 64-wide k-blocks of K
@@ -578,6 +579,43 @@ __device__ __noinline__ void finalize_tile(const GemmParams& p, const Smem& s, c
   }
 }
 
+// Cooperative final epilogue of split tile t (p.coop): every one of its C
+// contributors, once all C partials are written, sums them (in CTA order, as
+// finalize_tile does) for its own share [r0, r1) of the activation rows and
+// runs the fused elementwise work on those rows, so the tile's epilogue is
+// spread over its C CTAs instead of waiting on one.  Rows below xr were
+// staged at the segment's start.
+__device__ __noinline__ void finalize_rows(const GemmParams& p, const Smem& s, const EpiCol& col, int t,
+                                           int c_first, int C, int m, int r0, int r1) {
+  const int blk = p.n * BM;
+  const float* part = p.part + static_cast<size_t>(t + c_first) * blk;
+  float* const xch = s.xch;
+  for (int jc = r0; jc < r1; jc += p.xr) {
+    const int nj = min(p.xr, r1 - jc);
+    if (jc > 0) stage_row_inputs(p, s, t, jc, nj, m);
+#pragma unroll 1
+    for (int h = 0; h < nj; h += 16) {
+      const int nh = min(16, nj - h);
+      const float* src = part + static_cast<size_t>(jc + h) * BM + m;
+      float a[16];
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) a[jj] = jj < nh ? __ldcg(src + jj * BM) : 0.f;
+#pragma unroll 4
+      for (int c = 1; c < C; ++c) {
+        const float* sc = src + static_cast<size_t>(c) * blk;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          if (jj < nh) a[jj] += __ldcg(sc + jj * BM);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj)
+        if (jj < nh) xch[(h + jj) * BM + m] = a[jj];
+    }
+    sm100::named_barrier(1, EPI_THREADS);
+    epilogue_chunk(p, s, col, t, jc, nj, m);
+  }
+}
+
 // Tensor maps of one launch: the (up to three) weight matrices as 4-D
 // grouped maps, their 2-D tail maps, and the activation operand.
 struct GemmMaps {
@@ -903,6 +941,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
       __syncwarp();
       if (lane == 0) sm100::mbar_arrive(&s.tempty[buf]);
       sm100::named_barrier(1, EPI_THREADS);     // every epilogue thread's partial stores come first
+      if (p.coop) {
+        // The contributors for which tile t is their last segment wait for
+        // every partial, then finalize a share of its activation rows each;
+        // the one whose work continues past the tile (the last contributor,
+        // unless it stops inside it) only arrives.  The counter counts C
+        // arrivals, then the W waiters' departures; the last one resets it.
+        const int C = c_last - c_first + 1;
+        const long long end_last = static_cast<long long>(c_last + 1) * U_sk / G;   // c_last's share ends here
+        const int lastw = end_last <= static_cast<long long>(t + 1) * p.kb ? c_last : c_last - 1;
+        const int W = lastw - c_first + 1;
+        if (cta > lastw) {
+          if (et == 0) arrive_acq_rel(&p.counters[t]);
+          continue;
+        }
+        if (et == 0) {
+          arrive_acq_rel(&p.counters[t]);
+          const uint64_t w0 = globaltimer_ns();
+          int ok = 1;
+          while (ld_acquire(&p.counters[t]) < C) {
+            if (*abort_flag || globaltimer_ns() - w0 > WAIT_LIMIT_NS) {
+              ok = 0;
+              break;
+            }
+            __nanosleep(64);
+          }
+          s.flags[1] = ok;
+        }
+        sm100::named_barrier(1, EPI_THREADS);
+        if (!s.flags[1]) {
+          if (et == 0) {
+            *abort_flag = 1;
+            set_status(p.status, EAGLE_ERR_TIMEOUT);
+          }
+          cp_async_wait_all();
+          break;
+        }
+        const int ci = cta - c_first;
+        const int r0 = static_cast<int>(static_cast<long long>(ci) * p.n / W);
+        const int r1 = static_cast<int>(static_cast<long long>(ci + 1) * p.n / W);
+        if (r0 < r1) finalize_rows(p, s, col, t, c_first, C, m, r0, r1);
+        sm100::named_barrier(1, EPI_THREADS);
+        if (et == 0 && arrive_acq_rel(&p.counters[t]) == C + W - 1) p.counters[t] = 0;
+        continue;
+      }
       if (et == 0) {
         const int prev = arrive_acq_rel(&p.counters[t]);
         const int last = prev == c_last - c_first;
@@ -1121,6 +1203,15 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   // the remaining tiles are split stream-K and processed first
   p.dp_waves = p.m_tiles / grid;
   p.sk_tiles = p.m_tiles - p.dp_waves * grid;
+  // the split tiles' contributors wait for one another only when every tile
+  // is split (no data-parallel tiles follow a CTA's split ones) and the whole
+  // grid is resident at once; else the last arriver finalizes alone
+  {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, gemm_stream_kernel, NUM_THREADS, smem) != cudaSuccess)
+      occ = 0;
+    p.coop = p.dp_waves == 0 && occ >= per_sm && grid <= occ * ctx->sm_count ? 1 : 0;
+  }
   // partial slots t + cta of split tiles stay inside the workspace's array
   if (p.sk_tiles > 0 && p.sk_tiles - 1 + grid - 1 >= W.max_mtiles + 2 * ctx->sm_count)
     return cudaErrorInvalidConfiguration;
