@@ -111,14 +111,16 @@ struct Smem {
   float* red;       // [4][32]
   float* rs;        // [32]
   int* rowi;        // [2 * XCH_MAX]
-  float* stg2;      // [xr][128], 16-byte aligned: the tile's row inputs from earlier kernels
+  float* stg2;      // [xr][sw], 16-byte aligned: the tile's row inputs from earlier kernels (last)
 };
 
-__host__ __device__ inline size_t smem_bytes_for(int stages, uint32_t a_stage, uint32_t b_stage, int xr) {
+// sw: floats per staged row input (BM residual columns, or a row's norm
+// partials at a stride of ss_in_tiles + 1), so s.stg2 holds xr * sw floats.
+__host__ __device__ inline size_t smem_bytes_for(int stages, uint32_t a_stage, uint32_t b_stage, int xr, int sw) {
   size_t s = 1024;                                  // alignment slack
   s += static_cast<size_t>(stages) * (a_stage + b_stage);
   s += (2 * stages + 4) * 8 + 64;
-  s += static_cast<size_t>(xr) * BM * 4 + 4 * 32 * 4 + 32 * 4 + 2 * XCH_MAX * 4 + static_cast<size_t>(xr) * BM * 4;
+  s += static_cast<size_t>(xr) * BM * 4 + 4 * 32 * 4 + 32 * 4 + 2 * XCH_MAX * 4 + static_cast<size_t>(xr) * sw * 4;
   return s;
 }
 
@@ -305,11 +307,14 @@ __device__ __noinline__ void stage_row_inputs(const GemmParams& p, const Smem& s
       if (q < ncol) cp_async16(s.stg2 + r * BM + q, p.resid + static_cast<size_t>(jc + r) * p.d + t * BM + q);
     }
   } else if (p.epi == EPI_QKV || p.epi == EPI_GATEUP || p.epi == EPI_KV) {   // norm partials of rows jc..jc+nj-1
+    // row r at stg2 + r * (tiles + 1): with a stride one longer than the
+    // row, the threads summing one row each no longer share a bank
     const float* ss = p.ss_in + static_cast<size_t>(jc) * tiles;
-    if (tiles % 4 == 0) {
-      stage_block(s.stg2, ss, nj * tiles, et);
-    } else {
-      for (int i = et; i < nj * tiles; i += EPI_THREADS) s.stg2[i] = __ldcg(ss + i);
+    const int n = nj * tiles;
+#pragma unroll 4
+    for (int i = et; i < n; i += EPI_THREADS) {
+      const int r = i / tiles;
+      s.stg2[i + r] = __ldcg(ss + i);
     }
     if (p.epi == EPI_QKV && m < nj) {
       const int j = jc + m, b = j / p.rpr, e = p.e0 + j % p.rpr;
@@ -353,7 +358,7 @@ __device__ __noinline__ void epilogue_chunk(const GemmParams& p, const Smem& s, 
     for (int jj = 0; jj < nj; ++jj) xch[jj * BM + m] += stg2[jj * BM + m];
   }
   if ((p.epi == EPI_QKV || p.epi == EPI_GATEUP || p.epi == EPI_KV) && m < nj) {   // RMSNorm scale of input row jc + m
-    const float* ss = stg2 + m * tiles;
+    const float* ss = stg2 + m * (tiles + 1);
     float acc4[4] = {0.f, 0.f, 0.f, 0.f};
     int i = 0;
 #pragma unroll 1
@@ -1153,6 +1158,7 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   for (int i = 0; i < 3; ++i) p.full_rows[i] = i < p.n_mats ? rows[i] / 8 * 8 : 0;
   p.full_kb = K / BK;
   p.xr = p.n > 16 ? XCH_MAX : 16;
+  const int sw = p.ss_in_tiles + 1 > BM ? p.ss_in_tiles + 1 : BM;
   const int acc_cols = 2 * p.NP;
   p.acc_stride = acc_cols < 32 ? 32 : (acc_cols + 31) / 32 * 32;
   p.n_acc = 2 * p.acc_stride <= 512 ? 2 : 1;
@@ -1167,20 +1173,20 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   // The others keep one CTA per SM (whole tiles of their own at the end).
   const size_t half_cap = static_cast<size_t>(113) * 1024;
   const int per_sm = p.m_tiles < ctx->sm_count && cols <= 256 &&
-                     smem_bytes_for(2, BM * KBLK_BYTES, 2 * p.NP * KBLK_BYTES, p.xr) <= half_cap ? 2 : 1;
+                     smem_bytes_for(2, BM * KBLK_BYTES, 2 * p.NP * KBLK_BYTES, p.xr, sw) <= half_cap ? 2 : 1;
   const size_t smem_cap = per_sm == 2 ? half_cap : 232448;
   const int min_ring = per_sm == 2 ? 2 : 3;
   // two k-blocks per stage while that still leaves a ring of min_ring stages
-  p.kps = smem_bytes_for(min_ring, BM * KBLK_BYTES * 2, 2 * p.NP * KBLK_BYTES * 2, p.xr) <= smem_cap ? 2 : 1;
+  p.kps = smem_bytes_for(min_ring, BM * KBLK_BYTES * 2, 2 * p.NP * KBLK_BYTES * 2, p.xr, sw) <= smem_cap ? 2 : 1;
   p.a_stage_bytes = static_cast<uint32_t>(BM * KBLK_BYTES * p.kps);
   p.b_stage_bytes = static_cast<uint32_t>(2 * p.NP * KBLK_BYTES * p.kps);
   p.kb = ceil_div(K, BK * p.kps);
   p.total_units = static_cast<long long>(p.m_tiles) * p.kb;
 
   int stages = 8;
-  while (stages > 2 && smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes, p.xr) > smem_cap) --stages;
+  while (stages > 2 && smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes, p.xr, sw) > smem_cap) --stages;
   p.stages = stages;
-  size_t smem = smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes, p.xr);
+  size_t smem = smem_bytes_for(stages, p.a_stage_bytes, p.b_stage_bytes, p.xr, sw);
   if (smem > smem_cap) return cudaErrorInvalidConfiguration;
   if (per_sm == 1 && smem < 120 * 1024) smem = 120 * 1024;    // keeps one CTA per SM
 
