@@ -906,6 +906,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
         c_first = cta_of_unit(static_cast<long long>(t) * p.kb, U_sk, G);
         c_last = cta_of_unit(static_cast<long long>(t) * p.kb + p.kb - 1, U_sk, G);
       }
+      if (c_first == c_last && p.n_acc == 1 && t >= p.sk_tiles && t + G < p.m_tiles) {
+        // the whole tile is this CTA's and its only accumulator is wanted by
+        // the CTA's next tile: the summed accumulator goes to this CTA's own
+        // slot in global memory at once, freeing tensor memory for the next
+        // tile's MMAs while the epilogue runs from the slot
+        const int slot = p.sk_tiles + G + cta;
+        for (int c0 = 0; c0 < p.NP; c0 += 8) {
+          float hi[8], lo[8];
+          sm100::tmem_ld8(lane_addr + c0, hi);
+          sm100::tmem_ld8(lane_addr + p.NP + c0, lo);
+          sm100::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int j = c0 + i;
+            if (j < p.n) p.part[(static_cast<size_t>(slot) * p.n + j) * BM + m] = hi[i] + lo[i];
+          }
+        }
+        sm100::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) sm100::mbar_arrive(&s.tempty[buf]);
+        // each thread reads back only what it wrote (its tile row m)
+        finalize_rows(p, s, col, t, slot - t, 1, m, 0, p.n);
+        sm100::named_barrier(1, EPI_THREADS);
+        continue;
+      }
       if (c_first == c_last) {
         // the whole tile is this CTA's: epilogue straight from tensor memory
         for (int jc = 0; jc < p.n; jc += p.xr) {
@@ -1218,8 +1243,12 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
       occ = 0;
     p.coop = p.dp_waves == 0 && occ >= per_sm && grid <= occ * ctx->sm_count ? 1 : 0;
   }
-  // partial slots t + cta of split tiles stay inside the workspace's array
+  // partial slots t + cta of split tiles, and sk_tiles + grid + cta of the
+  // own tiles' accumulators (one accumulator, more than one own tile), stay
+  // inside the workspace's array
   if (p.sk_tiles > 0 && p.sk_tiles - 1 + grid - 1 >= W.max_mtiles + 2 * ctx->sm_count)
+    return cudaErrorInvalidConfiguration;
+  if (p.n_acc == 1 && p.dp_waves > 1 && p.sk_tiles + 2 * grid - 1 >= W.max_mtiles + 2 * ctx->sm_count)
     return cudaErrorInvalidConfiguration;
   const int kid = epi == EPI_KV ? static_cast<int>(EAGLE_K_REFRESH)
                                  : (epi == EPI_FUSE ? static_cast<int>(EAGLE_K_FUSE) : epi);
