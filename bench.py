@@ -40,9 +40,9 @@ ALPHA = (0.9, 0.7, 0.6, 0.6, 0.6, 0.6)   # injected per-layer acceptance profile
 # DRAM bytes (read + write) per gemm_stream_kernel launch at 7b_static26,
 # averaged over the 30 launches of one round in one ncu capture.  Reported
 # only while the kernel's sources hash to the ones the counters were taken on.
-GEMM_TRAFFIC = {"workload": "7b_static26", "bytes_per_launch": 125034121,
+GEMM_TRAFFIC = {"workload": "7b_static26", "bytes_per_launch": 125024973,
                 "sources": ("gemm.cu", "sm100.cuh", "common.cuh"),
-                "sha256": "47f99e00e489a134f4d56b75f2956ed5a6b44b54d553f0da45be29cd3b99da18"}
+                "sha256": "3bdfe7af88a96425057dc423236863e94aedc6d8e782fe95ffce6d7c08bf60f8"}
 
 
 def gemm_traffic(workload: str):
