@@ -68,6 +68,7 @@ struct GemmParams {
   int full_kb;              // whole 64-wide k-blocks of K
   int sk_tiles;             // tiles [0, sk_tiles) split stream-K over all CTAs (processed first)
   int dp_waves;             // then tiles sk_tiles + c + i * grid, i < dp_waves, owned by CTA c alone
+  int sk_whole;             // fewer stream-K units than CTAs: tile c < sk_tiles whole to CTA c
   int rpr, e0, E;
   int d, F, V, Hq, Hkv, dh;
   float eps;
@@ -193,6 +194,13 @@ __device__ __forceinline__ CtaWork cta_work(const GemmParams& p) {
   wk.cta = blockIdx.x;
   wk.grid = gridDim.x;
   const long long U = static_cast<long long>(p.sk_tiles) * p.kb;
+  if (p.sk_whole) {
+    // an even split would leave CTAs without units, and a tile's
+    // contributors would no longer be every CTA between its first and last
+    wk.sk_begin = wk.cta < p.sk_tiles ? static_cast<long long>(wk.cta) * p.kb : U;
+    wk.sk_end = wk.cta < p.sk_tiles ? static_cast<long long>(wk.cta + 1) * p.kb : U;
+    return wk;
+  }
   wk.sk_begin = static_cast<long long>(wk.cta) * U / wk.grid;
   wk.sk_end = static_cast<long long>(wk.cta + 1) * U / wk.grid;
   return wk;
@@ -902,7 +910,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 2)
       const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                  static_cast<uint32_t>(buf * p.acc_stride);
       int c_first = cta, c_last = cta;
-      if (t < p.sk_tiles) {
+      if (t < p.sk_tiles && !p.sk_whole) {
         c_first = cta_of_unit(static_cast<long long>(t) * p.kb, U_sk, G);
         c_last = cta_of_unit(static_cast<long long>(t) * p.kb + p.kb - 1, U_sk, G);
       }
@@ -1234,6 +1242,7 @@ cudaError_t launch_gemm(eagle_ctx* ctx, int epi, const DraftLaunch& L, cudaStrea
   // the remaining tiles are split stream-K and processed first
   p.dp_waves = p.m_tiles / grid;
   p.sk_tiles = p.m_tiles - p.dp_waves * grid;
+  p.sk_whole = p.sk_tiles > 0 && static_cast<long long>(p.sk_tiles) * p.kb < grid ? 1 : 0;
   // the split tiles' contributors wait for one another only when every tile
   // is split (no data-parallel tiles follow a CTA's split ones) and the whole
   // grid is resident at once; else the last arriver finalizes alone

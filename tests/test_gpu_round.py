@@ -28,6 +28,13 @@ SMALL = {
     "small_rows160_two_mma": S.variant("70b_x16_eagle2", name="small_rows160_two_mma", d=128, n_q_heads=4,
                                        n_kv_heads=2, head_dim=32, d_ff=256, vocab=700, prefix_len=64,
                                        weight_std=0.05),
+    # 160 activation rows against a 19520-wide MLP: one accumulator fits
+    # (2 x 160 columns), gate/up's 305 tiles over 152 CTAs, so CTAs own two
+    # whole tiles after their split share and free the accumulator of the
+    # first before its epilogue
+    "small_mlp_rows160_f19520": S.variant("70b_x16_eagle2", name="small_mlp_rows160_f19520", d=128, n_q_heads=4,
+                                          n_kv_heads=2, head_dim=32, d_ff=19520, vocab=1000, prefix_len=64,
+                                          temps=(0.0,), depth=3, top_m=20, weight_std=0.05),
     # trees past 63 nodes (multi-word ancestor masks): EAGLE-2 pools of 73 and
     # 71 expanded slots (two mask words) with trees of 121 and 256 slots (two
     # and four words), and a 120-node static template
