@@ -35,6 +35,11 @@ SMALL = {
     "small_mlp_rows160_f19520": S.variant("70b_x16_eagle2", name="small_mlp_rows160_f19520", d=128, n_q_heads=4,
                                           n_kv_heads=2, head_dim=32, d_ff=19520, vocab=1000, prefix_len=64,
                                           temps=(0.0,), depth=3, top_m=20, weight_std=0.05),
+    # an odd vocabulary (1001: the selection's unvectorised slice reads, the
+    # LM head's row tail) with greedy and sampled requests mixed
+    "small_eagle2_v1001_mixed": S.variant("70b_x16_eagle2", name="small_eagle2_v1001_mixed", d=128, n_q_heads=4,
+                                          n_kv_heads=2, head_dim=32, d_ff=256, vocab=1001, batch=4,
+                                          prefix_len=80, top_k=4, depth=3, top_m=12, weight_std=0.05),
     # trees past 63 nodes (multi-word ancestor masks): EAGLE-2 pools of 73 and
     # 71 expanded slots (two mask words) with trees of 121 and 256 slots (two
     # and four words), and a 120-node static template
