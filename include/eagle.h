@@ -272,6 +272,11 @@ const char* eagle_status_string(eagle_status s);
  * another warp's hand-off) is bounded: after 2 s it gives up, sets
  * EAGLE_ERR_TIMEOUT in the status word and returns, so a lost arrival ends
  * the launch with an error instead of a hang and the context stays usable.
+ * One wait is on other CTAs of the same launch: when every tile of a
+ * contraction is split and the whole grid fits the GPU at once, a split
+ * tile's contributors wait for one another before sharing its epilogue; a
+ * kernel of another stream that kept enough SMs busy for 2 s while the
+ * grid started would end that launch with EAGLE_ERR_TIMEOUT.
  * This launches one CTA whose only wait, that same bounded wait, is on a
  * barrier nothing arrives at: about 2 s later the status word holds
  * EAGLE_ERR_TIMEOUT (read and clear it with eagle_read_device_status).
